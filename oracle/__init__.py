@@ -1,0 +1,279 @@
+"""Plain, slow CPU oracle for the Q4 decode matmul, its decode stream and the
+MoE prefill layer.
+
+TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
+benchmark's CPU-baseline / reference leg may import this package.  It shares no
+code with the CUDA library (``bit_quantized_gemv_q4_gb300``) and never imports
+it; inputs come from ``q4synth`` (random draws only).
+
+Pieces and the passages they follow:
+
+* ``gemv``: the C oracle in ``q4_oracle.c`` -- the plain definition of the
+  fused-dequant matmul (BaseRT: optimal LLM inference on Apple Silicon with
+  native Metal, §3.3 "Kernel fusion and specialisation"), fp64, k in order.
+* ``decode_*``: one decode step as a chain of GEMVs (BaseRT §3.3: GEMV for
+  decode, M=1, fused QKV / FFN launches; MetalRT: AI inference performance
+  optimisation on Apple Silicon, §2.2 decode throughput; "Mac on-device AI
+  performance breakthrough", §2.2: the QKV products merged into one).  The pages
+  do not give the dataflow between the GEMVs.  This oracle takes the plainest
+  reading that keeps every matrix of the layer on the path (listed in the
+  design notes):
+      q,k,v = Wq h, Wk h, Wv h      (k, v stored, not consumed)
+      a     = q                     (stand-in for attention, which is not on
+                                     the matmul path)
+      h'    = fp16(h + Wo a)
+      act   = fp16(SiLU(Wg h') * (Wu h'))
+      h''   = fp16(h' + Wd act)
+    and after the last layer  logits = Wlm h.
+  Every activation the GPU stores as fp16 is rounded here too, RNE, from the
+  fp64 value.
+* ``moe_*``: routed-expert prefill (BaseRT abstract and Fig. 1: MoE prefill on
+  a Qwen3-30B-A3B-shaped model; §3.4 "Prefill": GEMM for M>1).  The pages do not
+  describe routing.  Reading taken: top-k of the fp16 router logits, ties to
+  the lower expert index; weights = softmax over the k chosen logits; rows
+  sorted stably by (expert, token, rank); per row gate/up -> fp16(SiLU(g)*u)
+  -> down; output[t] = sum over ranks k = 0..topk-1 of p[t,k] * Y[pos[t,k]].
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "q4_oracle.c")
+
+
+def lib_path(mutant: int = 0) -> str:
+    return os.path.join(_HERE, "libq4oracle.so" if mutant == 0 else f"libq4oracle_mut{mutant}.so")
+
+
+def build(mutant: int = 0, force: bool = False) -> str:
+    """Compile the C oracle with gcc (OpenMP).  ``mutant`` > 0 builds a
+    deliberately wrong variant used only by the pin tests."""
+    out = lib_path(mutant)
+    if force or not os.path.exists(out) or os.path.getmtime(out) < os.path.getmtime(_SRC):
+        tmp = out + f".tmp{os.getpid()}"
+        cmd = ["gcc", "-O2", "-fPIC", "-shared", "-fopenmp", f"-DQ4O_MUTANT={mutant}",
+               _SRC, "-o", tmp, "-lm"]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, out)
+    return out
+
+
+_libs: dict[int, ctypes.CDLL] = {}
+
+
+def _lib(mutant: int = 0) -> ctypes.CDLL:
+    if mutant not in _libs:
+        L = ctypes.CDLL(build(mutant))
+        L.q4o_half_to_double.restype = ctypes.c_double
+        L.q4o_half_to_double.argtypes = [ctypes.c_uint16]
+        L.q4o_code.restype = ctypes.c_int
+        L.q4o_code.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+        L.q4o_gemv.restype = ctypes.c_int
+        L.q4o_gemv.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [
+            ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        L.q4o_max_threads.restype = ctypes.c_int
+        _libs[mutant] = L
+    return _libs[mutant]
+
+
+def max_threads() -> int:
+    return _lib().q4o_max_threads()
+
+
+def half_to_double(bits: int) -> float:
+    return _lib().q4o_half_to_double(int(bits) & 0xFFFF)
+
+
+def _p(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def gemv(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
+    """y[M, R], A[M, R] in fp64 for W [N, K] (storage format) and fp16 x [M, K].
+
+    ``rows`` (optional) selects output rows; R = len(rows) (else N)."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.float16)
+    biases = np.ascontiguousarray(biases, dtype=np.float16)
+    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float16)
+    N, W = Wq.shape
+    K = W * 8
+    M = x.shape[0]
+    if x.shape[1] != K or scales.shape != (N, K // 64) or biases.shape != (N, K // 64):
+        raise ValueError("shape mismatch")
+    if rows is None:
+        R, rp = N, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        if rows.size and (rows.min() < 0 or rows.max() >= N):
+            raise ValueError("row out of range")
+        R, rp = rows.size, _p(rows)
+    y = np.empty((M, R), np.float64)
+    A = np.empty((M, R), np.float64)
+    if R == 0:
+        return y, A
+    rc = _lib(mutant).q4o_gemv(_p(Wq), _p(scales.view(np.uint16)), _p(biases.view(np.uint16)),
+                               _p(x.view(np.uint16)), M, N, K, rp, R, _p(y), _p(A), nthreads)
+    if rc != 0:
+        raise ValueError("oracle rejected arguments")
+    return y, A
+
+
+def fp16(v) -> np.ndarray:
+    """Round fp64 values to fp16, round-to-nearest-even (numpy converts
+    directly from double, not through float32)."""
+    return np.asarray(v, dtype=np.float64).astype(np.float16)
+
+
+def silu(g):
+    g = np.asarray(g, dtype=np.float64)
+    return g / (1.0 + np.exp(-g))
+
+
+def ulp16(v) -> np.ndarray:
+    """Spacing of fp16 numbers at |v| (2^-24 in the subnormal range)."""
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
+    return np.exp2(e - 10)
+
+
+# ------------------------------------------------------------------ decode ---
+
+def _mat(m):
+    return m.Wq, m.scales, m.biases
+
+
+def decode_qkv(layer, h, rows=None):
+    """q, k, v = fp16(W h) for the fused QKV stage; returns dict of (y, A)."""
+    out = {}
+    for nm in ("q", "k", "v"):
+        r = None if rows is None else rows.get(nm)
+        out[nm] = gemv(*_mat(layer[nm]), h, rows=r)
+    return out
+
+
+def decode_o(layer, a, h, rows=None):
+    """h' = fp16(h + Wo a): returns (fp64 pre-rounding value, A incl. |h|)."""
+    y, A = gemv(*_mat(layer["o"]), a, rows=rows)
+    hh = np.atleast_2d(h).astype(np.float64)
+    if rows is not None:
+        hh = hh[:, rows]
+    return hh + y, A + np.abs(hh)
+
+
+def decode_glu(layer, h, rows=None):
+    """g, u and act = SiLU(g) * u (fp64, before the fp16 store)."""
+    g, Ag = gemv(*_mat(layer["gate"]), h, rows=rows)
+    u, Au = gemv(*_mat(layer["up"]), h, rows=rows)
+    return g, Ag, u, Au, silu(g) * u
+
+
+def decode_down(layer, act, h, rows=None):
+    y, A = gemv(*_mat(layer["down"]), act, rows=rows)
+    hh = np.atleast_2d(h).astype(np.float64)
+    if rows is not None:
+        hh = hh[:, rows]
+    return hh + y, A + np.abs(hh)
+
+
+def decode_layer(layer, h):
+    """One layer, every stored activation rounded to fp16 as the GPU stores it."""
+    qkv = decode_qkv(layer, h)
+    q = fp16(qkv["q"][0])
+    hm = fp16(decode_o(layer, q, h)[0])
+    act = fp16(decode_glu(layer, hm)[4])
+    ho = fp16(decode_down(layer, act, hm)[0])
+    return {"q": q, "k": fp16(qkv["k"][0]), "v": fp16(qkv["v"][0]), "h_mid": hm, "act": act, "h": ho}
+
+
+def decode_step(layers, lm_head, x):
+    """Whole decode step: fp16 x [M, hidden] -> fp64 logits [M, vocab]."""
+    h = np.atleast_2d(x).astype(np.float16)
+    for layer in layers:
+        h = decode_layer(layer, h)["h"]
+    y, A = gemv(*_mat(lm_head), h)
+    return y, A, h
+
+
+# --------------------------------------------------------------------- MoE ---
+
+def moe_route(logits, topk: int):
+    """Top-k routing of fp16 logits [T, E].
+
+    Returns ids [T, topk] (by descending logit, ties to the lower expert),
+    weights [T, topk] fp64 (softmax over the chosen logits), offsets [E+1],
+    token_of [R], expert_of [R], rank_of [R] (R = T*topk rows sorted stably by
+    (expert, token, rank)), pos [T, topk] (sorted row of each (t, k))."""
+    logits = np.asarray(logits, dtype=np.float16)
+    T, E = logits.shape
+    ids = np.empty((T, topk), np.int32)
+    wts = np.empty((T, topk), np.float64)
+    for t in range(T):
+        vals = [float(v) for v in logits[t]]
+        order = sorted(range(E), key=lambda e: (-vals[e], e))[:topk]
+        ids[t] = order
+        chosen = np.array([vals[e] for e in order], np.float64)
+        ex = np.exp(chosen - chosen.max())
+        wts[t] = ex / ex.sum()
+    triples = sorted((int(ids[t, k]), t, k) for t in range(T) for k in range(topk))
+    R = T * topk
+    token_of = np.empty(R, np.int32)
+    expert_of = np.empty(R, np.int32)
+    rank_of = np.empty(R, np.int32)
+    pos = np.empty((T, topk), np.int32)
+    counts = np.zeros(E, np.int64)
+    for r, (e, t, k) in enumerate(triples):
+        token_of[r], expert_of[r], rank_of[r] = t, e, k
+        pos[t, k] = r
+        counts[e] += 1
+    offsets = np.zeros(E + 1, np.int32)
+    offsets[1:] = np.cumsum(counts)
+    return {"ids": ids, "weights": wts, "offsets": offsets, "token_of": token_of,
+            "expert_of": expert_of, "rank_of": rank_of, "pos": pos}
+
+
+def _expert(m, e):
+    return m.Wq[e], m.scales[e], m.biases[e]
+
+
+def moe_gate_up_rows(gu, X_rows, experts, ffn: int):
+    """For each row r: g = Wg[e] X_r, u = Wu[e] X_r (gate = rows 0..ffn-1 and up =
+    rows ffn..2ffn-1 of the fused expert matrix).  Returns g, Ag, u, Au, act
+    (fp64, before the fp16 store), each [len(rows), ffn]."""
+    n = len(experts)
+    g = np.empty((n, ffn)); Ag = np.empty((n, ffn)); u = np.empty((n, ffn)); Au = np.empty((n, ffn))
+    gate_rows = np.arange(ffn, dtype=np.int64)
+    up_rows = gate_rows + ffn
+    for i, e in enumerate(experts):
+        W = _expert(gu, int(e))
+        yg, ag = gemv(*W, X_rows[i:i + 1], rows=gate_rows)
+        yu, au = gemv(*W, X_rows[i:i + 1], rows=up_rows)
+        g[i], Ag[i], u[i], Au[i] = yg[0], ag[0], yu[0], au[0]
+    return g, Ag, u, Au, silu(g) * u
+
+
+def moe_down_rows(dn, H_rows, experts, cols=None):
+    """Y_r = Wd[e] H_r for each row; returns (y, A) [len(rows), len(cols) or N]."""
+    out_y, out_a = [], []
+    for i, e in enumerate(experts):
+        y, A = gemv(*_expert(dn, int(e)), H_rows[i:i + 1], rows=cols)
+        out_y.append(y[0]); out_a.append(A[0])
+    return np.array(out_y), np.array(out_a)
+
+
+def moe_combine(Y, pos, weights):
+    """out[t] = sum_{k=0}^{topk-1} p[t,k] * Y[pos[t,k]], k in rank order, fp64."""
+    Y = np.asarray(Y, dtype=np.float64)
+    T, topk = pos.shape
+    out = np.zeros((T, Y.shape[1]))
+    mag = np.zeros((T, Y.shape[1]))
+    for t in range(T):
+        for k in range(topk):
+            out[t] += weights[t, k] * Y[pos[t, k]]
+            mag[t] += np.abs(weights[t, k] * Y[pos[t, k]])
+    return out, mag
