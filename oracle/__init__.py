@@ -16,15 +16,23 @@ Pieces and the passages they follow:
   optimisation on Apple Silicon, §2.2 decode throughput; "Mac on-device AI
   performance breakthrough", §2.2: the QKV products merged into one).  The pages
   do not give the dataflow between the GEMVs.  This oracle takes the plainest
-  reading that keeps every matrix of the layer on the path (listed in the
-  design notes):
-      q,k,v = Wq h, Wk h, Wv h      (k, v stored, not consumed)
+  reading that keeps every matrix of the layer on the path and the values
+  bounded, with the pre-norm RMSNorm of Qwen3/Llama-style layers (BaseRT §3.3
+  lists normalisation among its kernels and fuses operator sequences of the
+  attention path and FFN; MetalRT §5.1 keeps LayerNorm in fp32).  Without the
+  norms the synthetic chain overflows fp16 within a few layers (SiLU*up grows
+  quadratically):
+      n     = rmsnorm(h) * g_attn   (fp64, not rounded: the GPU fuses it into
+                                     the GEMV prologue and keeps it in fp32)
+      q,k,v = Wq n, Wk n, Wv n      (stored fp16; k, v not consumed)
       a     = q                     (stand-in for attention, which is not on
                                      the matmul path)
       h'    = fp16(h + Wo a)
-      act   = fp16(SiLU(Wg h') * (Wu h'))
+      act   = fp16(SiLU(Wg n') * (Wu n')),  n' = rmsnorm(h') * g_ffn
       h''   = fp16(h' + Wd act)
-    and after the last layer  logits = Wlm h.
+    and after the last layer  logits = Wlm (rmsnorm(h) * g_final).
+    rmsnorm(v) = v / sqrt(mean(v^2) + eps); the norm weights g default to 1
+    (their random-init value).
   Every activation the GPU stores as fp16 is rounded here too, RNE, from the
   fp64 value.
 * ``moe_*``: routed-expert prefill (BaseRT abstract and Fig. 1: MoE prefill on
@@ -76,6 +84,8 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
         L.q4o_gemv.restype = ctypes.c_int
         L.q4o_gemv.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [
             ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        L.q4o_gemv_f64.restype = ctypes.c_int
+        L.q4o_gemv_f64.argtypes = L.q4o_gemv.argtypes
         L.q4o_max_threads.restype = ctypes.c_int
         _libs[mutant] = L
     return _libs[mutant]
@@ -94,13 +104,16 @@ def _p(a: np.ndarray):
 
 
 def gemv(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
-    """y[M, R], A[M, R] in fp64 for W [N, K] (storage format) and fp16 x [M, K].
+    """y[M, R], A[M, R] in fp64 for W [N, K] (storage format) and x [M, K].
 
-    ``rows`` (optional) selects output rows; R = len(rows) (else N)."""
+    x is fp16 (converted exactly) or fp64 (used as is).  ``rows`` (optional)
+    selects output rows; R = len(rows) (else N)."""
     Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
     scales = np.ascontiguousarray(scales, dtype=np.float16)
     biases = np.ascontiguousarray(biases, dtype=np.float16)
-    x = np.ascontiguousarray(np.atleast_2d(x), dtype=np.float16)
+    x = np.atleast_2d(x)
+    f64 = x.dtype == np.float64
+    x = np.ascontiguousarray(x, dtype=np.float64 if f64 else np.float16)
     N, W = Wq.shape
     K = W * 8
     M = x.shape[0]
@@ -117,8 +130,11 @@ def gemv(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
     A = np.empty((M, R), np.float64)
     if R == 0:
         return y, A
-    rc = _lib(mutant).q4o_gemv(_p(Wq), _p(scales.view(np.uint16)), _p(biases.view(np.uint16)),
-                               _p(x.view(np.uint16)), M, N, K, rp, R, _p(y), _p(A), nthreads)
+    L = _lib(mutant)
+    fn = L.q4o_gemv_f64 if f64 else L.q4o_gemv
+    xp = _p(x) if f64 else _p(x.view(np.uint16))
+    rc = fn(_p(Wq), _p(scales.view(np.uint16)), _p(biases.view(np.uint16)), xp, M, N, K, rp, R, _p(y), _p(A),
+            nthreads)
     if rc != 0:
         raise ValueError("oracle rejected arguments")
     return y, A
@@ -144,21 +160,34 @@ def ulp16(v) -> np.ndarray:
 
 # ------------------------------------------------------------------ decode ---
 
+DEFAULT_EPS = 1e-6
+
+
+def rmsnorm(h, gamma=None, eps: float = DEFAULT_EPS):
+    """h / sqrt(mean(h^2) + eps) * gamma, per row, in fp64 (gamma None = 1)."""
+    h = np.atleast_2d(np.asarray(h, dtype=np.float64))
+    r = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + eps)
+    if gamma is not None:
+        r = r * np.asarray(gamma, dtype=np.float64)[None, :]
+    return r
+
+
 def _mat(m):
     return m.Wq, m.scales, m.biases
 
 
-def decode_qkv(layer, h, rows=None):
-    """q, k, v = fp16(W h) for the fused QKV stage; returns dict of (y, A)."""
+def decode_qkv(layer, h, rows=None, eps: float = DEFAULT_EPS):
+    """q, k, v = W rmsnorm(h) for the fused QKV stage; dict of (y, A)."""
+    n = rmsnorm(h, layer.get("attn_norm"), eps)
     out = {}
     for nm in ("q", "k", "v"):
         r = None if rows is None else rows.get(nm)
-        out[nm] = gemv(*_mat(layer[nm]), h, rows=r)
+        out[nm] = gemv(*_mat(layer[nm]), n, rows=r)
     return out
 
 
 def decode_o(layer, a, h, rows=None):
-    """h' = fp16(h + Wo a): returns (fp64 pre-rounding value, A incl. |h|)."""
+    """h' = h + Wo a (fp64, before the fp16 store), A incl. |h|."""
     y, A = gemv(*_mat(layer["o"]), a, rows=rows)
     hh = np.atleast_2d(h).astype(np.float64)
     if rows is not None:
@@ -166,10 +195,11 @@ def decode_o(layer, a, h, rows=None):
     return hh + y, A + np.abs(hh)
 
 
-def decode_glu(layer, h, rows=None):
-    """g, u and act = SiLU(g) * u (fp64, before the fp16 store)."""
-    g, Ag = gemv(*_mat(layer["gate"]), h, rows=rows)
-    u, Au = gemv(*_mat(layer["up"]), h, rows=rows)
+def decode_glu(layer, h, rows=None, eps: float = DEFAULT_EPS):
+    """g, u from rmsnorm(h') and act = SiLU(g) * u (fp64, before the store)."""
+    n = rmsnorm(h, layer.get("ffn_norm"), eps)
+    g, Ag = gemv(*_mat(layer["gate"]), n, rows=rows)
+    u, Au = gemv(*_mat(layer["up"]), n, rows=rows)
     return g, Ag, u, Au, silu(g) * u
 
 
@@ -181,22 +211,26 @@ def decode_down(layer, act, h, rows=None):
     return hh + y, A + np.abs(hh)
 
 
-def decode_layer(layer, h):
+def decode_logits(lm_head, h, final_norm=None, rows=None, eps: float = DEFAULT_EPS):
+    return gemv(*_mat(lm_head), rmsnorm(h, final_norm, eps), rows=rows)
+
+
+def decode_layer(layer, h, eps: float = DEFAULT_EPS):
     """One layer, every stored activation rounded to fp16 as the GPU stores it."""
-    qkv = decode_qkv(layer, h)
+    qkv = decode_qkv(layer, h, eps=eps)
     q = fp16(qkv["q"][0])
     hm = fp16(decode_o(layer, q, h)[0])
-    act = fp16(decode_glu(layer, hm)[4])
+    act = fp16(decode_glu(layer, hm, eps=eps)[4])
     ho = fp16(decode_down(layer, act, hm)[0])
     return {"q": q, "k": fp16(qkv["k"][0]), "v": fp16(qkv["v"][0]), "h_mid": hm, "act": act, "h": ho}
 
 
-def decode_step(layers, lm_head, x):
+def decode_step(layers, lm_head, x, final_norm=None, eps: float = DEFAULT_EPS):
     """Whole decode step: fp16 x [M, hidden] -> fp64 logits [M, vocab]."""
     h = np.atleast_2d(x).astype(np.float16)
     for layer in layers:
-        h = decode_layer(layer, h)["h"]
-    y, A = gemv(*_mat(lm_head), h)
+        h = decode_layer(layer, h, eps)["h"]
+    y, A = decode_logits(lm_head, h, final_norm, eps=eps)
     return y, A, h
 
 

@@ -89,23 +89,18 @@ static double q4o_weight(const uint32_t *row, const uint16_t *s_row, const uint1
 
 /*
  * y[m][i], A[m][i] for the rows listed in rows[0..nrows) (all rows 0..N-1
- * when rows == NULL, nrows = N).  Layout: x [M][K], y and A [M][nrows].
- * A may be NULL.  nthreads <= 0 uses the OpenMP default.
+ * when rows == NULL, nrows = N), with x given in fp64: x [M][K], y and A
+ * [M][nrows].  A may be NULL.  nthreads <= 0 uses the OpenMP default.
  * Returns 0, or -1 on a bad argument.
  */
-int q4o_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
-             const uint16_t *x, int64_t M, int64_t N, int64_t K,
-             const int64_t *rows, int64_t nrows, double *y, double *A, int nthreads)
+int q4o_gemv_f64(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                 const double *xd, int64_t M, int64_t N, int64_t K,
+                 const int64_t *rows, int64_t nrows, double *y, double *A, int nthreads)
 {
-    if (!Wq || !scales || !biases || !x || !y || M < 1 || N < 0 || K < 64 || K % 64)
+    if (!Wq || !scales || !biases || !xd || !y || M < 1 || N < 0 || K < 64 || K % 64)
         return -1;
     if (!rows)
         nrows = N;
-    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K));
-    if (!xd)
-        return -1;
-    for (int64_t i = 0; i < M * K; ++i)
-        xd[i] = q4o_half_to_double(x[i]);
     int64_t words = K / 8, groups = K / 64;
 #ifdef _OPENMP
     if (nthreads <= 0)
@@ -134,8 +129,24 @@ int q4o_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                 A[m * nrows + i] = mag;
         }
     }
-    free(xd);
     return 0;
+}
+
+/* Same with x given as fp16 bit patterns (converted exactly to fp64). */
+int q4o_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+             const uint16_t *x, int64_t M, int64_t N, int64_t K,
+             const int64_t *rows, int64_t nrows, double *y, double *A, int nthreads)
+{
+    if (!x || M < 1 || K < 64)
+        return -1;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K));
+    if (!xd)
+        return -1;
+    for (int64_t i = 0; i < M * K; ++i)
+        xd[i] = q4o_half_to_double(x[i]);
+    int rc = q4o_gemv_f64(Wq, scales, biases, xd, M, N, K, rows, nrows, y, A, nthreads);
+    free(xd);
+    return rc;
 }
 
 /* Number of OpenMP threads this library would use by default (1 without OpenMP). */

@@ -33,28 +33,36 @@ def diag_values(m):
 
 
 def test_diagonal_decode_step_reduces_to_elementwise():
+    """With diagonal weights every GEMV is an elementwise product, so the whole
+    stack (norms, residuals, SiLU*up, fp16 stores) can be written out directly."""
     g = np.random.default_rng(3)
     layers = []
     for _ in range(2):
         d = {}
         for nm in ("q", "k", "v", "o", "gate", "up", "down"):
             d[nm] = diag_matrix(list(g.integers(0, 16, 64)), list(np.exp2(g.integers(-4, 1, 64)) * 0.75))
+        d["attn_norm"] = (g.random(64) + 0.5).astype(np.float16)
+        d["ffn_norm"] = (g.random(64) + 0.5).astype(np.float16)
         layers.append(d)
     lm = diag_matrix(list(g.integers(0, 16, 64)), list(np.exp2(g.integers(-3, 0, 64))))
+    fin = (g.random(64) + 0.5).astype(np.float16)
     x = q4synth.activations(9, 2, 64)
-    logits, A, h_last = oracle.decode_step(layers, lm, x)
+    eps = 1e-5
+    logits, A, h_last = oracle.decode_step(layers, lm, x, final_norm=fin, eps=eps)
 
     f16 = lambda v: np.asarray(v, np.float64).astype(np.float16).astype(np.float64)
+    nrm = lambda v, w: v / np.sqrt((v * v).mean(axis=1, keepdims=True) + eps) * w.astype(np.float64)
     h = x.astype(np.float64)
     for d in layers:
-        q = f16(diag_values(d["q"]) * h)
+        q = f16(diag_values(d["q"]) * nrm(h, d["attn_norm"]))
         hm = f16(h + diag_values(d["o"]) * q)
-        gg = diag_values(d["gate"]) * hm
-        act = f16(gg / (1 + np.exp(-gg)) * (diag_values(d["up"]) * hm))
+        n2 = nrm(hm, d["ffn_norm"])
+        gg = diag_values(d["gate"]) * n2
+        act = f16(gg / (1 + np.exp(-gg)) * (diag_values(d["up"]) * n2))
         h = f16(hm + diag_values(d["down"]) * act)
-    want = diag_values(lm) * h
+    want = diag_values(lm) * nrm(h, fin)
     assert np.array_equal(h_last.astype(np.float64), h)
-    assert np.array_equal(logits, want)
+    assert np.allclose(logits, want, rtol=1e-15, atol=0)
 
 
 def test_zero_o_and_down_leave_h_unchanged():
@@ -67,8 +75,23 @@ def test_zero_o_and_down_leave_h_unchanged():
             m.biases[:] = (-8.0 * m.scales.astype(np.float64)).astype(np.float16)
     x = q4synth.activations(78, 1, 128)
     logits, _, h = oracle.decode_step(layers, lm, x)
-    direct, _ = oracle.gemv(lm.Wq, lm.scales, lm.biases, x)
+    direct, _ = oracle.gemv(lm.Wq, lm.scales, lm.biases, oracle.rmsnorm(x))
     assert np.array_equal(h, x) and np.array_equal(logits, direct)
+
+
+def test_rmsnorm_closed_forms():
+    eps = 1e-6
+    for c in (0.5, -3.0, 1000.0):
+        v = np.full((1, 256), c)
+        r = oracle.rmsnorm(v, eps=eps)
+        assert np.allclose(r, np.sign(c) / np.sqrt(1 + eps / c ** 2), rtol=1e-15, atol=0)
+    h = q4synth.activations(5, 3, 512).astype(np.float64)
+    r = oracle.rmsnorm(h, eps=0.0)
+    assert np.allclose((r * r).mean(axis=1), 1.0, rtol=1e-14)          # unit mean square
+    assert np.allclose(oracle.rmsnorm(8.0 * h, eps=0.0), r, rtol=1e-14)  # scale invariance
+    w = np.linspace(0.5, 2, 512)
+    assert np.allclose(oracle.rmsnorm(h, w, eps=0.0), r * w, rtol=1e-15)
+    assert np.all(np.sign(r) == np.sign(h))
 
 
 # ---------------------------------------------------------------- routing --
