@@ -1,0 +1,369 @@
+"""Benchmark: Q4 decode-step matmul stream on one GB300 (or N replicas).
+
+Workload: the Qwen3-0.6B-shaped decode weight stream at M = 1 -- 28 layers of
+fused QKV (1024 -> 2048+1024+1024), o (2048 -> 1024, + residual), fused
+gate/up (1024 -> 2x3072, SiLU*up), down (3072 -> 1024, + residual), then
+lm_head (1024 -> 151936); Q4 group-64 weights with fp16 scale and bias,
+synthetic and seeded (random-init of that shape; no trained weights).  One
+step = one decode token = one replay of the captured stream (113 kernels).
+
+Prints ONE JSON line (rank 0).  `value` is whole-job decode tok/s with the
+inputs resident in HBM; `e2e` is the same through the C ABI with the input
+vector copied in from pinned host memory and the logits copied out every step;
+`roofline` is the dominant kernel (the Q4 GEMV kernel: every launch of the
+step) against the measured HBM copy bandwidth; `cpu_baseline` is the fp64 CPU
+oracle timed on the host cores on a bounded sample.  `--impl reference` times
+the oracle instead (the reference arm).
+
+Multi-GPU: replicas only (the path does not shard); each rank decodes its own
+stream, value = ranks x tokens / max-over-ranks time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "Q4 fused-dequant GEMV HBM GB/s (% of peak); decode-step matmul tok/s"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for nm in ("q4_gemv.cu", "q4_device.cuh"):
+        with open(os.path.join(ROOT, "bit_quantized_gemv_q4_gb300", "csrc", nm), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """Per-launch DRAM bytes of the GEMV kernel from the committed ncu summary,
+    or None if it was taken with a different kernel source."""
+    path = os.path.join(ROOT, "profiles", "q4_gemv_decode_qwen3_0p6b_traffic.txt")
+    try:
+        kv = {}
+        for ln in open(path):
+            if "=" in ln and not ln.startswith("#"):
+                k, v = ln.split("=", 1)
+                kv[k.strip()] = v.strip()
+        if kv.get("kernel_source_hash") != kernel_source_hash():
+            return None
+        return float(kv["dram_bytes_per_step"]), int(kv["launches_per_step"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            p = [v.strip() for v in ln.split(",")]
+            if len(p) < 7:
+                continue
+            try:
+                sm.append(float(p[0]))
+                mx = max(mx, float(p[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, p[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ workload
+
+def make_model(shape, device):
+    import torch
+
+    import q4synth
+
+    def dev(m):
+        return (torch.from_numpy(m.Wq.view("int32")).to(device), torch.from_numpy(m.scales).to(device),
+                torch.from_numpy(m.biases).to(device), m.N, m.K)
+
+    layers, lm = q4synth.decode_weights(shape)
+    return [{k: dev(v) for k, v in d.items()} for d in layers], dev(lm), (layers, lm)
+
+
+def cpu_oracle_rate(shape, host_model, seconds: float, one_sample: bool = False):
+    """Oracle throughput on a bounded sample, as decode tok/s of the full step.
+
+    Sample i = layer (i mod L)'s seven matrices plus the (i mod L)-th of L
+    equal slices of lm_head rows: together 1/L of a step's weights."""
+    import numpy as np
+
+    import oracle
+    import q4synth
+    layers, lm = host_model
+    L = shape.n_layers
+    x = q4synth.activations(q4synth.BASE_SEED + 4242, 1, shape.hidden)
+    xs = {}
+    done_w, t_total, i = 0, 0.0, 0
+    while True:
+        li = i % L
+        t0 = time.perf_counter()
+        w = 0
+        for nm, N, K in shape.layer_linears():
+            m = layers[li][nm]
+            if K not in xs:
+                xs[K] = q4synth.activations(q4synth.BASE_SEED + 4243 + K, 1, K)
+            oracle.gemv(m.Wq, m.scales, m.biases, xs[K])
+            w += N * K
+        rows = np.arange(li * shape.vocab // L, (li + 1) * shape.vocab // L)
+        oracle.gemv(lm.Wq, lm.scales, lm.biases, x, rows=rows)
+        w += rows.size * shape.hidden
+        t_total += time.perf_counter() - t0
+        done_w += w
+        i += 1
+        if one_sample or t_total >= seconds:
+            break
+    return done_w / t_total / shape.weights_per_step(), i, t_total
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+
+    import torch
+    import q4synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    shape = q4synth.QWEN3_0P6B
+    M = 1
+    algo_bytes = shape.weight_bytes_per_step() + 0  # vectors added below
+    # activation bytes per step: each GEMV reads its x once and writes y once
+    vec = 0
+    for nm, N, K in shape.layer_linears():
+        vec += M * (K + N) * 2
+    vec = shape.n_layers * vec + M * (shape.hidden * 2 + shape.vocab * 4)
+    algo_bytes += vec
+    config = {"workload": f"{shape.name} decode weight stream, M={M}", "layers": shape.n_layers,
+              "hidden": shape.hidden, "q": shape.q, "kv": shape.kv, "ffn": shape.ffn, "vocab": shape.vocab,
+              "format": "Q4 group-64, fp16 scale+bias, 8 codes per uint32",
+              "bytes_per_step": algo_bytes,
+              "l2": "no flush: per-step weight footprint 336.8 MB exceeds the 129 MB L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import oracle
+        oracle.build()
+        host_model = q4synth.decode_weights(shape)
+        for _ in range(args.warmup):
+            cpu_oracle_rate(shape, host_model, 0, one_sample=True)
+        t0 = time.perf_counter()
+        total_rate_w = 0.0
+        times = []
+        for _ in range(args.steps):
+            r, _, t = cpu_oracle_rate(shape, host_model, 0, one_sample=True)
+            times.append(t)
+        wall = time.perf_counter() - t0
+        # each step is 1/L of a token's weights
+        tok = args.steps / shape.n_layers
+        value = tok / sum(times)
+        out = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": args.gpus,
+               "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1000 * sum(times) / args.steps,
+               "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+               "data": "synthetic", "config": config,
+               "cpu_baseline": {"value": value, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
+                                "sample": f"per step: one layer's 7 matrices + 1/{shape.n_layers} of lm_head "
+                                          f"rows (1/{shape.n_layers} of a token's weights)"},
+               "e2e": {"value": value, "unit": "tok/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+               "wall_s": wall}
+        print(json.dumps(out))
+        return
+
+    import bit_quantized_gemv_q4_gb300 as q4
+    from bit_quantized_gemv_q4_gb300 import build as qbuild
+    qbuild.build()
+
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+
+    dl, dlm, host_model = make_model(shape, device)
+    table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
+    nws = q4.q4_decode_workspace_bytes(table)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    table.set_workspace(ws, nws)
+    x_host = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4242, M, shape.hidden))
+    x = x_host.to(device)
+    logits = torch.empty(M, shape.vocab, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+
+    for _ in range(args.warmup):
+        q4.q4_decode_step(table, x, logits, stream)
+    st = q4.q4_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after warm-up")
+
+    # ---- device-resident timed region
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier()
+        e0.record(stream)
+        for _ in range(args.steps):
+            q4.q4_decode_step(table, x, logits, stream)
+        e1.record(stream)
+        barrier()
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_per_step = ms / args.steps
+    value = world * M * args.steps / (ms / 1000.0)
+
+    # ---- end to end through the C ABI with host buffers
+    x_pin = x_host.pin_memory()
+    out_pin = torch.empty(M, shape.vocab, dtype=torch.float32).pin_memory()
+    for _ in range(3):
+        x.copy_(x_pin, non_blocking=True)
+        q4.q4_decode_step(table, x, logits, stream)
+        out_pin.copy_(logits, non_blocking=True)
+    barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        x.copy_(x_pin, non_blocking=True)
+        q4.q4_decode_step(table, x, logits, stream)
+        out_pin.copy_(logits, non_blocking=True)
+    e1.record(stream)
+    barrier()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([ms_e2e], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms_e2e = float(t.item())
+    e2e_value = world * M * args.steps / (ms_e2e / 1000.0)
+
+    # ---- the largest single launch alone (lm_head GEMV), back to back
+    lm_ms = None
+    if rank == 0:
+        Wq, s, b, N, K = dlm
+        yv = torch.empty(M, N, dtype=torch.float32, device=device)
+        for _ in range(5):
+            q4.q4_gemv(Wq, s, b, x, yv, M, N, K, stream)
+        e0.record(stream)
+        for _ in range(50):
+            q4.q4_gemv(Wq, s, b, x, yv, M, N, K, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        lm_ms = e0.elapsed_time(e1) / 50
+    st = q4.q4_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} after timing")
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return
+
+    peak, peak_kind = peaks()
+    launches_per_step = 4 * shape.n_layers + 1
+    achieved = algo_bytes / (ms_per_step / 1000.0) / 1e9
+    tr = recorded_traffic()
+    lm_bytes = shape.vocab * shape.hidden * 0.5625 + shape.hidden * 2 + shape.vocab * 4
+    out = {
+        "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
+        "hbm_gbs": achieved, "hbm_frac_of_measured": achieved / peak,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_kind": peak_kind,
+                     "kernel": "q4_gemv_kernel<1> (all 113 launches of a step; achieved = algorithmic bytes "
+                               "per step / step time)",
+                     "traffic": (tr[0] / tr[1]) if tr else None,
+                     "algorithmic_bytes_per_launch": algo_bytes / launches_per_step},
+        "lm_head_gemv": {"ms": lm_ms, "gbs": lm_bytes / (lm_ms / 1000.0) / 1e9 if lm_ms else None,
+                         "frac": (lm_bytes / (lm_ms / 1000.0) / 1e9) / peak if lm_ms else None,
+                         "shape": f"M={M} N={shape.vocab} K={shape.hidden}"},
+        "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": M * shape.hidden * 2,
+                "d2h_bytes_per_step": M * shape.vocab * 4},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk.summary(),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        import oracle
+        oracle.build()
+        rate, n, t = cpu_oracle_rate(shape, host_model, args.cpu_seconds)
+        out["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
+                               "sample": f"{n} samples of 1/{shape.n_layers} of a token's weights "
+                                         f"(one layer + a lm_head row slice), {t:.1f} s"}
+    print(json.dumps(out))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

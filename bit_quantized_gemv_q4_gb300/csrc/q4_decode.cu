@@ -1,0 +1,325 @@
+// Decode-step scheduler: a whole layer stack of fused GEMV launches, captured
+// once into a CUDA graph and replayed per token.
+//
+// BaseRT: optimal LLM inference on Apple Silicon with native Metal:
+// * §3 "BaseRT runtime design": a low-overhead dispatch path that removes
+//   per-operator dispatch, allocation and graph evaluation from the decode hot
+//   path.  Here the first call plans and captures; every later call is one
+//   cudaGraphLaunch.
+// * §3.1 "Data-driven architecture descriptor": the model is data (the
+//   q4_layer_table) and the engine never branches on the architecture.
+// * §3.2 "Zero-allocation decode loop": activations live in a caller-owned
+//   workspace laid out at plan time; replays allocate nothing.
+// * §3.3 "Kernel fusion and specialisation": fused QKV and gate/up launches,
+//   the pre-norm RMSNorms folded into the GEMV prologues, residual adds and
+//   SiLU*up folded into the GEMV epilogues.
+// Programmatic dependent launch links consecutive kernels so each kernel's
+// weight stream (which never depends on its predecessor) starts while the
+// predecessor is still running; only its activation reads wait.
+#include <cuda_runtime.h>
+
+#include <vector>
+
+#include "q4_internal.h"
+
+namespace q4i {
+namespace {
+
+struct Dims {
+    int hidden = 0, qN = 0, kvN = 0, ffn = 0, vocab = 0, M = 0, L = 0;
+};
+
+struct Layout {
+    size_t h = 0, h_mid = 0, q = 0, k = 0, v = 0, act = 0, total = 0;
+};
+
+struct Plan {
+    int device = -1;
+    Dims dims;
+    Layout lay;
+    std::vector<q4_layer_weights> layers;
+    q4_linear lm_head{};
+    const uint16_t* final_norm = nullptr;
+    float eps = 1e-6f;
+    q4_dtype logits_dtype = Q4_F32;
+    void* workspace = nullptr;
+    size_t workspace_bytes = 0;
+    int flags = 0;
+    const void* x_key = nullptr;
+    void* logits_key = nullptr;
+    std::vector<q4_gemv_desc> stages;
+    cudaStream_t capture_stream = nullptr;
+    cudaGraph_t graph = nullptr;
+    cudaGraphExec_t exec = nullptr;
+};
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+q4_status check_linear(const q4_linear& w, int N, int K, const char* what, int layer) {
+    if (!w.Wq || !w.scales || !w.biases)
+        return fail(Q4_ERR_INVALID_ARG, "layer %d %s: NULL weights", layer, what);
+    if ((N > 0 && w.N != N) || (K > 0 && w.K != K) || w.N < 1 || w.K < 64 || w.K % 64)
+        return fail(Q4_ERR_INVALID_ARG, "layer %d %s: shape %dx%d does not fit (want N=%d K=%d)", layer,
+                    what, w.N, w.K, N, K);
+    if (!aligned16(w.Wq) || !aligned16(w.scales) || !aligned16(w.biases))
+        return fail(Q4_ERR_MISALIGNED, "layer %d %s: weights must be 16-byte aligned", layer, what);
+    return Q4_OK;
+}
+
+q4_status table_dims(const q4_layer_table* t, Dims* d) {
+    if (!t) return fail(Q4_ERR_INVALID_ARG, "table is NULL");
+    if (t->n_layers < 0 || t->hidden < 64 || t->hidden % 64)
+        return fail(Q4_ERR_INVALID_ARG, "n_layers=%d hidden=%d", t->n_layers, t->hidden);
+    if (t->M < 1 || t->M > 8) return fail(Q4_ERR_UNSUPPORTED, "M=%d outside 1..8", t->M);
+    if (t->n_layers > 0 && !t->layers) return fail(Q4_ERR_INVALID_ARG, "layers is NULL");
+    if (t->logits_dtype != Q4_F32 && t->logits_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "bad logits_dtype");
+    d->hidden = t->hidden;
+    d->M = t->M;
+    d->L = t->n_layers;
+    q4_status st;
+    for (int l = 0; l < t->n_layers; ++l) {
+        const q4_layer_weights& w = t->layers[l];
+        const int H = t->hidden;
+        if ((st = check_linear(w.q, 0, H, "q", l)) != Q4_OK) return st;
+        if ((st = check_linear(w.k, 0, H, "k", l)) != Q4_OK) return st;
+        if ((st = check_linear(w.v, 0, H, "v", l)) != Q4_OK) return st;
+        if ((st = check_linear(w.o, H, w.q.N, "o", l)) != Q4_OK) return st;
+        if ((st = check_linear(w.gate, 0, H, "gate", l)) != Q4_OK) return st;
+        if ((st = check_linear(w.up, w.gate.N, H, "up", l)) != Q4_OK) return st;
+        if ((st = check_linear(w.down, H, w.gate.N, "down", l)) != Q4_OK) return st;
+        if (w.q.N % 8 || w.k.N % 8 || w.v.N % 8 || w.gate.N % 8)
+            return fail(Q4_ERR_MISALIGNED, "layer %d: q/k/v/gate widths must be multiples of 8", l);
+        if ((w.attn_norm && !aligned16(w.attn_norm)) || (w.ffn_norm && !aligned16(w.ffn_norm)))
+            return fail(Q4_ERR_MISALIGNED, "layer %d: norm weights must be 16-byte aligned", l);
+        if (d->qN < w.q.N) d->qN = w.q.N;
+        if (d->kvN < w.k.N) d->kvN = w.k.N;
+        if (d->kvN < w.v.N) d->kvN = w.v.N;
+        if (d->ffn < w.gate.N) d->ffn = w.gate.N;
+    }
+    if ((st = check_linear(t->lm_head, 0, t->hidden, "lm_head", -1)) != Q4_OK) return st;
+    if (t->final_norm && !aligned16(t->final_norm)) return fail(Q4_ERR_MISALIGNED, "final_norm must be 16-byte aligned");
+    if (!(t->norm_eps >= 0.f)) return fail(Q4_ERR_INVALID_ARG, "norm_eps must be >= 0");
+    d->vocab = t->lm_head.N;
+    return Q4_OK;
+}
+
+Layout layout_of(const Dims& d) {
+    Layout l;
+    size_t off = 0;
+    auto take = [&](size_t elems) {
+        size_t o = off;
+        off = align256(off + elems * 2);
+        return o;
+    };
+    l.h = take((size_t)d.M * d.hidden);
+    l.h_mid = take((size_t)d.M * d.hidden);
+    l.q = take((size_t)d.M * (d.qN > 0 ? d.qN : 1));
+    l.k = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
+    l.v = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
+    l.act = take((size_t)d.M * (d.ffn > 0 ? d.ffn : 1));
+    l.total = off;
+    return l;
+}
+
+q4_segment seg_of(const q4_linear& w, void* y, const uint16_t* residual) {
+    q4_segment s = {};
+    s.Wq = w.Wq;
+    s.scales = w.scales;
+    s.biases = w.biases;
+    s.N = w.N;
+    s.ldy = w.N;
+    s.y = y;
+    s.residual = residual;
+    return s;
+}
+
+void build_stages(Plan& p, const uint16_t* x, void* logits) {
+    uint8_t* ws = static_cast<uint8_t*>(p.workspace);
+    uint16_t* h = reinterpret_cast<uint16_t*>(ws + p.lay.h);
+    uint16_t* hm = reinterpret_cast<uint16_t*>(ws + p.lay.h_mid);
+    uint16_t* q = reinterpret_cast<uint16_t*>(ws + p.lay.q);
+    uint16_t* k = reinterpret_cast<uint16_t*>(ws + p.lay.k);
+    uint16_t* v = reinterpret_cast<uint16_t*>(ws + p.lay.v);
+    uint16_t* act = reinterpret_cast<uint16_t*>(ws + p.lay.act);
+    const int M = p.dims.M, H = p.dims.hidden;
+    p.stages.clear();
+    for (int l = 0; l < p.dims.L; ++l) {
+        const q4_layer_weights& w = p.layers[l];
+        const uint16_t* hin = l == 0 ? x : h;
+        q4_gemv_desc d = {};
+        // q, k, v in one launch
+        d.M = M; d.K = H; d.x = hin; d.ldx = H; d.out_dtype = Q4_F16; d.mode = Q4_GEMV_PLAIN;
+        d.x_rmsnorm = 1; d.norm_weight = w.attn_norm; d.norm_eps = p.eps;
+        d.n_segments = 3;
+        d.seg[0] = seg_of(w.q, q, nullptr);
+        d.seg[1] = seg_of(w.k, k, nullptr);
+        d.seg[2] = seg_of(w.v, v, nullptr);
+        p.stages.push_back(d);
+        // h' = h + Wo q
+        d = {};
+        d.M = M; d.K = w.o.K; d.x = q; d.ldx = w.o.K; d.out_dtype = Q4_F16; d.mode = Q4_GEMV_PLAIN;
+        d.n_segments = 1;
+        d.seg[0] = seg_of(w.o, hm, hin);
+        p.stages.push_back(d);
+        // act = SiLU(Wg h') * (Wu h')
+        d = {};
+        d.M = M; d.K = H; d.x = hm; d.ldx = H; d.out_dtype = Q4_F16; d.mode = Q4_GEMV_GLU;
+        d.x_rmsnorm = 1; d.norm_weight = w.ffn_norm; d.norm_eps = p.eps;
+        d.n_segments = 2;
+        d.seg[0] = seg_of(w.gate, act, nullptr);
+        d.seg[1] = seg_of(w.up, nullptr, nullptr);
+        p.stages.push_back(d);
+        // h = h' + Wd act
+        d = {};
+        d.M = M; d.K = w.down.K; d.x = act; d.ldx = w.down.K; d.out_dtype = Q4_F16; d.mode = Q4_GEMV_PLAIN;
+        d.n_segments = 1;
+        d.seg[0] = seg_of(w.down, h, hm);
+        p.stages.push_back(d);
+    }
+    q4_gemv_desc d = {};
+    d.M = M; d.K = H; d.x = p.dims.L > 0 ? h : x; d.ldx = H; d.out_dtype = p.logits_dtype;
+    d.mode = Q4_GEMV_PLAIN; d.n_segments = 1;
+    d.x_rmsnorm = 1; d.norm_weight = p.final_norm; d.norm_eps = p.eps;
+    d.seg[0] = seg_of(p.lm_head, logits, nullptr);
+    p.stages.push_back(d);
+}
+
+q4_status enqueue_stages(Plan& p, cudaStream_t s) {
+    const bool pdl = !(p.flags & Q4_DECODE_NO_PDL);
+    for (size_t i = 0; i < p.stages.size(); ++i) {
+        q4_status st = launch_gemv(p.stages[i], s, pdl && i > 0, true);
+        if (st != Q4_OK) return st;
+    }
+    return Q4_OK;
+}
+
+void drop_graph(Plan& p) {
+    if (p.exec) cudaGraphExecDestroy(p.exec);
+    if (p.graph) cudaGraphDestroy(p.graph);
+    p.exec = nullptr;
+    p.graph = nullptr;
+}
+
+q4_status capture(Plan& p) {
+    drop_graph(p);
+    cudaError_t e;
+    if (!p.capture_stream) {
+        e = cudaStreamCreateWithFlags(&p.capture_stream, cudaStreamNonBlocking);
+        if (e != cudaSuccess) return cuda_fail(e, "creating the capture stream");
+    }
+    e = cudaStreamBeginCapture(p.capture_stream, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamBeginCapture");
+    q4_status st = enqueue_stages(p, p.capture_stream);
+    cudaGraph_t g = nullptr;
+    e = cudaStreamEndCapture(p.capture_stream, &g);
+    if (st != Q4_OK) {
+        if (g) cudaGraphDestroy(g);
+        return st;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamEndCapture");
+    p.graph = g;
+    e = cudaGraphInstantiate(&p.exec, g, 0);
+    if (e != cudaSuccess) {
+        drop_graph(p);
+        return cuda_fail(e, "cudaGraphInstantiate");
+    }
+    return Q4_OK;
+}
+
+}  // namespace
+}  // namespace q4i
+
+using namespace q4i;
+
+extern "C" {
+
+size_t q4_decode_workspace_bytes(const q4_layer_table* table) {
+    clear_error();
+    Dims d;
+    if (table_dims(table, &d) != Q4_OK) return 0;
+    return layout_of(d).total;
+}
+
+q4_status q4_decode_buffers(const q4_layer_table* table, q4_decode_buffers_t* out) {
+    clear_error();
+    if (!out) return fail(Q4_ERR_INVALID_ARG, "out is NULL");
+    Dims d;
+    q4_status st = table_dims(table, &d);
+    if (st != Q4_OK) return st;
+    if (!table->workspace) return fail(Q4_ERR_INVALID_ARG, "workspace is NULL");
+    const Layout l = layout_of(d);
+    uint8_t* ws = static_cast<uint8_t*>(table->workspace);
+    out->h = reinterpret_cast<uint16_t*>(ws + l.h);
+    out->h_mid = reinterpret_cast<uint16_t*>(ws + l.h_mid);
+    out->q = reinterpret_cast<uint16_t*>(ws + l.q);
+    out->k = reinterpret_cast<uint16_t*>(ws + l.k);
+    out->v = reinterpret_cast<uint16_t*>(ws + l.v);
+    out->act = reinterpret_cast<uint16_t*>(ws + l.act);
+    return Q4_OK;
+}
+
+q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits, q4_stream_t stream) {
+    clear_error();
+    if (!table) return fail(Q4_ERR_INVALID_ARG, "table is NULL");
+    if (!x || !logits) return fail(Q4_ERR_INVALID_ARG, "x or logits is NULL");
+    if (!aligned16(x) || !aligned16(logits)) return fail(Q4_ERR_MISALIGNED, "x and logits must be 16-byte aligned");
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    Plan* p = static_cast<Plan*>(table->plan);
+    if (!p) {
+        // First call: validate, lay out the workspace, build the stage list.
+        Dims d;
+        q4_status st = table_dims(table, &d);
+        if (st != Q4_OK) return st;
+        const Layout l = layout_of(d);
+        if (!table->workspace) return fail(Q4_ERR_INVALID_ARG, "workspace is NULL");
+        if ((reinterpret_cast<uintptr_t>(table->workspace) & 255u) != 0)
+            return fail(Q4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+        if (table->workspace_bytes < l.total)
+            return fail(Q4_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", table->workspace_bytes, l.total);
+        p = new Plan();
+        cudaGetDevice(&p->device);
+        p->dims = d;
+        p->lay = l;
+        p->layers.assign(table->layers, table->layers + table->n_layers);
+        p->lm_head = table->lm_head;
+        p->final_norm = table->final_norm;
+        p->eps = table->norm_eps > 0.f ? table->norm_eps : 1e-6f;
+        p->logits_dtype = table->logits_dtype;
+        p->workspace = table->workspace;
+        p->workspace_bytes = table->workspace_bytes;
+        p->flags = table->flags;
+        table->plan = p;
+    }
+    int dev = -1;
+    cudaGetDevice(&dev);
+    if (dev != p->device) return fail(Q4_ERR_INVALID_ARG, "table was planned on device %d, current is %d", p->device, dev);
+    if (p->stages.empty() || x != p->x_key || logits != p->logits_key) {
+        build_stages(*p, x, logits);
+        p->x_key = x;
+        p->logits_key = logits;
+        drop_graph(*p);
+    }
+    if (p->flags & Q4_DECODE_NO_GRAPH) return enqueue_stages(*p, s);
+    if (!p->exec) {
+        q4_status st = capture(*p);
+        if (st != Q4_OK) return st;
+    }
+    cudaError_t e = cudaGraphLaunch(p->exec, s);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+    return Q4_OK;
+}
+
+q4_status q4_layer_table_release(q4_layer_table* table) {
+    clear_error();
+    if (!table) return fail(Q4_ERR_INVALID_ARG, "table is NULL");
+    Plan* p = static_cast<Plan*>(table->plan);
+    if (p) {
+        drop_graph(*p);
+        if (p->capture_stream) cudaStreamDestroy(p->capture_stream);
+        delete p;
+        table->plan = nullptr;
+    }
+    return Q4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,605 @@
+// Q4 group-64 GEMV for decode (M = 1) and batched decode (M = 2..8), with the
+// dequantisation inside the dot product (BaseRT: optimal LLM inference on
+// Apple Silicon with native Metal, §3.3 "Kernel fusion and specialisation"),
+// several matrices sharing one x per launch (same section: fused operator
+// sequences; "Mac on-device AI performance breakthrough" §2.2: Q, K, V merged
+// into one product) and fused prologue/epilogues (RMSNorm of x, fp16 store,
+// residual add, SiLU*up).
+//
+// GB300 design
+// ------------
+// * The output rows are cut into tiles of TR rows.  The rows of a tile are
+//   contiguous in all three arrays (Wq row n is K/2 bytes, its scales and
+//   biases K/32 bytes each), so one tile is three 1-D bulk copies
+//   (cp.async.bulk) into shared memory, completed on an mbarrier.  One
+//   producer warp keeps `stages` tiles in flight per CTA; the grid is at most
+//   (SMs x CTAs per SM) persistent CTAs that walk the tiles round-robin.
+// * Eight consumer warps dequantise and accumulate from shared memory.  A
+//   uint32 of 8 codes becomes four fp16 pairs with one AND-OR each (the code
+//   is OR-ed into the mantissa of 1024.0 or 64.0, giving 1024+q or 64+q
+//   exactly); w = s*(M+q) + (b - M*s) is then one mixed-precision FMA
+//   (fp16 x fp16 products are exact in fp32), and w*x is accumulated with the
+//   packed fp32x2 FMA, two weights per instruction, in fp32.
+// * x is converted once per CTA to fp32 (optionally RMS-normalised on the
+//   way: the first operation of a pre-norm sublayer, fused into the load),
+//   laid out so each lane's operands are conflict-free 16-byte shared loads,
+//   and reused across the rows a warp handles together.  Each warp reduces its
+//   rows with xor shuffles (fixed order, so results are bit-reproducible).
+// * Under programmatic dependent launch the weight copies start before the
+//   wait on the previous kernel (weights never depend on it); only the x load
+//   and the epilogue wait.
+// * Every mbarrier wait is bounded; on expiry the kernel latches an error bit
+//   and leaves.
+#include <cuda_fp16.h>
+#include <stdio.h>
+
+#include "q4_device.cuh"
+#include "q4_internal.h"
+
+namespace q4k {
+
+constexpr int kConsumerWarps = 8;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kMaxStages = 8;
+// Barriers (full + empty per stage) and the RMSNorm reduction scratch.
+constexpr uint32_t kBarBytes = 2 * kMaxStages * 8 + kConsumerWarps * 8 * 4;
+
+struct Seg {
+    const uint32_t* Wq;
+    const uint16_t* s;
+    const uint16_t* b;
+    void* y;
+    const uint16_t* res;
+    int N, ldy, tile_begin, tiles;
+};
+
+struct Params {
+    Seg seg[Q4_MAX_SEGMENTS];
+    const uint16_t* x;
+    int nseg, K, ldx, TR, rows_per_tile, total_tiles, stages;
+    int out_f16, glu, early_prefetch;
+    int norm;                // RMSNorm of each x row on load
+    const uint16_t* norm_w;  // fp16 [K] or nullptr (ones)
+    float norm_eps;
+    uint32_t stage_bytes, x_bytes;
+    int* err;
+};
+
+// Lane words (LW): how many uint32 (8 codes each) one lane handles per chunk.
+template <int M>
+struct Cfg {
+    static constexpr int LW = (M == 1) ? 4 : (M == 2 ? 2 : 1);
+    static constexpr int RB = (M <= 4) ? 4 : 2;  // rows processed together per warp
+    static constexpr int XV = LW * 2 * M;        // float4 of x per lane per chunk
+};
+
+__device__ __forceinline__ void find_tile(const Params& p, int t, int& si, int& n0, int& nrows) {
+    si = 0;
+    if (!p.glu) {
+#pragma unroll
+        for (int i = 1; i < Q4_MAX_SEGMENTS; ++i)
+            if (i < p.nseg && t >= p.seg[i].tile_begin) si = i;
+    }
+    n0 = (t - p.seg[si].tile_begin) * p.TR;
+    nrows = min(p.TR, p.seg[si].N - n0);
+}
+
+// ------------------------------------------------------------------ producer
+__device__ __forceinline__ void issue_rows(const Params& p, const Seg& sg, int n0, int nrows, int row_off,
+                                           uint8_t* stage, uint32_t full_bar, int lane, uint64_t pol) {
+    const int K = p.K, G = K / 64, R = p.rows_per_tile;
+    const uint32_t wq_bytes = (uint32_t)nrows * (uint32_t)(K / 2);
+    const uint32_t sb_bytes = (uint32_t)nrows * (uint32_t)G * 2u;
+    uint8_t* wq_dst = stage + (size_t)row_off * (K / 2);
+    uint8_t* s_dst = stage + (size_t)R * (K / 2) + (size_t)row_off * G * 2;
+    uint8_t* b_dst = s_dst + (size_t)R * G * 2;
+    const uint32_t* wq_src = sg.Wq + (size_t)n0 * (K / 8);
+    const uint16_t* s_src = sg.s + (size_t)n0 * G;
+    const uint16_t* b_src = sg.b + (size_t)n0 * G;
+    if (lane == 0) q4d::bulk_g2s_evict_first(q4d::smem_addr(wq_dst), wq_src, wq_bytes, full_bar, pol);
+    if ((sb_bytes & 15u) == 0) {
+        if (lane == 0) {
+            q4d::bulk_g2s(q4d::smem_addr(s_dst), s_src, sb_bytes, full_bar);
+            q4d::bulk_g2s(q4d::smem_addr(b_dst), b_src, sb_bytes, full_bar);
+        }
+    } else {
+        // Ragged last tile whose scale block is not a 16-byte multiple: the
+        // producer lanes copy it with ordinary loads.
+        uint16_t* sd = reinterpret_cast<uint16_t*>(s_dst);
+        uint16_t* bd = reinterpret_cast<uint16_t*>(b_dst);
+        for (uint32_t i = lane; i < sb_bytes / 2; i += 32) {
+            sd[i] = __ldg(s_src + i);
+            bd[i] = __ldg(b_src + i);
+        }
+    }
+}
+
+// Bytes the bulk copies of one segment's rows bring in (the expect-tx count).
+__device__ __forceinline__ uint32_t bulk_bytes(const Params& p, int nrows) {
+    const uint32_t wq_b = (uint32_t)nrows * (uint32_t)(p.K / 2);
+    const uint32_t sb_b = (uint32_t)nrows * (uint32_t)(p.K / 64) * 2u;
+    return wq_b + (((sb_b & 15u) == 0) ? 2 * sb_b : 0);
+}
+
+// ------------------------------------------------------------------ consumer
+// Dequantise one word of 8 codes and accumulate against the lane's x pairs.
+template <int M>
+__device__ __forceinline__ void word_mac(uint32_t q, uint16_t sh, float c1024, float c64, const float4* xa,
+                                         const float4* xb, float2* acc) {
+    const uint32_t q8 = q >> 8;
+    const uint32_t v0 = q4d::and_or(q, 0x000F000Fu, 0x64006400u);   // 1024+q0, 1024+q4
+    const uint32_t v1 = q4d::and_or(q, 0x00F000F0u, 0x54005400u);   // 64+q1,   64+q5
+    const uint32_t v2 = q4d::and_or(q8, 0x000F000Fu, 0x64006400u);  // 1024+q2, 1024+q6
+    const uint32_t v3 = q4d::and_or(q8, 0x00F000F0u, 0x54005400u);  // 64+q3,   64+q7
+    const float2 d0 = q4d::fma_h2_s_f32(v0, sh, c1024);             // w0, w4
+    const float2 d1 = q4d::fma_h2_s_f32(v1, sh, c64);               // w1, w5
+    const float2 d2 = q4d::fma_h2_s_f32(v2, sh, c1024);             // w2, w6
+    const float2 d3 = q4d::fma_h2_s_f32(v3, sh, c64);               // w3, w7
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        acc[m] = __ffma2_rn(d0, make_float2(xa[m].x, xa[m].y), acc[m]);
+        acc[m] = __ffma2_rn(d1, make_float2(xa[m].z, xa[m].w), acc[m]);
+        acc[m] = __ffma2_rn(d2, make_float2(xb[m].x, xb[m].y), acc[m]);
+        acc[m] = __ffma2_rn(d3, make_float2(xb[m].z, xb[m].w), acc[m]);
+    }
+}
+
+template <int LW>
+__device__ __forceinline__ void load_words(const uint32_t* src, uint32_t* w) {
+    if constexpr (LW == 4) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+    } else if constexpr (LW == 2) {
+        const uint2 v = *reinterpret_cast<const uint2*>(src);
+        w[0] = v.x;
+        w[1] = v.y;
+    } else {
+        w[0] = *src;
+    }
+}
+
+// Dot products of RB tile rows (shared-memory row indices `rows`) with all M
+// x vectors; every lane ends with all RB*M totals.
+template <int M, int RB>
+__device__ __forceinline__ void dot_rows(const Params& p, const uint32_t* wq, const uint16_t* ss,
+                                         const uint16_t* bs, const float4* xs, const int* rows, int lane,
+                                         float (*out)[M]) {
+    constexpr int LW = Cfg<M>::LW, XV = Cfg<M>::XV;
+    const int W8 = p.K / 8, G = p.K / 64;
+    const int chunk_words = 32 * LW;
+    const int nchunks = (W8 + chunk_words - 1) / chunk_words;
+    float2 acc[RB][M];
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) acc[r][m] = make_float2(0.f, 0.f);
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int j0 = c * chunk_words + lane * LW;
+        if (j0 < W8) {
+            float4 xr[XV];
+            const float4* xc = xs + (size_t)c * XV * 32 + lane;
+#pragma unroll
+            for (int i = 0; i < XV; ++i) xr[i] = xc[i * 32];
+            const int g = j0 >> 3;
+#pragma unroll
+            for (int r = 0; r < RB; ++r) {
+                uint32_t w[LW];
+                load_words<LW>(wq + (size_t)rows[r] * W8 + j0, w);
+                const uint16_t sh = ss[rows[r] * G + g];
+                const uint16_t bh = bs[rows[r] * G + g];
+                const float sf = __half2float(__ushort_as_half(sh));
+                const float bf = __half2float(__ushort_as_half(bh));
+                const float c1024 = fmaf(-1024.f, sf, bf);
+                const float c64 = fmaf(-64.f, sf, bf);
+#pragma unroll
+                for (int wi = 0; wi < LW; ++wi)
+                    word_mac<M>(w[wi], sh, c1024, c64, &xr[(wi * 2 + 0) * M], &xr[(wi * 2 + 1) * M], acc[r]);
+            }
+        }
+    }
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float v = acc[r][m].x + acc[r][m].y;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+            out[r][m] = v;
+        }
+}
+
+__device__ __forceinline__ void store_out(const Params& p, const Seg& sg, int m, int n, float v) {
+    if (p.out_f16) {
+        if (sg.res) v += __half2float(__ushort_as_half(sg.res[(size_t)m * sg.ldy + n]));
+        reinterpret_cast<uint16_t*>(sg.y)[(size_t)m * sg.ldy + n] = __half_as_ushort(__float2half_rn(v));
+    } else {
+        reinterpret_cast<float*>(sg.y)[(size_t)m * sg.ldy + n] = v;
+    }
+}
+
+template <int M, int RB>
+__device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, const uint16_t* ss,
+                                           const uint16_t* bs, const float4* xs, int warp, int lane,
+                                           int j_begin, int rpw, int si, int n0, int nrows) {
+    int rows[RB];
+    int locals[RB];
+#pragma unroll
+    for (int r = 0; r < RB; ++r) {
+        const int j = j_begin + r;
+        if (p.glu) {
+            // gate row and up row of the same output interleave: (g0, u0, g1, u1, ...)
+            const int local = warp * (rpw / 2) + (j >> 1);
+            locals[r] = local;
+            rows[r] = (j & 1) ? p.TR + local : local;
+        } else {
+            locals[r] = warp * rpw + j;
+            rows[r] = locals[r];
+        }
+    }
+    float out[RB][M];
+    dot_rows<M, RB>(p, wq, ss, bs, xs, rows, lane, out);
+    if (p.glu) {
+#pragma unroll
+        for (int r = 0; r < RB; r += 2) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                if (lane == (r / 2) * M + m && locals[r] < nrows) {
+                    const float g = out[r][m], u = out[r + 1][m];
+                    const float a = g / (1.0f + expf(-g)) * u;
+                    const Seg& sg = p.seg[0];
+                    reinterpret_cast<uint16_t*>(sg.y)[(size_t)m * sg.ldy + n0 + locals[r]] =
+                        __half_as_ushort(__float2half_rn(a));
+                }
+            }
+        }
+    } else {
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+            for (int m = 0; m < M; ++m)
+                if (lane == r * M + m && locals[r] < nrows) store_out(p, p.seg[si], m, n0 + locals[r], out[r][m]);
+    }
+}
+
+// 8 consecutive fp16 values (16 bytes) as fp32.
+__device__ __forceinline__ void load8_f32(const uint16_t* src, float* f) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(src);
+    const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&wv[h]));
+        f[2 * h] = t.x;
+        f[2 * h + 1] = t.y;
+    }
+}
+
+// Consumers: load x (RMS-normalised if asked) into shared memory as fp32 in
+// the lane-interleaved pair layout.
+template <int M>
+__device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, int warp, int lane) {
+    constexpr int LW = Cfg<M>::LW, XV = Cfg<M>::XV;
+    constexpr int kCT = kConsumerWarps * 32;
+    const int W8 = p.K / 8;
+    float scale[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) scale[m] = 1.0f;
+    if (p.norm) {
+        // scale = 1 / sqrt(mean(x^2) + eps) per row, fp32, reduced in a fixed
+        // order: thread partials, warp xor tree, warps in index order.
+        float ss[M];
+#pragma unroll
+        for (int m = 0; m < M; ++m) ss[m] = 0.f;
+        for (int j = threadIdx.x; j < W8; j += kCT) {
+#pragma unroll
+            for (int m = 0; m < M; ++m) {
+                float f[8];
+                load8_f32(p.x + (size_t)m * p.ldx + 8 * j, f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss[m] = fmaf(f[e], f[e], ss[m]);
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ss[m] += __shfl_xor_sync(0xffffffffu, ss[m], o);
+            if (lane == 0) red[warp * M + m] = ss[m];
+        }
+        q4d::named_bar(1, kCT);
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float t = 0.f;
+            for (int w = 0; w < kConsumerWarps; ++w) t += red[w * M + m];
+            scale[m] = rsqrtf(t / (float)p.K + p.norm_eps);
+        }
+    }
+    for (int j = threadIdx.x; j < W8; j += kCT) {
+        const int c = j / (32 * LW), rem = j % (32 * LW), l = rem / LW, wi = rem % LW;
+        float gm[8];
+        if (p.norm && p.norm_w) {
+            load8_f32(p.norm_w + 8 * j, gm);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) gm[e] = 1.0f;
+        }
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float f[8];
+            load8_f32(p.x + (size_t)m * p.ldx + 8 * j, f);
+            if (p.norm) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = f[e] * scale[m] * gm[e];
+            }
+            float4* dst = xs + (size_t)c * XV * 32 + l;
+            dst[((wi * 2 + 0) * M + m) * 32] = make_float4(f[0], f[4], f[1], f[5]);
+            dst[((wi * 2 + 1) * M + m) * 32] = make_float4(f[2], f[6], f[3], f[7]);
+        }
+    }
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_constant__ Params p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    constexpr int RB = Cfg<M>::RB;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = p.stages;
+    float4* xs = reinterpret_cast<float4*>(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.x_bytes);
+    float* red = reinterpret_cast<float*>(bars + 2 * kMaxStages);
+    uint8_t* stages = smem + p.x_bytes + kBarBytes;
+    const uint32_t full0 = q4d::smem_addr(bars), empty0 = q4d::smem_addr(bars + kMaxStages);
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            q4d::mbar_init(full0 + 8 * i, 32);               // every producer lane arrives
+            q4d::mbar_init(empty0 + 8 * i, kConsumerWarps);  // one arrival per consumer warp
+        }
+        q4d::fence_mbar_init();
+    }
+    __syncthreads();
+    q4d::pdl_trigger();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer warp
+        if (!p.early_prefetch) q4d::pdl_wait();
+        const uint64_t pol = q4d::policy_evict_first();
+        int i = 0;
+        for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++i) {
+            const int st = i % S, k = i / S;
+            if (k > 0 && !q4d::mbar_wait(empty0 + 8 * st, (k - 1) & 1, p.err)) return;
+            int si, n0, nrows;
+            find_tile(p, t, si, n0, nrows);
+            uint8_t* stage = stages + (size_t)st * p.stage_bytes;
+            const uint32_t fb = full0 + 8 * st;
+            // Expected bytes first, then the copies; the phase completes only
+            // when all 32 lanes have arrived and every byte has landed.
+            const uint32_t expect = (p.glu ? 2u : 1u) * bulk_bytes(p, nrows);
+            if (lane == 0)
+                asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(expect)
+                             : "memory");
+            __syncwarp();
+            issue_rows(p, p.seg[si], n0, nrows, 0, stage, fb, lane, pol);
+            if (p.glu) issue_rows(p, p.seg[1], n0, nrows, p.TR, stage, fb, lane, pol);
+            q4d::mbar_arrive(fb);
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------- consumers
+    q4d::pdl_wait();  // x and residuals may come from the previous kernel
+    load_x<M>(p, xs, red, warp, lane);
+    q4d::named_bar(1, kConsumerWarps * 32);
+
+    const int K = p.K, G = K / 64, R = p.rows_per_tile;
+    const int rpw = R / kConsumerWarps;  // rows per warp per tile (1, 2, 4, 8)
+    int i = 0;
+    for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++i) {
+        const int st = i % S, k = i / S;
+        if (!q4d::mbar_wait(full0 + 8 * st, k & 1, p.err)) return;
+        const uint8_t* stage = stages + (size_t)st * p.stage_bytes;
+        const uint32_t* wq = reinterpret_cast<const uint32_t*>(stage);
+        const uint16_t* ss = reinterpret_cast<const uint16_t*>(stage + (size_t)R * (K / 2));
+        const uint16_t* bs = ss + (size_t)R * G;
+        int si, n0, nrows;
+        find_tile(p, t, si, n0, nrows);
+        if (rpw >= RB) {
+            for (int j = 0; j < rpw; j += RB)
+                tile_batch<M, RB>(p, wq, ss, bs, xs, warp, lane, j, rpw, si, n0, nrows);
+        } else if (rpw == 2) {
+            tile_batch<M, 2>(p, wq, ss, bs, xs, warp, lane, 0, rpw, si, n0, nrows);
+        } else {
+            tile_batch<M, 1>(p, wq, ss, bs, xs, warp, lane, 0, rpw, si, n0, nrows);
+        }
+        __syncwarp();
+        if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
+    }
+}
+
+}  // namespace q4k
+
+namespace q4i {
+
+using q4k::Params;
+
+q4_status validate_gemv(const q4_gemv_desc& d) {
+    if (d.M < 1 || d.M > 8) return fail(d.M < 1 ? Q4_ERR_INVALID_ARG : Q4_ERR_UNSUPPORTED, "M=%d outside 1..8", d.M);
+    if (d.K < 64 || d.K % 64) return fail(Q4_ERR_INVALID_ARG, "K=%d is not a positive multiple of 64", d.K);
+    if (d.K > (1 << 20)) return fail(Q4_ERR_UNSUPPORTED, "K=%d above 1048576", d.K);
+    if (!d.x) return fail(Q4_ERR_INVALID_ARG, "x is NULL");
+    const int ldx = d.ldx ? d.ldx : d.K;
+    if (ldx < d.K) return fail(Q4_ERR_INVALID_ARG, "ldx=%d < K=%d", ldx, d.K);
+    if (!aligned16(d.x) || ldx % 8) return fail(Q4_ERR_MISALIGNED, "x must be 16-byte aligned with ldx %% 8 == 0");
+    if (d.n_segments < 1 || d.n_segments > Q4_MAX_SEGMENTS)
+        return fail(Q4_ERR_INVALID_ARG, "n_segments=%d outside 1..%d", d.n_segments, Q4_MAX_SEGMENTS);
+    if (d.out_dtype != Q4_F32 && d.out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "bad out_dtype");
+    if (d.mode != Q4_GEMV_PLAIN && d.mode != Q4_GEMV_GLU) return fail(Q4_ERR_INVALID_ARG, "bad mode");
+    if (d.mode == Q4_GEMV_GLU) {
+        if (d.n_segments != 2) return fail(Q4_ERR_INVALID_ARG, "GLU mode needs exactly 2 segments");
+        if (d.seg[0].N != d.seg[1].N) return fail(Q4_ERR_INVALID_ARG, "GLU gate/up widths differ");
+        if (d.out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "GLU mode writes fp16");
+        if (d.seg[0].residual || d.seg[1].residual) return fail(Q4_ERR_INVALID_ARG, "GLU mode takes no residual");
+    }
+    if (d.x_rmsnorm != 0 && d.x_rmsnorm != 1) return fail(Q4_ERR_INVALID_ARG, "x_rmsnorm must be 0 or 1");
+    if (d.x_rmsnorm && !(d.norm_eps >= 0.f)) return fail(Q4_ERR_INVALID_ARG, "norm_eps must be >= 0");
+    if (d.x_rmsnorm && d.norm_weight && !aligned16(d.norm_weight))
+        return fail(Q4_ERR_MISALIGNED, "norm_weight must be 16-byte aligned");
+    for (int i = 0; i < d.n_segments; ++i) {
+        const q4_segment& s = d.seg[i];
+        if (!s.Wq || !s.scales || !s.biases) return fail(Q4_ERR_INVALID_ARG, "segment %d: NULL weights", i);
+        if (s.N < 1) return fail(Q4_ERR_INVALID_ARG, "segment %d: N=%d", i, s.N);
+        if (!(d.mode == Q4_GEMV_GLU && i == 1) && !s.y) return fail(Q4_ERR_INVALID_ARG, "segment %d: y is NULL", i);
+        const int ldy = s.ldy ? s.ldy : s.N;
+        if (ldy < s.N) return fail(Q4_ERR_INVALID_ARG, "segment %d: ldy < N", i);
+        if (!aligned16(s.Wq) || !aligned16(s.scales) || !aligned16(s.biases))
+            return fail(Q4_ERR_MISALIGNED, "segment %d: Wq/scales/biases must be 16-byte aligned", i);
+        if (s.residual && d.out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "segment %d: residual needs fp16 output", i);
+    }
+    return Q4_OK;
+}
+
+namespace {
+
+int lane_words_rt(int M) { return M == 1 ? 4 : (M == 2 ? 2 : 1); }
+
+uint32_t x_smem_bytes(int M, int K) {
+    const int LW = lane_words_rt(M);
+    const int chunk_words = 32 * LW;
+    const int nchunks = (K / 8 + chunk_words - 1) / chunk_words;
+    return (uint32_t)nchunks * (uint32_t)(LW * 2 * M) * 32u * 16u;
+}
+
+template <int M>
+cudaError_t launch_m(const Params& p, dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
+    auto kern = q4k::q4_gemv_kernel<M>;
+    static int configured_smem[64] = {0};  // per device: largest dynamic smem set so far
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && (int)smem > configured_smem[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured_smem[dev] = (int)smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(q4k::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, p);
+}
+
+}  // namespace
+
+q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch) {
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+
+    Params p = {};
+    const int M = d.M, K = d.K, G = K / 64;
+    const bool glu = d.mode == Q4_GEMV_GLU;
+    p.x = d.x;
+    p.K = K;
+    p.ldx = d.ldx ? d.ldx : K;
+    p.nseg = d.n_segments;
+    p.out_f16 = d.out_dtype == Q4_F16;
+    p.glu = glu;
+    p.early_prefetch = early_prefetch ? 1 : 0;
+    p.norm = d.x_rmsnorm ? 1 : 0;
+    p.norm_w = d.norm_weight;
+    p.norm_eps = d.norm_eps;
+    p.err = dev->err_word;
+
+    // Tile rows: largest of 32/16/8 (per matrix) whose tile count still
+    // covers every SM, with a stage of at most 48 KB.
+    const uint32_t row_bytes = (uint32_t)(K / 2 + G * 4);
+    int TR = 32;
+    while (TR > 8) {
+        const uint32_t stage = (uint32_t)(glu ? 2 * TR : TR) * row_bytes;
+        long tiles = 0;
+        for (int i = 0; i < (glu ? 1 : d.n_segments); ++i) tiles += (d.seg[i].N + TR - 1) / TR;
+        if (stage <= 48u * 1024u && tiles >= dev->sms) break;
+        TR /= 2;
+    }
+    p.TR = TR;
+    p.rows_per_tile = glu ? 2 * TR : TR;
+    int tiles = 0;
+    for (int i = 0; i < (glu ? 2 : d.n_segments); ++i) {
+        const q4_segment& s = d.seg[i];
+        q4k::Seg& g = p.seg[i];
+        g.Wq = s.Wq;
+        g.s = s.scales;
+        g.b = s.biases;
+        g.y = s.y;
+        g.res = s.residual;
+        g.N = s.N;
+        g.ldy = s.ldy ? s.ldy : s.N;
+        g.tile_begin = glu ? 0 : tiles;
+        g.tiles = (s.N + TR - 1) / TR;
+        if (!glu) tiles += g.tiles;
+    }
+    if (glu) tiles = p.seg[0].tiles;
+    p.total_tiles = tiles;
+
+    p.stage_bytes = ((uint32_t)p.rows_per_tile * row_bytes + 127u) & ~127u;
+    p.x_bytes = (x_smem_bytes(M, K) + 127u) & ~127u;
+    const uint32_t fixed = p.x_bytes + q4k::kBarBytes;
+    // Two CTAs per SM when they fit (lets the next kernel's CTAs start
+    // streaming their weights under programmatic dependent launch).
+    const uint32_t budget_two = (uint32_t)dev->smem_per_sm / 2 - 1024u;
+    uint32_t budget = budget_two;
+    int ctas_per_sm = 2;
+    if (fixed + 2 * p.stage_bytes > budget_two) {
+        budget = (uint32_t)dev->smem_optin;
+        ctas_per_sm = 1;
+    }
+    if (fixed + 2 * p.stage_bytes > budget) {
+        // x for all M rows does not fit next to two weight stages: run the
+        // rows of x in two halves (the weights are then streamed twice).
+        if (M == 1) return fail(Q4_ERR_UNSUPPORTED, "K=%d needs more shared memory than the device has", K);
+        q4_gemv_desc lo = d, hi = d;
+        lo.M = (M + 1) / 2;
+        hi.M = M - lo.M;
+        const int ldx = d.ldx ? d.ldx : K;
+        hi.x = d.x + (size_t)lo.M * ldx;
+        lo.ldx = hi.ldx = ldx;
+        const size_t esz = d.out_dtype == Q4_F16 ? 2 : 4;
+        for (int i = 0; i < d.n_segments; ++i) {
+            const int ldy = d.seg[i].ldy ? d.seg[i].ldy : d.seg[i].N;
+            lo.seg[i].ldy = hi.seg[i].ldy = ldy;
+            if (d.seg[i].y) hi.seg[i].y = static_cast<uint8_t*>(d.seg[i].y) + (size_t)lo.M * ldy * esz;
+            if (d.seg[i].residual) hi.seg[i].residual = d.seg[i].residual + (size_t)lo.M * ldy;
+        }
+        st = launch_gemv(lo, stream, pdl, early_prefetch);
+        if (st != Q4_OK) return st;
+        return launch_gemv(hi, stream, pdl, early_prefetch);
+    }
+    int S = (int)((budget - fixed) / p.stage_bytes);
+    if (S > q4k::kMaxStages) S = q4k::kMaxStages;
+    p.stages = S;
+    const size_t smem = fixed + (size_t)S * p.stage_bytes;
+    const int grid = tiles < dev->sms * ctas_per_sm ? tiles : dev->sms * ctas_per_sm;
+
+    cudaError_t e = cudaSuccess;
+    switch (M) {
+        case 1: e = launch_m<1>(p, dim3(grid), smem, stream, pdl); break;
+        case 2: e = launch_m<2>(p, dim3(grid), smem, stream, pdl); break;
+        case 3: e = launch_m<3>(p, dim3(grid), smem, stream, pdl); break;
+        case 4: e = launch_m<4>(p, dim3(grid), smem, stream, pdl); break;
+        case 5: e = launch_m<5>(p, dim3(grid), smem, stream, pdl); break;
+        case 6: e = launch_m<6>(p, dim3(grid), smem, stream, pdl); break;
+        case 7: e = launch_m<7>(p, dim3(grid), smem, stream, pdl); break;
+        case 8: e = launch_m<8>(p, dim3(grid), smem, stream, pdl); break;
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "q4_gemv kernel launch");
+    return Q4_OK;
+}
+
+}  // namespace q4i

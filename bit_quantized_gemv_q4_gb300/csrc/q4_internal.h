@@ -1,0 +1,41 @@
+// Host-side internals shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/q4.h"
+
+namespace q4i {
+
+// Records printf-style text as the calling thread's last error; returns s.
+q4_status fail(q4_status s, const char* fmt, ...) __attribute__((format(printf, 2, 3)));
+q4_status cuda_fail(cudaError_t e, const char* what);
+void clear_error();
+
+struct DeviceInfo {
+    int device = -1;
+    int sms = 0;
+    int smem_optin = 0;       // max dynamic shared memory per block (opt-in)
+    int smem_per_sm = 0;
+    int cc_major = 0, cc_minor = 0;
+    int* err_word = nullptr;  // device address of the error word (q4_api.cu)
+};
+
+// Info for the current device (cached per device).  Fails with
+// Q4_ERR_NO_DEVICE if there is no device or it is not compute capability 10.3.
+q4_status current_device(const DeviceInfo** out);
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ---- fused multi-segment GEMV (q4_gemv.cu) --------------------------------
+q4_status validate_gemv(const q4_gemv_desc& d);
+// early_prefetch: weight copies may start before the programmatic-dependency
+// wait (only when the weights are not written by a preceding kernel).
+q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch);
+
+// ---- MoE (q4_moe.cu, q4_moe_gemm.cu) ---------------------------------------
+size_t moe_route_workspace_bytes(int T, int E, int topk);
+
+}  // namespace q4i

@@ -1,0 +1,261 @@
+// MoE prefill around the grouped GEMM: routing, gather of token rows into
+// expert order, and the weighted combine.
+//
+// BaseRT: optimal LLM inference on Apple Silicon with native Metal, abstract
+// and Fig. 1: MoE prefill on a Qwen3-30B-A3B-shaped model is where BaseRT's
+// lead is largest.  The page does not describe routing; this library takes
+//   * top-k of the fp16 router logits per token, ties to the lower expert;
+//   * weights = softmax over the k chosen logits (fp32);
+//   * rows sorted stably by (expert, token, rank); a token holds an expert at
+//     most once, so (expert, token) already orders every row;
+//   * out[t] = sum over ranks k of w[t][k] * Y[pos[t][k]], fp32, k in order.
+// All integer outputs are deterministic (no atomics decide an order).
+#include <cuda_fp16.h>
+
+#include "q4_device.cuh"
+#include "q4_internal.h"
+
+namespace q4m {
+
+constexpr int kMaxTopk = 8;
+constexpr int kMaxExperts = 256;
+constexpr int kBlockTokens = 32;  // tokens per counting block (one warp)
+
+// Order-preserving 16-bit key of an fp16 value (-0 folded onto +0).
+__device__ __forceinline__ uint32_t half_key(uint16_t h) {
+    if (h == 0x8000u) h = 0;
+    return (h & 0x8000u) ? (uint32_t)(~h & 0xFFFFu) : (uint32_t)(h | 0x8000u);
+}
+
+// One warp per token: top-k by repeated warp arg-max over (key, -expert).
+__global__ void route_topk_kernel(const uint16_t* __restrict__ logits, int T, int E, int topk,
+                                  int32_t* __restrict__ ids, float* __restrict__ wts) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= T) return;
+    const uint16_t* row = logits + (size_t)warp * E;
+    constexpr int kPer = kMaxExperts / 32;
+    uint32_t key[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) {
+        const int e = lane + 32 * i;
+        key[i] = e < E ? ((half_key(row[e]) << 16) | (uint32_t)(0xFFFF - e)) : 0u;
+    }
+    uint32_t chosen[kMaxTopk];
+    for (int k = 0; k < topk; ++k) {
+        uint32_t best = 0;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) best = key[i] > best ? key[i] : best;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const uint32_t other = __shfl_xor_sync(0xffffffffu, best, o);
+            best = other > best ? other : best;
+        }
+        chosen[k] = best;
+#pragma unroll
+        for (int i = 0; i < kPer; ++i)
+            if (key[i] == best) key[i] = 0;
+    }
+    if (lane == 0) {
+        float l[kMaxTopk];
+        float mx = -INFINITY;
+        for (int k = 0; k < topk; ++k) {
+            const int e = 0xFFFF - (int)(chosen[k] & 0xFFFFu);
+            ids[(size_t)warp * topk + k] = e;
+            l[k] = __half2float(__ushort_as_half(row[e]));
+            mx = fmaxf(mx, l[k]);
+        }
+        float sum = 0.f;
+        for (int k = 0; k < topk; ++k) {
+            l[k] = expf(l[k] - mx);
+            sum += l[k];
+        }
+        for (int k = 0; k < topk; ++k) wts[(size_t)warp * topk + k] = l[k] / sum;
+    }
+}
+
+// count[e * B + b] = tokens of block b routed to expert e.  One warp per block.
+__global__ void route_count_kernel(const int32_t* __restrict__ ids, int T, int E, int topk, int B,
+                                   int32_t* __restrict__ count) {
+    __shared__ int32_t c[kMaxExperts];
+    const int b = blockIdx.x;
+    for (int e = threadIdx.x; e < E; e += 32) c[e] = 0;
+    __syncwarp();
+    const int t = b * kBlockTokens + threadIdx.x;
+    if (t < T)
+        for (int k = 0; k < topk; ++k) atomicAdd(&c[ids[(size_t)t * topk + k]], 1);
+    __syncwarp();
+    for (int e = threadIdx.x; e < E; e += 32) count[(size_t)e * B + b] = c[e];
+}
+
+// Exclusive scan of count[E*B] in (expert, block) order, in place; also
+// offsets[e] = start of expert e, offsets[E] = total.  One CTA.
+__global__ void route_scan_kernel(int32_t* __restrict__ count, int E, int B, int32_t* __restrict__ offsets) {
+    __shared__ int32_t part[1024];
+    const int n = E * B;
+    const int per = (n + blockDim.x - 1) / blockDim.x;
+    const int lo = threadIdx.x * per, hi = min(n, lo + per);
+    int32_t s = 0;
+    for (int i = lo; i < hi; ++i) s += count[i];
+    part[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = 1; o < (int)blockDim.x; o <<= 1) {
+        const int32_t v = threadIdx.x >= (unsigned)o ? part[threadIdx.x - o] : 0;
+        __syncthreads();
+        part[threadIdx.x] += v;
+        __syncthreads();
+    }
+    int32_t run = part[threadIdx.x] - s;  // exclusive prefix of this thread's range
+    for (int i = lo; i < hi; ++i) {
+        const int32_t c = count[i];
+        count[i] = run;
+        if (i % B == 0) offsets[i / B] = run;
+        run += c;
+    }
+    if (threadIdx.x == blockDim.x - 1) offsets[E] = part[threadIdx.x];
+}
+
+// Row of each (token, rank): base[e][b] + number of earlier tokens of the
+// block that hold expert e.  One warp per block.
+__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int T, int topk, int B,
+                                     const int32_t* __restrict__ base, int32_t* __restrict__ token_of,
+                                     int32_t* __restrict__ expert_of, int32_t* __restrict__ pos) {
+    __shared__ int32_t tab[kBlockTokens][kMaxTopk];
+    const int b = blockIdx.x, lane = threadIdx.x;
+    const int t = b * kBlockTokens + lane;
+    for (int k = 0; k < kMaxTopk; ++k) tab[lane][k] = (t < T && k < topk) ? ids[(size_t)t * topk + k] : -1;
+    __syncwarp();
+    if (t >= T) return;
+    for (int k = 0; k < topk; ++k) {
+        const int e = tab[lane][k];
+        int before = 0;
+        for (int l = 0; l < lane; ++l)
+            for (int kk = 0; kk < topk; ++kk) before += tab[l][kk] == e;
+        const int r = base[(size_t)e * B + b] + before;
+        token_of[r] = t;
+        expert_of[r] = e;
+        pos[(size_t)t * topk + k] = r;
+    }
+}
+
+__global__ void gather_kernel(const uint16_t* __restrict__ X, int K, const int32_t* __restrict__ token_of,
+                              int R, uint16_t* __restrict__ Xs) {
+    const int vec = K / 8;  // 16-byte vectors per row
+    const size_t total = (size_t)R * vec;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int r = (int)(i / vec), c = (int)(i % vec);
+        const uint4 v = reinterpret_cast<const uint4*>(X + (size_t)token_of[r] * K)[c];
+        reinterpret_cast<uint4*>(Xs + (size_t)r * K)[c] = v;
+    }
+}
+
+template <bool YF16, bool OF16>
+__global__ void combine_kernel(const void* __restrict__ Y, int N, const int32_t* __restrict__ pos,
+                               const float* __restrict__ w, int T, int topk, void* __restrict__ out) {
+    const size_t total = (size_t)T * N;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / N), n = (int)(i % N);
+        float acc = 0.f;
+        for (int k = 0; k < topk; ++k) {
+            const size_t r = (size_t)pos[(size_t)t * topk + k];
+            const float y = YF16 ? __half2float(__ushort_as_half(static_cast<const uint16_t*>(Y)[r * N + n]))
+                                 : static_cast<const float*>(Y)[r * N + n];
+            acc = fmaf(w[(size_t)t * topk + k], y, acc);
+        }
+        if (OF16)
+            static_cast<uint16_t*>(out)[i] = __half_as_ushort(__float2half_rn(acc));
+        else
+            static_cast<float*>(out)[i] = acc;
+    }
+}
+
+}  // namespace q4m
+
+namespace q4i {
+size_t moe_route_workspace_bytes(int T, int E, int topk) {
+    (void)topk;
+    if (T < 1 || E < 1) return 0;
+    const size_t B = (size_t)(T + q4m::kBlockTokens - 1) / q4m::kBlockTokens;
+    return (B * (size_t)E * sizeof(int32_t) + 255) & ~size_t(255);
+}
+}  // namespace q4i
+
+using namespace q4i;
+
+extern "C" {
+
+size_t q4_moe_route_workspace_bytes(int T, int E, int topk) {
+    clear_error();
+    return moe_route_workspace_bytes(T, E, topk);
+}
+
+q4_status q4_moe_route(const uint16_t* logits, int T, int E, int topk, int32_t* topk_ids, float* topk_weights,
+                       int32_t* offsets, int32_t* token_of, int32_t* expert_of, int32_t* pos, void* workspace,
+                       size_t workspace_bytes, q4_stream_t stream) {
+    clear_error();
+    if (!logits || !topk_ids || !topk_weights || !offsets || !token_of || !expert_of || !pos || !workspace)
+        return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (T < 1 || E < 1 || E > q4m::kMaxExperts || topk < 1 || topk > q4m::kMaxTopk || topk > E)
+        return fail(Q4_ERR_INVALID_ARG, "T=%d E=%d topk=%d (need T>=1, 1<=E<=%d, 1<=topk<=min(E,%d))", T, E,
+                    topk, q4m::kMaxExperts, q4m::kMaxTopk);
+    if ((long long)T * topk > (1ll << 30)) return fail(Q4_ERR_UNSUPPORTED, "T*topk too large");
+    const size_t need = moe_route_workspace_bytes(T, E, topk);
+    if (workspace_bytes < need) return fail(Q4_ERR_INVALID_ARG, "workspace %zu bytes, need %zu", workspace_bytes, need);
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int B = (T + q4m::kBlockTokens - 1) / q4m::kBlockTokens;
+    int32_t* count = static_cast<int32_t*>(workspace);
+    q4m::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights);
+    q4m::route_count_kernel<<<B, 32, 0, s>>>(topk_ids, T, E, topk, B, count);
+    q4m::route_scan_kernel<<<1, 1024, 0, s>>>(count, E, B, offsets);
+    q4m::route_scatter_kernel<<<B, 32, 0, s>>>(topk_ids, T, topk, B, count, token_of, expert_of, pos);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "q4_moe_route launch");
+    return Q4_OK;
+}
+
+q4_status q4_moe_gather(const uint16_t* X, int T, int K, const int32_t* token_of, int R, uint16_t* X_sorted,
+                        q4_stream_t stream) {
+    clear_error();
+    if (!X || !token_of || !X_sorted) return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (T < 1 || R < 1 || K < 8 || K % 8) return fail(Q4_ERR_INVALID_ARG, "T=%d R=%d K=%d (K %% 8 == 0)", T, R, K);
+    if (!aligned16(X) || !aligned16(X_sorted)) return fail(Q4_ERR_MISALIGNED, "X and X_sorted must be 16-byte aligned");
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    const size_t total = (size_t)R * (K / 8);
+    const int grid = (int)((total + 255) / 256 < (size_t)dev->sms * 8 ? (total + 255) / 256 : (size_t)dev->sms * 8);
+    q4m::gather_kernel<<<grid, 256, 0, reinterpret_cast<cudaStream_t>(stream)>>>(X, K, token_of, R, X_sorted);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "q4_moe_gather launch");
+    return Q4_OK;
+}
+
+q4_status q4_moe_combine(const void* Y, q4_dtype y_dtype, int N, const int32_t* pos, const float* topk_weights,
+                         int T, int topk, void* out, q4_dtype out_dtype, q4_stream_t stream) {
+    clear_error();
+    if (!Y || !pos || !topk_weights || !out) return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (N < 1 || T < 1 || topk < 1 || topk > q4m::kMaxTopk) return fail(Q4_ERR_INVALID_ARG, "N=%d T=%d topk=%d", N, T, topk);
+    if ((y_dtype != Q4_F32 && y_dtype != Q4_F16) || (out_dtype != Q4_F32 && out_dtype != Q4_F16))
+        return fail(Q4_ERR_INVALID_ARG, "bad dtype");
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    const size_t total = (size_t)T * N;
+    const int grid = (int)((total + 255) / 256 < (size_t)dev->sms * 8 ? (total + 255) / 256 : (size_t)dev->sms * 8);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (y_dtype == Q4_F16 && out_dtype == Q4_F16)
+        q4m::combine_kernel<true, true><<<grid, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+    else if (y_dtype == Q4_F16)
+        q4m::combine_kernel<true, false><<<grid, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+    else if (out_dtype == Q4_F16)
+        q4m::combine_kernel<false, true><<<grid, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+    else
+        q4m::combine_kernel<false, false><<<grid, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "q4_moe_combine launch");
+    return Q4_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,302 @@
+/*
+ * q4.h -- C ABI of the GB300 Q4 group-64 decode-matmul library.
+ *
+ * The library computes the decode-time matrix products of a 4-bit
+ * group-quantised LLM with the dequantisation folded into the inner loop of
+ * each kernel, never writing dequantised weights to memory (BaseRT: optimal
+ * LLM inference on Apple Silicon with native Metal, §3.3 "Kernel fusion and
+ * specialisation": dedicated GEMV (decode, M=1) and GEMM (prefill, M>1)
+ * kernels per quantisation format, dequantisation integrated into the inner
+ * loop, traffic reduced by the compression ratio).  It exposes a C API for
+ * cross-language use (BaseRT §3, "BaseRT runtime design") and allocates
+ * nothing on its hot calls: every buffer belongs to the caller (BaseRT §3.2,
+ * "Zero-allocation decode loop"); error text lives in a static thread-local
+ * buffer (same section).
+ *
+ * Conventions for every call
+ * --------------------------
+ * - Pointers are DEVICE pointers on the current CUDA device unless stated.
+ *   The caller owns every buffer; the library never frees or keeps them
+ *   beyond the call, except where a call's comment says so.
+ * - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream).  They return after enqueueing.  A launch failure returns
+ *   Q4_ERR_CUDA.  A condition detected on the device (a bounded wait that ran
+ *   out, or bad routing offsets) is latched in a device error word and
+ *   reported by q4_device_status().
+ * - On any error the call enqueues nothing and q4_last_error() describes it.
+ * - "fp16" means IEEE binary16 bit patterns passed as uint16_t.
+ *
+ * Q4 storage format (one matrix W of N output rows by K inputs, y = W x)
+ * -----------------------------------------------------------------------
+ * - Wq:     uint32 [N][K/8], row-major.  Weight k of row n is the 4-bit code
+ *           q in bits 4*(k%8) .. 4*(k%8)+3 of word k/8 (lowest nibble first).
+ * - scales: fp16 [N][K/64], row-major; biases: fp16 [N][K/64].
+ * - w[n][k] = scales[n][k/64] * q + biases[n][k/64], q in 0..15.
+ * - K must be a positive multiple of 64.  Wq, scales, biases and x must be
+ *   16-byte aligned.
+ * The pages name MLX/GGUF 4-bit files (MetalRT: AI inference performance
+ * optimisation on Apple Silicon, §2.1) but print no bit layout; this is the
+ * affine scale+bias group format with the layout fixed above.
+ */
+#ifndef Q4_H
+#define Q4_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *q4_stream_t;
+
+typedef enum q4_status {
+    Q4_OK = 0,
+    Q4_ERR_INVALID_ARG = -1,  /* null pointer, bad size or shape */
+    Q4_ERR_UNSUPPORTED = -2,  /* valid request this build does not serve (e.g. M > 8) */
+    Q4_ERR_MISALIGNED = -3,   /* a pointer or leading dimension breaks the alignment rule */
+    Q4_ERR_CUDA = -4,         /* a CUDA runtime call failed; see q4_last_error() */
+    Q4_ERR_TIMEOUT = -5,      /* a device-side bounded wait ran out (reported by q4_device_status) */
+    Q4_ERR_NO_DEVICE = -6,    /* no usable sm_103 device is current */
+    Q4_ERR_DEVICE_CHECK = -7  /* device-side validation rejected data (e.g. routing offsets) */
+} q4_status;
+
+typedef enum q4_dtype { Q4_F32 = 0, Q4_F16 = 1 } q4_dtype;
+
+/* Text of the last error raised on the calling thread ("" if none).  Static,
+ * thread-local storage: valid until this thread's next library call. */
+const char *q4_last_error(void);
+
+/* Fixed text for a status code. */
+const char *q4_status_string(q4_status status);
+
+/* Library ABI version (major*100 + minor). */
+int q4_version(void);
+
+/* Synchronise `stream`, then read and clear the current device's error word.
+ * Returns Q4_OK, Q4_ERR_TIMEOUT, Q4_ERR_DEVICE_CHECK or Q4_ERR_CUDA. */
+q4_status q4_device_status(q4_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * 1. q4_gemv -- y[m][n] = sum_k w[n][k] * x[m][k], m < M, n < N.
+ *
+ * Decode matmul with the dequantisation inside the dot product (BaseRT §3.3).
+ * x: fp16 [M][K] row-major.  y: fp32 [M][N] row-major (written, not read).
+ * 1 <= M <= 8 (M = 1 is single-token decode; 2..8 is batched decode, each
+ * weight is read once and used M times).  N >= 1.  Accumulation is fp32; the
+ * per-element error is below 1e-3 * sum_k |w x| and the sum order is fixed,
+ * so repeated calls give identical bits.
+ * ------------------------------------------------------------------------ */
+q4_status q4_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                  const uint16_t *x, float *y, int M, int N, int K, q4_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * 2. q4_gemv_ex -- several matrices that share one input x in ONE launch,
+ *    with fused epilogues.
+ *
+ * BaseRT §3.3 fuses operator sequences of the attention path and the FFN
+ * into single kernels (one launch and one global round trip saved each);
+ * "Mac on-device AI performance breakthrough" §2.2 merges the Q, K, V
+ * products into one operation.  Segments i < n_segments each compute
+ * y_i = W_i x for the same x and K:
+ *
+ *   mode Q4_GEMV_PLAIN: y_i written in out_dtype.  If residual_i is set
+ *     (out_dtype must be Q4_F16) the stored value is fp16(acc + residual)
+ *     with the add in fp32; residual_i may alias y_i.
+ *   mode Q4_GEMV_GLU: exactly two segments of equal N: seg[0] = gate,
+ *     seg[1] = up.  Stores fp16( SiLU(gate x) * (up x) ) into seg[0].y
+ *     (fp32 SiLU and product, one fp16 rounding); seg[1].y is ignored;
+ *     out_dtype must be Q4_F16 and residuals must be NULL.
+ *
+ * Output rows of segment i are y_i[m*ldy_i + n]; ldy 0 means N_i.  x rows
+ * are x[m*ldx + k]; ldx 0 means K; ldx must be a multiple of 8.
+ *
+ * x_rmsnorm = 1 applies an RMSNorm to each x row as it is loaded, the first
+ * operation of a pre-norm transformer sublayer fused into the matmul (BaseRT
+ * §3.3 fuses operator sequences of the attention path and the FFN; MetalRT
+ * §5.1 keeps the norm in fp32):
+ *     xn[m][k] = x[m][k] / sqrt(mean_k x[m][k]^2 + norm_eps) * norm_weight[k]
+ * in fp32, used unrounded.  norm_weight: fp16 [K], NULL means all ones.
+ * ------------------------------------------------------------------------ */
+#define Q4_MAX_SEGMENTS 4
+
+typedef enum q4_gemv_mode { Q4_GEMV_PLAIN = 0, Q4_GEMV_GLU = 1 } q4_gemv_mode;
+
+typedef struct q4_segment {
+    const uint32_t *Wq;
+    const uint16_t *scales;
+    const uint16_t *biases;
+    int N;
+    int ldy;
+    void *y;
+    const uint16_t *residual;
+} q4_segment;
+
+typedef struct q4_gemv_desc {
+    int M;
+    int K;
+    const uint16_t *x;
+    int ldx;
+    int n_segments;
+    q4_segment seg[Q4_MAX_SEGMENTS];
+    q4_dtype out_dtype;
+    q4_gemv_mode mode;
+    int x_rmsnorm;
+    const uint16_t *norm_weight;
+    float norm_eps;
+} q4_gemv_desc;
+
+q4_status q4_gemv_ex(const q4_gemv_desc *desc, q4_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * 3. q4_decode_step -- one decode step over a whole layer stack.
+ *
+ * Runs the matmul part of a transformer decode step as one stream of fused
+ * GEMV launches: per layer a fused QKV launch, the o projection with the
+ * residual add, a fused gate/up launch with the SiLU*up epilogue, the down
+ * projection with the residual add; then lm_head.  BaseRT §3 removes
+ * per-operator dispatch from the decode hot path and §3.1 describes the model
+ * by a data descriptor the engine never branches on -- here that descriptor is
+ * q4_layer_table.  The pages do not fix the dataflow between the GEMVs; this
+ * library computes a pre-norm layer, for each layer, with h = x before the
+ * first layer and rms(v) = v / sqrt(mean(v^2) + norm_eps):
+ *
+ *   n   = rms(h) * attn_norm                      (fused into the QKV launch)
+ *   q, k, v = fp16(Wq n), fp16(Wk n), fp16(Wv n)  (k, v kept in the workspace)
+ *   h'  = fp16(h + Wo q)          (q stands in for the attention output)
+ *   n'  = rms(h') * ffn_norm                      (fused into the gate/up launch)
+ *   act = fp16(SiLU(Wgate n') * (Wup n'))
+ *   h   = fp16(h' + Wdown act)
+ *
+ * and finally logits = Wlm (rms(h) * final_norm) in logits_dtype.  Attention
+ * and RoPE are not part of this matmul path.
+ *
+ * The first call on a table validates it, plans the launches and captures
+ * them into a CUDA graph (programmatic dependent launch between the kernels,
+ * so each kernel's weight stream starts before its predecessor ends); later
+ * calls replay the graph.  A call with different x or logits pointers
+ * re-captures.  Host memory for the plan is allocated on that first call
+ * (load time); replays allocate nothing.  x: fp16 [M][hidden].  logits:
+ * [M][vocab].  The workspace (device, >= q4_decode_workspace_bytes) holds the
+ * activations; after a step it holds the LAST layer's q, k, v, h', act and the
+ * final h (see q4_decode_buffers).  Weights must not change between calls
+ * without q4_layer_table_release() (the plan caches their pointers).
+ * ------------------------------------------------------------------------ */
+typedef struct q4_linear {
+    const uint32_t *Wq;
+    const uint16_t *scales;
+    const uint16_t *biases;
+    int N; /* outputs */
+    int K; /* inputs, multiple of 64 */
+} q4_linear;
+
+typedef struct q4_layer_weights {
+    q4_linear q, k, v, o, gate, up, down;
+    const uint16_t *attn_norm; /* fp16 [hidden] RMSNorm weight before QKV; NULL = ones */
+    const uint16_t *ffn_norm;  /* fp16 [hidden] RMSNorm weight before gate/up; NULL = ones */
+} q4_layer_weights;
+
+#define Q4_DECODE_NO_GRAPH 1 /* launch the kernels directly each call (no capture) */
+#define Q4_DECODE_NO_PDL 2   /* no programmatic dependent launch between kernels */
+
+typedef struct q4_layer_table {
+    int n_layers;
+    int hidden;
+    int M;                          /* tokens decoded together, 1..8 */
+    const q4_layer_weights *layers; /* HOST array [n_layers]; read by the first call */
+    q4_linear lm_head;
+    const uint16_t *final_norm; /* fp16 [hidden] RMSNorm weight before lm_head; NULL = ones */
+    float norm_eps;             /* 0 means 1e-6 */
+    q4_dtype logits_dtype;
+    void *workspace; /* device, 256-byte aligned */
+    size_t workspace_bytes;
+    int flags;  /* Q4_DECODE_* */
+    void *plan; /* library-owned cache; zero-initialise, free with q4_layer_table_release */
+} q4_layer_table;
+
+/* Workspace bytes the table needs (0 if the table is malformed). */
+size_t q4_decode_workspace_bytes(const q4_layer_table *table);
+
+/* Device pointers into the workspace (all fp16, row-major [M][width]). */
+typedef struct q4_decode_buffers_t {
+    uint16_t *h;     /* [M][hidden] final h (input of lm_head) */
+    uint16_t *h_mid; /* [M][hidden] last layer's h' */
+    uint16_t *q;     /* [M][q.N] last layer's q */
+    uint16_t *k;     /* [M][k.N] */
+    uint16_t *v;     /* [M][v.N] */
+    uint16_t *act;   /* [M][gate.N] last layer's SiLU(g)*u */
+} q4_decode_buffers_t;
+
+q4_status q4_decode_buffers(const q4_layer_table *table, q4_decode_buffers_t *out);
+
+q4_status q4_decode_step(q4_layer_table *table, const uint16_t *x, void *logits,
+                         q4_stream_t stream);
+
+/* Frees the plan and its graph; the table can be used again afterwards. */
+q4_status q4_layer_table_release(q4_layer_table *table);
+
+/* ------------------------------------------------------------------------ *
+ * 4. Mixture-of-experts prefill: route -> gather -> grouped GEMM (gate/up
+ *    with SiLU*up, then down) -> combine.
+ *
+ * BaseRT's abstract and Fig. 1 report its largest lead on MoE prefill
+ * (Qwen3-30B-A3B, 4-bit), and §3.4 "Prefill" runs prompts as GEMMs whose
+ * arithmetic intensity grows with the sequence length.  The pages do not
+ * describe routing; this library takes top-k of the fp16 router logits with
+ * ties to the lower expert index, weights = softmax over the k chosen logits,
+ * and sorts the T*topk routed rows stably by (expert, token, rank).
+ * ------------------------------------------------------------------------ */
+
+/* Workspace bytes q4_moe_route needs for T tokens and E experts. */
+size_t q4_moe_route_workspace_bytes(int T, int E, int topk);
+
+/* logits: fp16 [T][E].  Outputs (all written): topk_ids int32 [T][topk]
+ * (descending logit), topk_weights fp32 [T][topk], offsets int32 [E+1]
+ * (rows of expert e are offsets[e] .. offsets[e+1]-1), token_of / expert_of
+ * int32 [T*topk] (source token and expert of each sorted row), pos int32
+ * [T][topk] (sorted row of each (token, rank)).  1 <= topk <= min(E, 8),
+ * E <= 256.  Integer outputs are bit-exact. */
+q4_status q4_moe_route(const uint16_t *logits, int T, int E, int topk, int32_t *topk_ids,
+                       float *topk_weights, int32_t *offsets, int32_t *token_of,
+                       int32_t *expert_of, int32_t *pos, void *workspace,
+                       size_t workspace_bytes, q4_stream_t stream);
+
+/* X_sorted[r][:] = X[token_of[r]][:] for r < R.  X: fp16 [T][K], K % 8 == 0. */
+q4_status q4_moe_gather(const uint16_t *X, int T, int K, const int32_t *token_of, int R,
+                        uint16_t *X_sorted, q4_stream_t stream);
+
+typedef struct q4_moe_desc {
+    int E; /* experts */
+    int N; /* outputs per expert (GLU: width of gate = width of up) */
+    int K; /* inputs, multiple of 64 */
+    int R; /* routed rows in X */
+    q4_gemv_mode mode; /* PLAIN: Y = X W_e^T; GLU: W_e holds 2N rows, gate then up,
+                          Y = fp16(SiLU(X Wg^T) * (X Wu^T)) */
+    q4_dtype out_dtype; /* GLU requires Q4_F16 */
+} q4_moe_desc;
+
+/* Grouped GEMM over routed experts: for every expert e and row r in
+ * offsets[e] .. offsets[e+1]-1, Y[r][:] = (dequantised W_e) X[r][:].
+ * Wq: uint32 [E][rows_e][K/8] with rows_e = N (PLAIN) or 2N (GLU); scales,
+ * biases: fp16 [E][rows_e][K/64].  X: fp16 [R][K] sorted by expert.
+ * expert_ids: int32 [R], the expert of each row (checked against offsets on
+ * the device; a mismatch latches Q4_ERR_DEVICE_CHECK).  Y: [R][N].
+ * Runs on the tensor cores (tcgen05, fp16 x fp16 -> fp32), weights
+ * dequantised to fp16 in shared memory, never in global memory. */
+q4_status q4_moe_gemm(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                      const uint16_t *X, const int32_t *expert_ids, const int32_t *offsets,
+                      void *Y, const q4_moe_desc *desc, q4_stream_t stream);
+
+/* out[t][:] = sum_{k<topk} topk_weights[t][k] * Y[pos[t][k]][:], k in rank
+ * order, fp32 accumulation.  Y: [T*topk][N] in y_dtype; out: [T][N] in
+ * out_dtype. */
+q4_status q4_moe_combine(const void *Y, q4_dtype y_dtype, int N, const int32_t *pos,
+                         const float *topk_weights, int T, int topk, void *out,
+                         q4_dtype out_dtype, q4_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q4_H */
