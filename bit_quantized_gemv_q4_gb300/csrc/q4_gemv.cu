@@ -20,9 +20,11 @@
 //   exactly); w = s*(M+q) + (b - M*s) is then one mixed-precision FMA
 //   (fp16 x fp16 products are exact in fp32), and w*x is accumulated with the
 //   packed fp32x2 FMA, two weights per instruction, in fp32.
-// * x is converted once per CTA to fp32 (optionally RMS-normalised on the
-//   way: the first operation of a pre-norm sublayer, fused into the load),
-//   laid out so each lane's operands are conflict-free 16-byte shared loads,
+// * x is converted once per CTA to fp32 (optionally RMS-normalised: the first
+//   operation of a pre-norm sublayer, fused into the load -- the norm weights
+//   are staged before the dependency wait, the sum of squares is reduced as x
+//   streams in, and the scalar 1/rms multiplies the dot products), laid out so
+//   each lane's operands are conflict-free 16-byte shared loads,
 //   and reused across the rows a warp handles together.  Each warp reduces its
 //   rows with xor shuffles (fixed order, so results are bit-reproducible).
 // * Under programmatic dependent launch the weight copies start before the
@@ -69,7 +71,7 @@ struct Params {
 template <int M>
 struct Cfg {
     static constexpr int LW = (M == 1) ? 4 : (M == 2 ? 2 : 1);
-    static constexpr int RB = (M <= 4) ? 4 : 2;  // rows processed together per warp
+    static constexpr int RB = (M == 1) ? 8 : (M <= 4 ? 4 : 2);  // rows processed together per warp
     static constexpr int XV = LW * 2 * M;        // float4 of x per lane per chunk
 };
 
@@ -223,8 +225,8 @@ __device__ __forceinline__ void store_out(const Params& p, const Seg& sg, int m,
 
 template <int M, int RB>
 __device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, const uint16_t* ss,
-                                           const uint16_t* bs, const float4* xs, int warp, int lane,
-                                           int j_begin, int rpw, int si, int n0, int nrows) {
+                                           const uint16_t* bs, const float4* xs, const float* scale, int warp,
+                                           int lane, int j_begin, int rpw, int si, int n0, int nrows) {
     int rows[RB];
     int locals[RB];
 #pragma unroll
@@ -242,6 +244,10 @@ __device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, 
     }
     float out[RB][M];
     dot_rows<M, RB>(p, wq, ss, bs, xs, rows, lane, out);
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) out[r][m] *= scale[m];
     if (p.glu) {
 #pragma unroll
         for (int r = 0; r < RB; r += 2) {
@@ -277,65 +283,87 @@ __device__ __forceinline__ void load8_f32(const uint16_t* src, float* f) {
     }
 }
 
-// Consumers: load x (RMS-normalised if asked) into shared memory as fp32 in
-// the lane-interleaved pair layout.
+// Shared-memory float4 slots of x word j (8 values) for row m, in the
+// lane-interleaved pair layout the dot product reads.
 template <int M>
-__device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, int warp, int lane) {
+__device__ __forceinline__ float4* x_slot(float4* xs, int j, int m, int half) {
     constexpr int LW = Cfg<M>::LW, XV = Cfg<M>::XV;
+    const int c = j / (32 * LW), rem = j % (32 * LW), l = rem / LW, wi = rem % LW;
+    return xs + ((size_t)c * XV + (wi * 2 + half) * M + m) * 32 + l;
+}
+
+// Consumers, before the dependency wait: the RMSNorm weights (a weight, not
+// an activation) are staged into the x slots so the post-wait pass only
+// multiplies.
+template <int M>
+__device__ __forceinline__ void stage_norm_weight(const Params& p, float4* xs) {
     constexpr int kCT = kConsumerWarps * 32;
     const int W8 = p.K / 8;
-    float scale[M];
+    for (int j = threadIdx.x; j < W8; j += kCT) {
+        float g[8];
+        load8_f32(p.norm_w + 8 * j, g);
 #pragma unroll
-    for (int m = 0; m < M; ++m) scale[m] = 1.0f;
-    if (p.norm) {
-        // scale = 1 / sqrt(mean(x^2) + eps) per row, fp32, reduced in a fixed
-        // order: thread partials, warp xor tree, warps in index order.
-        float ss[M];
-#pragma unroll
-        for (int m = 0; m < M; ++m) ss[m] = 0.f;
-        for (int j = threadIdx.x; j < W8; j += kCT) {
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                float f[8];
-                load8_f32(p.x + (size_t)m * p.ldx + 8 * j, f);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) ss[m] = fmaf(f[e], f[e], ss[m]);
-            }
+        for (int m = 0; m < M; ++m) {
+            *x_slot<M>(xs, j, m, 0) = make_float4(g[0], g[4], g[1], g[5]);
+            *x_slot<M>(xs, j, m, 1) = make_float4(g[2], g[6], g[3], g[7]);
         }
+    }
+}
+
+// Consumers, after the dependency wait: x (times the staged norm weights, if
+// any) into shared memory as fp32 in one pass over global memory.  With the
+// RMSNorm the per-row sum of squares is reduced on the way (thread partials,
+// warp xor tree; the warps' partials are added in index order by
+// norm_scales); the scalar 1/rms is applied to the dot products in the
+// epilogue, so x is read once.
+template <int M>
+__device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, int warp, int lane) {
+    constexpr int kCT = kConsumerWarps * 32;
+    const int W8 = p.K / 8;
+    const bool gw = p.norm && p.norm_w;
+    float ss[M];
+#pragma unroll
+    for (int m = 0; m < M; ++m) ss[m] = 0.f;
+    for (int j = threadIdx.x; j < W8; j += kCT) {
+#pragma unroll
+        for (int m = 0; m < M; ++m) {
+            float f[8];
+            load8_f32(p.x + (size_t)m * p.ldx + 8 * j, f);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) ss[m] = fmaf(f[e], f[e], ss[m]);
+            float4* d0 = x_slot<M>(xs, j, m, 0);
+            float4* d1 = x_slot<M>(xs, j, m, 1);
+            float4 a = make_float4(f[0], f[4], f[1], f[5]), b = make_float4(f[2], f[6], f[3], f[7]);
+            if (gw) {
+                const float4 ga = *d0, gb = *d1;
+                a = make_float4(a.x * ga.x, a.y * ga.y, a.z * ga.z, a.w * ga.w);
+                b = make_float4(b.x * gb.x, b.y * gb.y, b.z * gb.z, b.w * gb.w);
+            }
+            *d0 = a;
+            *d1 = b;
+        }
+    }
+    if (p.norm) {
 #pragma unroll
         for (int m = 0; m < M; ++m) {
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) ss[m] += __shfl_xor_sync(0xffffffffu, ss[m], o);
             if (lane == 0) red[warp * M + m] = ss[m];
         }
-        q4d::named_bar(1, kCT);
+    }
+}
+
+// 1/sqrt(mean(x^2) + eps) per row (after the barrier that follows load_x).
+template <int M>
+__device__ __forceinline__ void norm_scales(const Params& p, const float* red, float* scale) {
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            float t = 0.f;
+    for (int m = 0; m < M; ++m) {
+        float t = 0.f;
+        if (p.norm) {
             for (int w = 0; w < kConsumerWarps; ++w) t += red[w * M + m];
             scale[m] = rsqrtf(t / (float)p.K + p.norm_eps);
-        }
-    }
-    for (int j = threadIdx.x; j < W8; j += kCT) {
-        const int c = j / (32 * LW), rem = j % (32 * LW), l = rem / LW, wi = rem % LW;
-        float gm[8];
-        if (p.norm && p.norm_w) {
-            load8_f32(p.norm_w + 8 * j, gm);
         } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) gm[e] = 1.0f;
-        }
-#pragma unroll
-        for (int m = 0; m < M; ++m) {
-            float f[8];
-            load8_f32(p.x + (size_t)m * p.ldx + 8 * j, f);
-            if (p.norm) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) f[e] = f[e] * scale[m] * gm[e];
-            }
-            float4* dst = xs + (size_t)c * XV * 32 + l;
-            dst[((wi * 2 + 0) * M + m) * 32] = make_float4(f[0], f[4], f[1], f[5]);
-            dst[((wi * 2 + 1) * M + m) * 32] = make_float4(f[2], f[6], f[3], f[7]);
+            scale[m] = 1.0f;
         }
     }
 }
@@ -369,7 +397,12 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
         int i = 0;
         for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++i) {
             const int st = i % S, k = i / S;
-            if (k > 0 && !q4d::mbar_wait(empty0 + 8 * st, (k - 1) & 1, p.err)) return;
+            if (k > 0) {
+                // lane 0 waits (suspended in hardware); the others park at the shuffle
+                int ok = 1;
+                if (lane == 0) ok = q4d::mbar_wait(empty0 + 8 * st, (k - 1) & 1, p.err) ? 1 : 0;
+                if (!__shfl_sync(0xffffffffu, ok, 0)) return;
+            }
             int si, n0, nrows;
             find_tile(p, t, si, n0, nrows);
             uint8_t* stage = stages + (size_t)st * p.stage_bytes;
@@ -389,9 +422,12 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
     }
 
     // ---------------------------------------------------------- consumers
+    if (p.norm && p.norm_w) stage_norm_weight<M>(p, xs);
     q4d::pdl_wait();  // x and residuals may come from the previous kernel
     load_x<M>(p, xs, red, warp, lane);
     q4d::named_bar(1, kConsumerWarps * 32);
+    float scale[M];
+    norm_scales<M>(p, red, scale);
 
     const int K = p.K, G = K / 64, R = p.rows_per_tile;
     const int rpw = R / kConsumerWarps;  // rows per warp per tile (1, 2, 4, 8)
@@ -407,11 +443,13 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
         find_tile(p, t, si, n0, nrows);
         if (rpw >= RB) {
             for (int j = 0; j < rpw; j += RB)
-                tile_batch<M, RB>(p, wq, ss, bs, xs, warp, lane, j, rpw, si, n0, nrows);
+                tile_batch<M, RB>(p, wq, ss, bs, xs, scale, warp, lane, j, rpw, si, n0, nrows);
+        } else if (rpw == 4) {
+            tile_batch<M, (RB < 4 ? RB : 4)>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows);
         } else if (rpw == 2) {
-            tile_batch<M, 2>(p, wq, ss, bs, xs, warp, lane, 0, rpw, si, n0, nrows);
+            tile_batch<M, 2>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows);
         } else {
-            tile_batch<M, 1>(p, wq, ss, bs, xs, warp, lane, 0, rpw, si, n0, nrows);
+            tile_batch<M, 1>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows);
         }
         __syncwarp();
         if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
@@ -517,10 +555,10 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     p.norm_eps = d.norm_eps;
     p.err = dev->err_word;
 
-    // Tile rows: largest of 32/16/8 (per matrix) whose tile count still
+    // Tile rows: largest of 64/32/16/8 (per matrix) whose tile count still
     // covers every SM, with a stage of at most 48 KB.
     const uint32_t row_bytes = (uint32_t)(K / 2 + G * 4);
-    int TR = 32;
+    int TR = 64;
     while (TR > 8) {
         const uint32_t stage = (uint32_t)(glu ? 2 * TR : TR) * row_bytes;
         long tiles = 0;
