@@ -1,14 +1,548 @@
-// Grouped GEMM over routed experts (tcgen05).  Not built yet: the entry point
-// reports Q4_ERR_UNSUPPORTED.
+// Grouped GEMM over routed experts on the 5th-generation tensor cores, with
+// the Q4 dequantisation done in shared memory on the way to the MMA.
+//
+// BaseRT: optimal LLM inference on Apple Silicon with native Metal, §3.4
+// "Prefill": prompts run as GEMMs whose arithmetic intensity grows with the
+// sequence length; §3.3: every matmul kernel dequantises in its inner loop
+// (never materialising dequantised weights in global memory); abstract and
+// Fig. 1: MoE prefill (Qwen3-30B-A3B, 4-bit) is where BaseRT's lead is largest.
+//
+// Shape: for expert e and its routed rows r in offsets[e] .. offsets[e+1]-1,
+// Y[r][n] = sum_k w_e[n][k] * X[r][k].  GLU mode: W_e holds 2N rows (gate then
+// up) and Y = fp16(SiLU(gate) * up).
+//
+// GB300 design (one CTA per SM, persistent):
+// * Work unit = (expert, token tile of up to 128 rows, 128-row output tile),
+//   decoded on the device from `offsets` (no host readback).  The weight rows
+//   of a unit fill the MMA's M = 128; the tokens are its N (16..128, padded to
+//   a multiple of 16): small token counts per expert still use the tensor core.
+// * Warp 0 (TMA): per 64-wide K step, the packed codes of the unit's 128 rows
+//   (one 2-D tensor-map copy per matrix, 128 rows x 32 bytes) and the X tile
+//   (128 rows x 64 fp16, 128-byte swizzle = the canonical K-major UMMA layout).
+// * Warps 2..9 (dequant): codes -> fp16 w = s*q + b with the code OR-ed into
+//   the mantissa of 1024.0/64.0 (exact), one fp16 subtract and one fp16 FMA per
+//   pair (w rounded once to fp16), written as the A tile in the same swizzled
+//   K-major layout, fenced to the async proxy.
+// * Warp 1 (MMA): one thread issues tcgen05.mma kind::f16 (fp16 x fp16 ->
+//   fp32) into a double-buffered TMEM accumulator (gate and up side by side),
+//   committing to mbarriers to release input stages and hand the accumulator
+//   to the epilogue.
+// * Warps 10..13 (epilogue): tcgen05.ld of the accumulator, SiLU*up or plain,
+//   coalesced stores.
+// * Every mbarrier wait is bounded; on expiry the CTA latches an error bit,
+//   winds down, and still frees its tensor memory.
+#include <cuda.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include "q4_device.cuh"
 #include "q4_internal.h"
+
+namespace q4g {
+
+constexpr int kTN = 128;          // tokens per unit (MMA N, max)
+constexpr int kRows = 128;        // weight rows per unit (MMA M)
+constexpr int kKS = 64;           // K per step (one swizzle atom row of fp16, one Q4 group)
+constexpr int kInStages = 3;      // codes + X ring
+constexpr int kAStages = 2;       // dequantised A ring
+constexpr int kDeqWarps = 8;
+constexpr int kEpiWarps = 4;
+constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;
+constexpr int kDeqThreads = kDeqWarps * 32;
+constexpr int kMaxExperts = 256;
+constexpr uint32_t kTmemCols = 512;   // 2 accumulator buffers x (gate + up) x 128 columns
+
+constexpr uint32_t kCodesBytes = kRows * 32;         // one matrix, one K step
+constexpr uint32_t kXBytes = kTN * kKS * 2;          // 16 KB
+constexpr uint32_t kInStageBytes = 2 * kCodesBytes + kXBytes;  // 24 KB, X at offset 8 KB (1024-aligned)
+constexpr uint32_t kATileBytes = kRows * kKS * 2;    // 16 KB
+constexpr uint32_t kAStageBytes = 2 * kATileBytes;
+
+struct Params {
+    const uint16_t* scales;
+    const uint16_t* biases;
+    const int32_t* offsets;
+    void* Y;
+    int E, N, K, R, rows_e, nmat, glu, out_f16;
+    int n_tiles, nK, G;
+    uint32_t sb_bytes;
+    int* err;
+};
+
+struct Smem {
+    uint64_t in_full[kInStages], in_empty[kInStages];
+    uint64_t a_full[kAStages], a_empty[kAStages];
+    uint64_t acc_full[2], acc_empty[2];
+    uint64_t drain;  // completion probe for in-flight MMAs on the abort path
+    uint32_t tmem_base;
+    volatile int abort;
+    int total_units;
+    int prefix[kMaxExperts + 1];  // token tiles before expert e
+};
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], "
+        "[%4];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+        : "memory");
+}
+
+// UMMA shared-memory descriptor: K-major, 128-byte swizzle, 8-row atoms of
+// 1024 bytes (stride byte offset), version 1 (sm_100 family).
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t addr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((addr >> 4) & 0x3FFF);
+    d |= (uint64_t)1 << 16;                    // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;          // stride byte offset
+    d |= (uint64_t)1 << 46;                    // descriptor version
+    d |= (uint64_t)2 << 61;                    // SWIZZLE_128B
+    return d;
+}
+
+// Instruction descriptor, kind::f16: D fp32, A and B fp16, both K-major.
+__device__ __forceinline__ uint32_t idesc_f16(int n) {
+    return (1u << 4) | ((uint32_t)(n >> 3) << 17) | ((uint32_t)(kRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(
+            d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+}
+
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+    uint32_t d;
+    asm("prmt.b32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(sel));
+    return d;
+}
+
+// Bounded wait that also gives up when another role has aborted.
+__device__ __forceinline__ bool wait_bar(Smem& sm, uint64_t& bar, uint32_t parity, int* err) {
+    if (sm.abort) return false;
+    if (!q4d::mbar_wait(q4d::smem_addr(&bar), parity, err)) {
+        sm.abort = 1;
+        return false;
+    }
+    return true;
+}
+
+struct Unit {
+    int e, r0, tn, nt;  // expert, first token row, valid tokens, output tile index
+};
+
+__device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int u) {
+    const int tt = u / p.n_tiles;
+    int lo = 0, hi = p.E;  // largest e with prefix[e] <= tt
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (sm.prefix[mid] <= tt) lo = mid;
+        else hi = mid;
+    }
+    Unit un;
+    un.e = lo;
+    const int j = tt - sm.prefix[lo];
+    int a = p.offsets[lo], b = p.offsets[lo + 1];
+    a = max(0, min(a, p.R));
+    b = max(a, min(b, p.R));
+    un.r0 = a + j * kTN;
+    un.tn = min(kTN, b - un.r0);
+    un.nt = u % p.n_tiles;
+    return un;
+}
+
+// Dequantise one word of 8 codes to 8 fp16 weights in k order.
+__device__ __forceinline__ uint4 dequant_word(uint32_t q, __half2 s2, __half2 b2) {
+    const __half2 m1024 = __float2half2_rn(-1024.f), m64 = __float2half2_rn(-64.f);
+    const uint32_t q8 = q >> 8;
+    uint32_t v0 = q4d::and_or(q, 0x000F000Fu, 0x64006400u);   // 1024+q0, 1024+q4
+    uint32_t v1 = q4d::and_or(q, 0x00F000F0u, 0x54005400u);   // 64+q1,   64+q5
+    uint32_t v2 = q4d::and_or(q8, 0x000F000Fu, 0x64006400u);  // 1024+q2, 1024+q6
+    uint32_t v3 = q4d::and_or(q8, 0x00F000F0u, 0x54005400u);  // 64+q3,   64+q7
+    __half2 h0 = __hfma2(__hadd2(*reinterpret_cast<__half2*>(&v0), m1024), s2, b2);  // w0, w4
+    __half2 h1 = __hfma2(__hadd2(*reinterpret_cast<__half2*>(&v1), m64), s2, b2);    // w1, w5
+    __half2 h2 = __hfma2(__hadd2(*reinterpret_cast<__half2*>(&v2), m1024), s2, b2);  // w2, w6
+    __half2 h3 = __hfma2(__hadd2(*reinterpret_cast<__half2*>(&v3), m64), s2, b2);    // w3, w7
+    const uint32_t a0 = *reinterpret_cast<uint32_t*>(&h0), a1 = *reinterpret_cast<uint32_t*>(&h1);
+    const uint32_t a2 = *reinterpret_cast<uint32_t*>(&h2), a3 = *reinterpret_cast<uint32_t*>(&h3);
+    return make_uint4(prmt(a0, a1, 0x5410), prmt(a2, a3, 0x5410), prmt(a0, a1, 0x7632), prmt(a2, a3, 0x7632));
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    q4_moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
+                       const __grid_constant__ Params p) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // 1024-byte alignment for the swizzled tiles.
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* in_ring = base;
+    uint8_t* a_ring = in_ring + kInStages * kInStageBytes;
+    uint32_t* sb = reinterpret_cast<uint32_t*>(a_ring + kAStages * kAStageBytes);
+    Smem& sm = *reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sb) + p.sb_bytes);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kInStages; ++i) {
+            q4d::mbar_init(q4d::smem_addr(&sm.in_full[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&sm.in_empty[i]), kDeqWarps + 1);
+        }
+        for (int i = 0; i < kAStages; ++i) {
+            q4d::mbar_init(q4d::smem_addr(&sm.a_full[i]), kDeqWarps);
+            q4d::mbar_init(q4d::smem_addr(&sm.a_empty[i]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            q4d::mbar_init(q4d::smem_addr(&sm.acc_full[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&sm.acc_empty[i]), kEpiWarps);
+        }
+        q4d::mbar_init(q4d::smem_addr(&sm.drain), 1);
+        sm.abort = 0;
+        q4d::fence_mbar_init();
+    }
+    if (warp == 0) {
+        // token tiles per expert -> prefix sums (offsets clamped to [0, R])
+        if (lane == 0) {
+            int run = 0;
+            for (int e = 0; e < p.E; ++e) {
+                sm.prefix[e] = run;
+                int a = max(0, min(p.offsets[e], p.R));
+                int b = max(a, min(p.offsets[e + 1], p.R));
+                run += (b - a + kTN - 1) / kTN;
+            }
+            sm.prefix[p.E] = run;
+            sm.total_units = run * p.n_tiles;
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         q4d::smem_addr(&sm.tmem_base)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sm.tmem_base;
+    const int U = sm.total_units;
+    const int nK = p.nK;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA
+        if (lane == 0) {
+            int it = 0;
+            for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x) {
+                const Unit un = decode_unit(sm, p, u);
+                const int wrow = un.e * p.rows_e + un.nt * kRows;
+                for (int ks = 0; ks < nK; ++ks, ++it) {
+                    const int s = it % kInStages;
+                    if (it >= kInStages && !wait_bar(sm, sm.in_empty[s], ((it / kInStages) - 1) & 1, p.err)) break;
+                    uint8_t* st = in_ring + s * kInStageBytes;
+                    const uint32_t fb = q4d::smem_addr(&sm.in_full[s]);
+                    q4d::mbar_arrive_expect_tx(fb, p.nmat * kCodesBytes + kXBytes);
+                    tma_load_2d(q4d::smem_addr(st), &tmW, ks * 32, wrow, fb);
+                    if (p.glu) tma_load_2d(q4d::smem_addr(st + kCodesBytes), &tmW, ks * 32, wrow + p.N, fb);
+                    tma_load_2d(q4d::smem_addr(st + 2 * kCodesBytes), &tmX, ks * kKS, un.r0, fb);
+                }
+            }
+            if (sm.abort) {
+                // let this thread's last copies land before the CTA can exit
+                for (int j = (it > kInStages ? it - kInStages : 0); j < it; ++j)
+                    q4d::mbar_wait(q4d::smem_addr(&sm.in_full[j % kInStages]), (j / kInStages) & 1, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA
+        if (lane == 0) {
+            int it = 0, acc_it = 0;
+            for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++acc_it) {
+                const Unit un = decode_unit(sm, p, u);
+                const int npad = ((un.tn + 15) / 16) * 16;
+                const uint32_t idesc = idesc_f16(npad);
+                const int buf = acc_it & 1;
+                if (acc_it >= 2 && !wait_bar(sm, sm.acc_empty[buf], ((acc_it >> 1) - 1) & 1, p.err)) break;
+                tc_fence_after();
+                const uint32_t d0 = tmem + (uint32_t)(buf * 2 * kTN);
+                bool ok = true;
+                for (int ks = 0; ks < nK; ++ks, ++it) {
+                    const int s = it % kInStages, a = it % kAStages;
+                    if (!wait_bar(sm, sm.in_full[s], (it / kInStages) & 1, p.err) ||
+                        !wait_bar(sm, sm.a_full[a], (it / kAStages) & 1, p.err)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t xs = q4d::smem_addr(in_ring + s * kInStageBytes + 2 * kCodesBytes);
+                    const uint32_t as = q4d::smem_addr(a_ring + a * kAStageBytes);
+                    for (int m = 0; m < p.nmat; ++m) {
+#pragma unroll
+                        for (int kk = 0; kk < kKS / 16; ++kk)
+                            mma_f16(d0 + (uint32_t)(m * kTN), sw128_desc(as + m * kATileBytes + kk * 32),
+                                    sw128_desc(xs + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    mma_commit(q4d::smem_addr(&sm.in_empty[s]));
+                    mma_commit(q4d::smem_addr(&sm.a_empty[a]));
+                }
+                if (!ok) break;
+                mma_commit(q4d::smem_addr(&sm.acc_full[buf]));
+            }
+        }
+    } else if (warp < 2 + kDeqWarps) {
+        // ------------------------------------------------------------ dequant
+        // Thread dt owns weight row `row` of the tile: in GLU mode matrix
+        // `part` (gate or up), in plain mode words 4*part..4*part+3 of each
+        // 8-word K step.  Its scales/biases live in private shared slots (no
+        // cross-thread sharing, so no barrier that an aborting warp could
+        // leave the others waiting on).
+        const int dt = threadIdx.x - 64;          // 0..255
+        const int row = dt & (kRows - 1);
+        const int part = dt >> 7;
+        const int m = p.glu ? part : 0;
+        const int G = p.G, Gp = G + 1;
+        uint32_t* my_sb = sb + (size_t)dt * Gp;
+        int it = 0;
+        for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x) {
+            const Unit un = decode_unit(sm, p, u);
+            const size_t grow = (size_t)un.e * p.rows_e + (size_t)m * p.N + (size_t)un.nt * kRows + row;
+            const uint16_t* sp = p.scales + grow * G;
+            const uint16_t* bp = p.biases + grow * G;
+            for (int g = 0; g < G; ++g) my_sb[g] = (uint32_t)__ldg(sp + g) | ((uint32_t)__ldg(bp + g) << 16);
+            bool ok = true;
+            for (int ks = 0; ks < nK; ++ks, ++it) {
+                const int s = it % kInStages, a = it % kAStages;
+                bool w = wait_bar(sm, sm.in_full[s], (it / kInStages) & 1, p.err);
+                if (w && it >= kAStages) w = wait_bar(sm, sm.a_empty[a], ((it / kAStages) - 1) & 1, p.err);
+                if (!__all_sync(0xffffffffu, w)) {
+                    sm.abort = 1;
+                    ok = false;
+                    break;
+                }
+                const uint8_t* st = in_ring + s * kInStageBytes;
+                uint8_t* at = a_ring + a * kAStageBytes;
+                const int w0 = p.glu ? 0 : part * 4, nw = p.glu ? 8 : 4;
+                const uint32_t sbv = my_sb[ks];
+                const __half sh = __ushort_as_half((uint16_t)(sbv & 0xFFFF));
+                const __half bh = __ushort_as_half((uint16_t)(sbv >> 16));
+                const __half2 s2 = __halves2half2(sh, sh), b2 = __halves2half2(bh, bh);
+                const uint4* cw = reinterpret_cast<const uint4*>(st + m * kCodesBytes + row * 32);
+                uint8_t* arow = at + m * kATileBytes + (row >> 3) * 1024 + (row & 7) * 128;
+                for (int h = 0; h < nw / 4; ++h) {
+                    const uint4 c = cw[(w0 >> 2) + h];
+                    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                    for (int wi = 0; wi < 4; ++wi) {
+                        const int j = w0 + h * 4 + wi;   // 16-byte chunk = 8 consecutive k
+                        *reinterpret_cast<uint4*>(arow + ((j ^ (row & 7)) << 4)) = dequant_word(words[wi], s2, b2);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    q4d::mbar_arrive(q4d::smem_addr(&sm.in_empty[s]));
+                    q4d::mbar_arrive(q4d::smem_addr(&sm.a_full[a]));
+                }
+            }
+            if (!ok) break;
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue
+        const int q = warp & 3;                   // TMEM lane quarter this warp may access
+        const int row = q * 32 + lane;            // accumulator lane = weight row in the tile
+        int acc_it = 0;
+        for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++acc_it) {
+            const Unit un = decode_unit(sm, p, u);
+            const int buf = acc_it & 1;
+            if (!__all_sync(0xffffffffu, wait_bar(sm, sm.acc_full[buf], (acc_it >> 1) & 1, p.err))) {
+                sm.abort = 1;
+                break;
+            }
+            tc_fence_after();
+            const int n = un.nt * kRows + row;
+            const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * kTN);
+            for (int c0 = 0; c0 < un.tn; c0 += 16) {
+                uint32_t g[16], v[16];
+                tmem_ld16(t0 + c0, g);
+                if (p.glu) tmem_ld16(t0 + kTN + c0, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    if (c0 + c < un.tn) {
+                        const size_t o = (size_t)(un.r0 + c0 + c) * p.N + n;
+                        float y = __uint_as_float(g[c]);
+                        if (p.glu) {
+                            const float up = __uint_as_float(v[c]);
+                            y = y / (1.0f + expf(-y)) * up;
+                        }
+                        if (p.out_f16)
+                            static_cast<uint16_t*>(p.Y)[o] = __half_as_ushort(__float2half_rn(y));
+                        else
+                            static_cast<float*>(p.Y)[o] = y;
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&sm.acc_empty[buf]));
+        }
+    }
+
+    // Wind down: every role has left its loop (all waits are bounded).  The
+    // last accumulator hand-off already waited for all issued MMAs; on abort
+    // give in-flight tensor-core work a bounded moment via one more commit.
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        if (sm.abort) {
+            if (lane == 0) {
+                // completes once every MMA this thread issued has finished
+                mma_commit(q4d::smem_addr(&sm.drain));
+                q4d::mbar_wait(q4d::smem_addr(&sm.drain), 0, nullptr);
+            }
+            __syncwarp();
+        }
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// Device-side check that expert_ids agrees with offsets (and that offsets
+// are a monotone partition of 0..R-1).
+__global__ void check_routing_kernel(const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ offsets,
+                                     int E, int R, int* err) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) {
+        bool ok = offsets[0] == 0 && offsets[E] == R;
+        for (int e = 0; e < E && ok; ++e) ok = offsets[e] <= offsets[e + 1];
+        if (!ok) atomicOr(err, q4d::kErrDeviceCheck);
+    }
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < R; r += gridDim.x * blockDim.x) {
+        const int e = expert_ids[r];
+        if (e < 0 || e >= E || r < offsets[e] || r >= offsets[e + 1]) atomicOr(err, q4d::kErrDeviceCheck);
+    }
+}
+
+}  // namespace q4g
+
+namespace q4i {
+namespace {
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+q4_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = fn(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+    return Q4_OK;
+}
+
+}  // namespace
+}  // namespace q4i
 
 using namespace q4i;
 
 extern "C" q4_status q4_moe_gemm(const uint32_t* Wq, const uint16_t* scales, const uint16_t* biases,
                                  const uint16_t* X, const int32_t* expert_ids, const int32_t* offsets, void* Y,
-                                 const q4_moe_desc* desc, q4_stream_t stream) {
-    (void)Wq; (void)scales; (void)biases; (void)X; (void)expert_ids; (void)offsets; (void)Y; (void)desc;
-    (void)stream;
+                                 const q4_moe_desc* d, q4_stream_t stream) {
     clear_error();
-    return fail(Q4_ERR_UNSUPPORTED, "q4_moe_gemm is not built in this version");
+    if (!d) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");
+    if (!Wq || !scales || !biases || !X || !expert_ids || !offsets || !Y)
+        return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (d->E < 1 || d->E > q4g::kMaxExperts) return fail(Q4_ERR_INVALID_ARG, "E=%d outside 1..%d", d->E, q4g::kMaxExperts);
+    if (d->K < 64 || d->K % 64) return fail(Q4_ERR_INVALID_ARG, "K=%d is not a positive multiple of 64", d->K);
+    if (d->N < 1) return fail(Q4_ERR_INVALID_ARG, "N=%d", d->N);
+    if (d->N % 128) return fail(Q4_ERR_UNSUPPORTED, "N=%d is not a multiple of 128", d->N);
+    if (d->R < 0) return fail(Q4_ERR_INVALID_ARG, "R=%d", d->R);
+    if (d->mode != Q4_GEMV_PLAIN && d->mode != Q4_GEMV_GLU) return fail(Q4_ERR_INVALID_ARG, "bad mode");
+    if (d->out_dtype != Q4_F32 && d->out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "bad out_dtype");
+    if (d->mode == Q4_GEMV_GLU && d->out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "GLU mode writes fp16");
+    if (!aligned16(Wq) || !aligned16(X)) return fail(Q4_ERR_MISALIGNED, "Wq and X must be 16-byte aligned");
+    if ((long long)d->E * (d->mode == Q4_GEMV_GLU ? 2 : 1) * d->N > (1ll << 31))
+        return fail(Q4_ERR_UNSUPPORTED, "too many weight rows");
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    if (d->R == 0) return Q4_OK;
+
+    q4g::Params p = {};
+    p.scales = scales;
+    p.biases = biases;
+    p.offsets = offsets;
+    p.Y = Y;
+    p.E = d->E;
+    p.N = d->N;
+    p.K = d->K;
+    p.R = d->R;
+    p.glu = d->mode == Q4_GEMV_GLU;
+    p.nmat = p.glu ? 2 : 1;
+    p.rows_e = p.nmat * d->N;
+    p.out_f16 = d->out_dtype == Q4_F16;
+    p.n_tiles = d->N / q4g::kRows;
+    p.nK = d->K / q4g::kKS;
+    p.G = d->K / 64;
+    p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqThreads * (p.G + 1) * 4 + 127) & ~size_t(127));
+    p.err = dev->err_word;
+
+    CUtensorMap tmW, tmX;
+    const uint64_t wrows = (uint64_t)d->E * p.rows_e;
+    st = make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)d->K / 2, wrows, (uint64_t)d->K / 2, 32,
+                  q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != Q4_OK) return st;
+    st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)d->K, (uint64_t)d->R, (uint64_t)d->K * 2,
+                  q4g::kKS, q4g::kTN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != Q4_OK) return st;
+
+    const size_t smem = 1024 + (size_t)q4g::kInStages * q4g::kInStageBytes + (size_t)q4g::kAStages * q4g::kAStageBytes +
+                        p.sb_bytes + sizeof(q4g::Smem);
+    if (smem > (size_t)dev->smem_optin)
+        return fail(Q4_ERR_UNSUPPORTED, "K=%d needs %zu bytes of shared memory", d->K, smem);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    q4g::check_routing_kernel<<<(d->R + 255) / 256 < dev->sms ? (d->R + 255) / 256 : dev->sms, 256, 0, s>>>(
+        expert_ids, offsets, d->E, d->R, dev->err_word);
+    cudaError_t e = cudaFuncSetAttribute(q4g::q4_moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
+    q4g::q4_moe_gemm_kernel<<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmX, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "q4_moe_gemm launch");
+    return Q4_OK;
 }
