@@ -173,6 +173,85 @@ def cpu_oracle_rate(shape, host_model, seconds: float, one_sample: bool = False)
     return done_w / t_total / shape.weights_per_step(), i, t_total
 
 
+def moe_prefill(device, iters: int = 20, warmup: int = 5, token_counts=(128, 512, 2048)):
+    """MoE prefill layer (Qwen3-30B-A3B-shaped: 128 experts, top-8, hidden
+    2048, expert FFN 768): route -> gather -> gate/up GEMM (SiLU*up) -> down
+    GEMM -> combine, timed with CUDA events per stage and as a whole."""
+    import torch
+
+    import bit_quantized_gemv_q4_gb300 as q4
+    import q4synth
+    S = q4synth.QWEN3_30B_A3B_MOE
+    E, k, H, F = S.experts, S.topk, S.hidden, S.ffn
+    gu, dn = q4synth.moe_weights(S)
+
+    def dev(m):
+        return (torch.from_numpy(m.Wq.view("int32")).to(device), torch.from_numpy(m.scales).to(device),
+                torch.from_numpy(m.biases).to(device))
+
+    dgu, ddn = dev(gu), dev(dn)
+    weight_bytes = gu.nbytes() + dn.nbytes()
+    stream = torch.cuda.current_stream(device)
+    out = {"shape": f"{S.name}: E={E} top{k} hidden={H} ffn={F}", "weight_bytes": weight_bytes}
+    for T in token_counts:
+        R = T * k
+        logits = torch.from_numpy(q4synth.router_logits(q4synth.BASE_SEED + 7 + T, T, E)).to(device)
+        X = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 8 + T, T, H)).to(device)
+        ids = torch.empty(T, k, dtype=torch.int32, device=device)
+        w = torch.empty(T, k, device=device)
+        off = torch.empty(E + 1, dtype=torch.int32, device=device)
+        tok = torch.empty(R, dtype=torch.int32, device=device)
+        eid = torch.empty(R, dtype=torch.int32, device=device)
+        pos = torch.empty(T, k, dtype=torch.int32, device=device)
+        nws = q4.q4_moe_route_workspace_bytes(T, E, k)
+        ws = torch.empty(nws, dtype=torch.uint8, device=device)
+        Xs = torch.empty(R, H, dtype=torch.float16, device=device)
+        Hh = torch.empty(R, F, dtype=torch.float16, device=device)
+        Y = torch.empty(R, H, dtype=torch.float16, device=device)
+        o = torch.empty(T, H, dtype=torch.float16, device=device)
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+
+        def layer(record):
+            if record:
+                ev[0].record(stream)
+            q4.q4_moe_route(logits, T, E, k, ids, w, off, tok, eid, pos, ws, nws, stream)
+            q4.q4_moe_gather(X, T, H, tok, R, Xs, stream)
+            if record:
+                ev[1].record(stream)
+            q4.q4_moe_gemm(*dgu, Xs, eid, off, Hh, E, F, H, R, q4.Q4_GEMV_GLU, q4.Q4_F16, stream)
+            if record:
+                ev[2].record(stream)
+            q4.q4_moe_gemm(*ddn, Hh, eid, off, Y, E, H, F, R, q4.Q4_GEMV_PLAIN, q4.Q4_F16, stream)
+            if record:
+                ev[3].record(stream)
+            q4.q4_moe_combine(Y, q4.Q4_F16, H, pos, w, T, k, o, q4.Q4_F16, stream)
+            if record:
+                ev[4].record(stream)
+
+        for _ in range(warmup):
+            layer(False)
+        tot = {"route_gather": 0.0, "gate_up": 0.0, "down": 0.0, "combine": 0.0}
+        for _ in range(iters):
+            layer(True)
+            torch.cuda.synchronize(device)
+            tot["route_gather"] += ev[0].elapsed_time(ev[1])
+            tot["gate_up"] += ev[1].elapsed_time(ev[2])
+            tot["down"] += ev[2].elapsed_time(ev[3])
+            tot["combine"] += ev[3].elapsed_time(ev[4])
+        if q4.q4_device_status(stream) != 0:
+            raise RuntimeError("device status after MoE timing")
+        us = {kk: 1000 * v / iters for kk, v in tot.items()}
+        gemm_us = us["gate_up"] + us["down"]
+        flops = 2.0 * R * (2 * F * H + H * F)
+        out[f"T={T}"] = {
+            "layer_us": sum(us.values()), **{f"{kk}_us": v for kk, v in us.items()},
+            "gemm_tflops": flops / (gemm_us * 1e-6) / 1e12,
+            "gemm_weight_gbs": weight_bytes / (gemm_us * 1e-6) / 1e9,
+            "prefill_tok_per_s": T / (sum(us.values()) * 1e-6),
+        }
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -181,6 +260,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--section", default="all", choices=["all", "decode", "moe"],
+                    help="moe: only the MoE prefill timings (for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -242,6 +323,9 @@ def main():
 
     torch.cuda.set_device(local)
     device = torch.device("cuda", local)
+    if args.section == "moe":
+        print(json.dumps({"moe_prefill": moe_prefill(device)}))
+        return
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
@@ -360,6 +444,8 @@ def main():
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if args.section == "all":
+        out["moe_prefill"] = moe_prefill(device)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
