@@ -34,8 +34,8 @@ STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q
 # Every symbol include/q4.h declares.
 EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status", "q4_gemv",
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
-           "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_gather",
-           "q4_moe_gemm", "q4_moe_combine"]
+           "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
+           "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine"]
 
 
 class Q4Error(RuntimeError):
@@ -118,6 +118,8 @@ def lib() -> ctypes.CDLL:
         L.q4_moe_route_workspace_bytes.argtypes = [i32, i32, i32]
         L.q4_moe_route.restype = st
         L.q4_moe_route.argtypes = [vp, i32, i32, i32] + [vp] * 7 + [ctypes.c_size_t, vp]
+        L.q4_moe_route_noalloc.restype = st
+        L.q4_moe_route_noalloc.argtypes = [vp, i32, i32, i32] + [vp] * 6 + [vp]
         L.q4_moe_gather.restype = st
         L.q4_moe_gather.argtypes = [vp, i32, i32, vp, i32, vp, vp]
         L.q4_moe_gemm.restype = st
@@ -264,6 +266,14 @@ def q4_moe_route(logits, T, E, topk, topk_ids, topk_weights, offsets, token_of, 
     _check(lib().q4_moe_route(_ptr(logits), T, E, topk, _ptr(topk_ids), _ptr(topk_weights), _ptr(offsets),
                               _ptr(token_of), _ptr(expert_of), _ptr(pos), _ptr(workspace), workspace_bytes,
                               _stream(stream)), "q4_moe_route")
+
+
+def q4_moe_route_noalloc(logits, T, E, topk, topk_ids, topk_weights, offsets, token_of, expert_of, pos,
+                         stream=None):
+    """q4_moe_route with the library's static scratch instead of a workspace."""
+    _check(lib().q4_moe_route_noalloc(_ptr(logits), T, E, topk, _ptr(topk_ids), _ptr(topk_weights), _ptr(offsets),
+                                      _ptr(token_of), _ptr(expert_of), _ptr(pos), _stream(stream)),
+           "q4_moe_route_noalloc")
 
 
 def q4_moe_gather(X, T, K, token_of, R, X_sorted, stream=None):

@@ -12,6 +12,8 @@
 // All integer outputs are deterministic (no atomics decide an order).
 #include <cuda_fp16.h>
 
+#include <mutex>
+
 #include "q4_device.cuh"
 #include "q4_internal.h"
 
@@ -259,3 +261,69 @@ q4_status q4_moe_combine(const void* Y, q4_dtype y_dtype, int N, const int32_t* 
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Allocation-free routing.
+//
+// Some callers cannot allocate device memory: a plugin inside a host runtime
+// that owns every device buffer and hands the plugin only the tensors it
+// works on, or a serving loop whose allocator is fixed at load time.  For
+// them q4_moe_route_noalloc runs the same four routing kernels as
+// q4_moe_route, with the per-(expert, 32-token block) counters in the
+// file-scope array below instead of a caller workspace.  The array lives on
+// every device that loads the library until the process exits.
+// ---------------------------------------------------------------------------
+namespace q4m {
+constexpr int kStaticRouteCounters = 1 << 16;  // 65536 int32 = 256 KB
+static __device__ __align__(256) int32_t g_route_scratch[kStaticRouteCounters];
+}  // namespace q4m
+
+namespace {
+std::mutex g_route_scratch_mutex;
+int32_t* g_route_scratch_ptr[64];  // device address of the array, per device ordinal
+}  // namespace
+
+extern "C" q4_status q4_moe_route_noalloc(const uint16_t* logits, int T, int E, int topk, int32_t* topk_ids,
+                                          float* topk_weights, int32_t* offsets, int32_t* token_of,
+                                          int32_t* expert_of, int32_t* pos, q4_stream_t stream) {
+    clear_error();
+    if (!logits || !topk_ids || !topk_weights || !offsets || !token_of || !expert_of || !pos)
+        return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (T < 1 || E < 1 || E > q4m::kMaxExperts || topk < 1 || topk > q4m::kMaxTopk || topk > E)
+        return fail(Q4_ERR_INVALID_ARG, "T=%d E=%d topk=%d (need T>=1, 1<=E<=%d, 1<=topk<=min(E,%d))", T, E,
+                    topk, q4m::kMaxExperts, q4m::kMaxTopk);
+    const long long B = (T + q4m::kBlockTokens - 1) / q4m::kBlockTokens;
+    if (B * E > q4m::kStaticRouteCounters)
+        return fail(Q4_ERR_UNSUPPORTED,
+                    "T=%d, E=%d need %lld counters; the static scratch holds %d (at most %lld tokens for E=%d); "
+                    "use q4_moe_route with a workspace",
+                    T, E, B * E, q4m::kStaticRouteCounters,
+                    (long long)q4m::kBlockTokens * (q4m::kStaticRouteCounters / E), E);
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    int32_t* scratch = nullptr;
+    {
+        // Set-up, once per device, with that device current: the host-side
+        // name of the array is not a device address; ask the runtime for it.
+        std::lock_guard<std::mutex> lock(g_route_scratch_mutex);
+        if (!g_route_scratch_ptr[dev->device]) {
+            void* p = nullptr;
+            cudaError_t e = cudaGetSymbolAddress(&p, q4m::g_route_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(routing scratch)");
+            g_route_scratch_ptr[dev->device] = static_cast<int32_t*>(p);
+        }
+        scratch = g_route_scratch_ptr[dev->device];
+    }
+    // Every counter the kernels read is written first by route_count_kernel,
+    // so nothing in the array has to start at zero.
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int Bi = (int)B;
+    q4m::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights);
+    q4m::route_count_kernel<<<Bi, 32, 0, s>>>(topk_ids, T, E, topk, Bi, scratch);
+    q4m::route_scan_kernel<<<1, 1024, 0, s>>>(scratch, E, Bi, offsets);
+    q4m::route_scatter_kernel<<<Bi, 32, 0, s>>>(topk_ids, T, topk, Bi, scratch, token_of, expert_of, pos);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "q4_moe_route_noalloc launch");
+    return Q4_OK;
+}

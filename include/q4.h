@@ -262,6 +262,27 @@ q4_status q4_moe_route(const uint16_t *logits, int T, int E, int topk, int32_t *
                        int32_t *expert_of, int32_t *pos, void *workspace,
                        size_t workspace_bytes, q4_stream_t stream);
 
+/* q4_moe_route without a caller workspace: the pages have no counterpart to
+ * this entry point.  It is for callers that cannot allocate device memory --
+ * a plugin inside a host runtime that owns every device buffer and passes in
+ * only the tensors to work on, or a serving loop whose allocations are fixed
+ * at load time -- so it calls no cudaMalloc, cudaFree or allocating library
+ * routine.  Same arguments, outputs and results as q4_moe_route.
+ *
+ * Its scratch (the per-(expert, 32-token block) counters) is a static
+ * 256 KB array in the library, present on every device that loads the library
+ * until the process exits: ceil(T/32) * E must not exceed 65536 (e.g. at most
+ * 16384 tokens for 128 experts); larger requests fail with Q4_ERR_UNSUPPORTED
+ * before anything is enqueued.  The first call on a device looks up the
+ * array's device address with that device current (a host-side set-up step;
+ * make that first call before any stream capture).  Every call shares the
+ * one array and the kernels write every counter they read, so nothing needs
+ * clearing between calls; calls that can overlap on the GPU (other streams,
+ * other host threads) race on it and must be ordered by the caller. */
+q4_status q4_moe_route_noalloc(const uint16_t *logits, int T, int E, int topk, int32_t *topk_ids,
+                               float *topk_weights, int32_t *offsets, int32_t *token_of,
+                               int32_t *expert_of, int32_t *pos, q4_stream_t stream);
+
 /* X_sorted[r][:] = X[token_of[r]][:] for r < R.  X: fp16 [T][K], K % 8 == 0. */
 q4_status q4_moe_gather(const uint16_t *X, int T, int K, const int32_t *token_of, int R,
                         uint16_t *X_sorted, q4_stream_t stream);
