@@ -206,12 +206,35 @@ __device__ __forceinline__ void dot_rows(const Params& p, const uint32_t* wq, co
 #pragma unroll
     for (int r = 0; r < RB; ++r)
 #pragma unroll
-        for (int m = 0; m < M; ++m) {
-            float v = acc[r][m].x + acc[r][m].y;
+        for (int m = 0; m < M; ++m) out[r][m] = acc[r][m].x + acc[r][m].y;
+}
+
+// Sum V values (power of two, V <= 32) across the 32 lanes of a warp with a
+// transposing butterfly: each halving round exchanges half of the values
+// still held, so V values cost about 4*(V-1) + 2*(5 - log2 V) instructions
+// instead of 10*V.  On return lane L holds the total of value index
+// (L >> (5 - log2 V)) in v[0]; the order of additions is fixed.
+template <int V>
+__device__ __forceinline__ void warp_sum_transpose(float* v, int lane) {
+    constexpr int LOGV = (V >= 32) ? 5 : (V >= 16) ? 4 : (V >= 8) ? 3 : (V >= 4) ? 2 : (V >= 2) ? 1 : 0;
+    int n = V;
 #pragma unroll
-            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-            out[r][m] = v;
+    for (int r = 0; r < LOGV; ++r) {
+        const int o = 16 >> r;
+        const bool upper = (lane & o) != 0;
+        const int half = n >> 1;
+#pragma unroll
+        for (int i = 0; i < V / 2; ++i) {
+            if (i < half) {
+                const float send = upper ? v[i] : v[i + half];
+                const float keep = upper ? v[i + half] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
         }
+        n = half;
+    }
+#pragma unroll
+    for (int o = 16 >> LOGV; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
 __device__ __forceinline__ void store_out(const Params& p, const Seg& sg, int m, int n, float v) {
@@ -244,30 +267,43 @@ __device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, 
     }
     float out[RB][M];
     dot_rows<M, RB>(p, wq, ss, bs, xs, rows, lane, out);
+    // Reduce all RB*M values at once; afterwards lane L holds value index
+    // idx = L >> SH (idx = r*M + m), and the lanes with L % 2^SH == 0 store.
+    constexpr int V = RB * M;
+    constexpr int VP = (V > 16) ? 32 : (V > 8) ? 16 : (V > 4) ? 8 : (V > 2) ? 4 : (V > 1) ? 2 : 1;  // power of two
+    constexpr int SH = 5 - ((VP >= 32) ? 5 : (VP >= 16) ? 4 : (VP >= 8) ? 3 : (VP >= 4) ? 2 : (VP >= 2) ? 1 : 0);
+    float v[VP];
+#pragma unroll
+    for (int i = V; i < VP; ++i) v[i] = 0.f;
 #pragma unroll
     for (int r = 0; r < RB; ++r)
 #pragma unroll
-        for (int m = 0; m < M; ++m) out[r][m] *= scale[m];
+        for (int m = 0; m < M; ++m) v[r * M + m] = out[r][m];
+    warp_sum_transpose<VP>(v, lane);
+    const int idx_raw = lane >> SH;
+    const bool holds = idx_raw < V;   // lanes past V hold padding
+    const int idx = holds ? idx_raw : 0;
+    const int r_l = idx / M, m_l = idx - r_l * M;
+    int local = 0;
+    float sc = 1.0f;
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+        if (r == r_l) local = locals[r];
+#pragma unroll
+    for (int m = 0; m < M; ++m)
+        if (m == m_l) sc = scale[m];
+    const float y = v[0] * sc;
     if (p.glu) {
-#pragma unroll
-        for (int r = 0; r < RB; r += 2) {
-#pragma unroll
-            for (int m = 0; m < M; ++m) {
-                if (lane == (r / 2) * M + m && locals[r] < nrows) {
-                    const float g = out[r][m], u = out[r + 1][m];
-                    const float a = g / (1.0f + expf(-g)) * u;
-                    const Seg& sg = p.seg[0];
-                    reinterpret_cast<uint16_t*>(sg.y)[(size_t)m * sg.ldy + n0 + locals[r]] =
-                        __half_as_ushort(__float2half_rn(a));
-                }
-            }
+        // gate (even r) and up (odd r) of one output row: the up total sits M
+        // value indices further on
+        const float u = __shfl_down_sync(0xffffffffu, y, M << SH);
+        if (holds && (lane & ((1 << SH) - 1)) == 0 && (r_l & 1) == 0 && local < nrows) {
+            const float a = y / (1.0f + expf(-y)) * u;
+            const Seg& sg = p.seg[0];
+            reinterpret_cast<uint16_t*>(sg.y)[(size_t)m_l * sg.ldy + n0 + local] = __half_as_ushort(__float2half_rn(a));
         }
-    } else {
-#pragma unroll
-        for (int r = 0; r < RB; ++r)
-#pragma unroll
-            for (int m = 0; m < M; ++m)
-                if (lane == r * M + m && locals[r] < nrows) store_out(p, p.seg[si], m, n0 + locals[r], out[r][m]);
+    } else if (holds && (lane & ((1 << SH) - 1)) == 0 && local < nrows) {
+        store_out(p, p.seg[si], m_l, n0 + local, y);
     }
 }
 
