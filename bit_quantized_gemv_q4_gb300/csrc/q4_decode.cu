@@ -30,7 +30,9 @@ struct Dims {
 };
 
 struct Layout {
-    size_t h = 0, h_mid = 0, q = 0, k = 0, v = 0, act = 0, total = 0;
+    size_t h = 0, h_mid = 0, q = 0, k = 0, v = 0, act = 0;
+    // tagged copies of the activations that later stages read, and counters
+    size_t h_t = 0, hm_t = 0, q_t = 0, act_t = 0, ctr = 0, tagged_begin = 0, total = 0;
 };
 
 struct Plan {
@@ -48,6 +50,9 @@ struct Plan {
     const void* x_key = nullptr;
     void* logits_key = nullptr;
     std::vector<q4_gemv_desc> stages;
+    std::vector<GemvTagged> tagged;  // per stage, used when tagged_mode
+    bool tagged_mode = false;
+    bool tagged_ready = false;       // tagged region zeroed
     cudaStream_t capture_stream = nullptr;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -117,6 +122,12 @@ Layout layout_of(const Dims& d) {
     l.k = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
     l.v = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
     l.act = take((size_t)d.M * (d.ffn > 0 ? d.ffn : 1));
+    l.tagged_begin = off;
+    l.h_t = take((size_t)d.M * d.hidden * 2);
+    l.hm_t = take((size_t)d.M * d.hidden * 2);
+    l.q_t = take((size_t)d.M * (d.qN > 0 ? d.qN : 1) * 2);
+    l.act_t = take((size_t)d.M * (d.ffn > 0 ? d.ffn : 1) * 2);
+    l.ctr = take(128);
     l.total = off;
     return l;
 }
@@ -142,7 +153,49 @@ void build_stages(Plan& p, const uint16_t* x, void* logits) {
     uint16_t* v = reinterpret_cast<uint16_t*>(ws + p.lay.v);
     uint16_t* act = reinterpret_cast<uint16_t*>(ws + p.lay.act);
     const int M = p.dims.M, H = p.dims.hidden;
+    uint32_t* h_t = reinterpret_cast<uint32_t*>(ws + p.lay.h_t);
+    uint32_t* hm_t = reinterpret_cast<uint32_t*>(ws + p.lay.hm_t);
+    uint32_t* q_t = reinterpret_cast<uint32_t*>(ws + p.lay.q_t);
+    uint32_t* act_t = reinterpret_cast<uint32_t*>(ws + p.lay.act_t);
+    uint32_t* ctr = reinterpret_cast<uint32_t*>(ws + p.lay.ctr);
+    const int NS = 4 * p.dims.L + 1;
+    auto tagged = [&](int stage, const uint32_t* x, int x_stage) {
+        GemvTagged t;
+        t.x = x;
+        t.x_stage = x_stage;
+        t.step_ctr = ctr;
+        t.done_ctr = ctr + 1;
+        t.stage = stage;
+        t.n_stages = NS;
+        return t;
+    };
     p.stages.clear();
+    p.tagged.clear();
+    for (int l = 0; l < p.dims.L; ++l) {
+        // stages of layer l: 4l QKV, 4l+1 o, 4l+2 gate/up, 4l+3 down
+        const uint32_t* h_in_t = l == 0 ? nullptr : h_t;  // layer 0 reads the caller's plain x
+        GemvTagged t = tagged(4 * l, h_in_t, 4 * l - 1);
+        t.y[0] = q_t;
+        p.tagged.push_back(t);
+        t = tagged(4 * l + 1, q_t, 4 * l);
+        t.y[0] = hm_t;
+        t.res[0] = h_in_t;
+        t.res_stage = 4 * l - 1;
+        p.tagged.push_back(t);
+        t = tagged(4 * l + 2, hm_t, 4 * l + 1);
+        t.y[0] = act_t;
+        p.tagged.push_back(t);
+        t = tagged(4 * l + 3, act_t, 4 * l + 2);
+        t.y[0] = h_t;
+        t.res[0] = hm_t;
+        t.res_stage = 4 * l + 1;
+        p.tagged.push_back(t);
+    }
+    {
+        GemvTagged t = tagged(NS - 1, p.dims.L > 0 ? h_t : nullptr, NS - 2);
+        t.last = true;
+        p.tagged.push_back(t);
+    }
     for (int l = 0; l < p.dims.L; ++l) {
         const q4_layer_weights& w = p.layers[l];
         const uint16_t* hin = l == 0 ? x : h;
@@ -187,7 +240,7 @@ void build_stages(Plan& p, const uint16_t* x, void* logits) {
 q4_status enqueue_stages(Plan& p, cudaStream_t s) {
     const bool pdl = !(p.flags & Q4_DECODE_NO_PDL);
     for (size_t i = 0; i < p.stages.size(); ++i) {
-        q4_status st = launch_gemv(p.stages[i], s, pdl && i > 0, true);
+        q4_status st = launch_gemv(p.stages[i], s, pdl && i > 0, true, p.tagged_mode ? &p.tagged[i] : nullptr);
         if (st != Q4_OK) return st;
     }
     return Q4_OK;
@@ -288,6 +341,12 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
         p->workspace = table->workspace;
         p->workspace_bytes = table->workspace_bytes;
         p->flags = table->flags;
+        p->tagged_mode = (table->flags & Q4_DECODE_TAGGED) != 0;
+        for (int l = 0; l < d.L && p->tagged_mode; ++l) {
+            const q4_layer_weights& w = table->layers[l];
+            p->tagged_mode = gemv_fits_unsplit(d.M, d.hidden) && gemv_fits_unsplit(d.M, w.o.K) &&
+                             gemv_fits_unsplit(d.M, w.down.K);
+        }
         table->plan = p;
     }
     int dev = -1;
@@ -298,6 +357,14 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
         p->x_key = x;
         p->logits_key = logits;
         drop_graph(*p);
+    }
+    if (p->tagged_mode && !p->tagged_ready) {
+        // Once, on the caller's stream and outside any capture: tags start at
+        // 1, so zeroed words never look ready; the step counter starts at 0.
+        cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(p->workspace) + p->lay.tagged_begin, 0,
+                                        p->lay.total - p->lay.tagged_begin, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the tagged activations");
+        p->tagged_ready = true;
     }
     if (p->flags & Q4_DECODE_NO_GRAPH) return enqueue_stages(*p, s);
     if (!p->exec) {

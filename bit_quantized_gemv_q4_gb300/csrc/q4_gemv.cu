@@ -52,20 +52,71 @@ struct Seg {
     const uint16_t* b;
     void* y;
     const uint16_t* res;
+    uint32_t* y_tag;          // tagged copy of y (decode step), or nullptr
+    const uint32_t* res_tag;  // tagged residual (decode step), or nullptr
     int N, ldy, tile_begin, tiles;
 };
 
 struct Params {
     Seg seg[Q4_MAX_SEGMENTS];
     const uint16_t* x;
+    const uint32_t* x_tag;    // tagged x (decode step), or nullptr
     int nseg, K, ldx, TR, rows_per_tile, total_tiles, stages;
     int out_f16, glu, early_prefetch;
     int norm;                // RMSNorm of each x row on load
     const uint16_t* norm_w;  // fp16 [K] or nullptr (ones)
     float norm_eps;
     uint32_t stage_bytes, x_bytes;
+    // decode-step tags: tag(stage) = 1 + (step * n_stages + stage) mod 65535
+    const uint32_t* step_ctr;
+    uint32_t* done_ctr;
+    int stage, n_stages, x_stage, res_stage, last;
     int* err;
 };
+
+__device__ __forceinline__ uint32_t tag_of(uint32_t step, int stage, int n_stages) {
+    return 1u + (uint32_t)(((unsigned long long)step * (unsigned)n_stages + (unsigned)stage) % 65535ull);
+}
+
+// Poll tagged words until every tag equals `tag` (bounded; on expiry the
+// error word is latched and whatever was read is used).
+template <int NW>
+__device__ __forceinline__ void poll_tagged(const uint32_t* src, uint32_t tag, uint32_t* w, int* err) {
+    unsigned long long t0 = 0;
+    while (true) {
+        bool ok = true;
+        if constexpr (NW == 8) {
+            const uint4 a = q4d::ld_relaxed_v4(src), b = q4d::ld_relaxed_v4(src + 4);
+            w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w; w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+        } else {
+            w[0] = q4d::ld_relaxed(src);
+        }
+#pragma unroll
+        for (int i = 0; i < NW; ++i) ok &= (w[i] >> 16) == tag;
+        if (ok) return;
+        if (t0 == 0) {
+            t0 = q4d::globaltimer();
+        } else if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
+            atomicOr(err, q4d::kErrTimeout);
+            return;
+        }
+        __nanosleep(100);  // let the producing kernel use the issue slots and L2
+    }
+}
+
+// One warp waits for a sample of a tagged x (the last word of each 32nd of
+// every row) before the whole CTA reads it: a poll then moves 128 bytes per
+// row instead of the whole vector, which leaves L2 to the producing grid.
+template <int M>
+__device__ __forceinline__ void gate_tagged_x(const Params& p, uint32_t tag, int lane) {
+    const int W = p.K / 32;  // words per 32nd of a row (K is a multiple of 64)
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        uint32_t w;
+        poll_tagged<1>(p.x_tag + (size_t)m * p.ldx + (size_t)(lane + 1) * W - 1, tag, &w, p.err);
+    }
+    __syncwarp();
+}
 
 // Lane words (LW): how many uint32 (8 codes each) one lane handles per chunk.
 template <int M>
@@ -237,19 +288,35 @@ __device__ __forceinline__ void warp_sum_transpose(float* v, int lane) {
     for (int o = 16 >> LOGV; o > 0; o >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
 }
 
-__device__ __forceinline__ void store_out(const Params& p, const Seg& sg, int m, int n, float v) {
+// fp16 store of one output, plus its tagged copy when the stage publishes one.
+__device__ __forceinline__ void store_f16(const Seg& sg, size_t i, float v, uint32_t tag) {
+    const uint16_t h = __half_as_ushort(__float2half_rn(v));
+    reinterpret_cast<uint16_t*>(sg.y)[i] = h;
+    if (sg.y_tag) q4d::st_relaxed(sg.y_tag + i, (tag << 16) | h);
+}
+
+__device__ __forceinline__ void store_out(const Params& p, const Seg& sg, int m, int n, float v, uint32_t ytag,
+                                          uint32_t rtag) {
+    const size_t i = (size_t)m * sg.ldy + n;
     if (p.out_f16) {
-        if (sg.res) v += __half2float(__ushort_as_half(sg.res[(size_t)m * sg.ldy + n]));
-        reinterpret_cast<uint16_t*>(sg.y)[(size_t)m * sg.ldy + n] = __half_as_ushort(__float2half_rn(v));
+        if (sg.res_tag) {
+            uint32_t w;
+            poll_tagged<1>(sg.res_tag + i, rtag, &w, p.err);
+            v += __half2float(__ushort_as_half((uint16_t)(w & 0xFFFFu)));
+        } else if (sg.res) {
+            v += __half2float(__ushort_as_half(sg.res[i]));
+        }
+        store_f16(sg, i, v, ytag);
     } else {
-        reinterpret_cast<float*>(sg.y)[(size_t)m * sg.ldy + n] = v;
+        reinterpret_cast<float*>(sg.y)[i] = v;
     }
 }
 
 template <int M, int RB>
 __device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, const uint16_t* ss,
                                            const uint16_t* bs, const float4* xs, const float* scale, int warp,
-                                           int lane, int j_begin, int rpw, int si, int n0, int nrows) {
+                                           int lane, int j_begin, int rpw, int si, int n0, int nrows,
+                                           uint32_t ytag, uint32_t rtag) {
     int rows[RB];
     int locals[RB];
 #pragma unroll
@@ -300,10 +367,10 @@ __device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, 
         if (holds && (lane & ((1 << SH) - 1)) == 0 && (r_l & 1) == 0 && local < nrows) {
             const float a = y / (1.0f + expf(-y)) * u;
             const Seg& sg = p.seg[0];
-            reinterpret_cast<uint16_t*>(sg.y)[(size_t)m_l * sg.ldy + n0 + local] = __half_as_ushort(__float2half_rn(a));
+            store_f16(sg, (size_t)m_l * sg.ldy + n0 + local, a, ytag);
         }
     } else if (holds && (lane & ((1 << SH) - 1)) == 0 && local < nrows) {
-        store_out(p, p.seg[si], m_l, n0 + local, y);
+        store_out(p, p.seg[si], m_l, n0 + local, y, ytag, rtag);
     }
 }
 
@@ -353,7 +420,7 @@ __device__ __forceinline__ void stage_norm_weight(const Params& p, float4* xs) {
 // norm_scales); the scalar 1/rms is applied to the dot products in the
 // epilogue, so x is read once.
 template <int M>
-__device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, int warp, int lane) {
+__device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, int warp, int lane, uint32_t xtag) {
     constexpr int kCT = kConsumerWarps * 32;
     const int W8 = p.K / 8;
     const bool gw = p.norm && p.norm_w;
@@ -364,7 +431,14 @@ __device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, 
 #pragma unroll
         for (int m = 0; m < M; ++m) {
             float f[8];
-            load8_f32(p.x + (size_t)m * p.ldx + 8 * j, f);
+            if (p.x_tag) {
+                uint32_t w[8];
+                poll_tagged<8>(p.x_tag + (size_t)m * p.ldx + 8 * j, xtag, w, p.err);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) f[e] = __half2float(__ushort_as_half((uint16_t)(w[e] & 0xFFFFu)));
+            } else {
+                load8_f32(p.x + (size_t)m * p.ldx + 8 * j, f);
+            }
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss[m] = fmaf(f[e], f[e], ss[m]);
             float4* d0 = x_slot<M>(xs, j, m, 0);
@@ -416,15 +490,22 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
     uint8_t* stages = smem + p.x_bytes + kBarBytes;
     const uint32_t full0 = q4d::smem_addr(bars), empty0 = q4d::smem_addr(bars + kMaxStages);
 
+    __shared__ uint32_t step_sh;
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             q4d::mbar_init(full0 + 8 * i, 32);               // every producer lane arrives
             q4d::mbar_init(empty0 + 8 * i, kConsumerWarps);  // one arrival per consumer warp
         }
         q4d::fence_mbar_init();
+        // decode-step counter, read at launch (off the critical path when the
+        // kernel was launched early)
+        step_sh = p.step_ctr ? q4d::ld_relaxed(p.step_ctr) : 0u;
     }
     __syncthreads();
-    q4d::pdl_trigger();
+    // With a plain x the dependents may launch at once (they only stream
+    // weights until this grid completes); with a tagged x they launch once
+    // this grid holds its x, so at most one grid polls at a time.
+    if (!p.x_tag) q4d::pdl_trigger();
 
     if (warp == kConsumerWarps) {
         // ------------------------------------------------------ producer warp
@@ -459,9 +540,24 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
 
     // ---------------------------------------------------------- consumers
     if (p.norm && p.norm_w) stage_norm_weight<M>(p, xs);
-    q4d::pdl_wait();  // x and residuals may come from the previous kernel
-    load_x<M>(p, xs, red, warp, lane);
+    uint32_t xtag = 0, ytag = 0, rtag = 0;
+    if (p.step_ctr) {
+        const uint32_t step = step_sh;
+        xtag = tag_of(step, p.x_stage, p.n_stages);
+        ytag = tag_of(step, p.stage, p.n_stages);
+        rtag = tag_of(step, p.res_stage, p.n_stages);
+    }
+    // A tagged x is polled directly (its producer may still be running); a
+    // plain x and plain residuals wait for the previous grid to complete.
+    if (!p.x_tag) {
+        q4d::pdl_wait();
+    } else {
+        if (warp == 0) gate_tagged_x<M>(p, xtag, lane);
+        q4d::named_bar(1, kConsumerWarps * 32);
+    }
+    load_x<M>(p, xs, red, warp, lane, xtag);
     q4d::named_bar(1, kConsumerWarps * 32);
+    if (p.x_tag) q4d::pdl_trigger();
     float scale[M];
     norm_scales<M>(p, red, scale);
 
@@ -470,7 +566,9 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
     int i = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++i) {
         const int st = i % S, k = i / S;
-        if (!q4d::mbar_wait(full0 + 8 * st, k & 1, p.err)) return;
+        // on a timeout leave the loop (not the kernel): every consumer warp
+        // must still reach the barrier below
+        if (!q4d::mbar_wait(full0 + 8 * st, k & 1, p.err)) break;
         const uint8_t* stage = stages + (size_t)st * p.stage_bytes;
         const uint32_t* wq = reinterpret_cast<const uint32_t*>(stage);
         const uint16_t* ss = reinterpret_cast<const uint16_t*>(stage + (size_t)R * (K / 2));
@@ -479,16 +577,28 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
         find_tile(p, t, si, n0, nrows);
         if (rpw >= RB) {
             for (int j = 0; j < rpw; j += RB)
-                tile_batch<M, RB>(p, wq, ss, bs, xs, scale, warp, lane, j, rpw, si, n0, nrows);
+                tile_batch<M, RB>(p, wq, ss, bs, xs, scale, warp, lane, j, rpw, si, n0, nrows, ytag, rtag);
         } else if (rpw == 4) {
-            tile_batch<M, (RB < 4 ? RB : 4)>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows);
+            tile_batch<M, (RB < 4 ? RB : 4)>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
         } else if (rpw == 2) {
-            tile_batch<M, 2>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows);
+            tile_batch<M, 2>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
         } else {
-            tile_batch<M, 1>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows);
+            tile_batch<M, 1>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
         }
         __syncwarp();
         if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
+    }
+    if (p.last) {
+        // The last stage of a decode step: the last CTA to finish advances the
+        // step counter (every CTA of this launch read it at its start).
+        q4d::named_bar(1, kConsumerWarps * 32);
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(p.done_ctr, 1u) == gridDim.x - 1) {
+                *p.done_ctr = 0;
+                atomicAdd(const_cast<uint32_t*>(p.step_ctr), 1u);
+            }
+        }
     }
 }
 
@@ -571,7 +681,17 @@ cudaError_t launch_m(const Params& p, dim3 grid, size_t smem, cudaStream_t strea
 
 }  // namespace
 
-q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch) {
+bool gemv_fits_unsplit(int M, int K) {
+    const DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != Q4_OK) return false;
+    const uint32_t row_bytes = (uint32_t)(K / 2 + (K / 64) * 4);
+    const uint32_t stage = ((uint32_t)(2 * 8) * row_bytes + 127u) & ~127u;  // smallest GLU tile
+    const uint32_t fixed = ((x_smem_bytes(M, K) + 127u) & ~127u) + q4k::kBarBytes;
+    return fixed + 2 * stage <= (uint32_t)dev->smem_optin;
+}
+
+q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch,
+                      const GemvTagged* tg) {
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
@@ -590,6 +710,17 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     p.norm_w = d.norm_weight;
     p.norm_eps = d.norm_eps;
     p.err = dev->err_word;
+    p.n_stages = 1;
+    if (tg) {
+        p.x_tag = tg->x;
+        p.x_stage = tg->x_stage;
+        p.res_stage = tg->res_stage;
+        p.step_ctr = tg->step_ctr;
+        p.done_ctr = tg->done_ctr;
+        p.stage = tg->stage;
+        p.n_stages = tg->n_stages;
+        p.last = tg->last ? 1 : 0;
+    }
 
     // Tile rows: largest of 64/32/16/8 (per matrix) whose tile count still
     // covers every SM, with a stage of at most 48 KB.
@@ -613,6 +744,8 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
         g.b = s.biases;
         g.y = s.y;
         g.res = s.residual;
+        g.y_tag = tg ? tg->y[i] : nullptr;
+        g.res_tag = tg ? tg->res[i] : nullptr;
         g.N = s.N;
         g.ldy = s.ldy ? s.ldy : s.N;
         g.tile_begin = glu ? 0 : tiles;
@@ -638,6 +771,7 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
         // x for all M rows does not fit next to two weight stages: run the
         // rows of x in two halves (the weights are then streamed twice).
         if (M == 1) return fail(Q4_ERR_UNSUPPORTED, "K=%d needs more shared memory than the device has", K);
+        if (tg) return fail(Q4_ERR_UNSUPPORTED, "M=%d, K=%d does not fit one launch of a decode stage", M, K);
         q4_gemv_desc lo = d, hi = d;
         lo.M = (M + 1) / 2;
         hi.M = M - lo.M;

@@ -31,9 +31,29 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 // ---- fused multi-segment GEMV (q4_gemv.cu) --------------------------------
 q4_status validate_gemv(const q4_gemv_desc& d);
+
+// Tagged activations, used inside a decode step: every activation element is
+// a 32-bit word (fp16 value | 16-bit tag << 16), the tag naming the decode
+// step and the stage that wrote it.  A kernel whose x is tagged does not wait
+// for its predecessor grid to complete; it polls the words it needs.
+struct GemvTagged {
+    const uint32_t* x = nullptr;                       // tagged x, or nullptr (plain desc.x)
+    int x_stage = 0;                                   // stage that writes x
+    uint32_t* y[Q4_MAX_SEGMENTS] = {};                 // tagged copies of the outputs (optional)
+    const uint32_t* res[Q4_MAX_SEGMENTS] = {};         // tagged residuals (instead of plain ones)
+    int res_stage = 0;
+    const uint32_t* step_ctr = nullptr;                // decode-step counter
+    uint32_t* done_ctr = nullptr;                      // CTA completion counter (last stage only)
+    int stage = 0, n_stages = 1;
+    bool last = false;                                 // this launch advances step_ctr when done
+};
+
 // early_prefetch: weight copies may start before the programmatic-dependency
 // wait (only when the weights are not written by a preceding kernel).
-q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch);
+q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch,
+                      const GemvTagged* tg = nullptr);
+// True when one launch of (M, K) fits in shared memory without splitting M.
+bool gemv_fits_unsplit(int M, int K);
 
 // ---- MoE (q4_moe.cu, q4_moe_gemm.cu) ---------------------------------------
 size_t moe_route_workspace_bytes(int T, int E, int topk);

@@ -176,7 +176,13 @@ q4_status q4_gemv_ex(const q4_gemv_desc *desc, q4_stream_t stream);
  * them into a CUDA graph (programmatic dependent launch between the kernels,
  * so each kernel's weight stream starts before its predecessor ends); later
  * calls replay the graph.  A call with different x or logits pointers
- * re-captures.  Host memory for the plan is allocated on that first call
+ * re-captures.  With Q4_DECODE_TAGGED, activations are handed from stage to
+ * stage as 32-bit words holding the fp16 value and a 16-bit tag naming the step
+ * and the writing stage; a stage polls the words it reads instead of waiting
+ * for the whole previous kernel to finish.  The workspace always reserves room
+ * for these tagged copies and a step counter; they are cleared on the first
+ * tagged call (on
+ * `stream`) and must not be shared with another table while in use.  Host memory for the plan is allocated on that first call
  * (load time); replays allocate nothing.  x: fp16 [M][hidden].  logits:
  * [M][vocab].  The workspace (device, >= q4_decode_workspace_bytes) holds the
  * activations; after a step it holds the LAST layer's q, k, v, h', act and the
@@ -199,6 +205,8 @@ typedef struct q4_layer_weights {
 
 #define Q4_DECODE_NO_GRAPH 1 /* launch the kernels directly each call (no capture) */
 #define Q4_DECODE_NO_PDL 2   /* no programmatic dependent launch between kernels */
+#define Q4_DECODE_TAGGED 4    /* stages poll tagged activation words (see below) instead of
+                                 waiting for their predecessor grid to complete */
 
 typedef struct q4_layer_table {
     int n_layers;

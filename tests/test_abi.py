@@ -137,8 +137,9 @@ def test_decode_table_validation_and_workspace(L):
              "up": lin(192, 64), "down": lin(64, 192)}
     t = q4.LayerTable([layer, layer], lin(100, 64), hidden=64, M=2)
     n = q4.q4_decode_workspace_bytes(t)
-    # h, h_mid: 2*64*2 bytes each; q: 2*128*2; k, v: 2*64*2; act: 2*192*2; each rounded to 256
-    assert n == 256 + 256 + 512 + 256 + 256 + 768
+    # plain fp16: h, h_mid 2*64*2 B each; q 2*128*2; k, v 2*64*2; act 2*192*2;
+    # tagged 32-bit copies of h, h_mid, q, act; 256 B of counters; each slice rounded to 256
+    assert n == (256 + 256 + 512 + 256 + 256 + 768) + (512 + 512 + 1024 + 1536) + 256
     bad = dict(layer, o=lin(64, 96))
     t2 = q4.LayerTable([layer, bad], lin(100, 64), hidden=64, M=2)
     assert L.q4_decode_workspace_bytes(ctypes.byref(t2.t)) == 0

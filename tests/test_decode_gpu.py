@@ -3,8 +3,9 @@
 Per stage: each stage's output is compared with the oracle applied to the
 GPU's own fp16 input of that stage (the tight per-element bound applies).
 End to end: logits against the oracle's whole chain (relative L2 <= 1e-3).
-Also: CUDA-graph replay, direct launches and launches without programmatic
-dependent launch give identical bits; pointer changes re-capture."""
+Also: CUDA-graph replay, direct launches, launches without programmatic
+dependent launch and the tagged hand-off give identical bits; pointer changes
+re-capture; tags stay correct past their 16-bit wrap."""
 import numpy as np
 import pytest
 
@@ -118,12 +119,12 @@ def tiny_gamma():
                     seed=q4synth.BASE_SEED + 50, gammas=True, eps=1e-5)
 
 
-def run_every_stage(model, M, seed):
+def run_every_stage(model, M, seed, flags=0):
     x = q4synth.activations(seed, M, model.shape.hidden)
     h_in = x
     eps = model.oracle_eps
     for n in range(1, model.shape.n_layers + 1):
-        out = model.step(n, x)
+        out = model.step(n, x, flags=flags)
         check_layer(model.layers[n - 1], h_in, out, what=f"layer {n - 1} M={M}", eps=eps)
         y_ref, A = oracle.decode_logits(model.lm, out["h"], model.final_norm, eps=eps)
         assert_parity(out["logits"], y_ref, A, what=f"logits after {n} layers")
@@ -141,6 +142,11 @@ def test_tiny_model_every_stage_and_end_to_end(tiny, M):
 @pytest.mark.parametrize("M", [1, 3, 8])
 def test_norm_weights_every_stage_and_end_to_end(tiny_gamma, M):
     run_every_stage(tiny_gamma, M, q4synth.BASE_SEED + 600 + M)
+
+
+@pytest.mark.parametrize("M", [1, 5])
+def test_tagged_hand_off_every_stage_and_end_to_end(tiny_gamma, M):
+    run_every_stage(tiny_gamma, M, q4synth.BASE_SEED + 650 + M, flags=q4.Q4_DECODE_TAGGED)
 
 
 def test_zero_layers_is_lm_head(tiny):
@@ -163,8 +169,32 @@ def test_graph_direct_and_no_pdl_agree(tiny):
     b = tiny.step(3, x, flags=q4.Q4_DECODE_NO_GRAPH)["logits"]
     c = tiny.step(3, x, flags=q4.Q4_DECODE_NO_PDL)["logits"]
     d = tiny.step(3, x, flags=q4.Q4_DECODE_NO_PDL | q4.Q4_DECODE_NO_GRAPH)["logits"]
-    for o in (b, c, d):
+    e = tiny.step(3, x, flags=q4.Q4_DECODE_TAGGED)["logits"]
+    f = tiny.step(3, x, flags=q4.Q4_DECODE_TAGGED | q4.Q4_DECODE_NO_GRAPH)["logits"]
+    for o in (b, c, d, e, f):
         assert np.array_equal(a.view(np.uint32), o.view(np.uint32))
+
+
+def test_many_replays_stay_correct(tiny):
+    """Tags advance every step; 5200 replays of one captured 13-stage step
+    (past the 16-bit tag space: 5200 * 13 > 65535) keep matching the oracle."""
+    t = tiny.table(3, 1, flags=q4.Q4_DECODE_TAGGED)
+    xs = q4synth.activations(150, 1, tiny.shape.hidden)
+    x_dev = torch_dev(xs)
+    lg = torch.empty(1, tiny.shape.vocab, device="cuda")
+    first = None
+    for i in range(5200):
+        q4.q4_decode_step(t, x_dev, lg)
+        if i == 0:
+            torch.cuda.synchronize()
+            first = lg.cpu().numpy().copy()
+    torch.cuda.synchronize()
+    assert q4.q4_device_status() == 0
+    last = lg.cpu().numpy()
+    t.release()
+    assert np.array_equal(first.view(np.uint32), last.view(np.uint32))
+    ref, _, _ = oracle.decode_step(tiny.layers, tiny.lm, xs)
+    assert np.linalg.norm(last - ref) / np.linalg.norm(ref) <= 1e-3
 
 
 def test_replay_and_recapture(tiny):
