@@ -19,6 +19,7 @@ __all__ = [
     "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine",
     "Q4_F32", "Q4_F16", "Q4_GEMV_PLAIN", "Q4_GEMV_GLU", "Q4_DECODE_NO_GRAPH", "Q4_DECODE_NO_PDL",
     "Q4_DECODE_TAGGED",
+    "Q4_DECODE_PERSISTENT",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -26,7 +27,7 @@ LIB_PATH = os.path.join(HERE, "libq4gb300.so")
 
 Q4_F32, Q4_F16 = 0, 1
 Q4_GEMV_PLAIN, Q4_GEMV_GLU = 0, 1
-Q4_DECODE_NO_GRAPH, Q4_DECODE_NO_PDL, Q4_DECODE_TAGGED = 1, 2, 4
+Q4_DECODE_NO_GRAPH, Q4_DECODE_NO_PDL, Q4_DECODE_TAGGED, Q4_DECODE_PERSISTENT = 1, 2, 4, 8
 Q4_MAX_SEGMENTS = 4
 
 STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q4_ERR_MISALIGNED",

@@ -31,6 +31,7 @@ struct Dims {
 
 struct Layout {
     size_t h = 0, h_mid = 0, q = 0, k = 0, v = 0, act = 0;
+    size_t params = 0;  // per-stage kernel parameters of the persistent launch
     // tagged copies of the activations that later stages read, and counters
     size_t h_t = 0, hm_t = 0, q_t = 0, act_t = 0, ctr = 0, tagged_begin = 0, total = 0;
 };
@@ -50,8 +51,11 @@ struct Plan {
     const void* x_key = nullptr;
     void* logits_key = nullptr;
     std::vector<q4_gemv_desc> stages;
-    std::vector<GemvTagged> tagged;  // per stage, used when tagged_mode
+    std::vector<GemvTagged> tagged;  // per stage, used when tagged_mode or persistent
     bool tagged_mode = false;
+    bool persistent = false;         // one cooperative launch per step
+    PersistentGeom geom;
+    std::vector<uint8_t> params_host;  // kept alive for the asynchronous upload
     bool tagged_ready = false;       // tagged region zeroed
     cudaStream_t capture_stream = nullptr;
     cudaGraph_t graph = nullptr;
@@ -122,6 +126,7 @@ Layout layout_of(const Dims& d) {
     l.k = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
     l.v = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
     l.act = take((size_t)d.M * (d.ffn > 0 ? d.ffn : 1));
+    l.params = take((size_t)(4 * d.L + 1) * gemv_params_bytes() / 2);
     l.tagged_begin = off;
     l.h_t = take((size_t)d.M * d.hidden * 2);
     l.hm_t = take((size_t)d.M * d.hidden * 2);
@@ -357,8 +362,22 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
         p->x_key = x;
         p->logits_key = logits;
         drop_graph(*p);
+        p->persistent = false;
+        if (p->flags & Q4_DECODE_PERSISTENT) {
+            const int n = (int)p->stages.size();
+            p->params_host.assign((size_t)n * gemv_params_bytes(), 0);
+            bool fits = false;
+            q4_status st = persistent_plan(p->stages.data(), p->tagged.data(), n, p->params_host.data(), &p->geom, &fits);
+            if (st != Q4_OK) return st;
+            if (fits) {
+                cudaError_t e = cudaMemcpyAsync(static_cast<uint8_t*>(p->workspace) + p->lay.params,
+                                                p->params_host.data(), p->params_host.size(), cudaMemcpyHostToDevice, s);
+                if (e != cudaSuccess) return cuda_fail(e, "uploading the stage parameters");
+                p->persistent = true;
+            }
+        }
     }
-    if (p->tagged_mode && !p->tagged_ready) {
+    if ((p->tagged_mode || p->persistent) && !p->tagged_ready) {
         // Once, on the caller's stream and outside any capture: tags start at
         // 1, so zeroed words never look ready; the step counter starts at 0.
         cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(p->workspace) + p->lay.tagged_begin, 0,
@@ -366,6 +385,8 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
         if (e != cudaSuccess) return cuda_fail(e, "clearing the tagged activations");
         p->tagged_ready = true;
     }
+    if (p->persistent)
+        return persistent_launch(p->geom, static_cast<uint8_t*>(p->workspace) + p->lay.params, s);
     if (p->flags & Q4_DECODE_NO_GRAPH) return enqueue_stages(*p, s);
     if (!p->exec) {
         q4_status st = capture(*p);

@@ -57,7 +57,7 @@ struct Seg {
     int N, ldy, tile_begin, tiles;
 };
 
-struct Params {
+struct alignas(16) Params {
     Seg seg[Q4_MAX_SEGMENTS];
     const uint16_t* x;
     const uint32_t* x_tag;    // tagged x (decode step), or nullptr
@@ -71,6 +71,7 @@ struct Params {
     const uint32_t* step_ctr;
     uint32_t* done_ctr;
     int stage, n_stages, x_stage, res_stage, last;
+    int tile_base;  // persistent step: tiles of all earlier stages (round-robin origin)
     int* err;
 };
 
@@ -79,9 +80,9 @@ __device__ __forceinline__ uint32_t tag_of(uint32_t step, int stage, int n_stage
 }
 
 // Poll tagged words until every tag equals `tag` (bounded; on expiry the
-// error word is latched and whatever was read is used).
+// error word is latched, whatever was read is used and false is returned).
 template <int NW>
-__device__ __forceinline__ void poll_tagged(const uint32_t* src, uint32_t tag, uint32_t* w, int* err) {
+__device__ __forceinline__ bool poll_tagged(const uint32_t* src, uint32_t tag, uint32_t* w, int* err) {
     unsigned long long t0 = 0;
     while (true) {
         bool ok = true;
@@ -93,12 +94,12 @@ __device__ __forceinline__ void poll_tagged(const uint32_t* src, uint32_t tag, u
         }
 #pragma unroll
         for (int i = 0; i < NW; ++i) ok &= (w[i] >> 16) == tag;
-        if (ok) return;
+        if (ok) return true;
         if (t0 == 0) {
             t0 = q4d::globaltimer();
         } else if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
             atomicOr(err, q4d::kErrTimeout);
-            return;
+            return false;
         }
         __nanosleep(100);  // let the producing kernel use the issue slots and L2
     }
@@ -113,7 +114,7 @@ __device__ __forceinline__ void gate_tagged_x(const Params& p, uint32_t tag, int
 #pragma unroll
     for (int m = 0; m < M; ++m) {
         uint32_t w;
-        poll_tagged<1>(p.x_tag + (size_t)m * p.ldx + (size_t)(lane + 1) * W - 1, tag, &w, p.err);
+        if (!poll_tagged<1>(p.x_tag + (size_t)m * p.ldx + (size_t)(lane + 1) * W - 1, tag, &w, p.err)) break;
     }
     __syncwarp();
 }
@@ -295,13 +296,14 @@ __device__ __forceinline__ void store_f16(const Seg& sg, size_t i, float v, uint
     if (sg.y_tag) q4d::st_relaxed(sg.y_tag + i, (tag << 16) | h);
 }
 
-__device__ __forceinline__ void store_out(const Params& p, const Seg& sg, int m, int n, float v, uint32_t ytag,
+__device__ __forceinline__ bool store_out(const Params& p, const Seg& sg, int m, int n, float v, uint32_t ytag,
                                           uint32_t rtag) {
     const size_t i = (size_t)m * sg.ldy + n;
+    bool ok = true;
     if (p.out_f16) {
         if (sg.res_tag) {
             uint32_t w;
-            poll_tagged<1>(sg.res_tag + i, rtag, &w, p.err);
+            ok = poll_tagged<1>(sg.res_tag + i, rtag, &w, p.err);
             v += __half2float(__ushort_as_half((uint16_t)(w & 0xFFFFu)));
         } else if (sg.res) {
             v += __half2float(__ushort_as_half(sg.res[i]));
@@ -310,10 +312,11 @@ __device__ __forceinline__ void store_out(const Params& p, const Seg& sg, int m,
     } else {
         reinterpret_cast<float*>(sg.y)[i] = v;
     }
+    return ok;
 }
 
 template <int M, int RB>
-__device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, const uint16_t* ss,
+__device__ __forceinline__ bool tile_batch(const Params& p, const uint32_t* wq, const uint16_t* ss,
                                            const uint16_t* bs, const float4* xs, const float* scale, int warp,
                                            int lane, int j_begin, int rpw, int si, int n0, int nrows,
                                            uint32_t ytag, uint32_t rtag) {
@@ -370,8 +373,9 @@ __device__ __forceinline__ void tile_batch(const Params& p, const uint32_t* wq, 
             store_f16(sg, (size_t)m_l * sg.ldy + n0 + local, a, ytag);
         }
     } else if (holds && (lane & ((1 << SH) - 1)) == 0 && local < nrows) {
-        store_out(p, p.seg[si], m_l, n0 + local, y, ytag, rtag);
+        return store_out(p, p.seg[si], m_l, n0 + local, y, ytag, rtag);
     }
+    return true;
 }
 
 // 8 consecutive fp16 values (16 bytes) as fp32.
@@ -420,10 +424,11 @@ __device__ __forceinline__ void stage_norm_weight(const Params& p, float4* xs) {
 // norm_scales); the scalar 1/rms is applied to the dot products in the
 // epilogue, so x is read once.
 template <int M>
-__device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, int warp, int lane, uint32_t xtag) {
+__device__ __forceinline__ bool load_x(const Params& p, float4* xs, float* red, int warp, int lane, uint32_t xtag) {
     constexpr int kCT = kConsumerWarps * 32;
     const int W8 = p.K / 8;
     const bool gw = p.norm && p.norm_w;
+    bool ok = true;
     float ss[M];
 #pragma unroll
     for (int m = 0; m < M; ++m) ss[m] = 0.f;
@@ -433,7 +438,12 @@ __device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, 
             float f[8];
             if (p.x_tag) {
                 uint32_t w[8];
-                poll_tagged<8>(p.x_tag + (size_t)m * p.ldx + 8 * j, xtag, w, p.err);
+                if (ok) {
+                    ok = poll_tagged<8>(p.x_tag + (size_t)m * p.ldx + 8 * j, xtag, w, p.err);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) w[e] = 0;  // after a timeout: no further waits
+                }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) f[e] = __half2float(__ushort_as_half((uint16_t)(w[e] & 0xFFFFu)));
             } else {
@@ -461,6 +471,7 @@ __device__ __forceinline__ void load_x(const Params& p, float4* xs, float* red, 
             if (lane == 0) red[warp * M + m] = ss[m];
         }
     }
+    return ok;
 }
 
 // 1/sqrt(mean(x^2) + eps) per row (after the barrier that follows load_x).
@@ -478,10 +489,38 @@ __device__ __forceinline__ void norm_scales(const Params& p, const float* red, f
     }
 }
 
+// One consumer warp's share of tile t (its rows, all M vectors), read from the
+// shared-memory stage that holds the tile.  False if a residual wait expired.
+template <int M>
+__device__ __forceinline__ bool consume_tile(const Params& p, const uint8_t* stage, const float4* xs,
+                                             const float* scale, int warp, int lane, int t, uint32_t ytag,
+                                             uint32_t rtag) {
+    constexpr int RB = Cfg<M>::RB;
+    const int K = p.K, G = K / 64, R = p.rows_per_tile;
+    const int rpw = R / kConsumerWarps;  // rows per warp per tile (1, 2, 4, 8)
+    const uint32_t* wq = reinterpret_cast<const uint32_t*>(stage);
+    const uint16_t* ss = reinterpret_cast<const uint16_t*>(stage + (size_t)R * (K / 2));
+    const uint16_t* bs = ss + (size_t)R * G;
+    int si, n0, nrows;
+    find_tile(p, t, si, n0, nrows);
+    bool ok = true;
+    if (rpw >= RB) {
+        for (int j = 0; j < rpw; j += RB)
+            ok &= tile_batch<M, RB>(p, wq, ss, bs, xs, scale, warp, lane, j, rpw, si, n0, nrows, ytag, rtag);
+    } else if (rpw == 4) {
+        ok = tile_batch<M, (RB < 4 ? RB : 4)>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag,
+                                              rtag);
+    } else if (rpw == 2) {
+        ok = tile_batch<M, 2>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
+    } else {
+        ok = tile_batch<M, 1>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
+    }
+    return ok;
+}
+
 template <int M>
 __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
-    constexpr int RB = Cfg<M>::RB;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int S = p.stages;
     float4* xs = reinterpret_cast<float4*>(smem);
@@ -561,30 +600,13 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
     float scale[M];
     norm_scales<M>(p, red, scale);
 
-    const int K = p.K, G = K / 64, R = p.rows_per_tile;
-    const int rpw = R / kConsumerWarps;  // rows per warp per tile (1, 2, 4, 8)
     int i = 0;
     for (int t = blockIdx.x; t < p.total_tiles; t += gridDim.x, ++i) {
         const int st = i % S, k = i / S;
         // on a timeout leave the loop (not the kernel): every consumer warp
         // must still reach the barrier below
         if (!q4d::mbar_wait(full0 + 8 * st, k & 1, p.err)) break;
-        const uint8_t* stage = stages + (size_t)st * p.stage_bytes;
-        const uint32_t* wq = reinterpret_cast<const uint32_t*>(stage);
-        const uint16_t* ss = reinterpret_cast<const uint16_t*>(stage + (size_t)R * (K / 2));
-        const uint16_t* bs = ss + (size_t)R * G;
-        int si, n0, nrows;
-        find_tile(p, t, si, n0, nrows);
-        if (rpw >= RB) {
-            for (int j = 0; j < rpw; j += RB)
-                tile_batch<M, RB>(p, wq, ss, bs, xs, scale, warp, lane, j, rpw, si, n0, nrows, ytag, rtag);
-        } else if (rpw == 4) {
-            tile_batch<M, (RB < 4 ? RB : 4)>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
-        } else if (rpw == 2) {
-            tile_batch<M, 2>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
-        } else {
-            tile_batch<M, 1>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
-        }
+        consume_tile<M>(p, stages + (size_t)st * p.stage_bytes, xs, scale, warp, lane, t, ytag, rtag);
         __syncwarp();
         if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
     }
@@ -598,6 +620,174 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
                 *p.done_ctr = 0;
                 atomicAdd(const_cast<uint32_t*>(p.step_ctr), 1u);
             }
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Persistent decode step.  One CTA per SM (a cooperative launch, so all CTAs
+// are resident together) walks every stage of the step in order, which
+// removes the per-stage kernel launch and grid-completion wait.  The tiles of
+// all stages are numbered one after another and dealt round-robin to the
+// CTAs.  Because weights never depend on activations, the producer warp
+// streams a CTA's tiles through one shared-memory ring across stage
+// boundaries, as far ahead as the ring allows; the consumers of stage s wait
+// only for their x: the tagged words (fp16 value | tag of step and stage) the
+// CTAs of stage s-1 publish.  Stage parameters live in a device table; the
+// consumers copy the next stage's entry into shared memory while they work on
+// the current one.  Every wait is bounded; an expired wait is OR-ed over the
+// consumers at the end of the stage and the CTA then stops, waits (bounded)
+// for its copies in flight and leaves.
+constexpr int kMaxSlots = 16;
+constexpr uint32_t kStepBarBytes = 2 * kMaxSlots * 8 + kConsumerWarps * 8 * 4;
+
+struct StepParams {
+    const Params* stages;  // device table [n]
+    int n;
+    int slots;             // ring slots
+    uint32_t slot_bytes;   // bytes per slot (largest tile of any stage)
+    uint32_t x_bytes;      // x region (largest K)
+    const uint32_t* step_ctr;
+    uint32_t* done_ctr;
+    int* err;
+};
+
+// First tile of a stage that CTA c owns: tile t goes to CTA (tile_base + t) mod G.
+__device__ __forceinline__ int first_tile(int tile_base, int G, int c) {
+    const int r = tile_base % G;
+    return c >= r ? c - r : c - r + G;
+}
+
+// A stage's parameters move to shared memory 16 bytes per consumer thread:
+// loaded into a register early (the load's latency then hides behind the wait
+// for x) and stored once the shared slot is free.
+constexpr int kParamWords = (int)(sizeof(Params) / 16);
+static_assert(sizeof(Params) % 16 == 0 && kParamWords <= kConsumerWarps * 32, "Params size");
+__device__ __forceinline__ uint4 load_param_word(const Params* src, int tid) {
+    return tid < kParamWords ? __ldg(reinterpret_cast<const uint4*>(src) + tid) : make_uint4(0, 0, 0, 0);
+}
+__device__ __forceinline__ void store_param_word(Params* dst, int tid, uint4 v) {
+    if (tid < kParamWords) reinterpret_cast<uint4*>(dst)[tid] = v;
+}
+
+template <int M>
+__global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const __grid_constant__ StepParams sp) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = sp.slots, G = gridDim.x, c = blockIdx.x;
+    float4* xs = reinterpret_cast<float4*>(smem);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sp.x_bytes);
+    float* red = reinterpret_cast<float*>(bars + 2 * kMaxSlots);
+    Params* prm = reinterpret_cast<Params*>(smem + sp.x_bytes + kStepBarBytes);
+    uint8_t* ring = smem + sp.x_bytes + kStepBarBytes + 2 * sizeof(Params);
+    const uint32_t full0 = q4d::smem_addr(bars), empty0 = q4d::smem_addr(bars + kMaxSlots);
+
+    __shared__ uint32_t step_sh;
+    __shared__ int issued_sh, consumed_sh;
+    __shared__ volatile int abort_sh;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            q4d::mbar_init(full0 + 8 * i, 32);
+            q4d::mbar_init(empty0 + 8 * i, kConsumerWarps);
+        }
+        q4d::fence_mbar_init();
+        step_sh = q4d::ld_relaxed(sp.step_ctr);
+        issued_sh = 0;
+        consumed_sh = 0x7fffffff;
+        abort_sh = 0;
+    }
+    __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ------------------------------------------------------ producer warp
+        const uint64_t pol = q4d::policy_evict_first();
+        int i = 0;
+        bool ok = true;
+        for (int s = 0; s < sp.n && ok; ++s) {
+            const Params& p = sp.stages[s];
+            for (int t = first_tile(p.tile_base, G, c); t < p.total_tiles; t += G, ++i) {
+                const int st = i % S, k = i / S;
+                if (k > 0) {
+                    int w_ok = 1;
+                    if (lane == 0) w_ok = (q4d::mbar_wait(empty0 + 8 * st, (k - 1) & 1, sp.err) && !abort_sh) ? 1 : 0;
+                    if (!__shfl_sync(0xffffffffu, w_ok, 0)) {
+                        ok = false;
+                        break;
+                    }
+                }
+                int si, n0, nrows;
+                find_tile(p, t, si, n0, nrows);
+                uint8_t* stage = ring + (size_t)st * sp.slot_bytes;
+                const uint32_t fb = full0 + 8 * st;
+                const uint32_t expect = (p.glu ? 2u : 1u) * bulk_bytes(p, nrows);
+                if (lane == 0)
+                    asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(expect)
+                                 : "memory");
+                __syncwarp();
+                issue_rows(p, p.seg[si], n0, nrows, 0, stage, fb, lane, pol);
+                if (p.glu) issue_rows(p, p.seg[1], n0, nrows, p.TR, stage, fb, lane, pol);
+                q4d::mbar_arrive(fb);
+            }
+        }
+        if (lane == 0) issued_sh = i;
+    } else {
+        // ---------------------------------------------------------- consumers
+        constexpr uint32_t kCT = kConsumerWarps * 32;
+        const int tid = threadIdx.x;
+        store_param_word(&prm[0], tid, load_param_word(sp.stages, tid));
+        q4d::named_bar(1, kCT);
+        const uint32_t step = step_sh;
+        int i = 0;
+        bool bad = false;
+        for (int s = 0; s < sp.n; ++s) {
+            const Params& p = prm[s & 1];
+            const int T = p.total_tiles;
+            const int t0 = first_tile(p.tile_base, G, c);
+            const uint32_t xtag = tag_of(step, p.x_stage, p.n_stages);
+            const uint32_t ytag = tag_of(step, p.stage, p.n_stages);
+            const uint32_t rtag = tag_of(step, p.res_stage, p.n_stages);
+            float scale[M];
+            const uint4 next = s + 1 < sp.n ? load_param_word(sp.stages + s + 1, tid) : make_uint4(0, 0, 0, 0);
+            if (t0 < T) {
+                if (p.norm && p.norm_w) stage_norm_weight<M>(p, xs);
+                if (!load_x<M>(p, xs, red, warp, lane, xtag)) bad = true;
+                q4d::named_bar(1, kCT);
+                norm_scales<M>(p, red, scale);
+            }
+            // the other parameter slot was last read in stage s-1, which every
+            // consumer has left (end-of-stage barrier below)
+            if (s + 1 < sp.n) store_param_word(&prm[(s + 1) & 1], tid, next);
+            if (t0 < T && !bad) {
+                for (int t = t0; t < T; t += G, ++i) {
+                    const int st = i % S, k = i / S;
+                    if (!q4d::mbar_wait(full0 + 8 * st, k & 1, sp.err)) {
+                        bad = true;
+                        break;
+                    }
+                    if (!consume_tile<M>(p, ring + (size_t)st * sp.slot_bytes, xs, scale, warp, lane, t, ytag, rtag))
+                        bad = true;
+                    __syncwarp();
+                    if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
+                }
+            }
+            if (q4d::named_bar_or(1, kCT, bad)) {
+                if (tid == 0) abort_sh = 1;
+                break;
+            }
+        }
+        if (lane == 0) atomicMin(&consumed_sh, i);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // After an abort, copies may still be landing in slots nobody will
+        // read: wait for them (bounded) before the CTA's shared memory goes.
+        for (int j = consumed_sh; j < issued_sh; ++j) q4d::mbar_wait(full0 + 8 * (j % S), (j / S) & 1, nullptr);
+        // The last CTA to finish advances the step counter (every CTA read it
+        // at its start).
+        __threadfence();
+        if (atomicAdd(sp.done_ctr, 1u) == gridDim.x - 1) {
+            *sp.done_ctr = 0;
+            atomicAdd(const_cast<uint32_t*>(sp.step_ctr), 1u);
         }
     }
 }
@@ -679,25 +869,12 @@ cudaError_t launch_m(const Params& p, dim3 grid, size_t smem, cudaStream_t strea
     return cudaLaunchKernelEx(&cfg, kern, p);
 }
 
-}  // namespace
-
-bool gemv_fits_unsplit(int M, int K) {
-    const DeviceInfo* dev = nullptr;
-    if (current_device(&dev) != Q4_OK) return false;
-    const uint32_t row_bytes = (uint32_t)(K / 2 + (K / 64) * 4);
-    const uint32_t stage = ((uint32_t)(2 * 8) * row_bytes + 127u) & ~127u;  // smallest GLU tile
-    const uint32_t fixed = ((x_smem_bytes(M, K) + 127u) & ~127u) + q4k::kBarBytes;
-    return fixed + 2 * stage <= (uint32_t)dev->smem_optin;
-}
-
-q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch,
-                      const GemvTagged* tg) {
-    const DeviceInfo* dev = nullptr;
-    q4_status st = current_device(&dev);
-    if (st != Q4_OK) return st;
-
-    Params p = {};
-    const int M = d.M, K = d.K, G = K / 64;
+// Kernel parameters of one fused GEMV (everything but the shared-memory
+// geometry).
+void fill_params(const q4_gemv_desc& d, const GemvTagged* tg, bool early_prefetch, int min_tiles,
+                 uint32_t max_stage, int* err, Params& p) {
+    p = {};
+    const int K = d.K, G = K / 64;
     const bool glu = d.mode == Q4_GEMV_GLU;
     p.x = d.x;
     p.K = K;
@@ -709,7 +886,7 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     p.norm = d.x_rmsnorm ? 1 : 0;
     p.norm_w = d.norm_weight;
     p.norm_eps = d.norm_eps;
-    p.err = dev->err_word;
+    p.err = err;
     p.n_stages = 1;
     if (tg) {
         p.x_tag = tg->x;
@@ -723,14 +900,14 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     }
 
     // Tile rows: largest of 64/32/16/8 (per matrix) whose tile count still
-    // covers every SM, with a stage of at most 48 KB.
+    // reaches min_tiles, with a stage of at most max_stage bytes.
     const uint32_t row_bytes = (uint32_t)(K / 2 + G * 4);
     int TR = 64;
     while (TR > 8) {
         const uint32_t stage = (uint32_t)(glu ? 2 * TR : TR) * row_bytes;
         long tiles = 0;
         for (int i = 0; i < (glu ? 1 : d.n_segments); ++i) tiles += (d.seg[i].N + TR - 1) / TR;
-        if (stage <= 48u * 1024u && tiles >= dev->sms) break;
+        if (stage <= max_stage && tiles >= min_tiles) break;
         TR /= 2;
     }
     p.TR = TR;
@@ -756,6 +933,28 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     p.total_tiles = tiles;
 
     p.stage_bytes = ((uint32_t)p.rows_per_tile * row_bytes + 127u) & ~127u;
+}
+
+}  // namespace
+
+bool gemv_fits_unsplit(int M, int K) {
+    const DeviceInfo* dev = nullptr;
+    if (current_device(&dev) != Q4_OK) return false;
+    const uint32_t row_bytes = (uint32_t)(K / 2 + (K / 64) * 4);
+    const uint32_t stage = ((uint32_t)(2 * 8) * row_bytes + 127u) & ~127u;  // smallest GLU tile
+    const uint32_t fixed = ((x_smem_bytes(M, K) + 127u) & ~127u) + q4k::kBarBytes;
+    return fixed + 2 * stage <= (uint32_t)dev->smem_optin - 256u;
+}
+
+q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch,
+                      const GemvTagged* tg) {
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+
+    Params p;
+    fill_params(d, tg, early_prefetch, dev->sms, 48u * 1024u, dev->err_word, p);
+    const int M = d.M, K = d.K;
     p.x_bytes = (x_smem_bytes(M, K) + 127u) & ~127u;
     const uint32_t fixed = p.x_bytes + q4k::kBarBytes;
     // Two CTAs per SM when they fit (lets the next kernel's CTAs start
@@ -764,7 +963,7 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     uint32_t budget = budget_two;
     int ctas_per_sm = 2;
     if (fixed + 2 * p.stage_bytes > budget_two) {
-        budget = (uint32_t)dev->smem_optin;
+        budget = (uint32_t)dev->smem_optin - 256u;  // the kernel's static shared variables
         ctas_per_sm = 1;
     }
     if (fixed + 2 * p.stage_bytes > budget) {
@@ -793,6 +992,7 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     if (S > q4k::kMaxStages) S = q4k::kMaxStages;
     p.stages = S;
     const size_t smem = fixed + (size_t)S * p.stage_bytes;
+    const int tiles = p.total_tiles;
     const int grid = tiles < dev->sms * ctas_per_sm ? tiles : dev->sms * ctas_per_sm;
 
     cudaError_t e = cudaSuccess;
@@ -807,6 +1007,110 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
         case 8: e = launch_m<8>(p, dim3(grid), smem, stream, pdl); break;
     }
     if (e != cudaSuccess) return cuda_fail(e, "q4_gemv kernel launch");
+    return Q4_OK;
+}
+
+
+size_t gemv_params_bytes() { return sizeof(Params); }
+
+q4_status persistent_plan(const q4_gemv_desc* d, const GemvTagged* tg, int n, void* host_params,
+                          PersistentGeom* g, bool* fits) {
+    *fits = false;
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    if (n < 1) return fail(Q4_ERR_INVALID_ARG, "no stages");
+    const int M = d[0].M;
+    Params* P = static_cast<Params*>(host_params);
+    uint32_t slot = 0, xb = 0;
+    int base = 0;
+    for (int s = 0; s < n; ++s) {
+        if (d[s].M != M) return Q4_OK;
+        // Tiles of at most 24 KB, and at least one per SM where the matrix allows.
+        fill_params(d[s], &tg[s], true, dev->sms, 24u * 1024u, dev->err_word, P[s]);
+        P[s].tile_base = base;
+        base += P[s].total_tiles;
+        if (P[s].stage_bytes > slot) slot = P[s].stage_bytes;
+        const uint32_t x = (x_smem_bytes(M, d[s].K) + 127u) & ~127u;
+        if (x > xb) xb = x;
+    }
+    const size_t fixed = (size_t)xb + q4k::kStepBarBytes + 2 * sizeof(Params);
+    const size_t avail = (size_t)dev->smem_optin - 256;  // the kernel's static shared variables
+    const int per_sm = 1;
+    if (fixed + 2 * (size_t)slot > avail) return Q4_OK;  // does not fit: the caller plans launches
+    int slots = (int)((avail - fixed) / slot);
+    if (slots > q4k::kMaxSlots) slots = q4k::kMaxSlots;
+    for (int s = 0; s < n; ++s) {
+        P[s].x_bytes = xb;
+        P[s].stages = slots;
+    }
+    g->M = M;
+    g->n = n;
+    g->grid = dev->sms * per_sm;
+    g->slots = slots;
+    g->slot_bytes = slot;
+    g->x_bytes = xb;
+    g->smem = fixed + (size_t)slots * slot;
+    g->step_ctr = tg[0].step_ctr;
+    g->done_ctr = tg[0].done_ctr;
+    *fits = true;
+    return Q4_OK;
+}
+
+namespace {
+template <int M>
+cudaError_t launch_persistent_m(const q4k::StepParams& sp, const PersistentGeom& g, cudaStream_t stream) {
+    auto kern = q4k::q4_decode_persistent_kernel<M>;
+    static int configured_smem[64] = {0};
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 64 && (int)g.smem > configured_smem[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
+        if (e != cudaSuccess) return e;
+        configured_smem[dev] = (int)g.smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(g.grid);
+    cfg.blockDim = dim3(q4k::kThreads);
+    cfg.dynamicSmemBytes = g.smem;
+    cfg.stream = stream;
+    // cooperative: the launch fails unless every CTA can be resident at once,
+    // which the waits between CTAs rely on
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, sp);
+}
+}  // namespace
+
+q4_status persistent_launch(const PersistentGeom& g, const void* dev_params, cudaStream_t stream) {
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    q4k::StepParams sp = {};
+    sp.stages = static_cast<const Params*>(dev_params);
+    sp.n = g.n;
+    sp.slots = g.slots;
+    sp.slot_bytes = g.slot_bytes;
+    sp.x_bytes = g.x_bytes;
+    sp.step_ctr = g.step_ctr;
+    sp.done_ctr = g.done_ctr;
+    sp.err = dev->err_word;
+    cudaError_t e = cudaSuccess;
+    switch (g.M) {
+        case 1: e = launch_persistent_m<1>(sp, g, stream); break;
+        case 2: e = launch_persistent_m<2>(sp, g, stream); break;
+        case 3: e = launch_persistent_m<3>(sp, g, stream); break;
+        case 4: e = launch_persistent_m<4>(sp, g, stream); break;
+        case 5: e = launch_persistent_m<5>(sp, g, stream); break;
+        case 6: e = launch_persistent_m<6>(sp, g, stream); break;
+        case 7: e = launch_persistent_m<7>(sp, g, stream); break;
+        case 8: e = launch_persistent_m<8>(sp, g, stream); break;
+        default: return fail(Q4_ERR_UNSUPPORTED, "M=%d", g.M);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "persistent decode kernel launch");
     return Q4_OK;
 }
 

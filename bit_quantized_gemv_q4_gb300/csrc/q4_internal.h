@@ -55,6 +55,27 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
 // True when one launch of (M, K) fits in shared memory without splitting M.
 bool gemv_fits_unsplit(int M, int K);
 
+// ---- persistent decode step (q4_gemv.cu) -----------------------------------
+// One cooperative launch runs every stage of a decode step (tagged hand-off
+// between stages).  The per-stage kernel parameters are an opaque table of
+// n * gemv_params_bytes() bytes that the caller copies to device memory.
+size_t gemv_params_bytes();
+
+struct PersistentGeom {
+    int M = 0, n = 0, grid = 0, slots = 0;
+    uint32_t slot_bytes = 0, x_bytes = 0;
+    size_t smem = 0;
+    const uint32_t* step_ctr = nullptr;
+    uint32_t* done_ctr = nullptr;
+};
+
+// Fills host_params (n entries) and g from the stages and their tagged
+// hand-off; *fits is false (and Q4_OK returned) when the step does not fit
+// one persistent launch.
+q4_status persistent_plan(const q4_gemv_desc* d, const GemvTagged* tg, int n, void* host_params,
+                          PersistentGeom* g, bool* fits);
+q4_status persistent_launch(const PersistentGeom& g, const void* dev_params, cudaStream_t stream);
+
 // ---- MoE (q4_moe.cu, q4_moe_gemm.cu) ---------------------------------------
 size_t moe_route_workspace_bytes(int T, int E, int topk);
 

@@ -172,17 +172,29 @@ q4_status q4_gemv_ex(const q4_gemv_desc *desc, q4_stream_t stream);
  * and finally logits = Wlm (rms(h) * final_norm) in logits_dtype.  Attention
  * and RoPE are not part of this matmul path.
  *
- * The first call on a table validates it, plans the launches and captures
- * them into a CUDA graph (programmatic dependent launch between the kernels,
- * so each kernel's weight stream starts before its predecessor ends); later
- * calls replay the graph.  A call with different x or logits pointers
- * re-captures.  With Q4_DECODE_TAGGED, activations are handed from stage to
- * stage as 32-bit words holding the fp16 value and a 16-bit tag naming the step
- * and the writing stage; a stage polls the words it reads instead of waiting
- * for the whole previous kernel to finish.  The workspace always reserves room
- * for these tagged copies and a step counter; they are cleared on the first
- * tagged call (on
- * `stream`) and must not be shared with another table while in use.  Host memory for the plan is allocated on that first call
+ * The first call on a table validates it and plans the step.  By default
+ * each stage is its own kernel launch: the first call captures them into a
+ * CUDA graph (programmatic dependent launch between the kernels, so each
+ * kernel's weight stream starts before its predecessor ends); later calls
+ * replay the graph.  With Q4_DECODE_PERSISTENT a step is ONE cooperative
+ * kernel launch instead: one CTA per SM walks every stage in order, streaming
+ * each stage's weights ahead through shared memory while it waits for that
+ * stage's input, and the stages hand activations on as tagged words (below)
+ * instead of kernel boundaries; the per-stage kernel parameters are uploaded
+ * into the workspace on `stream` on the first call and after a pointer
+ * change, and calls on one table must then be ordered on one stream.  If the
+ * step does not fit one persistent launch (x of the widest stage plus two
+ * weight tiles exceeds shared memory) the flag is ignored.  A call with
+ * different x or logits
+ * pointers re-plans (and re-captures).  In the persistent launch, and with
+ * Q4_DECODE_TAGGED for per-stage launches, activations pass from stage to
+ * stage as 32-bit words holding the fp16 value and a 16-bit tag naming the
+ * step and the writing stage; a stage polls the words it reads instead of
+ * waiting for the whole previous kernel to finish.  The workspace therefore
+ * also holds the stage parameters, these tagged copies and a step counter;
+ * the tagged region is cleared on the first such call (on `stream`), and the
+ * workspace must not be shared with another table while in use.  Host memory
+ * for the plan is allocated on that first call
  * (load time); replays allocate nothing.  x: fp16 [M][hidden].  logits:
  * [M][vocab].  The workspace (device, >= q4_decode_workspace_bytes) holds the
  * activations; after a step it holds the LAST layer's q, k, v, h', act and the
@@ -207,6 +219,8 @@ typedef struct q4_layer_weights {
 #define Q4_DECODE_NO_PDL 2   /* no programmatic dependent launch between kernels */
 #define Q4_DECODE_TAGGED 4    /* stages poll tagged activation words (see below) instead of
                                  waiting for their predecessor grid to complete */
+#define Q4_DECODE_PERSISTENT 8 /* one persistent cooperative launch per step (see below);
+                                  the three flags above then do not apply */
 
 typedef struct q4_layer_table {
     int n_layers;

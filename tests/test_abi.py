@@ -138,8 +138,16 @@ def test_decode_table_validation_and_workspace(L):
     t = q4.LayerTable([layer, layer], lin(100, 64), hidden=64, M=2)
     n = q4.q4_decode_workspace_bytes(t)
     # plain fp16: h, h_mid 2*64*2 B each; q 2*128*2; k, v 2*64*2; act 2*192*2;
-    # tagged 32-bit copies of h, h_mid, q, act; 256 B of counters; each slice rounded to 256
-    assert n == (256 + 256 + 512 + 256 + 256 + 768) + (512 + 512 + 1024 + 1536) + 256
+    # tagged 32-bit copies of h, h_mid, q, act; 256 B of counters; each slice
+    # rounded to 256; plus one parameter block per stage (4 per layer + lm_head)
+    base = (256 + 256 + 512 + 256 + 256 + 768) + (512 + 512 + 1024 + 1536) + 256
+    extra = n - base
+    n4 = q4.q4_decode_workspace_bytes(q4.LayerTable([layer] * 4, lin(100, 64), hidden=64, M=2))
+    extra4 = n4 - base
+    assert extra % 256 == 0 and extra4 % 256 == 0
+    assert 9 * 128 <= extra <= 9 * 1024 + 255      # 9 stages
+    assert 17 * 128 <= extra4 <= 17 * 1024 + 255   # 17 stages
+    assert extra4 > extra
     bad = dict(layer, o=lin(64, 96))
     t2 = q4.LayerTable([layer, bad], lin(100, 64), hidden=64, M=2)
     assert L.q4_decode_workspace_bytes(ctypes.byref(t2.t)) == 0

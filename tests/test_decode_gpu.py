@@ -3,9 +3,10 @@
 Per stage: each stage's output is compared with the oracle applied to the
 GPU's own fp16 input of that stage (the tight per-element bound applies).
 End to end: logits against the oracle's whole chain (relative L2 <= 1e-3).
-Also: CUDA-graph replay, direct launches, launches without programmatic
-dependent launch and the tagged hand-off give identical bits; pointer changes
-re-capture; tags stay correct past their 16-bit wrap."""
+Per-stage launches (CUDA-graph replay, direct launches, without programmatic
+dependent launch, with the tagged hand-off) and the one persistent launch per
+step give the same bits; pointer changes re-plan; tags stay correct past their
+16-bit wrap."""
 import numpy as np
 import pytest
 
@@ -144,9 +145,17 @@ def test_norm_weights_every_stage_and_end_to_end(tiny_gamma, M):
     run_every_stage(tiny_gamma, M, q4synth.BASE_SEED + 600 + M)
 
 
+PERSISTENT = q4.Q4_DECODE_PERSISTENT
+
+
 @pytest.mark.parametrize("M", [1, 5])
 def test_tagged_hand_off_every_stage_and_end_to_end(tiny_gamma, M):
     run_every_stage(tiny_gamma, M, q4synth.BASE_SEED + 650 + M, flags=q4.Q4_DECODE_TAGGED)
+
+
+@pytest.mark.parametrize("M", [1, 2, 4, 7, 8])
+def test_persistent_step_every_stage_and_end_to_end(tiny_gamma, M):
+    run_every_stage(tiny_gamma, M, q4synth.BASE_SEED + 660 + M, flags=PERSISTENT)
 
 
 def test_zero_layers_is_lm_head(tiny):
@@ -163,22 +172,23 @@ def test_fp16_logits(tiny):
     assert_parity(out["logits"], y_ref, A, fp16_out=True)
 
 
-def test_graph_direct_and_no_pdl_agree(tiny):
-    x = q4synth.activations(9, 4, tiny.shape.hidden)
-    a = tiny.step(3, x)["logits"]
-    b = tiny.step(3, x, flags=q4.Q4_DECODE_NO_GRAPH)["logits"]
-    c = tiny.step(3, x, flags=q4.Q4_DECODE_NO_PDL)["logits"]
-    d = tiny.step(3, x, flags=q4.Q4_DECODE_NO_PDL | q4.Q4_DECODE_NO_GRAPH)["logits"]
-    e = tiny.step(3, x, flags=q4.Q4_DECODE_TAGGED)["logits"]
-    f = tiny.step(3, x, flags=q4.Q4_DECODE_TAGGED | q4.Q4_DECODE_NO_GRAPH)["logits"]
-    for o in (b, c, d, e, f):
-        assert np.array_equal(a.view(np.uint32), o.view(np.uint32))
+@pytest.mark.parametrize("M", [1, 4])
+def test_persistent_and_per_stage_modes_agree(tiny, M):
+    x = q4synth.activations(9, M, tiny.shape.hidden)
+    a = tiny.step(3, x)
+    for fl in (q4.Q4_DECODE_NO_GRAPH, q4.Q4_DECODE_NO_PDL, q4.Q4_DECODE_NO_PDL | q4.Q4_DECODE_NO_GRAPH,
+               q4.Q4_DECODE_TAGGED, q4.Q4_DECODE_TAGGED | q4.Q4_DECODE_NO_GRAPH, PERSISTENT):
+        o = tiny.step(3, x, flags=fl)
+        for k in a:
+            assert np.array_equal(a[k].view(np.uint32) if a[k].dtype == np.float32 else a[k],
+                                  o[k].view(np.uint32) if o[k].dtype == np.float32 else o[k]), (fl, k)
 
 
-def test_many_replays_stay_correct(tiny):
-    """Tags advance every step; 5200 replays of one captured 13-stage step
-    (past the 16-bit tag space: 5200 * 13 > 65535) keep matching the oracle."""
-    t = tiny.table(3, 1, flags=q4.Q4_DECODE_TAGGED)
+@pytest.mark.parametrize("flags", [PERSISTENT, q4.Q4_DECODE_TAGGED])
+def test_many_replays_stay_correct(tiny, flags):
+    """Tags advance every step; 5200 steps of 13 stages (past the 16-bit tag
+    space: 5200 * 13 > 65535) keep matching the oracle."""
+    t = tiny.table(3, 1, flags=flags)
     xs = q4synth.activations(150, 1, tiny.shape.hidden)
     x_dev = torch_dev(xs)
     lg = torch.empty(1, tiny.shape.vocab, device="cuda")
@@ -197,9 +207,10 @@ def test_many_replays_stay_correct(tiny):
     assert np.linalg.norm(last - ref) / np.linalg.norm(ref) <= 1e-3
 
 
-def test_replay_and_recapture(tiny):
+@pytest.mark.parametrize("flags", [0, PERSISTENT])
+def test_replay_and_recapture(tiny, flags):
     M = 1
-    t = tiny.table(3, M)
+    t = tiny.table(3, M, flags=flags)
     xs = [q4synth.activations(100 + i, M, tiny.shape.hidden) for i in range(3)]
     l1 = torch.empty(M, tiny.shape.vocab, device="cuda")
     l2 = torch.empty(M, tiny.shape.vocab, device="cuda")
@@ -239,3 +250,5 @@ def test_qwen3_0p6b_full_size(qwen06):
     l_ref, _, _ = oracle.decode_step(qwen06.layers, qwen06.lm, x)
     rel = np.linalg.norm(out["logits"] - l_ref) / np.linalg.norm(l_ref)
     assert rel <= 1e-3, rel
+    persistent = qwen06.step(s.n_layers, x, flags=PERSISTENT)
+    assert np.array_equal(out["logits"].view(np.uint32), persistent["logits"].view(np.uint32))
