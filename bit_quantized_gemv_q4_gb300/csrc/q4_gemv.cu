@@ -296,17 +296,25 @@ __device__ __forceinline__ void store_f16(const Seg& sg, size_t i, float v, uint
     if (sg.y_tag) q4d::st_relaxed(sg.y_tag + i, (tag << 16) | h);
 }
 
+// The residual word of output i, read before the dot products so its latency
+// overlaps them: a tagged word (checked, and polled again if not yet current,
+// by add_residual) or a plain fp16 value.
+__device__ __forceinline__ uint32_t prefetch_residual(const Seg& sg, size_t i) {
+    if (sg.res_tag) return q4d::ld_relaxed(sg.res_tag + i);
+    if (sg.res) return sg.res[i];
+    return 0;
+}
+
 __device__ __forceinline__ bool store_out(const Params& p, const Seg& sg, int m, int n, float v, uint32_t ytag,
-                                          uint32_t rtag) {
+                                          uint32_t rtag, uint32_t resw) {
     const size_t i = (size_t)m * sg.ldy + n;
     bool ok = true;
     if (p.out_f16) {
         if (sg.res_tag) {
-            uint32_t w;
-            ok = poll_tagged<1>(sg.res_tag + i, rtag, &w, p.err);
-            v += __half2float(__ushort_as_half((uint16_t)(w & 0xFFFFu)));
+            if ((resw >> 16) != rtag) ok = poll_tagged<1>(sg.res_tag + i, rtag, &resw, p.err);
+            v += __half2float(__ushort_as_half((uint16_t)(resw & 0xFFFFu)));
         } else if (sg.res) {
-            v += __half2float(__ushort_as_half(sg.res[i]));
+            v += __half2float(__ushort_as_half((uint16_t)resw));
         }
         store_f16(sg, i, v, ytag);
     } else {
@@ -335,21 +343,12 @@ __device__ __forceinline__ bool tile_batch(const Params& p, const uint32_t* wq, 
             rows[r] = locals[r];
         }
     }
-    float out[RB][M];
-    dot_rows<M, RB>(p, wq, ss, bs, xs, rows, lane, out);
-    // Reduce all RB*M values at once; afterwards lane L holds value index
-    // idx = L >> SH (idx = r*M + m), and the lanes with L % 2^SH == 0 store.
+    // After the reduction below lane L holds value index idx = L >> SH
+    // (idx = r*M + m), and the lanes with L % 2^SH == 0 store it.  Which
+    // output a lane stores is known now, so its residual is fetched first.
     constexpr int V = RB * M;
     constexpr int VP = (V > 16) ? 32 : (V > 8) ? 16 : (V > 4) ? 8 : (V > 2) ? 4 : (V > 1) ? 2 : 1;  // power of two
     constexpr int SH = 5 - ((VP >= 32) ? 5 : (VP >= 16) ? 4 : (VP >= 8) ? 3 : (VP >= 4) ? 2 : (VP >= 2) ? 1 : 0);
-    float v[VP];
-#pragma unroll
-    for (int i = V; i < VP; ++i) v[i] = 0.f;
-#pragma unroll
-    for (int r = 0; r < RB; ++r)
-#pragma unroll
-        for (int m = 0; m < M; ++m) v[r * M + m] = out[r][m];
-    warp_sum_transpose<VP>(v, lane);
     const int idx_raw = lane >> SH;
     const bool holds = idx_raw < V;   // lanes past V hold padding
     const int idx = holds ? idx_raw : 0;
@@ -362,18 +361,36 @@ __device__ __forceinline__ bool tile_batch(const Params& p, const uint32_t* wq, 
 #pragma unroll
     for (int m = 0; m < M; ++m)
         if (m == m_l) sc = scale[m];
+    const bool storer = holds && (lane & ((1 << SH) - 1)) == 0 && local < nrows;
+    uint32_t resw = 0;
+    if (!p.glu && storer && p.out_f16) {
+        const Seg& sg = p.seg[si];
+        resw = prefetch_residual(sg, (size_t)m_l * sg.ldy + n0 + local);
+    }
+
+    float out[RB][M];
+    dot_rows<M, RB>(p, wq, ss, bs, xs, rows, lane, out);
+    // Reduce all RB*M values at once.
+    float v[VP];
+#pragma unroll
+    for (int i = V; i < VP; ++i) v[i] = 0.f;
+#pragma unroll
+    for (int r = 0; r < RB; ++r)
+#pragma unroll
+        for (int m = 0; m < M; ++m) v[r * M + m] = out[r][m];
+    warp_sum_transpose<VP>(v, lane);
     const float y = v[0] * sc;
     if (p.glu) {
         // gate (even r) and up (odd r) of one output row: the up total sits M
         // value indices further on
         const float u = __shfl_down_sync(0xffffffffu, y, M << SH);
-        if (holds && (lane & ((1 << SH) - 1)) == 0 && (r_l & 1) == 0 && local < nrows) {
+        if (storer && (r_l & 1) == 0) {
             const float a = y / (1.0f + expf(-y)) * u;
             const Seg& sg = p.seg[0];
             store_f16(sg, (size_t)m_l * sg.ldy + n0 + local, a, ytag);
         }
-    } else if (holds && (lane & ((1 << SH) - 1)) == 0 && local < nrows) {
-        return store_out(p, p.seg[si], m_l, n0 + local, y, ytag, rtag);
+    } else if (storer) {
+        return store_out(p, p.seg[si], m_l, n0 + local, y, ytag, rtag, resw);
     }
     return true;
 }
@@ -424,7 +441,8 @@ __device__ __forceinline__ void stage_norm_weight(const Params& p, float4* xs) {
 // norm_scales); the scalar 1/rms is applied to the dot products in the
 // epilogue, so x is read once.
 template <int M>
-__device__ __forceinline__ bool load_x(const Params& p, float4* xs, float* red, int warp, int lane, uint32_t xtag) {
+__device__ __forceinline__ bool load_x(const Params& p, float4* xs, float* red, int warp, int lane, uint32_t xtag,
+                                       const uint16_t* gamma_sm = nullptr) {
     constexpr int kCT = kConsumerWarps * 32;
     const int W8 = p.K / 8;
     const bool gw = p.norm && p.norm_w;
@@ -454,7 +472,12 @@ __device__ __forceinline__ bool load_x(const Params& p, float4* xs, float* red, 
             float4* d0 = x_slot<M>(xs, j, m, 0);
             float4* d1 = x_slot<M>(xs, j, m, 1);
             float4 a = make_float4(f[0], f[4], f[1], f[5]), b = make_float4(f[2], f[6], f[3], f[7]);
-            if (gw) {
+            if (gamma_sm) {
+                float g[8];
+                load8_f32(gamma_sm + 8 * j, g);
+                a = make_float4(a.x * g[0], a.y * g[4], a.z * g[1], a.w * g[5]);
+                b = make_float4(b.x * g[2], b.y * g[6], b.z * g[3], b.w * g[7]);
+            } else if (gw) {
                 const float4 ga = *d0, gb = *d1;
                 a = make_float4(a.x * ga.x, a.y * ga.y, a.z * ga.z, a.w * ga.w);
                 b = make_float4(b.x * gb.x, b.y * gb.y, b.z * gb.z, b.w * gb.w);
@@ -640,12 +663,16 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
 // for its copies in flight and leaves.
 constexpr int kMaxSlots = 16;
 constexpr uint32_t kStepBarBytes = 2 * kMaxSlots * 8 + kConsumerWarps * 8 * 4;
+constexpr int kParamWords = (int)(sizeof(Params) / 16);
+static_assert(sizeof(Params) % 16 == 0 && kParamWords <= kConsumerWarps * 32, "Params size");
 
 struct StepParams {
     const Params* stages;  // device table [n]
     int n;
     int slots;             // ring slots
-    uint32_t slot_bytes;   // bytes per slot (largest tile of any stage)
+    uint32_t slot_bytes;   // bytes per slot
+    uint32_t meta_off;     // offset in a slot of the stage parameters (then the norm weights)
+    uint32_t ring_off;     // offset of the ring in shared memory
     uint32_t x_bytes;      // x region (largest K)
     const uint32_t* step_ctr;
     uint32_t* done_ctr;
@@ -658,16 +685,10 @@ __device__ __forceinline__ int first_tile(int tile_base, int G, int c) {
     return c >= r ? c - r : c - r + G;
 }
 
-// A stage's parameters move to shared memory 16 bytes per consumer thread:
-// loaded into a register early (the load's latency then hides behind the wait
-// for x) and stored once the shared slot is free.
-constexpr int kParamWords = (int)(sizeof(Params) / 16);
-static_assert(sizeof(Params) % 16 == 0 && kParamWords <= kConsumerWarps * 32, "Params size");
-__device__ __forceinline__ uint4 load_param_word(const Params* src, int tid) {
-    return tid < kParamWords ? __ldg(reinterpret_cast<const uint4*>(src) + tid) : make_uint4(0, 0, 0, 0);
-}
-__device__ __forceinline__ void store_param_word(Params* dst, int tid, uint4 v) {
-    if (tid < kParamWords) reinterpret_cast<uint4*>(dst)[tid] = v;
+// Bytes of stage metadata that travel with a CTA's first tile of a stage: the
+// stage's parameter block and, for a normalised x, its norm weights.
+__device__ __forceinline__ uint32_t meta_bytes(const Params& p) {
+    return (uint32_t)sizeof(Params) + ((p.norm && p.norm_w) ? (uint32_t)p.K * 2u : 0u);
 }
 
 template <int M>
@@ -679,7 +700,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + sp.x_bytes);
     float* red = reinterpret_cast<float*>(bars + 2 * kMaxSlots);
     Params* prm = reinterpret_cast<Params*>(smem + sp.x_bytes + kStepBarBytes);
-    uint8_t* ring = smem + sp.x_bytes + kStepBarBytes + 2 * sizeof(Params);
+    int2* tt = reinterpret_cast<int2*>(smem + sp.x_bytes + kStepBarBytes + sizeof(Params));
+    uint8_t* ring = smem + sp.ring_off;
     const uint32_t full0 = q4d::smem_addr(bars), empty0 = q4d::smem_addr(bars + kMaxSlots);
 
     __shared__ uint32_t step_sh;
@@ -696,6 +718,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
         consumed_sh = 0x7fffffff;
         abort_sh = 0;
     }
+    // (tile origin, tile count) of every stage, for the consumers
+    for (int s = threadIdx.x; s < sp.n; s += blockDim.x)
+        tt[s] = make_int2(sp.stages[s].tile_base, sp.stages[s].total_tiles);
     __syncthreads();
 
     if (warp == kConsumerWarps) {
@@ -705,7 +730,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
         bool ok = true;
         for (int s = 0; s < sp.n && ok; ++s) {
             const Params& p = sp.stages[s];
-            for (int t = first_tile(p.tile_base, G, c); t < p.total_tiles; t += G, ++i) {
+            const int t0 = first_tile(p.tile_base, G, c);
+            for (int t = t0; t < p.total_tiles; t += G, ++i) {
                 const int st = i % S, k = i / S;
                 if (k > 0) {
                     int w_ok = 1;
@@ -719,13 +745,19 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
                 find_tile(p, t, si, n0, nrows);
                 uint8_t* stage = ring + (size_t)st * sp.slot_bytes;
                 const uint32_t fb = full0 + 8 * st;
-                const uint32_t expect = (p.glu ? 2u : 1u) * bulk_bytes(p, nrows);
+                const uint32_t expect = (p.glu ? 2u : 1u) * bulk_bytes(p, nrows) + (t == t0 ? meta_bytes(p) : 0u);
                 if (lane == 0)
                     asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;" ::"r"(fb), "r"(expect)
                                  : "memory");
                 __syncwarp();
                 issue_rows(p, p.seg[si], n0, nrows, 0, stage, fb, lane, pol);
                 if (p.glu) issue_rows(p, p.seg[1], n0, nrows, p.TR, stage, fb, lane, pol);
+                if (t == t0 && lane == 0) {
+                    q4d::bulk_g2s(q4d::smem_addr(stage + sp.meta_off), &sp.stages[s], (uint32_t)sizeof(Params), fb);
+                    if (p.norm && p.norm_w)
+                        q4d::bulk_g2s(q4d::smem_addr(stage + sp.meta_off + sizeof(Params)), p.norm_w,
+                                      (uint32_t)p.K * 2u, fb);
+                }
                 q4d::mbar_arrive(fb);
             }
         }
@@ -734,40 +766,46 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
         // ---------------------------------------------------------- consumers
         constexpr uint32_t kCT = kConsumerWarps * 32;
         const int tid = threadIdx.x;
-        store_param_word(&prm[0], tid, load_param_word(sp.stages, tid));
-        q4d::named_bar(1, kCT);
         const uint32_t step = step_sh;
         int i = 0;
         bool bad = false;
         for (int s = 0; s < sp.n; ++s) {
-            const Params& p = prm[s & 1];
-            const int T = p.total_tiles;
-            const int t0 = first_tile(p.tile_base, G, c);
-            const uint32_t xtag = tag_of(step, p.x_stage, p.n_stages);
-            const uint32_t ytag = tag_of(step, p.stage, p.n_stages);
-            const uint32_t rtag = tag_of(step, p.res_stage, p.n_stages);
-            float scale[M];
-            const uint4 next = s + 1 < sp.n ? load_param_word(sp.stages + s + 1, tid) : make_uint4(0, 0, 0, 0);
+            const int2 st_ = tt[s];
+            const int t0 = first_tile(st_.x, G, c), T = st_.y;
             if (t0 < T) {
-                if (p.norm && p.norm_w) stage_norm_weight<M>(p, xs);
-                if (!load_x<M>(p, xs, red, warp, lane, xtag)) bad = true;
+                // The first tile's slot also holds the stage's parameters and
+                // norm weights; they are read from there until the x barrier
+                // (the slot is released only after that tile is consumed).
+                const int sl = i % S;
+                if (!q4d::mbar_wait(full0 + 8 * sl, (i / S) & 1, sp.err)) bad = true;
+                const uint8_t* slot = ring + (size_t)sl * sp.slot_bytes;
+                const Params& ps = *reinterpret_cast<const Params*>(slot + sp.meta_off);
+                if (tid < kParamWords)
+                    reinterpret_cast<uint4*>(prm)[tid] = reinterpret_cast<const uint4*>(&ps)[tid];
+                const uint32_t xtag = tag_of(step, ps.x_stage, ps.n_stages);
+                const uint16_t* gam =
+                    (ps.norm && ps.norm_w) ? reinterpret_cast<const uint16_t*>(slot + sp.meta_off + sizeof(Params))
+                                           : nullptr;
+                if (!bad && !load_x<M>(ps, xs, red, warp, lane, xtag, gam)) bad = true;
                 q4d::named_bar(1, kCT);
+                const Params& p = *prm;
+                const uint32_t ytag = tag_of(step, p.stage, p.n_stages);
+                const uint32_t rtag = tag_of(step, p.res_stage, p.n_stages);
+                float scale[M];
                 norm_scales<M>(p, red, scale);
-            }
-            // the other parameter slot was last read in stage s-1, which every
-            // consumer has left (end-of-stage barrier below)
-            if (s + 1 < sp.n) store_param_word(&prm[(s + 1) & 1], tid, next);
-            if (t0 < T && !bad) {
-                for (int t = t0; t < T; t += G, ++i) {
-                    const int st = i % S, k = i / S;
-                    if (!q4d::mbar_wait(full0 + 8 * st, k & 1, sp.err)) {
-                        bad = true;
-                        break;
+                if (!bad) {
+                    for (int t = t0; t < T; t += G, ++i) {
+                        const int st = i % S, k = i / S;
+                        if (!q4d::mbar_wait(full0 + 8 * st, k & 1, sp.err)) {
+                            bad = true;
+                            break;
+                        }
+                        if (!consume_tile<M>(p, ring + (size_t)st * sp.slot_bytes, xs, scale, warp, lane, t, ytag,
+                                             rtag))
+                            bad = true;
+                        __syncwarp();
+                        if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
                     }
-                    if (!consume_tile<M>(p, ring + (size_t)st * sp.slot_bytes, xs, scale, warp, lane, t, ytag, rtag))
-                        bad = true;
-                    __syncwarp();
-                    if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
                 }
             }
             if (q4d::named_bar_or(1, kCT, bad)) {
@@ -1022,7 +1060,7 @@ q4_status persistent_plan(const q4_gemv_desc* d, const GemvTagged* tg, int n, vo
     if (n < 1) return fail(Q4_ERR_INVALID_ARG, "no stages");
     const int M = d[0].M;
     Params* P = static_cast<Params*>(host_params);
-    uint32_t slot = 0, xb = 0;
+    uint32_t tile_max = 0, gamma_max = 0, xb = 0;
     int base = 0;
     for (int s = 0; s < n; ++s) {
         if (d[s].M != M) return Q4_OK;
@@ -1030,13 +1068,17 @@ q4_status persistent_plan(const q4_gemv_desc* d, const GemvTagged* tg, int n, vo
         fill_params(d[s], &tg[s], true, dev->sms, 24u * 1024u, dev->err_word, P[s]);
         P[s].tile_base = base;
         base += P[s].total_tiles;
-        if (P[s].stage_bytes > slot) slot = P[s].stage_bytes;
+        if (P[s].stage_bytes > tile_max) tile_max = P[s].stage_bytes;
+        if (P[s].norm && P[s].norm_w && (uint32_t)d[s].K * 2u > gamma_max) gamma_max = (uint32_t)d[s].K * 2u;
         const uint32_t x = (x_smem_bytes(M, d[s].K) + 127u) & ~127u;
         if (x > xb) xb = x;
     }
-    const size_t fixed = (size_t)xb + q4k::kStepBarBytes + 2 * sizeof(Params);
+    // A slot: tile data, then (first tile of a stage only) the parameter block
+    // and the norm weights at a fixed offset.
+    const uint32_t slot = (tile_max + (uint32_t)sizeof(Params) + gamma_max + 127u) & ~127u;
+    const size_t fixed =
+        ((size_t)xb + q4k::kStepBarBytes + sizeof(Params) + (((size_t)n * 8 + 15) & ~(size_t)15) + 127) & ~(size_t)127;
     const size_t avail = (size_t)dev->smem_optin - 256;  // the kernel's static shared variables
-    const int per_sm = 1;
     if (fixed + 2 * (size_t)slot > avail) return Q4_OK;  // does not fit: the caller plans launches
     int slots = (int)((avail - fixed) / slot);
     if (slots > q4k::kMaxSlots) slots = q4k::kMaxSlots;
@@ -1046,9 +1088,11 @@ q4_status persistent_plan(const q4_gemv_desc* d, const GemvTagged* tg, int n, vo
     }
     g->M = M;
     g->n = n;
-    g->grid = dev->sms * per_sm;
+    g->grid = dev->sms;
     g->slots = slots;
     g->slot_bytes = slot;
+    g->meta_off = slot - (uint32_t)sizeof(Params) - gamma_max;
+    g->ring_off = (uint32_t)fixed;
     g->x_bytes = xb;
     g->smem = fixed + (size_t)slots * slot;
     g->step_ctr = tg[0].step_ctr;
@@ -1094,6 +1138,8 @@ q4_status persistent_launch(const PersistentGeom& g, const void* dev_params, cud
     sp.n = g.n;
     sp.slots = g.slots;
     sp.slot_bytes = g.slot_bytes;
+    sp.meta_off = g.meta_off;
+    sp.ring_off = g.ring_off;
     sp.x_bytes = g.x_bytes;
     sp.step_ctr = g.step_ctr;
     sp.done_ctr = g.done_ctr;

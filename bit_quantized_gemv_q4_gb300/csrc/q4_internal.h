@@ -63,7 +63,7 @@ size_t gemv_params_bytes();
 
 struct PersistentGeom {
     int M = 0, n = 0, grid = 0, slots = 0;
-    uint32_t slot_bytes = 0, x_bytes = 0;
+    uint32_t slot_bytes = 0, meta_off = 0, ring_off = 0, x_bytes = 0;
     size_t smem = 0;
     const uint32_t* step_ctr = nullptr;
     uint32_t* done_ctr = nullptr;
