@@ -79,6 +79,7 @@ class ClockSampler:
 
     def __init__(self, index: int):
         self.index, self.proc, self.lines = index, None, []
+        self.t0 = self.t1 = None
 
     def __enter__(self):
         try:
@@ -87,13 +88,23 @@ class ClockSampler:
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
+            deadline = time.time() + 5.0  # the first reading, so sampling covers the region
+            while not self.lines and time.time() < deadline and self.proc.poll() is None:
+                time.sleep(0.01)
         except Exception:
             self.proc = None
         return self
 
     def _read(self):
         for ln in self.proc.stdout:
-            self.lines.append(ln.strip())
+            self.lines.append((time.time(), ln.strip()))
+
+    def start(self):
+        self.t0 = time.time()
+
+    def stop(self):
+        self.t1 = time.time()
+        time.sleep(0.25)  # let the reading that follows the region arrive
 
     def __exit__(self, *a):
         if self.proc:
@@ -104,9 +115,19 @@ class ClockSampler:
                 self.proc.kill()
 
     def summary(self):
+        """Median SM clock and active slowdown reasons over the readings taken
+        inside [start, stop]; a region shorter than the 100 ms reading period
+        uses the first reading after it (noted in "window")."""
+        t0 = self.t0 if self.t0 is not None else 0.0
+        t1 = self.t1 if self.t1 is not None else float("inf")
+        inside = [ln for ts, ln in self.lines if t0 <= ts <= t1]
+        window = "timed region"
+        if not inside:
+            after = [ln for ts, ln in self.lines if ts > t1][:1]
+            inside, window = after, "first reading after the timed region (region shorter than 100 ms)"
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ln in inside:
             p = [v.strip() for v in ln.split(",")]
             if len(p) < 7:
                 continue
@@ -120,12 +141,13 @@ class ClockSampler:
                     reasons.add(nm)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm),
+                "window": window}
 
 
 # ------------------------------------------------------------------ workload
 
-def make_model(shape, device):
+def make_model(shape, device, layers=True):
     import torch
 
     import q4synth
@@ -134,6 +156,9 @@ def make_model(shape, device):
         return (torch.from_numpy(m.Wq.view("int32")).to(device), torch.from_numpy(m.scales).to(device),
                 torch.from_numpy(m.biases).to(device), m.N, m.K)
 
+    if not layers:  # the lm_head alone, with the seed the whole stack gives it
+        lm = q4synth.q4_matrix(q4synth.BASE_SEED + 16 * shape.n_layers, shape.vocab, shape.hidden)
+        return None, dev(lm), None
     layers, lm = q4synth.decode_weights(shape)
     return [{k: dev(v) for k, v in d.items()} for d in layers], dev(lm), (layers, lm)
 
@@ -252,6 +277,30 @@ def moe_prefill(device, iters: int = 20, warmup: int = 5, token_counts=(128, 512
     return out
 
 
+def lm_head_ms(q4, dlm, x, M, stream, device):
+    """The largest single launch alone (the lm_head GEMV shape): 8 warm-up
+    launches, then 64 timed back to back over 4 distinct weight copies
+    (350 MB > L2, so no launch hits in L2)."""
+    import torch
+    Wq, s, b, N, K = dlm
+    mats = [(Wq, s, b)]
+    for i in range(3):
+        g = torch.Generator(device=device).manual_seed(100 + i)
+        mats.append((torch.randint(-2**31, 2**31 - 1, Wq.shape, dtype=torch.int32, device=device, generator=g),
+                     s.roll(i + 1, 0).contiguous(), b.roll(i + 1, 0).contiguous()))
+    yv = torch.empty(M, N, dtype=torch.float32, device=device)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    for i in range(8):
+        q4.q4_gemv(*mats[i % 4], x, yv, M, N, K, stream)
+    e0.record(stream)
+    for i in range(64):
+        q4.q4_gemv(*mats[i % 4], x, yv, M, N, K, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    return e0.elapsed_time(e1) / 64
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -260,8 +309,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--section", default="all", choices=["all", "decode", "moe"],
-                    help="moe: only the MoE prefill timings (for profiling runs)")
+    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head"],
+                    help="moe / lm_head: only the MoE prefill timings / the lm_head GEMV timing "
+                         "(for profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -330,6 +380,16 @@ def main():
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=device)
 
+    if args.section == "lm_head":
+        _, dlm, _ = make_model(shape, device, layers=False)
+        xl = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4242, M, shape.hidden)).to(device)
+        ms_l = lm_head_ms(q4, dlm, xl, M, torch.cuda.current_stream(device), device)
+        nb = shape.vocab * shape.hidden * 0.5625 + shape.hidden * 2 + shape.vocab * 4
+        peak, peak_kind = peaks()
+        print(json.dumps({"lm_head_gemv": {"ms": ms_l, "gbs": nb / (ms_l / 1000.0) / 1e9,
+                                           "frac": nb / (ms_l / 1000.0) / 1e9 / peak, "peak_kind": peak_kind,
+                                           "shape": f"M={M} N={shape.vocab} K={shape.hidden}, 4 rotating copies"}}))
+        return
     dl, dlm, host_model = make_model(shape, device)
     table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
     nws = q4.q4_decode_workspace_bytes(table)
@@ -356,11 +416,13 @@ def main():
     e1 = torch.cuda.Event(enable_timing=True)
     with ClockSampler(local) as clk:
         barrier()
+        clk.start()
         e0.record(stream)
         for _ in range(args.steps):
             q4.q4_decode_step(table, x, logits, stream)
         e1.record(stream)
         barrier()
+        clk.stop()
     ms = e0.elapsed_time(e1)
     if world > 1:
         t = torch.tensor([ms], device=device)
@@ -391,26 +453,7 @@ def main():
         ms_e2e = float(t.item())
     e2e_value = world * M * args.steps / (ms_e2e / 1000.0)
 
-    # ---- the largest single launch alone (the lm_head GEMV shape), back to
-    # back over 4 distinct weight copies (350 MB > L2) so no launch hits in L2
-    lm_ms = None
-    if rank == 0:
-        Wq, s, b, N, K = dlm
-        mats = [(Wq, s, b)]
-        for i in range(3):
-            g = torch.Generator(device=device).manual_seed(100 + i)
-            mats.append((torch.randint(-2**31, 2**31 - 1, Wq.shape, dtype=torch.int32, device=device, generator=g),
-                         s.roll(i + 1, 0).contiguous(), b.roll(i + 1, 0).contiguous()))
-        yv = torch.empty(M, N, dtype=torch.float32, device=device)
-        for i in range(8):
-            q4.q4_gemv(*mats[i % 4], x, yv, M, N, K, stream)
-        e0.record(stream)
-        for i in range(64):
-            q4.q4_gemv(*mats[i % 4], x, yv, M, N, K, stream)
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-        lm_ms = e0.elapsed_time(e1) / 64
-        del mats
+    lm_ms = lm_head_ms(q4, dlm, x, M, stream, device) if rank == 0 else None
     st = q4.q4_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {st} after timing")
