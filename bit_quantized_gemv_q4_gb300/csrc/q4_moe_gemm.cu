@@ -19,6 +19,9 @@
 // * Warp 0 (TMA): per 64-wide K step, the packed codes of the unit's 128 rows
 //   (one 2-D tensor-map copy per matrix, 128 rows x 32 bytes) and the X tile
 //   (128 rows x 64 fp16, 128-byte swizzle = the canonical K-major UMMA layout).
+// * Warp 0 also bulk-copies each unit's scale and bias block (the unit's 128
+//   rows are contiguous in both arrays) into a staging buffer; the dequant
+//   threads move their row's values into private shared slots at unit start.
 // * Warps 2..9 (dequant): codes -> fp16 w = s*q + b with the code OR-ed into
 //   the mantissa of 1024.0/64.0 (exact), one fp16 subtract and one fp16 FMA per
 //   pair (w rounded once to fp16), written as the A tile in the same swizzled
@@ -65,7 +68,8 @@ struct Params {
     void* Y;
     int E, N, K, R, rows_e, nmat, glu, out_f16;
     int n_tiles, nK, G;
-    uint32_t sb_bytes;
+    uint32_t sb_bytes;   // private per-thread scale/bias slots
+    uint32_t stg_bytes;  // staging buffer: the unit's scale and bias blocks
     int* err;
 };
 
@@ -73,6 +77,7 @@ struct Smem {
     uint64_t in_full[kInStages], in_empty[kInStages];
     uint64_t a_full[kAStages], a_empty[kAStages];
     uint64_t acc_full[2], acc_empty[2];
+    uint64_t sb_full, sb_empty;  // staging buffer of the unit's scales and biases
     uint64_t drain;  // completion probe for in-flight MMAs on the abort path
     uint32_t tmem_base;
     volatile int abort;
@@ -197,7 +202,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* in_ring = base;
     uint8_t* a_ring = in_ring + kInStages * kInStageBytes;
     uint32_t* sb = reinterpret_cast<uint32_t*>(a_ring + kAStages * kAStageBytes);
-    Smem& sm = *reinterpret_cast<Smem*>(reinterpret_cast<uint8_t*>(sb) + p.sb_bytes);
+    uint8_t* stg = reinterpret_cast<uint8_t*>(sb) + p.sb_bytes;
+    Smem& sm = *reinterpret_cast<Smem*>(stg + p.stg_bytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -214,6 +220,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             q4d::mbar_init(q4d::smem_addr(&sm.acc_full[i]), 1);
             q4d::mbar_init(q4d::smem_addr(&sm.acc_empty[i]), kEpiWarps);
         }
+        q4d::mbar_init(q4d::smem_addr(&sm.sb_full), 1);
+        q4d::mbar_init(q4d::smem_addr(&sm.sb_empty), kDeqWarps);
         q4d::mbar_init(q4d::smem_addr(&sm.drain), 1);
         sm.abort = 0;
         q4d::fence_mbar_init();
@@ -249,10 +257,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
-            int it = 0;
-            for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x) {
+            int it = 0, uu = 0, staged = 0;
+            const uint32_t blk = (uint32_t)kRows * (uint32_t)p.G * 2u;  // one matrix's scales (or biases) of a unit
+            for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++uu) {
                 const Unit un = decode_unit(sm, p, u);
                 const int wrow = un.e * p.rows_e + un.nt * kRows;
+                // the staging buffer is free once every dequant warp has read the previous unit's values
+                if (uu > 0 && !wait_bar(sm, sm.sb_empty, (uu - 1) & 1, p.err)) break;
+                {
+                    const uint32_t fb = q4d::smem_addr(&sm.sb_full);
+                    q4d::mbar_arrive_expect_tx(fb, (uint32_t)p.nmat * 2u * blk);
+                    for (int m = 0; m < p.nmat; ++m) {
+                        const size_t r = (size_t)wrow + (size_t)m * p.N;
+                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m) * blk), p.scales + r * p.G, blk, fb);
+                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m + 1) * blk), p.biases + r * p.G, blk, fb);
+                    }
+                    ++staged;
+                }
                 for (int ks = 0; ks < nK; ++ks, ++it) {
                     const int s = it % kInStages;
                     if (it >= kInStages && !wait_bar(sm, sm.in_empty[s], ((it / kInStages) - 1) & 1, p.err)) break;
@@ -268,6 +289,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // let this thread's last copies land before the CTA can exit
                 for (int j = (it > kInStages ? it - kInStages : 0); j < it; ++j)
                     q4d::mbar_wait(q4d::smem_addr(&sm.in_full[j % kInStages]), (j / kInStages) & 1, nullptr);
+                if (staged > 0) q4d::mbar_wait(q4d::smem_addr(&sm.sb_full), (staged - 1) & 1, nullptr);
             }
         }
     } else if (warp == 1) {
@@ -319,13 +341,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int m = p.glu ? part : 0;
         const int G = p.G, Gp = G + 1;
         uint32_t* my_sb = sb + (size_t)dt * Gp;
-        int it = 0;
-        for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x) {
-            const Unit un = decode_unit(sm, p, u);
-            const size_t grow = (size_t)un.e * p.rows_e + (size_t)m * p.N + (size_t)un.nt * kRows + row;
-            const uint16_t* sp = p.scales + grow * G;
-            const uint16_t* bp = p.biases + grow * G;
-            for (int g = 0; g < G; ++g) my_sb[g] = (uint32_t)__ldg(sp + g) | ((uint32_t)__ldg(bp + g) << 16);
+        const uint32_t blk = (uint32_t)kRows * (uint32_t)G * 2u;
+        const uint16_t* sp = reinterpret_cast<const uint16_t*>(stg + (2 * m) * blk) + (size_t)row * G;
+        const uint16_t* bp = reinterpret_cast<const uint16_t*>(stg + (2 * m + 1) * blk) + (size_t)row * G;
+        int it = 0, uu = 0;
+        for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++uu) {
+            // this unit's scales and biases, from the staging buffer into private slots
+            if (!__all_sync(0xffffffffu, wait_bar(sm, sm.sb_full, uu & 1, p.err))) {
+                sm.abort = 1;
+                break;
+            }
+            if ((G & 3) == 0) {
+                for (int g = 0; g < G; g += 4) {  // 8-byte loads: 4 values of a row
+                    const uint2 s4 = *reinterpret_cast<const uint2*>(sp + g);
+                    const uint2 b4 = *reinterpret_cast<const uint2*>(bp + g);
+                    my_sb[g] = prmt(s4.x, b4.x, 0x5410);
+                    my_sb[g + 1] = prmt(s4.x, b4.x, 0x7632);
+                    my_sb[g + 2] = prmt(s4.y, b4.y, 0x5410);
+                    my_sb[g + 3] = prmt(s4.y, b4.y, 0x7632);
+                }
+            } else {
+                for (int g = 0; g < G; ++g) my_sb[g] = (uint32_t)sp[g] | ((uint32_t)bp[g] << 16);
+            }
+            __syncwarp();
+            if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&sm.sb_empty));
             bool ok = true;
             for (int ks = 0; ks < nK; ++ks, ++it) {
                 const int s = it % kInStages, a = it % kAStages;
@@ -496,7 +535,8 @@ extern "C" q4_status q4_moe_gemm(const uint32_t* Wq, const uint16_t* scales, con
     if (d->mode != Q4_GEMV_PLAIN && d->mode != Q4_GEMV_GLU) return fail(Q4_ERR_INVALID_ARG, "bad mode");
     if (d->out_dtype != Q4_F32 && d->out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "bad out_dtype");
     if (d->mode == Q4_GEMV_GLU && d->out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "GLU mode writes fp16");
-    if (!aligned16(Wq) || !aligned16(X)) return fail(Q4_ERR_MISALIGNED, "Wq and X must be 16-byte aligned");
+    if (!aligned16(Wq) || !aligned16(X) || !aligned16(scales) || !aligned16(biases))
+        return fail(Q4_ERR_MISALIGNED, "Wq, X, scales and biases must be 16-byte aligned");
     if ((long long)d->E * (d->mode == Q4_GEMV_GLU ? 2 : 1) * d->N > (1ll << 31))
         return fail(Q4_ERR_UNSUPPORTED, "too many weight rows");
     const DeviceInfo* dev = nullptr;
@@ -521,6 +561,7 @@ extern "C" q4_status q4_moe_gemm(const uint32_t* Wq, const uint16_t* scales, con
     p.nK = d->K / q4g::kKS;
     p.G = d->K / 64;
     p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqThreads * (p.G + 1) * 4 + 127) & ~size_t(127));
+    p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
     p.err = dev->err_word;
 
     CUtensorMap tmW, tmX;
@@ -533,7 +574,7 @@ extern "C" q4_status q4_moe_gemm(const uint32_t* Wq, const uint16_t* scales, con
     if (st != Q4_OK) return st;
 
     const size_t smem = 1024 + (size_t)q4g::kInStages * q4g::kInStageBytes + (size_t)q4g::kAStages * q4g::kAStageBytes +
-                        p.sb_bytes + sizeof(q4g::Smem);
+                        p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
     if (smem > (size_t)dev->smem_optin)
         return fail(Q4_ERR_UNSUPPORTED, "K=%d needs %zu bytes of shared memory", d->K, smem);
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

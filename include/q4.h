@@ -326,7 +326,11 @@ typedef struct q4_moe_desc {
  * expert_ids: int32 [R], the expert of each row (checked against offsets on
  * the device; a mismatch latches Q4_ERR_DEVICE_CHECK).  Y: [R][N].
  * Runs on the tensor cores (tcgen05, fp16 x fp16 -> fp32), weights
- * dequantised to fp16 in shared memory, never in global memory. */
+ * dequantised to fp16 in shared memory, never in global memory.
+ * N must be a multiple of 128 (else Q4_ERR_UNSUPPORTED); Wq, scales, biases
+ * and X must be 16-byte aligned (else Q4_ERR_MISALIGNED); a K whose tiles do
+ * not fit in shared memory (K above 2560 in GLU mode, 3584 in PLAIN mode) returns
+ * Q4_ERR_UNSUPPORTED. */
 q4_status q4_moe_gemm(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                       const uint16_t *X, const int32_t *expert_ids, const int32_t *offsets,
                       void *Y, const q4_moe_desc *desc, q4_stream_t stream);
