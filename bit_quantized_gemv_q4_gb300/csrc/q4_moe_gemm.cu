@@ -26,10 +26,14 @@
 //   the mantissa of 1024.0/64.0 (exact), one fp16 subtract and one fp16 FMA per
 //   pair (w rounded once to fp16), written as the A tile in the same swizzled
 //   K-major layout, fenced to the async proxy.
-// * Warp 1 (MMA): one thread issues tcgen05.mma kind::f16 (fp16 x fp16 ->
-//   fp32) into a double-buffered TMEM accumulator (gate and up side by side),
-//   committing to mbarriers to release input stages and hand the accumulator
-//   to the epilogue.
+// * Warp 1 (MMA; in GLU mode warp 14 for the up matrix): one thread per
+//   matrix issues tcgen05.mma kind::f16 (fp16 x fp16 -> fp32) into a
+//   double-buffered TMEM accumulator (gate and up side by side), committing
+//   to mbarriers to release input stages and hand the accumulator to the
+//   epilogue.  With few tokens per unit an MMA is small and the issuing
+//   thread, not the tensor core, sets the pace (a per-role timestamp trace
+//   measured ~70 ns per 128x16x16 tcgen05.mma), so gate and up get an issuer
+//   each.
 // * Warps 10..13 (epilogue): tcgen05.ld of the accumulator, SiLU*up or plain,
 //   coalesced stores.
 // * Every mbarrier wait is bounded; on expiry the CTA latches an error bit,
@@ -50,7 +54,8 @@ constexpr int kInStages = 3;      // codes + X ring
 constexpr int kAStages = 2;       // dequantised A ring
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
-constexpr int kThreads = (2 + kDeqWarps + kEpiWarps) * 32;
+constexpr int kUpMmaWarp = 2 + kDeqWarps + kEpiWarps;  // 14
+constexpr int kThreads = (kUpMmaWarp + 1) * 32;
 constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kMaxExperts = 256;
 constexpr uint32_t kTmemCols = 512;   // 2 accumulator buffers x (gate + up) x 128 columns
@@ -210,19 +215,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < kInStages; ++i) {
             q4d::mbar_init(q4d::smem_addr(&sm.in_full[i]), 1);
-            q4d::mbar_init(q4d::smem_addr(&sm.in_empty[i]), kDeqWarps + 1);
+            q4d::mbar_init(q4d::smem_addr(&sm.in_empty[i]), kDeqWarps + p.nmat);
         }
         for (int i = 0; i < kAStages; ++i) {
             q4d::mbar_init(q4d::smem_addr(&sm.a_full[i]), kDeqWarps);
-            q4d::mbar_init(q4d::smem_addr(&sm.a_empty[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&sm.a_empty[i]), p.nmat);
         }
         for (int i = 0; i < 2; ++i) {
-            q4d::mbar_init(q4d::smem_addr(&sm.acc_full[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&sm.acc_full[i]), p.nmat);
             q4d::mbar_init(q4d::smem_addr(&sm.acc_empty[i]), kEpiWarps);
         }
         q4d::mbar_init(q4d::smem_addr(&sm.sb_full), 1);
         q4d::mbar_init(q4d::smem_addr(&sm.sb_empty), kDeqWarps);
-        q4d::mbar_init(q4d::smem_addr(&sm.drain), 1);
+        q4d::mbar_init(q4d::smem_addr(&sm.drain), p.nmat);
         sm.abort = 0;
         q4d::fence_mbar_init();
     }
@@ -292,9 +297,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (staged > 0) q4d::mbar_wait(q4d::smem_addr(&sm.sb_full), (staged - 1) & 1, nullptr);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == kUpMmaWarp) {
         // ------------------------------------------------------------ MMA
-        if (lane == 0) {
+        // matrix mi of the unit (0: the plain matrix or gate, 1: up)
+        const int mi = warp == 1 ? 0 : 1;
+        if (lane == 0 && mi < p.nmat) {
             int it = 0, acc_it = 0;
             for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++acc_it) {
                 const Unit un = decode_unit(sm, p, u);
@@ -315,11 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tc_fence_after();
                     const uint32_t xs = q4d::smem_addr(in_ring + s * kInStageBytes + 2 * kCodesBytes);
                     const uint32_t as = q4d::smem_addr(a_ring + a * kAStageBytes);
-                    for (int m = 0; m < p.nmat; ++m) {
+                    {
+                        // K-chunk kk advances both descriptors' start address by 32 bytes
+                        const uint64_t ad = sw128_desc(as + mi * kATileBytes), xd = sw128_desc(xs);
+                        const uint32_t dm = d0 + (uint32_t)(mi * kTN);
 #pragma unroll
                         for (int kk = 0; kk < kKS / 16; ++kk)
-                            mma_f16(d0 + (uint32_t)(m * kTN), sw128_desc(as + m * kATileBytes + kk * 32),
-                                    sw128_desc(xs + kk * 32), idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(q4d::smem_addr(&sm.in_empty[s]));
                     mma_commit(q4d::smem_addr(&sm.a_empty[a]));
@@ -449,6 +458,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // give in-flight tensor-core work a bounded moment via one more commit.
     tc_fence_before();
     __syncthreads();
+    if (warp == kUpMmaWarp && sm.abort && p.nmat == 2) {
+        if (lane == 0) {
+            // completes once every MMA of both issuers has finished
+            mma_commit(q4d::smem_addr(&sm.drain));
+            q4d::mbar_wait(q4d::smem_addr(&sm.drain), 0, nullptr);
+        }
+        __syncwarp();
+    }
     if (warp == 1) {
         if (sm.abort) {
             if (lane == 0) {
