@@ -277,6 +277,23 @@ def moe_prefill(device, iters: int = 20, warmup: int = 5, token_counts=(128, 512
     return out
 
 
+def max_over_ranks(ms: float, world: int, device=None) -> float:
+    """The slowest rank's time: replicas run independently, so the job takes
+    as long as its slowest replica (all-reduce MAX when world > 1)."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_rate(world: int, tokens_per_rank_step: int, steps: int, ms_max: float) -> float:
+    """Whole-job tokens per second: every rank decodes its own tokens."""
+    return world * tokens_per_rank_step * steps / (ms_max / 1000.0)
+
+
 def lm_head_ms(q4, dlm, x, M, stream, device):
     """The largest single launch alone (the lm_head GEMV shape): 8 warm-up
     launches, then 64 timed back to back over 4 distinct weight copies
@@ -304,7 +321,7 @@ def lm_head_ms(q4, dlm, x, M, stream, device):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)  # ~0.36 s timed: several clock readings
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
@@ -423,13 +440,9 @@ def main():
         e1.record(stream)
         barrier()
         clk.stop()
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world, device)
     ms_per_step = ms / args.steps
-    value = world * M * args.steps / (ms / 1000.0)
+    value = job_rate(world, M, args.steps, ms)
 
     # ---- end to end through the C ABI with host buffers
     x_pin = x_host.pin_memory()
@@ -446,12 +459,8 @@ def main():
         out_pin.copy_(logits, non_blocking=True)
     e1.record(stream)
     barrier()
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([ms_e2e], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms_e2e = float(t.item())
-    e2e_value = world * M * args.steps / (ms_e2e / 1000.0)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world, device)
+    e2e_value = job_rate(world, M, args.steps, ms_e2e)
 
     lm_ms = lm_head_ms(q4, dlm, x, M, stream, device) if rank == 0 else None
     st = q4.q4_device_status(stream)
