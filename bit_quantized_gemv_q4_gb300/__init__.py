@@ -13,7 +13,7 @@ import ctypes
 import os
 
 __all__ = [
-    "Q4Error", "lib", "q4_gemv", "q4_gemv_ex", "Segment", "q4_device_status",
+    "Q4Error", "lib", "q4_selftest_expired_wait", "q4_gemv", "q4_gemv_ex", "Segment", "q4_device_status",
     "LayerTable", "q4_decode_step", "q4_decode_workspace_bytes", "q4_decode_buffers",
     "q4_layer_table_release", "q4_moe_route", "q4_moe_route_workspace_bytes",
     "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine",
@@ -34,7 +34,8 @@ STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q
           -4: "Q4_ERR_CUDA", -5: "Q4_ERR_TIMEOUT", -6: "Q4_ERR_NO_DEVICE", -7: "Q4_ERR_DEVICE_CHECK"}
 
 # Every symbol include/q4.h declares.
-EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status", "q4_gemv",
+EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status",
+           "q4_selftest_expired_wait", "q4_gemv",
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
            "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
            "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine"]
@@ -104,6 +105,8 @@ def lib() -> ctypes.CDLL:
         L.q4_version.restype = i32
         L.q4_device_status.restype = st
         L.q4_device_status.argtypes = [vp]
+        L.q4_selftest_expired_wait.restype = st
+        L.q4_selftest_expired_wait.argtypes = [vp]
         L.q4_gemv.restype = st
         L.q4_gemv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
         L.q4_gemv_ex.restype = st
@@ -158,6 +161,11 @@ def _stream(stream) -> int | None:
 def q4_device_status(stream=None) -> int:
     """Synchronise and return (and clear) the device error status (0 = ok)."""
     return lib().q4_device_status(_stream(stream))
+
+
+def q4_selftest_expired_wait(stream=None):
+    """Enqueue the bounded-wait self-test (each wait expires after 2 s)."""
+    _check(lib().q4_selftest_expired_wait(_stream(stream)), "q4_selftest_expired_wait")
 
 
 # ------------------------------------------------------------------ GEMV ---

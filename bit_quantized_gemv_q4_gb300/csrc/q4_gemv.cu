@@ -830,7 +830,33 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
     }
 }
 
+// Failure-detection self-test: both bounded waits against conditions that
+// never come true; each latches kErrTimeout into the error word and returns.
+__device__ uint32_t g_never_written_tagged_word;  // stays 0: tag 0 is never a valid tag
+
+__global__ void expired_wait_kernel(int* err) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        uint32_t w;
+        poll_tagged<1>(&g_never_written_tagged_word, 1u, &w, err);
+        q4d::mbar_init(q4d::smem_addr(&bar), 1);
+        q4d::fence_mbar_init();
+        q4d::mbar_wait(q4d::smem_addr(&bar), 0, err);  // nothing arrives
+    }
+}
+
 }  // namespace q4k
+
+extern "C" q4_status q4_selftest_expired_wait(q4_stream_t stream) {
+    q4i::clear_error();
+    const q4i::DeviceInfo* dev = nullptr;
+    q4_status st = q4i::current_device(&dev);
+    if (st != Q4_OK) return st;
+    q4k::expired_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(dev->err_word);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return q4i::cuda_fail(e, "self-test kernel launch");
+    return Q4_OK;
+}
 
 namespace q4i {
 

@@ -78,6 +78,16 @@ int q4_version(void);
  * Returns Q4_OK, Q4_ERR_TIMEOUT, Q4_ERR_DEVICE_CHECK or Q4_ERR_CUDA. */
 q4_status q4_device_status(q4_stream_t stream);
 
+/* Failure-detection self-test (no counterpart in the pages): enqueues one
+ * small kernel on `stream` that runs the library's two bounded device waits
+ * against conditions nothing will ever satisfy -- a tagged activation word
+ * that no stage writes and an mbarrier no thread arrives on.  Each wait gives
+ * up after its limit (2 s), latches Q4_ERR_TIMEOUT into the device error word
+ * and returns, so the kernel ends normally (~4 s) and the context stays
+ * usable; q4_device_status() then reports Q4_ERR_TIMEOUT.  No fault, trap or
+ * endless loop is involved.  Returns launch errors only. */
+q4_status q4_selftest_expired_wait(q4_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * 1. q4_gemv -- y[m][n] = sum_k w[n][k] * x[m][k], m < M, n < N.
  *
