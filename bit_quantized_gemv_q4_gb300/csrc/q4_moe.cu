@@ -117,25 +117,28 @@ __global__ void route_scan_kernel(int32_t* __restrict__ count, int E, int B, int
 }
 
 // Row of each (token, rank): base[e][b] + number of earlier tokens of the
-// block that hold expert e.  One warp per block.
-__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int T, int topk, int B,
+// block that hold expert e.  One warp per block walks its tokens in order;
+// lane k < topk takes the token's k-th expert and bumps that expert's
+// counter (a token holds an expert at most once, so the lanes' counters are
+// distinct and the walk needs no atomics).
+__global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int topk, int B,
                                      const int32_t* __restrict__ base, int32_t* __restrict__ token_of,
                                      int32_t* __restrict__ expert_of, int32_t* __restrict__ pos) {
-    __shared__ int32_t tab[kBlockTokens][kMaxTopk];
+    __shared__ int32_t cnt[kMaxExperts];
     const int b = blockIdx.x, lane = threadIdx.x;
-    const int t = b * kBlockTokens + lane;
-    for (int k = 0; k < kMaxTopk; ++k) tab[lane][k] = (t < T && k < topk) ? ids[(size_t)t * topk + k] : -1;
+    for (int e = lane; e < E; e += 32) cnt[e] = 0;
     __syncwarp();
-    if (t >= T) return;
-    for (int k = 0; k < topk; ++k) {
-        const int e = tab[lane][k];
-        int before = 0;
-        for (int l = 0; l < lane; ++l)
-            for (int kk = 0; kk < topk; ++kk) before += tab[l][kk] == e;
-        const int r = base[(size_t)e * B + b] + before;
-        token_of[r] = t;
-        expert_of[r] = e;
-        pos[(size_t)t * topk + k] = r;
+    const int t_end = min(T, (b + 1) * kBlockTokens);
+    for (int t = b * kBlockTokens; t < t_end; ++t) {
+        if (lane < topk) {
+            const int e = ids[(size_t)t * topk + lane];
+            const int r = base[(size_t)e * B + b] + cnt[e];
+            cnt[e] += 1;
+            token_of[r] = t;
+            expert_of[r] = e;
+            pos[(size_t)t * topk + lane] = r;
+        }
+        __syncwarp();
     }
 }
 
@@ -211,7 +214,7 @@ q4_status q4_moe_route(const uint16_t* logits, int T, int E, int topk, int32_t* 
     q4m::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights);
     q4m::route_count_kernel<<<B, 32, 0, s>>>(topk_ids, T, E, topk, B, count);
     q4m::route_scan_kernel<<<1, 1024, 0, s>>>(count, E, B, offsets);
-    q4m::route_scatter_kernel<<<B, 32, 0, s>>>(topk_ids, T, topk, B, count, token_of, expert_of, pos);
+    q4m::route_scatter_kernel<<<B, 32, 0, s>>>(topk_ids, T, E, topk, B, count, token_of, expert_of, pos);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "q4_moe_route launch");
     return Q4_OK;
@@ -322,7 +325,7 @@ extern "C" q4_status q4_moe_route_noalloc(const uint16_t* logits, int T, int E, 
     q4m::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights);
     q4m::route_count_kernel<<<Bi, 32, 0, s>>>(topk_ids, T, E, topk, Bi, scratch);
     q4m::route_scan_kernel<<<1, 1024, 0, s>>>(scratch, E, Bi, offsets);
-    q4m::route_scatter_kernel<<<Bi, 32, 0, s>>>(topk_ids, T, topk, Bi, scratch, token_of, expert_of, pos);
+    q4m::route_scatter_kernel<<<Bi, 32, 0, s>>>(topk_ids, T, E, topk, Bi, scratch, token_of, expert_of, pos);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "q4_moe_route_noalloc launch");
     return Q4_OK;
