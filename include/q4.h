@@ -339,7 +339,8 @@ typedef struct q4_moe_desc {
  * dequantised to fp16 in shared memory, never in global memory.
  * N must be a multiple of 128 (else Q4_ERR_UNSUPPORTED); Wq, scales, biases
  * and X must be 16-byte aligned (else Q4_ERR_MISALIGNED); a K whose tiles do
- * not fit in shared memory (K above 2560 in GLU mode, 3584 in PLAIN mode) returns
+ * not fit in shared memory (with 227 KB per block: K above 2752 in GLU mode,
+ * 3712 in PLAIN mode) returns
  * Q4_ERR_UNSUPPORTED. */
 q4_status q4_moe_gemm(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                       const uint16_t *X, const int32_t *expert_ids, const int32_t *offsets,

@@ -183,3 +183,27 @@ def test_fused_rmsnorm_prologue(M, K, gamma):
     torch.cuda.synchronize()
     y_ref, A = oracle.gemv(mm.Wq, mm.scales, mm.biases, oracle.rmsnorm(x, gw, eps=1e-5))
     assert_parity(y.cpu().numpy(), y_ref, A, what="rmsnorm prologue")
+
+
+@pytest.mark.parametrize("M", [1, 3])
+def test_largest_k_in_one_launch(M):
+    """K = 16384: x and two weight stages fill one CTA's shared memory at M = 1;
+    M = 3 runs as launches of 2 and 1 rows (each streaming the weights)."""
+    N, K = 37, 16384
+    m = q4synth.q4_matrix(555, N, K)
+    x = q4synth.activations(556, M, K)
+    y = run_gemv(m, x)
+    y_ref, A = oracle.gemv(m.Wq, m.scales, m.biases, x)
+    assert_parity(y, y_ref, A, what=f"K={K} M={M}")
+
+
+def test_k_beyond_shared_memory_is_refused():
+    N, K = 8, 32768
+    Wq = torch.zeros(N, K // 8, dtype=torch.int32, device="cuda")
+    s = torch.zeros(N, K // 64, dtype=torch.float16, device="cuda")
+    x = torch.zeros(1, K, dtype=torch.float16, device="cuda")
+    y = torch.zeros(1, N, device="cuda")
+    with pytest.raises(q4.Q4Error) as ei:
+        q4.q4_gemv(Wq, s, s, x, y, 1, N, K)
+    assert ei.value.name == "Q4_ERR_UNSUPPORTED"
+    assert q4.q4_device_status() == 0

@@ -74,6 +74,52 @@ def test_glu_small_every_element():
     check_glu(W, X, eids, H, ffn, what="glu")
 
 
+def test_one_expert_one_row():
+    N, K = 128, 64
+    W = q4synth.q4_matrix(340, N, K, experts=1)
+    X = q4synth.activations(341, 1, K)
+    Y, eids = run_gemm(W, X, [1], N, K, q4.Q4_GEMV_PLAIN, q4.Q4_F32)
+    check_plain(W, X, eids, Y, what="E=1 R=1")
+
+
+def test_256_experts_mostly_empty():
+    counts = [0] * 256
+    for e, c in [(0, 2), (77, 1), (128, 19), (255, 4)]:
+        counts[e] = c
+    N, K = 128, 128
+    W = q4synth.q4_matrix(350, N, K, experts=256)
+    X = q4synth.activations(351, sum(counts), K)
+    Y, eids = run_gemm(W, X, counts, N, K, q4.Q4_GEMV_PLAIN, q4.Q4_F16)
+    check_plain(W, X, eids, Y, fp16_out=True, what="E=256")
+
+
+@pytest.mark.parametrize("mode,K", [(q4.Q4_GEMV_GLU, 2752), (q4.Q4_GEMV_PLAIN, 3712)])
+def test_largest_k(mode, K):
+    """The largest K whose tiles fit in 227 KB of shared memory per block."""
+    n_out, counts = 128, [3, 130]
+    rows = 2 * n_out if mode == q4.Q4_GEMV_GLU else n_out
+    W = q4synth.q4_matrix(360 + K, rows, K, experts=len(counts))
+    X = q4synth.activations(361 + K, sum(counts), K)
+    Y, eids = run_gemm(W, X, counts, n_out, K, mode, q4.Q4_F16)
+    if mode == q4.Q4_GEMV_GLU:
+        check_glu(W, X, eids, Y, n_out, what=f"GLU K={K}")
+    else:
+        check_plain(W, X, eids, Y, fp16_out=True, what=f"plain K={K}")
+
+
+def test_k_beyond_shared_memory_is_refused():
+    E, N, K, R = 1, 128, 2816, 1
+    Wq = torch.zeros(E, 2 * N, K // 8, dtype=torch.int32, device="cuda")
+    s = torch.zeros(E, 2 * N, K // 64, dtype=torch.float16, device="cuda")
+    X = torch.zeros(R, K, dtype=torch.float16, device="cuda")
+    ids = torch.zeros(R, dtype=torch.int32, device="cuda")
+    off = torch.tensor([0, R], dtype=torch.int32, device="cuda")
+    Y = torch.zeros(R, N, dtype=torch.float16, device="cuda")
+    with pytest.raises(q4.Q4Error) as ei:
+        q4.q4_moe_gemm(Wq, s, s, X, ids, off, Y, E, N, K, R, q4.Q4_GEMV_GLU, q4.Q4_F16)
+    assert ei.value.name == "Q4_ERR_UNSUPPORTED"
+
+
 def test_general_scales_and_biases():
     g = np.random.default_rng(320)
     E, N, K = 3, 128, 128
