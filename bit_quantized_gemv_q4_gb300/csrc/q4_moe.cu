@@ -153,6 +153,56 @@ __global__ void gather_kernel(const uint16_t* __restrict__ X, int K, const int32
     }
 }
 
+// 8 consecutive outputs per thread with 16-byte loads and stores (N % 8 == 0,
+// Y and out 16-byte aligned); per element the same fp32 FMAs in the same
+// rank order as combine_kernel, so the results are identical.
+template <bool YF16, bool OF16>
+__global__ void combine8_kernel(const void* __restrict__ Y, int N, const int32_t* __restrict__ pos,
+                                const float* __restrict__ w, int T, int topk, void* __restrict__ out) {
+    const int nv = N / 8;
+    const size_t total = (size_t)T * nv;
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < total; i += (size_t)gridDim.x * blockDim.x) {
+        const int t = (int)(i / nv), c = (int)(i % nv);
+        float acc[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+        for (int k = 0; k < topk; ++k) {
+            const size_t r = (size_t)pos[(size_t)t * topk + k];
+            const float wk = w[(size_t)t * topk + k];
+            float y[8];
+            if (YF16) {
+                const uint4 v = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(Y) + r * N)[c];
+                const uint32_t u[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                for (int h = 0; h < 4; ++h) {
+                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&u[h]));
+                    y[2 * h] = f.x;
+                    y[2 * h + 1] = f.y;
+                }
+            } else {
+                const float4* src = reinterpret_cast<const float4*>(static_cast<const float*>(Y) + r * N) + 2 * c;
+                const float4 a = src[0], b = src[1];
+                y[0] = a.x; y[1] = a.y; y[2] = a.z; y[3] = a.w;
+                y[4] = b.x; y[5] = b.y; y[6] = b.z; y[7] = b.w;
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) acc[e] = fmaf(wk, y[e], acc[e]);
+        }
+        if (OF16) {
+            uint32_t u[4];
+#pragma unroll
+            for (int h = 0; h < 4; ++h)
+                u[h] = (uint32_t)__half_as_ushort(__float2half_rn(acc[2 * h])) |
+                       ((uint32_t)__half_as_ushort(__float2half_rn(acc[2 * h + 1])) << 16);
+            reinterpret_cast<uint4*>(out)[i] = make_uint4(u[0], u[1], u[2], u[3]);
+        } else {
+            float4* dst = reinterpret_cast<float4*>(out) + 2 * i;
+            dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+        }
+    }
+}
+
 template <bool YF16, bool OF16>
 __global__ void combine_kernel(const void* __restrict__ Y, int N, const int32_t* __restrict__ pos,
                                const float* __restrict__ w, int T, int topk, void* __restrict__ out) {
@@ -247,9 +297,24 @@ q4_status q4_moe_combine(const void* Y, q4_dtype y_dtype, int N, const int32_t* 
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (N % 8 == 0 && aligned16(Y) && aligned16(out)) {
+        const size_t total8 = (size_t)T * (N / 8);
+        const int g8 = (int)((total8 + 255) / 256 < (size_t)dev->sms * 8 ? (total8 + 255) / 256 : (size_t)dev->sms * 8);
+        if (y_dtype == Q4_F16 && out_dtype == Q4_F16)
+            q4m::combine8_kernel<true, true><<<g8, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+        else if (y_dtype == Q4_F16)
+            q4m::combine8_kernel<true, false><<<g8, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+        else if (out_dtype == Q4_F16)
+            q4m::combine8_kernel<false, true><<<g8, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+        else
+            q4m::combine8_kernel<false, false><<<g8, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
+        const cudaError_t e8 = cudaGetLastError();
+        if (e8 != cudaSuccess) return cuda_fail(e8, "q4_moe_combine launch");
+        return Q4_OK;
+    }
     const size_t total = (size_t)T * N;
     const int grid = (int)((total + 255) / 256 < (size_t)dev->sms * 8 ? (total + 255) / 256 : (size_t)dev->sms * 8);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     if (y_dtype == Q4_F16 && out_dtype == Q4_F16)
         q4m::combine_kernel<true, true><<<grid, 256, 0, s>>>(Y, N, pos, topk_weights, T, topk, out);
     else if (y_dtype == Q4_F16)

@@ -80,3 +80,31 @@ def test_combine(ydt, odt):
     ref, mag = oracle.moe_combine(Y.astype(np.float64), r["pos"], w.astype(np.float64))
     # fp32 accumulation of 8 terms: relative 1e-6 of the magnitudes, plus the fp16 store
     assert_parity(out.float().cpu().numpy(), ref, mag, fp16_out=bool(odt), what="combine")
+
+
+@pytest.mark.parametrize("ydt,odt", [(1, 1), (0, 0)])
+def test_combine_vector_and_scalar_paths_agree(ydt, odt):
+    """N % 8 == 0 with aligned buffers takes the 16-byte path; a misaligned
+    output takes the per-element path: same arithmetic, identical bits.  An N
+    that is not a multiple of 8 is checked against the oracle."""
+    T, N, topk = 40, 1024, 8
+    r = oracle.moe_route(q4synth.router_logits(17, T, 64), topk)
+    Y = np.random.default_rng(18).standard_normal((T * topk, N))
+    Y = Y.astype(np.float16) if ydt else Y.astype(np.float32)
+    w = torch_dev(r["weights"].astype(np.float32))
+    pos = torch_dev(r["pos"])
+    dt = torch.float16 if odt else torch.float32
+    a = torch.empty(T, N, dtype=dt, device="cuda")
+    big = torch.empty(T * N + 1, dtype=dt, device="cuda")
+    b = big[1:]                                   # 2 or 4 bytes off a 16-byte boundary
+    q4.q4_moe_combine(torch_dev(Y), ydt, N, pos, w, T, topk, a, odt)
+    q4.q4_moe_combine(torch_dev(Y), ydt, N, pos, w, T, topk, b, odt)
+    torch.cuda.synchronize()
+    assert torch.equal(a.flatten(), b)
+    N2 = 100
+    Y2 = np.random.default_rng(19).standard_normal((T * topk, N2)).astype(Y.dtype)
+    c = torch.empty(T, N2, dtype=dt, device="cuda")
+    q4.q4_moe_combine(torch_dev(Y2), ydt, N2, pos, w, T, topk, c, odt)
+    torch.cuda.synchronize()
+    ref, mag = oracle.moe_combine(Y2.astype(np.float64), r["pos"], r["weights"].astype(np.float64))
+    assert_parity(c.float().cpu().numpy(), ref, mag, fp16_out=bool(odt), what="combine N=100")
