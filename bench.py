@@ -234,31 +234,34 @@ def moe_prefill(device, iters: int = 20, warmup: int = 5, token_counts=(128, 512
         Hh = torch.empty(R, F, dtype=torch.float16, device=device)
         Y = torch.empty(R, H, dtype=torch.float16, device=device)
         o = torch.empty(T, H, dtype=torch.float16, device=device)
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-
-        def layer(record):
-            if record:
+        def layer(ev=None):
+            if ev:
                 ev[0].record(stream)
             q4.q4_moe_route(logits, T, E, k, ids, w, off, tok, eid, pos, ws, nws, stream)
             q4.q4_moe_gather(X, T, H, tok, R, Xs, stream)
-            if record:
+            if ev:
                 ev[1].record(stream)
             q4.q4_moe_gemm(*dgu, Xs, eid, off, Hh, E, F, H, R, q4.Q4_GEMV_GLU, q4.Q4_F16, stream)
-            if record:
+            if ev:
                 ev[2].record(stream)
             q4.q4_moe_gemm(*ddn, Hh, eid, off, Y, E, H, F, R, q4.Q4_GEMV_PLAIN, q4.Q4_F16, stream)
-            if record:
+            if ev:
                 ev[3].record(stream)
             q4.q4_moe_combine(Y, q4.Q4_F16, H, pos, w, T, k, o, q4.Q4_F16, stream)
-            if record:
+            if ev:
                 ev[4].record(stream)
 
         for _ in range(warmup):
-            layer(False)
+            layer()
+        torch.cuda.synchronize(device)
+        # Enqueue every timed layer, synchronise once: the host runs ahead of
+        # the GPU, so the events measure device time, not launch gaps.
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(iters)]
+        for i in range(iters):
+            layer(evs[i])
+        torch.cuda.synchronize(device)
         tot = {"route_gather": 0.0, "gate_up": 0.0, "down": 0.0, "combine": 0.0}
-        for _ in range(iters):
-            layer(True)
-            torch.cuda.synchronize(device)
+        for ev in evs:
             tot["route_gather"] += ev[0].elapsed_time(ev[1])
             tot["gate_up"] += ev[1].elapsed_time(ev[2])
             tot["down"] += ev[2].elapsed_time(ev[3])

@@ -90,53 +90,71 @@ __global__ void route_count_kernel(const int32_t* __restrict__ ids, int T, int E
 }
 
 // Exclusive scan of count[E*B] in (expert, block) order, in place; also
-// offsets[e] = start of expert e, offsets[E] = total.  One CTA.
+// offsets[e] = start of expert e, offsets[E] = total.  One CTA of 1024
+// threads: each sums its contiguous range, the range sums are scanned with
+// warp shuffles (within each warp, then across the 32 warp totals), and each
+// thread rewrites its range with the running prefix.
 __global__ void route_scan_kernel(int32_t* __restrict__ count, int E, int B, int32_t* __restrict__ offsets) {
-    __shared__ int32_t part[1024];
+    __shared__ int32_t wsum[32];
     const int n = E * B;
     const int per = (n + blockDim.x - 1) / blockDim.x;
     const int lo = threadIdx.x * per, hi = min(n, lo + per);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int32_t s = 0;
     for (int i = lo; i < hi; ++i) s += count[i];
-    part[threadIdx.x] = s;
-    __syncthreads();
-    for (int o = 1; o < (int)blockDim.x; o <<= 1) {
-        const int32_t v = threadIdx.x >= (unsigned)o ? part[threadIdx.x - o] : 0;
-        __syncthreads();
-        part[threadIdx.x] += v;
-        __syncthreads();
+    int32_t v = s;  // inclusive scan within the warp
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int32_t u = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += u;
     }
-    int32_t run = part[threadIdx.x] - s;  // exclusive prefix of this thread's range
+    if (lane == 31) wsum[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        int32_t w = lane < (int)(blockDim.x >> 5) ? wsum[lane] : 0;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int32_t u = __shfl_up_sync(0xffffffffu, w, o);
+            if (lane >= o) w += u;
+        }
+        wsum[lane] = w;  // inclusive totals of warps 0..lane
+    }
+    __syncthreads();
+    const int32_t before = (warp ? wsum[warp - 1] : 0) + v - s;  // exclusive prefix of this thread's range
+    int32_t run = before;
     for (int i = lo; i < hi; ++i) {
         const int32_t c = count[i];
         count[i] = run;
         if (i % B == 0) offsets[i / B] = run;
         run += c;
     }
-    if (threadIdx.x == blockDim.x - 1) offsets[E] = part[threadIdx.x];
+    if (threadIdx.x == blockDim.x - 1) offsets[E] = before + s;
 }
 
 // Row of each (token, rank): base[e][b] + number of earlier tokens of the
-// block that hold expert e.  One warp per block walks its tokens in order;
-// lane k < topk takes the token's k-th expert and bumps that expert's
-// counter (a token holds an expert at most once, so the lanes' counters are
-// distinct and the walk needs no atomics).
+// block that hold expert e.  One warp per block: the block's expert ids and
+// each expert's base row are staged in shared memory, then the warp walks the
+// tokens in order; lane k < topk takes the token's k-th expert and advances
+// that expert's next row (a token holds an expert at most once, so the lanes'
+// entries are distinct and the walk needs no atomics).
 __global__ void route_scatter_kernel(const int32_t* __restrict__ ids, int T, int E, int topk, int B,
                                      const int32_t* __restrict__ base, int32_t* __restrict__ token_of,
                                      int32_t* __restrict__ expert_of, int32_t* __restrict__ pos) {
-    __shared__ int32_t cnt[kMaxExperts];
+    __shared__ int32_t next_row[kMaxExperts];
+    __shared__ int32_t ids_s[kBlockTokens * kMaxTopk];
     const int b = blockIdx.x, lane = threadIdx.x;
-    for (int e = lane; e < E; e += 32) cnt[e] = 0;
+    const int t0 = b * kBlockTokens, nt = min(T - t0, kBlockTokens);
+    for (int e = lane; e < E; e += 32) next_row[e] = base[(size_t)e * B + b];
+    for (int i = lane; i < nt * topk; i += 32) ids_s[i] = ids[(size_t)t0 * topk + i];
     __syncwarp();
-    const int t_end = min(T, (b + 1) * kBlockTokens);
-    for (int t = b * kBlockTokens; t < t_end; ++t) {
+    for (int j = 0; j < nt; ++j) {
         if (lane < topk) {
-            const int e = ids[(size_t)t * topk + lane];
-            const int r = base[(size_t)e * B + b] + cnt[e];
-            cnt[e] += 1;
-            token_of[r] = t;
+            const int e = ids_s[j * topk + lane];
+            const int r = next_row[e];
+            next_row[e] = r + 1;
+            token_of[r] = t0 + j;
             expert_of[r] = e;
-            pos[(size_t)t * topk + lane] = r;
+            pos[(size_t)(t0 + j) * topk + lane] = r;
         }
         __syncwarp();
     }

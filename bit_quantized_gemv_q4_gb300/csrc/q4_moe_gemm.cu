@@ -482,15 +482,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Device-side check that expert_ids agrees with offsets (and that offsets
-// are a monotone partition of 0..R-1).
+// are a monotone partition of 0..R-1); every check is one thread's work.
 __global__ void check_routing_kernel(const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ offsets,
                                      int E, int R, int* err) {
-    if (blockIdx.x == 0 && threadIdx.x == 0) {
-        bool ok = offsets[0] == 0 && offsets[E] == R;
-        for (int e = 0; e < E && ok; ++e) ok = offsets[e] <= offsets[e + 1];
-        if (!ok) atomicOr(err, q4d::kErrDeviceCheck);
-    }
-    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < R; r += gridDim.x * blockDim.x) {
+    const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthr = gridDim.x * blockDim.x;
+    if (tid == 0 && (offsets[0] != 0 || offsets[E] != R)) atomicOr(err, q4d::kErrDeviceCheck);
+    for (int e = tid; e < E; e += nthr)
+        if (offsets[e] > offsets[e + 1]) atomicOr(err, q4d::kErrDeviceCheck);
+    for (int r = tid; r < R; r += nthr) {
         const int e = expert_ids[r];
         if (e < 0 || e >= E || r < offsets[e] || r >= offsets[e + 1]) atomicOr(err, q4d::kErrDeviceCheck);
     }
