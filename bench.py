@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -47,10 +48,16 @@ def peaks():
 
 
 def kernel_source_hash() -> str:
+    """Hash of the GEMV kernel's code (q4_gemv.cu + q4_device.cuh) with
+    comments and whitespace removed, so a comment edit keeps the recorded
+    ncu traffic valid while any code change invalidates it."""
     h = hashlib.sha256()
     for nm in ("q4_gemv.cu", "q4_device.cuh"):
-        with open(os.path.join(ROOT, "bit_quantized_gemv_q4_gb300", "csrc", nm), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "bit_quantized_gemv_q4_gb300", "csrc", nm), encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
+        src = re.sub(r"//[^\n]*", " ", src)                   # line comments
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 

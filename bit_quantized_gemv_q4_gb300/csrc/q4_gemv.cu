@@ -25,13 +25,17 @@
 //   are staged before the dependency wait, the sum of squares is reduced as x
 //   streams in, and the scalar 1/rms multiplies the dot products), laid out so
 //   each lane's operands are conflict-free 16-byte shared loads,
-//   and reused across the rows a warp handles together.  Each warp reduces its
-//   rows with xor shuffles (fixed order, so results are bit-reproducible).
+//   and reused across the rows a warp handles together.  A warp reduces all
+//   the totals of its row batch at once with a transposing shuffle butterfly
+//   (fixed order, so results are bit-reproducible); the lane that stores an
+//   output fetches its residual before the dot products.
 // * Under programmatic dependent launch the weight copies start before the
 //   wait on the previous kernel (weights never depend on it); only the x load
-//   and the epilogue wait.
-// * Every mbarrier wait is bounded; on expiry the kernel latches an error bit
-//   and leaves.
+//   and the epilogue wait.  Inside a decode step x may instead arrive as
+//   tagged words that are polled (no wait for the previous grid), and the
+//   whole step may run as one persistent cooperative launch (end of file).
+// * Every wait is bounded; on expiry the kernel latches an error bit and
+//   leaves.
 #include <cuda_fp16.h>
 #include <stdio.h>
 
