@@ -87,6 +87,12 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
         L.q4o_gemv_f64.restype = ctypes.c_int
         L.q4o_gemv_f64.argtypes = L.q4o_gemv.argtypes
         L.q4o_max_threads.restype = ctypes.c_int
+        L.q8o_code.restype = ctypes.c_int
+        L.q8o_code.argtypes = [ctypes.c_void_p, ctypes.c_int64]
+        for fn in (L.q8o_gemv, L.q8o_gemv_f64):
+            fn.restype = ctypes.c_int
+            fn.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         _libs[mutant] = L
     return _libs[mutant]
 
@@ -138,6 +144,47 @@ def gemv(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
     if rc != 0:
         raise ValueError("oracle rejected arguments")
     return y, A
+
+
+def gemv8(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
+    """gemv() for 8-bit codes: Wq uint32 [N, K/4], code k in byte k % 4 of
+    word k // 4 (lowest byte first), q in 0..255, w = s * q + b per 64-group."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.float16)
+    biases = np.ascontiguousarray(biases, dtype=np.float16)
+    x = np.atleast_2d(x)
+    f64 = x.dtype == np.float64
+    x = np.ascontiguousarray(x, dtype=np.float64 if f64 else np.float16)
+    N, W = Wq.shape
+    K = W * 4
+    M = x.shape[0]
+    if x.shape[1] != K or scales.shape != (N, K // 64) or biases.shape != (N, K // 64):
+        raise ValueError("shape mismatch")
+    if rows is None:
+        R, rp = N, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        if rows.size and (rows.min() < 0 or rows.max() >= N):
+            raise ValueError("row out of range")
+        R, rp = rows.size, _p(rows)
+    y = np.empty((M, R), np.float64)
+    A = np.empty((M, R), np.float64)
+    if R == 0:
+        return y, A
+    L = _lib(mutant)
+    fn = L.q8o_gemv_f64 if f64 else L.q8o_gemv
+    xp = _p(x) if f64 else _p(x.view(np.uint16))
+    rc = fn(_p(Wq), _p(scales.view(np.uint16)), _p(biases.view(np.uint16)), xp, M, N, K, rp, R, _p(y), _p(A),
+            nthreads)
+    if rc != 0:
+        raise ValueError("oracle rejected arguments")
+    return y, A
+
+
+def code8(Wq_row, k: int, mutant: int = 0) -> int:
+    """The 8-bit code k of one packed row (as the oracle reads it)."""
+    row = np.ascontiguousarray(Wq_row, dtype=np.uint32)
+    return _lib(mutant).q8o_code(_p(row), k)
 
 
 def fp16(v) -> np.ndarray:

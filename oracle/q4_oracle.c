@@ -149,6 +149,81 @@ int q4o_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
     return rc;
 }
 
+/*
+ * The same product for 8-bit codes (the pages' 8-bit format, BaseRT §3.3 and
+ * §4.1: "Q4 and Q8 evaluated"; their bit layout is not printed, so the one
+ * the library fixes is used): Wq uint32 [N][K/4]; code k of row n is bits
+ * 8*(k%4) .. 8*(k%4)+7 of word k/4 (lowest byte first), q in 0..255; one fp16
+ * scale and bias per group of 64; w = s * q + b; fp64 accumulation in order
+ * k = 0 .. K-1, and A = sum_k |w x| as above.
+ */
+int q8o_code(const uint32_t *row, int64_t k)
+{
+#if Q4O_MUTANT == 6 /* mistake: highest byte first */
+    return (int)((row[k / 4] >> (8 * (3 - k % 4))) & 0xFFu);
+#elif Q4O_MUTANT == 7 /* mistake: only the low nibble of each byte */
+    return (int)((row[k / 4] >> (8 * (k % 4))) & 0x0Fu);
+#else
+    return (int)((row[k / 4] >> (8 * (k % 4))) & 0xFFu);
+#endif
+}
+
+int q8o_gemv_f64(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                 const double *xd, int64_t M, int64_t N, int64_t K,
+                 const int64_t *rows, int64_t nrows, double *y, double *A, int nthreads)
+{
+    if (!Wq || !scales || !biases || !xd || !y || M < 1 || N < 0 || K < 64 || K % 64)
+        return -1;
+    if (!rows)
+        nrows = N;
+    int64_t words = K / 4, groups = K / 64;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        const uint32_t *row = Wq + n * words;
+        const uint16_t *s_row = scales + n * groups;
+        const uint16_t *b_row = biases + n * groups;
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+#if Q4O_MUTANT == 8 /* mistake: group of 32 instead of 64 (clamped to stay in the row) */
+                int64_t g = k / 32 < groups ? k / 32 : groups - 1;
+#else
+                int64_t g = k / 64;
+#endif
+                double w = q4o_half_to_double(s_row[g]) * (double)q8o_code(row, k) + q4o_half_to_double(b_row[g]);
+                double t = w * xd[m * K + k];
+                acc += t;
+                mag += fabs(t);
+            }
+            y[m * nrows + i] = acc;
+            if (A)
+                A[m * nrows + i] = mag;
+        }
+    }
+    return 0;
+}
+
+int q8o_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+             const uint16_t *x, int64_t M, int64_t N, int64_t K,
+             const int64_t *rows, int64_t nrows, double *y, double *A, int nthreads)
+{
+    if (!x || M < 1 || K < 64)
+        return -1;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K));
+    if (!xd)
+        return -1;
+    for (int64_t i = 0; i < M * K; ++i)
+        xd[i] = q4o_half_to_double(x[i]);
+    int rc = q8o_gemv_f64(Wq, scales, biases, xd, M, N, K, rows, nrows, y, A, nthreads);
+    free(xd);
+    return rc;
+}
+
 /* Number of OpenMP threads this library would use by default (1 without OpenMP). */
 int q4o_max_threads(void)
 {

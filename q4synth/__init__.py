@@ -26,6 +26,10 @@ Recipe (all draws with numpy's PCG64 ``default_rng(seed)``):
 * ``bias  = -8 * scale`` from the fp16 scale (exact in fp16).
 * activations ``x ~ N(0, 1)`` rounded to fp16; router logits likewise.
 
+The 8-bit variant (``q8_matrix``) stores four codes per word, code ``k`` in
+byte ``k % 4`` of word ``k // 4`` (lowest byte first), ``q`` in ``0..255``;
+``scale = fp16(|N(0, 0.02)| / 127.5)``, ``bias = -128 * scale``.
+
 Per-tensor seeds are ``BASE_SEED + index`` so every tensor of a model can be
 regenerated alone (the oracle needs single matrices at full size).
 """
@@ -138,6 +142,41 @@ def decode_weights(shape: DecodeShape, base_seed: int = BASE_SEED):
         layers.append(d)
     lm_head = q4_matrix(base_seed + 16 * shape.n_layers, shape.vocab, shape.hidden)
     return layers, lm_head
+
+
+@dataclasses.dataclass
+class Q8Matrix:
+    """One matrix W[N, K] with 8-bit codes in storage format: ``Wq`` uint32
+    ``[N, K/4]`` (code k in byte k % 4 of word k // 4, lowest byte first),
+    fp16 ``scales`` and ``biases`` ``[N, K/64]``; ``w = scale * q + bias``."""
+    Wq: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+
+    @property
+    def N(self) -> int:
+        return self.Wq.shape[-2]
+
+    @property
+    def K(self) -> int:
+        return self.Wq.shape[-1] * 4
+
+    def nbytes(self) -> int:
+        return self.Wq.nbytes + self.scales.nbytes + self.biases.nbytes
+
+
+def q8_matrix(seed: int, N: int, K: int) -> Q8Matrix:
+    """Random 8-bit matrix: codes uniform in 0..255 (four independent uniform
+    bytes are a uniform word), scale = fp16(|N(0, 0.02)| / 127.5), bias =
+    -128 * scale (exact in fp16), so w spans about the same range as the
+    4-bit matrices."""
+    if K % GROUP:
+        raise ValueError(f"K={K} is not a multiple of {GROUP}")
+    g = rng(seed)
+    Wq = g.integers(0, 2**32, size=(N, K // 4), dtype=np.uint32)
+    s = (np.abs(g.standard_normal((N, K // GROUP))) * 0.02 / 127.5).astype(np.float16)
+    b = (-128.0 * s.astype(np.float64)).astype(np.float16)
+    return Q8Matrix(Wq, s, b)
 
 
 @dataclasses.dataclass(frozen=True)
