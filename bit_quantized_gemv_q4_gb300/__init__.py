@@ -13,7 +13,7 @@ import ctypes
 import os
 
 __all__ = [
-    "Q4Error", "lib", "q4_selftest_expired_wait", "q4_gemv", "q4_gemv_ex", "Segment", "q4_device_status",
+    "Q4Error", "lib", "q4_selftest_expired_wait", "q4_gemv", "q4_gemv8", "q4_gemv_ex", "Segment", "q4_device_status",
     "LayerTable", "q4_decode_step", "q4_decode_workspace_bytes", "q4_decode_buffers",
     "q4_layer_table_release", "q4_moe_route", "q4_moe_route_workspace_bytes",
     "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine",
@@ -35,7 +35,7 @@ STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q
 
 # Every symbol include/q4.h declares.
 EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status",
-           "q4_selftest_expired_wait", "q4_gemv",
+           "q4_selftest_expired_wait", "q4_gemv", "q4_gemv8",
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
            "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
            "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine"]
@@ -109,6 +109,8 @@ def lib() -> ctypes.CDLL:
         L.q4_selftest_expired_wait.argtypes = [vp]
         L.q4_gemv.restype = st
         L.q4_gemv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
+        L.q4_gemv8.restype = st
+        L.q4_gemv8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
         L.q4_gemv_ex.restype = st
         L.q4_gemv_ex.argtypes = [ctypes.POINTER(q4_gemv_desc), vp]
         L.q4_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -173,6 +175,12 @@ def q4_selftest_expired_wait(stream=None):
 def q4_gemv(Wq, scales, biases, x, y, M: int, N: int, K: int, stream=None):
     _check(lib().q4_gemv(_ptr(Wq), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K, _stream(stream)),
            "q4_gemv")
+
+
+def q4_gemv8(Wq, scales, biases, x, y, M: int, N: int, K: int, stream=None):
+    """q4_gemv for 8-bit codes: Wq uint32 [N, K/4], lowest byte first."""
+    _check(lib().q4_gemv8(_ptr(Wq), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K, _stream(stream)),
+           "q4_gemv8")
 
 
 class Segment:

@@ -132,6 +132,27 @@ q4_status q4_gemv(const uint32_t* Wq, const uint16_t* scales, const uint16_t* bi
     return launch_gemv(d, reinterpret_cast<cudaStream_t>(stream), false, false);
 }
 
+q4_status q4_gemv8(const uint32_t* Wq, const uint16_t* scales, const uint16_t* biases, const uint16_t* x,
+                   float* y, int M, int N, int K, q4_stream_t stream) {
+    clear_error();
+    q4_gemv_desc d = {};
+    d.M = M;
+    d.K = K;
+    d.x = x;
+    d.ldx = K;
+    d.n_segments = 1;
+    d.seg[0].Wq = Wq;
+    d.seg[0].scales = scales;
+    d.seg[0].biases = biases;
+    d.seg[0].N = N;
+    d.seg[0].y = y;
+    d.out_dtype = Q4_F32;
+    d.mode = Q4_GEMV_PLAIN;
+    q4_status st = validate_gemv(d);
+    if (st != Q4_OK) return st;
+    return launch_gemv(d, reinterpret_cast<cudaStream_t>(stream), false, false, nullptr, 8);
+}
+
 q4_status q4_gemv_ex(const q4_gemv_desc* desc, q4_stream_t stream) {
     clear_error();
     if (!desc) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");

@@ -76,6 +76,7 @@ struct alignas(16) Params {
     uint32_t* done_ctr;
     int stage, n_stages, x_stage, res_stage, last;
     int tile_base;  // persistent step: tiles of all earlier stages (round-robin origin)
+    int bits;       // code width: 4 (8 codes per word) or 8 (4 codes per word)
     int* err;
 };
 
@@ -146,12 +147,13 @@ __device__ __forceinline__ void find_tile(const Params& p, int t, int& si, int& 
 __device__ __forceinline__ void issue_rows(const Params& p, const Seg& sg, int n0, int nrows, int row_off,
                                            uint8_t* stage, uint32_t full_bar, int lane, uint64_t pol) {
     const int K = p.K, G = K / 64, R = p.rows_per_tile;
-    const uint32_t wq_bytes = (uint32_t)nrows * (uint32_t)(K / 2);
+    const int crb = K * p.bits / 8;  // code bytes per row
+    const uint32_t wq_bytes = (uint32_t)nrows * (uint32_t)crb;
     const uint32_t sb_bytes = (uint32_t)nrows * (uint32_t)G * 2u;
-    uint8_t* wq_dst = stage + (size_t)row_off * (K / 2);
-    uint8_t* s_dst = stage + (size_t)R * (K / 2) + (size_t)row_off * G * 2;
+    uint8_t* wq_dst = stage + (size_t)row_off * crb;
+    uint8_t* s_dst = stage + (size_t)R * crb + (size_t)row_off * G * 2;
     uint8_t* b_dst = s_dst + (size_t)R * G * 2;
-    const uint32_t* wq_src = sg.Wq + (size_t)n0 * (K / 8);
+    const uint32_t* wq_src = sg.Wq + (size_t)n0 * (crb / 4);
     const uint16_t* s_src = sg.s + (size_t)n0 * G;
     const uint16_t* b_src = sg.b + (size_t)n0 * G;
     if (lane == 0) q4d::bulk_g2s_evict_first(q4d::smem_addr(wq_dst), wq_src, wq_bytes, full_bar, pol);
@@ -174,7 +176,7 @@ __device__ __forceinline__ void issue_rows(const Params& p, const Seg& sg, int n
 
 // Bytes the bulk copies of one segment's rows bring in (the expect-tx count).
 __device__ __forceinline__ uint32_t bulk_bytes(const Params& p, int nrows) {
-    const uint32_t wq_b = (uint32_t)nrows * (uint32_t)(p.K / 2);
+    const uint32_t wq_b = (uint32_t)nrows * (uint32_t)(p.K * p.bits / 8);
     const uint32_t sb_b = (uint32_t)nrows * (uint32_t)(p.K / 64) * 2u;
     return wq_b + (((sb_b & 15u) == 0) ? 2 * sb_b : 0);
 }
@@ -202,9 +204,45 @@ __device__ __forceinline__ void word_mac(uint32_t q, uint16_t sh, float c1024, f
     }
 }
 
+// The same for 8-bit codes: two words a, b hold the 8 codes of one octet
+// (codes 0-3 in a, 4-7 in b, lowest byte first).  Masking every other byte
+// and OR-ing it into the mantissa of 1024.0 gives 1024+q exactly (q <= 255);
+// the pairs are (q0,q2), (q1,q3), (q4,q6), (q5,q7) and x is staged in that
+// pairing for 8-bit matrices (see load_x).
+template <int M>
+__device__ __forceinline__ void word_mac8(uint32_t a, uint32_t b, uint16_t sh, float c1024, const float4* xa,
+                                          const float4* xb, float2* acc) {
+    const uint32_t v0 = q4d::and_or(a, 0x00FF00FFu, 0x64006400u);       // 1024+q0, 1024+q2
+    const uint32_t v1 = q4d::and_or(a >> 8, 0x00FF00FFu, 0x64006400u);  // 1024+q1, 1024+q3
+    const uint32_t v2 = q4d::and_or(b, 0x00FF00FFu, 0x64006400u);       // 1024+q4, 1024+q6
+    const uint32_t v3 = q4d::and_or(b >> 8, 0x00FF00FFu, 0x64006400u);  // 1024+q5, 1024+q7
+    const float2 d0 = q4d::fma_h2_s_f32(v0, sh, c1024);
+    const float2 d1 = q4d::fma_h2_s_f32(v1, sh, c1024);
+    const float2 d2 = q4d::fma_h2_s_f32(v2, sh, c1024);
+    const float2 d3 = q4d::fma_h2_s_f32(v3, sh, c1024);
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        acc[m] = __ffma2_rn(d0, make_float2(xa[m].x, xa[m].y), acc[m]);
+        acc[m] = __ffma2_rn(d1, make_float2(xa[m].z, xa[m].w), acc[m]);
+        acc[m] = __ffma2_rn(d2, make_float2(xb[m].x, xb[m].y), acc[m]);
+        acc[m] = __ffma2_rn(d3, make_float2(xb[m].z, xb[m].w), acc[m]);
+    }
+}
+
 template <int LW>
 __device__ __forceinline__ void load_words(const uint32_t* src, uint32_t* w) {
-    if constexpr (LW == 4) {
+    if constexpr (LW == 8) {
+        const uint4 v = *reinterpret_cast<const uint4*>(src);
+        const uint4 u = *reinterpret_cast<const uint4*>(src + 4);
+        w[0] = v.x;
+        w[1] = v.y;
+        w[2] = v.z;
+        w[3] = v.w;
+        w[4] = u.x;
+        w[5] = u.y;
+        w[6] = u.z;
+        w[7] = u.w;
+    } else if constexpr (LW == 4) {
         const uint4 v = *reinterpret_cast<const uint4*>(src);
         w[0] = v.x;
         w[1] = v.y;
@@ -220,8 +258,9 @@ __device__ __forceinline__ void load_words(const uint32_t* src, uint32_t* w) {
 }
 
 // Dot products of RB tile rows (shared-memory row indices `rows`) with all M
-// x vectors; every lane ends with all RB*M totals.
-template <int M, int RB>
+// x vectors; every lane ends with all RB*M totals.  A lane handles LW octets
+// (8 codes each: one 4-bit word or two 8-bit words) per chunk.
+template <int M, int RB, int BITS>
 __device__ __forceinline__ void dot_rows(const Params& p, const uint32_t* wq, const uint16_t* ss,
                                          const uint16_t* bs, const float4* xs, const int* rows, int lane,
                                          float (*out)[M]) {
@@ -245,8 +284,9 @@ __device__ __forceinline__ void dot_rows(const Params& p, const uint32_t* wq, co
             const int g = j0 >> 3;
 #pragma unroll
             for (int r = 0; r < RB; ++r) {
-                uint32_t w[LW];
-                load_words<LW>(wq + (size_t)rows[r] * W8 + j0, w);
+                constexpr int WPO = BITS / 4;  // words per octet
+                uint32_t w[LW * WPO];
+                load_words<LW * WPO>(wq + ((size_t)rows[r] * W8 + j0) * WPO, w);
                 const uint16_t sh = ss[rows[r] * G + g];
                 const uint16_t bh = bs[rows[r] * G + g];
                 const float sf = __half2float(__ushort_as_half(sh));
@@ -254,8 +294,13 @@ __device__ __forceinline__ void dot_rows(const Params& p, const uint32_t* wq, co
                 const float c1024 = fmaf(-1024.f, sf, bf);
                 const float c64 = fmaf(-64.f, sf, bf);
 #pragma unroll
-                for (int wi = 0; wi < LW; ++wi)
-                    word_mac<M>(w[wi], sh, c1024, c64, &xr[(wi * 2 + 0) * M], &xr[(wi * 2 + 1) * M], acc[r]);
+                for (int wi = 0; wi < LW; ++wi) {
+                    if constexpr (BITS == 4)
+                        word_mac<M>(w[wi], sh, c1024, c64, &xr[(wi * 2 + 0) * M], &xr[(wi * 2 + 1) * M], acc[r]);
+                    else
+                        word_mac8<M>(w[2 * wi], w[2 * wi + 1], sh, c1024, &xr[(wi * 2 + 0) * M],
+                                     &xr[(wi * 2 + 1) * M], acc[r]);
+                }
             }
         }
     }
@@ -327,7 +372,7 @@ __device__ __forceinline__ bool store_out(const Params& p, const Seg& sg, int m,
     return ok;
 }
 
-template <int M, int RB>
+template <int M, int RB, int BITS>
 __device__ __forceinline__ bool tile_batch(const Params& p, const uint32_t* wq, const uint16_t* ss,
                                            const uint16_t* bs, const float4* xs, const float* scale, int warp,
                                            int lane, int j_begin, int rpw, int si, int n0, int nrows,
@@ -373,7 +418,7 @@ __device__ __forceinline__ bool tile_batch(const Params& p, const uint32_t* wq, 
     }
 
     float out[RB][M];
-    dot_rows<M, RB>(p, wq, ss, bs, xs, rows, lane, out);
+    dot_rows<M, RB, BITS>(p, wq, ss, bs, xs, rows, lane, out);
     // Reduce all RB*M values at once.
     float v[VP];
 #pragma unroll
@@ -423,7 +468,20 @@ __device__ __forceinline__ float4* x_slot(float4* xs, int j, int m, int half) {
 // Consumers, before the dependency wait: the RMSNorm weights (a weight, not
 // an activation) are staged into the x slots so the post-wait pass only
 // multiplies.
-template <int M>
+// Shared-memory order of one octet's 8 values: the pairing the dequantised
+// pairs meet (4-bit: (0,4) (1,5) | (2,6) (3,7); 8-bit: (0,2) (1,3) | (4,6) (5,7)).
+template <int BITS>
+__device__ __forceinline__ void octet_halves(const float* f, float4& a, float4& b) {
+    if constexpr (BITS == 4) {
+        a = make_float4(f[0], f[4], f[1], f[5]);
+        b = make_float4(f[2], f[6], f[3], f[7]);
+    } else {
+        a = make_float4(f[0], f[2], f[1], f[3]);
+        b = make_float4(f[4], f[6], f[5], f[7]);
+    }
+}
+
+template <int M, int BITS>
 __device__ __forceinline__ void stage_norm_weight(const Params& p, float4* xs) {
     constexpr int kCT = kConsumerWarps * 32;
     const int W8 = p.K / 8;
@@ -432,8 +490,10 @@ __device__ __forceinline__ void stage_norm_weight(const Params& p, float4* xs) {
         load8_f32(p.norm_w + 8 * j, g);
 #pragma unroll
         for (int m = 0; m < M; ++m) {
-            *x_slot<M>(xs, j, m, 0) = make_float4(g[0], g[4], g[1], g[5]);
-            *x_slot<M>(xs, j, m, 1) = make_float4(g[2], g[6], g[3], g[7]);
+            float4 a, b;
+            octet_halves<BITS>(g, a, b);
+            *x_slot<M>(xs, j, m, 0) = a;
+            *x_slot<M>(xs, j, m, 1) = b;
         }
     }
 }
@@ -444,7 +504,7 @@ __device__ __forceinline__ void stage_norm_weight(const Params& p, float4* xs) {
 // warp xor tree; the warps' partials are added in index order by
 // norm_scales); the scalar 1/rms is applied to the dot products in the
 // epilogue, so x is read once.
-template <int M>
+template <int M, int BITS>
 __device__ __forceinline__ bool load_x(const Params& p, float4* xs, float* red, int warp, int lane, uint32_t xtag,
                                        const uint16_t* gamma_sm = nullptr) {
     constexpr int kCT = kConsumerWarps * 32;
@@ -475,12 +535,15 @@ __device__ __forceinline__ bool load_x(const Params& p, float4* xs, float* red, 
             for (int e = 0; e < 8; ++e) ss[m] = fmaf(f[e], f[e], ss[m]);
             float4* d0 = x_slot<M>(xs, j, m, 0);
             float4* d1 = x_slot<M>(xs, j, m, 1);
-            float4 a = make_float4(f[0], f[4], f[1], f[5]), b = make_float4(f[2], f[6], f[3], f[7]);
+            float4 a, b;
+            octet_halves<BITS>(f, a, b);
             if (gamma_sm) {
                 float g[8];
                 load8_f32(gamma_sm + 8 * j, g);
-                a = make_float4(a.x * g[0], a.y * g[4], a.z * g[1], a.w * g[5]);
-                b = make_float4(b.x * g[2], b.y * g[6], b.z * g[3], b.w * g[7]);
+                float4 ga, gb;
+                octet_halves<BITS>(g, ga, gb);
+                a = make_float4(a.x * ga.x, a.y * ga.y, a.z * ga.z, a.w * ga.w);
+                b = make_float4(b.x * gb.x, b.y * gb.y, b.z * gb.z, b.w * gb.w);
             } else if (gw) {
                 const float4 ga = *d0, gb = *d1;
                 a = make_float4(a.x * ga.x, a.y * ga.y, a.z * ga.z, a.w * ga.w);
@@ -518,7 +581,7 @@ __device__ __forceinline__ void norm_scales(const Params& p, const float* red, f
 
 // One consumer warp's share of tile t (its rows, all M vectors), read from the
 // shared-memory stage that holds the tile.  False if a residual wait expired.
-template <int M>
+template <int M, int BITS>
 __device__ __forceinline__ bool consume_tile(const Params& p, const uint8_t* stage, const float4* xs,
                                              const float* scale, int warp, int lane, int t, uint32_t ytag,
                                              uint32_t rtag) {
@@ -526,26 +589,26 @@ __device__ __forceinline__ bool consume_tile(const Params& p, const uint8_t* sta
     const int K = p.K, G = K / 64, R = p.rows_per_tile;
     const int rpw = R / kConsumerWarps;  // rows per warp per tile (1, 2, 4, 8)
     const uint32_t* wq = reinterpret_cast<const uint32_t*>(stage);
-    const uint16_t* ss = reinterpret_cast<const uint16_t*>(stage + (size_t)R * (K / 2));
+    const uint16_t* ss = reinterpret_cast<const uint16_t*>(stage + (size_t)R * (K * BITS / 8));
     const uint16_t* bs = ss + (size_t)R * G;
     int si, n0, nrows;
     find_tile(p, t, si, n0, nrows);
     bool ok = true;
     if (rpw >= RB) {
         for (int j = 0; j < rpw; j += RB)
-            ok &= tile_batch<M, RB>(p, wq, ss, bs, xs, scale, warp, lane, j, rpw, si, n0, nrows, ytag, rtag);
+            ok &= tile_batch<M, RB, BITS>(p, wq, ss, bs, xs, scale, warp, lane, j, rpw, si, n0, nrows, ytag, rtag);
     } else if (rpw == 4) {
-        ok = tile_batch<M, (RB < 4 ? RB : 4)>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag,
-                                              rtag);
+        ok = tile_batch<M, (RB < 4 ? RB : 4), BITS>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows,
+                                                    ytag, rtag);
     } else if (rpw == 2) {
-        ok = tile_batch<M, 2>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
+        ok = tile_batch<M, 2, BITS>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
     } else {
-        ok = tile_batch<M, 1>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
+        ok = tile_batch<M, 1, BITS>(p, wq, ss, bs, xs, scale, warp, lane, 0, rpw, si, n0, nrows, ytag, rtag);
     }
     return ok;
 }
 
-template <int M>
+template <int M, int BITS>
 __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -605,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
     }
 
     // ---------------------------------------------------------- consumers
-    if (p.norm && p.norm_w) stage_norm_weight<M>(p, xs);
+    if (p.norm && p.norm_w) stage_norm_weight<M, BITS>(p, xs);
     uint32_t xtag = 0, ytag = 0, rtag = 0;
     if (p.step_ctr) {
         const uint32_t step = step_sh;
@@ -621,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
         if (warp == 0) gate_tagged_x<M>(p, xtag, lane);
         q4d::named_bar(1, kConsumerWarps * 32);
     }
-    load_x<M>(p, xs, red, warp, lane, xtag);
+    load_x<M, BITS>(p, xs, red, warp, lane, xtag);
     q4d::named_bar(1, kConsumerWarps * 32);
     if (p.x_tag) q4d::pdl_trigger();
     float scale[M];
@@ -633,7 +696,7 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
         // on a timeout leave the loop (not the kernel): every consumer warp
         // must still reach the barrier below
         if (!q4d::mbar_wait(full0 + 8 * st, k & 1, p.err)) break;
-        consume_tile<M>(p, stages + (size_t)st * p.stage_bytes, xs, scale, warp, lane, t, ytag, rtag);
+        consume_tile<M, BITS>(p, stages + (size_t)st * p.stage_bytes, xs, scale, warp, lane, t, ytag, rtag);
         __syncwarp();
         if (lane == 0) q4d::mbar_arrive(empty0 + 8 * st);
     }
@@ -790,7 +853,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
                 const uint16_t* gam =
                     (ps.norm && ps.norm_w) ? reinterpret_cast<const uint16_t*>(slot + sp.meta_off + sizeof(Params))
                                            : nullptr;
-                if (!bad && !load_x<M>(ps, xs, red, warp, lane, xtag, gam)) bad = true;
+                if (!bad && !load_x<M, 4>(ps, xs, red, warp, lane, xtag, gam)) bad = true;
                 q4d::named_bar(1, kCT);
                 const Params& p = *prm;
                 const uint32_t ytag = tag_of(step, p.stage, p.n_stages);
@@ -804,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
                             bad = true;
                             break;
                         }
-                        if (!consume_tile<M>(p, ring + (size_t)st * sp.slot_bytes, xs, scale, warp, lane, t, ytag,
+                        if (!consume_tile<M, 4>(p, ring + (size_t)st * sp.slot_bytes, xs, scale, warp, lane, t, ytag,
                                              rtag))
                             bad = true;
                         __syncwarp();
@@ -913,9 +976,9 @@ uint32_t x_smem_bytes(int M, int K) {
     return (uint32_t)nchunks * (uint32_t)(LW * 2 * M) * 32u * 16u;
 }
 
-template <int M>
+template <int M, int BITS>
 cudaError_t launch_m(const Params& p, dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
-    auto kern = q4k::q4_gemv_kernel<M>;
+    auto kern = q4k::q4_gemv_kernel<M, BITS>;
     static int configured_smem[64] = {0};  // per device: largest dynamic smem set so far
     int dev = 0;
     cudaGetDevice(&dev);
@@ -940,8 +1003,9 @@ cudaError_t launch_m(const Params& p, dim3 grid, size_t smem, cudaStream_t strea
 // Kernel parameters of one fused GEMV (everything but the shared-memory
 // geometry).
 void fill_params(const q4_gemv_desc& d, const GemvTagged* tg, bool early_prefetch, int min_tiles,
-                 uint32_t max_stage, int* err, Params& p) {
+                 uint32_t max_stage, int* err, Params& p, int bits = 4) {
     p = {};
+    p.bits = bits;
     const int K = d.K, G = K / 64;
     const bool glu = d.mode == Q4_GEMV_GLU;
     p.x = d.x;
@@ -969,7 +1033,7 @@ void fill_params(const q4_gemv_desc& d, const GemvTagged* tg, bool early_prefetc
 
     // Tile rows: largest of 64/32/16/8 (per matrix) whose tile count still
     // reaches min_tiles, with a stage of at most max_stage bytes.
-    const uint32_t row_bytes = (uint32_t)(K / 2 + G * 4);
+    const uint32_t row_bytes = (uint32_t)(K * bits / 8 + G * 4);
     int TR = 64;
     while (TR > 8) {
         const uint32_t stage = (uint32_t)(glu ? 2 * TR : TR) * row_bytes;
@@ -1015,13 +1079,14 @@ bool gemv_fits_unsplit(int M, int K) {
 }
 
 q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch,
-                      const GemvTagged* tg) {
+                      const GemvTagged* tg, int bits) {
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
+    if (bits != 4 && bits != 8) return fail(Q4_ERR_INVALID_ARG, "bits=%d", bits);
 
     Params p;
-    fill_params(d, tg, early_prefetch, dev->sms, 48u * 1024u, dev->err_word, p);
+    fill_params(d, tg, early_prefetch, dev->sms, 48u * 1024u, dev->err_word, p, bits);
     const int M = d.M, K = d.K;
     p.x_bytes = (x_smem_bytes(M, K) + 127u) & ~127u;
     const uint32_t fixed = p.x_bytes + q4k::kBarBytes;
@@ -1052,9 +1117,9 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
             if (d.seg[i].y) hi.seg[i].y = static_cast<uint8_t*>(d.seg[i].y) + (size_t)lo.M * ldy * esz;
             if (d.seg[i].residual) hi.seg[i].residual = d.seg[i].residual + (size_t)lo.M * ldy;
         }
-        st = launch_gemv(lo, stream, pdl, early_prefetch);
+        st = launch_gemv(lo, stream, pdl, early_prefetch, nullptr, bits);
         if (st != Q4_OK) return st;
-        return launch_gemv(hi, stream, pdl, early_prefetch);
+        return launch_gemv(hi, stream, pdl, early_prefetch, nullptr, bits);
     }
     int S = (int)((budget - fixed) / p.stage_bytes);
     if (S > q4k::kMaxStages) S = q4k::kMaxStages;
@@ -1064,16 +1129,22 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     const int grid = tiles < dev->sms * ctas_per_sm ? tiles : dev->sms * ctas_per_sm;
 
     cudaError_t e = cudaSuccess;
+#define Q4_LAUNCH_M(MM)                                                                          \
+    case MM:                                                                                     \
+        e = bits == 4 ? launch_m<MM, 4>(p, dim3(grid), smem, stream, pdl)                        \
+                      : launch_m<MM, 8>(p, dim3(grid), smem, stream, pdl);                       \
+        break;
     switch (M) {
-        case 1: e = launch_m<1>(p, dim3(grid), smem, stream, pdl); break;
-        case 2: e = launch_m<2>(p, dim3(grid), smem, stream, pdl); break;
-        case 3: e = launch_m<3>(p, dim3(grid), smem, stream, pdl); break;
-        case 4: e = launch_m<4>(p, dim3(grid), smem, stream, pdl); break;
-        case 5: e = launch_m<5>(p, dim3(grid), smem, stream, pdl); break;
-        case 6: e = launch_m<6>(p, dim3(grid), smem, stream, pdl); break;
-        case 7: e = launch_m<7>(p, dim3(grid), smem, stream, pdl); break;
-        case 8: e = launch_m<8>(p, dim3(grid), smem, stream, pdl); break;
+        Q4_LAUNCH_M(1)
+        Q4_LAUNCH_M(2)
+        Q4_LAUNCH_M(3)
+        Q4_LAUNCH_M(4)
+        Q4_LAUNCH_M(5)
+        Q4_LAUNCH_M(6)
+        Q4_LAUNCH_M(7)
+        Q4_LAUNCH_M(8)
     }
+#undef Q4_LAUNCH_M
     if (e != cudaSuccess) return cuda_fail(e, "q4_gemv kernel launch");
     return Q4_OK;
 }

@@ -50,8 +50,9 @@ struct GemvTagged {
 
 // early_prefetch: weight copies may start before the programmatic-dependency
 // wait (only when the weights are not written by a preceding kernel).
+// bits: code width, 4 (Wq [N][K/8]) or 8 (Wq [N][K/4]).
 q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool early_prefetch,
-                      const GemvTagged* tg = nullptr);
+                      const GemvTagged* tg = nullptr, int bits = 4);
 // True when one launch of (M, K) fits in shared memory without splitting M.
 bool gemv_fits_unsplit(int M, int K);
 

@@ -101,6 +101,15 @@ q4_status q4_selftest_expired_wait(q4_stream_t stream);
 q4_status q4_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                   const uint16_t *x, float *y, int M, int N, int K, q4_stream_t stream);
 
+/* 1b. q4_gemv8 -- the same product for 8-bit codes (BaseRT §3.3 and §4.1:
+ * the runtime's kernels cover 2- to 16-bit formats; Q4 and Q8 are the ones
+ * evaluated).  Wq: uint32 [N][K/4], 16-byte aligned; code k of row n is
+ * bits 8*(k%4) .. 8*(k%4)+7 of word k/4 (lowest byte first), q in 0..255;
+ * scales, biases: fp16 [N][K/64]; w = s*q + b.  Everything else (x, y, M, N,
+ * K, alignment, errors, accuracy, determinism) as q4_gemv. */
+q4_status q4_gemv8(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                   const uint16_t *x, float *y, int M, int N, int K, q4_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * 2. q4_gemv_ex -- several matrices that share one input x in ONE launch,
  *    with fused epilogues.
