@@ -287,6 +287,38 @@ def moe_prefill(device, iters: int = 20, warmup: int = 5, token_counts=(128, 512
     return out
 
 
+def q8_lm_head(q4, device, M: int = 1):
+    """The lm_head-shaped GEMV (N=151936, K=1024) with 8-bit codes: 8 warm-up
+    launches, then 64 timed over 4 distinct weight copies (4 x 166 MB > L2)."""
+    import torch
+
+    import q4synth
+    N, K = 151936, 1024
+    mats = []
+    for i in range(4):
+        g = torch.Generator(device=device).manual_seed(200 + i)
+        Wq = torch.randint(-2**31, 2**31 - 1, (N, K // 4), dtype=torch.int32, device=device, generator=g)
+        s = (torch.rand(N, K // 64, device=device, generator=g) * 2e-4).half()
+        mats.append((Wq, s, (-128 * s.float()).half()))
+    x = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4243, M, K)).to(device)
+    y = torch.empty(M, N, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for i in range(8):
+        q4.q4_gemv8(*mats[i % 4], x, y, M, N, K, stream)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(64):
+        q4.q4_gemv8(*mats[i % 4], x, y, M, N, K, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / 64
+    nb = N * K * (1.0 + 4.0 / 64) + K * 2 * M + N * 4 * M
+    peak, kind = peaks()
+    return {"ms": ms, "gbs": nb / (ms / 1000.0) / 1e9, "frac": nb / (ms / 1000.0) / 1e9 / peak, "peak_kind": kind,
+            "shape": f"M={M} N={N} K={K}, 8-bit codes (1.0625 B/weight), 4 rotating copies"}
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: replicas run independently, so the job takes
     as long as its slowest replica (all-reduce MAX when world > 1)."""
@@ -415,7 +447,8 @@ def main():
         peak, peak_kind = peaks()
         print(json.dumps({"lm_head_gemv": {"ms": ms_l, "gbs": nb / (ms_l / 1000.0) / 1e9,
                                            "frac": nb / (ms_l / 1000.0) / 1e9 / peak, "peak_kind": peak_kind,
-                                           "shape": f"M={M} N={shape.vocab} K={shape.hidden}, 4 rotating copies"}}))
+                                           "shape": f"M={M} N={shape.vocab} K={shape.hidden}, 4 rotating copies"},
+                          "lm_head_gemv8": q8_lm_head(q4, device)}))
         return
     dl, dlm, host_model = make_model(shape, device)
     table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
@@ -507,6 +540,7 @@ def main():
         "clocks": clk.summary(),
     }
     if args.section == "all":
+        out["lm_head_gemv8"] = q8_lm_head(q4, device)
         out["moe_prefill"] = moe_prefill(device)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
