@@ -281,6 +281,37 @@ def decode_step(layers, lm_head, x, final_norm=None, eps: float = DEFAULT_EPS):
     return y, A, h
 
 
+def prefill_layer(layer, h, eps: float = DEFAULT_EPS):
+    """One layer of the prefill stream (BaseRT §3.4 "Prefill": the prompt's
+    tokens go through each matrix together).  The per-token dataflow of
+    decode_layer, except that the two normalised activations are stored in
+    fp16 before their matrix products (the tensor-core GEMM takes fp16
+    operands); every stored activation is rounded to fp16 as the GPU stores it."""
+    n = fp16(rmsnorm(h, layer.get("attn_norm"), eps))
+    q = fp16(gemv(*_mat(layer["q"]), n)[0])
+    k = fp16(gemv(*_mat(layer["k"]), n)[0])
+    v = fp16(gemv(*_mat(layer["v"]), n)[0])
+    hm = fp16(decode_o(layer, q, h)[0])
+    n2 = fp16(rmsnorm(hm, layer.get("ffn_norm"), eps))
+    g = gemv(*_mat(layer["gate"]), n2)[0]
+    u = gemv(*_mat(layer["up"]), n2)[0]
+    act = fp16(silu(g) * u)
+    ho = fp16(decode_down(layer, act, hm)[0])
+    return {"n": n, "q": q, "k": k, "v": v, "h_mid": hm, "n2": n2, "act": act, "h": ho}
+
+
+def prefill(layers, lm_head, x, final_norm=None, eps: float = DEFAULT_EPS):
+    """Prefill of T tokens: fp16 x [T, hidden] -> (final h [T, hidden] as
+    fp16 values, logits y [1, vocab] and A of the LAST token).  The tokens do
+    not interact in this stack (no attention), so chunking does not change
+    the result; the logits come from the decode path's lm_head product."""
+    h = np.atleast_2d(x).astype(np.float16)
+    for layer in layers:
+        h = prefill_layer(layer, h, eps)["h"]
+    y, A = decode_logits(lm_head, h[-1:], final_norm, eps=eps)
+    return h, y, A
+
+
 # --------------------------------------------------------------------- MoE ---
 
 def moe_route(logits, topk: int):

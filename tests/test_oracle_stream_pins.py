@@ -193,3 +193,83 @@ def test_expert_gate_up_split_matches_full_gemv():
     for i, e in enumerate(experts):
         full, _ = oracle.gemv(dn.Wq[e], dn.scales[e], dn.biases[e], H[i:i + 1])
         assert np.array_equal(y[i], full[0])
+
+
+# ---------------------------------------------------------------- prefill --
+
+def diag_stack(seed, n_layers=2):
+    g = np.random.default_rng(seed)
+    layers = []
+    for _ in range(n_layers):
+        d = {}
+        for nm in ("q", "k", "v", "o", "gate", "up", "down"):
+            d[nm] = diag_matrix(list(g.integers(0, 16, 64)), list(np.exp2(g.integers(-4, 1, 64)) * 0.75))
+        d["attn_norm"] = (g.random(64) + 0.5).astype(np.float16)
+        d["ffn_norm"] = (g.random(64) + 0.5).astype(np.float16)
+        layers.append(d)
+    lm = diag_matrix(list(g.integers(0, 16, 64)), list(np.exp2(g.integers(-3, 0, 64))))
+    fin = (g.random(64) + 0.5).astype(np.float16)
+    return layers, lm, fin
+
+
+def test_diagonal_prefill_reduces_to_elementwise():
+    """Diagonal weights again, now with both normalised activations stored in
+    fp16 before their products, and the last token's logits."""
+    layers, lm, fin = diag_stack(13)
+    x = q4synth.activations(14, 5, 64)
+    eps = 1e-5
+    h_o, logits, A = oracle.prefill(layers, lm, x, final_norm=fin, eps=eps)
+
+    f16 = lambda v: np.asarray(v, np.float64).astype(np.float16).astype(np.float64)
+    nrm = lambda v, w: v / np.sqrt((v * v).mean(axis=1, keepdims=True) + eps) * w.astype(np.float64)
+    h = x.astype(np.float64)
+    for d in layers:
+        n = f16(nrm(h, d["attn_norm"]))
+        q = f16(diag_values(d["q"]) * n)
+        hm = f16(h + diag_values(d["o"]) * q)
+        n2 = f16(nrm(hm, d["ffn_norm"]))
+        gg = diag_values(d["gate"]) * n2
+        act = f16(gg / (1 + np.exp(-gg)) * (diag_values(d["up"]) * n2))
+        h = f16(hm + diag_values(d["down"]) * act)
+    assert np.array_equal(h_o.astype(np.float64), h)
+    want = diag_values(lm) * nrm(h[-1:], fin)
+    assert np.allclose(logits, want, rtol=1e-15, atol=0)
+
+
+def test_prefill_tokens_are_independent():
+    """No attention in this stack: each token's result is that of the token
+    alone, and the logits are those of the last token."""
+    shape = q4synth.tiny_decode_shape(n_layers=2, hidden=128, q=256, kv=128, ffn=256, vocab=96)
+    layers, lm = q4synth.decode_weights(shape, base_seed=91)
+    x = q4synth.activations(92, 4, 128)
+    h_all, y_all, _ = oracle.prefill(layers, lm, x)
+    for t in range(4):
+        h_t, y_t, _ = oracle.prefill(layers, lm, x[t:t + 1])
+        assert np.array_equal(h_all[t], h_t[0])
+    assert np.array_equal(y_all, y_t)
+
+
+def test_prefill_equals_decode_when_norms_are_fp16_exact():
+    """With eps = 0, zero o and down products and a constant-magnitude x,
+    rms(h) * gamma = sign(h) * gamma is exact in fp16, so storing the norm in
+    fp16 changes nothing and the prefill stream equals the decode stream."""
+    shape = q4synth.tiny_decode_shape(n_layers=2, hidden=128, q=128, kv=128, ffn=256, vocab=64)
+    layers, lm = q4synth.decode_weights(shape, base_seed=93)
+    for d in layers:
+        for nm in ("o", "down"):
+            m = d[nm]
+            m.Wq[:] = 0x88888888
+            m.biases[:] = (-8.0 * m.scales.astype(np.float64)).astype(np.float16)
+        d["attn_norm"] = np.linspace(0.5, 1.5, 128).astype(np.float16)
+        d["ffn_norm"] = np.linspace(1.5, 0.5, 128).astype(np.float16)
+    g = np.random.default_rng(94)
+    x = (np.where(g.random((3, 128)) < 0.5, -1.0, 1.0) * 0.75).astype(np.float16)
+    h_p, y_p, _ = oracle.prefill(layers, lm, x, eps=0.0)
+    y_d, _, h_d = oracle.decode_step(layers, lm, x, eps=0.0)
+    assert np.array_equal(h_p, h_d)
+    assert np.array_equal(y_p, y_d[-1:])
+    for d in layers:   # and the stage values agree too
+        a = oracle.prefill_layer(d, x, eps=0.0)
+        b = oracle.decode_layer(d, x, eps=0.0)
+        for nm in ("q", "k", "v", "h_mid", "act", "h"):
+            assert np.array_equal(a[nm], b[nm]), nm
