@@ -287,6 +287,58 @@ def moe_prefill(device, iters: int = 20, warmup: int = 5, token_counts=(128, 512
     return out
 
 
+def tensor_peak():
+    """Measured dense bf16 tensor throughput (TFLOP/s, burst); fp16 runs at the same rate."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured (bf16 burst; fp16 same rate)"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def dense_prefill(device, dl, dlm, shape, iters: int = 5, warmup: int = 3, cases=((512, 512), (2048, 512),
+                                                                                  (2048, 2048))):
+    """Chunked prefill of the whole layer stack (q4_prefill: per chunk and
+    layer an RMSNorm kernel and five tensor-core GEMMs, then the lm_head GEMV
+    of the last token), as (prompt tokens, chunk) cases; the prompt is reset
+    from a resident copy before each timed call (a device copy inside the
+    timed region, <1 % of it)."""
+    import torch
+
+    import bit_quantized_gemv_q4_gb300 as q4
+    import q4synth
+    table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=1)
+    stream = torch.cuda.current_stream(device)
+    per_tok = 2.0 * sum(N * K for _, N, K in shape.layer_linears()) * shape.n_layers
+    peak, kind = tensor_peak()
+    out = {"shape": f"{shape.name}, {shape.n_layers} layers", "peak_tflops": peak, "peak_kind": kind}
+    for T, C in cases:
+        x0 = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 9100 + T, T, shape.hidden)).to(device)
+        h = torch.empty_like(x0)
+        nws = q4.q4_prefill_workspace_bytes(table, C)
+        ws = torch.empty(nws, dtype=torch.uint8, device=device)
+        lg = torch.empty(shape.vocab, dtype=torch.float32, device=device)
+        for _ in range(warmup):
+            h.copy_(x0)
+            q4.q4_prefill(table, h, T, C, lg, ws, nws, stream)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(iters):
+            h.copy_(x0)
+            q4.q4_prefill(table, h, T, C, lg, ws, nws, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if q4.q4_device_status(stream) != 0:
+            raise RuntimeError("device status after prefill timing")
+        ms = e0.elapsed_time(e1) / iters
+        tf = per_tok * T / (ms * 1e-3) / 1e12
+        out[f"T={T} chunk={C}"] = {"ms": ms, "tok_per_s": T / (ms * 1e-3), "gemm_tflops": tf,
+                                   "tensor_frac": tf / peak}
+    table.release()
+    return out
+
+
 def q8_lm_head(q4, device, M: int = 1):
     """The lm_head-shaped GEMV (N=151936, K=1024) with 8-bit codes: 8 warm-up
     launches, then 64 timed over 4 distinct weight copies (4 x 166 MB > L2)."""
@@ -368,7 +420,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head"],
+    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head", "prefill"],
                     help="moe / lm_head: only the MoE prefill timings / the lm_head GEMV timing "
                          "(for profiling runs)")
     args = ap.parse_args()
@@ -451,6 +503,9 @@ def main():
                           "lm_head_gemv8": q8_lm_head(q4, device)}))
         return
     dl, dlm, host_model = make_model(shape, device)
+    if args.section == "prefill":
+        print(json.dumps({"dense_prefill": dense_prefill(device, dl, dlm, shape)}))
+        return
     table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
     nws = q4.q4_decode_workspace_bytes(table)
     ws = torch.empty(nws, dtype=torch.uint8, device=device)
@@ -542,6 +597,7 @@ def main():
     if args.section == "all":
         out["lm_head_gemv8"] = q8_lm_head(q4, device)
         out["moe_prefill"] = moe_prefill(device)
+        out["dense_prefill"] = dense_prefill(device, dl, dlm, shape)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

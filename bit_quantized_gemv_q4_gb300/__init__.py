@@ -38,7 +38,8 @@ EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status"
            "q4_selftest_expired_wait", "q4_gemv", "q4_gemv8",
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
            "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
-           "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine"]
+           "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine", "q4_gemm", "q4_prefill_workspace_bytes",
+           "q4_prefill"]
 
 
 class Q4Error(RuntimeError):
@@ -87,6 +88,11 @@ class q4_moe_desc(ctypes.Structure):
     _fields_ = [("E", i32), ("N", i32), ("K", i32), ("R", i32), ("mode", i32), ("out_dtype", i32)]
 
 
+class q4_gemm_desc(ctypes.Structure):
+    _fields_ = [("M", i32), ("X", vp), ("w", q4_linear), ("up", q4_linear), ("mode", i32), ("out_dtype", i32),
+                ("Y", vp), ("residual", vp)]
+
+
 _lib = None
 
 
@@ -133,6 +139,12 @@ def lib() -> ctypes.CDLL:
         L.q4_moe_gemm.argtypes = [vp] * 7 + [ctypes.POINTER(q4_moe_desc), vp]
         L.q4_moe_combine.restype = st
         L.q4_moe_combine.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]
+        L.q4_gemm.restype = st
+        L.q4_gemm.argtypes = [ctypes.POINTER(q4_gemm_desc), vp]
+        L.q4_prefill_workspace_bytes.restype = ctypes.c_size_t
+        L.q4_prefill_workspace_bytes.argtypes = [ctypes.POINTER(q4_layer_table), i32]
+        L.q4_prefill.restype = st
+        L.q4_prefill.argtypes = [ctypes.POINTER(q4_layer_table), vp, i32, i32, vp, vp, ctypes.c_size_t, vp]
         _lib = L
     return _lib
 
@@ -309,3 +321,29 @@ def q4_moe_gemm(Wq, scales, biases, X, expert_ids, offsets, Y, E, N, K, R, mode=
 def q4_moe_combine(Y, y_dtype, N, pos, topk_weights, T, topk, out, out_dtype, stream=None):
     _check(lib().q4_moe_combine(_ptr(Y), y_dtype, N, _ptr(pos), _ptr(topk_weights), T, topk, _ptr(out),
                                 out_dtype, _stream(stream)), "q4_moe_combine")
+
+
+# --------------------------------------------------------------- prefill ---
+
+def q4_gemm(w, X, Y, M: int, mode=Q4_GEMV_PLAIN, out_dtype=Q4_F32, up=None, residual=None, stream=None):
+    """Dense Y[M, N] = X[M, K] W^T on the tensor cores.  ``w`` (and ``up`` in
+    GLU mode) are (Wq, scales, biases, N, K)."""
+    d = q4_gemm_desc()
+    d.M, d.X, d.w = M, _ptr(X), _linear(*w)
+    if up is not None:
+        d.up = _linear(*up)
+    d.mode, d.out_dtype, d.Y, d.residual = mode, out_dtype, _ptr(Y), _ptr(residual)
+    _check(lib().q4_gemm(ctypes.byref(d), _stream(stream)), "q4_gemm")
+
+
+def q4_prefill_workspace_bytes(table: LayerTable, chunk: int) -> int:
+    n = lib().q4_prefill_workspace_bytes(ctypes.byref(table.t), chunk)
+    if n == 0:
+        raise Q4Error(-1, "q4_prefill_workspace_bytes", lib().q4_last_error().decode())
+    return n
+
+
+def q4_prefill(table: LayerTable, h, T: int, chunk: int, logits, workspace, workspace_bytes: int, stream=None):
+    """Chunked prefill: h fp16 [T, hidden] in place; logits of the last token (or None)."""
+    _check(lib().q4_prefill(ctypes.byref(table.t), _ptr(h), T, chunk, _ptr(logits), _ptr(workspace),
+                            workspace_bytes, _stream(stream)), "q4_prefill")

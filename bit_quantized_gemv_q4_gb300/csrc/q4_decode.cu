@@ -16,6 +16,7 @@
 // Programmatic dependent launch links consecutive kernels so each kernel's
 // weight stream (which never depends on its predecessor) starts while the
 // predecessor is still running; only its activation reads wait.
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
 #include <vector>
@@ -284,12 +285,174 @@ q4_status capture(Plan& p) {
     return Q4_OK;
 }
 
+// ---------------------------------------------------------------- prefill
+// n[r] = fp16(h[r] / sqrt(mean(h[r]^2) + eps) * gamma), one warp per row,
+// fp32 arithmetic; 16-byte accesses (hidden is a multiple of 64).
+__global__ void rmsnorm_rows_kernel(const uint16_t* __restrict__ h, const uint16_t* __restrict__ gamma,
+                                    uint16_t* __restrict__ n, int rows, int hidden, float eps) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const uint4* src = reinterpret_cast<const uint4*>(h + (size_t)warp * hidden);
+    const int nv = hidden / 8;
+    float ss = 0.f;
+    for (int i = lane; i < nv; i += 32) {
+        const uint4 v = src[i];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss / (float)hidden + eps);
+    uint4* dst = reinterpret_cast<uint4*>(n + (size_t)warp * hidden);
+    const uint4* gv = reinterpret_cast<const uint4*>(gamma);
+    for (int i = lane; i < nv; i += 32) {
+        const uint4 v = src[i];
+        const uint4 g = gamma ? gv[i] : make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+            const float2 gg = __half22float2(*reinterpret_cast<const __half2*>(&gw[j]));
+            const __half2 hv = __floats2half2_rn(f.x * r * gg.x, f.y * r * gg.y);
+            o[j] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+struct PrefillLayout {
+    size_t n = 0, q = 0, k = 0, v = 0, act = 0, total = 0;
+};
+
+PrefillLayout prefill_layout(const Dims& d, int chunk) {
+    PrefillLayout l;
+    size_t off = 0;
+    auto take = [&](size_t elems) {
+        size_t o = off;
+        off = align256(off + elems * 2);
+        return o;
+    };
+    const size_t C = (size_t)chunk;
+    l.n = take(C * d.hidden);
+    l.q = take(C * (d.qN > 0 ? d.qN : 1));
+    l.k = take(C * (d.kvN > 0 ? d.kvN : 1));
+    l.v = take(C * (d.kvN > 0 ? d.kvN : 1));
+    l.act = take(C * (d.ffn > 0 ? d.ffn : 1));
+    l.total = off;
+    return l;
+}
+
+q4_status prefill_dims(const q4_layer_table* t, int chunk, Dims* d) {
+    if (!t) return fail(Q4_ERR_INVALID_ARG, "table is NULL");
+    if (chunk < 1) return fail(Q4_ERR_INVALID_ARG, "chunk=%d", chunk);
+    q4_layer_table c = *t;
+    c.M = 1;  // the prefill ignores M
+    return table_dims(&c, d);
+}
+
+q4_status gemm_of(const q4_linear& w, const q4_linear* up, const uint16_t* X, int M, void* Y,
+                  const uint16_t* residual, cudaStream_t s) {
+    q4_gemm_desc g = {};
+    g.M = M;
+    g.X = X;
+    g.w = w;
+    if (up) g.up = *up;
+    g.mode = up ? Q4_GEMV_GLU : Q4_GEMV_PLAIN;
+    g.out_dtype = Q4_F16;
+    g.Y = Y;
+    g.residual = residual;
+    return gemm_launch(&g, reinterpret_cast<q4_stream_t>(s));
+}
+
 }  // namespace
 }  // namespace q4i
 
 using namespace q4i;
 
 extern "C" {
+
+size_t q4_prefill_workspace_bytes(const q4_layer_table* table, int chunk) {
+    clear_error();
+    Dims d;
+    if (prefill_dims(table, chunk, &d) != Q4_OK) return 0;
+    return prefill_layout(d, chunk).total;
+}
+
+q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk, void* logits, void* workspace,
+                     size_t workspace_bytes, q4_stream_t stream) {
+    clear_error();
+    Dims d;
+    q4_status st = prefill_dims(table, chunk, &d);
+    if (st != Q4_OK) return st;
+    if (T < 0) return fail(Q4_ERR_INVALID_ARG, "T=%d", T);
+    if (T > 0 && !h) return fail(Q4_ERR_INVALID_ARG, "h is NULL");
+    if (!aligned16(h) || (logits && !aligned16(logits))) return fail(Q4_ERR_MISALIGNED, "h and logits must be 16-byte aligned");
+    const PrefillLayout l = prefill_layout(d, chunk);
+    if (!workspace) return fail(Q4_ERR_INVALID_ARG, "workspace is NULL");
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(Q4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
+    if (workspace_bytes < l.total) return fail(Q4_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, l.total);
+    for (int i = 0; i < d.L; ++i) {
+        const q4_layer_weights& w = table->layers[i];
+        if (w.q.N % 128 || w.k.N % 128 || w.v.N % 128 || w.o.N % 128 || w.gate.N % 128 || w.down.N % 128)
+            return fail(Q4_ERR_UNSUPPORTED, "layer %d: the prefill GEMM needs output widths that are multiples of 128", i);
+    }
+    const DeviceInfo* dev = nullptr;
+    if ((st = current_device(&dev)) != Q4_OK) return st;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const float eps = table->norm_eps > 0.f ? table->norm_eps : 1e-6f;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    uint16_t* n = reinterpret_cast<uint16_t*>(ws + l.n);
+    uint16_t* q = reinterpret_cast<uint16_t*>(ws + l.q);
+    uint16_t* k = reinterpret_cast<uint16_t*>(ws + l.k);
+    uint16_t* v = reinterpret_cast<uint16_t*>(ws + l.v);
+    uint16_t* act = reinterpret_cast<uint16_t*>(ws + l.act);
+    const int H = d.hidden;
+    for (int t0 = 0; t0 < T; t0 += chunk) {
+        const int C = T - t0 < chunk ? T - t0 : chunk;
+        uint16_t* hc = h + (size_t)t0 * H;
+        const int nb = (C + 7) / 8;
+        for (int i = 0; i < d.L; ++i) {
+            const q4_layer_weights& w = table->layers[i];
+            rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.attn_norm, n, C, H, eps);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+            if ((st = gemm_of(w.q, nullptr, n, C, q, nullptr, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.k, nullptr, n, C, k, nullptr, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.v, nullptr, n, C, v, nullptr, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.o, nullptr, q, C, hc, hc, s)) != Q4_OK) return st;  // h' = h + Wo q
+            rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.ffn_norm, n, C, H, eps);
+            if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+            if ((st = gemm_of(w.gate, &w.up, n, C, act, nullptr, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.down, nullptr, act, C, hc, hc, s)) != Q4_OK) return st;  // h = h' + Wdown act
+        }
+    }
+    if (logits && T > 0) {
+        q4_gemv_desc g = {};
+        g.M = 1;
+        g.K = H;
+        g.x = h + (size_t)(T - 1) * H;
+        g.n_segments = 1;
+        g.seg[0].Wq = table->lm_head.Wq;
+        g.seg[0].scales = table->lm_head.scales;
+        g.seg[0].biases = table->lm_head.biases;
+        g.seg[0].N = table->lm_head.N;
+        g.seg[0].y = logits;
+        g.out_dtype = table->logits_dtype;
+        g.mode = Q4_GEMV_PLAIN;
+        g.x_rmsnorm = 1;
+        g.norm_weight = table->final_norm;
+        g.norm_eps = eps;
+        if ((st = validate_gemv(g)) != Q4_OK) return st;
+        return launch_gemv(g, s, false, true);
+    }
+    return Q4_OK;
+}
 
 size_t q4_decode_workspace_bytes(const q4_layer_table* table) {
     clear_error();

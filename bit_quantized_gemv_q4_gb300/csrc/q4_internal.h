@@ -29,6 +29,9 @@ q4_status current_device(const DeviceInfo** out);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---- dense GEMM on the grouped-GEMM kernel (q4_moe_gemm.cu) ---------------
+q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream);
+
 // ---- fused multi-segment GEMV (q4_gemv.cu) --------------------------------
 q4_status validate_gemv(const q4_gemv_desc& d);
 

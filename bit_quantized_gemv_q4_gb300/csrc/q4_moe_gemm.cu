@@ -69,9 +69,12 @@ constexpr uint32_t kAStageBytes = 2 * kATileBytes;
 struct Params {
     const uint16_t* scales;
     const uint16_t* biases;
-    const int32_t* offsets;
+    const uint16_t* scales_u;  // the up matrix's scales and biases (GLU): its rows are
+    const uint16_t* biases_u;  // e * rows_e + up_off + n of these arrays
+    const uint16_t* residual;  // PLAIN, fp16 out: Y = fp16(residual + acc); may alias Y
+    const int32_t* offsets;    // NULL: dense, one expert holding rows 0..R-1
     void* Y;
-    int E, N, K, R, rows_e, nmat, glu, out_f16;
+    int E, N, K, R, rows_e, up_off, nmat, glu, out_f16;
     int n_tiles, nK, G;
     uint32_t sb_bytes;   // private per-thread scale/bias slots
     uint32_t stg_bytes;  // staging buffer: the unit's scale and bias blocks
@@ -172,7 +175,7 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int
     Unit un;
     un.e = lo;
     const int j = tt - sm.prefix[lo];
-    int a = p.offsets[lo], b = p.offsets[lo + 1];
+    int a = p.offsets ? p.offsets[lo] : 0, b = p.offsets ? p.offsets[lo + 1] : p.R;
     a = max(0, min(a, p.R));
     b = max(a, min(b, p.R));
     un.r0 = a + j * kTN;
@@ -199,8 +202,8 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t q, __half2 s2, __half2 b2
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    q4_moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                       const __grid_constant__ Params p) {
+    q4_moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
+                       const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles.
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -237,8 +240,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             int run = 0;
             for (int e = 0; e < p.E; ++e) {
                 sm.prefix[e] = run;
-                int a = max(0, min(p.offsets[e], p.R));
-                int b = max(a, min(p.offsets[e + 1], p.R));
+                int a = p.offsets ? max(0, min(p.offsets[e], p.R)) : 0;
+                int b = p.offsets ? max(a, min(p.offsets[e + 1], p.R)) : p.R;
                 run += (b - a + kTN - 1) / kTN;
             }
             sm.prefix[p.E] = run;
@@ -267,15 +270,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++uu) {
                 const Unit un = decode_unit(sm, p, u);
                 const int wrow = un.e * p.rows_e + un.nt * kRows;
+                const int wrow_u = un.e * p.rows_e + p.up_off + un.nt * kRows;
                 // the staging buffer is free once every dequant warp has read the previous unit's values
                 if (uu > 0 && !wait_bar(sm, sm.sb_empty, (uu - 1) & 1, p.err)) break;
                 {
                     const uint32_t fb = q4d::smem_addr(&sm.sb_full);
                     q4d::mbar_arrive_expect_tx(fb, (uint32_t)p.nmat * 2u * blk);
                     for (int m = 0; m < p.nmat; ++m) {
-                        const size_t r = (size_t)wrow + (size_t)m * p.N;
-                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m) * blk), p.scales + r * p.G, blk, fb);
-                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m + 1) * blk), p.biases + r * p.G, blk, fb);
+                        const size_t r = (size_t)(m ? wrow_u : wrow) * p.G;
+                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m) * blk), (m ? p.scales_u : p.scales) + r, blk, fb);
+                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m + 1) * blk), (m ? p.biases_u : p.biases) + r, blk,
+                                      fb);
                     }
                     ++staged;
                 }
@@ -286,7 +291,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t fb = q4d::smem_addr(&sm.in_full[s]);
                     q4d::mbar_arrive_expect_tx(fb, p.nmat * kCodesBytes + kXBytes);
                     tma_load_2d(q4d::smem_addr(st), &tmW, ks * 32, wrow, fb);
-                    if (p.glu) tma_load_2d(q4d::smem_addr(st + kCodesBytes), &tmW, ks * 32, wrow + p.N, fb);
+                    if (p.glu) tma_load_2d(q4d::smem_addr(st + kCodesBytes), &tmWu, ks * 32, wrow_u, fb);
                     tma_load_2d(q4d::smem_addr(st + 2 * kCodesBytes), &tmX, ks * kKS, un.r0, fb);
                 }
             }
@@ -440,6 +445,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             const float up = __uint_as_float(v[c]);
                             y = y / (1.0f + expf(-y)) * up;
                         }
+                        if (p.residual) y += __half2float(__ushort_as_half(p.residual[o]));
                         if (p.out_f16)
                             static_cast<uint16_t*>(p.Y)[o] = __half_as_ushort(__float2half_rn(y));
                         else
@@ -531,7 +537,135 @@ q4_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uin
     return Q4_OK;
 }
 
+
+// One launch of the grouped GEMM.  Routed (offsets != NULL): E experts, rows
+// of W_e at e * rows_e, the up matrix at + N rows of the same arrays.  Dense
+// (offsets == NULL): one expert over rows 0..R-1, the up matrix given apart.
+struct GroupedArgs {
+    const uint32_t* Wq;
+    const uint16_t *scales, *biases;
+    const uint32_t* Wq_u;  // GLU: the up matrix (may be Wq)
+    const uint16_t *scales_u, *biases_u;
+    int up_off;            // row of the up matrix's first row within Wq_u's expert block
+    const uint16_t* X;
+    const int32_t *expert_ids, *offsets;
+    void* Y;
+    const uint16_t* residual;
+    int E, N, K, R;
+    q4_gemv_mode mode;
+    q4_dtype out_dtype;
+};
+
+q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
+    if (a.E < 1 || a.E > q4g::kMaxExperts) return fail(Q4_ERR_INVALID_ARG, "E=%d outside 1..%d", a.E, q4g::kMaxExperts);
+    if (a.K < 64 || a.K % 64) return fail(Q4_ERR_INVALID_ARG, "K=%d is not a positive multiple of 64", a.K);
+    if (a.N < 1) return fail(Q4_ERR_INVALID_ARG, "N=%d", a.N);
+    if (a.N % 128) return fail(Q4_ERR_UNSUPPORTED, "N=%d is not a multiple of 128", a.N);
+    if (a.R < 0) return fail(Q4_ERR_INVALID_ARG, "R=%d", a.R);
+    if (a.mode != Q4_GEMV_PLAIN && a.mode != Q4_GEMV_GLU) return fail(Q4_ERR_INVALID_ARG, "bad mode");
+    if (a.out_dtype != Q4_F32 && a.out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "bad out_dtype");
+    if (a.mode == Q4_GEMV_GLU && a.out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "GLU mode writes fp16");
+    if (a.residual && (a.mode != Q4_GEMV_PLAIN || a.out_dtype != Q4_F16))
+        return fail(Q4_ERR_INVALID_ARG, "a residual needs PLAIN mode and fp16 output");
+    const bool glu = a.mode == Q4_GEMV_GLU;
+    if (!aligned16(a.Wq) || !aligned16(a.X) || !aligned16(a.scales) || !aligned16(a.biases) ||
+        (glu && (!aligned16(a.Wq_u) || !aligned16(a.scales_u) || !aligned16(a.biases_u))))
+        return fail(Q4_ERR_MISALIGNED, "Wq, X, scales and biases must be 16-byte aligned");
+    const int rows_e = a.offsets ? (glu ? 2 : 1) * a.N : a.N;
+    if ((long long)a.E * rows_e > (1ll << 31)) return fail(Q4_ERR_UNSUPPORTED, "too many weight rows");
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    if (a.R == 0) return Q4_OK;
+
+    q4g::Params p = {};
+    p.scales = a.scales;
+    p.biases = a.biases;
+    p.scales_u = a.scales_u;
+    p.biases_u = a.biases_u;
+    p.residual = a.residual;
+    p.offsets = a.offsets;
+    p.Y = a.Y;
+    p.E = a.E;
+    p.N = a.N;
+    p.K = a.K;
+    p.R = a.R;
+    p.glu = glu;
+    p.nmat = glu ? 2 : 1;
+    p.rows_e = rows_e;
+    p.up_off = a.up_off;
+    p.out_f16 = a.out_dtype == Q4_F16;
+    p.n_tiles = a.N / q4g::kRows;
+    p.nK = a.K / q4g::kKS;
+    p.G = a.K / 64;
+    p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqThreads * (p.G + 1) * 4 + 127) & ~size_t(127));
+    p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
+    p.err = dev->err_word;
+
+    const size_t smem = 1024 + (size_t)q4g::kInStages * q4g::kInStageBytes + (size_t)q4g::kAStages * q4g::kAStageBytes +
+                        p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
+    if (smem > (size_t)dev->smem_optin)
+        return fail(Q4_ERR_UNSUPPORTED, "K=%d needs %zu bytes of shared memory", a.K, smem);
+
+    CUtensorMap tmW, tmWu, tmX;
+    const uint64_t wrows = (uint64_t)a.E * rows_e;
+    st = make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, (uint64_t)a.K / 2, wrows, (uint64_t)a.K / 2, 32,
+                  q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (st != Q4_OK) return st;
+    tmWu = tmW;
+    if (glu && a.Wq_u != a.Wq) {
+        st = make_map(&tmWu, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq_u, (uint64_t)a.K / 2, wrows, (uint64_t)a.K / 2, 32,
+                      q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != Q4_OK) return st;
+    }
+    st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, (uint64_t)a.K, (uint64_t)a.R, (uint64_t)a.K * 2,
+                  q4g::kKS, q4g::kTN, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (st != Q4_OK) return st;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (a.offsets)
+        q4g::check_routing_kernel<<<(a.R + 255) / 256 < dev->sms ? (a.R + 255) / 256 : dev->sms, 256, 0, s>>>(
+            a.expert_ids, a.offsets, a.E, a.R, dev->err_word);
+    cudaError_t e = cudaFuncSetAttribute(q4g::q4_moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
+    q4g::q4_moe_gemm_kernel<<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
+    return Q4_OK;
+}
+
 }  // namespace
+
+q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream) {
+    if (!d) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");
+    const bool glu = d->mode == Q4_GEMV_GLU;
+    if (!d->w.Wq || !d->w.scales || !d->w.biases || !d->X || !d->Y)
+        return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (glu && (!d->up.Wq || !d->up.scales || !d->up.biases))
+        return fail(Q4_ERR_INVALID_ARG, "GLU mode needs the up matrix");
+    if (glu && (d->up.N != d->w.N || d->up.K != d->w.K))
+        return fail(Q4_ERR_INVALID_ARG, "gate %dx%d and up %dx%d differ", d->w.N, d->w.K, d->up.N, d->up.K);
+    if (d->M < 0) return fail(Q4_ERR_INVALID_ARG, "M=%d", d->M);
+    GroupedArgs a = {};
+    a.Wq = d->w.Wq;
+    a.scales = d->w.scales;
+    a.biases = d->w.biases;
+    a.Wq_u = glu ? d->up.Wq : d->w.Wq;
+    a.scales_u = glu ? d->up.scales : d->w.scales;
+    a.biases_u = glu ? d->up.biases : d->w.biases;
+    a.up_off = 0;
+    a.X = d->X;
+    a.Y = d->Y;
+    a.residual = d->residual;
+    a.E = 1;
+    a.N = d->w.N;
+    a.K = d->w.K;
+    a.R = d->M;
+    a.mode = d->mode;
+    a.out_dtype = d->out_dtype;
+    return launch_grouped(a, stream);
+}
+
 }  // namespace q4i
 
 using namespace q4i;
@@ -543,63 +677,25 @@ extern "C" q4_status q4_moe_gemm(const uint32_t* Wq, const uint16_t* scales, con
     if (!d) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");
     if (!Wq || !scales || !biases || !X || !expert_ids || !offsets || !Y)
         return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
-    if (d->E < 1 || d->E > q4g::kMaxExperts) return fail(Q4_ERR_INVALID_ARG, "E=%d outside 1..%d", d->E, q4g::kMaxExperts);
-    if (d->K < 64 || d->K % 64) return fail(Q4_ERR_INVALID_ARG, "K=%d is not a positive multiple of 64", d->K);
-    if (d->N < 1) return fail(Q4_ERR_INVALID_ARG, "N=%d", d->N);
-    if (d->N % 128) return fail(Q4_ERR_UNSUPPORTED, "N=%d is not a multiple of 128", d->N);
-    if (d->R < 0) return fail(Q4_ERR_INVALID_ARG, "R=%d", d->R);
-    if (d->mode != Q4_GEMV_PLAIN && d->mode != Q4_GEMV_GLU) return fail(Q4_ERR_INVALID_ARG, "bad mode");
-    if (d->out_dtype != Q4_F32 && d->out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "bad out_dtype");
-    if (d->mode == Q4_GEMV_GLU && d->out_dtype != Q4_F16) return fail(Q4_ERR_INVALID_ARG, "GLU mode writes fp16");
-    if (!aligned16(Wq) || !aligned16(X) || !aligned16(scales) || !aligned16(biases))
-        return fail(Q4_ERR_MISALIGNED, "Wq, X, scales and biases must be 16-byte aligned");
-    if ((long long)d->E * (d->mode == Q4_GEMV_GLU ? 2 : 1) * d->N > (1ll << 31))
-        return fail(Q4_ERR_UNSUPPORTED, "too many weight rows");
-    const DeviceInfo* dev = nullptr;
-    q4_status st = current_device(&dev);
-    if (st != Q4_OK) return st;
-    if (d->R == 0) return Q4_OK;
+    GroupedArgs a = {};
+    a.Wq = a.Wq_u = Wq;
+    a.scales = a.scales_u = scales;
+    a.biases = a.biases_u = biases;
+    a.up_off = d->N;
+    a.X = X;
+    a.expert_ids = expert_ids;
+    a.offsets = offsets;
+    a.Y = Y;
+    a.E = d->E;
+    a.N = d->N;
+    a.K = d->K;
+    a.R = d->R;
+    a.mode = d->mode;
+    a.out_dtype = d->out_dtype;
+    return launch_grouped(a, stream);
+}
 
-    q4g::Params p = {};
-    p.scales = scales;
-    p.biases = biases;
-    p.offsets = offsets;
-    p.Y = Y;
-    p.E = d->E;
-    p.N = d->N;
-    p.K = d->K;
-    p.R = d->R;
-    p.glu = d->mode == Q4_GEMV_GLU;
-    p.nmat = p.glu ? 2 : 1;
-    p.rows_e = p.nmat * d->N;
-    p.out_f16 = d->out_dtype == Q4_F16;
-    p.n_tiles = d->N / q4g::kRows;
-    p.nK = d->K / q4g::kKS;
-    p.G = d->K / 64;
-    p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqThreads * (p.G + 1) * 4 + 127) & ~size_t(127));
-    p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
-    p.err = dev->err_word;
-
-    CUtensorMap tmW, tmX;
-    const uint64_t wrows = (uint64_t)d->E * p.rows_e;
-    st = make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, Wq, (uint64_t)d->K / 2, wrows, (uint64_t)d->K / 2, 32,
-                  q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (st != Q4_OK) return st;
-    st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, X, (uint64_t)d->K, (uint64_t)d->R, (uint64_t)d->K * 2,
-                  q4g::kKS, q4g::kTN, CU_TENSOR_MAP_SWIZZLE_128B);
-    if (st != Q4_OK) return st;
-
-    const size_t smem = 1024 + (size_t)q4g::kInStages * q4g::kInStageBytes + (size_t)q4g::kAStages * q4g::kAStageBytes +
-                        p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
-    if (smem > (size_t)dev->smem_optin)
-        return fail(Q4_ERR_UNSUPPORTED, "K=%d needs %zu bytes of shared memory", d->K, smem);
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    q4g::check_routing_kernel<<<(d->R + 255) / 256 < dev->sms ? (d->R + 255) / 256 : dev->sms, 256, 0, s>>>(
-        expert_ids, offsets, d->E, d->R, dev->err_word);
-    cudaError_t e = cudaFuncSetAttribute(q4g::q4_moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
-    q4g::q4_moe_gemm_kernel<<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmX, p);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "q4_moe_gemm launch");
-    return Q4_OK;
+extern "C" q4_status q4_gemm(const q4_gemm_desc* desc, q4_stream_t stream) {
+    clear_error();
+    return gemm_launch(desc, stream);
 }

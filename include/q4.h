@@ -362,6 +362,60 @@ q4_status q4_moe_combine(const void *Y, q4_dtype y_dtype, int N, const int32_t *
                          const float *topk_weights, int T, int topk, void *out,
                          q4_dtype out_dtype, q4_stream_t stream);
 
+/* ------------------------------------------------------------------------ *
+ * 5. Dense prefill: a GEMM over M tokens, and the chunked prefill of a whole
+ *    layer stack.
+ *
+ * BaseRT §3.4 "Prefill": the prompt's tokens go through each matrix together,
+ * as GEMMs whose arithmetic intensity grows with the token count, in chunks;
+ * §3.3: the GEMM kernels dequantise in their inner loop like the GEMV.  The
+ * GEMM here is the kernel of section 4 with one expert and no routing: codes
+ * dequantised to fp16 in shared memory (w rounded once to fp16), tcgen05
+ * fp16 x fp16 -> fp32 MMA, so X must be fp16.
+ * ------------------------------------------------------------------------ */
+
+typedef struct q4_gemm_desc {
+    int M;                     /* tokens: rows of X and Y, >= 0 */
+    const uint16_t *X;         /* fp16 [M][K], K = w.K; 16-byte aligned */
+    q4_linear w;               /* the [N][K] matrix (PLAIN) or the gate matrix (GLU) */
+    q4_linear up;              /* GLU: the up matrix, same N and K; ignored in PLAIN */
+    q4_gemv_mode mode;         /* PLAIN: Y = X W^T; GLU: Y = fp16(SiLU(X Wg^T) * (X Wu^T)) */
+    q4_dtype out_dtype;        /* GLU requires Q4_F16 */
+    void *Y;                   /* [M][N] */
+    const uint16_t *residual;  /* PLAIN with fp16 output only: Y = fp16(residual + X W^T),
+                                  fp16 [M][N], may be the same buffer as Y; NULL = none */
+} q4_gemm_desc;
+
+/* Y = X W^T on the tensor cores.  N must be a multiple of 128 (else
+ * Q4_ERR_UNSUPPORTED); the shared-memory limit on K is that of q4_moe_gemm
+ * (K above 2752 in GLU mode or 3712 in PLAIN mode returns
+ * Q4_ERR_UNSUPPORTED).  Wq, scales, biases and X must be 16-byte aligned. */
+q4_status q4_gemm(const q4_gemm_desc *desc, q4_stream_t stream);
+
+/* Workspace bytes q4_prefill needs with chunks of `chunk` tokens (0 if the
+ * table is malformed). */
+size_t q4_prefill_workspace_bytes(const q4_layer_table *table, int chunk);
+
+/* Prefill of T prompt tokens through the layer stack of `table`, `chunk`
+ * tokens at a time, with the per-token dataflow of q4_decode_step (section 3):
+ * per chunk and layer, an RMSNorm kernel writes n = fp16(rms(h) * attn_norm)
+ * (the MMA takes fp16 operands, so n is stored in fp16 where the decode GEMV
+ * keeps it in fp32), q, k, v = GEMMs of n, h' = fp16(h + Wo q), n' from h'
+ * likewise, act = GLU GEMM of n', h = fp16(h' + Wdown act).
+ * h: fp16 [T][hidden], 16-byte aligned; on entry the prompt's activations, on
+ * return the final h (updated in place, chunk by chunk).  logits: [vocab] in
+ * table->logits_dtype for the LAST token, = Wlm (rms(h[T-1]) * final_norm)
+ * by the decode GEMV; NULL = none.  workspace: device, 256-byte aligned,
+ * >= q4_prefill_workspace_bytes(table, chunk) bytes; after the call it holds
+ * the last chunk's n', q, k, v and act (fp16 [chunk][width] each, in that
+ * order, each slice 256-byte aligned).  Every output width of the stack
+ * except lm_head must be a multiple of 128 (else Q4_ERR_UNSUPPORTED), and the
+ * GEMM's K limit applies.  Uses table->layers, hidden, norm_eps, lm_head,
+ * final_norm and logits_dtype; ignores M, workspace, flags and plan.
+ * chunk >= 1, T >= 0; allocates nothing. */
+q4_status q4_prefill(const q4_layer_table *table, uint16_t *h, int T, int chunk, void *logits,
+                     void *workspace, size_t workspace_bytes, q4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

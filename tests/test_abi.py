@@ -58,7 +58,9 @@ def test_struct_layouts_match_c(tmp_path):
 #define O(T, f) printf(#T "." #f " %zu\\n", offsetof(T, f));
 int main(void) {
   P(q4_segment) P(q4_gemv_desc) P(q4_linear) P(q4_layer_weights) P(q4_layer_table)
-  P(q4_decode_buffers_t) P(q4_moe_desc)
+  P(q4_decode_buffers_t) P(q4_moe_desc) P(q4_gemm_desc)
+  O(q4_gemm_desc, X) O(q4_gemm_desc, w) O(q4_gemm_desc, up) O(q4_gemm_desc, mode) O(q4_gemm_desc, Y)
+  O(q4_gemm_desc, residual)
   O(q4_gemv_desc, seg) O(q4_gemv_desc, out_dtype) O(q4_gemv_desc, mode)
   O(q4_segment, y) O(q4_segment, residual)
   O(q4_layer_table, layers) O(q4_layer_table, lm_head) O(q4_layer_table, workspace)
@@ -75,7 +77,8 @@ int main(void) {
                                                           check=True).stdout.split("\n") if ln)
     S = {"q4_segment": q4.q4_segment, "q4_gemv_desc": q4.q4_gemv_desc, "q4_linear": q4.q4_linear,
          "q4_layer_weights": q4.q4_layer_weights, "q4_layer_table": q4.q4_layer_table,
-         "q4_decode_buffers_t": q4.q4_decode_buffers_t, "q4_moe_desc": q4.q4_moe_desc}
+         "q4_decode_buffers_t": q4.q4_decode_buffers_t, "q4_moe_desc": q4.q4_moe_desc,
+         "q4_gemm_desc": q4.q4_gemm_desc}
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")
@@ -156,6 +159,27 @@ def test_decode_table_validation_and_workspace(L):
     assert L.q4_decode_workspace_bytes(ctypes.byref(t3.t)) == 0
     # A step without a workspace fails on the host.
     assert L.q4_decode_step(ctypes.byref(t.t), FAKE, FAKE, None) == -1
+
+
+def test_gemm_and_prefill_validation(L):
+    d = q4.q4_gemm_desc()
+    assert L.q4_gemm(None, None) == -1
+    d.M, d.X, d.Y = 4, FAKE, FAKE
+    d.w = q4.q4_linear(FAKE, FAKE, FAKE, 128, 64)
+    d.mode, d.out_dtype = q4.Q4_GEMV_GLU, q4.Q4_F16
+    assert L.q4_gemm(ctypes.byref(d), None) == -1          # GLU without the up matrix
+    d.up = q4.q4_linear(FAKE, FAKE, FAKE, 256, 64)
+    assert L.q4_gemm(ctypes.byref(d), None) == -1          # gate and up differ
+    layer = {"q": lin(128, 64), "k": lin(128, 64), "v": lin(128, 64), "o": lin(64, 128), "gate": lin(256, 64),
+             "up": lin(256, 64), "down": lin(64, 256)}
+    t = q4.LayerTable([layer], lin(100, 64), hidden=64, M=1)
+    n8 = q4.q4_prefill_workspace_bytes(t, 8)
+    # n [8][64], q [8][128], k, v [8][128], act [8][256] fp16, each slice rounded to 256 B
+    assert n8 == 1024 + 2048 + 2048 + 2048 + 4096
+    assert L.q4_prefill_workspace_bytes(ctypes.byref(t.t), 0) == 0
+    assert L.q4_prefill(ctypes.byref(t.t), FAKE, 4, 0, None, FAKE, n8, None) == -1      # chunk 0
+    assert L.q4_prefill(ctypes.byref(t.t), FAKE, 4, 16, None, FAKE * 256, n8, None) == -1  # workspace too small
+    assert L.q4_prefill(ctypes.byref(t.t), FAKE, -1, 8, None, FAKE * 256, n8, None) == -1
 
 
 def test_moe_validation(L):
