@@ -50,8 +50,8 @@ namespace q4g {
 constexpr int kTN = 128;          // tokens per unit (MMA N, max)
 constexpr int kRows = 128;        // weight rows per unit (MMA M)
 constexpr int kKS = 64;           // K per step (one swizzle atom row of fp16, one Q4 group)
-constexpr int kInStages = 3;      // codes + X ring
-constexpr int kAStages = 2;       // dequantised A ring
+constexpr int kMaxInStages = 8;   // codes + X ring (stage count set per launch)
+constexpr int kMaxAStages = 4;    // dequantised A ring (stage count set per launch)
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kUpMmaWarp = 2 + kDeqWarps + kEpiWarps;  // 14
@@ -62,9 +62,10 @@ constexpr uint32_t kTmemCols = 512;   // 2 accumulator buffers x (gate + up) x 1
 
 constexpr uint32_t kCodesBytes = kRows * 32;         // one matrix, one K step
 constexpr uint32_t kXBytes = kTN * kKS * 2;          // 16 KB
-constexpr uint32_t kInStageBytes = 2 * kCodesBytes + kXBytes;  // 24 KB, X at offset 8 KB (1024-aligned)
 constexpr uint32_t kATileBytes = kRows * kKS * 2;    // 16 KB
-constexpr uint32_t kAStageBytes = 2 * kATileBytes;
+// An input stage holds one K step's codes of each matrix, then X (at a
+// 1024-byte multiple, as the 128-byte swizzle needs): 20 KB plain, 24 KB GLU.
+// An A stage holds one dequantised tile per matrix: 16 KB plain, 32 KB GLU.
 
 struct Params {
     const uint16_t* scales;
@@ -76,14 +77,17 @@ struct Params {
     void* Y;
     int E, N, K, R, rows_e, up_off, nmat, glu, out_f16;
     int n_tiles, nK, G;
+    int in_stages, a_stages;       // ring depths (the rest of shared memory, see launch_grouped)
+    uint32_t in_bytes, a_bytes;    // bytes per input / A stage
+    uint32_t x_off;                // X's offset in an input stage
     uint32_t sb_bytes;   // private per-thread scale/bias slots
     uint32_t stg_bytes;  // staging buffer: the unit's scale and bias blocks
     int* err;
 };
 
 struct Smem {
-    uint64_t in_full[kInStages], in_empty[kInStages];
-    uint64_t a_full[kAStages], a_empty[kAStages];
+    uint64_t in_full[kMaxInStages], in_empty[kMaxInStages];
+    uint64_t a_full[kMaxAStages], a_empty[kMaxAStages];
     uint64_t acc_full[2], acc_empty[2];
     uint64_t sb_full, sb_empty;  // staging buffer of the unit's scales and biases
     uint64_t drain;  // completion probe for in-flight MMAs on the abort path
@@ -150,6 +154,19 @@ __device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
     return d;
 }
 
+// Position in a ring of n stages: the stage index and how often the ring has
+// wrapped (whose low bit is the mbarrier phase parity), advanced without a
+// division (the stage counts are launch parameters).
+struct RingPos {
+    int s = 0, r = 0;
+    __device__ __forceinline__ void next(int n) {
+        if (++s == n) {
+            s = 0;
+            ++r;
+        }
+    }
+};
+
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_bar(Smem& sm, uint64_t& bar, uint32_t parity, int* err) {
     if (sm.abort) return false;
@@ -208,19 +225,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // 1024-byte alignment for the swizzled tiles.
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* in_ring = base;
-    uint8_t* a_ring = in_ring + kInStages * kInStageBytes;
-    uint32_t* sb = reinterpret_cast<uint32_t*>(a_ring + kAStages * kAStageBytes);
+    uint8_t* a_ring = in_ring + (size_t)p.in_stages * p.in_bytes;
+    uint32_t* sb = reinterpret_cast<uint32_t*>(a_ring + (size_t)p.a_stages * p.a_bytes);
+    const int IS = p.in_stages, AS = p.a_stages;
     uint8_t* stg = reinterpret_cast<uint8_t*>(sb) + p.sb_bytes;
     Smem& sm = *reinterpret_cast<Smem*>(stg + p.stg_bytes);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     if (threadIdx.x == 0) {
-        for (int i = 0; i < kInStages; ++i) {
+        for (int i = 0; i < IS; ++i) {
             q4d::mbar_init(q4d::smem_addr(&sm.in_full[i]), 1);
             q4d::mbar_init(q4d::smem_addr(&sm.in_empty[i]), kDeqWarps + p.nmat);
         }
-        for (int i = 0; i < kAStages; ++i) {
+        for (int i = 0; i < AS; ++i) {
             q4d::mbar_init(q4d::smem_addr(&sm.a_full[i]), kDeqWarps);
             q4d::mbar_init(q4d::smem_addr(&sm.a_empty[i]), p.nmat);
         }
@@ -266,6 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ TMA
         if (lane == 0) {
             int it = 0, uu = 0, staged = 0;
+            RingPos ip;
             const uint32_t blk = (uint32_t)kRows * (uint32_t)p.G * 2u;  // one matrix's scales (or biases) of a unit
             for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++uu) {
                 const Unit un = decode_unit(sm, p, u);
@@ -285,20 +304,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ++staged;
                 }
                 for (int ks = 0; ks < nK; ++ks, ++it) {
-                    const int s = it % kInStages;
-                    if (it >= kInStages && !wait_bar(sm, sm.in_empty[s], ((it / kInStages) - 1) & 1, p.err)) break;
-                    uint8_t* st = in_ring + s * kInStageBytes;
+                    const int s = ip.s;
+                    if (ip.r > 0 && !wait_bar(sm, sm.in_empty[s], (ip.r - 1) & 1, p.err)) break;
+                    uint8_t* st = in_ring + (size_t)s * p.in_bytes;
                     const uint32_t fb = q4d::smem_addr(&sm.in_full[s]);
                     q4d::mbar_arrive_expect_tx(fb, p.nmat * kCodesBytes + kXBytes);
                     tma_load_2d(q4d::smem_addr(st), &tmW, ks * 32, wrow, fb);
                     if (p.glu) tma_load_2d(q4d::smem_addr(st + kCodesBytes), &tmWu, ks * 32, wrow_u, fb);
-                    tma_load_2d(q4d::smem_addr(st + 2 * kCodesBytes), &tmX, ks * kKS, un.r0, fb);
+                    tma_load_2d(q4d::smem_addr(st + p.x_off), &tmX, ks * kKS, un.r0, fb);
+                    ip.next(IS);
                 }
             }
             if (sm.abort) {
                 // let this thread's last copies land before the CTA can exit
-                for (int j = (it > kInStages ? it - kInStages : 0); j < it; ++j)
-                    q4d::mbar_wait(q4d::smem_addr(&sm.in_full[j % kInStages]), (j / kInStages) & 1, nullptr);
+                for (int j = (it > IS ? it - IS : 0); j < it; ++j)
+                    q4d::mbar_wait(q4d::smem_addr(&sm.in_full[j % IS]), (j / IS) & 1, nullptr);
                 if (staged > 0) q4d::mbar_wait(q4d::smem_addr(&sm.sb_full), (staged - 1) & 1, nullptr);
             }
         }
@@ -308,6 +328,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int mi = warp == 1 ? 0 : 1;
         if (lane == 0 && mi < p.nmat) {
             int it = 0, acc_it = 0;
+            RingPos ip, ap;
             for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++acc_it) {
                 const Unit un = decode_unit(sm, p, u);
                 const int npad = ((un.tn + 15) / 16) * 16;
@@ -318,15 +339,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d0 = tmem + (uint32_t)(buf * 2 * kTN);
                 bool ok = true;
                 for (int ks = 0; ks < nK; ++ks, ++it) {
-                    const int s = it % kInStages, a = it % kAStages;
-                    if (!wait_bar(sm, sm.in_full[s], (it / kInStages) & 1, p.err) ||
-                        !wait_bar(sm, sm.a_full[a], (it / kAStages) & 1, p.err)) {
+                    const int s = ip.s, a = ap.s;
+                    if (!wait_bar(sm, sm.in_full[s], ip.r & 1, p.err) || !wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t xs = q4d::smem_addr(in_ring + s * kInStageBytes + 2 * kCodesBytes);
-                    const uint32_t as = q4d::smem_addr(a_ring + a * kAStageBytes);
+                    const uint32_t xs = q4d::smem_addr(in_ring + (size_t)s * p.in_bytes + p.x_off);
+                    const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
                     {
                         // K-chunk kk advances both descriptors' start address by 32 bytes
                         const uint64_t ad = sw128_desc(as + mi * kATileBytes), xd = sw128_desc(xs);
@@ -337,6 +357,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     mma_commit(q4d::smem_addr(&sm.in_empty[s]));
                     mma_commit(q4d::smem_addr(&sm.a_empty[a]));
+                    ip.next(IS);
+                    ap.next(AS);
                 }
                 if (!ok) break;
                 mma_commit(q4d::smem_addr(&sm.acc_full[buf]));
@@ -359,6 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint16_t* sp = reinterpret_cast<const uint16_t*>(stg + (2 * m) * blk) + (size_t)row * G;
         const uint16_t* bp = reinterpret_cast<const uint16_t*>(stg + (2 * m + 1) * blk) + (size_t)row * G;
         int it = 0, uu = 0;
+        RingPos ip, ap;
         for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++uu) {
             // this unit's scales and biases, from the staging buffer into private slots
             if (!__all_sync(0xffffffffu, wait_bar(sm, sm.sb_full, uu & 1, p.err))) {
@@ -381,16 +404,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&sm.sb_empty));
             bool ok = true;
             for (int ks = 0; ks < nK; ++ks, ++it) {
-                const int s = it % kInStages, a = it % kAStages;
-                bool w = wait_bar(sm, sm.in_full[s], (it / kInStages) & 1, p.err);
-                if (w && it >= kAStages) w = wait_bar(sm, sm.a_empty[a], ((it / kAStages) - 1) & 1, p.err);
+                const int s = ip.s, a = ap.s;
+                bool w = wait_bar(sm, sm.in_full[s], ip.r & 1, p.err);
+                if (w && ap.r > 0) w = wait_bar(sm, sm.a_empty[a], (ap.r - 1) & 1, p.err);
                 if (!__all_sync(0xffffffffu, w)) {
                     sm.abort = 1;
                     ok = false;
                     break;
                 }
-                const uint8_t* st = in_ring + s * kInStageBytes;
-                uint8_t* at = a_ring + a * kAStageBytes;
+                const uint8_t* st = in_ring + (size_t)s * p.in_bytes;
+                uint8_t* at = a_ring + (size_t)a * p.a_bytes;
                 const int w0 = p.glu ? 0 : part * 4, nw = p.glu ? 8 : 4;
                 const uint32_t sbv = my_sb[ks];
                 const __half sh = __ushort_as_half((uint16_t)(sbv & 0xFFFF));
@@ -413,6 +436,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q4d::mbar_arrive(q4d::smem_addr(&sm.in_empty[s]));
                     q4d::mbar_arrive(q4d::smem_addr(&sm.a_full[a]));
                 }
+                ip.next(IS);
+                ap.next(AS);
             }
             if (!ok) break;
         }
@@ -602,10 +627,26 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
     p.err = dev->err_word;
 
-    const size_t smem = 1024 + (size_t)q4g::kInStages * q4g::kInStageBytes + (size_t)q4g::kAStages * q4g::kAStageBytes +
-                        p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
-    if (smem > (size_t)dev->smem_optin)
-        return fail(Q4_ERR_UNSUPPORTED, "K=%d needs %zu bytes of shared memory", a.K, smem);
+    // Rings: whatever shared memory the scale/bias buffers leave, A ring up to
+    // 4 stages (3 in GLU mode, whose stages are twice the size), input ring
+    // up to 8; at least 2 of each.
+    p.x_off = (uint32_t)p.nmat * q4g::kCodesBytes;
+    p.in_bytes = p.x_off + q4g::kXBytes;
+    p.a_bytes = (uint32_t)p.nmat * q4g::kATileBytes;
+    const size_t fixed = 1024 + (size_t)p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
+    const size_t avail = (size_t)dev->smem_optin > fixed ? (size_t)dev->smem_optin - fixed : 0;
+    int as = glu ? 3 : q4g::kMaxAStages, is = 0;
+    for (; as >= 2; --as) {
+        const size_t left = avail > (size_t)as * p.a_bytes ? avail - (size_t)as * p.a_bytes : 0;
+        is = (int)(left / p.in_bytes);
+        if (is > q4g::kMaxInStages) is = q4g::kMaxInStages;
+        if (is >= 4 || (as == 2 && is >= 2)) break;
+    }
+    if (as < 2 || is < 2)
+        return fail(Q4_ERR_UNSUPPORTED, "K=%d: its scale/bias buffers leave no room for two pipeline stages", a.K);
+    p.in_stages = is;
+    p.a_stages = as;
+    const size_t smem = fixed + (size_t)is * p.in_bytes + (size_t)as * p.a_bytes;
 
     CUtensorMap tmW, tmWu, tmX;
     const uint64_t wrows = (uint64_t)a.E * rows_e;

@@ -347,9 +347,9 @@ typedef struct q4_moe_desc {
  * Runs on the tensor cores (tcgen05, fp16 x fp16 -> fp32), weights
  * dequantised to fp16 in shared memory, never in global memory.
  * N must be a multiple of 128 (else Q4_ERR_UNSUPPORTED); Wq, scales, biases
- * and X must be 16-byte aligned (else Q4_ERR_MISALIGNED); a K whose tiles do
- * not fit in shared memory (with 227 KB per block: K above 2752 in GLU mode,
- * 3712 in PLAIN mode) returns
+ * and X must be 16-byte aligned (else Q4_ERR_MISALIGNED); a K whose scale/bias
+ * buffers leave no room for two pipeline stages in shared memory (with 227 KB
+ * per block: K above 3520 in GLU mode, 6464 in PLAIN mode) returns
  * Q4_ERR_UNSUPPORTED. */
 q4_status q4_moe_gemm(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                       const uint16_t *X, const int32_t *expert_ids, const int32_t *offsets,
@@ -388,7 +388,7 @@ typedef struct q4_gemm_desc {
 
 /* Y = X W^T on the tensor cores.  N must be a multiple of 128 (else
  * Q4_ERR_UNSUPPORTED); the shared-memory limit on K is that of q4_moe_gemm
- * (K above 2752 in GLU mode or 3712 in PLAIN mode returns
+ * (K above 3520 in GLU mode or 6464 in PLAIN mode returns
  * Q4_ERR_UNSUPPORTED).  Wq, scales, biases and X must be 16-byte aligned. */
 q4_status q4_gemm(const q4_gemm_desc *desc, q4_stream_t stream);
 
