@@ -667,8 +667,13 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (a.offsets)
         q4g::check_routing_kernel<<<(a.R + 255) / 256 < dev->sms ? (a.R + 255) / 256 : dev->sms, 256, 0, s>>>(
             a.expert_ids, a.offsets, a.E, a.R, dev->err_word);
-    cudaError_t e = cudaFuncSetAttribute(q4g::q4_moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
+    static int configured_smem[64] = {0};  // per device: the largest dynamic size set so far
+    cudaError_t e = cudaSuccess;
+    if (dev->device < 0 || dev->device >= 64 || (int)smem > configured_smem[dev->device]) {
+        e = cudaFuncSetAttribute(q4g::q4_moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
+        if (dev->device >= 0 && dev->device < 64) configured_smem[dev->device] = (int)smem;
+    }
     q4g::q4_moe_gemm_kernel<<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
