@@ -312,6 +312,80 @@ def prefill(layers, lm_head, x, final_norm=None, eps: float = DEFAULT_EPS):
     return h, y, A
 
 
+# ------------------------------------------------------- decode attention ---
+
+DEFAULT_ROPE_THETA = 1.0e6
+
+
+def rope(x, pos: int, head_dim: int, theta: float = DEFAULT_ROPE_THETA):
+    """Rotary position embedding of every head of x [..., H*head_dim] at one
+    position, rotate-half form: for i < d/2 the pair (x_i, x_{i+d/2}) turns by
+    pos * theta^(-2i/d).  fp64."""
+    x = np.asarray(x, dtype=np.float64)
+    d = head_dim
+    xs = x.reshape(x.shape[:-1] + (-1, d))
+    i = np.arange(d // 2, dtype=np.float64)
+    ang = pos * theta ** (-2.0 * i / d)
+    c, s = np.cos(ang), np.sin(ang)
+    lo, hi = xs[..., : d // 2], xs[..., d // 2:]
+    out = np.concatenate([lo * c - hi * s, hi * c + lo * s], axis=-1)
+    return out.reshape(x.shape)
+
+
+def attention(q, k_cache, v_cache, n: int, head_dim: int, pos: int, theta: float = DEFAULT_ROPE_THETA):
+    """Decode attention of one token: q [Hq*d] (fp16 values, not yet rotated)
+    against positions 0..n-1 of the caches [Hkv, max_seq, d] (keys stored
+    rotated).  Query head h reads key/value head h // (Hq / Hkv).  Returns
+    a [Hq*d] and A [Hq*d] = sum_j p_j |v_j| (fp64)."""
+    d = head_dim
+    qr = rope(q, pos, d, theta).reshape(-1, d)
+    Hq, Hkv = qr.shape[0], k_cache.shape[0]
+    g = Hq // Hkv
+    a = np.empty((Hq, d))
+    A = np.empty((Hq, d))
+    for h in range(Hq):
+        K = k_cache[h // g, :n].astype(np.float64)
+        V = v_cache[h // g, :n].astype(np.float64)
+        s = K @ qr[h] / np.sqrt(d)
+        w = np.exp(s - s.max())
+        w /= w.sum()
+        a[h] = w @ V
+        A[h] = w @ np.abs(V)
+    return a.reshape(-1), A.reshape(-1)
+
+
+def decode_layer_attn(layer, h, k_cache, v_cache, pos: int, head_dim: int, theta: float = DEFAULT_ROPE_THETA,
+                      eps: float = DEFAULT_EPS):
+    """decode_layer with attention in place of the stand-in a := q (BaseRT
+    §3.3 lists RoPE and attention among the decode kernels): the new key
+    (rotated) and value are written to position `pos` of the caches (fp16,
+    in place), a = attention over positions 0..pos, rounded to fp16, feeds o."""
+    qkv = decode_qkv(layer, h, eps=eps)
+    q = fp16(qkv["q"][0])[0]
+    k = fp16(qkv["k"][0])[0]
+    v = fp16(qkv["v"][0])[0]
+    Hkv = k_cache.shape[0]
+    k_cache[:, pos] = fp16(rope(k, pos, head_dim, theta)).reshape(Hkv, head_dim)
+    v_cache[:, pos] = v.reshape(Hkv, head_dim)
+    a = fp16(attention(q, k_cache, v_cache, pos + 1, head_dim, pos, theta)[0])[None, :]
+    hm = fp16(decode_o(layer, a, h)[0])
+    act = fp16(decode_glu(layer, hm, eps=eps)[4])
+    ho = fp16(decode_down(layer, act, hm)[0])
+    return {"q": q, "k": k, "v": v, "a": a, "h_mid": hm, "act": act, "h": ho}
+
+
+def decode_step_attn(layers, lm_head, x, caches, pos: int, head_dim: int, theta: float = DEFAULT_ROPE_THETA,
+                     final_norm=None, eps: float = DEFAULT_EPS):
+    """One decode step of one sequence with attention: x fp16 [1, hidden];
+    caches = [(k_cache, v_cache)] per layer, updated at `pos`.  Returns
+    (logits [1, vocab], A, final h)."""
+    h = np.atleast_2d(x).astype(np.float16)
+    for layer, (kc, vc) in zip(layers, caches):
+        h = decode_layer_attn(layer, h, kc, vc, pos, head_dim, theta, eps)["h"]
+    y, A = decode_logits(lm_head, h, final_norm, eps=eps)
+    return y, A, h
+
+
 # --------------------------------------------------------------------- MoE ---
 
 def moe_route(logits, topk: int):
