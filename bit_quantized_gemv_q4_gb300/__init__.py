@@ -28,6 +28,7 @@ LIB_PATH = os.path.join(HERE, "libq4gb300.so")
 Q4_F32, Q4_F16 = 0, 1
 Q4_GEMV_PLAIN, Q4_GEMV_GLU = 0, 1
 Q4_DECODE_NO_GRAPH, Q4_DECODE_NO_PDL, Q4_DECODE_TAGGED, Q4_DECODE_PERSISTENT = 1, 2, 4, 8
+Q4_DECODE_ATTENTION = 16
 Q4_MAX_SEGMENTS = 4
 
 STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q4_ERR_MISALIGNED",
@@ -39,7 +40,7 @@ EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status"
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
            "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
            "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine", "q4_gemm", "q4_prefill_workspace_bytes",
-           "q4_prefill"]
+           "q4_prefill", "q4_attention_workspace_bytes", "q4_attention"]
 
 
 class Q4Error(RuntimeError):
@@ -70,22 +71,29 @@ class q4_linear(ctypes.Structure):
 
 class q4_layer_weights(ctypes.Structure):
     _fields_ = [(n, q4_linear) for n in ("q", "k", "v", "o", "gate", "up", "down")] + [
-        ("attn_norm", vp), ("ffn_norm", vp)]
+        ("attn_norm", vp), ("ffn_norm", vp), ("k_cache", vp), ("v_cache", vp)]
 
 
 class q4_layer_table(ctypes.Structure):
     _fields_ = [("n_layers", i32), ("hidden", i32), ("M", i32), ("layers", ctypes.POINTER(q4_layer_weights)),
                 ("lm_head", q4_linear), ("final_norm", vp), ("norm_eps", ctypes.c_float),
                 ("logits_dtype", i32), ("workspace", vp),
-                ("workspace_bytes", ctypes.c_size_t), ("flags", i32), ("plan", vp)]
+                ("workspace_bytes", ctypes.c_size_t), ("flags", i32), ("plan", vp),
+                ("head_dim", i32), ("max_seq", i32), ("rope_theta", ctypes.c_float), ("pos", vp)]
 
 
 class q4_decode_buffers_t(ctypes.Structure):
-    _fields_ = [(n, vp) for n in ("h", "h_mid", "q", "k", "v", "act")]
+    _fields_ = [(n, vp) for n in ("h", "h_mid", "q", "k", "v", "act", "a")]
 
 
 class q4_moe_desc(ctypes.Structure):
     _fields_ = [("E", i32), ("N", i32), ("K", i32), ("R", i32), ("mode", i32), ("out_dtype", i32)]
+
+
+class q4_attention_desc(ctypes.Structure):
+    _fields_ = [("q", vp), ("k", vp), ("v", vp), ("k_cache", vp), ("v_cache", vp), ("pos", vp),
+                ("n_q_heads", i32), ("n_kv_heads", i32), ("head_dim", i32), ("max_seq", i32),
+                ("rope_theta", ctypes.c_float), ("a", vp), ("workspace", vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class q4_gemm_desc(ctypes.Structure):
@@ -145,6 +153,10 @@ def lib() -> ctypes.CDLL:
         L.q4_prefill_workspace_bytes.argtypes = [ctypes.POINTER(q4_layer_table), i32]
         L.q4_prefill.restype = st
         L.q4_prefill.argtypes = [ctypes.POINTER(q4_layer_table), vp, i32, i32, vp, vp, ctypes.c_size_t, vp]
+        L.q4_attention_workspace_bytes.restype = ctypes.c_size_t
+        L.q4_attention_workspace_bytes.argtypes = [i32, i32, i32]
+        L.q4_attention.restype = st
+        L.q4_attention.argtypes = [ctypes.POINTER(q4_attention_desc), vp]
         _lib = L
     return _lib
 
@@ -230,8 +242,9 @@ class LayerTable:
     device tensors; ``lm_head`` likewise; ``final_norm`` optional."""
 
     def __init__(self, layers, lm_head, hidden: int, M: int, workspace=None, workspace_bytes: int = 0,
-                 logits_dtype=Q4_F32, flags: int = 0, final_norm=None, norm_eps: float = 0.0):
-        self._keep = (layers, lm_head, workspace, final_norm)
+                 logits_dtype=Q4_F32, flags: int = 0, final_norm=None, norm_eps: float = 0.0,
+                 head_dim: int = 0, max_seq: int = 0, rope_theta: float = 1.0e6, pos=None):
+        self._keep = (layers, lm_head, workspace, final_norm, pos)
         n = len(layers)
         self._arr = (q4_layer_weights * max(n, 1))()
         for i, d in enumerate(layers):
@@ -239,6 +252,8 @@ class LayerTable:
                 setattr(self._arr[i], nm, _linear(*d[nm]))
             self._arr[i].attn_norm = _ptr(d.get("attn_norm"))
             self._arr[i].ffn_norm = _ptr(d.get("ffn_norm"))
+            self._arr[i].k_cache = _ptr(d.get("k_cache"))
+            self._arr[i].v_cache = _ptr(d.get("v_cache"))
         t = q4_layer_table()
         t.n_layers, t.hidden, t.M = n, hidden, M
         t.layers = ctypes.cast(self._arr, ctypes.POINTER(q4_layer_weights))
@@ -247,10 +262,11 @@ class LayerTable:
         t.logits_dtype, t.flags = logits_dtype, flags
         t.workspace, t.workspace_bytes = _ptr(workspace), workspace_bytes
         t.plan = None
+        t.head_dim, t.max_seq, t.rope_theta, t.pos = head_dim, max_seq, rope_theta, _ptr(pos)
         self.t = t
 
     def set_workspace(self, workspace, nbytes: int):
-        self._keep = self._keep[:2] + (workspace, self._keep[3])
+        self._keep = self._keep[:2] + (workspace,) + self._keep[3:]
         self.t.workspace, self.t.workspace_bytes = _ptr(workspace), nbytes
 
     def release(self):
@@ -274,7 +290,7 @@ def q4_decode_workspace_bytes(table: LayerTable) -> int:
 def q4_decode_buffers(table: LayerTable) -> dict:
     b = q4_decode_buffers_t()
     _check(lib().q4_decode_buffers(ctypes.byref(table.t), ctypes.byref(b)), "q4_decode_buffers")
-    return {n: getattr(b, n) for n in ("h", "h_mid", "q", "k", "v", "act")}
+    return {n: getattr(b, n) for n in ("h", "h_mid", "q", "k", "v", "act", "a")}
 
 
 def q4_decode_step(table: LayerTable, x, logits, stream=None):
@@ -347,3 +363,17 @@ def q4_prefill(table: LayerTable, h, T: int, chunk: int, logits, workspace, work
     """Chunked prefill: h fp16 [T, hidden] in place; logits of the last token (or None)."""
     _check(lib().q4_prefill(ctypes.byref(table.t), _ptr(h), T, chunk, _ptr(logits), _ptr(workspace),
                             workspace_bytes, _stream(stream)), "q4_prefill")
+
+
+# ------------------------------------------------------------- attention ---
+
+def q4_attention_workspace_bytes(n_q_heads: int, head_dim: int, max_seq: int) -> int:
+    return lib().q4_attention_workspace_bytes(n_q_heads, head_dim, max_seq)
+
+
+def q4_attention(q, k, v, k_cache, v_cache, pos, n_q_heads: int, n_kv_heads: int, head_dim: int, max_seq: int,
+                 a, workspace, workspace_bytes: int, rope_theta: float = 1.0e6, stream=None):
+    """One token's cache append and decode attention (pos: device int32, not advanced)."""
+    d = q4_attention_desc(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(pos), n_q_heads,
+                          n_kv_heads, head_dim, max_seq, rope_theta, _ptr(a), _ptr(workspace), workspace_bytes)
+    _check(lib().q4_attention(ctypes.byref(d), _stream(stream)), "q4_attention")

@@ -28,10 +28,13 @@ namespace {
 
 struct Dims {
     int hidden = 0, qN = 0, kvN = 0, ffn = 0, vocab = 0, M = 0, L = 0;
+    bool attn = false;  // Q4_DECODE_ATTENTION
+    int hd = 0, max_seq = 0;
 };
 
 struct Layout {
     size_t h = 0, h_mid = 0, q = 0, k = 0, v = 0, act = 0;
+    size_t a = 0, attn_ws = 0, attn_ws_bytes = 0;  // attention output and its scratch (Q4_DECODE_ATTENTION)
     size_t params = 0;  // per-stage kernel parameters of the persistent launch
     // tagged copies of the activations that later stages read, and counters
     size_t h_t = 0, hm_t = 0, q_t = 0, act_t = 0, ctr = 0, tagged_begin = 0, total = 0;
@@ -52,6 +55,9 @@ struct Plan {
     const void* x_key = nullptr;
     void* logits_key = nullptr;
     std::vector<q4_gemv_desc> stages;
+    std::vector<q4_attention_desc> attn;  // per layer, with Q4_DECODE_ATTENTION
+    int32_t* pos = nullptr;
+    float rope_theta = 0.f;
     std::vector<GemvTagged> tagged;  // per stage, used when tagged_mode or persistent
     bool tagged_mode = false;
     bool persistent = false;         // one cooperative launch per step
@@ -107,6 +113,35 @@ q4_status table_dims(const q4_layer_table* t, Dims* d) {
         if (d->ffn < w.gate.N) d->ffn = w.gate.N;
     }
     if ((st = check_linear(t->lm_head, 0, t->hidden, "lm_head", -1)) != Q4_OK) return st;
+    if (t->flags & Q4_DECODE_ATTENTION) {
+        if (t->M != 1) return fail(Q4_ERR_UNSUPPORTED, "Q4_DECODE_ATTENTION needs M = 1 (M=%d)", t->M);
+        if (t->flags & (Q4_DECODE_TAGGED | Q4_DECODE_PERSISTENT))
+            return fail(Q4_ERR_UNSUPPORTED, "Q4_DECODE_ATTENTION runs without TAGGED and PERSISTENT");
+        if (!t->pos) return fail(Q4_ERR_INVALID_ARG, "pos is NULL");
+        for (int l = 0; l < t->n_layers; ++l) {
+            const q4_layer_weights& w = t->layers[l];
+            q4_attention_desc a = {};
+            a.q = a.k = a.v = a.a = reinterpret_cast<uint16_t*>(16);  // shapes only
+            a.workspace = reinterpret_cast<void*>(256);
+            a.k_cache = w.k_cache;
+            a.v_cache = w.v_cache;
+            a.pos = t->pos;
+            a.head_dim = t->head_dim;
+            a.max_seq = t->max_seq;
+            a.rope_theta = t->rope_theta;
+            if (t->head_dim < 1 || w.q.N % t->head_dim || w.k.N % t->head_dim || w.v.N != w.k.N)
+                return fail(Q4_ERR_INVALID_ARG, "layer %d: q, k, v widths do not split into heads of %d", l,
+                            t->head_dim);
+            a.n_q_heads = w.q.N / t->head_dim;
+            a.n_kv_heads = w.k.N / t->head_dim;
+            a.workspace_bytes = attn_workspace_bytes(a.n_q_heads, a.head_dim, a.max_seq > 0 ? a.max_seq : 1);
+            if ((st = attn_validate(a)) != Q4_OK) return st;
+            if (w.o.K != w.q.N) return fail(Q4_ERR_INVALID_ARG, "layer %d: o.K != q.N", l);
+        }
+        d->attn = true;
+        d->hd = t->head_dim;
+        d->max_seq = t->max_seq;
+    }
     if (t->final_norm && !aligned16(t->final_norm)) return fail(Q4_ERR_MISALIGNED, "final_norm must be 16-byte aligned");
     if (!(t->norm_eps >= 0.f)) return fail(Q4_ERR_INVALID_ARG, "norm_eps must be >= 0");
     d->vocab = t->lm_head.N;
@@ -127,6 +162,11 @@ Layout layout_of(const Dims& d) {
     l.k = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
     l.v = take((size_t)d.M * (d.kvN > 0 ? d.kvN : 1));
     l.act = take((size_t)d.M * (d.ffn > 0 ? d.ffn : 1));
+    if (d.attn) {
+        l.a = take((size_t)d.M * (d.qN > 0 ? d.qN : 1));
+        l.attn_ws_bytes = attn_workspace_bytes(d.qN / d.hd, d.hd, d.max_seq);
+        l.attn_ws = take(l.attn_ws_bytes / 2 + 1);
+    }
     l.params = take((size_t)(4 * d.L + 1) * gemv_params_bytes() / 2);
     l.tagged_begin = off;
     l.h_t = take((size_t)d.M * d.hidden * 2);
@@ -158,6 +198,7 @@ void build_stages(Plan& p, const uint16_t* x, void* logits) {
     uint16_t* k = reinterpret_cast<uint16_t*>(ws + p.lay.k);
     uint16_t* v = reinterpret_cast<uint16_t*>(ws + p.lay.v);
     uint16_t* act = reinterpret_cast<uint16_t*>(ws + p.lay.act);
+    uint16_t* a_buf = reinterpret_cast<uint16_t*>(ws + p.lay.a);
     const int M = p.dims.M, H = p.dims.hidden;
     uint32_t* h_t = reinterpret_cast<uint32_t*>(ws + p.lay.h_t);
     uint32_t* hm_t = reinterpret_cast<uint32_t*>(ws + p.lay.hm_t);
@@ -177,6 +218,7 @@ void build_stages(Plan& p, const uint16_t* x, void* logits) {
     };
     p.stages.clear();
     p.tagged.clear();
+    p.attn.clear();
     for (int l = 0; l < p.dims.L; ++l) {
         // stages of layer l: 4l QKV, 4l+1 o, 4l+2 gate/up, 4l+3 down
         const uint32_t* h_in_t = l == 0 ? nullptr : h_t;  // layer 0 reads the caller's plain x
@@ -214,9 +256,27 @@ void build_stages(Plan& p, const uint16_t* x, void* logits) {
         d.seg[1] = seg_of(w.k, k, nullptr);
         d.seg[2] = seg_of(w.v, v, nullptr);
         p.stages.push_back(d);
-        // h' = h + Wo q
+        if (p.dims.attn) {
+            q4_attention_desc ad = {};
+            ad.q = q;
+            ad.k = k;
+            ad.v = v;
+            ad.k_cache = w.k_cache;
+            ad.v_cache = w.v_cache;
+            ad.pos = p.pos;
+            ad.head_dim = p.dims.hd;
+            ad.n_q_heads = w.q.N / p.dims.hd;
+            ad.n_kv_heads = w.k.N / p.dims.hd;
+            ad.max_seq = p.dims.max_seq;
+            ad.rope_theta = p.rope_theta;
+            ad.a = a_buf;
+            ad.workspace = ws + p.lay.attn_ws;
+            ad.workspace_bytes = p.lay.attn_ws_bytes;
+            p.attn.push_back(ad);
+        }
+        // h' = h + Wo a (a = q without attention)
         d = {};
-        d.M = M; d.K = w.o.K; d.x = q; d.ldx = w.o.K; d.out_dtype = Q4_F16; d.mode = Q4_GEMV_PLAIN;
+        d.M = M; d.K = w.o.K; d.x = p.dims.attn ? a_buf : q; d.ldx = w.o.K; d.out_dtype = Q4_F16; d.mode = Q4_GEMV_PLAIN;
         d.n_segments = 1;
         d.seg[0] = seg_of(w.o, hm, hin);
         p.stages.push_back(d);
@@ -248,7 +308,12 @@ q4_status enqueue_stages(Plan& p, cudaStream_t s) {
     for (size_t i = 0; i < p.stages.size(); ++i) {
         q4_status st = launch_gemv(p.stages[i], s, pdl && i > 0, true, p.tagged_mode ? &p.tagged[i] : nullptr);
         if (st != Q4_OK) return st;
+        // after layer l's QKV stage (stage 4l): append to the caches and attend
+        if (p.dims.attn && i % 4 == 0 && i / 4 < p.attn.size()) {
+            if ((st = attn_enqueue(p.attn[i / 4], s)) != Q4_OK) return st;
+        }
     }
+    if (p.dims.attn) return pos_advance(p.pos, s);
     return Q4_OK;
 }
 
@@ -476,6 +541,7 @@ q4_status q4_decode_buffers(const q4_layer_table* table, q4_decode_buffers_t* ou
     out->k = reinterpret_cast<uint16_t*>(ws + l.k);
     out->v = reinterpret_cast<uint16_t*>(ws + l.v);
     out->act = reinterpret_cast<uint16_t*>(ws + l.act);
+    out->a = d.attn ? reinterpret_cast<uint16_t*>(ws + l.a) : nullptr;
     return Q4_OK;
 }
 
@@ -509,6 +575,8 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
         p->workspace = table->workspace;
         p->workspace_bytes = table->workspace_bytes;
         p->flags = table->flags;
+        p->pos = table->pos;
+        p->rope_theta = table->rope_theta;
         p->tagged_mode = (table->flags & Q4_DECODE_TAGGED) != 0;
         for (int l = 0; l < d.L && p->tagged_mode; ++l) {
             const q4_layer_weights& w = table->layers[l];

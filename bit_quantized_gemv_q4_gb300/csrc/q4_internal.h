@@ -29,6 +29,12 @@ q4_status current_device(const DeviceInfo** out);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// ---- decode attention (q4_attn.cu) -----------------------------------------
+size_t attn_workspace_bytes(int n_q_heads, int head_dim, int max_seq);
+q4_status attn_validate(const q4_attention_desc& d);
+q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s);
+q4_status pos_advance(int32_t* pos, cudaStream_t s);
+
 // ---- dense GEMM on the grouped-GEMM kernel (q4_moe_gemm.cu) ---------------
 q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream);
 

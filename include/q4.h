@@ -188,8 +188,14 @@ q4_status q4_gemv_ex(const q4_gemv_desc *desc, q4_stream_t stream);
  *   act = fp16(SiLU(Wgate n') * (Wup n'))
  *   h   = fp16(h' + Wdown act)
  *
- * and finally logits = Wlm (rms(h) * final_norm) in logits_dtype.  Attention
- * and RoPE are not part of this matmul path.
+ * and finally logits = Wlm (rms(h) * final_norm) in logits_dtype.  By default
+ * q stands in for the attention output (the matmul path alone).  With
+ * Q4_DECODE_ATTENTION (M = 1), after the QKV stage the new key, rotated by
+ * RoPE at position p = *table->pos, and the new value are written to position
+ * p of the layer's caches, and a = fp16(attention of the RoPE-rotated q over
+ * positions 0..p) replaces q as the input of o (section 6 describes the
+ * attention); the step ends with *pos += 1.  A position outside
+ * [0, max_seq) latches Q4_ERR_DEVICE_CHECK and leaves the caches alone.
  *
  * The first call on a table validates it and plans the step.  By default
  * each stage is its own kernel launch: the first call captures them into a
@@ -232,6 +238,8 @@ typedef struct q4_layer_weights {
     q4_linear q, k, v, o, gate, up, down;
     const uint16_t *attn_norm; /* fp16 [hidden] RMSNorm weight before QKV; NULL = ones */
     const uint16_t *ffn_norm;  /* fp16 [hidden] RMSNorm weight before gate/up; NULL = ones */
+    uint16_t *k_cache;         /* Q4_DECODE_ATTENTION only: fp16 [k.N/head_dim][max_seq][head_dim] */
+    uint16_t *v_cache;         /* likewise for the values; both 16-byte aligned */
 } q4_layer_weights;
 
 #define Q4_DECODE_NO_GRAPH 1 /* launch the kernels directly each call (no capture) */
@@ -240,6 +248,9 @@ typedef struct q4_layer_weights {
                                  waiting for their predecessor grid to complete */
 #define Q4_DECODE_PERSISTENT 8 /* one persistent cooperative launch per step (see below);
                                   the three flags above then do not apply */
+#define Q4_DECODE_ATTENTION 16 /* decode attention over each layer's KV cache replaces the
+                                  a := q stand-in (see below); M must be 1, and
+                                  Q4_DECODE_TAGGED / Q4_DECODE_PERSISTENT are refused */
 
 typedef struct q4_layer_table {
     int n_layers;
@@ -254,6 +265,12 @@ typedef struct q4_layer_table {
     size_t workspace_bytes;
     int flags;  /* Q4_DECODE_* */
     void *plan; /* library-owned cache; zero-initialise, free with q4_layer_table_release */
+    /* Q4_DECODE_ATTENTION only: */
+    int head_dim;     /* 64 or 128; q.N and k.N = v.N are multiples, q heads a multiple of kv heads */
+    int max_seq;      /* cache length in positions */
+    float rope_theta; /* rotary base (> 1) */
+    int32_t *pos;     /* device int32: the position this step writes and attends up to; the step
+                         advances it by one after its last kernel */
 } q4_layer_table;
 
 /* Workspace bytes the table needs (0 if the table is malformed). */
@@ -267,6 +284,7 @@ typedef struct q4_decode_buffers_t {
     uint16_t *k;     /* [M][k.N] */
     uint16_t *v;     /* [M][v.N] */
     uint16_t *act;   /* [M][gate.N] last layer's SiLU(g)*u */
+    uint16_t *a;     /* [M][q.N] last layer's attention output (Q4_DECODE_ATTENTION), else NULL */
 } q4_decode_buffers_t;
 
 q4_status q4_decode_buffers(const q4_layer_table *table, q4_decode_buffers_t *out);
@@ -415,6 +433,41 @@ size_t q4_prefill_workspace_bytes(const q4_layer_table *table, int chunk);
  * chunk >= 1, T >= 0; allocates nothing. */
 q4_status q4_prefill(const q4_layer_table *table, uint16_t *h, int T, int chunk, void *logits,
                      void *workspace, size_t workspace_bytes, q4_stream_t stream);
+
+/* ------------------------------------------------------------------------ *
+ * 6. Decode attention of one token over a preallocated KV cache.
+ *
+ * BaseRT §3.3 lists RoPE, attention and normalisation among the decode
+ * kernels and §3.2 preallocates the KV cache; the pages print no formula.
+ * RoPE (rotate-half form): for i < d/2 the pair (x_i, x_{i+d/2}) of every
+ * head turns by p * theta^(-2i/d).  Query head h reads key/value head
+ * h / (Hq / Hkv).  a_h = sum_j softmax_j(q_h . k_j / sqrt(d)) v_j over
+ * positions j = 0..p, fp32 arithmetic, a stored in fp16.
+ * ------------------------------------------------------------------------ */
+
+typedef struct q4_attention_desc {
+    const uint16_t *q;   /* fp16 [Hq * head_dim]: this token's queries, not rotated */
+    const uint16_t *k;   /* fp16 [Hkv * head_dim]: its key, not rotated */
+    const uint16_t *v;   /* fp16 [Hkv * head_dim]: its value */
+    uint16_t *k_cache;   /* fp16 [Hkv][max_seq][head_dim]; position p receives the rotated key */
+    uint16_t *v_cache;   /* fp16 [Hkv][max_seq][head_dim]; position p receives v */
+    int32_t *pos;        /* device int32 p (read, not advanced); outside [0, max_seq) latches
+                            Q4_ERR_DEVICE_CHECK and nothing is written */
+    int n_q_heads, n_kv_heads;
+    int head_dim;        /* 64 or 128 */
+    int max_seq;
+    float rope_theta;    /* > 1 */
+    uint16_t *a;         /* fp16 [Hq * head_dim] out */
+    void *workspace;     /* device, 256-byte aligned, >= q4_attention_workspace_bytes */
+    size_t workspace_bytes;
+} q4_attention_desc;
+
+/* Scratch bytes for the per-chunk partial results (0 for bad sizes). */
+size_t q4_attention_workspace_bytes(int n_q_heads, int head_dim, int max_seq);
+
+/* Three kernels on `stream`: cache append, per-chunk attention, merge.  At
+ * most 8 query heads per kv head (else Q4_ERR_UNSUPPORTED). */
+q4_status q4_attention(const q4_attention_desc *desc, q4_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -60,7 +60,9 @@ int main(void) {
   P(q4_segment) P(q4_gemv_desc) P(q4_linear) P(q4_layer_weights) P(q4_layer_table)
   P(q4_decode_buffers_t) P(q4_moe_desc) P(q4_gemm_desc)
   O(q4_gemm_desc, X) O(q4_gemm_desc, w) O(q4_gemm_desc, up) O(q4_gemm_desc, mode) O(q4_gemm_desc, Y)
-  O(q4_gemm_desc, residual)
+  O(q4_gemm_desc, residual) P(q4_attention_desc) O(q4_attention_desc, rope_theta) O(q4_attention_desc, a)
+  O(q4_attention_desc, workspace_bytes) O(q4_layer_weights, k_cache) O(q4_layer_weights, v_cache)
+  O(q4_layer_table, head_dim) O(q4_layer_table, rope_theta) O(q4_layer_table, pos) O(q4_decode_buffers_t, a)
   O(q4_gemv_desc, seg) O(q4_gemv_desc, out_dtype) O(q4_gemv_desc, mode)
   O(q4_segment, y) O(q4_segment, residual)
   O(q4_layer_table, layers) O(q4_layer_table, lm_head) O(q4_layer_table, workspace)
@@ -78,7 +80,7 @@ int main(void) {
     S = {"q4_segment": q4.q4_segment, "q4_gemv_desc": q4.q4_gemv_desc, "q4_linear": q4.q4_linear,
          "q4_layer_weights": q4.q4_layer_weights, "q4_layer_table": q4.q4_layer_table,
          "q4_decode_buffers_t": q4.q4_decode_buffers_t, "q4_moe_desc": q4.q4_moe_desc,
-         "q4_gemm_desc": q4.q4_gemm_desc}
+         "q4_gemm_desc": q4.q4_gemm_desc, "q4_attention_desc": q4.q4_attention_desc}
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")
@@ -191,3 +193,37 @@ def test_moe_validation(L):
     assert L.q4_moe_gather(FAKE, 4, 12, FAKE, 8, FAKE, None) == -1
     assert L.q4_moe_gather(FAKE + 8, 4, 64, FAKE, 8, FAKE, None) == -3
     assert L.q4_moe_combine(FAKE, 0, 64, FAKE, FAKE, 4, 9, FAKE, 0, None) == -1
+
+
+def test_attention_validation(L):
+    # (max, sum) per head and 256-position chunk, then the partial outputs
+    assert L.q4_attention_workspace_bytes(16, 128, 4096) == 16 * 16 * 2 * 4 + 16 * 16 * 128 * 4
+    assert L.q4_attention_workspace_bytes(0, 128, 4096) == 0
+    assert L.q4_attention(None, None) == -1
+    d = q4.q4_attention_desc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 8, 128, 4096, 1e6, FAKE, FAKE * 256, 1 << 20)
+    bad = [("head_dim", 96, -2), ("n_kv_heads", 5, -1), ("n_kv_heads", 1, -2), ("rope_theta", 1.0, -1),
+           ("workspace_bytes", 100, -1), ("max_seq", 0, -1)]
+    for f, v, want in bad:
+        e = q4.q4_attention_desc.from_buffer_copy(d)
+        setattr(e, f, v)
+        assert L.q4_attention(ctypes.byref(e), None) == want, f
+    e = q4.q4_attention_desc.from_buffer_copy(d)
+    e.k_cache = FAKE + 8
+    assert L.q4_attention(ctypes.byref(e), None) == -3
+
+
+def test_decode_attention_table_validation(L):
+    layer = {"q": lin(128, 64), "k": lin(64, 64), "v": lin(64, 64), "o": lin(64, 128), "gate": lin(192, 64),
+             "up": lin(192, 64), "down": lin(64, 192), "k_cache": FAKE, "v_cache": FAKE}
+    t = q4.LayerTable([layer], lin(100, 64), hidden=64, M=1, flags=q4.Q4_DECODE_ATTENTION, head_dim=64,
+                      max_seq=32, pos=FAKE)
+    n = L.q4_decode_workspace_bytes(ctypes.byref(t.t))
+    plain = q4.q4_decode_workspace_bytes(q4.LayerTable([layer], lin(100, 64), hidden=64, M=1))
+    assert n > plain                                   # + the attention output and its scratch
+    for kw, frag in ((dict(M=2), b"M = 1"), (dict(head_dim=96), b"head"), (dict(pos=None), b"pos"),
+                     (dict(flags=q4.Q4_DECODE_ATTENTION | q4.Q4_DECODE_TAGGED), b"TAGGED")):
+        args = dict(hidden=64, M=1, flags=q4.Q4_DECODE_ATTENTION, head_dim=64, max_seq=32, pos=FAKE)
+        args.update(kw)
+        tb = q4.LayerTable([layer], lin(100, 64), **args)
+        assert L.q4_decode_workspace_bytes(ctypes.byref(tb.t)) == 0, kw
+        assert frag in L.q4_last_error(), (kw, L.q4_last_error())
