@@ -339,6 +339,55 @@ def dense_prefill(device, dl, dlm, shape, iters: int = 5, warmup: int = 3, cases
     return out
 
 
+def decode_attention(device, dl, dlm, shape, contexts=(1024, 4096), steps: int = 200, warmup: int = 10):
+    """Decode step with attention (Q4_DECODE_ATTENTION, M = 1): the weight
+    stream plus RoPE, KV-cache append and attention over `context` cached
+    positions (random fp16 cache contents; head_dim 128, so 16 query and 8
+    kv heads on the Qwen3-0.6B shape).  Graph replays back to back."""
+    import torch
+
+    import bit_quantized_gemv_q4_gb300 as q4
+    import q4synth
+    hd = 128
+    hkv = shape.kv // hd
+    out = {"shape": f"{shape.name}, head_dim {hd}, {shape.q // hd} q / {hkv} kv heads"}
+    max_seq = max(contexts) + steps + warmup + 1
+    gen = torch.Generator(device=device).manual_seed(77)
+    caches = [(torch.randn(hkv, max_seq, hd, device=device, generator=gen).half(),
+               torch.randn(hkv, max_seq, hd, device=device, generator=gen).half()) for _ in range(shape.n_layers)]
+    layers = [dict(d, k_cache=kc, v_cache=vc) for d, (kc, vc) in zip(dl, caches)]
+    pos = torch.zeros(1, dtype=torch.int32, device=device)
+    table = q4.LayerTable(layers, dlm, hidden=shape.hidden, M=1, flags=q4.Q4_DECODE_ATTENTION, head_dim=hd,
+                          max_seq=max_seq, pos=pos)
+    nws = q4.q4_decode_workspace_bytes(table)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    table.set_workspace(ws, nws)
+    x = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4244, 1, shape.hidden)).to(device)
+    logits = torch.empty(1, shape.vocab, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for ctx in contexts:
+        pos.fill_(ctx)
+        for _ in range(warmup):
+            q4.q4_decode_step(table, x, logits, stream)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            q4.q4_decode_step(table, x, logits, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if q4.q4_device_status(stream) != 0:
+            raise RuntimeError("device status after attention timing")
+        ms = e0.elapsed_time(e1) / steps
+        n_mid = ctx + warmup + steps / 2
+        kv_bytes = shape.n_layers * 2 * hkv * n_mid * hd * 2
+        byts = shape.weight_bytes_per_step() + kv_bytes
+        out[f"context={ctx}"] = {"ms": ms, "tok_per_s": 1000.0 / ms, "kv_bytes_per_step": kv_bytes,
+                                 "gbs": byts / (ms * 1e-3) / 1e9}
+    table.release()
+    return out
+
+
 def q8_lm_head(q4, device, M: int = 1):
     """The lm_head-shaped GEMV (N=151936, K=1024) with 8-bit codes: 8 warm-up
     launches, then 64 timed over 4 distinct weight copies (4 x 166 MB > L2)."""
@@ -420,7 +469,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head", "prefill"],
+    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head", "prefill", "attention"],
                     help="moe / lm_head: only the MoE prefill timings / the lm_head GEMV timing "
                          "(for profiling runs)")
     args = ap.parse_args()
@@ -505,6 +554,9 @@ def main():
     dl, dlm, host_model = make_model(shape, device)
     if args.section == "prefill":
         print(json.dumps({"dense_prefill": dense_prefill(device, dl, dlm, shape)}))
+        return
+    if args.section == "attention":
+        print(json.dumps({"decode_attention": decode_attention(device, dl, dlm, shape)}))
         return
     table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
     nws = q4.q4_decode_workspace_bytes(table)
@@ -598,6 +650,7 @@ def main():
         out["lm_head_gemv8"] = q8_lm_head(q4, device)
         out["moe_prefill"] = moe_prefill(device)
         out["dense_prefill"] = dense_prefill(device, dl, dlm, shape)
+        out["decode_attention"] = decode_attention(device, dl, dlm, shape)
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()

@@ -11,13 +11,17 @@
 //
 // GB300 design: attention of one token is a memory-bound pass over the cache
 // (2 x Hkv x d x 2 bytes per position), so it is split over positions
-// (flash-decoding): one CTA per (kv head, chunk of 256 positions) scores all
-// query heads of the group against the chunk's keys (a warp per position,
-// lanes across d, 8-byte loads), turns the scores into exp(s - max) in shared
-// memory, and accumulates the values (a thread per dimension, coalesced 2-byte
-// loads); a second kernel merges the chunks' (max, sum, partial output) per
-// head.  The rotation angle pos * theta^(-2i/d) and its sine and cosine are
-// computed in fp64 (a few operations per pair), the rotation itself in fp32.
+// (flash-decoding): one CTA per (kv head, chunk of 128 positions) brings the
+// chunk's keys and values into shared memory with two bulk copies (the
+// positions of a head are contiguous, 32 KB each at d = 128) on one mbarrier,
+// rotates the group's queries meanwhile, scores every query head of the group
+// (a warp per position, lanes across d), turns the scores into exp(s - max),
+// and accumulates the values (threads across d and positions, the partial
+// sums added in shared memory); a second kernel merges
+// the chunks' (max, sum, partial output) per head.  The rotation's sines and
+// cosines are computed once per step in fp64 (the angle pos * theta^(-2i/d)
+// reaches thousands of radians) by the first append kernel of the step into a
+// table the other kernels read; the rotations themselves are fp32.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -26,8 +30,8 @@
 
 namespace q4a {
 
-constexpr int kChunk = 256;   // positions per CTA
-constexpr int kThreads = 128;
+constexpr int kChunk = 128;   // positions per CTA
+constexpr int kThreads = 256;
 constexpr int kMaxGroup = 8;  // query heads per kv head
 
 __device__ __forceinline__ void rope_cs(int pos, int i, int d, double log2_theta, float& c, float& s) {
@@ -47,15 +51,25 @@ __device__ __forceinline__ bool pos_ok(int pos, int max_seq, int* err) {
 }
 
 // The new key, rotated, and the new value into position *pos of the caches.
-// Grid Hkv, block d/2: thread i turns the pair (i, i + d/2).
+// Grid Hkv, block d/2: thread i turns the pair (i, i + d/2).  With kTable the
+// sines and cosines are computed here (fp64) and block 0 stores them in `cs`
+// for the other kernels of the step; otherwise they are read from `cs`.
+template <bool kTable>
 __global__ void rope_append_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                                    uint16_t* __restrict__ kc, uint16_t* __restrict__ vc, const int32_t* pos_p, int d,
-                                   int max_seq, double log2_theta, int* err) {
+                                   int max_seq, double log2_theta, float2* cs, int* err) {
     const int h = blockIdx.x, i = threadIdx.x, half = d / 2;
     const int pos = *pos_p;
     if (!pos_ok(pos, max_seq, err)) return;
     float c, s;
-    rope_cs(pos, i, d, log2_theta, c, s);
+    if constexpr (kTable) {
+        rope_cs(pos, i, d, log2_theta, c, s);
+        if (h == 0) cs[i] = make_float2(c, s);
+    } else {
+        const float2 t = cs[i];
+        c = t.x;
+        s = t.y;
+    }
     const float lo = __half2float(__ushort_as_half(k[h * d + i]));
     const float hi = __half2float(__ushort_as_half(k[h * d + i + half]));
     const size_t base = ((size_t)h * max_seq + pos) * d;
@@ -65,70 +79,104 @@ __global__ void rope_append_kernel(const uint16_t* __restrict__ k, const uint16_
     vc[base + i + half] = v[h * d + i + half];
 }
 
+// Dynamic shared memory of the split kernel: the chunk's keys and values,
+// the rotated queries, the scores and the value pass's partial sums.
+constexpr size_t split_smem(int D) {
+    return (size_t)2 * kChunk * D * 2 + (size_t)kMaxGroup * D * 4 + (size_t)kMaxGroup * kChunk * 4 +
+           (size_t)kThreads * kMaxGroup * 4;
+}
+
 // One (kv head, chunk) of the attention: for each query head g of the group,
 // m = max score, l = sum exp(s - m), acc = sum exp(s - m) v over the chunk.
 template <int D>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const uint16_t* __restrict__ q,
                                                               const uint16_t* __restrict__ kc,
                                                               const uint16_t* __restrict__ vc, const int32_t* pos_p,
-                                                              int G, int max_seq, int n_splits, double log2_theta,
+                                                              int G, int max_seq, int n_splits,
+                                                              const float2* __restrict__ cs,
                                                               float* __restrict__ part_ml,
                                                               float* __restrict__ part_acc, int* err) {
-    __shared__ float qr[kMaxGroup][D];
-    __shared__ float sc[kMaxGroup][kChunk];
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);  // [kChunk][D]
+    uint16_t* vs = ks + kChunk * D;                    // [kChunk][D]
+    float* qr = reinterpret_cast<float*>(vs + kChunk * D);  // [kMaxGroup][D]
+    float* sc = qr + kMaxGroup * D;                         // [kMaxGroup][kChunk]
+    float* red = sc + kMaxGroup * kChunk;                   // [kThreads / D][kMaxGroup][D]
+    __shared__ __align__(8) uint64_t bar;
     const int kvh = blockIdx.x, split = blockIdx.y, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int pos = *pos_p;
     if (!pos_ok(pos, max_seq, err)) return;
     const int n = pos + 1, j0 = split * kChunk, j1 = min(j0 + kChunk, n), cnt = j1 - j0;
     const int h0 = kvh * G;
-    if (cnt <= 0) return;  // past the context: the combine step reads only the live chunks
-    // rotated queries, scaled by 1/sqrt(d)
+    if (cnt <= 0) return;  // past the context: the merge reads only the live chunks
+    const uint32_t b = q4d::smem_addr(&bar);
+    if (tid == 0) {
+        q4d::mbar_init(b, 1);
+        q4d::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0) {
+        const uint32_t bytes = (uint32_t)cnt * D * 2;
+        q4d::mbar_arrive_expect_tx(b, 2 * bytes);
+        q4d::bulk_g2s(q4d::smem_addr(ks), kc + ((size_t)kvh * max_seq + j0) * D, bytes, b);
+        q4d::bulk_g2s(q4d::smem_addr(vs), vc + ((size_t)kvh * max_seq + j0) * D, bytes, b);
+    }
+    // rotated queries, scaled by 1/sqrt(d), while the copies are in flight
     const float scale = rsqrtf((float)D);
     for (int t = tid; t < G * (D / 2); t += kThreads) {
         const int g = t / (D / 2), i = t % (D / 2);
-        float c, s;
-        rope_cs(pos, i, D, log2_theta, c, s);
+        const float2 r = cs[i];
         const float lo = __half2float(__ushort_as_half(q[(h0 + g) * D + i]));
         const float hi = __half2float(__ushort_as_half(q[(h0 + g) * D + i + D / 2]));
-        qr[g][i] = (lo * c - hi * s) * scale;
-        qr[g][i + D / 2] = (hi * c + lo * s) * scale;
+        qr[g * D + i] = (lo * r.x - hi * r.y) * scale;
+        qr[g * D + i + D / 2] = (hi * r.x + lo * r.y) * scale;
     }
-    __syncthreads();
+    // every thread waits (bounded) for the chunk; on expiry (latched in
+    // `err`) the block waits once more for its copies, then leaves
+    const bool late = !q4d::mbar_wait(b, 0, err);
+    if (__syncthreads_or(late)) {
+        q4d::mbar_wait(b, 0, nullptr);
+        return;
+    }
     // scores: a warp per position, lanes across d
     constexpr int E = D / 32;  // elements per lane (2 or 4)
-    const uint16_t* kbase = kc + (size_t)kvh * max_seq * D;
-    for (int j = j0 + warp; j < j1; j += kThreads / 32) {
+    for (int j = warp; j < cnt; j += kThreads / 32) {
         float kf[E];
         if constexpr (E == 4) {
-            const uint2 raw = *reinterpret_cast<const uint2*>(kbase + (size_t)j * D + lane * 4);
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-            const float2 b = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-            kf[0] = a.x; kf[1] = a.y; kf[2] = b.x; kf[3] = b.y;
+            const uint2 raw = *reinterpret_cast<const uint2*>(ks + j * D + lane * 4);
+            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+            const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+            kf[0] = x.x; kf[1] = x.y; kf[2] = y.x; kf[3] = y.y;
         } else {
-            const uint32_t raw = *reinterpret_cast<const uint32_t*>(kbase + (size_t)j * D + lane * 2);
-            const float2 a = __half22float2(*reinterpret_cast<const __half2*>(&raw));
-            kf[0] = a.x; kf[1] = a.y;
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(ks + j * D + lane * 2);
+            const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+            kf[0] = x.x; kf[1] = x.y;
         }
         for (int g = 0; g < G; ++g) {
             float acc = 0.f;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc = fmaf(qr[g][lane * E + e], kf[e], acc);
+            if constexpr (E == 4) {
+                const float4 qq = reinterpret_cast<const float4*>(qr + g * D)[lane];
+                acc = fmaf(qq.x, kf[0], fmaf(qq.y, kf[1], fmaf(qq.z, kf[2], qq.w * kf[3])));
+            } else {
+                const float2 qq = reinterpret_cast<const float2*>(qr + g * D)[lane];
+                acc = fmaf(qq.x, kf[0], qq.y * kf[1]);
+            }
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-            if (lane == 0) sc[g][j - j0] = acc;
+            if (lane == 0) sc[g * kChunk + j] = acc;
         }
     }
     __syncthreads();
     // per head: max, exp, sum (a warp per head)
     for (int g = warp; g < G; g += kThreads / 32) {
         float m = -INFINITY;
-        for (int j = lane; j < cnt; j += 32) m = fmaxf(m, sc[g][j]);
+        for (int j = lane; j < cnt; j += 32) m = fmaxf(m, sc[g * kChunk + j]);
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float l = 0.f;
         for (int j = lane; j < cnt; j += 32) {
-            const float p = expf(sc[g][j] - m);
-            sc[g][j] = p;
+            const float p = expf(sc[g * kChunk + j] - m);
+            sc[g * kChunk + j] = p;
             l += p;
         }
 #pragma unroll
@@ -140,21 +188,30 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const uint16_t* __
         }
     }
     __syncthreads();
-    // values: a thread per dimension
-    if (tid < D) {
-        float acc[kMaxGroup];
-#pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g) acc[g] = 0.f;
-        const uint16_t* vb = vc + (size_t)kvh * max_seq * D + (size_t)j0 * D + tid;
-        for (int j = 0; j < cnt; ++j) {
-            const float vv = __half2float(__ushort_as_half(vb[(size_t)j * D]));
-#pragma unroll
-            for (int g = 0; g < kMaxGroup; ++g)
-                if (g < G) acc[g] = fmaf(sc[g][j], vv, acc[g]);
+    // values: thread t takes dimension t % D and every (kThreads / D)-th
+    // position from t / D on; the parts are added in index order after
+    {
+        constexpr int VS = kThreads / D;  // 2 (d = 128) or 4 (d = 64)
+        const int dim = tid % D, part = tid / D;
+        for (int g = 0; g < G; ++g) {
+            const float* pg = sc + g * kChunk;
+            float a0 = 0.f, a1 = 0.f;
+            int j = part;
+            for (; j + VS < cnt; j += 2 * VS) {
+                a0 = fmaf(pg[j], __half2float(__ushort_as_half(vs[j * D + dim])), a0);
+                a1 = fmaf(pg[j + VS], __half2float(__ushort_as_half(vs[(j + VS) * D + dim])), a1);
+            }
+            if (j < cnt) a0 = fmaf(pg[j], __half2float(__ushort_as_half(vs[j * D + dim])), a0);
+            red[(part * kMaxGroup + g) * D + dim] = a0 + a1;
         }
+        __syncthreads();
+        for (int t2 = tid; t2 < G * D; t2 += kThreads) {
+            const int g = t2 / D, dd = t2 % D;
+            float s = 0.f;
 #pragma unroll
-        for (int g = 0; g < kMaxGroup; ++g)
-            if (g < G) part_acc[((size_t)(h0 + g) * n_splits + split) * D + tid] = acc[g];
+            for (int pp = 0; pp < VS; ++pp) s += red[(pp * kMaxGroup + g) * D + dd];
+            part_acc[((size_t)(h0 + g) * n_splits + split) * D + dd] = s;
+        }
     }
 }
 
@@ -184,10 +241,13 @@ __global__ void pos_advance_kernel(int32_t* pos_p) { *pos_p += 1; }
 
 namespace q4i {
 
+// Workspace: the step's (cos, sin) table, then (max, sum) per head and chunk,
+// then the chunks' partial outputs; each part 256-byte aligned.
 size_t attn_workspace_bytes(int n_q_heads, int head_dim, int max_seq) {
     const size_t ns = (size_t)(max_seq + q4a::kChunk - 1) / q4a::kChunk;
     const size_t ml = (size_t)n_q_heads * ns * 2 * 4;
-    return ((ml + 255) & ~size_t(255)) + (size_t)n_q_heads * ns * head_dim * 4;
+    return 256 * (((size_t)head_dim / 2 * 8 + 255) / 256) + ((ml + 255) & ~size_t(255)) +
+           (size_t)n_q_heads * ns * head_dim * 4;
 }
 
 q4_status attn_validate(const q4_attention_desc& d) {
@@ -209,25 +269,43 @@ q4_status attn_validate(const q4_attention_desc& d) {
     return Q4_OK;
 }
 
-q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s) {
+q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_table) {
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
     const int D = d.head_dim, G = d.n_q_heads / d.n_kv_heads;
     const int ns = (d.max_seq + q4a::kChunk - 1) / q4a::kChunk;
     const double l2t = log2((double)d.rope_theta);
-    float* ml = static_cast<float*>(d.workspace);
-    float* acc = reinterpret_cast<float*>(static_cast<uint8_t*>(d.workspace) +
+    uint8_t* w = static_cast<uint8_t*>(d.workspace);
+    float2* cs = reinterpret_cast<float2*>(w);
+    float* ml = reinterpret_cast<float*>(w + 256 * (((size_t)D / 2 * 8 + 255) / 256));
+    float* acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ml) +
                                           (((size_t)d.n_q_heads * ns * 2 * 4 + 255) & ~size_t(255)));
-    q4a::rope_append_kernel<<<d.n_kv_heads, D / 2, 0, s>>>(d.k, d.v, d.k_cache, d.v_cache, d.pos, D, d.max_seq, l2t,
-                                                            dev->err_word);
+    if (compute_table)
+        q4a::rope_append_kernel<true><<<d.n_kv_heads, D / 2, 0, s>>>(d.k, d.v, d.k_cache, d.v_cache, d.pos, D,
+                                                                      d.max_seq, l2t, cs, dev->err_word);
+    else
+        q4a::rope_append_kernel<false><<<d.n_kv_heads, D / 2, 0, s>>>(d.k, d.v, d.k_cache, d.v_cache, d.pos, D,
+                                                                       d.max_seq, l2t, cs, dev->err_word);
+    static bool configured[64][2] = {};
+    const int di = dev->device >= 0 && dev->device < 64 ? dev->device : 0, ti = D == 128 ? 1 : 0;
+    if (!configured[di][ti]) {
+        cudaError_t e = D == 128 ? cudaFuncSetAttribute(q4a::attn_split_kernel<128>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        (int)q4a::split_smem(128))
+                                 : cudaFuncSetAttribute(q4a::attn_split_kernel<64>,
+                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                        (int)q4a::split_smem(64));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_split_kernel)");
+        configured[di][ti] = true;
+    }
     const dim3 grid(d.n_kv_heads, ns);
     if (D == 128)
-        q4a::attn_split_kernel<128><<<grid, q4a::kThreads, 0, s>>>(d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns,
-                                                                   l2t, ml, acc, dev->err_word);
+        q4a::attn_split_kernel<128><<<grid, q4a::kThreads, q4a::split_smem(128), s>>>(
+            d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns, cs, ml, acc, dev->err_word);
     else
-        q4a::attn_split_kernel<64><<<grid, q4a::kThreads, 0, s>>>(d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns,
-                                                                  l2t, ml, acc, dev->err_word);
+        q4a::attn_split_kernel<64><<<grid, q4a::kThreads, q4a::split_smem(64), s>>>(
+            d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns, cs, ml, acc, dev->err_word);
     q4a::attn_combine_kernel<<<d.n_q_heads, D, 0, s>>>(ml, acc, d.pos, D, d.max_seq, ns, d.a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
@@ -255,5 +333,5 @@ extern "C" q4_status q4_attention(const q4_attention_desc* desc, q4_stream_t str
     if (!desc) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");
     q4_status st = attn_validate(*desc);
     if (st != Q4_OK) return st;
-    return attn_enqueue(*desc, reinterpret_cast<cudaStream_t>(stream));
+    return attn_enqueue(*desc, reinterpret_cast<cudaStream_t>(stream), true);
 }

@@ -310,7 +310,7 @@ q4_status enqueue_stages(Plan& p, cudaStream_t s) {
         if (st != Q4_OK) return st;
         // after layer l's QKV stage (stage 4l): append to the caches and attend
         if (p.dims.attn && i % 4 == 0 && i / 4 < p.attn.size()) {
-            if ((st = attn_enqueue(p.attn[i / 4], s)) != Q4_OK) return st;
+            if ((st = attn_enqueue(p.attn[i / 4], s, i == 0)) != Q4_OK) return st;
         }
     }
     if (p.dims.attn) return pos_advance(p.pos, s);

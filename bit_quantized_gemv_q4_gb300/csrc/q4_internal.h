@@ -32,7 +32,9 @@ inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 // ---- decode attention (q4_attn.cu) -----------------------------------------
 size_t attn_workspace_bytes(int n_q_heads, int head_dim, int max_seq);
 q4_status attn_validate(const q4_attention_desc& d);
-q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s);
+// compute_table: this launch computes the step's RoPE (cos, sin) table (the
+// first attention of a step); later ones read it from the same workspace.
+q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_table);
 q4_status pos_advance(int32_t* pos, cudaStream_t s);
 
 // ---- dense GEMM on the grouped-GEMM kernel (q4_moe_gemm.cu) ---------------
