@@ -93,6 +93,12 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
             fn.restype = ctypes.c_int
             fn.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [
                 ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+        L.qbo_code.restype = ctypes.c_int
+        L.qbo_code.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_int]
+        for fn in (L.qbo_gemv, L.qbo_gemv_f64):
+            fn.restype = ctypes.c_int
+            fn.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_int64] * 3 + [ctypes.c_int] + [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
         _libs[mutant] = L
     return _libs[mutant]
 
@@ -179,6 +185,48 @@ def gemv8(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
     if rc != 0:
         raise ValueError("oracle rejected arguments")
     return y, A
+
+
+def gemvb(Wq, scales, biases, x, bits: int, rows=None, nthreads: int = 0, mutant: int = 0):
+    """gemv() for b-bit codes (b in 2..8): Wq uint32 [N, K*b/32], code k of
+    a row in bits b*k .. b*k+b-1 of the row's little-endian bit stream,
+    q in 0..2^b-1, w = s * q + b per 64-group."""
+    Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
+    scales = np.ascontiguousarray(scales, dtype=np.float16)
+    biases = np.ascontiguousarray(biases, dtype=np.float16)
+    x = np.atleast_2d(x)
+    f64 = x.dtype == np.float64
+    x = np.ascontiguousarray(x, dtype=np.float64 if f64 else np.float16)
+    N, W = Wq.shape
+    K = W * 32 // bits
+    M = x.shape[0]
+    if W * 32 != K * bits or x.shape[1] != K or scales.shape != (N, K // 64) or biases.shape != (N, K // 64):
+        raise ValueError("shape mismatch")
+    if rows is None:
+        R, rp = N, None
+    else:
+        rows = np.ascontiguousarray(rows, dtype=np.int64)
+        if rows.size and (rows.min() < 0 or rows.max() >= N):
+            raise ValueError("row out of range")
+        R, rp = rows.size, _p(rows)
+    y = np.empty((M, R), np.float64)
+    A = np.empty((M, R), np.float64)
+    if R == 0:
+        return y, A
+    L = _lib(mutant)
+    fn = L.qbo_gemv_f64 if f64 else L.qbo_gemv
+    xp = _p(x) if f64 else _p(x.view(np.uint16))
+    rc = fn(_p(Wq), _p(scales.view(np.uint16)), _p(biases.view(np.uint16)), xp, M, N, K, bits, rp, R, _p(y), _p(A),
+            nthreads)
+    if rc != 0:
+        raise ValueError("oracle rejected arguments")
+    return y, A
+
+
+def codeb(Wq_row, k: int, bits: int, mutant: int = 0) -> int:
+    """The b-bit code k of one packed row (as the oracle reads it)."""
+    row = np.ascontiguousarray(Wq_row, dtype=np.uint32)
+    return _lib(mutant).qbo_code(_p(row), k, bits)
 
 
 def code8(Wq_row, k: int, mutant: int = 0) -> int:

@@ -224,6 +224,88 @@ int q8o_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
     return rc;
 }
 
+/* b-bit codes, b in 2..8 (BaseRT §3.3 and §4.1: dedicated kernels per
+ * quantisation format, 2- to 8-bit): code k of a row occupies bits
+ * b*k .. b*k+b-1 of the row's little-endian bit stream, i.e. of its uint32
+ * words taken lowest bit first, a code crossing a word boundary continuing in
+ * the low bits of the next word.  For b = 4 and 8 this is the layout above. */
+int qbo_code(const uint32_t *row, int64_t k, int bits)
+{
+#if Q4O_MUTANT == 9 /* mistake: codes packed one bit further on */
+    int64_t p = (int64_t)bits * k + 1;
+#else
+    int64_t p = (int64_t)bits * k;
+#endif
+    int64_t w = p / 32;
+    int sh = (int)(p % 32);
+    uint64_t v = row[w] >> sh;
+#if Q4O_MUTANT == 10 /* mistake: a code crossing a word boundary loses its high bits */
+    (void)0;
+#else
+    if (sh + bits > 32)
+        v |= (uint64_t)row[w + 1] << (32 - sh);
+#endif
+    return (int)(v & ((1u << bits) - 1u));
+}
+
+int qbo_gemv_f64(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                 const double *xd, int64_t M, int64_t N, int64_t K, int bits,
+                 const int64_t *rows, int64_t nrows, double *y, double *A, int nthreads)
+{
+    if (!Wq || !scales || !biases || !xd || !y || M < 1 || N < 0 || K < 64 || K % 64 || bits < 2 || bits > 8)
+        return -1;
+    if (!rows)
+        nrows = N;
+    int64_t words = K * bits / 32, groups = K / 64;
+#ifdef _OPENMP
+    if (nthreads <= 0)
+        nthreads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 4) num_threads(nthreads)
+#endif
+    for (int64_t i = 0; i < nrows; ++i) {
+        int64_t n = rows ? rows[i] : i;
+        const uint32_t *row = Wq + n * words;
+        const uint16_t *s_row = scales + n * groups;
+        const uint16_t *b_row = biases + n * groups;
+        for (int64_t m = 0; m < M; ++m) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+#if Q4O_MUTANT == 9
+                /* the shifted stream runs one bit past the last code: clamp to stay in the row */
+                int c = k == K - 1 ? qbo_code(row, k - 1, bits) : qbo_code(row, k, bits);
+#else
+                int c = qbo_code(row, k, bits);
+#endif
+                int64_t g = k / 64;
+                double w = q4o_half_to_double(s_row[g]) * (double)c + q4o_half_to_double(b_row[g]);
+                double t = w * xd[m * K + k];
+                acc += t;
+                mag += fabs(t);
+            }
+            y[m * nrows + i] = acc;
+            if (A)
+                A[m * nrows + i] = mag;
+        }
+    }
+    return 0;
+}
+
+int qbo_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+             const uint16_t *x, int64_t M, int64_t N, int64_t K, int bits,
+             const int64_t *rows, int64_t nrows, double *y, double *A, int nthreads)
+{
+    if (!x || M < 1 || K < 64)
+        return -1;
+    double *xd = (double *)malloc(sizeof(double) * (size_t)(M * K));
+    if (!xd)
+        return -1;
+    for (int64_t i = 0; i < M * K; ++i)
+        xd[i] = q4o_half_to_double(x[i]);
+    int rc = qbo_gemv_f64(Wq, scales, biases, xd, M, N, K, bits, rows, nrows, y, A, nthreads);
+    free(xd);
+    return rc;
+}
+
 /* Number of OpenMP threads this library would use by default (1 without OpenMP). */
 int q4o_max_threads(void)
 {

@@ -30,6 +30,11 @@ The 8-bit variant (``q8_matrix``) stores four codes per word, code ``k`` in
 byte ``k % 4`` of word ``k // 4`` (lowest byte first), ``q`` in ``0..255``;
 ``scale = fp16(|N(0, 0.02)| / 127.5)``, ``bias = -128 * scale``.
 
+The b-bit variant (``qb_matrix``, b in 2..8) packs the codes as a
+little-endian bit stream per row: code k in bits b*k .. b*k+b-1 of the row
+(crossing into the next uint32 when it must); ``scale = fp16(|N(0, 0.02)| /
+((2^b - 1)/2))``, ``bias = -2^(b-1) * scale``.
+
 Per-tensor seeds are ``BASE_SEED + index`` so every tensor of a model can be
 regenerated alone (the oracle needs single matrices at full size).
 """
@@ -177,6 +182,57 @@ def q8_matrix(seed: int, N: int, K: int) -> Q8Matrix:
     s = (np.abs(g.standard_normal((N, K // GROUP))) * 0.02 / 127.5).astype(np.float16)
     b = (-128.0 * s.astype(np.float64)).astype(np.float16)
     return Q8Matrix(Wq, s, b)
+
+
+@dataclasses.dataclass
+class QbMatrix:
+    """One matrix W[N, K] with b-bit codes in storage format: ``Wq`` uint32
+    ``[N, K*b/32]``, code k of a row in bits b*k .. b*k+b-1 of the row's
+    little-endian bit stream (a code may cross into the next word); fp16
+    ``scales`` and ``biases`` ``[N, K/64]``; ``w = scale * q + bias``.
+    ``codes`` keeps the drawn codes [N, K] (test input, not read by the
+    library or the oracle)."""
+    Wq: np.ndarray
+    scales: np.ndarray
+    biases: np.ndarray
+    bits: int
+    codes: np.ndarray
+
+    @property
+    def N(self) -> int:
+        return self.Wq.shape[-2]
+
+    @property
+    def K(self) -> int:
+        return self.Wq.shape[-1] * 32 // self.bits
+
+    def nbytes(self) -> int:
+        return self.Wq.nbytes + self.scales.nbytes + self.biases.nbytes
+
+
+def pack_codes(codes: np.ndarray, bits: int) -> np.ndarray:
+    """Pack codes [N, K] (each < 2^bits) into uint32 words [N, K*bits/32],
+    code k at bits bits*k .. of the row's little-endian bit stream."""
+    N, K = codes.shape
+    if (K * bits) % 32:
+        raise ValueError("K * bits is not a multiple of 32")
+    c = codes.astype(np.uint32)
+    bitarr = ((c[:, :, None] >> np.arange(bits, dtype=np.uint32)[None, None, :]) & 1).astype(np.uint8)
+    packed = np.packbits(bitarr.reshape(N, K * bits), axis=1, bitorder="little")
+    return np.ascontiguousarray(packed).view("<u4").astype(np.uint32)
+
+
+def qb_matrix(seed: int, N: int, K: int, bits: int) -> QbMatrix:
+    """Random b-bit matrix: codes uniform in 0..2^b-1, scale =
+    fp16(|N(0, 0.02)| / ((2^b - 1) / 2)), bias = -2^(b-1) * scale (exact in
+    fp16), so w spans about the same range as the 4-bit matrices."""
+    if K % GROUP:
+        raise ValueError(f"K={K} is not a multiple of {GROUP}")
+    g = rng(seed)
+    codes = g.integers(0, 1 << bits, size=(N, K), dtype=np.uint32)
+    s = (np.abs(g.standard_normal((N, K // GROUP))) * 0.02 / ((2 ** bits - 1) / 2)).astype(np.float16)
+    b = (-(2.0 ** (bits - 1)) * s.astype(np.float64)).astype(np.float16)
+    return QbMatrix(pack_codes(codes, bits), s, b, bits, codes)
 
 
 @dataclasses.dataclass(frozen=True)
