@@ -420,6 +420,42 @@ def q8_lm_head(q4, device, M: int = 1):
             "shape": f"M={M} N={N} K={K}, 8-bit codes (1.0625 B/weight), 4 rotating copies"}
 
 
+def bits_lm_head(q4, device, widths=(2, 3, 5, 6)):
+    """The lm_head-shaped GEMV (M=1, N=151936, K=1024) with b-bit codes:
+    8 warm-up launches, then 64 timed over 4 distinct weight copies (> L2)."""
+    import torch
+
+    import q4synth
+    N, K = 151936, 1024
+    peak, kind = peaks()
+    x = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4245, 1, K)).to(device)
+    y = torch.empty(1, N, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    out = {}
+    for bits in widths:
+        mats = []
+        for i in range(4):
+            g = torch.Generator(device=device).manual_seed(300 + 10 * bits + i)
+            Wq = torch.randint(-2**31, 2**31 - 1, (N, K * bits // 32), dtype=torch.int32, device=device, generator=g)
+            s = (torch.rand(N, K // 64, device=device, generator=g) * 4e-3 / 2 ** bits).half()
+            mats.append((Wq, s, (-(2 ** (bits - 1)) * s.float()).half()))
+        for i in range(8):
+            q4.q4_gemv_bits(*mats[i % 4], x, y, 1, N, K, bits, stream)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for i in range(64):
+            q4.q4_gemv_bits(*mats[i % 4], x, y, 1, N, K, bits, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        ms = e0.elapsed_time(e1) / 64
+        nb = N * K * (bits / 8.0 + 4.0 / 64) + K * 2 + N * 4
+        out[str(bits)] = {"ms": ms, "gbs": nb / (ms / 1000.0) / 1e9, "frac": nb / (ms / 1000.0) / 1e9 / peak,
+                          "bytes_per_weight": bits / 8.0 + 4.0 / 64, "peak_kind": kind}
+        del mats
+    return out
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: replicas run independently, so the job takes
     as long as its slowest replica (all-reduce MAX when world > 1)."""
@@ -549,7 +585,8 @@ def main():
         print(json.dumps({"lm_head_gemv": {"ms": ms_l, "gbs": nb / (ms_l / 1000.0) / 1e9,
                                            "frac": nb / (ms_l / 1000.0) / 1e9 / peak, "peak_kind": peak_kind,
                                            "shape": f"M={M} N={shape.vocab} K={shape.hidden}, 4 rotating copies"},
-                          "lm_head_gemv8": q8_lm_head(q4, device)}))
+                          "lm_head_gemv8": q8_lm_head(q4, device),
+                          "lm_head_gemv_bits": bits_lm_head(q4, device)}))
         return
     dl, dlm, host_model = make_model(shape, device)
     if args.section == "prefill":
@@ -648,6 +685,7 @@ def main():
     }
     if args.section == "all":
         out["lm_head_gemv8"] = q8_lm_head(q4, device)
+        out["lm_head_gemv_bits"] = bits_lm_head(q4, device)
         out["moe_prefill"] = moe_prefill(device)
         out["dense_prefill"] = dense_prefill(device, dl, dlm, shape)
         out["decode_attention"] = decode_attention(device, dl, dlm, shape)

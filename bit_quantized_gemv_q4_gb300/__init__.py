@@ -36,7 +36,7 @@ STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q
 
 # Every symbol include/q4.h declares.
 EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status",
-           "q4_selftest_expired_wait", "q4_gemv", "q4_gemv8",
+           "q4_selftest_expired_wait", "q4_gemv", "q4_gemv8", "q4_gemv_bits",
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
            "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
            "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine", "q4_gemm", "q4_prefill_workspace_bytes",
@@ -125,6 +125,8 @@ def lib() -> ctypes.CDLL:
         L.q4_gemv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
         L.q4_gemv8.restype = st
         L.q4_gemv8.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, vp]
+        L.q4_gemv_bits.restype = st
+        L.q4_gemv_bits.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, vp]
         L.q4_gemv_ex.restype = st
         L.q4_gemv_ex.argtypes = [ctypes.POINTER(q4_gemv_desc), vp]
         L.q4_decode_workspace_bytes.restype = ctypes.c_size_t
@@ -205,6 +207,13 @@ def q4_gemv8(Wq, scales, biases, x, y, M: int, N: int, K: int, stream=None):
     """q4_gemv for 8-bit codes: Wq uint32 [N, K/4], lowest byte first."""
     _check(lib().q4_gemv8(_ptr(Wq), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K, _stream(stream)),
            "q4_gemv8")
+
+
+def q4_gemv_bits(Wq, scales, biases, x, y, M: int, N: int, K: int, bits: int, stream=None):
+    """q4_gemv for b-bit codes (b in 2, 3, 4, 5, 6, 8): Wq uint32 [N, K*b/32],
+    a little-endian bit stream per row."""
+    _check(lib().q4_gemv_bits(_ptr(Wq), _ptr(scales), _ptr(biases), _ptr(x), _ptr(y), M, N, K, bits,
+                              _stream(stream)), "q4_gemv_bits")
 
 
 class Segment:

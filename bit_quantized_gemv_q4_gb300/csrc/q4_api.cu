@@ -153,6 +153,29 @@ q4_status q4_gemv8(const uint32_t* Wq, const uint16_t* scales, const uint16_t* b
     return launch_gemv(d, reinterpret_cast<cudaStream_t>(stream), false, false, nullptr, 8);
 }
 
+q4_status q4_gemv_bits(const uint32_t* Wq, const uint16_t* scales, const uint16_t* biases, const uint16_t* x,
+                       float* y, int M, int N, int K, int bits, q4_stream_t stream) {
+    clear_error();
+    if (bits < 2 || bits > 8 || bits == 7) return fail(Q4_ERR_INVALID_ARG, "bits=%d (2, 3, 4, 5, 6 or 8)", bits);
+    q4_gemv_desc d = {};
+    d.M = M;
+    d.K = K;
+    d.x = x;
+    d.ldx = K;
+    d.n_segments = 1;
+    d.seg[0].Wq = Wq;
+    d.seg[0].scales = scales;
+    d.seg[0].biases = biases;
+    d.seg[0].N = N;
+    d.seg[0].y = y;
+    d.out_dtype = Q4_F32;
+    d.mode = Q4_GEMV_PLAIN;
+    q4_status st = validate_gemv(d);
+    if (st != Q4_OK) return st;
+    if (bits != 4 && bits != 8 && M != 1) return fail(Q4_ERR_UNSUPPORTED, "%d-bit codes need M = 1", bits);
+    return launch_gemv(d, reinterpret_cast<cudaStream_t>(stream), false, false, nullptr, bits);
+}
+
 q4_status q4_gemv_ex(const q4_gemv_desc* desc, q4_stream_t stream) {
     clear_error();
     if (!desc) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");

@@ -39,6 +39,8 @@
 #include <cuda_fp16.h>
 #include <stdio.h>
 
+#include <utility>
+
 #include "q4_device.cuh"
 #include "q4_internal.h"
 
@@ -156,7 +158,14 @@ __device__ __forceinline__ void issue_rows(const Params& p, const Seg& sg, int n
     const uint32_t* wq_src = sg.Wq + (size_t)n0 * (crb / 4);
     const uint16_t* s_src = sg.s + (size_t)n0 * G;
     const uint16_t* b_src = sg.b + (size_t)n0 * G;
-    if (lane == 0) q4d::bulk_g2s_evict_first(q4d::smem_addr(wq_dst), wq_src, wq_bytes, full_bar, pol);
+    if ((wq_bytes & 15u) == 0) {
+        if (lane == 0) q4d::bulk_g2s_evict_first(q4d::smem_addr(wq_dst), wq_src, wq_bytes, full_bar, pol);
+    } else {
+        // A ragged last tile of 3- or 5-bit codes whose code block is not a
+        // 16-byte multiple: the producer lanes copy it word by word.
+        uint32_t* wd = reinterpret_cast<uint32_t*>(wq_dst);
+        for (uint32_t i = lane; i < wq_bytes / 4; i += 32) wd[i] = __ldg(wq_src + i);
+    }
     if ((sb_bytes & 15u) == 0) {
         if (lane == 0) {
             q4d::bulk_g2s(q4d::smem_addr(s_dst), s_src, sb_bytes, full_bar);
@@ -178,7 +187,7 @@ __device__ __forceinline__ void issue_rows(const Params& p, const Seg& sg, int n
 __device__ __forceinline__ uint32_t bulk_bytes(const Params& p, int nrows) {
     const uint32_t wq_b = (uint32_t)nrows * (uint32_t)(p.K * p.bits / 8);
     const uint32_t sb_b = (uint32_t)nrows * (uint32_t)(p.K / 64) * 2u;
-    return wq_b + (((sb_b & 15u) == 0) ? 2 * sb_b : 0);
+    return (((wq_b & 15u) == 0) ? wq_b : 0) + (((sb_b & 15u) == 0) ? 2 * sb_b : 0);
 }
 
 // ------------------------------------------------------------------ consumer
@@ -229,6 +238,47 @@ __device__ __forceinline__ void word_mac8(uint32_t a, uint32_t b, uint16_t sh, f
     }
 }
 
+// 2-, 3-, 5- and 6-bit codes (M = 1): a lane's 32 codes are exactly BITS
+// words of the row's little-endian bit stream.  Code c sits at bit BITS*c;
+// one funnel shift brings it to the bottom of a register and one AND-OR puts
+// it under the mantissa of 1024.0 in the low half (1024+q, exact), so each
+// code is dequantised by one mixed-precision FMA on a low half, and pairs of
+// codes meet their x in the packed fp32x2 FMA.
+template <int BITS, int C>
+__device__ __forceinline__ uint32_t code_at(const uint32_t* w) {
+    constexpr int P = BITS * C, W = P >> 5, S = P & 31;
+    uint32_t v;
+    if constexpr (S == 0) {
+        v = w[W];
+    } else if constexpr (S + BITS <= 32) {
+        v = w[W] >> S;
+    } else {
+        v = __funnelshift_r(w[W], w[W + 1], S);
+    }
+    return q4d::and_or(v, (1u << BITS) - 1u, 0x6400u);
+}
+
+__device__ __forceinline__ float fma_lo_s_f32(uint32_t v, uint16_t s, float c) {
+    float r;
+    asm("{ .reg .b16 l, h; mov.b32 {l, h}, %1; fma.rn.f32.f16 %0, l, %2, %3; }" : "=f"(r) : "r"(v), "h"(s), "f"(c));
+    return r;
+}
+
+template <int BITS, int C>
+__device__ __forceinline__ void pair_mac(const uint32_t* w, uint16_t sh, float c1024, const float4* xr, float2& acc) {
+    const float wa = fma_lo_s_f32(code_at<BITS, C>(w), sh, c1024);
+    const float wb = fma_lo_s_f32(code_at<BITS, C + 1>(w), sh, c1024);
+    const float4 xq = xr[C / 4];
+    const float2 xp = (C % 4 == 0) ? make_float2(xq.x, xq.y) : make_float2(xq.z, xq.w);
+    acc = __ffma2_rn(make_float2(wa, wb), xp, acc);
+}
+
+template <int BITS, int... Cs>
+__device__ __forceinline__ void chunk_mac(const uint32_t* w, uint16_t sh, float c1024, const float4* xr, float2& acc,
+                                          std::integer_sequence<int, Cs...>) {
+    (pair_mac<BITS, 2 * Cs>(w, sh, c1024, xr, acc), ...);
+}
+
 template <int LW>
 __device__ __forceinline__ void load_words(const uint32_t* src, uint32_t* w) {
     if constexpr (LW == 8) {
@@ -274,40 +324,68 @@ __device__ __forceinline__ void dot_rows(const Params& p, const uint32_t* wq, co
 #pragma unroll
         for (int m = 0; m < M; ++m) acc[r][m] = make_float2(0.f, 0.f);
 
-    for (int c = 0; c < nchunks; ++c) {
-        const int j0 = c * chunk_words + lane * LW;
-        if (j0 < W8) {
-            float4 xr[XV];
-            const float4* xc = xs + (size_t)c * XV * 32 + lane;
+    if constexpr (BITS != 4 && BITS != 8) {
+        static_assert(M == 1 && LW == 4, "2/3/5/6-bit codes: M = 1 (32 codes per lane chunk)");
+        const int words_row = W8 * BITS / 4;
+        for (int c = 0; c < nchunks; ++c) {
+            const int j0 = c * chunk_words + lane * LW;
+            if (j0 < W8) {
+                float4 xr[XV];
+                const float4* xc = xs + (size_t)c * XV * 32 + lane;
 #pragma unroll
-            for (int i = 0; i < XV; ++i) xr[i] = xc[i * 32];
-            const int g = j0 >> 3;
+                for (int i = 0; i < XV; ++i) xr[i] = xc[i * 32];
+                const int g = j0 >> 3;
 #pragma unroll
-            for (int r = 0; r < RB; ++r) {
-                constexpr int WPO = BITS / 4;  // words per octet
-                uint32_t w[LW * WPO];
-                load_words<LW * WPO>(wq + ((size_t)rows[r] * W8 + j0) * WPO, w);
-                const uint16_t sh = ss[rows[r] * G + g];
-                const uint16_t bh = bs[rows[r] * G + g];
-                const float sf = __half2float(__ushort_as_half(sh));
-                const float bf = __half2float(__ushort_as_half(bh));
-                const float c1024 = fmaf(-1024.f, sf, bf);
-                const float c64 = fmaf(-64.f, sf, bf);
+                for (int r = 0; r < RB; ++r) {
+                    const uint32_t* src = wq + (size_t)rows[r] * words_row + j0 * BITS / 4;
+                    uint32_t w[BITS];
 #pragma unroll
-                for (int wi = 0; wi < LW; ++wi) {
-                    if constexpr (BITS == 4)
-                        word_mac<M>(w[wi], sh, c1024, c64, &xr[(wi * 2 + 0) * M], &xr[(wi * 2 + 1) * M], acc[r]);
-                    else
-                        word_mac8<M>(w[2 * wi], w[2 * wi + 1], sh, c1024, &xr[(wi * 2 + 0) * M],
-                                     &xr[(wi * 2 + 1) * M], acc[r]);
+                    for (int i = 0; i < BITS; ++i) w[i] = src[i];
+                    const uint16_t sh = ss[rows[r] * G + g];
+                    const float sf = __half2float(__ushort_as_half(sh));
+                    const float c1024 = fmaf(-1024.f, sf, __half2float(__ushort_as_half(bs[rows[r] * G + g])));
+                    chunk_mac<BITS>(w, sh, c1024, xr, acc[r][0], std::make_integer_sequence<int, 16>{});
                 }
             }
         }
+#pragma unroll
+        for (int r = 0; r < RB; ++r) out[r][0] = acc[r][0].x + acc[r][0].y;
+    } else {
+        for (int c = 0; c < nchunks; ++c) {
+            const int j0 = c * chunk_words + lane * LW;
+            if (j0 < W8) {
+                float4 xr[XV];
+                const float4* xc = xs + (size_t)c * XV * 32 + lane;
+#pragma unroll
+                for (int i = 0; i < XV; ++i) xr[i] = xc[i * 32];
+                const int g = j0 >> 3;
+#pragma unroll
+                for (int r = 0; r < RB; ++r) {
+                    constexpr int WPO = BITS / 4;  // words per octet
+                    uint32_t w[LW * WPO];
+                    load_words<LW * WPO>(wq + ((size_t)rows[r] * W8 + j0) * WPO, w);
+                    const uint16_t sh = ss[rows[r] * G + g];
+                    const uint16_t bh = bs[rows[r] * G + g];
+                    const float sf = __half2float(__ushort_as_half(sh));
+                    const float bf = __half2float(__ushort_as_half(bh));
+                    const float c1024 = fmaf(-1024.f, sf, bf);
+                    const float c64 = fmaf(-64.f, sf, bf);
+#pragma unroll
+                    for (int wi = 0; wi < LW; ++wi) {
+                        if constexpr (BITS == 4)
+                            word_mac<M>(w[wi], sh, c1024, c64, &xr[(wi * 2 + 0) * M], &xr[(wi * 2 + 1) * M], acc[r]);
+                        else
+                            word_mac8<M>(w[2 * wi], w[2 * wi + 1], sh, c1024, &xr[(wi * 2 + 0) * M],
+                                         &xr[(wi * 2 + 1) * M], acc[r]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int r = 0; r < RB; ++r)
+#pragma unroll
+            for (int m = 0; m < M; ++m) out[r][m] = acc[r][m].x + acc[r][m].y;
     }
-#pragma unroll
-    for (int r = 0; r < RB; ++r)
-#pragma unroll
-        for (int m = 0; m < M; ++m) out[r][m] = acc[r][m].x + acc[r][m].y;
 }
 
 // Sum V values (power of two, V <= 32) across the 32 lanes of a warp with a
@@ -475,9 +553,12 @@ __device__ __forceinline__ void octet_halves(const float* f, float4& a, float4& 
     if constexpr (BITS == 4) {
         a = make_float4(f[0], f[4], f[1], f[5]);
         b = make_float4(f[2], f[6], f[3], f[7]);
-    } else {
+    } else if constexpr (BITS == 8) {
         a = make_float4(f[0], f[2], f[1], f[3]);
         b = make_float4(f[4], f[6], f[5], f[7]);
+    } else {  // 2, 3, 5, 6 bits: codes are dequantised one by one, pairs in order
+        a = make_float4(f[0], f[1], f[2], f[3]);
+        b = make_float4(f[4], f[5], f[6], f[7]);
     }
 }
 
@@ -1083,7 +1164,8 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
-    if (bits != 4 && bits != 8) return fail(Q4_ERR_INVALID_ARG, "bits=%d", bits);
+    if (bits < 2 || bits > 8 || bits == 7) return fail(Q4_ERR_INVALID_ARG, "bits=%d", bits);
+    if (bits != 4 && bits != 8 && d.M != 1) return fail(Q4_ERR_UNSUPPORTED, "%d-bit codes need M = 1", bits);
 
     Params p;
     fill_params(d, tg, early_prefetch, dev->sms, 48u * 1024u, dev->err_word, p, bits);
@@ -1134,6 +1216,16 @@ q4_status launch_gemv(const q4_gemv_desc& d, cudaStream_t stream, bool pdl, bool
         e = bits == 4 ? launch_m<MM, 4>(p, dim3(grid), smem, stream, pdl)                        \
                       : launch_m<MM, 8>(p, dim3(grid), smem, stream, pdl);                       \
         break;
+    if (bits != 4 && bits != 8) {
+        switch (bits) {
+            case 2: e = launch_m<1, 2>(p, dim3(grid), smem, stream, pdl); break;
+            case 3: e = launch_m<1, 3>(p, dim3(grid), smem, stream, pdl); break;
+            case 5: e = launch_m<1, 5>(p, dim3(grid), smem, stream, pdl); break;
+            default: e = launch_m<1, 6>(p, dim3(grid), smem, stream, pdl); break;
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "q4_gemv kernel launch");
+        return Q4_OK;
+    }
     switch (M) {
         Q4_LAUNCH_M(1)
         Q4_LAUNCH_M(2)

@@ -168,6 +168,19 @@ typedef struct q4_gemv_desc {
 
 q4_status q4_gemv_ex(const q4_gemv_desc *desc, q4_stream_t stream);
 
+/* q4_gemv for b-bit codes, b in {2, 3, 4, 5, 6, 8} (BaseRT §3.3 and §4.1:
+ * a kernel per quantisation format, 2 to 16 bits).  Wq: uint32 [N][K*b/32];
+ * code k of a row occupies bits b*k .. b*k+b-1 of the row's little-endian bit
+ * stream (lowest bit first; a code crossing a word boundary continues in the
+ * low bits of the next word) -- for b = 4 and 8 exactly the layouts of
+ * q4_gemv and q4_gemv8.  scales, biases: fp16 [N][K/64]; w = s * q + b with
+ * q in 0..2^b-1.  b = 2, 3, 5, 6 need M = 1 (else Q4_ERR_UNSUPPORTED);
+ * b = 7 or outside 2..8 returns Q4_ERR_INVALID_ARG.  Other rules as
+ * q4_gemv. */
+q4_status q4_gemv_bits(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
+                       const uint16_t *x, float *y, int M, int N, int K, int bits,
+                       q4_stream_t stream);
+
 /* ------------------------------------------------------------------------ *
  * 3. q4_decode_step -- one decode step over a whole layer stack.
  *

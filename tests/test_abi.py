@@ -101,6 +101,11 @@ def test_gemv_rejects_bad_sizes(L, M, N, K, expect):
     assert L.q4_last_error() != b""
 
 
+def test_gemv_bits_refusals(L):
+    for bits, M, want in ((7, 1, -1), (1, 1, -1), (9, 1, -1), (3, 2, -2), (6, 4, -2)):
+        assert L.q4_gemv_bits(FAKE, FAKE, FAKE, FAKE, FAKE, M, 8, 64, bits, None) == want, (bits, M)
+
+
 def test_gemv_rejects_null_and_misaligned(L):
     assert L.q4_gemv(None, FAKE, FAKE, FAKE, FAKE, 1, 8, 64, None) == -1
     assert L.q4_gemv(FAKE + 4, FAKE, FAKE, FAKE, FAKE, 1, 8, 64, None) == -3
