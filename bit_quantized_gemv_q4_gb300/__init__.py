@@ -40,7 +40,7 @@ EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status"
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
            "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
            "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine", "q4_gemm", "q4_prefill_workspace_bytes",
-           "q4_prefill", "q4_attention_workspace_bytes", "q4_attention"]
+           "q4_prefill", "q4_attention_workspace_bytes", "q4_attention", "q4_gemm_workspace_bytes"]
 
 
 class Q4Error(RuntimeError):
@@ -98,7 +98,7 @@ class q4_attention_desc(ctypes.Structure):
 
 class q4_gemm_desc(ctypes.Structure):
     _fields_ = [("M", i32), ("X", vp), ("w", q4_linear), ("up", q4_linear), ("mode", i32), ("out_dtype", i32),
-                ("Y", vp), ("residual", vp)]
+                ("Y", vp), ("residual", vp), ("workspace", vp), ("workspace_bytes", ctypes.c_size_t)]
 
 
 _lib = None
@@ -149,6 +149,8 @@ def lib() -> ctypes.CDLL:
         L.q4_moe_gemm.argtypes = [vp] * 7 + [ctypes.POINTER(q4_moe_desc), vp]
         L.q4_moe_combine.restype = st
         L.q4_moe_combine.argtypes = [vp, i32, i32, vp, vp, i32, i32, vp, i32, vp]
+        L.q4_gemm_workspace_bytes.restype = ctypes.c_size_t
+        L.q4_gemm_workspace_bytes.argtypes = [i32, i32, i32, i32]
         L.q4_gemm.restype = st
         L.q4_gemm.argtypes = [ctypes.POINTER(q4_gemm_desc), vp]
         L.q4_prefill_workspace_bytes.restype = ctypes.c_size_t
@@ -350,14 +352,20 @@ def q4_moe_combine(Y, y_dtype, N, pos, topk_weights, T, topk, out, out_dtype, st
 
 # --------------------------------------------------------------- prefill ---
 
-def q4_gemm(w, X, Y, M: int, mode=Q4_GEMV_PLAIN, out_dtype=Q4_F32, up=None, residual=None, stream=None):
+def q4_gemm_workspace_bytes(M: int, N: int, K: int, mode=Q4_GEMV_PLAIN) -> int:
+    return lib().q4_gemm_workspace_bytes(M, N, K, mode)
+
+
+def q4_gemm(w, X, Y, M: int, mode=Q4_GEMV_PLAIN, out_dtype=Q4_F32, up=None, residual=None, workspace=None,
+            workspace_bytes: int = 0, stream=None):
     """Dense Y[M, N] = X[M, K] W^T on the tensor cores.  ``w`` (and ``up`` in
-    GLU mode) are (Wq, scales, biases, N, K)."""
+    GLU mode) are (Wq, scales, biases, N, K); a workspace lets K split."""
     d = q4_gemm_desc()
     d.M, d.X, d.w = M, _ptr(X), _linear(*w)
     if up is not None:
         d.up = _linear(*up)
     d.mode, d.out_dtype, d.Y, d.residual = mode, out_dtype, _ptr(Y), _ptr(residual)
+    d.workspace, d.workspace_bytes = _ptr(workspace), workspace_bytes
     _check(lib().q4_gemm(ctypes.byref(d), _stream(stream)), "q4_gemm")
 
 

@@ -392,10 +392,10 @@ __global__ void rmsnorm_rows_kernel(const uint16_t* __restrict__ h, const uint16
 }
 
 struct PrefillLayout {
-    size_t n = 0, q = 0, k = 0, v = 0, act = 0, total = 0;
+    size_t n = 0, q = 0, k = 0, v = 0, act = 0, part = 0, part_bytes = 0, total = 0;
 };
 
-PrefillLayout prefill_layout(const Dims& d, int chunk) {
+PrefillLayout prefill_layout(const Dims& d, int chunk, const q4_layer_table* t) {
     PrefillLayout l;
     size_t off = 0;
     auto take = [&](size_t elems) {
@@ -409,6 +409,20 @@ PrefillLayout prefill_layout(const Dims& d, int chunk) {
     l.k = take(C * (d.kvN > 0 ? d.kvN : 1));
     l.v = take(C * (d.kvN > 0 ? d.kvN : 1));
     l.act = take(C * (d.ffn > 0 ? d.ffn : 1));
+    // fp32 partial sums for the GEMMs that split K (small chunks leave output tiles for few SMs)
+    size_t pb = 0;
+    for (int i = 0; i < d.L; ++i) {
+        const q4_layer_weights& w = t->layers[i];
+        const size_t s[6] = {gemm_split_bytes(chunk, w.q.N, w.q.K, false),
+                             gemm_split_bytes(chunk, w.k.N, w.k.K, false),
+                             gemm_split_bytes(chunk, w.v.N, w.v.K, false),
+                             gemm_split_bytes(chunk, w.o.N, w.o.K, false),
+                             gemm_split_bytes(chunk, w.gate.N, w.gate.K, true),
+                             gemm_split_bytes(chunk, w.down.N, w.down.K, false)};
+        for (size_t b : s) pb = b > pb ? b : pb;
+    }
+    l.part_bytes = pb;
+    l.part = take(pb / 2 + 1);
     l.total = off;
     return l;
 }
@@ -422,7 +436,7 @@ q4_status prefill_dims(const q4_layer_table* t, int chunk, Dims* d) {
 }
 
 q4_status gemm_of(const q4_linear& w, const q4_linear* up, const uint16_t* X, int M, void* Y,
-                  const uint16_t* residual, cudaStream_t s) {
+                  const uint16_t* residual, void* part, size_t part_bytes, cudaStream_t s) {
     q4_gemm_desc g = {};
     g.M = M;
     g.X = X;
@@ -432,6 +446,8 @@ q4_status gemm_of(const q4_linear& w, const q4_linear* up, const uint16_t* X, in
     g.out_dtype = Q4_F16;
     g.Y = Y;
     g.residual = residual;
+    g.workspace = part;
+    g.workspace_bytes = part_bytes;
     return gemm_launch(&g, reinterpret_cast<q4_stream_t>(s));
 }
 
@@ -446,7 +462,7 @@ size_t q4_prefill_workspace_bytes(const q4_layer_table* table, int chunk) {
     clear_error();
     Dims d;
     if (prefill_dims(table, chunk, &d) != Q4_OK) return 0;
-    return prefill_layout(d, chunk).total;
+    return prefill_layout(d, chunk, table).total;
 }
 
 q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk, void* logits, void* workspace,
@@ -458,7 +474,7 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
     if (T < 0) return fail(Q4_ERR_INVALID_ARG, "T=%d", T);
     if (T > 0 && !h) return fail(Q4_ERR_INVALID_ARG, "h is NULL");
     if (!aligned16(h) || (logits && !aligned16(logits))) return fail(Q4_ERR_MISALIGNED, "h and logits must be 16-byte aligned");
-    const PrefillLayout l = prefill_layout(d, chunk);
+    const PrefillLayout l = prefill_layout(d, chunk, table);
     if (!workspace) return fail(Q4_ERR_INVALID_ARG, "workspace is NULL");
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return fail(Q4_ERR_MISALIGNED, "workspace must be 256-byte aligned");
     if (workspace_bytes < l.total) return fail(Q4_ERR_INVALID_ARG, "workspace has %zu bytes, needs %zu", workspace_bytes, l.total);
@@ -467,8 +483,6 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
         if (w.q.N % 128 || w.k.N % 128 || w.v.N % 128 || w.o.N % 128 || w.gate.N % 128 || w.down.N % 128)
             return fail(Q4_ERR_UNSUPPORTED, "layer %d: the prefill GEMM needs output widths that are multiples of 128", i);
     }
-    const DeviceInfo* dev = nullptr;
-    if ((st = current_device(&dev)) != Q4_OK) return st;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const float eps = table->norm_eps > 0.f ? table->norm_eps : 1e-6f;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -477,6 +491,8 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
     uint16_t* k = reinterpret_cast<uint16_t*>(ws + l.k);
     uint16_t* v = reinterpret_cast<uint16_t*>(ws + l.v);
     uint16_t* act = reinterpret_cast<uint16_t*>(ws + l.act);
+    void* part = ws + l.part;
+    const size_t pb = l.part_bytes;
     const int H = d.hidden;
     for (int t0 = 0; t0 < T; t0 += chunk) {
         const int C = T - t0 < chunk ? T - t0 : chunk;
@@ -487,14 +503,14 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
             rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.attn_norm, n, C, H, eps);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
-            if ((st = gemm_of(w.q, nullptr, n, C, q, nullptr, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.k, nullptr, n, C, k, nullptr, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.v, nullptr, n, C, v, nullptr, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.o, nullptr, q, C, hc, hc, s)) != Q4_OK) return st;  // h' = h + Wo q
+            if ((st = gemm_of(w.q, nullptr, n, C, q, nullptr, part, pb, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.k, nullptr, n, C, k, nullptr, part, pb, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.v, nullptr, n, C, v, nullptr, part, pb, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.o, nullptr, q, C, hc, hc, part, pb, s)) != Q4_OK) return st;  // h' = h + Wo q
             rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.ffn_norm, n, C, H, eps);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
-            if ((st = gemm_of(w.gate, &w.up, n, C, act, nullptr, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.down, nullptr, act, C, hc, hc, s)) != Q4_OK) return st;  // h = h' + Wdown act
+            if ((st = gemm_of(w.gate, &w.up, n, C, act, nullptr, part, pb, s)) != Q4_OK) return st;
+            if ((st = gemm_of(w.down, nullptr, act, C, hc, hc, part, pb, s)) != Q4_OK) return st;  // h = h' + Wdown act
         }
     }
     if (logits && T > 0) {

@@ -39,6 +39,8 @@ q4_status pos_advance(int32_t* pos, cudaStream_t s);
 
 // ---- dense GEMM on the grouped-GEMM kernel (q4_moe_gemm.cu) ---------------
 q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream);
+// Bytes of fp32 partials a dense GEMM of this shape splits K into (0 = no split).
+size_t gemm_split_bytes(int M, int N, int K, bool glu);
 
 // ---- fused multi-segment GEMV (q4_gemv.cu) --------------------------------
 q4_status validate_gemv(const q4_gemv_desc& d);

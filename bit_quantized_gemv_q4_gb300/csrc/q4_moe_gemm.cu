@@ -77,6 +77,8 @@ struct Params {
     void* Y;
     int E, N, K, R, rows_e, up_off, nmat, glu, out_f16;
     int n_tiles, nK, G;
+    int kparts, ksteps;   // split of K over units (dense, few units): K steps per part
+    float* part;          // kparts > 1: fp32 partials [kparts][nmat][R][N], reduced by reduce_parts_kernel
     int in_stages, a_stages;       // ring depths (the rest of shared memory, see launch_grouped)
     uint32_t in_bytes, a_bytes;    // bytes per input / A stage
     uint32_t x_off;                // X's offset in an input stage
@@ -178,10 +180,12 @@ __device__ __forceinline__ bool wait_bar(Smem& sm, uint64_t& bar, uint32_t parit
 }
 
 struct Unit {
-    int e, r0, tn, nt;  // expert, first token row, valid tokens, output tile index
+    int e, r0, tn, nt, kp;  // expert, first token row, valid tokens, output tile index, K part
 };
 
 __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int u) {
+    const int kp = u % p.kparts;
+    u /= p.kparts;
     const int tt = u / p.n_tiles;
     int lo = 0, hi = p.E;  // largest e with prefix[e] <= tt
     while (hi - lo > 1) {
@@ -198,6 +202,7 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int
     un.r0 = a + j * kTN;
     un.tn = min(kTN, b - un.r0);
     un.nt = u % p.n_tiles;
+    un.kp = kp;
     return un;
 }
 
@@ -263,7 +268,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 run += (b - a + kTN - 1) / kTN;
             }
             sm.prefix[p.E] = run;
-            sm.total_units = run * p.n_tiles;
+            sm.total_units = run * p.n_tiles * p.kparts;
         }
     }
     if (warp == 1) {
@@ -278,7 +283,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
     const int U = sm.total_units;
-    const int nK = p.nK;
 
     if (warp == 0) {
         // ------------------------------------------------------------ TMA
@@ -303,7 +307,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     ++staged;
                 }
-                for (int ks = 0; ks < nK; ++ks, ++it) {
+                const int ks0 = un.kp * p.ksteps, ks1 = ks0 + p.ksteps;
+                for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int s = ip.s;
                     if (ip.r > 0 && !wait_bar(sm, sm.in_empty[s], (ip.r - 1) & 1, p.err)) break;
                     uint8_t* st = in_ring + (size_t)s * p.in_bytes;
@@ -338,7 +343,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d0 = tmem + (uint32_t)(buf * 2 * kTN);
                 bool ok = true;
-                for (int ks = 0; ks < nK; ++ks, ++it) {
+                const int ks0 = un.kp * p.ksteps, ks1 = ks0 + p.ksteps;
+                for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int s = ip.s, a = ap.s;
                     if (!wait_bar(sm, sm.in_full[s], ip.r & 1, p.err) || !wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
                         ok = false;
@@ -353,7 +359,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t dm = d0 + (uint32_t)(mi * kTN);
 #pragma unroll
                         for (int kk = 0; kk < kKS / 16; ++kk)
-                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (ks > 0 || kk > 0) ? 1u : 0u);
+                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (ks > ks0 || kk > 0) ? 1u : 0u);
                     }
                     mma_commit(q4d::smem_addr(&sm.in_empty[s]));
                     mma_commit(q4d::smem_addr(&sm.a_empty[a]));
@@ -403,7 +409,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&sm.sb_empty));
             bool ok = true;
-            for (int ks = 0; ks < nK; ++ks, ++it) {
+            const int ks0 = (u % p.kparts) * p.ksteps, ks1 = ks0 + p.ksteps;
+            for (int ks = ks0; ks < ks1; ++ks, ++it) {
                 const int s = ip.s, a = ap.s;
                 bool w = wait_bar(sm, sm.in_full[s], ip.r & 1, p.err);
                 if (w && ap.r > 0) w = wait_bar(sm, sm.a_empty[a], (ap.r - 1) & 1, p.err);
@@ -465,6 +472,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int c = 0; c < 16; ++c) {
                     if (c0 + c < un.tn) {
                         const size_t o = (size_t)(un.r0 + c0 + c) * p.N + n;
+                        if (p.kparts > 1) {
+                            // one K part: raw fp32 sums, reduced (and finished) by reduce_parts_kernel
+                            const size_t pr = (size_t)p.R * p.N;
+                            p.part[(size_t)(un.kp * p.nmat) * pr + o] = __uint_as_float(g[c]);
+                            if (p.glu) p.part[(size_t)(un.kp * p.nmat + 1) * pr + o] = __uint_as_float(v[c]);
+                            continue;
+                        }
                         float y = __uint_as_float(g[c]);
                         if (p.glu) {
                             const float up = __uint_as_float(v[c]);
@@ -509,6 +523,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols)
                      : "memory");
+    }
+}
+
+// Sum of the K parts of a split launch, then the epilogue the unsplit kernel
+// applies: SiLU(g) * u in GLU mode, + residual, fp16 or fp32 store.  Four
+// outputs per thread (N is a multiple of 128).
+__global__ void reduce_parts_kernel(const float* __restrict__ part, int kparts, int nmat, int R, int N, int glu,
+                                    const uint16_t* residual, void* Y, int out_f16) {
+    const size_t pr = (size_t)R * N;
+    const size_t i = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+    if (i >= pr) return;
+    float4 g = make_float4(0.f, 0.f, 0.f, 0.f), u = g;
+    for (int k = 0; k < kparts; ++k) {
+        const float4 a = *reinterpret_cast<const float4*>(part + (size_t)(k * nmat) * pr + i);
+        g = make_float4(g.x + a.x, g.y + a.y, g.z + a.z, g.w + a.w);
+        if (glu) {
+            const float4 b = *reinterpret_cast<const float4*>(part + (size_t)(k * nmat + 1) * pr + i);
+            u = make_float4(u.x + b.x, u.y + b.y, u.z + b.z, u.w + b.w);
+        }
+    }
+    float y[4] = {g.x, g.y, g.z, g.w};
+    const float uu[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+        if (glu) y[e] = y[e] / (1.0f + expf(-y[e])) * uu[e];
+        if (residual) y[e] += __half2float(__ushort_as_half(residual[i + e]));
+    }
+    if (out_f16) {
+        uint16_t* o = static_cast<uint16_t*>(Y) + i;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) o[e] = __half_as_ushort(__float2half_rn(y[e]));
+    } else {
+        *reinterpret_cast<float4*>(static_cast<float*>(Y) + i) = make_float4(y[0], y[1], y[2], y[3]);
     }
 }
 
@@ -579,6 +626,8 @@ struct GroupedArgs {
     int E, N, K, R;
     q4_gemv_mode mode;
     q4_dtype out_dtype;
+    int kparts = 1;        // split K over this many units (dense only); 1 = no split
+    float* part = nullptr; // kparts > 1: fp32 [kparts][nmat][R][N]
 };
 
 q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
@@ -623,6 +672,9 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.n_tiles = a.N / q4g::kRows;
     p.nK = a.K / q4g::kKS;
     p.G = a.K / 64;
+    p.kparts = a.kparts > 1 ? a.kparts : 1;
+    p.ksteps = p.nK / p.kparts;
+    p.part = a.part;
     p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqThreads * (p.G + 1) * 4 + 127) & ~size_t(127));
     p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
     p.err = dev->err_word;
@@ -677,10 +729,43 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     q4g::q4_moe_gemm_kernel<<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
+    if (p.kparts > 1) {
+        const size_t quads = (size_t)a.R * a.N / 4;
+        q4g::reduce_parts_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(
+            p.part, p.kparts, p.nmat, a.R, a.N, p.glu, a.residual, a.Y, p.out_f16);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "split reduction launch");
+    }
     return Q4_OK;
 }
 
 }  // namespace
+
+// K parts for a dense GEMM whose output tiles do not fill the GPU: the
+// smallest divisor of the K steps that gives at least 152 units (one per SM
+// of a GB300; a fixed target keeps workspace sizes computable without a
+// device), with at least 4 K steps per unit.
+constexpr int kSplitTargetUnits = 152;
+
+int gemm_split_parts(int M, int N, int K) {
+    if (M < 1 || N < 128 || K < 64) return 1;
+    const int units = ((M + q4g::kTN - 1) / q4g::kTN) * (N / q4g::kRows);
+    const int nK = K / q4g::kKS;
+    const int sms = kSplitTargetUnits;
+    if (units >= sms) return 1;
+    int best = 1;
+    for (int d = 2; d <= nK / 4; ++d) {
+        if (nK % d) continue;
+        best = d;
+        if (units * d >= sms) break;
+    }
+    return best;
+}
+
+size_t gemm_split_bytes(int M, int N, int K, bool glu) {
+    const int kp = gemm_split_parts(M, N, K);
+    return kp > 1 ? (size_t)kp * (glu ? 2 : 1) * (size_t)M * N * 4 : 0;
+}
 
 q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream) {
     if (!d) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");
@@ -709,6 +794,13 @@ q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream) {
     a.R = d->M;
     a.mode = d->mode;
     a.out_dtype = d->out_dtype;
+    if (d->workspace && d->M > 0 && d->w.N % 128 == 0 && d->w.K % 64 == 0) {
+        const size_t need = gemm_split_bytes(d->M, d->w.N, d->w.K, glu);
+        if (need > 0 && d->workspace_bytes >= need && (reinterpret_cast<uintptr_t>(d->workspace) & 15u) == 0) {
+            a.kparts = gemm_split_parts(d->M, d->w.N, d->w.K);
+            a.part = static_cast<float*>(d->workspace);
+        }
+    }
     return launch_grouped(a, stream);
 }
 
@@ -739,6 +831,11 @@ extern "C" q4_status q4_moe_gemm(const uint32_t* Wq, const uint16_t* scales, con
     a.mode = d->mode;
     a.out_dtype = d->out_dtype;
     return launch_grouped(a, stream);
+}
+
+extern "C" size_t q4_gemm_workspace_bytes(int M, int N, int K, q4_gemv_mode mode) {
+    clear_error();
+    return gemm_split_bytes(M, N, K, mode == Q4_GEMV_GLU);
 }
 
 extern "C" q4_status q4_gemm(const q4_gemm_desc* desc, q4_stream_t stream) {

@@ -415,7 +415,18 @@ typedef struct q4_gemm_desc {
     void *Y;                   /* [M][N] */
     const uint16_t *residual;  /* PLAIN with fp16 output only: Y = fp16(residual + X W^T),
                                   fp16 [M][N], may be the same buffer as Y; NULL = none */
+    void *workspace;           /* optional, 16-byte aligned: when the output tiles do not
+                                  fill the GPU and workspace_bytes >= q4_gemm_workspace_bytes,
+                                  K is split over more units, fp32 partial sums go here and a
+                                  second kernel adds them and applies the epilogue; NULL =
+                                  never split */
+    size_t workspace_bytes;
 } q4_gemm_desc;
+
+/* Workspace bytes that let q4_gemm split K for this shape (0: it would not
+ * split).  The split aims at 152 units of work (one per GB300 SM) with at
+ * least 4 K steps of 64 per unit. */
+size_t q4_gemm_workspace_bytes(int M, int N, int K, q4_gemv_mode mode);
 
 /* Y = X W^T on the tensor cores.  N must be a multiple of 128 (else
  * Q4_ERR_UNSUPPORTED); the shared-memory limit on K is that of q4_moe_gemm
@@ -439,7 +450,8 @@ size_t q4_prefill_workspace_bytes(const q4_layer_table *table, int chunk);
  * by the decode GEMV; NULL = none.  workspace: device, 256-byte aligned,
  * >= q4_prefill_workspace_bytes(table, chunk) bytes; after the call it holds
  * the last chunk's n', q, k, v and act (fp16 [chunk][width] each, in that
- * order, each slice 256-byte aligned).  Every output width of the stack
+ * order, each slice 256-byte aligned), then room for the fp32 partial sums of
+ * the GEMMs that split K (q4_gemm's workspace).  Every output width of the stack
  * except lm_head must be a multiple of 128 (else Q4_ERR_UNSUPPORTED), and the
  * GEMM's K limit applies.  Uses table->layers, hidden, norm_eps, lm_head,
  * final_norm and logits_dtype; ignores M, workspace, flags and plan.

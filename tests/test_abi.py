@@ -60,7 +60,7 @@ int main(void) {
   P(q4_segment) P(q4_gemv_desc) P(q4_linear) P(q4_layer_weights) P(q4_layer_table)
   P(q4_decode_buffers_t) P(q4_moe_desc) P(q4_gemm_desc)
   O(q4_gemm_desc, X) O(q4_gemm_desc, w) O(q4_gemm_desc, up) O(q4_gemm_desc, mode) O(q4_gemm_desc, Y)
-  O(q4_gemm_desc, residual) P(q4_attention_desc) O(q4_attention_desc, rope_theta) O(q4_attention_desc, a)
+  O(q4_gemm_desc, residual) O(q4_gemm_desc, workspace_bytes) P(q4_attention_desc) O(q4_attention_desc, rope_theta) O(q4_attention_desc, a)
   O(q4_attention_desc, workspace_bytes) O(q4_layer_weights, k_cache) O(q4_layer_weights, v_cache)
   O(q4_layer_table, head_dim) O(q4_layer_table, rope_theta) O(q4_layer_table, pos) O(q4_decode_buffers_t, a)
   O(q4_gemv_desc, seg) O(q4_gemv_desc, out_dtype) O(q4_gemv_desc, mode)
@@ -181,8 +181,14 @@ def test_gemm_and_prefill_validation(L):
              "up": lin(256, 64), "down": lin(64, 256)}
     t = q4.LayerTable([layer], lin(100, 64), hidden=64, M=1)
     n8 = q4.q4_prefill_workspace_bytes(t, 8)
-    # n [8][64], q [8][128], k, v [8][128], act [8][256] fp16, each slice rounded to 256 B
-    assert n8 == 1024 + 2048 + 2048 + 2048 + 4096
+    # n [8][64], q [8][128], k, v [8][128], act [8][256] fp16, each slice rounded
+    # to 256 B, then the fp32 partials of split GEMMs: none here (K <= 256 is
+    # at most 4 K steps), so one 256-byte slice
+    assert n8 == 1024 + 2048 + 2048 + 2048 + 4096 + 256
+    assert L.q4_gemm_workspace_bytes(512, 1024, 3072, 0) == 6 * 512 * 1024 * 4   # 32 tiles -> 6 parts of 8 K steps
+    assert L.q4_gemm_workspace_bytes(512, 3072, 1024, 1) == 2 * 2 * 512 * 3072 * 4
+    assert L.q4_gemm_workspace_bytes(2048, 2048, 1024, 0) == 0                    # 256 tiles: no split
+    assert L.q4_gemm_workspace_bytes(512, 1024, 192, 0) == 0                      # 3 K steps: too few to split
     assert L.q4_prefill_workspace_bytes(ctypes.byref(t.t), 0) == 0
     assert L.q4_prefill(ctypes.byref(t.t), FAKE, 4, 0, None, FAKE, n8, None) == -1      # chunk 0
     assert L.q4_prefill(ctypes.byref(t.t), FAKE, 4, 16, None, FAKE * 256, n8, None) == -1  # workspace too small

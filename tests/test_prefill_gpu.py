@@ -25,7 +25,8 @@ def lin(m):
     return (*dev_q4(m), m.N, m.K)
 
 
-def run_gemm(w, X, mode=q4.Q4_GEMV_PLAIN, out_dtype=q4.Q4_F32, up=None, residual=None, in_place=False):
+def run_gemm(w, X, mode=q4.Q4_GEMV_PLAIN, out_dtype=q4.Q4_F32, up=None, residual=None, in_place=False,
+             split=False):
     M, N = X.shape[0], w.N
     dt = torch.float16 if out_dtype == q4.Q4_F16 else torch.float32
     if in_place:
@@ -34,7 +35,13 @@ def run_gemm(w, X, mode=q4.Q4_GEMV_PLAIN, out_dtype=q4.Q4_F32, up=None, residual
     else:
         Y = torch.full((M, N), float("nan"), dtype=dt, device="cuda")
         res = None if residual is None else torch_dev(residual)
-    q4.q4_gemm(lin(w), torch_dev(X), Y, M, mode, out_dtype, up=None if up is None else lin(up), residual=res)
+    ws, nws = None, 0
+    if split:
+        nws = q4.q4_gemm_workspace_bytes(M, N, w.K, mode)
+        assert nws > 0, "this shape should split K"
+        ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    q4.q4_gemm(lin(w), torch_dev(X), Y, M, mode, out_dtype, up=None if up is None else lin(up), residual=res,
+               workspace=ws, workspace_bytes=nws)
     torch.cuda.synchronize()
     assert q4.q4_device_status() == 0
     return Y.float().cpu().numpy()
@@ -79,6 +86,27 @@ def test_gemm_residual_epilogue(in_place):
     y, A = oracle.gemv(W.Wq, W.scales, W.biases, X)
     r = R.astype(np.float64)
     assert_parity(Y, r + y, A + np.abs(r), fp16_out=True, what=f"residual in_place={in_place}")
+
+
+@pytest.mark.parametrize("M", [1, 130, 512])
+def test_gemm_split_k_every_element(M):
+    """Few output tiles: K split over units, fp32 partials, reduce kernel
+    (plain fp32 and fp16, GLU, residual in place)."""
+    N, K = 256, 1024
+    W = q4synth.q4_matrix(550 + M, N, K)
+    X = q4synth.activations(551 + M, M, K)
+    y_ref, A = oracle.gemv(W.Wq, W.scales, W.biases, X)
+    for out_dtype in (0, 1):
+        Y = run_gemm(W, X, out_dtype=out_dtype, split=True)
+        assert_parity(Y, y_ref, A, fp16_out=bool(out_dtype), what=f"split M={M}")
+    R = q4synth.activations(552 + M, M, N)
+    Y = run_gemm(W, X, out_dtype=q4.Q4_F16, residual=R, in_place=True, split=True)
+    r = R.astype(np.float64)
+    assert_parity(Y, r + y_ref, A + np.abs(r), fp16_out=True, what=f"split residual M={M}")
+    gate, up = q4synth.q4_matrix(553, N, K), q4synth.q4_matrix(554, N, K)
+    H = run_gemm(gate, X, q4.Q4_GEMV_GLU, q4.Q4_F16, up=up, split=True)
+    act, A2 = glu_ref(gate, up, X)
+    assert_parity(H, act, A2, fp16_out=True, what=f"split glu M={M}")
 
 
 def test_gemm_qwen3_shapes_sampled_rows():
