@@ -287,18 +287,13 @@ q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_
     else
         q4a::rope_append_kernel<false><<<d.n_kv_heads, D / 2, 0, s>>>(d.k, d.v, d.k_cache, d.v_cache, d.pos, D,
                                                                        d.max_seq, l2t, cs, dev->err_word);
-    static bool configured[64][2] = {};
-    const int di = dev->device >= 0 && dev->device < 64 ? dev->device : 0, ti = D == 128 ? 1 : 0;
-    if (!configured[di][ti]) {
-        cudaError_t e = D == 128 ? cudaFuncSetAttribute(q4a::attn_split_kernel<128>,
-                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                        (int)q4a::split_smem(128))
-                                 : cudaFuncSetAttribute(q4a::attn_split_kernel<64>,
-                                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                        (int)q4a::split_smem(64));
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(attn_split_kernel)");
-        configured[di][ti] = true;
-    }
+    static std::atomic<int> marks128[64], marks64[64];
+    const cudaError_t ea =
+        D == 128 ? ensure_smem_attr(reinterpret_cast<const void*>(q4a::attn_split_kernel<128>), marks128,
+                                    (int)q4a::split_smem(128))
+                 : ensure_smem_attr(reinterpret_cast<const void*>(q4a::attn_split_kernel<64>), marks64,
+                                    (int)q4a::split_smem(64));
+    if (ea != cudaSuccess) return cuda_fail(ea, "cudaFuncSetAttribute(attn_split_kernel)");
     const dim3 grid(d.n_kv_heads, ns);
     if (D == 128)
         q4a::attn_split_kernel<128><<<grid, q4a::kThreads, q4a::split_smem(128), s>>>(

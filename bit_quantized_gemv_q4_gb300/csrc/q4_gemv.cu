@@ -1060,14 +1060,9 @@ uint32_t x_smem_bytes(int M, int K) {
 template <int M, int BITS>
 cudaError_t launch_m(const Params& p, dim3 grid, size_t smem, cudaStream_t stream, bool pdl) {
     auto kern = q4k::q4_gemv_kernel<M, BITS>;
-    static int configured_smem[64] = {0};  // per device: largest dynamic smem set so far
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && (int)smem > configured_smem[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured_smem[dev] = (int)smem;
-    }
+    static std::atomic<int> smem_marks[64];
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem_marks, (int)smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = dim3(q4k::kThreads);
@@ -1298,14 +1293,9 @@ namespace {
 template <int M>
 cudaError_t launch_persistent_m(const q4k::StepParams& sp, const PersistentGeom& g, cudaStream_t stream) {
     auto kern = q4k::q4_decode_persistent_kernel<M>;
-    static int configured_smem[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && (int)g.smem > configured_smem[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)g.smem);
-        if (e != cudaSuccess) return e;
-        configured_smem[dev] = (int)g.smem;
-    }
+    static std::atomic<int> smem_marks[64];
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), smem_marks, (int)g.smem);
+    if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(g.grid);
     cfg.blockDim = dim3(q4k::kThreads);

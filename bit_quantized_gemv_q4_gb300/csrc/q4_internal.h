@@ -2,6 +2,8 @@
 #pragma once
 
 #include <cuda_runtime.h>
+
+#include <atomic>
 #include <stddef.h>
 #include <stdint.h>
 
@@ -28,6 +30,24 @@ struct DeviceInfo {
 q4_status current_device(const DeviceInfo** out);
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Raise a kernel's dynamic shared-memory limit to `bytes` on the current
+// device when it is not already that high (the attribute persists).  `marks`
+// is the call site's per-device high-water mark (64 devices), kept in atomics
+// so concurrent host threads may launch; two threads may both set the
+// attribute, which is harmless.
+inline cudaError_t ensure_smem_attr(const void* kern, std::atomic<int>* marks, int bytes) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const bool tracked = dev >= 0 && dev < 64;
+    if (tracked && bytes <= marks[dev].load(std::memory_order_acquire)) return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess || !tracked) return e;
+    int cur = marks[dev].load(std::memory_order_relaxed);
+    while (bytes > cur && !marks[dev].compare_exchange_weak(cur, bytes, std::memory_order_acq_rel)) {
+    }
+    return cudaSuccess;
+}
 
 // ---- decode attention (q4_attn.cu) -----------------------------------------
 size_t attn_workspace_bytes(int n_q_heads, int head_dim, int max_seq);

@@ -583,15 +583,16 @@ typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
 EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
+    // looked up once (thread-safe initialisation of a function-local static)
+    static const EncodeTiledFn fn = [] {
         void* p = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
+            return reinterpret_cast<EncodeTiledFn>(p);
+        return static_cast<EncodeTiledFn>(nullptr);
+    }();
     return fn;
 }
 
@@ -719,13 +720,9 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (a.offsets)
         q4g::check_routing_kernel<<<(a.R + 255) / 256 < dev->sms ? (a.R + 255) / 256 : dev->sms, 256, 0, s>>>(
             a.expert_ids, a.offsets, a.E, a.R, dev->err_word);
-    static int configured_smem[64] = {0};  // per device: the largest dynamic size set so far
-    cudaError_t e = cudaSuccess;
-    if (dev->device < 0 || dev->device >= 64 || (int)smem > configured_smem[dev->device]) {
-        e = cudaFuncSetAttribute(q4g::q4_moe_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
-        if (dev->device >= 0 && dev->device < 64) configured_smem[dev->device] = (int)smem;
-    }
+    static std::atomic<int> smem_marks[64];
+    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel), smem_marks, (int)smem);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
     q4g::q4_moe_gemm_kernel<<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
