@@ -21,7 +21,9 @@
 // the chunks' (max, sum, partial output) per head.  The rotation's sines and
 // cosines are computed once per step in fp64 (the angle pos * theta^(-2i/d)
 // reaches thousands of radians) by the first append kernel of the step into a
-// table the other kernels read; the rotations themselves are fp32.
+// table the other kernels read; the rotations themselves are fp32.  Inside a
+// decode step only the first layer launches that append kernel: in the other
+// layers the CTA whose chunk holds the new position appends the token itself.
 #include <cuda_fp16.h>
 #include <math.h>
 
@@ -90,12 +92,16 @@ constexpr size_t split_smem(int D) {
 // m = max score, l = sum exp(s - m), acc = sum exp(s - m) v over the chunk.
 template <int D>
 __global__ void __launch_bounds__(kThreads) attn_split_kernel(const uint16_t* __restrict__ q,
-                                                              const uint16_t* __restrict__ kc,
-                                                              const uint16_t* __restrict__ vc, const int32_t* pos_p,
+                                                              const uint16_t* kc,  // bulk-copy sources; the
+                                                              const uint16_t* vc,  // append writes via kc_w / vc_w
+                                                              const int32_t* pos_p,
                                                               int G, int max_seq, int n_splits,
                                                               const float2* __restrict__ cs,
                                                               float* __restrict__ part_ml,
-                                                              float* __restrict__ part_acc, int* err) {
+                                                              float* __restrict__ part_acc,
+                                                              const uint16_t* __restrict__ k_new,
+                                                              const uint16_t* __restrict__ v_new,
+                                                              uint16_t* kc_w, uint16_t* vc_w, int* err) {
     extern __shared__ __align__(128) uint8_t smem[];
     uint16_t* ks = reinterpret_cast<uint16_t*>(smem);  // [kChunk][D]
     uint16_t* vs = ks + kChunk * D;                    // [kChunk][D]
@@ -137,6 +143,30 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const uint16_t* __
     if (__syncthreads_or(late)) {
         q4d::mbar_wait(b, 0, nullptr);
         return;
+    }
+    // Without a separate append launch (k_new set), the CTA whose chunk holds
+    // the new position rotates the token's key, stores key and value in the
+    // cache and over the stale row of its shared copy.
+    if (k_new && pos >= j0 && pos < j1) {
+        const int rs = pos - j0;
+        const size_t base = ((size_t)kvh * max_seq + pos) * D;
+        for (int i = tid; i < D / 2; i += kThreads) {
+            const float2 r = cs[i];
+            const float lo = __half2float(__ushort_as_half(k_new[kvh * D + i]));
+            const float hi = __half2float(__ushort_as_half(k_new[kvh * D + i + D / 2]));
+            const uint16_t klo = __half_as_ushort(__float2half_rn(lo * r.x - hi * r.y));
+            const uint16_t khi = __half_as_ushort(__float2half_rn(hi * r.x + lo * r.y));
+            const uint16_t vlo = v_new[kvh * D + i], vhi = v_new[kvh * D + i + D / 2];
+            ks[rs * D + i] = klo;
+            ks[rs * D + i + D / 2] = khi;
+            vs[rs * D + i] = vlo;
+            vs[rs * D + i + D / 2] = vhi;
+            kc_w[base + i] = klo;
+            kc_w[base + i + D / 2] = khi;
+            vc_w[base + i] = vlo;
+            vc_w[base + i + D / 2] = vhi;
+        }
+        __syncthreads();
     }
     // scores: a warp per position, lanes across d
     constexpr int E = D / 32;  // elements per lane (2 or 4)
@@ -281,12 +311,12 @@ q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_
     float* ml = reinterpret_cast<float*>(w + 256 * (((size_t)D / 2 * 8 + 255) / 256));
     float* acc = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(ml) +
                                           (((size_t)d.n_q_heads * ns * 2 * 4 + 255) & ~size_t(255)));
+    // The first attention of a step computes the cos/sin table in its append
+    // kernel; later ones append inside the split kernel (one launch fewer).
     if (compute_table)
         q4a::rope_append_kernel<true><<<d.n_kv_heads, D / 2, 0, s>>>(d.k, d.v, d.k_cache, d.v_cache, d.pos, D,
                                                                       d.max_seq, l2t, cs, dev->err_word);
-    else
-        q4a::rope_append_kernel<false><<<d.n_kv_heads, D / 2, 0, s>>>(d.k, d.v, d.k_cache, d.v_cache, d.pos, D,
-                                                                       d.max_seq, l2t, cs, dev->err_word);
+    const uint16_t* k_new = compute_table ? nullptr : d.k;
     static std::atomic<int> marks128[64], marks64[64];
     const cudaError_t ea =
         D == 128 ? ensure_smem_attr(reinterpret_cast<const void*>(q4a::attn_split_kernel<128>), marks128,
@@ -297,10 +327,12 @@ q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_
     const dim3 grid(d.n_kv_heads, ns);
     if (D == 128)
         q4a::attn_split_kernel<128><<<grid, q4a::kThreads, q4a::split_smem(128), s>>>(
-            d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns, cs, ml, acc, dev->err_word);
+            d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns, cs, ml, acc, k_new, d.v, d.k_cache, d.v_cache,
+            dev->err_word);
     else
         q4a::attn_split_kernel<64><<<grid, q4a::kThreads, q4a::split_smem(64), s>>>(
-            d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns, cs, ml, acc, dev->err_word);
+            d.q, d.k_cache, d.v_cache, d.pos, G, d.max_seq, ns, cs, ml, acc, k_new, d.v, d.k_cache, d.v_cache,
+            dev->err_word);
     q4a::attn_combine_kernel<<<d.n_q_heads, D, 0, s>>>(ml, acc, d.pos, D, d.max_seq, ns, d.a);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "attention launch");
