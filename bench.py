@@ -420,6 +420,54 @@ def q8_lm_head(q4, device, M: int = 1):
             "shape": f"M={M} N={N} K={K}, 8-bit codes (1.0625 B/weight), 4 rotating copies"}
 
 
+def decode_streams(device, steps: int = 200, warmup: int = 10):
+    """Decode steps of the larger stacks the parity tests cover: Llama-3.2-3B
+    shaped at M = 1 and M = 4, Qwen3-4B shaped at M = 1 (random Q4 weights
+    drawn on the device; 1.8-2.3 GB per step, so no L2 reuse)."""
+    import torch
+
+    import bit_quantized_gemv_q4_gb300 as q4
+    import q4synth
+    peak, kind = peaks()
+    out = {"peak_kind": kind}
+    for shape, M in ((q4synth.LLAMA32_3B, 1), (q4synth.LLAMA32_3B, 4), (q4synth.QWEN3_4B, 1)):
+        gen = torch.Generator(device=device).manual_seed(4000 + M)
+
+        def mat(N, K):
+            Wq = torch.randint(-2**31, 2**31 - 1, (N, K // 8), dtype=torch.int32, device=device, generator=gen)
+            s = (torch.rand(N, K // 64, device=device, generator=gen) * 0.005).half()
+            return (Wq, s, (-8 * s.float()).half(), N, K)
+
+        dl = [{nm: mat(N, K) for nm, N, K in shape.layer_linears()} for _ in range(shape.n_layers)]
+        dlm = mat(shape.vocab, shape.hidden)
+        table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
+        nws = q4.q4_decode_workspace_bytes(table)
+        ws = torch.empty(nws, dtype=torch.uint8, device=device)
+        table.set_workspace(ws, nws)
+        x = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4246, M, shape.hidden)).to(device)
+        logits = torch.empty(M, shape.vocab, dtype=torch.float32, device=device)
+        stream = torch.cuda.current_stream(device)
+        for _ in range(warmup):
+            q4.q4_decode_step(table, x, logits, stream)
+        torch.cuda.synchronize(device)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            q4.q4_decode_step(table, x, logits, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if q4.q4_device_status(stream) != 0:
+            raise RuntimeError("device status after stream timing")
+        ms = e0.elapsed_time(e1) / steps
+        gbs = shape.weight_bytes_per_step() / (ms * 1e-3) / 1e9  # weight bytes only (activations < 0.1 %)
+        out[f"{shape.name} M={M}"] = {"ms": ms, "tok_per_s": M * 1000.0 / ms, "launches": 4 * shape.n_layers + 1,
+                                      "weight_bytes": shape.weight_bytes_per_step(), "gbs": gbs, "frac": gbs / peak}
+        table.release()
+        del dl, dlm, table, ws
+        torch.cuda.empty_cache()
+    return out
+
+
 def bits_lm_head(q4, device, widths=(2, 3, 5, 6)):
     """The lm_head-shaped GEMV (M=1, N=151936, K=1024) with b-bit codes:
     8 warm-up launches, then 64 timed over 4 distinct weight copies (> L2)."""
@@ -505,7 +553,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head", "prefill", "attention"],
+    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head", "prefill", "attention", "streams"],
                     help="moe / lm_head: only the MoE prefill timings / the lm_head GEMV timing "
                          "(for profiling runs)")
     args = ap.parse_args()
@@ -571,6 +619,9 @@ def main():
     device = torch.device("cuda", local)
     if args.section == "moe":
         print(json.dumps({"moe_prefill": moe_prefill(device)}))
+        return
+    if args.section == "streams":
+        print(json.dumps({"decode_streams": decode_streams(device)}))
         return
     if world > 1:
         import torch.distributed as dist
