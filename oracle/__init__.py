@@ -434,6 +434,47 @@ def decode_step_attn(layers, lm_head, x, caches, pos: int, head_dim: int, theta:
     return y, A, h
 
 
+def prefill_layer_attn(layer, h, k_cache, v_cache, pos0: int, head_dim: int, theta: float = DEFAULT_ROPE_THETA,
+                       eps: float = DEFAULT_EPS):
+    """prefill_layer with attention: tokens t = 0..T-1 sit at positions
+    pos0 + t; their rotated keys and values are written to the caches (fp16),
+    then token t attends over positions 0..pos0+t (causal), a rounded to fp16
+    feeds o.  The normalised activations are stored in fp16 as in
+    prefill_layer."""
+    h = np.atleast_2d(h)
+    T = h.shape[0]
+    Hkv = k_cache.shape[0]
+    n = fp16(rmsnorm(h, layer.get("attn_norm"), eps))
+    q = fp16(gemv(*_mat(layer["q"]), n)[0])
+    k = fp16(gemv(*_mat(layer["k"]), n)[0])
+    v = fp16(gemv(*_mat(layer["v"]), n)[0])
+    for t in range(T):
+        k_cache[:, pos0 + t] = fp16(rope(k[t], pos0 + t, head_dim, theta)).reshape(Hkv, head_dim)
+        v_cache[:, pos0 + t] = v[t].reshape(Hkv, head_dim)
+    a = np.stack([fp16(attention(q[t], k_cache, v_cache, pos0 + t + 1, head_dim, pos0 + t, theta)[0])
+                  for t in range(T)])
+    hm = fp16(decode_o(layer, a, h)[0])
+    n2 = fp16(rmsnorm(hm, layer.get("ffn_norm"), eps))
+    g = gemv(*_mat(layer["gate"]), n2)[0]
+    u = gemv(*_mat(layer["up"]), n2)[0]
+    act = fp16(silu(g) * u)
+    ho = fp16(decode_down(layer, act, hm)[0])
+    return {"n": n, "q": q, "k": k, "v": v, "a": a, "h_mid": hm, "n2": n2, "act": act, "h": ho}
+
+
+def prefill_attn(layers, lm_head, x, caches, pos0: int, head_dim: int, theta: float = DEFAULT_ROPE_THETA,
+                 final_norm=None, eps: float = DEFAULT_EPS):
+    """Prefill of T tokens at positions pos0.. with attention, filling the
+    caches: (final h [T, hidden], logits y [1, vocab] and A of the last token).
+    Chunking does not change the result (keys of earlier chunks are in the
+    cache before later tokens attend to them)."""
+    h = np.atleast_2d(x).astype(np.float16)
+    for layer, (kc, vc) in zip(layers, caches):
+        h = prefill_layer_attn(layer, h, kc, vc, pos0, head_dim, theta, eps)["h"]
+    y, A = decode_logits(lm_head, h[-1:], final_norm, eps=eps)
+    return h, y, A
+
+
 # --------------------------------------------------------------------- MoE ---
 
 def moe_route(logits, topk: int):

@@ -108,3 +108,46 @@ def test_layer_with_attention_wiring():
     hi = np.maximum(vc[:, 0], vc[:, 1])[[0, 0, 1, 1]].reshape(-1)
     a = o1["a"][0].astype(np.float64)
     assert np.all(a >= lo - 1e-3 * np.abs(lo)) and np.all(a <= hi + 1e-3 * np.abs(hi))
+
+
+def test_prefill_with_attention_equals_token_by_token_decode():
+    """Prefill of T tokens with causal attention equals T decode steps with
+    the normalised activations stored in fp16 -- checked against a decode
+    composition built here from the pinned pieces (rmsnorm, gemv, rope,
+    attention) one token at a time, with the caches filled in order."""
+    import q4synth
+    shape = q4synth.tiny_decode_shape(n_layers=2, hidden=128, q=256, kv=128, ffn=256, vocab=64)
+    layers, lm = q4synth.decode_weights(shape, base_seed=97)
+    d, Hkv, T, pos0 = 64, 2, 5, 3
+    g = np.random.default_rng(98)
+    base_k = g.standard_normal((2, Hkv, 16, d)).astype(np.float16)
+    base_v = g.standard_normal((2, Hkv, 16, d)).astype(np.float16)
+    caches_a = [(base_k[i].copy(), base_v[i].copy()) for i in range(2)]
+    caches_b = [(base_k[i].copy(), base_v[i].copy()) for i in range(2)]
+    x = q4synth.activations(99, T, 128)
+    h_a, y_a, _ = oracle.prefill_attn(layers, lm, x, caches_a, pos0, d)
+    hs = []
+    for t in range(T):
+        h = x[t:t + 1].astype(np.float16)
+        for layer, (kc, vc) in zip(layers, caches_b):
+            n = oracle.fp16(oracle.rmsnorm(h, layer.get("attn_norm")))
+            qkv = {nm: oracle.fp16(oracle.gemv(layer[nm].Wq, layer[nm].scales, layer[nm].biases, n)[0])[0]
+                   for nm in ("q", "k", "v")}
+            kc[:, pos0 + t] = oracle.fp16(oracle.rope(qkv["k"], pos0 + t, d)).reshape(Hkv, d)
+            vc[:, pos0 + t] = qkv["v"].reshape(Hkv, d)
+            a = oracle.fp16(oracle.attention(qkv["q"], kc, vc, pos0 + t + 1, d, pos0 + t)[0])[None, :]
+            hm = oracle.fp16(oracle.decode_o(layer, a, h)[0])
+            n2 = oracle.fp16(oracle.rmsnorm(hm, layer.get("ffn_norm")))
+            gg = oracle.gemv(layer["gate"].Wq, layer["gate"].scales, layer["gate"].biases, n2)[0]
+            uu = oracle.gemv(layer["up"].Wq, layer["up"].scales, layer["up"].biases, n2)[0]
+            act = oracle.fp16(oracle.silu(gg) * uu)
+            h = oracle.fp16(oracle.decode_down(layer, act, hm)[0]).astype(np.float16)
+        hs.append(h[0])
+    assert np.array_equal(h_a, np.stack(hs))
+    for (ka, va), (kb, vb) in zip(caches_a, caches_b):
+        assert np.array_equal(ka, kb) and np.array_equal(va, vb)
+    # chunking: the first 2 tokens, then the other 3, from the same start
+    caches_c = [(base_k[i].copy(), base_v[i].copy()) for i in range(2)]
+    h1, _, _ = oracle.prefill_attn(layers, lm, x[:2], caches_c, pos0, d)
+    h2, y2, _ = oracle.prefill_attn(layers, lm, x[2:], caches_c, pos0 + 2, d)
+    assert np.array_equal(np.concatenate([h1, h2]), h_a) and np.array_equal(y2, y_a)
