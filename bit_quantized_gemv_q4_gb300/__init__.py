@@ -40,7 +40,8 @@ EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status"
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
            "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
            "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine", "q4_gemm", "q4_prefill_workspace_bytes",
-           "q4_prefill", "q4_attention_workspace_bytes", "q4_attention", "q4_gemm_workspace_bytes"]
+           "q4_prefill", "q4_attention_workspace_bytes", "q4_attention", "q4_gemm_workspace_bytes",
+           "q4_prefill_buffers"]
 
 
 class Q4Error(RuntimeError):
@@ -94,6 +95,10 @@ class q4_attention_desc(ctypes.Structure):
     _fields_ = [("q", vp), ("k", vp), ("v", vp), ("k_cache", vp), ("v_cache", vp), ("pos", vp),
                 ("n_q_heads", i32), ("n_kv_heads", i32), ("head_dim", i32), ("max_seq", i32),
                 ("rope_theta", ctypes.c_float), ("a", vp), ("workspace", vp), ("workspace_bytes", ctypes.c_size_t)]
+
+
+class q4_prefill_buffers_t(ctypes.Structure):
+    _fields_ = [(n, vp) for n in ("n", "q", "k", "v", "act", "a")]
 
 
 class q4_gemm_desc(ctypes.Structure):
@@ -157,6 +162,8 @@ def lib() -> ctypes.CDLL:
         L.q4_prefill_workspace_bytes.argtypes = [ctypes.POINTER(q4_layer_table), i32]
         L.q4_prefill.restype = st
         L.q4_prefill.argtypes = [ctypes.POINTER(q4_layer_table), vp, i32, i32, vp, vp, ctypes.c_size_t, vp]
+        L.q4_prefill_buffers.restype = st
+        L.q4_prefill_buffers.argtypes = [ctypes.POINTER(q4_layer_table), i32, vp, ctypes.POINTER(q4_prefill_buffers_t)]
         L.q4_attention_workspace_bytes.restype = ctypes.c_size_t
         L.q4_attention_workspace_bytes.argtypes = [i32, i32, i32]
         L.q4_attention.restype = st
@@ -394,3 +401,10 @@ def q4_attention(q, k, v, k_cache, v_cache, pos, n_q_heads: int, n_kv_heads: int
     d = q4_attention_desc(_ptr(q), _ptr(k), _ptr(v), _ptr(k_cache), _ptr(v_cache), _ptr(pos), n_q_heads,
                           n_kv_heads, head_dim, max_seq, rope_theta, _ptr(a), _ptr(workspace), workspace_bytes)
     _check(lib().q4_attention(ctypes.byref(d), _stream(stream)), "q4_attention")
+
+
+def q4_prefill_buffers(table: LayerTable, chunk: int, workspace) -> dict:
+    b = q4_prefill_buffers_t()
+    _check(lib().q4_prefill_buffers(ctypes.byref(table.t), chunk, _ptr(workspace), ctypes.byref(b)),
+           "q4_prefill_buffers")
+    return {n: getattr(b, n) for n in ("n", "q", "k", "v", "act", "a")}

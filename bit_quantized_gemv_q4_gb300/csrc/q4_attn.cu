@@ -265,7 +265,170 @@ __global__ void attn_combine_kernel(const float* __restrict__ part_ml, const flo
     a[h * d + t] = __half_as_ushort(__float2half_rn(acc / L));
 }
 
-__global__ void pos_advance_kernel(int32_t* pos_p) { *pos_p += 1; }
+__global__ void pos_advance_kernel(int32_t* pos_p, int by) { *pos_p += by; }
+
+// ------------------------------------------------------------ prefill ---
+// Prompt tokens t = 0..C-1 of a chunk sit at positions *pos_p + t0 + t.
+
+// (cos, sin) of every (token, pair) of the chunk, fp64 angles (one table per
+// chunk, shared by every layer).  Grid C, block d/2.
+__global__ void prefill_cs_kernel(const int32_t* pos_p, int t0, int d, double log2_theta, float2* cs) {
+    const int t = blockIdx.x, i = threadIdx.x;
+    float c, s;
+    rope_cs(*pos_p + t0 + t, i, d, log2_theta, c, s);
+    cs[(size_t)t * (d / 2) + i] = make_float2(c, s);
+}
+
+// Rotated keys and values of the chunk into the caches.  Grid (C, Hkv),
+// block d/2.  k, v: [C][Hkv*d].
+__global__ void prefill_append_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
+                                      uint16_t* __restrict__ kc, uint16_t* __restrict__ vc, const int32_t* pos_p,
+                                      int t0, int C, int Hkv, int d, int max_seq, const float2* __restrict__ cs,
+                                      int* err) {
+    const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = d / 2;
+    const int p0 = *pos_p + t0;
+    if (p0 < 0 || p0 + C > max_seq) {
+        if (t == 0 && h == 0 && i == 0) atomicOr(err, q4d::kErrDeviceCheck);
+        return;
+    }
+    const float2 r = cs[(size_t)t * half + i];
+    const size_t src = (size_t)t * Hkv * d + (size_t)h * d;
+    const float lo = __half2float(__ushort_as_half(k[src + i]));
+    const float hi = __half2float(__ushort_as_half(k[src + i + half]));
+    const size_t base = ((size_t)h * max_seq + p0 + t) * d;
+    kc[base + i] = __half_as_ushort(__float2half_rn(lo * r.x - hi * r.y));
+    kc[base + i + half] = __half_as_ushort(__float2half_rn(hi * r.x + lo * r.y));
+    vc[base + i] = v[src + i];
+    vc[base + i + half] = v[src + i + half];
+}
+
+constexpr int kPQ = 8;   // query tokens per CTA (a warp each)
+constexpr int kPK = 64;  // key positions per staged chunk
+
+constexpr size_t prefill_smem(int D) { return (size_t)2 * kPK * D * 2 + (size_t)kPQ * kPK * 4; }
+
+// Causal attention of the chunk's tokens for query head blockIdx.x: token t
+// attends over positions 0..p0+t.  Key/value chunks of 64 positions are
+// bulk-copied into shared memory (one mbarrier phase per chunk); each warp
+// scores its token against the chunk (lanes across d), then updates its
+// running max, sum and output with the chunk's exp(s - max).
+template <int D>
+__global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* __restrict__ q,
+                                                                const uint16_t* kc, const uint16_t* vc,
+                                                                const int32_t* pos_p, int t0, int C, int Hq,
+                                                                int G, int max_seq, const float2* __restrict__ cs,
+                                                                uint16_t* __restrict__ a, int* err) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);  // [kPK][D]
+    uint16_t* vs = ks + kPK * D;                       // [kPK][D]
+    float* sc = reinterpret_cast<float*>(vs + kPK * D);  // [kPQ][kPK]
+    __shared__ __align__(8) uint64_t bar;
+    constexpr int E = D / 32;
+    const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int kvh = h / G;
+    const int p0 = *pos_p + t0;
+    if (p0 < 0 || p0 + C > max_seq) return;  // latched by the append kernel
+    const int tq0 = blockIdx.y * kPQ;
+    const int t = tq0 + warp;
+    const bool live = t < C;
+    const int last = min(tq0 + kPQ, C) - 1;  // the block's last token
+    const int n_keys = p0 + last + 1;
+    // this warp's rotated query, scaled by 1/sqrt(d): lane holds dims
+    // lane*E .. lane*E+E-1; the pair partner of dim i < d/2 is in lane ^ 16
+    float qr[E];
+    if (live) {
+        const float scale = rsqrtf((float)D);
+        const uint16_t* qrow = q + (size_t)t * Hq * D + (size_t)h * D;
+#pragma unroll
+        for (int e = 0; e < E; ++e) {
+            const float mine = __half2float(__ushort_as_half(qrow[lane * E + e]));
+            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
+            const int i = (lane & 15) * E + e;
+            const float2 r = cs[(size_t)t * (D / 2) + i];
+            qr[e] = (lane < 16 ? mine * r.x - other * r.y : mine * r.x + other * r.y) * scale;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < E; ++e) qr[e] = 0.f;  // a warp past the chunk's last token
+    }
+    const uint32_t b = q4d::smem_addr(&bar);
+    if (threadIdx.x == 0) {
+        q4d::mbar_init(b, 1);
+        q4d::fence_mbar_init();
+    }
+    __syncthreads();
+    float m = -INFINITY, l = 0.f, acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    const int my_n = live ? p0 + t + 1 : 0;  // keys this token sees
+    int phase = 0;
+    for (int j0 = 0; j0 < n_keys; j0 += kPK, phase ^= 1) {
+        const int cnt = min(kPK, n_keys - j0);
+        if (threadIdx.x == 0) {
+            const uint32_t bytes = (uint32_t)cnt * D * 2;
+            q4d::mbar_arrive_expect_tx(b, 2 * bytes);
+            q4d::bulk_g2s(q4d::smem_addr(ks), kc + ((size_t)kvh * max_seq + j0) * D, bytes, b);
+            q4d::bulk_g2s(q4d::smem_addr(vs), vc + ((size_t)kvh * max_seq + j0) * D, bytes, b);
+        }
+        const bool late = !q4d::mbar_wait(b, (uint32_t)phase, err);
+        if (__syncthreads_or(late)) {
+            q4d::mbar_wait(b, (uint32_t)phase, nullptr);
+            return;
+        }
+        const int mine = min(cnt, my_n - j0);  // keys of this chunk the token sees
+        if (mine > 0) {
+            float cmax = -INFINITY;
+            for (int j = 0; j < mine; ++j) {
+                float s = 0.f;
+                if constexpr (E == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(ks + j * D + lane * 4);
+                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+                    const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+                    s = fmaf(qr[0], x.x, fmaf(qr[1], x.y, fmaf(qr[2], y.x, qr[3] * y.y)));
+                } else {
+                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(ks + j * D + lane * 2);
+                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+                    s = fmaf(qr[0], x.x, qr[1] * x.y);
+                }
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+                if (lane == 0) sc[warp * kPK + j] = s;
+                cmax = fmaxf(cmax, s);
+            }
+            __syncwarp();
+            const float mn = fmaxf(m, cmax);
+            const float corr = expf(m - mn);  // 0 on the first chunk (m = -inf)
+            l *= corr;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] *= corr;
+            for (int j = 0; j < mine; ++j) {
+                const float pj = expf(sc[warp * kPK + j] - mn);
+                l += pj;
+                if constexpr (E == 4) {
+                    const uint2 raw = *reinterpret_cast<const uint2*>(vs + j * D + lane * 4);
+                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
+                    const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
+                    acc[0] = fmaf(pj, x.x, acc[0]);
+                    acc[1] = fmaf(pj, x.y, acc[1]);
+                    acc[2] = fmaf(pj, y.x, acc[2]);
+                    acc[3] = fmaf(pj, y.y, acc[3]);
+                } else {
+                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(vs + j * D + lane * 2);
+                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw));
+                    acc[0] = fmaf(pj, x.x, acc[0]);
+                    acc[1] = fmaf(pj, x.y, acc[1]);
+                }
+            }
+            m = mn;
+        }
+        __syncthreads();  // the chunk buffers are refilled next
+    }
+    if (live) {
+        uint16_t* arow = a + (size_t)t * Hq * D + (size_t)h * D + lane * E;
+#pragma unroll
+        for (int e = 0; e < E; ++e) arow[e] = __half_as_ushort(__float2half_rn(acc[e] / l));
+    }
+}
 
 }  // namespace q4a
 
@@ -339,8 +502,45 @@ q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_
     return Q4_OK;
 }
 
-q4_status pos_advance(int32_t* pos, cudaStream_t s) {
-    q4a::pos_advance_kernel<<<1, 1, 0, s>>>(pos);
+size_t prefill_attn_cs_bytes(int chunk, int head_dim) { return (size_t)chunk * head_dim / 2 * 8; }
+
+q4_status prefill_attn_table(const int32_t* pos, int t0, int C, int head_dim, float theta, void* cs, cudaStream_t s) {
+    q4a::prefill_cs_kernel<<<C, head_dim / 2, 0, s>>>(pos, t0, head_dim, log2((double)theta),
+                                                      static_cast<float2*>(cs));
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "prefill rotation table launch");
+    return Q4_OK;
+}
+
+q4_status prefill_attn_enqueue(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* k_cache,
+                               uint16_t* v_cache, const int32_t* pos, int t0, int C, int Hq, int Hkv, int D,
+                               int max_seq, const void* cs, uint16_t* a, cudaStream_t s) {
+    const DeviceInfo* dev = nullptr;
+    q4_status st = current_device(&dev);
+    if (st != Q4_OK) return st;
+    const float2* csp = static_cast<const float2*>(cs);
+    q4a::prefill_append_kernel<<<dim3(C, Hkv), D / 2, 0, s>>>(k, v, k_cache, v_cache, pos, t0, C, Hkv, D, max_seq,
+                                                              csp, dev->err_word);
+    static std::atomic<int> marks128[64], marks64[64];
+    cudaError_t e = D == 128 ? ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_kernel<128>), marks128,
+                                                (int)q4a::prefill_smem(128))
+                             : ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_kernel<64>), marks64,
+                                                (int)q4a::prefill_smem(64));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_attn_kernel)");
+    const dim3 grid(Hq, (C + q4a::kPQ - 1) / q4a::kPQ);
+    if (D == 128)
+        q4a::prefill_attn_kernel<128><<<grid, q4a::kPQ * 32, q4a::prefill_smem(128), s>>>(
+            q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a, dev->err_word);
+    else
+        q4a::prefill_attn_kernel<64><<<grid, q4a::kPQ * 32, q4a::prefill_smem(64), s>>>(
+            q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a, dev->err_word);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
+    return Q4_OK;
+}
+
+q4_status pos_advance(int32_t* pos, cudaStream_t s, int by) {
+    q4a::pos_advance_kernel<<<1, 1, 0, s>>>(pos, by);
     const cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "position advance launch");
     return Q4_OK;

@@ -393,6 +393,7 @@ __global__ void rmsnorm_rows_kernel(const uint16_t* __restrict__ h, const uint16
 
 struct PrefillLayout {
     size_t n = 0, q = 0, k = 0, v = 0, act = 0, part = 0, part_bytes = 0, total = 0;
+    size_t cs = 0, a = 0;  // with attention: the chunk's rotation table and attention output
 };
 
 PrefillLayout prefill_layout(const Dims& d, int chunk, const q4_layer_table* t) {
@@ -423,6 +424,10 @@ PrefillLayout prefill_layout(const Dims& d, int chunk, const q4_layer_table* t) 
     }
     l.part_bytes = pb;
     l.part = take(pb / 2 + 1);
+    if (d.attn) {
+        l.cs = take(prefill_attn_cs_bytes(chunk, d.hd) / 2);
+        l.a = take(C * (d.qN > 0 ? d.qN : 1));
+    }
     l.total = off;
     return l;
 }
@@ -465,6 +470,23 @@ size_t q4_prefill_workspace_bytes(const q4_layer_table* table, int chunk) {
     return prefill_layout(d, chunk, table).total;
 }
 
+q4_status q4_prefill_buffers(const q4_layer_table* table, int chunk, void* workspace, q4_prefill_buffers_t* out) {
+    clear_error();
+    if (!out || !workspace) return fail(Q4_ERR_INVALID_ARG, "out or workspace is NULL");
+    Dims d;
+    q4_status st = prefill_dims(table, chunk, &d);
+    if (st != Q4_OK) return st;
+    const PrefillLayout l = prefill_layout(d, chunk, table);
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    out->n = reinterpret_cast<uint16_t*>(ws + l.n);
+    out->q = reinterpret_cast<uint16_t*>(ws + l.q);
+    out->k = reinterpret_cast<uint16_t*>(ws + l.k);
+    out->v = reinterpret_cast<uint16_t*>(ws + l.v);
+    out->act = reinterpret_cast<uint16_t*>(ws + l.act);
+    out->a = d.attn ? reinterpret_cast<uint16_t*>(ws + l.a) : nullptr;
+    return Q4_OK;
+}
+
 q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk, void* logits, void* workspace,
                      size_t workspace_bytes, q4_stream_t stream) {
     clear_error();
@@ -493,11 +515,15 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
     uint16_t* act = reinterpret_cast<uint16_t*>(ws + l.act);
     void* part = ws + l.part;
     const size_t pb = l.part_bytes;
+    void* cs = ws + l.cs;
+    uint16_t* a_buf = reinterpret_cast<uint16_t*>(ws + l.a);
     const int H = d.hidden;
     for (int t0 = 0; t0 < T; t0 += chunk) {
         const int C = T - t0 < chunk ? T - t0 : chunk;
         uint16_t* hc = h + (size_t)t0 * H;
         const int nb = (C + 7) / 8;
+        if (d.attn && (st = prefill_attn_table(table->pos, t0, C, d.hd, table->rope_theta, cs, s)) != Q4_OK)
+            return st;
         for (int i = 0; i < d.L; ++i) {
             const q4_layer_weights& w = table->layers[i];
             rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.attn_norm, n, C, H, eps);
@@ -506,13 +532,21 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
             if ((st = gemm_of(w.q, nullptr, n, C, q, nullptr, part, pb, s)) != Q4_OK) return st;
             if ((st = gemm_of(w.k, nullptr, n, C, k, nullptr, part, pb, s)) != Q4_OK) return st;
             if ((st = gemm_of(w.v, nullptr, n, C, v, nullptr, part, pb, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.o, nullptr, q, C, hc, hc, part, pb, s)) != Q4_OK) return st;  // h' = h + Wo q
+            const uint16_t* o_in = q;
+            if (d.attn) {
+                if ((st = prefill_attn_enqueue(q, k, v, w.k_cache, w.v_cache, table->pos, t0, C, w.q.N / d.hd,
+                                               w.k.N / d.hd, d.hd, d.max_seq, cs, a_buf, s)) != Q4_OK)
+                    return st;
+                o_in = a_buf;
+            }
+            if ((st = gemm_of(w.o, nullptr, o_in, C, hc, hc, part, pb, s)) != Q4_OK) return st;  // h' = h + Wo a
             rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.ffn_norm, n, C, H, eps);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
             if ((st = gemm_of(w.gate, &w.up, n, C, act, nullptr, part, pb, s)) != Q4_OK) return st;
             if ((st = gemm_of(w.down, nullptr, act, C, hc, hc, part, pb, s)) != Q4_OK) return st;  // h = h' + Wdown act
         }
     }
+    if (d.attn && T > 0 && (st = pos_advance(table->pos, s, T)) != Q4_OK) return st;
     if (logits && T > 0) {
         q4_gemv_desc g = {};
         g.M = 1;

@@ -454,10 +454,25 @@ size_t q4_prefill_workspace_bytes(const q4_layer_table *table, int chunk);
  * the GEMMs that split K (q4_gemm's workspace).  Every output width of the stack
  * except lm_head must be a multiple of 128 (else Q4_ERR_UNSUPPORTED), and the
  * GEMM's K limit applies.  Uses table->layers, hidden, norm_eps, lm_head,
- * final_norm and logits_dtype; ignores M, workspace, flags and plan.
- * chunk >= 1, T >= 0; allocates nothing. */
+ * final_norm and logits_dtype; ignores M, workspace and plan, and of the
+ * flags reads only Q4_DECODE_ATTENTION: with it, token t of the prompt sits
+ * at position p = *table->pos + t, its RoPE-rotated key and value are
+ * written to position p of every layer's cache, it attends causally over
+ * positions 0..p (a = fp16 attention output, replacing q as the input of o),
+ * and *pos advances by T at the end, so decode steps continue the sequence;
+ * positions beyond max_seq latch Q4_ERR_DEVICE_CHECK.  chunk >= 1, T >= 0;
+ * allocates nothing. */
 q4_status q4_prefill(const q4_layer_table *table, uint16_t *h, int T, int chunk, void *logits,
                      void *workspace, size_t workspace_bytes, q4_stream_t stream);
+
+/* Device pointers into a q4_prefill workspace (fp16, [chunk][width]): the
+ * last chunk's n' (the ffn norm output), q, k, v, act and, with
+ * Q4_DECODE_ATTENTION, the attention output a (else NULL). */
+typedef struct q4_prefill_buffers_t {
+    uint16_t *n, *q, *k, *v, *act, *a;
+} q4_prefill_buffers_t;
+
+q4_status q4_prefill_buffers(const q4_layer_table *table, int chunk, void *workspace, q4_prefill_buffers_t *out);
 
 /* ------------------------------------------------------------------------ *
  * 6. Decode attention of one token over a preallocated KV cache.

@@ -63,6 +63,7 @@ int main(void) {
   O(q4_gemm_desc, residual) O(q4_gemm_desc, workspace_bytes) P(q4_attention_desc) O(q4_attention_desc, rope_theta) O(q4_attention_desc, a)
   O(q4_attention_desc, workspace_bytes) O(q4_layer_weights, k_cache) O(q4_layer_weights, v_cache)
   O(q4_layer_table, head_dim) O(q4_layer_table, rope_theta) O(q4_layer_table, pos) O(q4_decode_buffers_t, a)
+  P(q4_prefill_buffers_t) O(q4_prefill_buffers_t, a)
   O(q4_gemv_desc, seg) O(q4_gemv_desc, out_dtype) O(q4_gemv_desc, mode)
   O(q4_segment, y) O(q4_segment, residual)
   O(q4_layer_table, layers) O(q4_layer_table, lm_head) O(q4_layer_table, workspace)
@@ -80,7 +81,8 @@ int main(void) {
     S = {"q4_segment": q4.q4_segment, "q4_gemv_desc": q4.q4_gemv_desc, "q4_linear": q4.q4_linear,
          "q4_layer_weights": q4.q4_layer_weights, "q4_layer_table": q4.q4_layer_table,
          "q4_decode_buffers_t": q4.q4_decode_buffers_t, "q4_moe_desc": q4.q4_moe_desc,
-         "q4_gemm_desc": q4.q4_gemm_desc, "q4_attention_desc": q4.q4_attention_desc}
+         "q4_gemm_desc": q4.q4_gemm_desc, "q4_attention_desc": q4.q4_attention_desc,
+         "q4_prefill_buffers_t": q4.q4_prefill_buffers_t}
     for key, val in got.items():
         if "." in key:
             t, f = key.split(".")

@@ -165,3 +165,87 @@ def test_decode_attention_graph_replay_matches_direct_launches():
         assert torch.equal(a, b)
     for (ka, va), (kb, vb) in zip(outs[0][1], outs[1][1]):
         assert torch.equal(ka, kb) and torch.equal(va, vb)
+
+
+# ---------------------------------------------------- prefill with attention ---
+
+def prefill_attn_run(shape, layers, lm, dc, pos, x, chunk):
+    t, _ = gpu_attn_table(shape, layers, lm, dc[0][0].shape[1], dc, pos)
+    T = x.shape[0]
+    h = torch_dev(x).clone()
+    nws = q4.q4_prefill_workspace_bytes(t, chunk)
+    ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
+    lg = torch.full((shape.vocab,), float("nan"), device="cuda")
+    q4.q4_prefill(t, h, T, chunk, lg, ws, nws)
+    st = q4.q4_device_status()
+    return t, st, h, lg, ws
+
+
+@pytest.mark.parametrize("start,chunk", [(0, 16), (100, 16), (100, 64)])
+def test_prefill_with_attention(start, chunk):
+    shape, layers, lm = attn_model(1600 + start, n_layers=2)
+    max_seq, T = 160, 37
+    hc = host_caches(shape, max_seq, start, 1601)
+    dc = [(torch_dev(kc), torch_dev(vc)) for kc, vc in hc]
+    pos = torch.tensor([start], dtype=torch.int32, device="cuda")
+    x = q4synth.activations(1602, T, shape.hidden)
+    t, st, h, lg, ws = prefill_attn_run(shape, layers, lm, dc, pos, x, chunk)
+    assert st == 0 and int(pos.item()) == start + T
+    # stage check on the last layer's last chunk: each token's attention
+    # output against the oracle fed the GPU's q and caches
+    b = q4.q4_prefill_buffers(t, chunk, ws)
+    C = T - (T - 1) // chunk * chunk
+    t0 = T - C
+    kl, vl = dc[-1][0].cpu().numpy(), dc[-1][1].cpu().numpy()
+    for i in range(C):
+        qg = read16(ws, b["q"] + 2 * i * shape.q, shape.q).astype(np.float16)
+        ag = read16(ws, b["a"] + 2 * i * shape.q, shape.q)
+        p = start + t0 + i
+        a_ref, A_a = oracle.attention(qg, kl, vl, p + 1, D_HEAD, p)
+        assert_parity(ag[None, :], a_ref[None, :], A_a[None, :], fp16_out=True, what=f"prefill attention t={t0 + i}")
+    # end to end against the oracle's own prefill (its own caches)
+    h_ref, y_ref, _ = oracle.prefill_attn(layers, lm, x, hc, start, D_HEAD)
+    r_h = np.linalg.norm(h.float().cpu().numpy() - h_ref) / np.linalg.norm(h_ref.astype(np.float64))
+    r_y = np.linalg.norm(lg.cpu().numpy() - y_ref[0]) / np.linalg.norm(y_ref[0])
+    assert r_h <= 1e-3 and r_y <= 1e-3, (r_h, r_y)
+    for (kc, vc), (dk, dv) in zip(hc, dc):
+        gk, gv = dk.cpu().numpy().astype(np.float64), dv.cpu().numpy().astype(np.float64)
+        sl = slice(start, start + T)
+        assert np.allclose(gk[:, sl], kc[:, sl], rtol=2e-2, atol=2e-2)
+        assert np.allclose(gv[:, sl], vc[:, sl], rtol=2e-2, atol=2e-2)
+        assert np.array_equal(gk[:, :start], kc[:, :start].astype(np.float64))
+        assert np.array_equal(gk[:, start + T:], kc[:, start + T:].astype(np.float64))
+    t.release()
+
+
+def test_prefill_then_decode_continues_the_sequence():
+    shape, layers, lm = attn_model(1700, n_layers=2)
+    max_seq, T = 96, 20
+    hc = host_caches(shape, max_seq, 0, 1701)
+    dc = [(torch_dev(kc), torch_dev(vc)) for kc, vc in hc]
+    pos = torch.tensor([0], dtype=torch.int32, device="cuda")
+    x = q4synth.activations(1702, T, shape.hidden)
+    t, st, h, lg, _ = prefill_attn_run(shape, layers, lm, dc, pos, x, 8)
+    assert st == 0 and int(pos.item()) == T
+    oracle.prefill_attn(layers, lm, x, hc, 0, D_HEAD)
+    logits = torch.empty(1, shape.vocab, device="cuda")
+    for s in range(3):
+        xs = q4synth.activations(1703 + s, 1, shape.hidden)
+        q4.q4_decode_step(t, torch_dev(xs), logits)
+        assert q4.q4_device_status() == 0 and int(pos.item()) == T + s + 1
+        y_ref, _, _ = oracle.decode_step_attn(layers, lm, xs, hc, T + s, D_HEAD)
+        r = np.linalg.norm(logits.cpu().numpy() - y_ref) / np.linalg.norm(y_ref)
+        assert r <= 1e-3, (s, r)
+    t.release()
+
+
+def test_prefill_past_the_cache_is_refused_on_the_device():
+    shape, layers, lm = attn_model(1800, n_layers=1)
+    hc = host_caches(shape, 40, 0, 1801)
+    dc = [(torch_dev(kc), torch_dev(vc)) for kc, vc in hc]
+    pos = torch.tensor([35], dtype=torch.int32, device="cuda")  # 35 + 8 > 40: every chunk refused
+    t, st, _, _, _ = prefill_attn_run(shape, layers, lm, dc, pos, q4synth.activations(1802, 16, shape.hidden), 8)
+    assert st == -7
+    for (kc, _), (dk, _) in zip(hc, dc):
+        assert np.array_equal(dk.cpu().numpy(), kc)
+    t.release()
