@@ -336,6 +336,36 @@ def dense_prefill(device, dl, dlm, shape, iters: int = 5, warmup: int = 3, cases
         out[f"T={T} chunk={C}"] = {"ms": ms, "tok_per_s": T / (ms * 1e-3), "gemm_tflops": tf,
                                    "tensor_frac": tf / peak}
     table.release()
+    # with attention (the prompt fills a KV cache; head_dim 128: 16 q / 8 kv heads)
+    hd = 128
+    hkv = shape.kv // hd
+    T, C = 2048, 2048
+    caches = [(torch.zeros(hkv, T, hd, dtype=torch.float16, device=device),
+               torch.zeros(hkv, T, hd, dtype=torch.float16, device=device)) for _ in range(shape.n_layers)]
+    pos = torch.zeros(1, dtype=torch.int32, device=device)
+    ta = q4.LayerTable([dict(d, k_cache=kc, v_cache=vc) for d, (kc, vc) in zip(dl, caches)], dlm,
+                       hidden=shape.hidden, M=1, flags=q4.Q4_DECODE_ATTENTION, head_dim=hd, max_seq=T, pos=pos)
+    x0 = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 9200, T, shape.hidden)).to(device)
+    h = torch.empty_like(x0)
+    nws = q4.q4_prefill_workspace_bytes(ta, C)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    lg = torch.empty(shape.vocab, dtype=torch.float32, device=device)
+    times = []
+    for it in range(warmup + iters):
+        h.copy_(x0)
+        pos.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        q4.q4_prefill(ta, h, T, C, lg, ws, nws, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        if it >= warmup:
+            times.append(e0.elapsed_time(e1))
+    if q4.q4_device_status(stream) != 0:
+        raise RuntimeError("device status after prefill-with-attention timing")
+    ms = sum(times) / len(times)
+    out[f"T={T} chunk={C} attention"] = {"ms": ms, "tok_per_s": T / (ms * 1e-3)}
+    ta.release()
     return out
 
 
