@@ -11,9 +11,9 @@
 //
 // GB300 design: attention of one token is a memory-bound pass over the cache
 // (2 x Hkv x d x 2 bytes per position), so it is split over positions
-// (flash-decoding): one CTA per (kv head, chunk of 128 positions) brings the
+// (flash-decoding): one CTA per (kv head, chunk of 64 positions) brings the
 // chunk's keys and values into shared memory with two bulk copies (the
-// positions of a head are contiguous, 32 KB each at d = 128) on one mbarrier,
+// positions of a head are contiguous, 16 KB each at d = 128) on one mbarrier,
 // rotates the group's queries meanwhile, scores every query head of the group
 // (a warp per position, lanes across d), turns the scores into exp(s - max),
 // and accumulates the values (threads across d and positions, the partial
@@ -32,7 +32,7 @@
 
 namespace q4a {
 
-constexpr int kChunk = 128;   // positions per CTA
+constexpr int kChunk = 64;    // positions per CTA
 constexpr int kThreads = 256;
 constexpr int kMaxGroup = 8;  // query heads per kv head
 
@@ -246,23 +246,52 @@ __global__ void __launch_bounds__(kThreads) attn_split_kernel(const uint16_t* __
 }
 
 // a[h] = sum_s acc_s e^(m_s - M) / sum_s l_s e^(m_s - M) over the live chunks.
+// The chunks' (max, sum) pairs are staged in shared memory with one load per
+// thread; the partial outputs are read 4 chunks at a time.
+constexpr int kMaxLive = 1024;  // chunks merged in one pass (max_seq <= 1024 * kChunk)
+
 __global__ void attn_combine_kernel(const float* __restrict__ part_ml, const float* __restrict__ part_acc,
                                     const int32_t* pos_p, int d, int max_seq, int n_splits,
                                     uint16_t* __restrict__ a) {
+    __shared__ float2 mls[kMaxLive];
+    __shared__ float wsh[kMaxLive];
+    __shared__ float red[2];
     const int h = blockIdx.x, t = threadIdx.x;
     const int pos = *pos_p;
     if (pos < 0 || pos >= max_seq) return;  // latched by the split kernel
-    const int live = pos / kChunk + 1;
-    const float* ml = part_ml + (size_t)h * n_splits * 2;
-    float M = -INFINITY;
-    for (int s = 0; s < live; ++s) M = fmaxf(M, ml[2 * s]);
-    float L = 0.f, acc = 0.f;
-    for (int s = 0; s < live; ++s) {
-        const float w = expf(ml[2 * s] - M);
-        L = fmaf(ml[2 * s + 1], w, L);
-        acc = fmaf(part_acc[((size_t)h * n_splits + s) * d + t], w, acc);
+    const int live = min(pos / kChunk + 1, kMaxLive);
+    const float2* ml = reinterpret_cast<const float2*>(part_ml) + (size_t)h * n_splits;
+    for (int s = t; s < live; s += blockDim.x) mls[s] = ml[s];
+    __syncthreads();
+    if (t < 32) {
+        float M = -INFINITY;
+        for (int s = t; s < live; s += 32) M = fmaxf(M, mls[s].x);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+        float L = 0.f;
+        for (int s = t; s < live; s += 32) {
+            const float w = expf(mls[s].x - M);
+            wsh[s] = w;
+            L = fmaf(mls[s].y, w, L);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+        if (t == 0) red[0] = L;
     }
-    a[h * d + t] = __half_as_ushort(__float2half_rn(acc / L));
+    __syncthreads();
+    const float* pa = part_acc + (size_t)h * n_splits * d + t;
+    float acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+    int s = 0;
+    for (; s + 3 < live; s += 4) {
+        const float x0 = pa[(size_t)s * d], x1 = pa[(size_t)(s + 1) * d], x2 = pa[(size_t)(s + 2) * d],
+                    x3 = pa[(size_t)(s + 3) * d];
+        acc0 = fmaf(x0, wsh[s], acc0);
+        acc1 = fmaf(x1, wsh[s + 1], acc1);
+        acc2 = fmaf(x2, wsh[s + 2], acc2);
+        acc3 = fmaf(x3, wsh[s + 3], acc3);
+    }
+    for (; s < live; ++s) acc0 = fmaf(pa[(size_t)s * d], wsh[s], acc0);
+    a[h * d + t] = __half_as_ushort(__float2half_rn(((acc0 + acc1) + (acc2 + acc3)) / red[0]));
 }
 
 __global__ void pos_advance_kernel(int32_t* pos_p, int by) { *pos_p += by; }
@@ -452,6 +481,8 @@ q4_status attn_validate(const q4_attention_desc& d) {
     if (d.n_q_heads / d.n_kv_heads > q4a::kMaxGroup)
         return fail(Q4_ERR_UNSUPPORTED, "more than %d query heads per kv head", q4a::kMaxGroup);
     if (d.max_seq < 1) return fail(Q4_ERR_INVALID_ARG, "max_seq=%d", d.max_seq);
+    if (d.max_seq > q4a::kMaxLive * q4a::kChunk)
+        return fail(Q4_ERR_UNSUPPORTED, "max_seq=%d above %d", d.max_seq, q4a::kMaxLive * q4a::kChunk);
     if (!(d.rope_theta > 1.0f)) return fail(Q4_ERR_INVALID_ARG, "rope_theta must be > 1");
     if ((reinterpret_cast<uintptr_t>(d.k_cache) & 15u) || (reinterpret_cast<uintptr_t>(d.v_cache) & 15u) ||
         (reinterpret_cast<uintptr_t>(d.workspace) & 255u))

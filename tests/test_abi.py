@@ -209,8 +209,8 @@ def test_moe_validation(L):
 
 
 def test_attention_validation(L):
-    # the (cos, sin) table, (max, sum) per head and 128-position chunk, then the partial outputs
-    assert L.q4_attention_workspace_bytes(16, 128, 4096) == 64 * 8 + 16 * 32 * 2 * 4 + 16 * 32 * 128 * 4
+    # the (cos, sin) table, (max, sum) per head and 64-position chunk, then the partial outputs
+    assert L.q4_attention_workspace_bytes(16, 128, 4096) == 64 * 8 + 16 * 64 * 2 * 4 + 16 * 64 * 128 * 4
     assert L.q4_attention_workspace_bytes(0, 128, 4096) == 0
     assert L.q4_attention(None, None) == -1
     d = q4.q4_attention_desc(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 16, 8, 128, 4096, 1e6, FAKE, FAKE * 256, 1 << 20)

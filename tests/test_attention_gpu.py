@@ -1,7 +1,7 @@
 """GPU parity of decode attention (RoPE, KV-cache append, split attention,
 merge) against the fp64 oracle, standalone and inside the decode step.
 
-Standalone: positions on both sides of the 128-position chunk boundaries,
+Standalone: positions on both sides of the 64-position chunk boundaries,
 head groups of 1, 2 and 8 query heads per kv head, head_dim 64 and 128; the
 appended cache position is checked to 1 ulp and every other position is
 untouched; a position outside the cache latches a device-check status and
@@ -40,7 +40,7 @@ def run_attention(q, k, v, kc, vc, pos, Hq, Hkv, d, theta=1e6):
 
 
 @pytest.mark.parametrize("Hq,Hkv,d", [(16, 8, 128), (4, 4, 64), (16, 2, 128)])
-@pytest.mark.parametrize("pos", [0, 1, 127, 128, 255, 256, 700])
+@pytest.mark.parametrize("pos", [0, 1, 63, 64, 127, 128, 700])
 def test_attention_standalone(Hq, Hkv, d, pos):
     g = np.random.default_rng(1000 + pos + Hq + d)
     max_seq = 768
