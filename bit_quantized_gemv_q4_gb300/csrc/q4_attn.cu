@@ -334,13 +334,18 @@ __global__ void prefill_append_kernel(const uint16_t* __restrict__ k, const uint
 constexpr int kPQ = 8;   // query tokens per CTA (a warp each)
 constexpr int kPK = 64;  // key positions per staged chunk
 
-constexpr size_t prefill_smem(int D) { return (size_t)2 * kPK * D * 2 + (size_t)kPQ * kPK * 4; }
+constexpr size_t prefill_smem(int D) {
+    return (size_t)2 * kPK * D * 2 + (size_t)kPQ * D * 4 + (size_t)kPQ * kPK * 4;
+}
 
 // Causal attention of the chunk's tokens for query head blockIdx.x: token t
 // attends over positions 0..p0+t.  Key/value chunks of 64 positions are
-// bulk-copied into shared memory (one mbarrier phase per chunk); each warp
-// scores its token against the chunk (lanes across d), then updates its
-// running max, sum and output with the chunk's exp(s - max).
+// bulk-copied into shared memory (one mbarrier phase per chunk).  Scores:
+// thread (i, j) of the 8 x 32 grid computes the whole dot products of token i
+// with keys j and j+32 from shared memory, lanes walking the dimensions in a
+// rotated order so the key rows do not collide in banks.  Then warp i takes
+// token i's online softmax over the chunk and accumulates the values (lanes
+// across dimensions).
 template <int D>
 __global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* __restrict__ q,
                                                                 const uint16_t* kc, const uint16_t* vc,
@@ -348,9 +353,10 @@ __global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* 
                                                                 int G, int max_seq, const float2* __restrict__ cs,
                                                                 uint16_t* __restrict__ a, int* err) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);  // [kPK][D]
-    uint16_t* vs = ks + kPK * D;                       // [kPK][D]
-    float* sc = reinterpret_cast<float*>(vs + kPK * D);  // [kPQ][kPK]
+    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);      // [kPK][D]
+    uint16_t* vs = ks + kPK * D;                           // [kPK][D]
+    float* qs = reinterpret_cast<float*>(vs + kPK * D);    // [kPQ][D] rotated, scaled queries
+    float* sc = qs + kPQ * D;                              // [kPQ][kPK]
     __shared__ __align__(8) uint64_t bar;
     constexpr int E = D / 32;
     const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -358,27 +364,27 @@ __global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* 
     const int p0 = *pos_p + t0;
     if (p0 < 0 || p0 + C > max_seq) return;  // latched by the append kernel
     const int tq0 = blockIdx.y * kPQ;
-    const int t = tq0 + warp;
+    const int t = tq0 + warp;  // this warp's token (softmax and values)
     const bool live = t < C;
-    const int last = min(tq0 + kPQ, C) - 1;  // the block's last token
+    const int last = min(tq0 + kPQ, C) - 1;
     const int n_keys = p0 + last + 1;
-    // this warp's rotated query, scaled by 1/sqrt(d): lane holds dims
-    // lane*E .. lane*E+E-1; the pair partner of dim i < d/2 is in lane ^ 16
-    float qr[E];
-    if (live) {
+    // rotated queries of the block's tokens into shared memory
+    {
         const float scale = rsqrtf((float)D);
-        const uint16_t* qrow = q + (size_t)t * Hq * D + (size_t)h * D;
-#pragma unroll
-        for (int e = 0; e < E; ++e) {
-            const float mine = __half2float(__ushort_as_half(qrow[lane * E + e]));
-            const float other = __shfl_xor_sync(0xffffffffu, mine, 16);
-            const int i = (lane & 15) * E + e;
-            const float2 r = cs[(size_t)t * (D / 2) + i];
-            qr[e] = (lane < 16 ? mine * r.x - other * r.y : mine * r.x + other * r.y) * scale;
+        for (int x = threadIdx.x; x < kPQ * (D / 2); x += kPQ * 32) {
+            const int i = x / (D / 2), pr = x % (D / 2);
+            float lo = 0.f, hi = 0.f;
+            if (tq0 + i < C) {
+                const uint16_t* qrow = q + (size_t)(tq0 + i) * Hq * D + (size_t)h * D;
+                const float2 r = cs[(size_t)(tq0 + i) * (D / 2) + pr];
+                const float l0 = __half2float(__ushort_as_half(qrow[pr]));
+                const float h0 = __half2float(__ushort_as_half(qrow[pr + D / 2]));
+                lo = (l0 * r.x - h0 * r.y) * scale;
+                hi = (h0 * r.x + l0 * r.y) * scale;
+            }
+            qs[i * D + pr] = lo;
+            qs[i * D + pr + D / 2] = hi;
         }
-    } else {
-#pragma unroll
-        for (int e = 0; e < E; ++e) qr[e] = 0.f;  // a warp past the chunk's last token
     }
     const uint32_t b = q4d::smem_addr(&bar);
     if (threadIdx.x == 0) {
@@ -389,7 +395,10 @@ __global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* 
     float m = -INFINITY, l = 0.f, acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    const int my_n = live ? p0 + t + 1 : 0;  // keys this token sees
+    const int my_n = live ? p0 + t + 1 : 0;  // keys token t sees
+    const int si = warp;                     // score grid row (token) of this thread
+    const int sn = p0 + tq0 + si + 1;        // keys token si sees
+    const float4* q4p = reinterpret_cast<const float4*>(qs + si * D);
     int phase = 0;
     for (int j0 = 0; j0 < n_keys; j0 += kPK, phase ^= 1) {
         const int cnt = min(kPK, n_keys - j0);
@@ -404,35 +413,49 @@ __global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* 
             q4d::mbar_wait(b, (uint32_t)phase, nullptr);
             return;
         }
-        const int mine = min(cnt, my_n - j0);  // keys of this chunk the token sees
-        if (mine > 0) {
-            float cmax = -INFINITY;
-            for (int j = 0; j < mine; ++j) {
-                float s = 0.f;
-                if constexpr (E == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2*>(ks + j * D + lane * 4);
+        // scores of token si with keys lane and lane + 32 (whole dot products)
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+            const int j = lane + 32 * kk;
+            float s = -INFINITY;
+            if (j < cnt && j0 + j < sn) {
+                const uint2* krow = reinterpret_cast<const uint2*>(ks + j * D);
+                float s0 = 0.f, s1 = 0.f;
+#pragma unroll 8
+                for (int c4 = 0; c4 < D / 4; ++c4) {
+                    const int dq = (c4 + lane) & (D / 4 - 1);  // rotated 4-dim group
+                    const uint2 raw = krow[dq];
                     const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
                     const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-                    s = fmaf(qr[0], x.x, fmaf(qr[1], x.y, fmaf(qr[2], y.x, qr[3] * y.y)));
-                } else {
-                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(ks + j * D + lane * 2);
-                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw));
-                    s = fmaf(qr[0], x.x, qr[1] * x.y);
+                    const float4 qq = q4p[dq];
+                    s0 = fmaf(qq.x, x.x, fmaf(qq.y, x.y, s0));
+                    s1 = fmaf(qq.z, y.x, fmaf(qq.w, y.y, s1));
                 }
-#pragma unroll
-                for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-                if (lane == 0) sc[warp * kPK + j] = s;
-                cmax = fmaxf(cmax, s);
+                s = s0 + s1;
             }
-            __syncwarp();
+            sc[si * kPK + j] = s;
+        }
+        __syncwarp();
+        // token t (= si): online softmax over the chunk, then the values
+        const int mine = min(cnt, my_n - j0);
+        if (mine > 0) {
+            float cmax = fmaxf(sc[warp * kPK + lane], sc[warp * kPK + lane + 32]);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
             const float mn = fmaxf(m, cmax);
             const float corr = expf(m - mn);  // 0 on the first chunk (m = -inf)
-            l *= corr;
+            const float p0v = expf(sc[warp * kPK + lane] - mn), p1v = expf(sc[warp * kPK + lane + 32] - mn);
+            sc[warp * kPK + lane] = p0v;
+            sc[warp * kPK + lane + 32] = p1v;
+            float ps = p0v + p1v;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+            l = l * corr + ps;
 #pragma unroll
             for (int e = 0; e < E; ++e) acc[e] *= corr;
+            __syncwarp();
             for (int j = 0; j < mine; ++j) {
-                const float pj = expf(sc[warp * kPK + j] - mn);
-                l += pj;
+                const float pj = sc[warp * kPK + j];
                 if constexpr (E == 4) {
                     const uint2 raw = *reinterpret_cast<const uint2*>(vs + j * D + lane * 4);
                     const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
