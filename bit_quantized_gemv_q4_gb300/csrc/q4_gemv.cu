@@ -803,8 +803,15 @@ __global__ void __launch_bounds__(kThreads, 2) q4_gemv_kernel(const __grid_const
 // CTAs.  Because weights never depend on activations, the producer warp
 // streams a CTA's tiles through one shared-memory ring across stage
 // boundaries, as far ahead as the ring allows; the consumers of stage s wait
-// only for their x: the tagged words (fp16 value | tag of step and stage) the
-// CTAs of stage s-1 publish.  Stage parameters live in a device table; the
+// only for their x.  Hand-off: a CTA that owns tiles of a stage adds one to a
+// stage-completion counter after its last tile of that stage (release); the
+// consumers of stage s poll that one word until it reaches the number of CTAs
+// owning tiles of stages 0..s-1.  Every stage reads only what earlier stages
+// wrote, so a CTA of stage s can add to the counter only after all of stages
+// 0..s-1 have, and the count therefore means that every earlier stage is
+// complete (which also covers residuals and the reuse of buffers).  The x
+// words are then read once; they still carry a tag (fp16 value | tag of step
+// and stage), which is checked.  The last CTA of the step resets the counter.  Stage parameters live in a device table; the
 // consumers copy the next stage's entry into shared memory while they work on
 // the current one.  Every wait is bounded; an expired wait is OR-ed over the
 // consumers at the end of the stage and the CTA then stops, waits (bounded)
@@ -824,8 +831,25 @@ struct StepParams {
     uint32_t x_bytes;      // x region (largest K)
     const uint32_t* step_ctr;
     uint32_t* done_ctr;
+    uint32_t* stage_ctr;   // CTA-stage completions in this step
     int* err;
 };
+
+// Bounded wait until the completion counter reaches `need` (acquire).
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t need, int* err) {
+    unsigned long long t0 = 0;
+    while (true) {
+        uint32_t v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= need) return true;
+        if (t0 == 0) {
+            t0 = q4d::globaltimer();
+        } else if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
+            atomicOr(err, q4d::kErrTimeout);
+            return false;
+        }
+    }
+}
 
 // First tile of a stage that CTA c owns: tile t goes to CTA (tile_base + t) mod G.
 __device__ __forceinline__ int first_tile(int tile_base, int G, int c) {
@@ -917,6 +941,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
         const uint32_t step = step_sh;
         int i = 0;
         bool bad = false;
+        uint32_t done_before = 0;  // CTAs owning tiles of the stages before s
         for (int s = 0; s < sp.n; ++s) {
             const int2 st_ = tt[s];
             const int t0 = first_tile(st_.x, G, c), T = st_.y;
@@ -934,6 +959,12 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
                 const uint16_t* gam =
                     (ps.norm && ps.norm_w) ? reinterpret_cast<const uint16_t*>(slot + sp.meta_off + sizeof(Params))
                                            : nullptr;
+                if (s > 0) {
+                    // every earlier stage complete (one poller, then the CTA)
+                    bool w_bad = bad;
+                    if (tid == 0 && !w_bad) w_bad = !wait_count(sp.stage_ctr, done_before, sp.err);
+                    if (q4d::named_bar_or(2, kCT, w_bad)) bad = true;
+                }
                 if (!bad && !load_x<M, 4>(ps, xs, red, warp, lane, xtag, gam)) bad = true;
                 q4d::named_bar(1, kCT);
                 const Params& p = *prm;
@@ -960,6 +991,11 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
                 if (tid == 0) abort_sh = 1;
                 break;
             }
+            if (t0 < T && tid == 0) {
+                // the consumers' stores of this stage precede the barrier above
+                asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sp.stage_ctr) : "memory");
+            }
+            done_before += (uint32_t)(T < G ? T : G);
         }
         if (lane == 0) atomicMin(&consumed_sh, i);
     }
@@ -973,6 +1009,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_decode_persistent_kernel(const
         __threadfence();
         if (atomicAdd(sp.done_ctr, 1u) == gridDim.x - 1) {
             *sp.done_ctr = 0;
+            *sp.stage_ctr = 0;
             atomicAdd(const_cast<uint32_t*>(sp.step_ctr), 1u);
         }
     }
@@ -1326,6 +1363,7 @@ q4_status persistent_launch(const PersistentGeom& g, const void* dev_params, cud
     sp.x_bytes = g.x_bytes;
     sp.step_ctr = g.step_ctr;
     sp.done_ctr = g.done_ctr;
+    sp.stage_ctr = g.done_ctr + 1;
     sp.err = dev->err_word;
     cudaError_t e = cudaSuccess;
     switch (g.M) {

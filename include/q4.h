@@ -217,8 +217,9 @@ q4_status q4_gemv_bits(const uint32_t *Wq, const uint16_t *scales, const uint16_
  * replay the graph.  With Q4_DECODE_PERSISTENT a step is ONE cooperative
  * kernel launch instead: one CTA per SM walks every stage in order, streaming
  * each stage's weights ahead through shared memory while it waits for that
- * stage's input, and the stages hand activations on as tagged words (below)
- * instead of kernel boundaries; the per-stage kernel parameters are uploaded
+ * stage's input; a stage starts once a completion counter in the workspace
+ * shows every earlier stage done, and reads its input as tagged words
+ * (below), instead of kernel boundaries; the per-stage kernel parameters are uploaded
  * into the workspace on `stream` on the first call and after a pointer
  * change, and calls on one table must then be ordered on one stream.  If the
  * step does not fit one persistent launch (x of the widest stage plus two
@@ -229,7 +230,8 @@ q4_status q4_gemv_bits(const uint32_t *Wq, const uint16_t *scales, const uint16_
  * stage as 32-bit words holding the fp16 value and a 16-bit tag naming the
  * step and the writing stage; a stage polls the words it reads instead of
  * waiting for the whole previous kernel to finish.  The workspace therefore
- * also holds the stage parameters, these tagged copies and a step counter;
+ * also holds the stage parameters, these tagged copies and the step and
+ * completion counters;
  * the tagged region is cleared on the first such call (on `stream`), and the
  * workspace must not be shared with another table while in use.  Host memory
  * for the plan is allocated on that first call
