@@ -331,47 +331,121 @@ __global__ void prefill_append_kernel(const uint16_t* __restrict__ k, const uint
     vc[base + i + half] = v[src + i + half];
 }
 
-constexpr int kPQ = 8;   // query tokens per CTA (a warp each)
-constexpr int kPK = 64;  // key positions per staged chunk
+// Causal attention of a prompt chunk on the tensor cores (mma.sync
+// m16n8k16, fp16 operands, fp32 accumulation), flash-attention style: a CTA
+// takes 64 of the chunk's tokens for one query head (a warp per 16 tokens) and
+// walks the keys 0..(position of its last token) in tiles of 64 positions,
+// keeping a running (max, sum, output) per token.  Key and value tiles are
+// staged by cp.async into shared memory (double-buffered), each 16-byte chunk
+// of a row placed at chunk ^ (row & 7) so the ldmatrix reads of eight rows hit
+// eight different bank groups.  The rotated query, scaled by log2(e)/sqrt(d),
+// is held as two fp16 parts (hi + lo), so the scores carry the fp32 query;
+// the probabilities enter the value product as fp16 (their sum stays fp32).
+constexpr int kFQ = 64;        // query tokens per CTA
+constexpr int kFK = 64;        // key positions per staged tile
+constexpr int kFThreads = 128;
 
-constexpr size_t prefill_smem(int D) {
-    return (size_t)2 * kPK * D * 2 + (size_t)kPQ * D * 4 + (size_t)kPQ * kPK * 4;
+constexpr size_t prefill_smem(int D) { return (size_t)kFQ * D * 4 + (size_t)4 * kFK * D * 2; }
+
+// Byte offset of 16-byte chunk `c` of row `r` in a swizzled [rows][D] fp16 tile.
+template <int D>
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+    return (uint32_t)(r * D * 2 + ((c ^ (r & 7)) << 4));
 }
 
-// Causal attention of the chunk's tokens for query head blockIdx.x: token t
-// attends over positions 0..p0+t.  Key/value chunks of 64 positions are
-// bulk-copied into shared memory (one mbarrier phase per chunk).  Scores:
-// thread (i, j) of the 8 x 32 grid computes the whole dot products of token i
-// with keys j and j+32 from shared memory, lanes walking the dimensions in a
-// rotated order so the key rows do not collide in banks.  Then warp i takes
-// token i's online softmax over the chunk and accumulates the values (lanes
-// across dimensions).
+// 16-byte global -> shared copy; src_bytes 0 fills the chunk with zeros.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr)
+                 : "memory");
+}
+
+// c += a * b for one 16x8x16 tile (a: 16x16 row-major fragment, b: 16x8).
+__device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// (x, y) as an fp16 pair plus the fp16 pair of what that rounding left out.
+__device__ __forceinline__ void split_h2(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 f = __half22float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = pack_h2(x - f.x, y - f.y);
+}
+
+// Grid (Hq, ceil(C / 64)), 128 threads.  Token t of the chunk (position
+// p0 + t) attends over positions 0..p0 + t of its kv head's cache.
+// Fragment layouts (PTX mma.m16n8k16): with g = lane / 4 and u = lane % 4, an
+// A register pair covers (row g or g + 8, columns 2u, 2u + 1 or 2u + 8, 2u + 9),
+// a B register (rows 2u, 2u + 1 or 2u + 8, 2u + 9, column g), an accumulator
+// (row g or g + 8, columns 2u, 2u + 1); the score accumulators of two
+// neighbouring 8-key tiles therefore are the A fragment of the probabilities
+// for one 16-key step of the value product.
 template <int D>
-__global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* __restrict__ q,
+__global__ void __launch_bounds__(kFThreads) prefill_attn_kernel(const uint16_t* __restrict__ q,
                                                                 const uint16_t* kc, const uint16_t* vc,
                                                                 const int32_t* pos_p, int t0, int C, int Hq,
                                                                 int G, int max_seq, const float2* __restrict__ cs,
-                                                                uint16_t* __restrict__ a, int* err) {
+                                                                uint16_t* __restrict__ a) {
     extern __shared__ __align__(128) uint8_t smem[];
-    uint16_t* ks = reinterpret_cast<uint16_t*>(smem);      // [kPK][D]
-    uint16_t* vs = ks + kPK * D;                           // [kPK][D]
-    float* qs = reinterpret_cast<float*>(vs + kPK * D);    // [kPQ][D] rotated, scaled queries
-    float* sc = qs + kPQ * D;                              // [kPQ][kPK]
-    __shared__ __align__(8) uint64_t bar;
-    constexpr int E = D / 32;
+    constexpr int NCH = D / 8;   // 16-byte chunks per row
+    constexpr int KS = D / 16;   // 16-wide steps over the head dimension
+    constexpr int DN = D / 8;    // 8-wide output tiles over the head dimension
+    constexpr uint32_t TB = kFK * D * 2;
+    float* qs = reinterpret_cast<float*>(smem);  // [kFQ][D] rotated, scaled queries
+    const uint32_t kv0 = q4d::smem_addr(smem + (size_t)kFQ * D * 4);  // K0 V0 K1 V1
     const int h = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, u = lane & 3;
     const int kvh = h / G;
     const int p0 = *pos_p + t0;
     if (p0 < 0 || p0 + C > max_seq) return;  // latched by the append kernel
-    const int tq0 = blockIdx.y * kPQ;
-    const int t = tq0 + warp;  // this warp's token (softmax and values)
-    const bool live = t < C;
-    const int last = min(tq0 + kPQ, C) - 1;
-    const int n_keys = p0 + last + 1;
-    // rotated queries of the block's tokens into shared memory
+    const int tq0 = blockIdx.y * kFQ;
+    const int n_keys = p0 + min(tq0 + kFQ, C);  // keys the CTA's last token sees
+    const int n_tiles = (n_keys + kFK - 1) / kFK;
+    const uint16_t* kh = kc + (size_t)kvh * max_seq * D;
+    const uint16_t* vh = vc + (size_t)kvh * max_seq * D;
+
+    // Tile j of keys and values into buffer j & 1; rows past n_keys are zero
+    // (stale cache rows could hold anything, and 0 * NaN would reach the sums).
+    auto issue = [&](int j) {
+        const uint32_t kb = kv0 + (uint32_t)(j & 1) * 2u * TB, vb = kb + TB;
+        for (int x = threadIdx.x; x < kFK * NCH; x += kFThreads) {
+            const int r = x / NCH, c = x % NCH;
+            const int key = j * kFK + r;
+            const bool ok = key < n_keys;
+            const size_t off = (size_t)(ok ? key : 0) * D + (size_t)c * 8;
+            const uint32_t so = swz<D>(r, c);
+            cp_async16(kb + so, kh + off, ok ? 16u : 0u);
+            cp_async16(vb + so, vh + off, ok ? 16u : 0u);
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+    };
+    issue(0);
+
     {
-        const float scale = rsqrtf((float)D);
-        for (int x = threadIdx.x; x < kPQ * (D / 2); x += kPQ * 32) {
+        const float scale = rsqrtf((float)D) * 1.4426950408889634f;  // log2(e) / sqrt(d)
+        for (int x = threadIdx.x; x < kFQ * (D / 2); x += kFThreads) {
             const int i = x / (D / 2), pr = x % (D / 2);
             float lo = 0.f, hi = 0.f;
             if (tq0 + i < C) {
@@ -386,99 +460,130 @@ __global__ void __launch_bounds__(kPQ * 32) prefill_attn_kernel(const uint16_t* 
             qs[i * D + pr + D / 2] = hi;
         }
     }
-    const uint32_t b = q4d::smem_addr(&bar);
-    if (threadIdx.x == 0) {
-        q4d::mbar_init(b, 1);
-        q4d::fence_mbar_init();
-    }
     __syncthreads();
-    float m = -INFINITY, l = 0.f, acc[E];
+    uint32_t qh[KS][4], ql[KS][4];
+    {
+        const float* r0 = qs + (warp * 16 + g) * D;
+        const float* r1 = r0 + 8 * D;
 #pragma unroll
-    for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    const int my_n = live ? p0 + t + 1 : 0;  // keys token t sees
-    const int si = warp;                     // score grid row (token) of this thread
-    const int sn = p0 + tq0 + si + 1;        // keys token si sees
-    const float4* q4p = reinterpret_cast<const float4*>(qs + si * D);
-    int phase = 0;
-    for (int j0 = 0; j0 < n_keys; j0 += kPK, phase ^= 1) {
-        const int cnt = min(kPK, n_keys - j0);
-        if (threadIdx.x == 0) {
-            const uint32_t bytes = (uint32_t)cnt * D * 2;
-            q4d::mbar_arrive_expect_tx(b, 2 * bytes);
-            q4d::bulk_g2s(q4d::smem_addr(ks), kc + ((size_t)kvh * max_seq + j0) * D, bytes, b);
-            q4d::bulk_g2s(q4d::smem_addr(vs), vc + ((size_t)kvh * max_seq + j0) * D, bytes, b);
+        for (int kk = 0; kk < KS; ++kk) {
+            const int c0 = 16 * kk + 2 * u, c1 = c0 + 8;
+            split_h2(r0[c0], r0[c0 + 1], qh[kk][0], ql[kk][0]);
+            split_h2(r1[c0], r1[c0 + 1], qh[kk][1], ql[kk][1]);
+            split_h2(r0[c1], r0[c1 + 1], qh[kk][2], ql[kk][2]);
+            split_h2(r1[c1], r1[c1 + 1], qh[kk][3], ql[kk][3]);
         }
-        const bool late = !q4d::mbar_wait(b, (uint32_t)phase, err);
-        if (__syncthreads_or(late)) {
-            q4d::mbar_wait(b, (uint32_t)phase, nullptr);
-            return;
-        }
-        // scores of token si with keys lane and lane + 32 (whole dot products)
-#pragma unroll
-        for (int kk = 0; kk < 2; ++kk) {
-            const int j = lane + 32 * kk;
-            float s = -INFINITY;
-            if (j < cnt && j0 + j < sn) {
-                const uint2* krow = reinterpret_cast<const uint2*>(ks + j * D);
-                float s0 = 0.f, s1 = 0.f;
-#pragma unroll 8
-                for (int c4 = 0; c4 < D / 4; ++c4) {
-                    const int dq = (c4 + lane) & (D / 4 - 1);  // rotated 4-dim group
-                    const uint2 raw = krow[dq];
-                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-                    const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-                    const float4 qq = q4p[dq];
-                    s0 = fmaf(qq.x, x.x, fmaf(qq.y, x.y, s0));
-                    s1 = fmaf(qq.z, y.x, fmaf(qq.w, y.y, s1));
-                }
-                s = s0 + s1;
-            }
-            sc[si * kPK + j] = s;
-        }
-        __syncwarp();
-        // token t (= si): online softmax over the chunk, then the values
-        const int mine = min(cnt, my_n - j0);
-        if (mine > 0) {
-            float cmax = fmaxf(sc[warp * kPK + lane], sc[warp * kPK + lane + 32]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-            const float mn = fmaxf(m, cmax);
-            const float corr = expf(m - mn);  // 0 on the first chunk (m = -inf)
-            const float p0v = expf(sc[warp * kPK + lane] - mn), p1v = expf(sc[warp * kPK + lane + 32] - mn);
-            sc[warp * kPK + lane] = p0v;
-            sc[warp * kPK + lane + 32] = p1v;
-            float ps = p0v + p1v;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
-            l = l * corr + ps;
-#pragma unroll
-            for (int e = 0; e < E; ++e) acc[e] *= corr;
-            __syncwarp();
-            for (int j = 0; j < mine; ++j) {
-                const float pj = sc[warp * kPK + j];
-                if constexpr (E == 4) {
-                    const uint2 raw = *reinterpret_cast<const uint2*>(vs + j * D + lane * 4);
-                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw.x));
-                    const float2 y = __half22float2(*reinterpret_cast<const __half2*>(&raw.y));
-                    acc[0] = fmaf(pj, x.x, acc[0]);
-                    acc[1] = fmaf(pj, x.y, acc[1]);
-                    acc[2] = fmaf(pj, y.x, acc[2]);
-                    acc[3] = fmaf(pj, y.y, acc[3]);
-                } else {
-                    const uint32_t raw = *reinterpret_cast<const uint32_t*>(vs + j * D + lane * 2);
-                    const float2 x = __half22float2(*reinterpret_cast<const __half2*>(&raw));
-                    acc[0] = fmaf(pj, x.x, acc[0]);
-                    acc[1] = fmaf(pj, x.y, acc[1]);
-                }
-            }
-            m = mn;
-        }
-        __syncthreads();  // the chunk buffers are refilled next
     }
-    if (live) {
-        uint16_t* arow = a + (size_t)t * Hq * D + (size_t)h * D + lane * E;
+
+    float o[DN][4];
 #pragma unroll
-        for (int e = 0; e < E; ++e) arow[e] = __half_as_ushort(__float2half_rn(acc[e] / l));
+    for (int dn = 0; dn < DN; ++dn) o[dn][0] = o[dn][1] = o[dn][2] = o[dn][3] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    const int wmin = p0 + tq0 + warp * 16;   // position of the warp's first token
+    const int wmax = wmin + 15;
+    const int pr0 = wmin + g, pr1 = pr0 + 8;  // positions of this thread's two rows
+    const bool wlive = tq0 + warp * 16 < C;
+
+    for (int j = 0; j < n_tiles; ++j) {
+        if (j + 1 < n_tiles) {
+            issue(j + 1);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        const uint32_t kb = kv0 + (uint32_t)(j & 1) * 2u * TB, vb = kb + TB;
+#pragma unroll
+        for (int sub = 0; sub < kFK / 32; ++sub) {
+            const int key0 = j * kFK + sub * 32;
+            if (!wlive || key0 > wmax) break;  // every key of the rest is masked for this warp
+            float sc[4][4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+#pragma unroll
+                for (int kk = 0; kk < KS; kk += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4(kb + swz<D>(sub * 32 + nt * 8 + (lane & 7), 2 * kk + (lane >> 3)), b0, b1, b2, b3);
+                    mma16816(sc[nt], qh[kk], b0, b1);
+                    mma16816(sc[nt], ql[kk], b0, b1);
+                    mma16816(sc[nt], qh[kk + 1], b2, b3);
+                    mma16816(sc[nt], ql[kk + 1], b2, b3);
+                }
+            }
+            if (key0 + 31 > wmin) {
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const int key = key0 + nt * 8 + 2 * u + (e & 1);
+                        if (key > (e < 2 ? pr0 : pr1)) sc[nt][e] = -INFINITY;
+                    }
+            }
+            float x0 = m0, x1 = m1;
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                x0 = fmaxf(x0, fmaxf(sc[nt][0], sc[nt][1]));
+                x1 = fmaxf(x1, fmaxf(sc[nt][2], sc[nt][3]));
+            }
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 1));
+            x0 = fmaxf(x0, __shfl_xor_sync(0xffffffffu, x0, 2));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 1));
+            x1 = fmaxf(x1, __shfl_xor_sync(0xffffffffu, x1, 2));
+            const float s0 = x0 == -INFINITY ? 0.f : x0, s1 = x1 == -INFINITY ? 0.f : x1;
+            const float c0 = exp2f(m0 - s0), c1 = exp2f(m1 - s1);  // 0 while nothing was seen
+            m0 = x0;
+            m1 = x1;
+            l0 *= c0;
+            l1 *= c1;
+#pragma unroll
+            for (int dn = 0; dn < DN; ++dn) {
+                o[dn][0] *= c0;
+                o[dn][1] *= c0;
+                o[dn][2] *= c1;
+                o[dn][3] *= c1;
+            }
+            uint32_t pa[2][4];
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const float e0 = exp2f(sc[nt][0] - s0), e1 = exp2f(sc[nt][1] - s0);
+                const float e2 = exp2f(sc[nt][2] - s1), e3 = exp2f(sc[nt][3] - s1);
+                l0 += e0 + e1;
+                l1 += e2 + e3;
+                pa[nt >> 1][(nt & 1) * 2 + 0] = pack_h2(e0, e1);
+                pa[nt >> 1][(nt & 1) * 2 + 1] = pack_h2(e2, e3);
+            }
+#pragma unroll
+            for (int kj = 0; kj < 2; ++kj) {
+#pragma unroll
+                for (int dn = 0; dn < DN; dn += 2) {
+                    uint32_t b0, b1, b2, b3;
+                    ldsm_x4_t(vb + swz<D>(sub * 32 + kj * 16 + (lane & 15), dn + (lane >> 4)), b0, b1, b2, b3);
+                    mma16816(o[dn], pa[kj], b0, b1);
+                    mma16816(o[dn + 1], pa[kj], b2, b3);
+                }
+            }
+        }
+        __syncthreads();  // buffer j & 1 is refilled by the next iteration's issue
+    }
+
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+    const int t_r0 = tq0 + warp * 16 + g;
+    if (t_r0 < C) {
+        uint16_t* ar = a + (size_t)t_r0 * Hq * D + (size_t)h * D + 2 * u;
+#pragma unroll
+        for (int dn = 0; dn < DN; ++dn)
+            *reinterpret_cast<uint32_t*>(ar + dn * 8) = pack_h2(o[dn][0] / l0, o[dn][1] / l0);
+    }
+    if (t_r0 + 8 < C) {
+        uint16_t* ar = a + (size_t)(t_r0 + 8) * Hq * D + (size_t)h * D + 2 * u;
+#pragma unroll
+        for (int dn = 0; dn < DN; ++dn)
+            *reinterpret_cast<uint32_t*>(ar + dn * 8) = pack_h2(o[dn][2] / l1, o[dn][3] / l1);
     }
 }
 
@@ -581,13 +686,13 @@ q4_status prefill_attn_enqueue(const uint16_t* q, const uint16_t* k, const uint1
                              : ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_kernel<64>), marks64,
                                                 (int)q4a::prefill_smem(64));
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_attn_kernel)");
-    const dim3 grid(Hq, (C + q4a::kPQ - 1) / q4a::kPQ);
+    const dim3 grid(Hq, (C + q4a::kFQ - 1) / q4a::kFQ);
     if (D == 128)
-        q4a::prefill_attn_kernel<128><<<grid, q4a::kPQ * 32, q4a::prefill_smem(128), s>>>(
-            q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a, dev->err_word);
+        q4a::prefill_attn_kernel<128><<<grid, q4a::kFThreads, q4a::prefill_smem(128), s>>>(
+            q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a);
     else
-        q4a::prefill_attn_kernel<64><<<grid, q4a::kPQ * 32, q4a::prefill_smem(64), s>>>(
-            q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a, dev->err_word);
+        q4a::prefill_attn_kernel<64><<<grid, q4a::kFThreads, q4a::prefill_smem(64), s>>>(
+            q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
     return Q4_OK;

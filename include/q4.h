@@ -54,7 +54,7 @@ typedef struct CUstream_st *q4_stream_t;
 typedef enum q4_status {
     Q4_OK = 0,
     Q4_ERR_INVALID_ARG = -1,  /* null pointer, bad size or shape */
-    Q4_ERR_UNSUPPORTED = -2,  /* valid request this build does not serve (e.g. M > 8) */
+    Q4_ERR_UNSUPPORTED = -2,  /* valid request the library does not serve (e.g. M > 8) */
     Q4_ERR_MISALIGNED = -3,   /* a pointer or leading dimension breaks the alignment rule */
     Q4_ERR_CUDA = -4,         /* a CUDA runtime call failed; see q4_last_error() */
     Q4_ERR_TIMEOUT = -5,      /* a device-side bounded wait ran out (reported by q4_device_status) */

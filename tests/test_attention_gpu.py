@@ -79,14 +79,14 @@ def attn_model(seed, n_layers=3):
     return shape, layers, lm
 
 
-def gpu_attn_table(shape, layers, lm, max_seq, caches, pos, flags=0):
+def gpu_attn_table(shape, layers, lm, max_seq, caches, pos, flags=0, d=D_HEAD):
     dl, keep = [], []
     for d, (kc, vc) in zip(layers, caches):
         e = {k: (*dev_q4(d[k]), d[k].N, d[k].K) for k in ("q", "k", "v", "o", "gate", "up", "down")}
         e["k_cache"], e["v_cache"] = kc, vc
         dl.append(e)
     t = q4.LayerTable(dl, (*dev_q4(lm), lm.N, lm.K), hidden=shape.hidden, M=1,
-                      flags=q4.Q4_DECODE_ATTENTION | flags, head_dim=D_HEAD, max_seq=max_seq, pos=pos)
+                      flags=q4.Q4_DECODE_ATTENTION | flags, head_dim=d, max_seq=max_seq, pos=pos)
     nws = q4.q4_decode_workspace_bytes(t)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     t.set_workspace(ws, nws)
@@ -98,15 +98,15 @@ def read16(ws, ptr, n):
     return ws[off:off + 2 * n].view(torch.float16).float().cpu().numpy()
 
 
-def host_caches(shape, max_seq, fill, seed):
+def host_caches(shape, max_seq, fill, seed, d=D_HEAD):
     g = np.random.default_rng(seed)
     out = []
     for _ in range(shape.n_layers):
-        kc = np.zeros((shape.kv // D_HEAD, max_seq, D_HEAD), np.float16)
+        kc = np.zeros((shape.kv // d, max_seq, d), np.float16)
         vc = np.zeros_like(kc)
         if fill:
-            kc[:, :fill] = rand16(g, shape.kv // D_HEAD, fill, D_HEAD)
-            vc[:, :fill] = rand16(g, shape.kv // D_HEAD, fill, D_HEAD)
+            kc[:, :fill] = rand16(g, shape.kv // d, fill, d)
+            vc[:, :fill] = rand16(g, shape.kv // d, fill, d)
         out.append((kc, vc))
     return out
 
@@ -169,8 +169,8 @@ def test_decode_attention_graph_replay_matches_direct_launches():
 
 # ---------------------------------------------------- prefill with attention ---
 
-def prefill_attn_run(shape, layers, lm, dc, pos, x, chunk):
-    t, _ = gpu_attn_table(shape, layers, lm, dc[0][0].shape[1], dc, pos)
+def prefill_attn_run(shape, layers, lm, dc, pos, x, chunk, d=D_HEAD):
+    t, _ = gpu_attn_table(shape, layers, lm, dc[0][0].shape[1], dc, pos, d=d)
     T = x.shape[0]
     h = torch_dev(x).clone()
     nws = q4.q4_prefill_workspace_bytes(t, chunk)
@@ -215,6 +215,33 @@ def test_prefill_with_attention(start, chunk):
         assert np.allclose(gv[:, sl], vc[:, sl], rtol=2e-2, atol=2e-2)
         assert np.array_equal(gk[:, :start], kc[:, :start].astype(np.float64))
         assert np.array_equal(gk[:, start + T:], kc[:, start + T:].astype(np.float64))
+    t.release()
+
+
+@pytest.mark.parametrize("d", [64, 128])
+def test_prefill_attention_several_query_blocks(d):
+    # one chunk of 150 tokens (query blocks of 64, 64 and a ragged 22) after
+    # 40 cached positions (key tiles of 64: 0..63, 64..127, 128..189); with
+    # hidden 256, head_dim 128 gives 2 query heads on 1 kv head
+    shape, layers, lm = attn_model(1900 + d, n_layers=2)
+    max_seq, start, T, chunk = 200, 40, 150, 160
+    hc = host_caches(shape, max_seq, start, 1901 + d, d)
+    dc = [(torch_dev(kc), torch_dev(vc)) for kc, vc in hc]
+    pos = torch.tensor([start], dtype=torch.int32, device="cuda")
+    x = q4synth.activations(1902 + d, T, shape.hidden)
+    t, st, h, lg, ws = prefill_attn_run(shape, layers, lm, dc, pos, x, chunk, d)
+    assert st == 0 and int(pos.item()) == start + T
+    b = q4.q4_prefill_buffers(t, chunk, ws)
+    kl, vl = dc[-1][0].cpu().numpy(), dc[-1][1].cpu().numpy()
+    for i in range(T):
+        qg = read16(ws, b["q"] + 2 * i * shape.q, shape.q).astype(np.float16)
+        ag = read16(ws, b["a"] + 2 * i * shape.q, shape.q)
+        a_ref, A_a = oracle.attention(qg, kl, vl, start + i + 1, d, start + i)
+        assert_parity(ag[None, :], a_ref[None, :], A_a[None, :], fp16_out=True, what=f"d={d} t={i}")
+    h_ref, y_ref, _ = oracle.prefill_attn(layers, lm, x, hc, start, d)
+    r_h = np.linalg.norm(h.float().cpu().numpy() - h_ref) / np.linalg.norm(h_ref.astype(np.float64))
+    r_y = np.linalg.norm(lg.cpu().numpy() - y_ref[0]) / np.linalg.norm(y_ref[0])
+    assert r_h <= 1e-3 and r_y <= 1e-3, (r_h, r_y)
     t.release()
 
 
