@@ -79,14 +79,14 @@ def attn_model(seed, n_layers=3):
     return shape, layers, lm
 
 
-def gpu_attn_table(shape, layers, lm, max_seq, caches, pos, flags=0, d=D_HEAD):
+def gpu_attn_table(shape, layers, lm, max_seq, caches, pos, flags=0, hd=D_HEAD):
     dl, keep = [], []
     for d, (kc, vc) in zip(layers, caches):
         e = {k: (*dev_q4(d[k]), d[k].N, d[k].K) for k in ("q", "k", "v", "o", "gate", "up", "down")}
         e["k_cache"], e["v_cache"] = kc, vc
         dl.append(e)
     t = q4.LayerTable(dl, (*dev_q4(lm), lm.N, lm.K), hidden=shape.hidden, M=1,
-                      flags=q4.Q4_DECODE_ATTENTION | flags, head_dim=d, max_seq=max_seq, pos=pos)
+                      flags=q4.Q4_DECODE_ATTENTION | flags, head_dim=hd, max_seq=max_seq, pos=pos)
     nws = q4.q4_decode_workspace_bytes(t)
     ws = torch.empty(nws, dtype=torch.uint8, device="cuda")
     t.set_workspace(ws, nws)
@@ -170,7 +170,7 @@ def test_decode_attention_graph_replay_matches_direct_launches():
 # ---------------------------------------------------- prefill with attention ---
 
 def prefill_attn_run(shape, layers, lm, dc, pos, x, chunk, d=D_HEAD):
-    t, _ = gpu_attn_table(shape, layers, lm, dc[0][0].shape[1], dc, pos, d=d)
+    t, _ = gpu_attn_table(shape, layers, lm, dc[0][0].shape[1], dc, pos, hd=d)
     T = x.shape[0]
     h = torch_dev(x).clone()
     nws = q4.q4_prefill_workspace_bytes(t, chunk)
