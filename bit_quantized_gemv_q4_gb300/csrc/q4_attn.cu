@@ -394,7 +394,8 @@ __device__ __forceinline__ void split_h2(float x, float y, uint32_t& hi, uint32_
     lo = pack_h2(x - f.x, y - f.y);
 }
 
-// Grid (Hq, ceil(C / 64)), 128 threads.  Token t of the chunk (position
+// Grid (Hq, ceil(C / 64)), 128 threads; block y takes token block
+// ceil(C / 64) - 1 - y.  Token t of the chunk (position
 // p0 + t) attends over positions 0..p0 + t of its kv head's cache.
 // Fragment layouts (PTX mma.m16n8k16): with g = lane / 4 and u = lane % 4, an
 // A register pair covers (row g or g + 8, columns 2u, 2u + 1 or 2u + 8, 2u + 9),
@@ -420,7 +421,8 @@ __global__ void __launch_bounds__(kFThreads) prefill_attn_kernel(const uint16_t*
     const int kvh = h / G;
     const int p0 = *pos_p + t0;
     if (p0 < 0 || p0 + C > max_seq) return;  // latched by the append kernel
-    const int tq0 = blockIdx.y * kFQ;
+    // the last token blocks (the most keys under the causal mask) start first
+    const int tq0 = (gridDim.y - 1 - blockIdx.y) * kFQ;
     const int n_keys = p0 + min(tq0 + kFQ, C);  // keys the CTA's last token sees
     const int n_tiles = (n_keys + kFK - 1) / kFK;
     const uint16_t* kh = kc + (size_t)kvh * max_seq * D;
