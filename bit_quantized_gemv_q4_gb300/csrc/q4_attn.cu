@@ -24,6 +24,12 @@
 // table the other kernels read; the rotations themselves are fp32.  Inside a
 // decode step only the first layer launches that append kernel: in the other
 // layers the CTA whose chunk holds the new position appends the token itself.
+//
+// Prefill (second half of the file): for a chunk of prompt tokens, one table
+// of rotations per chunk, an append kernel per layer writing the chunk's
+// rotated keys and values into the caches, and a causal attention that is a
+// dense contraction (every token against every earlier key), so it runs on
+// the tensor cores, flash-attention style.
 #include <cuda_fp16.h>
 #include <math.h>
 

@@ -1,10 +1,12 @@
-// Q4 group-64 GEMV for decode (M = 1) and batched decode (M = 2..8), with the
+// Group-64 GEMV for decode (M = 1) and batched decode (M = 2..8), with the
 // dequantisation inside the dot product (BaseRT: optimal LLM inference on
 // Apple Silicon with native Metal, §3.3 "Kernel fusion and specialisation"),
 // several matrices sharing one x per launch (same section: fused operator
 // sequences; "Mac on-device AI performance breakthrough" §2.2: Q, K, V merged
 // into one product) and fused prologue/epilogues (RMSNorm of x, fp16 store,
-// residual add, SiLU*up).
+// residual add, SiLU*up).  The code width is a template parameter: 4 bits
+// (the main path) and 8 bits at M = 1..8, 2, 3, 5 and 6 bits at M = 1 (BaseRT
+// §3.3 and §4.1: a kernel per quantisation format).
 //
 // GB300 design
 // ------------
@@ -33,7 +35,8 @@
 //   wait on the previous kernel (weights never depend on it); only the x load
 //   and the epilogue wait.  Inside a decode step x may instead arrive as
 //   tagged words that are polled (no wait for the previous grid), and the
-//   whole step may run as one persistent cooperative launch (end of file).
+//   whole step may run as one persistent cooperative launch whose stages
+//   start on a completion counter (end of file).
 // * Every wait is bounded; on expiry the kernel latches an error bit and
 //   leaves.
 #include <cuda_fp16.h>
