@@ -462,8 +462,11 @@ size_t q4_prefill_workspace_bytes(const q4_layer_table *table, int chunk);
  * written to position p of every layer's cache, it attends causally over
  * positions 0..p (a = fp16 attention output, replacing q as the input of o),
  * and *pos advances by T at the end, so decode steps continue the sequence;
- * positions beyond max_seq latch Q4_ERR_DEVICE_CHECK.  chunk >= 1, T >= 0;
- * allocates nothing. */
+ * positions beyond max_seq latch Q4_ERR_DEVICE_CHECK.  The prompt's attention
+ * runs on the tensor cores: its scores carry the fp32 rotated query (as an
+ * fp16 hi + lo pair) and its probabilities enter the value product in fp16
+ * (sum kept in fp32), an error below 5e-4 * sum_j p_j |v_j| per output
+ * element.  chunk >= 1, T >= 0; allocates nothing. */
 q4_status q4_prefill(const q4_layer_table *table, uint16_t *h, int T, int chunk, void *logits,
                      void *workspace, size_t workspace_bytes, q4_stream_t stream);
 
