@@ -178,11 +178,15 @@ def _check(status: int, where: str):
 
 
 def _ptr(t) -> int | None:
-    """Device pointer of a torch tensor, an int, or None."""
+    """Device pointer of a torch tensor in CUDA memory, an int (a raw device
+    pointer, passed as is), or None.  A tensor in host memory is refused here:
+    the kernels would dereference its address on the device."""
     if t is None:
         return None
     if isinstance(t, int):
         return t
+    if not t.is_cuda:
+        raise ValueError(f"expected a tensor in CUDA device memory, got one on {t.device}")
     return t.data_ptr()
 
 

@@ -240,3 +240,14 @@ def test_decode_attention_table_validation(L):
         tb = q4.LayerTable([layer], lin(100, 64), **args)
         assert L.q4_decode_workspace_bytes(ctypes.byref(tb.t)) == 0, kw
         assert frag in L.q4_last_error(), (kw, L.q4_last_error())
+
+
+def test_binding_refuses_host_tensors(L):
+    # a host address handed to a kernel would be dereferenced on the device:
+    # the binding refuses a tensor that is not in CUDA memory before any call
+    torch = pytest.importorskip("torch")
+    host = torch.zeros(64, dtype=torch.int32)
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        q4.q4_gemv(host, host, host, host, host, 1, 8, 64)
+    with pytest.raises(ValueError, match="CUDA device memory"):
+        q4.LayerTable([], (host, host, host, 8, 64), hidden=64, M=1)
