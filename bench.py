@@ -38,6 +38,9 @@ METRIC = "Q4 fused-dequant GEMV HBM GB/s (% of peak); decode-step matmul tok/s"
 FALLBACK_HBM_GBS = 6800.0
 
 
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e, nominal (context beside the measured copy bandwidth)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -760,6 +763,7 @@ def main():
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic", "config": config,
         "hbm_gbs": achieved, "hbm_frac_of_measured": achieved / peak,
+        "hbm_frac_of_nominal": achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind,
                      "kernel": "q4_gemv_kernel<1> (all 113 launches of a step; achieved = algorithmic bytes "
