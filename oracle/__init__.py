@@ -55,6 +55,8 @@ _SRC = os.path.join(_HERE, "q4_oracle.c")
 
 
 def lib_path(mutant: int = 0) -> str:
+    """Path of the compiled C oracle (or of a planted-mistake build). Infrastructure:
+    no passage."""
     return os.path.join(_HERE, "libq4oracle.so" if mutant == 0 else f"libq4oracle_mut{mutant}.so")
 
 
@@ -104,10 +106,15 @@ def _lib(mutant: int = 0) -> ctypes.CDLL:
 
 
 def max_threads() -> int:
+    """OpenMP threads the C oracle uses (reported beside the CPU baseline).
+    Infrastructure: no passage."""
     return _lib().q4o_max_threads()
 
 
 def half_to_double(bits: int) -> float:
+    """The C oracle's decoding of one IEEE binary16 bit pattern to fp64 (the fp16
+    scales, biases and activations of the storage format; pinned against numpy on every
+    pattern)."""
     return _lib().q4o_half_to_double(int(bits) & 0xFFFF)
 
 
@@ -119,7 +126,12 @@ def gemv(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
     """y[M, R], A[M, R] in fp64 for W [N, K] (storage format) and x [M, K].
 
     x is fp16 (converted exactly) or fp64 (used as is).  ``rows`` (optional)
-    selects output rows; R = len(rows) (else N)."""
+    selects output rows; R = len(rows) (else N).
+
+    Follows BaseRT §3.3 (the matmul with the dequantisation inside its loop; w =
+    scale*q + bias per 64-wide group) on the 4-bit files of MetalRT §2.1; the bit
+    layout is the reading this library fixes (lowest nibble first).
+    """
     Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
     scales = np.ascontiguousarray(scales, dtype=np.float16)
     biases = np.ascontiguousarray(biases, dtype=np.float16)
@@ -154,7 +166,11 @@ def gemv(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
 
 def gemv8(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
     """gemv() for 8-bit codes: Wq uint32 [N, K/4], code k in byte k % 4 of
-    word k // 4 (lowest byte first), q in 0..255, w = s * q + b per 64-group."""
+    word k // 4 (lowest byte first), q in 0..255, w = s * q + b per 64-group.
+
+    Follows BaseRT §3.3 and §4.1 (one kernel per quantisation format; Q8 is one of the
+    two evaluated).
+    """
     Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
     scales = np.ascontiguousarray(scales, dtype=np.float16)
     biases = np.ascontiguousarray(biases, dtype=np.float16)
@@ -190,7 +206,11 @@ def gemv8(Wq, scales, biases, x, rows=None, nthreads: int = 0, mutant: int = 0):
 def gemvb(Wq, scales, biases, x, bits: int, rows=None, nthreads: int = 0, mutant: int = 0):
     """gemv() for b-bit codes (b in 2..8): Wq uint32 [N, K*b/32], code k of
     a row in bits b*k .. b*k+b-1 of the row's little-endian bit stream,
-    q in 0..2^b-1, w = s * q + b per 64-group."""
+    q in 0..2^b-1, w = s * q + b per 64-group.
+
+    Follows BaseRT §3.3 and §4.1 (kernels for 2- to 16-bit formats); the bit-stream
+    layout is the reading this library fixes.
+    """
     Wq = np.ascontiguousarray(Wq, dtype=np.uint32)
     scales = np.ascontiguousarray(scales, dtype=np.float16)
     biases = np.ascontiguousarray(biases, dtype=np.float16)
@@ -224,30 +244,47 @@ def gemvb(Wq, scales, biases, x, bits: int, rows=None, nthreads: int = 0, mutant
 
 
 def codeb(Wq_row, k: int, bits: int, mutant: int = 0) -> int:
-    """The b-bit code k of one packed row (as the oracle reads it)."""
+    """The b-bit code k of one packed row (as the oracle reads it).
+
+    Follows BaseRT §3.3 and §4.1 (b-bit formats), in the bit-stream reading.
+    """
     row = np.ascontiguousarray(Wq_row, dtype=np.uint32)
     return _lib(mutant).qbo_code(_p(row), k, bits)
 
 
 def code8(Wq_row, k: int, mutant: int = 0) -> int:
-    """The 8-bit code k of one packed row (as the oracle reads it)."""
+    """The 8-bit code k of one packed row (as the oracle reads it).
+
+    Follows BaseRT §3.3 and §4.1 (the 8-bit format), lowest byte first.
+    """
     row = np.ascontiguousarray(Wq_row, dtype=np.uint32)
     return _lib(mutant).q8o_code(_p(row), k)
 
 
 def fp16(v) -> np.ndarray:
     """Round fp64 values to fp16, round-to-nearest-even (numpy converts
-    directly from double, not through float32)."""
+    directly from double, not through float32).
+
+    The pages do not say how stored activations round; the reading taken is IEEE
+    round-to-nearest-even, as the GPU's fp16 stores do.
+    """
     return np.asarray(v, dtype=np.float64).astype(np.float16)
 
 
 def silu(g):
+    """SiLU(g) = g / (1 + exp(-g)) in fp64: the gate of the fused gate/up FFN step
+    (BaseRT §3.3 fuses the FFN's operator sequence; the pages print no formula, this is
+    the standard definition)."""
     g = np.asarray(g, dtype=np.float64)
     return g / (1.0 + np.exp(-g))
 
 
 def ulp16(v) -> np.ndarray:
-    """Spacing of fp16 numbers at |v| (2^-24 in the subnormal range)."""
+    """Spacing of fp16 numbers at |v| (2^-24 in the subnormal range).
+
+    Helper of the parity bar (an fp16 store may round either way of a value within the
+    fp32 error). No passage.
+    """
     a = np.abs(np.asarray(v, dtype=np.float64))
     e = np.floor(np.log2(np.maximum(a, 2.0 ** -14)))
     return np.exp2(e - 10)
@@ -259,7 +296,12 @@ DEFAULT_EPS = 1e-6
 
 
 def rmsnorm(h, gamma=None, eps: float = DEFAULT_EPS):
-    """h / sqrt(mean(h^2) + eps) * gamma, per row, in fp64 (gamma None = 1)."""
+    """h / sqrt(mean(h^2) + eps) * gamma, per row, in fp64 (gamma None = 1).
+
+    Follows BaseRT §3.3 (normalisation kernels fused into the attention path and FFN)
+    and MetalRT §5.1 (the norm kept in fp32); the RMS form is the reading taken for the
+    pre-norm layer.
+    """
     h = np.atleast_2d(np.asarray(h, dtype=np.float64))
     r = h / np.sqrt(np.mean(h * h, axis=1, keepdims=True) + eps)
     if gamma is not None:
@@ -272,7 +314,11 @@ def _mat(m):
 
 
 def decode_qkv(layer, h, rows=None, eps: float = DEFAULT_EPS):
-    """q, k, v = W rmsnorm(h) for the fused QKV stage; dict of (y, A)."""
+    """q, k, v = W rmsnorm(h) for the fused QKV stage; dict of (y, A).
+
+    Follows "Mac on-device AI performance breakthrough" §2.2 (Q, K, V merged into one
+    product) and BaseRT §3.3 (the norm fused into the launch).
+    """
     n = rmsnorm(h, layer.get("attn_norm"), eps)
     out = {}
     for nm in ("q", "k", "v"):
@@ -282,7 +328,11 @@ def decode_qkv(layer, h, rows=None, eps: float = DEFAULT_EPS):
 
 
 def decode_o(layer, a, h, rows=None):
-    """h' = h + Wo a (fp64, before the fp16 store), A incl. |h|."""
+    """h' = h + Wo a (fp64, before the fp16 store), A incl. |h|.
+
+    Follows BaseRT §3 and §3.3 (the decode step as a chain of fused GEMVs; the residual
+    add fused into the o launch) in the pre-norm dataflow reading.
+    """
     y, A = gemv(*_mat(layer["o"]), a, rows=rows)
     hh = np.atleast_2d(h).astype(np.float64)
     if rows is not None:
@@ -291,7 +341,10 @@ def decode_o(layer, a, h, rows=None):
 
 
 def decode_glu(layer, h, rows=None, eps: float = DEFAULT_EPS):
-    """g, u from rmsnorm(h') and act = SiLU(g) * u (fp64, before the store)."""
+    """g, u from rmsnorm(h') and act = SiLU(g) * u (fp64, before the store).
+
+    Follows BaseRT §3.3 (gate and up products with SiLU*up fused into one FFN launch).
+    """
     n = rmsnorm(h, layer.get("ffn_norm"), eps)
     g, Ag = gemv(*_mat(layer["gate"]), n, rows=rows)
     u, Au = gemv(*_mat(layer["up"]), n, rows=rows)
@@ -299,6 +352,9 @@ def decode_glu(layer, h, rows=None, eps: float = DEFAULT_EPS):
 
 
 def decode_down(layer, act, h, rows=None):
+    """h + Wd act for the down stage, fp64 before the fp16 store, and A including |h|
+    (BaseRT §3.3: the FFN's operator sequence fused; the residual add is part of the
+    dataflow reading)."""
     y, A = gemv(*_mat(layer["down"]), act, rows=rows)
     hh = np.atleast_2d(h).astype(np.float64)
     if rows is not None:
@@ -307,11 +363,18 @@ def decode_down(layer, act, h, rows=None):
 
 
 def decode_logits(lm_head, h, final_norm=None, rows=None, eps: float = DEFAULT_EPS):
+    """Wlm (rmsnorm(h) * final_norm): the last GEMV of the decode step (BaseRT §3: the
+    decode hot path ends in the vocabulary projection; the final norm is part of the
+    pre-norm reading)."""
     return gemv(*_mat(lm_head), rmsnorm(h, final_norm, eps), rows=rows)
 
 
 def decode_layer(layer, h, eps: float = DEFAULT_EPS):
-    """One layer, every stored activation rounded to fp16 as the GPU stores it."""
+    """One layer, every stored activation rounded to fp16 as the GPU stores it.
+
+    Follows BaseRT §3 (one decode layer as a fixed sequence of kernels) in the pre-norm
+    dataflow reading.
+    """
     qkv = decode_qkv(layer, h, eps=eps)
     q = fp16(qkv["q"][0])
     hm = fp16(decode_o(layer, q, h)[0])
@@ -321,7 +384,11 @@ def decode_layer(layer, h, eps: float = DEFAULT_EPS):
 
 
 def decode_step(layers, lm_head, x, final_norm=None, eps: float = DEFAULT_EPS):
-    """Whole decode step: fp16 x [M, hidden] -> fp64 logits [M, vocab]."""
+    """Whole decode step: fp16 x [M, hidden] -> fp64 logits [M, vocab].
+
+    Follows BaseRT §3 and §3.1 (a whole decode step driven by a layer descriptor) in
+    the pre-norm dataflow reading.
+    """
     h = np.atleast_2d(x).astype(np.float16)
     for layer in layers:
         h = decode_layer(layer, h, eps)["h"]
@@ -352,7 +419,10 @@ def prefill(layers, lm_head, x, final_norm=None, eps: float = DEFAULT_EPS):
     """Prefill of T tokens: fp16 x [T, hidden] -> (final h [T, hidden] as
     fp16 values, logits y [1, vocab] and A of the LAST token).  The tokens do
     not interact in this stack (no attention), so chunking does not change
-    the result; the logits come from the decode path's lm_head product."""
+    the result; the logits come from the decode path's lm_head product.
+
+    Follows BaseRT §3.4 (the prompt processed as GEMMs, chunk by chunk).
+    """
     h = np.atleast_2d(x).astype(np.float16)
     for layer in layers:
         h = prefill_layer(layer, h, eps)["h"]
@@ -368,7 +438,11 @@ DEFAULT_ROPE_THETA = 1.0e6
 def rope(x, pos: int, head_dim: int, theta: float = DEFAULT_ROPE_THETA):
     """Rotary position embedding of every head of x [..., H*head_dim] at one
     position, rotate-half form: for i < d/2 the pair (x_i, x_{i+d/2}) turns by
-    pos * theta^(-2i/d).  fp64."""
+    pos * theta^(-2i/d).  fp64.
+
+    Follows BaseRT §3.3 (RoPE among the decode kernels); the pages print no formula, so
+    the rotate-half form of Qwen3/Llama is the reading taken.
+    """
     x = np.asarray(x, dtype=np.float64)
     d = head_dim
     xs = x.reshape(x.shape[:-1] + (-1, d))
@@ -384,7 +458,11 @@ def attention(q, k_cache, v_cache, n: int, head_dim: int, pos: int, theta: float
     """Decode attention of one token: q [Hq*d] (fp16 values, not yet rotated)
     against positions 0..n-1 of the caches [Hkv, max_seq, d] (keys stored
     rotated).  Query head h reads key/value head h // (Hq / Hkv).  Returns
-    a [Hq*d] and A [Hq*d] = sum_j p_j |v_j| (fp64)."""
+    a [Hq*d] and A [Hq*d] = sum_j p_j |v_j| (fp64).
+
+    Follows BaseRT §3.3 (attention among the decode kernels) and §3.2 (a preallocated
+    KV cache); softmax(q.K^T / sqrt(d)).V is the plain definition.
+    """
     d = head_dim
     qr = rope(q, pos, d, theta).reshape(-1, d)
     Hq, Hkv = qr.shape[0], k_cache.shape[0]
@@ -426,7 +504,11 @@ def decode_step_attn(layers, lm_head, x, caches, pos: int, head_dim: int, theta:
                      final_norm=None, eps: float = DEFAULT_EPS):
     """One decode step of one sequence with attention: x fp16 [1, hidden];
     caches = [(k_cache, v_cache)] per layer, updated at `pos`.  Returns
-    (logits [1, vocab], A, final h)."""
+    (logits [1, vocab], A, final h).
+
+    Follows BaseRT §3.2 and §3.3 (the decode step with its attention over the
+    preallocated cache).
+    """
     h = np.atleast_2d(x).astype(np.float16)
     for layer, (kc, vc) in zip(layers, caches):
         h = decode_layer_attn(layer, h, kc, vc, pos, head_dim, theta, eps)["h"]
@@ -440,7 +522,11 @@ def prefill_layer_attn(layer, h, k_cache, v_cache, pos0: int, head_dim: int, the
     pos0 + t; their rotated keys and values are written to the caches (fp16),
     then token t attends over positions 0..pos0+t (causal), a rounded to fp16
     feeds o.  The normalised activations are stored in fp16 as in
-    prefill_layer."""
+    prefill_layer.
+
+    Follows BaseRT §3.4 (prompt GEMMs) with causal attention over the cache (BaseRT
+    §3.2, §3.3).
+    """
     h = np.atleast_2d(h)
     T = h.shape[0]
     Hkv = k_cache.shape[0]
@@ -467,7 +553,11 @@ def prefill_attn(layers, lm_head, x, caches, pos0: int, head_dim: int, theta: fl
     """Prefill of T tokens at positions pos0.. with attention, filling the
     caches: (final h [T, hidden], logits y [1, vocab] and A of the last token).
     Chunking does not change the result (keys of earlier chunks are in the
-    cache before later tokens attend to them)."""
+    cache before later tokens attend to them).
+
+    Follows BaseRT §3.4 (prefill in chunks) with the cache filled for the decode steps
+    that follow (BaseRT §3.2).
+    """
     h = np.atleast_2d(x).astype(np.float16)
     for layer, (kc, vc) in zip(layers, caches):
         h = prefill_layer_attn(layer, h, kc, vc, pos0, head_dim, theta, eps)["h"]
@@ -483,7 +573,12 @@ def moe_route(logits, topk: int):
     Returns ids [T, topk] (by descending logit, ties to the lower expert),
     weights [T, topk] fp64 (softmax over the chosen logits), offsets [E+1],
     token_of [R], expert_of [R], rank_of [R] (R = T*topk rows sorted stably by
-    (expert, token, rank)), pos [T, topk] (sorted row of each (t, k))."""
+    (expert, token, rank)), pos [T, topk] (sorted row of each (t, k)).
+
+    Follows BaseRT, abstract and Fig. 1 (MoE prefill on a Qwen3-30B-A3B-shaped model);
+    the pages do not describe routing, so top-k with ties to the lower expert and a
+    softmax over the chosen logits is the reading taken.
+    """
     logits = np.asarray(logits, dtype=np.float16)
     T, E = logits.shape
     ids = np.empty((T, topk), np.int32)
@@ -519,7 +614,11 @@ def _expert(m, e):
 def moe_gate_up_rows(gu, X_rows, experts, ffn: int):
     """For each row r: g = Wg[e] X_r, u = Wu[e] X_r (gate = rows 0..ffn-1 and up =
     rows ffn..2ffn-1 of the fused expert matrix).  Returns g, Ag, u, Au, act
-    (fp64, before the fp16 store), each [len(rows), ffn]."""
+    (fp64, before the fp16 store), each [len(rows), ffn].
+
+    Follows BaseRT §3.4 (prefill GEMMs) on the routed experts of the abstract's MoE
+    model.
+    """
     n = len(experts)
     g = np.empty((n, ffn)); Ag = np.empty((n, ffn)); u = np.empty((n, ffn)); Au = np.empty((n, ffn))
     gate_rows = np.arange(ffn, dtype=np.int64)
@@ -533,7 +632,11 @@ def moe_gate_up_rows(gu, X_rows, experts, ffn: int):
 
 
 def moe_down_rows(dn, H_rows, experts, cols=None):
-    """Y_r = Wd[e] H_r for each row; returns (y, A) [len(rows), len(cols) or N]."""
+    """Y_r = Wd[e] H_r for each row; returns (y, A) [len(rows), len(cols) or N].
+
+    Follows BaseRT §3.4 (prefill GEMMs) on the routed experts of the abstract's MoE
+    model.
+    """
     out_y, out_a = [], []
     for i, e in enumerate(experts):
         y, A = gemv(*_expert(dn, int(e)), H_rows[i:i + 1], rows=cols)
@@ -542,7 +645,11 @@ def moe_down_rows(dn, H_rows, experts, cols=None):
 
 
 def moe_combine(Y, pos, weights):
-    """out[t] = sum_{k=0}^{topk-1} p[t,k] * Y[pos[t,k]], k in rank order, fp64."""
+    """out[t] = sum_{k=0}^{topk-1} p[t,k] * Y[pos[t,k]], k in rank order, fp64.
+
+    The weighted sum of the routed rows back per token; the pages do not describe it,
+    so rank order in fp64 is the reading taken (BaseRT abstract: MoE prefill).
+    """
     Y = np.asarray(Y, dtype=np.float64)
     T, topk = pos.shape
     out = np.zeros((T, Y.shape[1]))

@@ -56,7 +56,8 @@ double q4o_half_to_double(uint16_t h)
     return sign ? -v : v;
 }
 
-/* The 4-bit code of weight k in one packed row. */
+/* The 4-bit code of weight k in one packed row (the storage reading above:
+ * lowest nibble first; the pages print no layout). */
 int q4o_code(const uint32_t *row, int64_t k)
 {
 #if Q4O_MUTANT == 1 /* mistake: highest nibble first */
@@ -66,7 +67,8 @@ int q4o_code(const uint32_t *row, int64_t k)
 #endif
 }
 
-/* Dequantised weight w[n][k] = s * q + b, in fp64. */
+/* Dequantised weight w[n][k] = s * q + b, in fp64 (the affine group format
+ * the BaseRT §3.3 kernels dequantise in their inner loop). */
 static double q4o_weight(const uint32_t *row, const uint16_t *s_row, const uint16_t *b_row, int64_t k)
 {
 #if Q4O_MUTANT == 3 /* mistake: group of 32 instead of 64 */
@@ -88,10 +90,11 @@ static double q4o_weight(const uint32_t *row, const uint16_t *s_row, const uint1
 }
 
 /*
- * y[m][i], A[m][i] for the rows listed in rows[0..nrows) (all rows 0..N-1
- * when rows == NULL, nrows = N), with x given in fp64: x [M][K], y and A
- * [M][nrows].  A may be NULL.  nthreads <= 0 uses the OpenMP default.
- * Returns 0, or -1 on a bad argument.
+ * The definition at the top of this file (BaseRT §3.3): y[m][i], A[m][i] for
+ * the rows listed in rows[0..nrows) (all rows 0..N-1 when rows == NULL,
+ * nrows = N), with x given in fp64: x [M][K], y and A [M][nrows].  A may be
+ * NULL.  nthreads <= 0 uses the OpenMP default.  Returns 0, or -1 on a bad
+ * argument.
  */
 int q4o_gemv_f64(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                  const double *xd, int64_t M, int64_t N, int64_t K,
@@ -150,9 +153,9 @@ int q4o_gemv(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
 }
 
 /*
- * The same product for 8-bit codes (the pages' 8-bit format, BaseRT §3.3 and
- * §4.1: "Q4 and Q8 evaluated"; their bit layout is not printed, so the one
- * the library fixes is used): Wq uint32 [N][K/4]; code k of row n is bits
+ * The same product for 8-bit codes (the pages' 8-bit format: BaseRT §3.3 and
+ * §4.1 evaluate Q4 and Q8; the bit layout is not printed, so the one the
+ * library fixes is used): Wq uint32 [N][K/4]; code k of row n is bits
  * 8*(k%4) .. 8*(k%4)+7 of word k/4 (lowest byte first), q in 0..255; one fp16
  * scale and bias per group of 64; w = s * q + b; fp64 accumulation in order
  * k = 0 .. K-1, and A = sum_k |w x| as above.
