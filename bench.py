@@ -564,6 +564,72 @@ def job_rate(world: int, tokens_per_rank_step: int, steps: int, ms_max: float) -
     return world * tokens_per_rank_step * steps / (ms_max / 1000.0)
 
 
+def single_gemv(q4, device, isolated: int = 50, replays: int = 5):
+    """The single small GEMV (M = 1, K = 1024, N = 3072, 1.78 MB) two ways:
+    isolated (one launch between synchronisations, median of 50 over distinct
+    weight copies) and in steady state (a rotating pool of distinct copies
+    totalling more than 3x L2, launched back to back from one CUDA graph so no
+    launch hits L2; best and median of 5 replays).  The public q4_gemv
+    launches without programmatic dependent launch, so the steady state still
+    pays a kernel boundary per launch."""
+    import statistics
+
+    import torch
+
+    import q4synth
+    N, K, M = 3072, 1024, 1
+    nb = N * K * 0.5625 + K * 2 * M + N * 4 * M
+    props = torch.cuda.get_device_properties(device)
+    l2 = int(getattr(props, "L2_cache_size", 0) or (129 << 20))
+    n_copies = int(-(-3 * l2 // int(nb)))
+    gen = torch.Generator(device=device).manual_seed(q4synth.BASE_SEED + 8800)
+    copies = []
+    for _ in range(n_copies):
+        Wq = torch.randint(-2**31, 2**31 - 1, (N, K // 8), dtype=torch.int32, device=device, generator=gen)
+        sc = (torch.rand(N, K // 64, device=device, generator=gen) * 0.005).half()
+        copies.append((Wq, sc, (-8 * sc.float()).half()))
+    x = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 8801, M, K)).to(device)
+    y = torch.empty(M, N, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for c in copies:  # warm-up: every copy once
+        q4.q4_gemv(*c, x, y, M, N, K, stream)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    iso = []
+    for i in range(isolated):
+        torch.cuda.synchronize(device)
+        e0.record(stream)
+        q4.q4_gemv(*copies[i % n_copies], x, y, M, N, K, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        iso.append(e0.elapsed_time(e1))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for c in copies:
+            q4.q4_gemv(*c, x, y, M, N, K)  # the capture stream is current here
+    torch.cuda.synchronize(device)
+    g.replay()
+    torch.cuda.synchronize(device)
+    per = []
+    for _ in range(replays):
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        per.append(e0.elapsed_time(e1) / n_copies)
+    if q4.q4_device_status(stream) != 0:
+        raise RuntimeError("device status after the single-GEMV timing")
+    del g
+    peak, kind = peaks()
+    iso_ms, best, med = statistics.median(iso), min(per), statistics.median(per)
+    gbs = lambda ms: nb / (ms / 1000.0) / 1e9  # noqa: E731
+    return {"shape": f"M={M} N={N} K={K}", "bytes_per_launch": nb, "peak_kind": kind,
+            "isolated_us": iso_ms * 1000.0, "isolated_gbs": gbs(iso_ms),
+            "steady_copies": n_copies, "steady_us_best": best * 1000.0, "steady_us_median": med * 1000.0,
+            "steady_gbs_best": gbs(best), "steady_frac_of_measured": gbs(best) / peak,
+            "steady_frac_of_nominal": gbs(best) / NOMINAL_HBM_GBS}
+
+
 def lm_head_ms(q4, dlm, x, M, stream, device):
     """The largest single launch alone (the lm_head GEMV shape): 8 warm-up
     launches, then 64 timed back to back over 4 distinct weight copies
@@ -596,7 +662,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--section", default="all", choices=["all", "decode", "moe", "lm_head", "prefill", "attention", "streams"],
+    ap.add_argument("--section", default="all",
+                    choices=["all", "decode", "moe", "lm_head", "prefill", "attention", "streams", "gemv"],
                     help="moe / lm_head: only the MoE prefill timings / the lm_head GEMV timing "
                          "(for profiling runs)")
     args = ap.parse_args()
@@ -665,6 +732,9 @@ def main():
         return
     if args.section == "streams":
         print(json.dumps({"decode_streams": decode_streams(device)}))
+        return
+    if args.section == "gemv":
+        print(json.dumps({"single_gemv": single_gemv(q4, device)}))
         return
     if world > 1:
         import torch.distributed as dist
@@ -784,6 +854,10 @@ def main():
         out["moe_prefill"] = moe_prefill(device)
         out["dense_prefill"] = dense_prefill(device, dl, dlm, shape)
         out["decode_attention"] = decode_attention(device, dl, dlm, shape)
+        try:  # context only, measured last; the lines above stand if it fails
+            out["single_gemv"] = single_gemv(q4, device)
+        except Exception as e:  # noqa: BLE001
+            out["single_gemv"] = {"error": f"{type(e).__name__}: {e}"}
     if world == 1 and not args.no_cpu_baseline:
         import oracle
         oracle.build()
