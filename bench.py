@@ -183,11 +183,12 @@ def make_model(shape, device, layers=True):
     return [{k: dev(v) for k, v in d.items()} for d in layers], dev(lm), (layers, lm)
 
 
-def cpu_oracle_rate(shape, host_model, seconds: float, one_sample: bool = False):
+def cpu_oracle_rate(shape, host_model, seconds: float, one_sample: bool = False, nthreads: int = 0):
     """Oracle throughput on a bounded sample, as decode tok/s of the full step.
 
     Sample i = layer (i mod L)'s seven matrices plus the (i mod L)-th of L
-    equal slices of lm_head rows: together 1/L of a step's weights."""
+    equal slices of lm_head rows: together 1/L of a step's weights.
+    nthreads 0 = the oracle's OpenMP default (all cores)."""
     import numpy as np
 
     import oracle
@@ -205,10 +206,10 @@ def cpu_oracle_rate(shape, host_model, seconds: float, one_sample: bool = False)
             m = layers[li][nm]
             if K not in xs:
                 xs[K] = q4synth.activations(q4synth.BASE_SEED + 4243 + K, 1, K)
-            oracle.gemv(m.Wq, m.scales, m.biases, xs[K])
+            oracle.gemv(m.Wq, m.scales, m.biases, xs[K], nthreads=nthreads)
             w += N * K
         rows = np.arange(li * shape.vocab // L, (li + 1) * shape.vocab // L)
-        oracle.gemv(lm.Wq, lm.scales, lm.biases, x, rows=rows)
+        oracle.gemv(lm.Wq, lm.scales, lm.biases, x, rows=rows, nthreads=nthreads)
         w += rows.size * shape.hidden
         t_total += time.perf_counter() - t0
         done_w += w
@@ -862,9 +863,11 @@ def main():
         import oracle
         oracle.build()
         rate, n, t = cpu_oracle_rate(shape, host_model, args.cpu_seconds)
+        rate1, n1, t1 = cpu_oracle_rate(shape, host_model, args.cpu_seconds / 4, nthreads=1)
         out["cpu_baseline"] = {"value": rate, "unit": "tok/s", "cores": oracle.max_threads(), "kind": "oracle",
                                "sample": f"{n} samples of 1/{shape.n_layers} of a token's weights "
-                                         f"(one layer + a lm_head row slice), {t:.1f} s"}
+                                         f"(one layer + a lm_head row slice), {t:.1f} s",
+                               "one_thread": {"value": rate1, "unit": "tok/s", "samples": n1, "seconds": t1}}
     print(json.dumps(out))
     if world > 1:
         torch.distributed.destroy_process_group()
