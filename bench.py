@@ -824,6 +824,18 @@ def main():
             torch.distributed.destroy_process_group()
         return
 
+    # repetitions of the device-resident step (context beside the headline's
+    # single timed region): 5 runs of 200 steps, best and median
+    reps = []
+    for _ in range(5):
+        e0.record(stream)
+        for _ in range(200):
+            q4.q4_decode_step(table, x, logits, stream)
+        e1.record(stream)
+        torch.cuda.synchronize(device)
+        reps.append(e0.elapsed_time(e1) / 200)
+    reps_status = q4.q4_device_status(stream)
+
     peak, peak_kind = peaks()
     launches_per_step = 4 * shape.n_layers + 1
     achieved = algo_bytes / (ms_per_step / 1000.0) / 1e9
@@ -846,6 +858,9 @@ def main():
                          "shape": f"M={M} N={shape.vocab} K={shape.hidden}, 4 rotating copies"},
         "e2e": {"value": e2e_value, "unit": "tok/s", "h2d_bytes_per_step": M * shape.hidden * 2,
                 "d2h_bytes_per_step": M * shape.vocab * 4},
+        "decode_step_reps": {"runs": 5, "steps_per_run": 200, "ms_best": min(reps),
+                             "ms_median": statistics.median(reps), "tok_per_s_best": M * 1000.0 / min(reps),
+                             "device_status": reps_status},
         "gpu_launches": launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
