@@ -454,7 +454,8 @@ def rope(x, pos: int, head_dim: int, theta: float = DEFAULT_ROPE_THETA):
     return out.reshape(x.shape)
 
 
-def attention(q, k_cache, v_cache, n: int, head_dim: int, pos: int, theta: float = DEFAULT_ROPE_THETA):
+def attention(q, k_cache, v_cache, n: int, head_dim: int, pos: int, theta: float = DEFAULT_ROPE_THETA,
+              mutant: int = 0):
     """Decode attention of one token: q [Hq*d] (fp16 values, not yet rotated)
     against positions 0..n-1 of the caches [Hkv, max_seq, d] (keys stored
     rotated).  Query head h reads key/value head h // (Hq / Hkv).  Returns
@@ -462,6 +463,9 @@ def attention(q, k_cache, v_cache, n: int, head_dim: int, pos: int, theta: float
 
     Follows BaseRT §3.3 (attention among the decode kernels) and §3.2 (a preallocated
     KV cache); softmax(q.K^T / sqrt(d)).V is the plain definition.
+
+    ``mutant`` plants a known mistake for the pin tests only (1: scores
+    scaled by 1/d; 2: scores not scaled); 0 is the oracle.
     """
     d = head_dim
     qr = rope(q, pos, d, theta).reshape(-1, d)
@@ -469,10 +473,11 @@ def attention(q, k_cache, v_cache, n: int, head_dim: int, pos: int, theta: float
     g = Hq // Hkv
     a = np.empty((Hq, d))
     A = np.empty((Hq, d))
+    scale = {0: np.sqrt(d), 1: float(d), 2: 1.0}[mutant]
     for h in range(Hq):
         K = k_cache[h // g, :n].astype(np.float64)
         V = v_cache[h // g, :n].astype(np.float64)
-        s = K @ qr[h] / np.sqrt(d)
+        s = K @ qr[h] / scale
         w = np.exp(s - s.max())
         w /= w.sum()
         a[h] = w @ V

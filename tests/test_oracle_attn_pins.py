@@ -1,10 +1,13 @@
 """Pins for the oracle's rotary embedding and decode attention: a hand-worked
 rotation, identities of rotations (position 0, norms, composition), and
 special cases of attention with closed forms (one position, equal keys, a
-dominant key, the grouped-query head mapping)."""
+dominant key, the grouped-query head mapping, two keys whose scaled scores
+ln 3 and 0 weigh the values exactly 3/4 and 1/4 -- which fixes the 1/sqrt(d)
+score scale, with two planted scale mistakes that must fail it)."""
 import math
 
 import numpy as np
+import pytest
 
 import oracle
 
@@ -151,3 +154,35 @@ def test_prefill_with_attention_equals_token_by_token_decode():
     h1, _, _ = oracle.prefill_attn(layers, lm, x[:2], caches_c, pos0, d)
     h2, y2, _ = oracle.prefill_attn(layers, lm, x[2:], caches_c, pos0 + 2, d)
     assert np.array_equal(np.concatenate([h1, h2]), h_a) and np.array_equal(y2, y_a)
+
+
+def _two_key_weights(d, mutant=0):
+    """Two cached keys for one query head at position 0 (no rotation): the
+    query is ln(3) on dimension 0, key 1 is sqrt(d) on dimension 0 and key 2
+    is zero, so the scaled scores are ln 3 and 0 and the softmax weights are
+    exactly 3/4 and 1/4.  Returns the output and the two values."""
+    g = np.random.default_rng(5)
+    kc = np.zeros((1, 4, d), np.float16)
+    vc = np.zeros((1, 4, d), np.float16)
+    kc[0, 0, 0] = math.sqrt(d)              # exact in fp16 for d = 16, 64, 256
+    vc[0, :2] = g.standard_normal((2, d)).astype(np.float16)
+    q = np.zeros(d)
+    q[0] = math.log(3.0)
+    a, _ = oracle.attention(q, kc, vc, 2, d, pos=0, mutant=mutant)
+    return a, vc[0, 0].astype(np.float64), vc[0, 1].astype(np.float64)
+
+
+def test_attention_score_scale_closed_form():
+    """softmax(q.K^T / sqrt(d)): scores ln 3 and 0 weigh the values 3/4 and
+    1/4, at three head sizes (so a fixed constant in place of sqrt(d) fails
+    at least two of them)."""
+    for d in (16, 64, 256):
+        a, v1, v2 = _two_key_weights(d)
+        assert np.allclose(a, 0.75 * v1 + 0.25 * v2, rtol=0, atol=1e-14), d
+
+
+@pytest.mark.parametrize("mutant", [1, 2])
+def test_attention_planted_scale_mistakes_are_caught(mutant):
+    """Scores scaled by 1/d, or not scaled, fail the closed form."""
+    a, v1, v2 = _two_key_weights(64, mutant=mutant)
+    assert not np.allclose(a, 0.75 * v1 + 0.25 * v2, rtol=0, atol=1e-6)
