@@ -22,6 +22,9 @@ namespace q4m {
 constexpr int kMaxTopk = 8;
 constexpr int kMaxExperts = 256;
 constexpr int kBlockTokens = 32;  // tokens per counting block (one warp)
+// Largest token count either routing entry point accepts: keeps every index
+// the kernels form (token, block * experts, rows = tokens * topk) inside int.
+constexpr int kMaxRouteTokens = 1 << 24;
 
 // Order-preserving 16-bit key of an fp16 value (-0 folded onto +0).
 __device__ __forceinline__ uint32_t half_key(uint16_t h) {
@@ -32,8 +35,10 @@ __device__ __forceinline__ uint32_t half_key(uint16_t h) {
 // One warp per token: top-k by repeated warp arg-max over (key, -expert).
 __global__ void route_topk_kernel(const uint16_t* __restrict__ logits, int T, int E, int topk,
                                   int32_t* __restrict__ ids, float* __restrict__ wts) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= T) return;
+    const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (gw >= T) return;
+    const int warp = (int)gw;
     const uint16_t* row = logits + (size_t)warp * E;
     constexpr int kPer = kMaxExperts / 32;
     uint32_t key[kPer];
@@ -270,7 +275,7 @@ q4_status q4_moe_route(const uint16_t* logits, int T, int E, int topk, int32_t* 
     if (T < 1 || E < 1 || E > q4m::kMaxExperts || topk < 1 || topk > q4m::kMaxTopk || topk > E)
         return fail(Q4_ERR_INVALID_ARG, "T=%d E=%d topk=%d (need T>=1, 1<=E<=%d, 1<=topk<=min(E,%d))", T, E,
                     topk, q4m::kMaxExperts, q4m::kMaxTopk);
-    if ((long long)T * topk > (1ll << 30)) return fail(Q4_ERR_UNSUPPORTED, "T*topk too large");
+    if (T > q4m::kMaxRouteTokens) return fail(Q4_ERR_UNSUPPORTED, "T=%d above %d", T, q4m::kMaxRouteTokens);
     const size_t need = moe_route_workspace_bytes(T, E, topk);
     if (workspace_bytes < need) return fail(Q4_ERR_INVALID_ARG, "workspace %zu bytes, need %zu", workspace_bytes, need);
     const DeviceInfo* dev = nullptr;
@@ -365,8 +370,9 @@ static __device__ __align__(256) int32_t g_route_scratch[kStaticRouteCounters];
 }  // namespace q4m
 
 namespace {
+constexpr int kScratchDevices = 64;  // current_device() refuses ordinals from 64 up
 std::mutex g_route_scratch_mutex;
-int32_t* g_route_scratch_ptr[64];  // device address of the array, per device ordinal
+int32_t* g_route_scratch_ptr[kScratchDevices];  // device address of the array, per device ordinal
 }  // namespace
 
 extern "C" q4_status q4_moe_route_noalloc(const uint16_t* logits, int T, int E, int topk, int32_t* topk_ids,
@@ -378,7 +384,8 @@ extern "C" q4_status q4_moe_route_noalloc(const uint16_t* logits, int T, int E, 
     if (T < 1 || E < 1 || E > q4m::kMaxExperts || topk < 1 || topk > q4m::kMaxTopk || topk > E)
         return fail(Q4_ERR_INVALID_ARG, "T=%d E=%d topk=%d (need T>=1, 1<=E<=%d, 1<=topk<=min(E,%d))", T, E,
                     topk, q4m::kMaxExperts, q4m::kMaxTopk);
-    const long long B = (T + q4m::kBlockTokens - 1) / q4m::kBlockTokens;
+    if (T > q4m::kMaxRouteTokens) return fail(Q4_ERR_UNSUPPORTED, "T=%d above %d", T, q4m::kMaxRouteTokens);
+    const long long B = ((long long)T + q4m::kBlockTokens - 1) / q4m::kBlockTokens;
     if (B * E > q4m::kStaticRouteCounters)
         return fail(Q4_ERR_UNSUPPORTED,
                     "T=%d, E=%d need %lld counters; the static scratch holds %d (at most %lld tokens for E=%d); "
@@ -388,6 +395,8 @@ extern "C" q4_status q4_moe_route_noalloc(const uint16_t* logits, int T, int E, 
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
+    if (dev->device < 0 || dev->device >= kScratchDevices)
+        return fail(Q4_ERR_NO_DEVICE, "device ordinal %d outside 0..%d", dev->device, kScratchDevices - 1);
     int32_t* scratch = nullptr;
     {
         // Set-up, once per device, with that device current: the host-side

@@ -330,7 +330,8 @@ size_t q4_moe_route_workspace_bytes(int T, int E, int topk);
  * (rows of expert e are offsets[e] .. offsets[e+1]-1), token_of / expert_of
  * int32 [T*topk] (source token and expert of each sorted row), pos int32
  * [T][topk] (sorted row of each (token, rank)).  1 <= topk <= min(E, 8),
- * E <= 256.  Integer outputs are bit-exact. */
+ * E <= 256; T above 2^24 returns Q4_ERR_UNSUPPORTED before anything is
+ * enqueued.  Integer outputs are bit-exact. */
 q4_status q4_moe_route(const uint16_t *logits, int T, int E, int topk, int32_t *topk_ids,
                        float *topk_weights, int32_t *offsets, int32_t *token_of,
                        int32_t *expert_of, int32_t *pos, void *workspace,
@@ -346,8 +347,8 @@ q4_status q4_moe_route(const uint16_t *logits, int T, int E, int topk, int32_t *
  * Its scratch (the per-(expert, 32-token block) counters) is a static
  * 256 KB array in the library, present on every device that loads the library
  * until the process exits: ceil(T/32) * E must not exceed 65536 (e.g. at most
- * 16384 tokens for 128 experts); larger requests fail with Q4_ERR_UNSUPPORTED
- * before anything is enqueued.  The first call on a device looks up the
+ * 16384 tokens for 128 experts); larger requests (and T above 2^24) fail
+ * with Q4_ERR_UNSUPPORTED before anything is enqueued.  The first call on a device looks up the
  * array's device address with that device current (a host-side set-up step;
  * make that first call before any stream capture).  Every call shares the
  * one array and the kernels write every counter they read, so nothing needs

@@ -203,6 +203,9 @@ def test_moe_validation(L):
     assert L.q4_moe_route(FAKE, 16, 128, 9, *args[:6], FAKE, 1 << 20, None) == -1   # topk > 8
     assert L.q4_moe_route(FAKE, 16, 300, 8, *args[:6], FAKE, 1 << 20, None) == -1   # E > 256
     assert L.q4_moe_route(FAKE, 16, 128, 8, *args[:6], FAKE, 0, None) == -1         # workspace too small
+    # token counts whose indices would leave int: refused before anything is enqueued
+    assert L.q4_moe_route(FAKE, (1 << 24) + 1, 128, 4, *args[:6], FAKE, 1 << 40, None) == -2
+    assert L.q4_moe_route(FAKE, 2**31 - 1, 128, 1, *args[:6], FAKE, 1 << 40, None) == -2
     assert L.q4_moe_gather(FAKE, 4, 12, FAKE, 8, FAKE, None) == -1
     assert L.q4_moe_gather(FAKE + 8, 4, 64, FAKE, 8, FAKE, None) == -3
     assert L.q4_moe_combine(FAKE, 0, 64, FAKE, FAKE, 4, 9, FAKE, 0, None) == -1

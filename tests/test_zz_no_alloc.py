@@ -50,9 +50,10 @@ def route_both(T, E, k, seed):
 
 @pytest.mark.gpu
 def test_noalloc_route_matches_workspace_route_twice():
-    # two calls in a row; the second uses more blocks than the first, so it
-    # cannot pass on counters left over from the first
-    for T, seed in ((512, 501), (2048, 502)):
+    # calls in a row; the second uses more blocks than the first, so it
+    # cannot pass on counters left over from the first; then the exact fit
+    # (ceil(T/32) * E = 65536 counters) and a ragged last block (T % 32 != 0)
+    for T, seed in ((512, 501), (2048, 502), (16384, 503), (1000, 504)):
         ref, got = route_both(T, 128, 8, seed)
         for n in ("ids", "off", "tok", "eid", "pos"):
             assert np.array_equal(ref[n], got[n]), (T, n)
@@ -68,3 +69,6 @@ def test_noalloc_rejects_requests_beyond_the_static_scratch():
     assert b"static scratch" in L.q4_last_error()
     st = L.q4_moe_route_noalloc(fake, 16, 128, 9, *([fake] * 6), None)
     assert st == -1
+    # the block count is formed without int overflow: the largest int is refused
+    st = L.q4_moe_route_noalloc(fake, 2**31 - 1, 128, 8, *([fake] * 6), None)
+    assert st == -2
