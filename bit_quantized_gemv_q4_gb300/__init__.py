@@ -15,11 +15,11 @@ import os
 __all__ = [
     "Q4Error", "lib", "q4_selftest_expired_wait", "q4_gemv", "q4_gemv8", "q4_gemv_ex", "Segment", "q4_device_status",
     "LayerTable", "q4_decode_step", "q4_decode_workspace_bytes", "q4_decode_buffers",
-    "q4_layer_table_release", "q4_moe_route", "q4_moe_route_workspace_bytes",
+    "q4_layer_table_release", "q4_decode_path", "q4_moe_route", "q4_moe_route_workspace_bytes",
     "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine",
     "Q4_F32", "Q4_F16", "Q4_GEMV_PLAIN", "Q4_GEMV_GLU", "Q4_DECODE_NO_GRAPH", "Q4_DECODE_NO_PDL",
     "Q4_DECODE_TAGGED",
-    "Q4_DECODE_PERSISTENT",
+    "Q4_DECODE_PERSISTENT", "Q4_DECODE_CLUSTERED",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -29,6 +29,7 @@ Q4_F32, Q4_F16 = 0, 1
 Q4_GEMV_PLAIN, Q4_GEMV_GLU = 0, 1
 Q4_DECODE_NO_GRAPH, Q4_DECODE_NO_PDL, Q4_DECODE_TAGGED, Q4_DECODE_PERSISTENT = 1, 2, 4, 8
 Q4_DECODE_ATTENTION = 16
+Q4_DECODE_CLUSTERED = 32
 Q4_MAX_SEGMENTS = 4
 
 STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q4_ERR_MISALIGNED",
@@ -38,7 +39,8 @@ STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q
 EXPORTS = ["q4_last_error", "q4_status_string", "q4_version", "q4_device_status",
            "q4_selftest_expired_wait", "q4_gemv", "q4_gemv8", "q4_gemv_bits",
            "q4_gemv_ex", "q4_decode_workspace_bytes", "q4_decode_buffers", "q4_decode_step",
-           "q4_layer_table_release", "q4_moe_route_workspace_bytes", "q4_moe_route", "q4_moe_route_noalloc",
+           "q4_layer_table_release", "q4_decode_path", "q4_moe_route_workspace_bytes", "q4_moe_route",
+           "q4_moe_route_noalloc",
            "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine", "q4_gemm", "q4_prefill_workspace_bytes",
            "q4_prefill", "q4_attention_workspace_bytes", "q4_attention", "q4_gemm_workspace_bytes",
            "q4_prefill_buffers"]
@@ -142,6 +144,8 @@ def lib() -> ctypes.CDLL:
         L.q4_decode_step.argtypes = [ctypes.POINTER(q4_layer_table), vp, vp, vp]
         L.q4_layer_table_release.restype = st
         L.q4_layer_table_release.argtypes = [ctypes.POINTER(q4_layer_table)]
+        L.q4_decode_path.restype = ctypes.c_int
+        L.q4_decode_path.argtypes = [ctypes.POINTER(q4_layer_table)]
         L.q4_moe_route_workspace_bytes.restype = ctypes.c_size_t
         L.q4_moe_route_workspace_bytes.argtypes = [i32, i32, i32]
         L.q4_moe_route.restype = st
@@ -317,6 +321,11 @@ def q4_decode_buffers(table: LayerTable) -> dict:
 
 def q4_decode_step(table: LayerTable, x, logits, stream=None):
     _check(lib().q4_decode_step(ctypes.byref(table.t), _ptr(x), _ptr(logits), _stream(stream)), "q4_decode_step")
+
+
+def q4_decode_path(table: LayerTable) -> int:
+    """0 = not planned, 1 = per-stage launches, 2 = persistent launch, 3 = clustered step + lm_head."""
+    return lib().q4_decode_path(ctypes.byref(table.t))
 
 
 def q4_layer_table_release(table: LayerTable):

@@ -29,6 +29,7 @@ namespace {
 struct Dims {
     int hidden = 0, qN = 0, kvN = 0, ffn = 0, vocab = 0, M = 0, L = 0;
     bool attn = false;  // Q4_DECODE_ATTENTION
+    bool step = false;  // the clustered step may run the layers (the workspace holds its regions)
     int hd = 0, max_seq = 0;
 };
 
@@ -36,6 +37,9 @@ struct Layout {
     size_t h = 0, h_mid = 0, q = 0, k = 0, v = 0, act = 0;
     size_t a = 0, attn_ws = 0, attn_ws_bytes = 0;  // attention output and its scratch (Q4_DECODE_ATTENTION)
     size_t params = 0;  // per-stage kernel parameters of the persistent launch
+    // clustered step (M = 1 without attention): layer descriptors, tensor
+    // maps, the partial-sum exchange and its counters
+    size_t step_layers = 0, step_maps = 0, xch = 0, step_ctr = 0, step_end = 0;
     // tagged copies of the activations that later stages read, and counters
     size_t h_t = 0, hm_t = 0, q_t = 0, act_t = 0, ctr = 0, tagged_begin = 0, total = 0;
 };
@@ -64,6 +68,10 @@ struct Plan {
     PersistentGeom geom;
     std::vector<uint8_t> params_host;  // kept alive for the asynchronous upload
     bool tagged_ready = false;       // tagged region zeroed
+    bool fused = false;              // the clustered step runs the layers (then lm_head)
+    StepPlan step;
+    std::vector<uint8_t> step_layers_host, step_maps_host;  // kept alive for the upload
+    bool step_ready = false;         // exchange region and counters zeroed
     cudaStream_t capture_stream = nullptr;
     cudaGraph_t graph = nullptr;
     cudaGraphExec_t exec = nullptr;
@@ -142,6 +150,8 @@ q4_status table_dims(const q4_layer_table* t, Dims* d) {
         d->hd = t->head_dim;
         d->max_seq = t->max_seq;
     }
+    d->step = t->M == 1 && !d->attn && t->n_layers > 0 && (t->flags & Q4_DECODE_CLUSTERED) &&
+              !(t->flags & (Q4_DECODE_TAGGED | Q4_DECODE_PERSISTENT));
     if (t->final_norm && !aligned16(t->final_norm)) return fail(Q4_ERR_MISALIGNED, "final_norm must be 16-byte aligned");
     if (!(t->norm_eps >= 0.f)) return fail(Q4_ERR_INVALID_ARG, "norm_eps must be >= 0");
     d->vocab = t->lm_head.N;
@@ -168,6 +178,13 @@ Layout layout_of(const Dims& d) {
         l.attn_ws = take(l.attn_ws_bytes / 2 + 1);
     }
     l.params = take((size_t)(4 * d.L + 1) * gemv_params_bytes() / 2);
+    if (d.step) {
+        l.step_layers = take((size_t)d.L * step_layer_desc_bytes() / 2 + 1);
+        l.step_maps = take((size_t)6 * d.L * sizeof(CUtensorMap) / 2);
+        l.xch = take((size_t)2 * d.L * kStepMaxClusters * d.hidden * 4);
+        l.step_ctr = take(64);
+        l.step_end = off;
+    }
     l.tagged_begin = off;
     l.h_t = take((size_t)d.M * d.hidden * 2);
     l.hm_t = take((size_t)d.M * d.hidden * 2);
@@ -305,6 +322,11 @@ void build_stages(Plan& p, const uint16_t* x, void* logits) {
 
 q4_status enqueue_stages(Plan& p, cudaStream_t s) {
     const bool pdl = !(p.flags & Q4_DECODE_NO_PDL);
+    if (p.fused) {
+        q4_status st = step_launch(p.step, s);
+        if (st != Q4_OK) return st;
+        return launch_gemv(p.stages.back(), s, pdl, true);
+    }
     for (size_t i = 0; i < p.stages.size(); ++i) {
         q4_status st = launch_gemv(p.stages[i], s, pdl && i > 0, true, p.tagged_mode ? &p.tagged[i] : nullptr);
         if (st != Q4_OK) return st;
@@ -314,6 +336,51 @@ q4_status enqueue_stages(Plan& p, cudaStream_t s) {
         }
     }
     if (p.dims.attn) return pos_advance(p.pos, s);
+    return Q4_OK;
+}
+
+// Plans the clustered step when every layer has the same shape and the
+// device takes the clusters; uploads its tables into the workspace on `s`.
+q4_status plan_fused(Plan& p, const uint16_t* x, cudaStream_t s) {
+    const Dims& d = p.dims;
+    const q4_layer_weights& w0 = p.layers[0];
+    for (const q4_layer_weights& w : p.layers)
+        if (w.q.N != w0.q.N || w.k.N != w0.k.N || w.v.N != w0.k.N || w.gate.N != w0.gate.N) return Q4_OK;
+    uint8_t* ws = static_cast<uint8_t*>(p.workspace);
+    StepArgs a;
+    a.L = d.L;
+    a.H = d.hidden;
+    a.QN = w0.q.N;
+    a.KVN = w0.k.N;
+    a.F = w0.gate.N;
+    a.eps = p.eps;
+    a.layers = p.layers.data();
+    a.dev_layers = ws + p.lay.step_layers;
+    a.dev_maps = ws + p.lay.step_maps;
+    a.x = x;
+    a.h = reinterpret_cast<uint16_t*>(ws + p.lay.h);
+    a.h_mid = reinterpret_cast<uint16_t*>(ws + p.lay.h_mid);
+    a.q = reinterpret_cast<uint16_t*>(ws + p.lay.q);
+    a.k = reinterpret_cast<uint16_t*>(ws + p.lay.k);
+    a.v = reinterpret_cast<uint16_t*>(ws + p.lay.v);
+    a.act = reinterpret_cast<uint16_t*>(ws + p.lay.act);
+    a.xch = reinterpret_cast<unsigned long long*>(ws + p.lay.xch);
+    a.ctr = reinterpret_cast<uint32_t*>(ws + p.lay.step_ctr);
+    bool ok = false;
+    q4_status st = step_plan(a, &p.step, &ok);
+    if (st != Q4_OK || !ok) return st;
+    p.step_layers_host.assign((size_t)d.L * step_layer_desc_bytes(), 0);
+    p.step_maps_host.assign((size_t)6 * d.L * sizeof(CUtensorMap) + 64, 0);
+    // a 64-byte aligned host copy of the maps
+    uint8_t* mh = p.step_maps_host.data();
+    mh += (64 - (reinterpret_cast<uintptr_t>(mh) & 63)) & 63;
+    if ((st = step_bind(&p.step, a, p.step_layers_host.data(), mh)) != Q4_OK) return st;
+    cudaError_t e = cudaMemcpyAsync(ws + p.lay.step_layers, p.step_layers_host.data(), p.step_layers_host.size(),
+                                    cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(ws + p.lay.step_maps, mh, (size_t)6 * d.L * sizeof(CUtensorMap), cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(e, "uploading the clustered step's tables");
+    p.fused = true;
     return Q4_OK;
 }
 
@@ -644,6 +711,11 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
         p->logits_key = logits;
         drop_graph(*p);
         p->persistent = false;
+        p->fused = false;
+        if (p->dims.step) {
+            q4_status st = plan_fused(*p, x, s);
+            if (st != Q4_OK) return st;
+        }
         if (p->flags & Q4_DECODE_PERSISTENT) {
             const int n = (int)p->stages.size();
             p->params_host.assign((size_t)n * gemv_params_bytes(), 0);
@@ -666,6 +738,14 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
         if (e != cudaSuccess) return cuda_fail(e, "clearing the tagged activations");
         p->tagged_ready = true;
     }
+    if (p->fused && !p->step_ready) {
+        // Once, on the caller's stream and outside any capture: exchange tags
+        // start at 1, so zeroed words never look current; the step counter starts at 0.
+        cudaError_t e = cudaMemsetAsync(static_cast<uint8_t*>(p->workspace) + p->lay.xch, 0,
+                                        p->lay.step_end - p->lay.xch, s);
+        if (e != cudaSuccess) return cuda_fail(e, "clearing the exchange region");
+        p->step_ready = true;
+    }
     if (p->persistent)
         return persistent_launch(p->geom, static_cast<uint8_t*>(p->workspace) + p->lay.params, s);
     if (p->flags & Q4_DECODE_NO_GRAPH) return enqueue_stages(*p, s);
@@ -676,6 +756,16 @@ q4_status q4_decode_step(q4_layer_table* table, const uint16_t* x, void* logits,
     cudaError_t e = cudaGraphLaunch(p->exec, s);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
     return Q4_OK;
+}
+
+int q4_decode_path(const q4_layer_table* table) {
+    clear_error();
+    if (!table || !table->plan) return 0;
+    const Plan* p = static_cast<const Plan*>(table->plan);
+    if (p->stages.empty()) return 0;
+    if (p->fused) return 3;
+    if (p->persistent) return 2;
+    return 1;
 }
 
 q4_status q4_layer_table_release(q4_layer_table* table) {

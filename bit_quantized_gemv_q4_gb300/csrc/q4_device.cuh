@@ -175,4 +175,32 @@ __device__ __forceinline__ float2 fma_h2_s_f32(uint32_t v, uint16_t s, float c) 
     return make_float2(lo, hi);
 }
 
+// Dequantise one word of 8 codes and accumulate against x pairs: the codes
+// OR-ed into the mantissa of 1024.0 (nibbles 0, 2, 4, 6 as 1024+q) or 64.0
+// (nibbles 1, 3, 5, 7 as 64+q), w = s*(1024+q) + (b - 1024 s) (or the 64
+// form) by one fp16 x fp16 -> fp32 FMA each (the product is exact), and w*x
+// accumulated in fp32 two at a time.  xa holds (x0, x4, x1, x5) and xb
+// (x2, x6, x3, x7) of each of the M vectors; acc[m] gets the pairs' sums.
+template <int M>
+__device__ __forceinline__ void word_mac(uint32_t q, uint16_t sh, float c1024, float c64, const float4* xa,
+                                         const float4* xb, float2* acc) {
+    const uint32_t q8 = q >> 8;
+    const uint32_t v0 = and_or(q, 0x000F000Fu, 0x64006400u);   // 1024+q0, 1024+q4
+    const uint32_t v1 = and_or(q, 0x00F000F0u, 0x54005400u);   // 64+q1,   64+q5
+    const uint32_t v2 = and_or(q8, 0x000F000Fu, 0x64006400u);  // 1024+q2, 1024+q6
+    const uint32_t v3 = and_or(q8, 0x00F000F0u, 0x54005400u);  // 64+q3,   64+q7
+    const float2 d0 = fma_h2_s_f32(v0, sh, c1024);             // w0, w4
+    const float2 d1 = fma_h2_s_f32(v1, sh, c64);               // w1, w5
+    const float2 d2 = fma_h2_s_f32(v2, sh, c1024);             // w2, w6
+    const float2 d3 = fma_h2_s_f32(v3, sh, c64);               // w3, w7
+#pragma unroll
+    for (int m = 0; m < M; ++m) {
+        acc[m] = __ffma2_rn(d0, make_float2(xa[m].x, xa[m].y), acc[m]);
+        acc[m] = __ffma2_rn(d1, make_float2(xa[m].z, xa[m].w), acc[m]);
+        acc[m] = __ffma2_rn(d2, make_float2(xb[m].x, xb[m].y), acc[m]);
+        acc[m] = __ffma2_rn(d3, make_float2(xb[m].z, xb[m].w), acc[m]);
+    }
+}
+
+
 }  // namespace q4d

@@ -194,28 +194,6 @@ __device__ __forceinline__ uint32_t bulk_bytes(const Params& p, int nrows) {
 }
 
 // ------------------------------------------------------------------ consumer
-// Dequantise one word of 8 codes and accumulate against the lane's x pairs.
-template <int M>
-__device__ __forceinline__ void word_mac(uint32_t q, uint16_t sh, float c1024, float c64, const float4* xa,
-                                         const float4* xb, float2* acc) {
-    const uint32_t q8 = q >> 8;
-    const uint32_t v0 = q4d::and_or(q, 0x000F000Fu, 0x64006400u);   // 1024+q0, 1024+q4
-    const uint32_t v1 = q4d::and_or(q, 0x00F000F0u, 0x54005400u);   // 64+q1,   64+q5
-    const uint32_t v2 = q4d::and_or(q8, 0x000F000Fu, 0x64006400u);  // 1024+q2, 1024+q6
-    const uint32_t v3 = q4d::and_or(q8, 0x00F000F0u, 0x54005400u);  // 64+q3,   64+q7
-    const float2 d0 = q4d::fma_h2_s_f32(v0, sh, c1024);             // w0, w4
-    const float2 d1 = q4d::fma_h2_s_f32(v1, sh, c64);               // w1, w5
-    const float2 d2 = q4d::fma_h2_s_f32(v2, sh, c1024);             // w2, w6
-    const float2 d3 = q4d::fma_h2_s_f32(v3, sh, c64);               // w3, w7
-#pragma unroll
-    for (int m = 0; m < M; ++m) {
-        acc[m] = __ffma2_rn(d0, make_float2(xa[m].x, xa[m].y), acc[m]);
-        acc[m] = __ffma2_rn(d1, make_float2(xa[m].z, xa[m].w), acc[m]);
-        acc[m] = __ffma2_rn(d2, make_float2(xb[m].x, xb[m].y), acc[m]);
-        acc[m] = __ffma2_rn(d3, make_float2(xb[m].z, xb[m].w), acc[m]);
-    }
-}
-
 // The same for 8-bit codes: two words a, b hold the 8 codes of one octet
 // (codes 0-3 in a, 4-7 in b, lowest byte first).  Masking every other byte
 // and OR-ing it into the mantissa of 1024.0 gives 1024+q exactly (q <= 255);
@@ -376,7 +354,7 @@ __device__ __forceinline__ void dot_rows(const Params& p, const uint32_t* wq, co
 #pragma unroll
                     for (int wi = 0; wi < LW; ++wi) {
                         if constexpr (BITS == 4)
-                            word_mac<M>(w[wi], sh, c1024, c64, &xr[(wi * 2 + 0) * M], &xr[(wi * 2 + 1) * M], acc[r]);
+                            q4d::word_mac<M>(w[wi], sh, c1024, c64, &xr[(wi * 2 + 0) * M], &xr[(wi * 2 + 1) * M], acc[r]);
                         else
                             word_mac8<M>(w[2 * wi], w[2 * wi + 1], sh, c1024, &xr[(wi * 2 + 0) * M],
                                          &xr[(wi * 2 + 1) * M], acc[r]);

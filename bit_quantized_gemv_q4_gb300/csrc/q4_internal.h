@@ -1,6 +1,7 @@
 // Host-side internals shared by the library's translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include <atomic>
@@ -48,6 +49,11 @@ inline cudaError_t ensure_smem_attr(const void* kern, std::atomic<int>* marks, i
     }
     return cudaSuccess;
 }
+
+// 2-D tensor map (q4_moe_gemm.cu): `inner` x `outer` elements of type dt,
+// rows `row_bytes` apart, copied in boxes of box_inner x box_outer.
+q4_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uint64_t inner, uint64_t outer,
+                   uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle sw);
 
 // ---- decode attention (q4_attn.cu) -----------------------------------------
 size_t attn_workspace_bytes(int n_q_heads, int head_dim, int max_seq);
@@ -117,6 +123,37 @@ struct PersistentGeom {
 q4_status persistent_plan(const q4_gemv_desc* d, const GemvTagged* tg, int n, void* host_params,
                           PersistentGeom* g, bool* fits);
 q4_status persistent_launch(const PersistentGeom& g, const void* dev_params, cudaStream_t stream);
+
+// ---- clustered decode step (q4_step.cu) ------------------------------------
+// The layer stack of an M = 1 decode step as one launch of thread-block
+// clusters (two grid-wide hand-offs per layer); lm_head is launched after it.
+constexpr int kStepMaxClusters = 20;  // the exchange buffer holds this many clusters' partials
+
+struct StepArgs {
+    int L = 0, H = 0, QN = 0, KVN = 0, F = 0;
+    float eps = 1e-6f;
+    const q4_layer_weights* layers = nullptr;  // host [L]
+    const void* dev_layers = nullptr;          // workspace: L * step_layer_desc_bytes()
+    const void* dev_maps = nullptr;            // workspace: 6 L tensor maps (64-byte aligned)
+    const uint16_t* x = nullptr;
+    uint16_t *h = nullptr, *h_mid = nullptr, *q = nullptr, *k = nullptr, *v = nullptr, *act = nullptr;
+    unsigned long long* xch = nullptr;         // workspace: 2 L * kStepMaxClusters * H words
+    uint32_t* ctr = nullptr;                   // workspace: step and finished-CTA counters
+};
+
+struct StepPlan {
+    int S = 0, C = 0;  // cluster size and cluster count
+    size_t smem = 0;
+    alignas(64) unsigned char params[512];
+};
+
+size_t step_layer_desc_bytes();
+// *ok is false (and Q4_OK returned) when the shapes or the device do not allow the step.
+q4_status step_plan(const StepArgs& a, StepPlan* out, bool* ok);
+// Host copies of the layer descriptors (L entries) and tensor maps (6 L),
+// which the caller uploads to dev_layers / dev_maps, and the launch pointers.
+q4_status step_bind(StepPlan* sp, const StepArgs& a, void* host_layers, void* host_maps);
+q4_status step_launch(const StepPlan& sp, cudaStream_t stream);
 
 // ---- MoE (q4_moe.cu, q4_moe_gemm.cu) ---------------------------------------
 size_t moe_route_workspace_bytes(int T, int E, int topk);

@@ -576,7 +576,6 @@ __global__ void check_routing_kernel(const int32_t* __restrict__ expert_ids, con
 }  // namespace q4g
 
 namespace q4i {
-namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -609,6 +608,8 @@ q4_status make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, uin
     if (r != CUDA_SUCCESS) return fail(Q4_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
     return Q4_OK;
 }
+
+namespace {
 
 
 // One launch of the grouped GEMM.  Routed (offsets != NULL): E experts, rows

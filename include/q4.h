@@ -240,6 +240,25 @@ q4_status q4_gemv_bits(const uint32_t *Wq, const uint16_t *scales, const uint16_
  * activations; after a step it holds the LAST layer's q, k, v, h', act and the
  * final h (see q4_decode_buffers).  Weights must not change between calls
  * without q4_layer_table_release() (the plan caches their pointers).
+ *
+ * With Q4_DECODE_CLUSTERED (M = 1, no attention, every layer of the same
+ * shape, hidden, q.N and gate.N multiples of 512, and a device that holds at
+ * least two 16- or 8-CTA clusters of one CTA per SM at once; otherwise the
+ * flag is ignored) the layer stack is ONE launch of thread-block clusters and
+ * lm_head a second launch: cluster c owns a block of whole 64-row groups of q
+ * (and of act), its CTAs share those values through distributed shared
+ * memory, and each CTA multiplies its rows of the matching column block of
+ * Wo (Wdown); the clusters' partial sums meet in the workspace as 64-bit
+ * words tagged with the step and the exchange, every cluster adds them in
+ * the same fixed order and rounds h' (h) to fp16 as above -- two grid-wide
+ * hand-offs per layer instead of four kernel boundaries.  The o / down
+ * products are therefore summed in a different order than by the per-stage
+ * launches (same bound against the oracle, different last bits), and the
+ * step's results are the same bits run to run.  The workspace then also
+ * holds the layer table, the o / down tensor maps and the exchange words
+ * (zeroed on the first call, on `stream`; q4_decode_workspace_bytes counts
+ * them when the table asks for the flag), and calls on one table must be
+ * ordered on one stream.
  * ------------------------------------------------------------------------ */
 typedef struct q4_linear {
     const uint32_t *Wq;
@@ -266,6 +285,8 @@ typedef struct q4_layer_weights {
 #define Q4_DECODE_ATTENTION 16 /* decode attention over each layer's KV cache replaces the
                                   a := q stand-in (see below); M must be 1, and
                                   Q4_DECODE_TAGGED / Q4_DECODE_PERSISTENT are refused */
+#define Q4_DECODE_CLUSTERED 32 /* the layer stack as one launch of thread-block clusters
+                                  (see below); M = 1 without attention, else ignored */
 
 typedef struct q4_layer_table {
     int n_layers;
@@ -306,6 +327,12 @@ q4_status q4_decode_buffers(const q4_layer_table *table, q4_decode_buffers_t *ou
 
 q4_status q4_decode_step(q4_layer_table *table, const uint16_t *x, void *logits,
                          q4_stream_t stream);
+
+/* How the planned step runs (no counterpart in the pages; for tests and
+ * tuning): 0 = not planned yet, 1 = per-stage launches, 2 = one persistent
+ * cooperative launch (Q4_DECODE_PERSISTENT), 3 = the clustered step plus
+ * lm_head. */
+int q4_decode_path(const q4_layer_table *table);
 
 /* Frees the plan and its graph; the table can be used again afterwards. */
 q4_status q4_layer_table_release(q4_layer_table *table);

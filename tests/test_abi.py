@@ -236,6 +236,9 @@ def test_decode_attention_table_validation(L):
     n = L.q4_decode_workspace_bytes(ctypes.byref(t.t))
     plain = q4.q4_decode_workspace_bytes(q4.LayerTable([layer], lin(100, 64), hidden=64, M=1))
     assert n > plain                                   # + the attention output and its scratch
+    # the clustered step's tables and exchange region, for tables that ask for it
+    assert q4.q4_decode_workspace_bytes(q4.LayerTable([layer], lin(100, 64), hidden=64, M=1,
+                                                      flags=q4.Q4_DECODE_CLUSTERED)) > plain
     for kw, frag in ((dict(M=2), b"M = 1"), (dict(head_dim=96), b"head"), (dict(pos=None), b"pos"),
                      (dict(flags=q4.Q4_DECODE_ATTENTION | q4.Q4_DECODE_TAGGED), b"TAGGED")):
         args = dict(hidden=64, M=1, flags=q4.Q4_DECODE_ATTENTION, head_dim=64, max_seq=32, pos=FAKE)
