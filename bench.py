@@ -467,7 +467,8 @@ def q8_lm_head(q4, device, M: int = 1):
 def decode_streams(device, steps: int = 200, warmup: int = 10):
     """Decode steps of the larger stacks the parity tests cover: Llama-3.2-3B
     shaped at M = 1 and M = 4, Qwen3-4B shaped at M = 1 (random Q4 weights
-    drawn on the device; 1.8-2.3 GB per step, so no L2 reuse)."""
+    drawn on the device; 1.8-2.3 GB per step, so no L2 reuse); at M = 1 also
+    with the clustered step (Q4_DECODE_CLUSTERED)."""
     import torch
 
     import bit_quantized_gemv_q4_gb300 as q4
@@ -484,30 +485,34 @@ def decode_streams(device, steps: int = 200, warmup: int = 10):
 
         dl = [{nm: mat(N, K) for nm, N, K in shape.layer_linears()} for _ in range(shape.n_layers)]
         dlm = mat(shape.vocab, shape.hidden)
-        table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
-        nws = q4.q4_decode_workspace_bytes(table)
-        ws = torch.empty(nws, dtype=torch.uint8, device=device)
-        table.set_workspace(ws, nws)
-        x = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4246, M, shape.hidden)).to(device)
-        logits = torch.empty(M, shape.vocab, dtype=torch.float32, device=device)
-        stream = torch.cuda.current_stream(device)
-        for _ in range(warmup):
-            q4.q4_decode_step(table, x, logits, stream)
-        torch.cuda.synchronize(device)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        for _ in range(steps):
-            q4.q4_decode_step(table, x, logits, stream)
-        e1.record(stream)
-        torch.cuda.synchronize(device)
-        if q4.q4_device_status(stream) != 0:
-            raise RuntimeError("device status after stream timing")
-        ms = e0.elapsed_time(e1) / steps
-        gbs = shape.weight_bytes_per_step() / (ms * 1e-3) / 1e9  # weight bytes only (activations < 0.1 %)
-        out[f"{shape.name} M={M}"] = {"ms": ms, "tok_per_s": M * 1000.0 / ms, "launches": 4 * shape.n_layers + 1,
-                                      "weight_bytes": shape.weight_bytes_per_step(), "gbs": gbs, "frac": gbs / peak}
-        table.release()
-        del dl, dlm, table, ws
+        for flags in ((0, q4.Q4_DECODE_CLUSTERED) if M == 1 else (0,)):
+            table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M, flags=flags)
+            nws = q4.q4_decode_workspace_bytes(table)
+            ws = torch.empty(nws, dtype=torch.uint8, device=device)
+            table.set_workspace(ws, nws)
+            x = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4246, M, shape.hidden)).to(device)
+            logits = torch.empty(M, shape.vocab, dtype=torch.float32, device=device)
+            stream = torch.cuda.current_stream(device)
+            for _ in range(warmup):
+                q4.q4_decode_step(table, x, logits, stream)
+            torch.cuda.synchronize(device)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            for _ in range(steps):
+                q4.q4_decode_step(table, x, logits, stream)
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            if q4.q4_device_status(stream) != 0:
+                raise RuntimeError("device status after stream timing")
+            ms = e0.elapsed_time(e1) / steps
+            gbs = shape.weight_bytes_per_step() / (ms * 1e-3) / 1e9  # weight bytes only (activations < 0.1 %)
+            key = f"{shape.name} M={M}" + (" clustered" if flags else "")
+            out[key] = {"ms": ms, "tok_per_s": M * 1000.0 / ms, "path": q4.q4_decode_path(table),
+                        "launches": 2 if q4.q4_decode_path(table) == 3 else 4 * shape.n_layers + 1,
+                        "weight_bytes": shape.weight_bytes_per_step(), "gbs": gbs, "frac": gbs / peak}
+            table.release()
+            del table, ws
+        del dl, dlm
         torch.cuda.empty_cache()
     return out
 
@@ -548,6 +553,35 @@ def bits_lm_head(q4, device, widths=(2, 3, 5, 6)):
     return out
 
 
+def decode_clustered(q4, device, dl, dlm, shape, x, steps: int = 1000, warmup: int = 20):
+    """The same decode step with the clustered layer stack
+    (Q4_DECODE_CLUSTERED: one launch of thread-block clusters for the layers,
+    two grid-wide hand-offs per layer, then lm_head), device-resident, one
+    timed region of `steps` steps."""
+    import torch
+    table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=1, flags=q4.Q4_DECODE_CLUSTERED)
+    nws = q4.q4_decode_workspace_bytes(table)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    table.set_workspace(ws, nws)
+    logits = torch.empty(1, shape.vocab, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        q4.q4_decode_step(table, x, logits, stream)
+    torch.cuda.synchronize(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        q4.q4_decode_step(table, x, logits, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    if q4.q4_device_status(stream) != 0:
+        raise RuntimeError("device status after the clustered-step timing")
+    ms = e0.elapsed_time(e1) / steps
+    path = q4.q4_decode_path(table)
+    table.release()
+    return {"ms": ms, "tok_per_s": 1000.0 / ms, "path": path, "launches_per_step": 2 if path == 3 else None}
+
+
 def max_over_ranks(ms: float, world: int, device=None) -> float:
     """The slowest rank's time: replicas run independently, so the job takes
     as long as its slowest replica (all-reduce MAX when world > 1)."""
@@ -566,13 +600,14 @@ def job_rate(world: int, tokens_per_rank_step: int, steps: int, ms_max: float) -
 
 
 def single_gemv(q4, device, isolated: int = 50, replays: int = 5):
-    """The single small GEMV (M = 1, K = 1024, N = 3072, 1.78 MB) two ways:
+    """The single small GEMV (M = 1, K = 1024, N = 3072, 1.78 MB) three ways:
     isolated (one launch between synchronisations, median of 50 over distinct
-    weight copies) and in steady state (a rotating pool of distinct copies
-    totalling more than 3x L2, launched back to back from one CUDA graph so no
-    launch hits L2; best and median of 5 replays).  The public q4_gemv
-    launches without programmatic dependent launch, so the steady state still
-    pays a kernel boundary per launch."""
+    weight copies), and in steady state over a rotating pool of distinct
+    copies totalling more than 3x L2 launched back to back from one CUDA
+    graph (so no launch hits L2; best and median of 5 replays) -- once with
+    programmatic dependent launch (q4_gemv_ex with Q4_GEMV_EARLY_WEIGHTS: each
+    launch streams its weights while the one before it finishes; the
+    protocol's steady state) and once with plain launches (q4_gemv)."""
     import statistics
 
     import torch
@@ -604,31 +639,43 @@ def single_gemv(q4, device, isolated: int = 50, replays: int = 5):
         e1.record(stream)
         torch.cuda.synchronize(device)
         iso.append(e0.elapsed_time(e1))
-    g = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g):
-        for c in copies:
-            q4.q4_gemv(*c, x, y, M, N, K)  # the capture stream is current here
-    torch.cuda.synchronize(device)
-    g.replay()
-    torch.cuda.synchronize(device)
-    per = []
-    for _ in range(replays):
-        e0.record(stream)
-        g.replay()
-        e1.record(stream)
+    def steady(early: bool):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for c in copies:  # the capture stream is current here
+                if early:
+                    q4.q4_gemv_ex([q4.Segment(*c, N, y=y)], x, M, K, flags=q4.Q4_GEMV_EARLY_WEIGHTS)
+                else:
+                    q4.q4_gemv(*c, x, y, M, N, K)
         torch.cuda.synchronize(device)
-        per.append(e0.elapsed_time(e1) / n_copies)
+        g.replay()
+        torch.cuda.synchronize(device)
+        per = []
+        for _ in range(replays):
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            torch.cuda.synchronize(device)
+            per.append(e0.elapsed_time(e1) / n_copies)
+        del g
+        return min(per), statistics.median(per)
+
+    best, med = steady(True)
+    best_plain, med_plain = steady(False)
     if q4.q4_device_status(stream) != 0:
         raise RuntimeError("device status after the single-GEMV timing")
-    del g
     peak, kind = peaks()
-    iso_ms, best, med = statistics.median(iso), min(per), statistics.median(per)
+    iso_ms = statistics.median(iso)
     gbs = lambda ms: nb / (ms / 1000.0) / 1e9  # noqa: E731
     return {"shape": f"M={M} N={N} K={K}", "bytes_per_launch": nb, "peak_kind": kind,
             "isolated_us": iso_ms * 1000.0, "isolated_gbs": gbs(iso_ms),
-            "steady_copies": n_copies, "steady_us_best": best * 1000.0, "steady_us_median": med * 1000.0,
+            "steady_copies": n_copies, "steady": "graph of back-to-back launches with programmatic dependent "
+                                                 "launch (Q4_GEMV_EARLY_WEIGHTS)",
+            "steady_us_best": best * 1000.0, "steady_us_median": med * 1000.0,
             "steady_gbs_best": gbs(best), "steady_frac_of_measured": gbs(best) / peak,
-            "steady_frac_of_nominal": gbs(best) / NOMINAL_HBM_GBS}
+            "steady_frac_of_nominal": gbs(best) / NOMINAL_HBM_GBS,
+            "plain_launches": {"us_best": best_plain * 1000.0, "us_median": med_plain * 1000.0,
+                               "gbs_best": gbs(best_plain), "frac_of_measured": gbs(best_plain) / peak}}
 
 
 def lm_head_ms(q4, dlm, x, M, stream, device):
@@ -780,19 +827,32 @@ def main():
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
 
-    # ---- device-resident timed region
+    # ---- device-resident timed regions: each exactly K steps between a
+    # barrier and a synchronisation on both sides, repeated until the regions
+    # together last at least 100 ms so the clock samples fall inside them;
+    # value = the median region
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    region_ms = []
     with ClockSampler(local) as clk:
-        barrier()
         clk.start()
-        e0.record(stream)
-        for _ in range(args.steps):
-            q4.q4_decode_step(table, x, logits, stream)
-        e1.record(stream)
-        barrier()
+        while True:
+            barrier()
+            e0.record(stream)
+            for _ in range(args.steps):
+                q4.q4_decode_step(table, x, logits, stream)
+            e1.record(stream)
+            barrier()
+            region_ms.append(max_over_ranks(e0.elapsed_time(e1), world, device))
+            done = sum(region_ms) >= 100.0 or len(region_ms) >= 1000
+            if world > 1:  # every rank takes the same number of regions
+                flag = torch.tensor([1.0 if done else 0.0], device=device)
+                torch.distributed.all_reduce(flag, op=torch.distributed.ReduceOp.MIN)
+                done = flag.item() > 0.5
+            if done:
+                break
         clk.stop()
-    ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    ms = statistics.median(region_ms)
     ms_per_step = ms / args.steps
     value = job_rate(world, M, args.steps, ms)
 
@@ -862,6 +922,8 @@ def main():
                              "ms_median": statistics.median(reps), "tok_per_s_best": M * 1000.0 / min(reps),
                              "device_status": reps_status},
         "gpu_launches": launches_per_step * args.steps,
+        "timed_regions": {"count": len(region_ms), "steps_each": args.steps, "ms_median": ms,
+                          "ms_min": min(region_ms), "ms_max": max(region_ms), "ms_total": sum(region_ms)},
         "clocks": clk.summary(),
     }
     if args.section == "all":
@@ -870,6 +932,8 @@ def main():
         out["moe_prefill"] = moe_prefill(device)
         out["dense_prefill"] = dense_prefill(device, dl, dlm, shape)
         out["decode_attention"] = decode_attention(device, dl, dlm, shape)
+        out["decode_clustered"] = decode_clustered(q4, device, dl, dlm, shape, x)
+        out["decode_streams"] = decode_streams(device)
         try:  # context only, measured last; the lines above stand if it fails
             out["single_gemv"] = single_gemv(q4, device)
         except Exception as e:  # noqa: BLE001

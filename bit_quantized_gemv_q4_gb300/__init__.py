@@ -19,7 +19,7 @@ __all__ = [
     "q4_moe_gather", "q4_moe_gemm", "q4_moe_combine",
     "Q4_F32", "Q4_F16", "Q4_GEMV_PLAIN", "Q4_GEMV_GLU", "Q4_DECODE_NO_GRAPH", "Q4_DECODE_NO_PDL",
     "Q4_DECODE_TAGGED",
-    "Q4_DECODE_PERSISTENT", "Q4_DECODE_CLUSTERED",
+    "Q4_DECODE_PERSISTENT", "Q4_DECODE_CLUSTERED", "Q4_GEMV_EARLY_WEIGHTS",
 ]
 
 HERE = os.path.dirname(os.path.abspath(__file__))
@@ -30,6 +30,7 @@ Q4_GEMV_PLAIN, Q4_GEMV_GLU = 0, 1
 Q4_DECODE_NO_GRAPH, Q4_DECODE_NO_PDL, Q4_DECODE_TAGGED, Q4_DECODE_PERSISTENT = 1, 2, 4, 8
 Q4_DECODE_ATTENTION = 16
 Q4_DECODE_CLUSTERED = 32
+Q4_GEMV_EARLY_WEIGHTS = 1
 Q4_MAX_SEGMENTS = 4
 
 STATUS = {0: "Q4_OK", -1: "Q4_ERR_INVALID_ARG", -2: "Q4_ERR_UNSUPPORTED", -3: "Q4_ERR_MISALIGNED",
@@ -65,7 +66,7 @@ class q4_segment(ctypes.Structure):
 class q4_gemv_desc(ctypes.Structure):
     _fields_ = [("M", i32), ("K", i32), ("x", vp), ("ldx", i32), ("n_segments", i32),
                 ("seg", q4_segment * Q4_MAX_SEGMENTS), ("out_dtype", i32), ("mode", i32), ("x_rmsnorm", i32),
-                ("norm_weight", vp), ("norm_eps", ctypes.c_float)]
+                ("norm_weight", vp), ("norm_eps", ctypes.c_float), ("flags", i32)]
 
 
 class q4_linear(ctypes.Structure):
@@ -242,8 +243,9 @@ class Segment:
 
 
 def q4_gemv_ex(segments, x, M: int, K: int, out_dtype=Q4_F32, mode=Q4_GEMV_PLAIN, ldx: int = 0,
-               rmsnorm: bool = False, norm_weight=None, norm_eps: float = 1e-6, stream=None):
+               rmsnorm: bool = False, norm_weight=None, norm_eps: float = 1e-6, stream=None, flags: int = 0):
     d = q4_gemv_desc()
+    d.flags = flags
     d.M, d.K, d.x, d.ldx = M, K, _ptr(x), ldx
     d.x_rmsnorm, d.norm_weight, d.norm_eps = int(rmsnorm), _ptr(norm_weight), norm_eps
     d.n_segments = len(segments)

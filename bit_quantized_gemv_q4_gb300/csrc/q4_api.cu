@@ -181,7 +181,8 @@ q4_status q4_gemv_ex(const q4_gemv_desc* desc, q4_stream_t stream) {
     if (!desc) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");
     q4_status st = validate_gemv(*desc);
     if (st != Q4_OK) return st;
-    return launch_gemv(*desc, reinterpret_cast<cudaStream_t>(stream), false, false);
+    const bool early = (desc->flags & Q4_GEMV_EARLY_WEIGHTS) != 0;
+    return launch_gemv(*desc, reinterpret_cast<cudaStream_t>(stream), early, early);
 }
 
 }  // extern "C"

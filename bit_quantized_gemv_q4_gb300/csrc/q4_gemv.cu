@@ -1050,6 +1050,7 @@ q4_status validate_gemv(const q4_gemv_desc& d) {
     if (d.x_rmsnorm && !(d.norm_eps >= 0.f)) return fail(Q4_ERR_INVALID_ARG, "norm_eps must be >= 0");
     if (d.x_rmsnorm && d.norm_weight && !aligned16(d.norm_weight))
         return fail(Q4_ERR_MISALIGNED, "norm_weight must be 16-byte aligned");
+    if (d.flags & ~Q4_GEMV_EARLY_WEIGHTS) return fail(Q4_ERR_INVALID_ARG, "unknown flags 0x%x", d.flags);
     for (int i = 0; i < d.n_segments; ++i) {
         const q4_segment& s = d.seg[i];
         if (!s.Wq || !s.scales || !s.biases) return fail(Q4_ERR_INVALID_ARG, "segment %d: NULL weights", i);

@@ -164,7 +164,16 @@ typedef struct q4_gemv_desc {
     int x_rmsnorm;
     const uint16_t *norm_weight;
     float norm_eps;
+    int flags; /* Q4_GEMV_EARLY_WEIGHTS or 0 */
 } q4_gemv_desc;
+
+/* Launch with programmatic dependent launch and stream the weight tiles
+ * before the previous kernel on the stream completes (x, residuals and y
+ * still wait for it).  The caller promises that no kernel earlier on the
+ * stream writes Wq, scales or biases -- true for a model's weights between
+ * decode steps.  Back-to-back GEMVs then overlap one launch's weight stream
+ * with the previous launch's tail (BaseRT §3: low-overhead dispatch). */
+#define Q4_GEMV_EARLY_WEIGHTS 1
 
 q4_status q4_gemv_ex(const q4_gemv_desc *desc, q4_stream_t stream);
 

@@ -69,7 +69,7 @@ int main(void) {
   O(q4_layer_table, layers) O(q4_layer_table, lm_head) O(q4_layer_table, workspace)
   O(q4_layer_table, workspace_bytes) O(q4_layer_table, flags) O(q4_layer_table, plan)
   O(q4_layer_weights, down) O(q4_layer_weights, ffn_norm) O(q4_moe_desc, out_dtype)
-  O(q4_gemv_desc, x_rmsnorm) O(q4_gemv_desc, norm_weight) O(q4_gemv_desc, norm_eps)
+  O(q4_gemv_desc, x_rmsnorm) O(q4_gemv_desc, norm_weight) O(q4_gemv_desc, norm_eps) O(q4_gemv_desc, flags)
   O(q4_layer_table, final_norm) O(q4_layer_table, norm_eps) O(q4_layer_table, logits_dtype)
   return 0;
 }

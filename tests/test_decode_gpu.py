@@ -252,3 +252,45 @@ def test_qwen3_0p6b_full_size(qwen06):
     assert rel <= 1e-3, rel
     persistent = qwen06.step(s.n_layers, x, flags=PERSISTENT)
     assert np.array_equal(out["logits"].view(np.uint32), persistent["logits"].view(np.uint32))
+
+
+def full_size_check(model, M, seed, flags=0):
+    """Every stage of the last layer on sampled rows (from the GPU's own input
+    of that layer), sampled logits, and the end-to-end logits against the
+    oracle's whole chain."""
+    s = model.shape
+    x = q4synth.activations(seed, M, s.hidden)
+    prev = model.step(s.n_layers - 1, x, flags=flags)
+    out = model.step(s.n_layers, x, flags=flags)
+    g = np.random.default_rng(seed)
+    rows = {"qkv": {"q": g.integers(0, s.q, 192), "k": g.integers(0, s.kv, 96), "v": g.integers(0, s.kv, 96)},
+            "hidden": np.unique(g.integers(0, s.hidden, 192)), "ffn": np.unique(g.integers(0, s.ffn, 192))}
+    check_layer(model.layers[-1], prev["h"].astype(np.float16), out, rows=rows, what=f"{s.name} last layer M={M}")
+    lrows = np.unique(g.integers(0, s.vocab, 1024))
+    y_ref, A = oracle.decode_logits(model.lm, out["h"], rows=lrows)
+    assert_parity(out["logits"][:, lrows], y_ref, A, what=f"{s.name} logits sampled M={M}")
+    l_ref, _, _ = oracle.decode_step(model.layers, model.lm, x)
+    rel = np.linalg.norm(out["logits"] - l_ref) / np.linalg.norm(l_ref)
+    assert rel <= 1e-3, (s.name, M, rel)
+
+
+@pytest.fixture(scope="module")
+def llama3b():
+    return DevModel(q4synth.LLAMA32_3B)
+
+
+@pytest.mark.parametrize("M", [1, 4])
+def test_llama32_3b_full_size(llama3b, M):
+    """The Llama-3.2-3B-shaped stream (28 layers, hidden 3072, lm_head 3072 ->
+    128256) at M = 1 and in batched decode at M = 4."""
+    full_size_check(llama3b, M, q4synth.BASE_SEED + 780 + M)
+
+
+@pytest.fixture(scope="module")
+def qwen4b():
+    return DevModel(q4synth.QWEN3_4B)
+
+
+def test_qwen3_4b_full_size(qwen4b):
+    """The Qwen3-4B-shaped stream (36 layers, hidden 2560, lm_head 2560 -> 151936), M = 1."""
+    full_size_check(qwen4b, 1, q4synth.BASE_SEED + 790)

@@ -207,3 +207,34 @@ def test_k_beyond_shared_memory_is_refused():
         q4.q4_gemv(Wq, s, s, x, y, 1, N, K)
     assert ei.value.name == "Q4_ERR_UNSUPPORTED"
     assert q4.q4_device_status() == 0
+
+
+def test_early_weights_flag_chain():
+    """Q4_GEMV_EARLY_WEIGHTS: a chain of launches on one stream where each
+    reads the previous one's output (x, and the residual in place) gives the
+    same bits as the same chain launched without the flag -- the weights
+    stream early, the activations still wait for the kernel before."""
+    K, N = 1024, 1024
+    mats = [q4synth.q4_matrix(90 + i, N, K) for i in range(6)]
+    dev = [dev_q4(mm) for mm in mats]
+    x0 = q4synth.activations(96, 1, K)
+    outs = []
+    for flags in (0, q4.Q4_GEMV_EARLY_WEIGHTS):
+        h = torch_dev(x0).clone()
+        t = torch.empty(1, N, dtype=torch.float16, device="cuda")
+        for i in range(6):
+            # t = W_i h; then h += W_i' t (residual in place)
+            q4.q4_gemv_ex([q4.Segment(*dev[i], N, y=t)], h, 1, K, out_dtype=q4.Q4_F16, flags=flags)
+            q4.q4_gemv_ex([q4.Segment(*dev[(i + 3) % 6], N, y=h, residual=h)], t, 1, K, out_dtype=q4.Q4_F16,
+                          flags=flags)
+        torch.cuda.synchronize()
+        assert q4.q4_device_status() == 0
+        outs.append(h.cpu().numpy().copy())
+    assert np.array_equal(outs[0].view(np.uint16), outs[1].view(np.uint16))
+    # and the first link against the oracle
+    t = torch.empty(1, N, dtype=torch.float16, device="cuda")
+    q4.q4_gemv_ex([q4.Segment(*dev[0], N, y=t)], torch_dev(x0), 1, K, out_dtype=q4.Q4_F16,
+                  flags=q4.Q4_GEMV_EARLY_WEIGHTS)
+    torch.cuda.synchronize()
+    y_ref, A = oracle.gemv(mats[0].Wq, mats[0].scales, mats[0].biases, x0)
+    assert_parity(t.float().cpu().numpy(), y_ref, A, fp16_out=True, what="early weights")
