@@ -711,7 +711,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--section", default="all",
-                    choices=["all", "decode", "moe", "lm_head", "prefill", "attention", "streams", "gemv"],
+                    choices=["all", "decode", "moe", "lm_head", "prefill", "attention", "streams", "gemv",
+                             "clustered"],
                     help="moe / lm_head: only the MoE prefill timings / the lm_head GEMV timing "
                          "(for profiling runs)")
     args = ap.parse_args()
@@ -806,6 +807,11 @@ def main():
         return
     if args.section == "attention":
         print(json.dumps({"decode_attention": decode_attention(device, dl, dlm, shape)}))
+        return
+    if args.section == "clustered":
+        xc = torch.from_numpy(q4synth.activations(q4synth.BASE_SEED + 4242, M, shape.hidden)).to(device)
+        print(json.dumps({"decode_clustered": decode_clustered(q4, device, dl, dlm, shape, xc, steps=args.steps,
+                                                               warmup=args.warmup)}))
         return
     table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
     nws = q4.q4_decode_workspace_bytes(table)

@@ -47,6 +47,22 @@
 
 namespace q4s {
 
+// Per-phase timestamps (%globaltimer) of the first and the last CTA, for the
+// step-latency breakdown; compiled in only with -DQ4_STEP_TRACE (a separate
+// diagnostic build, bit_quantized_gemv_q4_gb300/trace_step.py).
+#ifdef Q4_STEP_TRACE
+__device__ unsigned long long g_step_trace[2 * 4096];
+#define Q4_TRACE(k)                                                                                  \
+    do {                                                                                             \
+        if (tid == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1) && l < 128)                  \
+            g_step_trace[(blockIdx.x ? 4096 : 0) + l * 32 + (k)] = q4d::globaltimer();                \
+    } while (0)
+#else
+#define Q4_TRACE(k) \
+    do {            \
+    } while (0)
+#endif
+
 constexpr int kWarps = 8;
 constexpr int kCT = kWarps * 32;       // consumer threads
 constexpr int kThreads = kCT + 32;     // + the producer warp
@@ -677,13 +693,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             unsigned long long* Xf = Xa + (size_t)C * H;
             // ---------------- attention half (input xs0): q rows (sent to the
             // cluster), the o partial, published; k, v while the partials travel
+            Q4_TRACE(0);
             const float rinv = rms_inv(nss0, H, p.eps, lane);
             int sl;
             const uint8_t* slot = item_wait(sl);
+            Q4_TRACE(1);
             const int nq = w.qb - w.qa;
             RowItem ri = row_item(H, nq, 0);
             if (slot) dot_rows(slot, ri, nq, 0, H, xs0, warp, lane, rowout);
             q4d::named_bar(1, kCT);
+            Q4_TRACE(2);
             if (slot) item_done(sl);
             for (int idx = tid; idx < nq * S; idx += kCT) {
                 const int r = idx / S, peer = idx - r * S;
@@ -692,13 +711,17 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
                 st_async_b32(peer_addr(q4d::smem_addr(qx + (w.qa + r - 64 * w.qg0)), (uint32_t)peer),
                              __float_as_uint(__half2float(__ushort_as_half(qh))), peer_addr(qbar, (uint32_t)peer));
             }
+            Q4_TRACE(3);
             // the cluster's q block is complete once every peer's share arrived
             if (!bad && !wait_cluster_bar(qbar, l & 1, p.err)) bad = true;
+            Q4_TRACE(4);
             if (tid == 0) q4d::mbar_arrive_expect_tx(qbar, q_bytes);  // the next layer's phase
             slot = item_wait(sl);
             col_partial(slot, col_item(ro, p.qspan, p.qspan_s), p.qspan, p.qspan_s, w.qg0, qx, ro, pg, red);
             if (slot) item_done(sl);
+            Q4_TRACE(5);
             publish(Xa, red, c, H, oa, ro, tag_of(2 * l));
+            Q4_TRACE(6);
             slot = item_wait(sl);
             const int nk = w.k1 - w.k0, nv = w.v1 - w.v0;
             ri = row_item(H, nk, nv);
@@ -711,19 +734,24 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
                 else p.v[w.v0 + r - nk] = hv;
             }
             bad = q4d::named_bar_or(1, kCT, bad);
+            Q4_TRACE(7);
             if (!bad && !collect(Xa, hown, gown + (size_t)(2 * l + 1) * ro, xs1, nss1, c == 0 ? p.h_mid : nullptr,
                                  C, H, S, oa, ro, tag_of(2 * l), hbar, p.err))
                 bad = true;
+            Q4_TRACE(8);
             wait_h(0);
+            Q4_TRACE(9);
             if (bad) break;
             // ---------------- FFN half (input xs1): act = SiLU(gate) * up
             // (sent to the cluster), the down partial
             const float rinv2 = rms_inv(nss1, H, p.eps, lane);
             slot = item_wait(sl);
+            Q4_TRACE(10);
             const int nf = w.fb - w.fa;
             ri = row_item(H, nf, nf);
             if (slot) dot_rows(slot, ri, nf, nf, H, xs1, warp, lane, rowout);
             q4d::named_bar(1, kCT);
+            Q4_TRACE(11);
             if (slot) item_done(sl);
             for (int idx = tid; idx < nf * S; idx += kCT) {
                 const int r = idx / S, peer = idx - r * S;
@@ -733,18 +761,24 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
                 st_async_b32(peer_addr(q4d::smem_addr(ax + (w.fa + r - 64 * w.fg0)), (uint32_t)peer),
                              __float_as_uint(__half2float(__ushort_as_half(ah))), peer_addr(abar, (uint32_t)peer));
             }
+            Q4_TRACE(12);
             if (!bad && !wait_cluster_bar(abar, l & 1, p.err)) bad = true;
+            Q4_TRACE(13);
             if (tid == 0) q4d::mbar_arrive_expect_tx(abar, a_bytes);
             slot = item_wait(sl);
             col_partial(slot, col_item(ro, p.fspan, p.fspan_s), p.fspan, p.fspan_s, w.fg0, ax, ro, pg, red);
             if (slot) item_done(sl);
+            Q4_TRACE(14);
             publish(Xf, red, c, H, oa, ro, tag_of(2 * l + 1));
             bad = q4d::named_bar_or(1, kCT, bad);
+            Q4_TRACE(15);
             const bool next = l + 1 < L;
             if (!bad && !collect(Xf, hown, next ? gown + (size_t)(2 * l + 2) * ro : nullptr, xs0, nss0,
                                  c == 0 ? p.h : nullptr, C, H, S, oa, ro, tag_of(2 * l + 1), hbar, p.err))
                 bad = true;
+            Q4_TRACE(16);
             if (next) wait_h(1);
+            Q4_TRACE(17);
         }
         if (bad && tid == 0) abort_sh = 1;
         if (lane == 0) atomicMin(&consumed_sh, n);
@@ -966,3 +1000,10 @@ q4_status step_launch(const StepPlan& sp, cudaStream_t stream) {
 }
 
 }  // namespace q4i
+
+#ifdef Q4_STEP_TRACE
+// Trace build only: copies the timestamps (2 x 4096 64-bit words) to `out`.
+extern "C" int q4_step_trace_read(void* out) {
+    return (int)cudaMemcpyFromSymbol(out, q4s::g_step_trace, sizeof(unsigned long long) * 2 * 4096);
+}
+#endif
