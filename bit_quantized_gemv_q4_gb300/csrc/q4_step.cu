@@ -63,11 +63,14 @@ __device__ unsigned long long g_step_trace[2 * 4096];
     } while (0)
 #endif
 
-constexpr int kWarps = 8;
-constexpr int kCT = kWarps * 32;       // consumer threads
-constexpr int kThreads = kCT + 32;     // + the producer warp
+constexpr int kWarps = 8;                        // consumer warps (the layer's critical path)
+constexpr int kCT = kWarps * 32;                 // consumer threads
+constexpr int kKvWarps = 4;                      // k / v warps (one per scheduler)
+constexpr int kProducerWarp = kWarps;            // then the k / v warps
+constexpr int kKvWarp0 = kWarps + 1;
+constexpr int kThreads = (kWarps + 1 + kKvWarps) * 32;
 constexpr int kMaxSlots = 16;
-constexpr int kItems = 5;              // weight pieces per layer and CTA
+constexpr int kItems = 4;                        // ring pieces per layer and CTA: q, o, gate/up, down
 
 struct Lin {
     const uint32_t* Wq;
@@ -95,12 +98,16 @@ struct Params {
     int qspan, fspan;          // column-block widths in groups (largest cluster share)
     int qspan_s, fspan_s;      // scale / bias box widths in groups (multiples of 8)
     int slots;
-    uint32_t slot_bytes;
-    // shared memory: x of the two halves (fp32, lane-interleaved), their
-    // per-octet sums of squares, this CTA's h block and norm weights, row
-    // totals, q / act blocks, partials (ro, then span x ro per group),
-    // barriers, the ring
-    uint32_t off_xs, xs_bytes, off_nss, off_hown, off_gown, off_rows, off_qx, off_ax, off_red, off_bar, off_ring;
+    uint32_t slot_bytes, kv_slot_bytes;
+    // shared memory: x of the attention half (two buffers, by layer parity,
+    // so the k / v warps may still read layer l's while layer l+1's arrives)
+    // and of the FFN half (fp32, lane-interleaved), their per-octet sums of
+    // squares (same three buffers), this CTA's h block and norm weights, row
+    // totals of the consumers and of the k / v warps, q / act blocks,
+    // partials (ro, then span x ro per group), barriers, the k / v ring (two
+    // slots), the ring
+    uint32_t off_xs, xs_bytes, off_nss, off_hown, off_gown, off_rows, off_kvrows, off_qx, off_ax, off_red, off_bar,
+        off_kvring, off_ring;
 };
 
 // [a, b) = part i of n split into `parts` nearly equal pieces.
@@ -143,10 +150,12 @@ __device__ __forceinline__ void st_async_v4(uint32_t raddr, uint4 v, uint32_t rb
                  "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w), "r"(rbar)
                  : "memory");
 }
-// Wait on a barrier that peers complete (acquire at cluster scope).
+// Wait on a barrier that peers complete (acquire at cluster scope).  The
+// clock is read every 16th attempt only (a read costs about as much as the
+// attempt), which bounds the wait all the same.
 __device__ __forceinline__ bool wait_cluster_bar(uint32_t bar, uint32_t parity, int* err) {
     unsigned long long t0 = 0;
-    while (true) {
+    for (uint32_t it = 1;; ++it) {
         uint32_t ok;
         asm volatile(
             "{ .reg .pred p; mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2; "
@@ -155,6 +164,7 @@ __device__ __forceinline__ bool wait_cluster_bar(uint32_t bar, uint32_t parity, 
             : "r"(bar), "r"(parity)
             : "memory");
         if (ok) return true;
+        if (it & 15u) continue;
         if (t0 == 0) {
             t0 = q4d::globaltimer();
         } else if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
@@ -322,18 +332,19 @@ __device__ __forceinline__ void word_mac_nat(uint32_t q, uint16_t sh, float c102
 }
 
 // Dot products of the rows of a row item (block A rows, then block B rows)
-// with x (K = H).  In each pass warp w takes rows w, w + 8, ..., w + 56 of the
-// next 64 (those that exist); a lane covers 4 words (32 inputs) of each
-// 128-word chunk, x is loaded once per chunk for all the warp's rows, and the
-// rows' totals are reduced together by a transposing butterfly.  Totals go to
-// out[row].  
+// with x (K = H), by NW warps.  In each pass warp w takes rows w, w + NW, ...,
+// w + 7 NW of the next 8 NW (those that exist); a lane covers 4 words (32
+// inputs) of each 128-word chunk, x is loaded once per chunk for all the
+// warp's rows, and the rows' totals are reduced together by a transposing
+// butterfly.  Totals go to out[row].
+template <int NW>
 __device__ __forceinline__ void dot_rows(const uint8_t* slot, RowItem ri, int nA, int nB, int H, const float4* xs,
-                                      int warp, int lane, float* out) {
+                                         int warp, int lane, float* out) {
     constexpr int RB = 8;
     const int W8 = H / 8, G = H / 64, n = nA + nB;
     const int nchunks = (W8 + 127) / 128;
-    for (int base = 0; base < n; base += RB * kWarps) {
-        int nr = (n - base - warp + kWarps - 1) / kWarps;  // rows of this warp in the pass
+    for (int base = 0; base < n; base += RB * NW) {
+        int nr = (n - base - warp + NW - 1) / NW;  // rows of this warp in the pass
         nr = nr < 0 ? 0 : (nr > RB ? RB : nr);
         if (nr == 0) continue;
         float2 acc[RB];
@@ -350,7 +361,7 @@ __device__ __forceinline__ void dot_rows(const uint8_t* slot, RowItem ri, int nA
 #pragma unroll
             for (int k = 0; k < RB; ++k) {
                 if (k < nr) {
-                    const int r = base + warp + k * kWarps;
+                    const int r = base + warp + k * NW;
                     const bool b = r >= nA;
                     const int q = b ? r - nA : r;
                     const uint4 v = *reinterpret_cast<const uint4*>(
@@ -390,7 +401,7 @@ __device__ __forceinline__ void dot_rows(const uint8_t* slot, RowItem ri, int nA
         v[0] += __shfl_xor_sync(0xffffffffu, v[0], 2);
         v[0] += __shfl_xor_sync(0xffffffffu, v[0], 1);
         const int k = lane >> 2;
-        if ((lane & 3) == 0 && k < nr) out[base + warp + k * kWarps] = v[0];
+        if ((lane & 3) == 0 && k < nr) out[base + warp + k * NW] = v[0];
     }
 }
 
@@ -467,12 +478,14 @@ __device__ __forceinline__ bool collect(const unsigned long long* X, uint16_t* h
             const unsigned long long* pb = pa + 4;
             unsigned long long a = ld_xch(pa), b = ld_xch(pb);
             unsigned long long t0 = 0;
-            while (ok && ((uint32_t)(a >> 32) != tag || (uint32_t)(b >> 32) != tag)) {
-                if (t0 == 0) {
-                    t0 = q4d::globaltimer();
-                } else if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
-                    atomicOr(err, q4d::kErrTimeout);
-                    ok = false;
+            for (uint32_t it = 1; ok && ((uint32_t)(a >> 32) != tag || (uint32_t)(b >> 32) != tag); ++it) {
+                if ((it & 15u) == 0) {  // the clock every 16th poll (a read costs about a poll)
+                    if (t0 == 0) {
+                        t0 = q4d::globaltimer();
+                    } else if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
+                        atomicOr(err, q4d::kErrTimeout);
+                        ok = false;
+                    }
                 }
                 a = ld_xch(pa);
                 b = ld_xch(pb);
@@ -535,34 +548,79 @@ __device__ __forceinline__ bool collect(const unsigned long long* X, uint16_t* h
     return ok;
 }
 
+// Hand-off counters between the consumer warps and the k / v warps of a CTA
+// (shared memory, release / acquire at CTA scope).  A counter only grows, so a
+// waiter can never mistake a later hand-off for the one it waits for.
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(q4d::smem_addr(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(q4d::smem_addr(p)) : "memory");
+    return v;
+}
+// Wait until *ctr >= target; false when the CTA aborted or the wait expired.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, const volatile int* abort_flag,
+                                           int* err) {
+    if (ld_acquire_cta(ctr) >= target) return true;
+    const unsigned long long t0 = q4d::globaltimer();
+    while (true) {
+        __nanosleep(32);
+        if (ld_acquire_cta(ctr) >= target) return true;
+        if (*abort_flag) return false;
+        if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
+            atomicOr(err, q4d::kErrTimeout);
+            return false;
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_constant__ Params p) {
     extern __shared__ __align__(128) uint8_t smem[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int c = (int)cluster_index(), i = (int)cluster_rank();
     const int S = p.S, C = p.C, H = p.H, ro = p.ro, L = p.L;
-    float4* xs0 = reinterpret_cast<float4*>(smem + p.off_xs);                 // attention half input
-    float4* xs1 = reinterpret_cast<float4*>(smem + p.off_xs + p.xs_bytes);    // FFN half input
-    float* nss0 = reinterpret_cast<float*>(smem + p.off_nss);                 // their octet sums of squares
-    float* nss1 = nss0 + H / 8;
+    // x of the attention half (by layer parity) and of the FFN half, and
+    // their octet sums of squares
+    auto xs0_of = [&](int l) { return reinterpret_cast<float4*>(smem + p.off_xs + (uint32_t)(l & 1) * p.xs_bytes); };
+    auto nss0_of = [&](int l) { return reinterpret_cast<float*>(smem + p.off_nss) + (l & 1) * (H / 8); };
+    float4* xs1 = reinterpret_cast<float4*>(smem + p.off_xs + 2 * p.xs_bytes);
+    float* nss1 = reinterpret_cast<float*>(smem + p.off_nss) + 2 * (H / 8);
     uint16_t* hown = reinterpret_cast<uint16_t*>(smem + p.off_hown);          // this CTA's block of h / h'
     uint16_t* gown = reinterpret_cast<uint16_t*>(smem + p.off_gown);          // [2L][ro] norm weights of that block
     float* rowout = reinterpret_cast<float*>(smem + p.off_rows);              // row totals of a row item
+    float* kvrows = reinterpret_cast<float*>(smem + p.off_kvrows);            // row totals of the k / v rows
     float* qx = reinterpret_cast<float*>(smem + p.off_qx);                    // the cluster's q block
     float* ax = reinterpret_cast<float*>(smem + p.off_ax);                    // the cluster's act block
     float* red = reinterpret_cast<float*>(smem + p.off_red);                  // [0, ro): this CTA's partials
     float* pg = red + ro;                                                     // per-group partials
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint8_t* ring = smem + p.off_ring;
+    uint8_t* kvring = smem + p.off_kvring;
     const uint32_t full0 = q4d::smem_addr(bars), empty0 = q4d::smem_addr(bars + kMaxSlots);
     const uint32_t qbar = q4d::smem_addr(bars + 2 * kMaxSlots), abar = qbar + 8, hbar = qbar + 16;
+    const uint32_t kvfull0 = qbar + 24;  // two: the k / v slots
     const Work w = work_of(p.QN, p.KVN, p.F, C, S, c, i);
     const int oa = i * ro;
     const uint32_t q_bytes = 64u * (uint32_t)(w.qg1 - w.qg0) * 4u, a_bytes = 64u * (uint32_t)(w.fg1 - w.fg0) * 4u;
     const uint32_t h_bytes = (uint32_t)(H / 8) * 36u;  // per octet: two float4 of x and a sum of squares
 
     __shared__ uint32_t step_sh;
-    __shared__ int issued_sh, consumed_sh;
+    __shared__ int issued_sh, consumed_sh, kv_issued_sh, kv_consumed_sh;
     __shared__ volatile int abort_sh;
+    // xrdy_sh: layers whose attention-half x is in place (consumers -> k / v
+    // warps); kvdone_sh: layers whose k / v rows are done (k / v warps ->
+    // consumers, who let peers overwrite that x buffer only afterwards)
+    __shared__ uint32_t xrdy_sh, kvdone_sh;
+    // The k / v warps also compute both norms' 1/rms for the consumers:
+    // nss1_sh counts layers whose FFN-half sums of squares are in place
+    // (consumers -> k / v warps), rinv_seq_sh the values published in
+    // rinv_sh (2l+1: attention half of layer l, 2l+2: its FFN half).
+    __shared__ uint32_t nss1_sh, rinv_seq_sh;
+    // pub_sh: layers whose attention-half partials are published; the k / v
+    // rows start then (the consumers only poll while the partials travel)
+    __shared__ uint32_t pub_sh;
+    __shared__ float rinv_sh[2];
     if (tid == 0) {
         for (int s = 0; s < p.slots; ++s) {
             q4d::mbar_init(full0 + 8 * s, 32);
@@ -571,11 +629,20 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         q4d::mbar_init(qbar, 1);
         q4d::mbar_init(abar, 1);
         q4d::mbar_init(hbar, 1);
+        q4d::mbar_init(kvfull0, 1);
+        q4d::mbar_init(kvfull0 + 8, 1);
         q4d::fence_mbar_init();
         step_sh = q4d::ld_relaxed(p.ctr);
         issued_sh = 0;
         consumed_sh = 0x7fffffff;
+        kv_issued_sh = 0;
+        kv_consumed_sh = 0;
         abort_sh = 0;
+        xrdy_sh = 1;
+        kvdone_sh = 0;
+        nss1_sh = 0;
+        rinv_seq_sh = 0;
+        pub_sh = 0;
     }
     // q / act blocks zeroed (their tails past the cluster's share stay zero,
     // so padded columns contribute nothing); the norm weights of this CTA's
@@ -591,6 +658,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
     for (int r = tid; r < ro; r += kThreads) hown[r] = p.x[oa + r];
     {
         const uint16_t* g0 = p.layers[0].attn_norm;
+        float4* xs = xs0_of(0);
+        float* nss = nss0_of(0);
         for (int j = tid; j < H / 8; j += kThreads) {
             float f[8], g[8];
             const uint4 raw = *reinterpret_cast<const uint4*>(p.x + 8 * j);
@@ -607,8 +676,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
                 ss = fmaf(f[e], f[e], ss);
                 g[e] = g0 ? __half2float(__ushort_as_half(g0[8 * j + e])) : 1.f;
             }
-            nss0[j] = ss;
-            float4* d = xs0 + xs_slot(j);
+            nss[j] = ss;
+            float4* d = xs + xs_slot(j);
             d[0] = make_float4(f[0] * g[0], f[4] * g[4], f[1] * g[1], f[5] * g[5]);
             d[32] = make_float4(f[2] * g[2], f[6] * g[6], f[3] * g[3], f[7] * g[7]);
         }
@@ -622,13 +691,15 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
     }
     cluster_sync();  // every peer's barriers are initialised before anything is sent
 
-    if (warp == kWarps) {
+    if (warp == kProducerWarp) {
         // ------------------------------------------------------ producer warp
+        // q rows, o column block, gate/up rows, down column block of every layer
         const uint64_t pol = q4d::policy_evict_first();
         int n = 0;
         for (int l = 0; l < L && !abort_sh; ++l) {
             const LayerDesc& Ld = p.layers[l];
-            for (int it = 0; it < kItems; ++it, ++n) {
+            for (int ii = 0; ii < kItems; ++ii, ++n) {
+                const int it = ii < 2 ? ii : ii + 1;  // item kinds 0, 1, 3, 4 (2 is the k / v rows)
                 const int st = n % p.slots, k = n / p.slots;
                 if (k > 0) {
                     int ok = 1;
@@ -651,6 +722,87 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             }
         }
         if (lane == 0) issued_sh = n;
+    } else if (warp >= kKvWarp0) {
+        // ---------------------------------------------------- k / v warps
+        // Layer l's k and v rows, off the layer's critical path: they start
+        // once the attention half's partials are published and need only
+        // layer l's attention-half x, kept in its parity buffer until these
+        // warps are done with it.  Their weights come through a ring of two
+        // slots that these warps refill themselves.  These warps also compute
+        // both halves' 1/rms for the consumers.
+        const int kw = warp - kKvWarp0, ktid = tid - kKvWarp0 * 32;
+        const int nk = w.k1 - w.k0, nv = w.v1 - w.v0;
+        const RowItem ri = row_item(H, nk, nv);
+        const uint64_t pol = q4d::policy_evict_first();
+        auto issue_kv = [&](int l) {  // one thread
+            uint8_t* slot = kvring + (size_t)(l & 1) * p.kv_slot_bytes;
+            const uint32_t fb = kvfull0 + 8 * (l & 1);
+            const uint32_t bytes = issue_item(p, p.layers[l], p.maps + 6 * l, w, 2, i, slot, fb, false, pol);
+            q4d::mbar_arrive_expect_tx(fb, bytes);
+            issue_item(p, p.layers[l], p.maps + 6 * l, w, 2, i, slot, fb, true, pol);
+        };
+        int issued = L < 2 ? L : 2, done = 0;
+        if (ktid == 0)
+            for (int l = 0; l < issued; ++l) issue_kv(l);
+        // Each k / v warp thread waits on `ctr` reaching `target` through lane 0
+        // of its warp; false (every k / v thread alike) when the CTA aborted.
+        auto kv_wait = [&](const uint32_t* ctr, uint32_t target) -> bool {
+            int ok = 1;
+            if (lane == 0) ok = wait_count(ctr, target, &abort_sh, p.err) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (q4d::named_bar_or(2, kKvWarps * 32, !ok)) {
+                if (ktid == 0) abort_sh = 1;
+                return false;
+            }
+            return true;
+        };
+        for (int l = 0; l < L; ++l) {
+            // layer l's attention-half x and this layer's k / v weights
+            if (!kv_wait(&xrdy_sh, (uint32_t)(l + 1))) break;
+            int ok = 1;
+            if (lane == 0) ok = q4d::mbar_wait(kvfull0 + 8 * (l & 1), (l >> 1) & 1, p.err) ? 1 : 0;
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (q4d::named_bar_or(2, kKvWarps * 32, !ok)) {
+                if (ktid == 0) abort_sh = 1;
+                break;
+            }
+            const float rinv = rms_inv(nss0_of(l), H, p.eps, lane);
+            if (ktid == 0) {
+                rinv_sh[0] = rinv;
+                st_release_cta(&rinv_seq_sh, (uint32_t)(2 * l + 1));
+            }
+            // the k and v rows once the attention half's partials are out
+            if (!kv_wait(&pub_sh, (uint32_t)(l + 1))) break;
+            dot_rows<kKvWarps>(kvring + (size_t)(l & 1) * p.kv_slot_bytes, ri, nk, nv, H, xs0_of(l), kw, lane,
+                               kvrows);
+            q4d::named_bar(2, kKvWarps * 32);  // the slot and layer l's x are read
+            ++done;
+            if (ktid == 0) {
+                st_release_cta(&kvdone_sh, (uint32_t)(l + 1));
+                if (l + 2 < L) {
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    issue_kv(l + 2);
+                }
+            }
+            if (l + 2 < L) ++issued;
+            for (int r = ktid; r < nk + nv; r += kKvWarps * 32) {
+                const uint16_t hv = __half_as_ushort(__float2half_rn(kvrows[r] * rinv));
+                if (r < nk) p.k[w.k0 + r] = hv;
+                else p.v[w.v0 + r - nk] = hv;
+            }
+            // the FFN half's 1/rms once the consumers have its sums of squares
+            if (!kv_wait(&nss1_sh, (uint32_t)(l + 1))) break;
+            const float rinv2 = rms_inv(nss1, H, p.eps, lane);
+            if (ktid == 0) {
+                rinv_sh[1] = rinv2;
+                st_release_cta(&rinv_seq_sh, (uint32_t)(2 * l + 2));
+            }
+            q4d::named_bar(2, kKvWarps * 32);  // kvrows is free again
+        }
+        if (ktid == 0) {
+            kv_issued_sh = issued;
+            kv_consumed_sh = done;
+        }
     } else {
         // ---------------------------------------------------------- consumers
         const uint32_t step = step_sh;
@@ -660,7 +812,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         // so `bad` stays uniform within a warp (the warp-wide shuffles need
         // every lane); named_bar_or makes it uniform across the CTA.  A failed
         // or skipped wait returns nullptr and the item is not released (its
-        // copies may still be in flight).
+        // copies may still be in flight).  Items are waited for ahead of the
+        // hand-off waits, so their arrival overlaps them.
         auto item_wait = [&](int& slot_idx) -> const uint8_t* {
             slot_idx = n % p.slots;
             int ok = 0;
@@ -688,97 +841,127 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             bad = q4d::named_bar_or(1, kCT, bad);
         };
 
+        // 1/rms of a half from the k / v warps (lane 0 waits, the warp shares it)
+        auto rinv_of = [&](uint32_t seq) -> float {
+            int ok = 0;
+            float r = 0.f;
+            if (lane == 0 && !bad) {
+                ok = wait_count(&rinv_seq_sh, seq, &abort_sh, p.err) ? 1 : 0;
+                r = rinv_sh[(seq - 1) & 1];
+            }
+            if (!__shfl_sync(0xffffffffu, ok, 0)) bad = true;
+            return __shfl_sync(0xffffffffu, r, 0);
+        };
+
+        int sl = 0;
+        const uint8_t* slot = item_wait(sl);  // layer 0's q rows
         for (int l = 0; l < L && !bad; ++l) {
             unsigned long long* Xa = p.xch + (size_t)(2 * l) * C * H;
             unsigned long long* Xf = Xa + (size_t)C * H;
-            // ---------------- attention half (input xs0): q rows (sent to the
-            // cluster), the o partial, published; k, v while the partials travel
+            // ---------------- attention half: q rows (sent to the cluster),
+            // the o partial, published; the next half's input collected
             Q4_TRACE(0);
-            const float rinv = rms_inv(nss0, H, p.eps, lane);
-            int sl;
-            const uint8_t* slot = item_wait(sl);
-            Q4_TRACE(1);
             const int nq = w.qb - w.qa;
             RowItem ri = row_item(H, nq, 0);
-            if (slot) dot_rows(slot, ri, nq, 0, H, xs0, warp, lane, rowout);
+            if (slot) dot_rows<kWarps>(slot, ri, nq, 0, H, xs0_of(l), warp, lane, rowout);
+            const float rinv = rinv_of((uint32_t)(2 * l + 1));
             q4d::named_bar(1, kCT);
-            Q4_TRACE(2);
+            Q4_TRACE(1);
             if (slot) item_done(sl);
-            for (int idx = tid; idx < nq * S; idx += kCT) {
-                const int r = idx / S, peer = idx - r * S;
-                const uint16_t qh = __half_as_ushort(__float2half_rn(rowout[r] * rinv));
-                if (peer == 0) p.q[w.qa + r] = qh;
-                st_async_b32(peer_addr(q4d::smem_addr(qx + (w.qa + r - 64 * w.qg0)), (uint32_t)peer),
-                             __float_as_uint(__half2float(__ushort_as_half(qh))), peer_addr(qbar, (uint32_t)peer));
+            // four rows per 16-byte store (a CTA's share of a cluster's rows is
+            // a multiple of 4, starting at a multiple of 4)
+            for (int idx = tid; idx < (nq / 4) * S; idx += kCT) {
+                const int r4 = idx / S, peer = idx - r4 * S;
+                uint16_t qh[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) qh[e] = __half_as_ushort(__float2half_rn(rowout[4 * r4 + e] * rinv));
+                if (peer == 0)
+                    *reinterpret_cast<uint2*>(p.q + w.qa + 4 * r4) =
+                        make_uint2(qh[0] | ((uint32_t)qh[1] << 16), qh[2] | ((uint32_t)qh[3] << 16));
+                st_async_v4(peer_addr(q4d::smem_addr(qx + (w.qa + 4 * r4 - 64 * w.qg0)), (uint32_t)peer),
+                            make_uint4(__float_as_uint(__half2float(__ushort_as_half(qh[0]))),
+                                       __float_as_uint(__half2float(__ushort_as_half(qh[1]))),
+                                       __float_as_uint(__half2float(__ushort_as_half(qh[2]))),
+                                       __float_as_uint(__half2float(__ushort_as_half(qh[3])))),
+                            peer_addr(qbar, (uint32_t)peer));
             }
-            Q4_TRACE(3);
+            Q4_TRACE(2);
+            slot = item_wait(sl);  // the o column block
             // the cluster's q block is complete once every peer's share arrived
             if (!bad && !wait_cluster_bar(qbar, l & 1, p.err)) bad = true;
-            Q4_TRACE(4);
+            Q4_TRACE(3);
             if (tid == 0) q4d::mbar_arrive_expect_tx(qbar, q_bytes);  // the next layer's phase
-            slot = item_wait(sl);
             col_partial(slot, col_item(ro, p.qspan, p.qspan_s), p.qspan, p.qspan_s, w.qg0, qx, ro, pg, red);
             if (slot) item_done(sl);
-            Q4_TRACE(5);
+            Q4_TRACE(4);
             publish(Xa, red, c, H, oa, ro, tag_of(2 * l));
-            Q4_TRACE(6);
-            slot = item_wait(sl);
-            const int nk = w.k1 - w.k0, nv = w.v1 - w.v0;
-            ri = row_item(H, nk, nv);
-            if (slot) dot_rows(slot, ri, nk, nv, H, xs0, warp, lane, rowout);
-            q4d::named_bar(1, kCT);
-            if (slot) item_done(sl);
-            for (int r = tid; r < nk + nv; r += kCT) {
-                const uint16_t hv = __half_as_ushort(__float2half_rn(rowout[r] * rinv));
-                if (r < nk) p.k[w.k0 + r] = hv;
-                else p.v[w.v0 + r - nk] = hv;
-            }
-            bad = q4d::named_bar_or(1, kCT, bad);
-            Q4_TRACE(7);
+            if (tid == 0) st_release_cta(&pub_sh, (uint32_t)(l + 1));
+            Q4_TRACE(5);
             if (!bad && !collect(Xa, hown, gown + (size_t)(2 * l + 1) * ro, xs1, nss1, c == 0 ? p.h_mid : nullptr,
                                  C, H, S, oa, ro, tag_of(2 * l), hbar, p.err))
                 bad = true;
-            Q4_TRACE(8);
+            Q4_TRACE(6);
+            slot = item_wait(sl);  // gate / up rows
             wait_h(0);
-            Q4_TRACE(9);
+            if (tid == 0 && !bad) st_release_cta(&nss1_sh, (uint32_t)(l + 1));  // for the k / v warps' 1/rms
+            Q4_TRACE(7);
             if (bad) break;
-            // ---------------- FFN half (input xs1): act = SiLU(gate) * up
-            // (sent to the cluster), the down partial
-            const float rinv2 = rms_inv(nss1, H, p.eps, lane);
-            slot = item_wait(sl);
-            Q4_TRACE(10);
+            // ---------------- FFN half: act = SiLU(gate) * up (sent to the
+            // cluster), the down partial, published; the next layer's input
+            // collected
             const int nf = w.fb - w.fa;
             ri = row_item(H, nf, nf);
-            if (slot) dot_rows(slot, ri, nf, nf, H, xs1, warp, lane, rowout);
-            q4d::named_bar(1, kCT);
-            Q4_TRACE(11);
+            if (slot) dot_rows<kWarps>(slot, ri, nf, nf, H, xs1, warp, lane, rowout);
+            const float rinv2 = rinv_of((uint32_t)(2 * l + 2));
+            // This layer's act lets peers reach the exchange that refills the
+            // attention-half x buffer of layer l - 1: the k / v warps must be
+            // done with it.
+            if (tid == 0 && l > 0 && !wait_count(&kvdone_sh, (uint32_t)l, &abort_sh, p.err)) bad = true;
+            bad = q4d::named_bar_or(1, kCT, bad);
+            Q4_TRACE(8);
+            if (bad) break;
             if (slot) item_done(sl);
-            for (int idx = tid; idx < nf * S; idx += kCT) {
-                const int r = idx / S, peer = idx - r * S;
-                const float g = rowout[r] * rinv2, u = rowout[nf + r] * rinv2;
-                const uint16_t ah = __half_as_ushort(__float2half_rn(g / (1.0f + expf(-g)) * u));
-                if (peer == 0) p.act[w.fa + r] = ah;
-                st_async_b32(peer_addr(q4d::smem_addr(ax + (w.fa + r - 64 * w.fg0)), (uint32_t)peer),
-                             __float_as_uint(__half2float(__ushort_as_half(ah))), peer_addr(abar, (uint32_t)peer));
+            for (int idx = tid; idx < (nf / 4) * S; idx += kCT) {
+                const int r4 = idx / S, peer = idx - r4 * S;
+                uint16_t ah[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int r = 4 * r4 + e;
+                    const float g = rowout[r] * rinv2, u = rowout[nf + r] * rinv2;
+                    ah[e] = __half_as_ushort(__float2half_rn(g / (1.0f + expf(-g)) * u));
+                }
+                if (peer == 0)
+                    *reinterpret_cast<uint2*>(p.act + w.fa + 4 * r4) =
+                        make_uint2(ah[0] | ((uint32_t)ah[1] << 16), ah[2] | ((uint32_t)ah[3] << 16));
+                st_async_v4(peer_addr(q4d::smem_addr(ax + (w.fa + 4 * r4 - 64 * w.fg0)), (uint32_t)peer),
+                            make_uint4(__float_as_uint(__half2float(__ushort_as_half(ah[0]))),
+                                       __float_as_uint(__half2float(__ushort_as_half(ah[1]))),
+                                       __float_as_uint(__half2float(__ushort_as_half(ah[2]))),
+                                       __float_as_uint(__half2float(__ushort_as_half(ah[3])))),
+                            peer_addr(abar, (uint32_t)peer));
             }
-            Q4_TRACE(12);
+            Q4_TRACE(9);
+            slot = item_wait(sl);  // the down column block
             if (!bad && !wait_cluster_bar(abar, l & 1, p.err)) bad = true;
-            Q4_TRACE(13);
+            Q4_TRACE(10);
             if (tid == 0) q4d::mbar_arrive_expect_tx(abar, a_bytes);
-            slot = item_wait(sl);
             col_partial(slot, col_item(ro, p.fspan, p.fspan_s), p.fspan, p.fspan_s, w.fg0, ax, ro, pg, red);
             if (slot) item_done(sl);
-            Q4_TRACE(14);
+            Q4_TRACE(11);
             publish(Xf, red, c, H, oa, ro, tag_of(2 * l + 1));
-            bad = q4d::named_bar_or(1, kCT, bad);
-            Q4_TRACE(15);
             const bool next = l + 1 < L;
-            if (!bad && !collect(Xf, hown, next ? gown + (size_t)(2 * l + 2) * ro : nullptr, xs0, nss0,
-                                 c == 0 ? p.h : nullptr, C, H, S, oa, ro, tag_of(2 * l + 1), hbar, p.err))
+            Q4_TRACE(12);
+            if (!bad && !collect(Xf, hown, next ? gown + (size_t)(2 * l + 2) * ro : nullptr, xs0_of(l + 1),
+                                 nss0_of(l + 1), c == 0 ? p.h : nullptr, C, H, S, oa, ro, tag_of(2 * l + 1), hbar,
+                                 p.err))
                 bad = true;
-            Q4_TRACE(16);
-            if (next) wait_h(1);
-            Q4_TRACE(17);
+            Q4_TRACE(13);
+            if (next) {
+                slot = item_wait(sl);  // the next layer's q rows
+                wait_h(1);
+                if (tid == 0 && !bad) st_release_cta(&xrdy_sh, (uint32_t)(l + 2));  // layer l+1's x is in place
+            }
+            Q4_TRACE(14);
         }
         if (bad && tid == 0) abort_sh = 1;
         if (lane == 0) atomicMin(&consumed_sh, n);
@@ -788,6 +971,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         // copies still landing in slots nobody will read (after an abort)
         for (int j = consumed_sh; j < issued_sh; ++j)
             q4d::mbar_wait(full0 + 8 * (j % p.slots), (j / p.slots) & 1, nullptr);
+        for (int j = kv_consumed_sh; j < kv_issued_sh; ++j)
+            q4d::mbar_wait(kvfull0 + 8 * (j & 1), (j >> 1) & 1, nullptr);
     }
     __syncthreads();
     cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
@@ -869,38 +1054,49 @@ q4_status step_plan(const StepArgs& a, StepPlan* out, bool* ok) {
         p.fspan = fs;
         p.qspan_s = (qs + 7 + 7) & ~7;
         p.fspan_s = (fs + 7 + 7) & ~7;
-        // slot size: the largest item of any CTA; the most rows a row item has
-        uint32_t slot = 0;
-        int max_rows = 0;
+        // slot size: the largest ring item of any CTA (q rows, gate/up rows,
+        // the column blocks) and the largest k / v item; the most rows each
+        // kind of row item has
+        uint32_t slot = 0, kv_slot = 0;
+        int max_rows = 0, max_kv_rows = 0;
         for (int cc = 0; cc < C; ++cc)
             for (int ii = 0; ii < S; ++ii) {
                 const q4s::Work w = q4s::work_of(QN, KVN, F, C, S, cc, ii);
-                const int nr[3][2] = {{w.qb - w.qa, 0}, {w.k1 - w.k0, w.v1 - w.v0}, {w.fb - w.fa, w.fb - w.fa}};
+                const int nr[2][2] = {{w.qb - w.qa, 0}, {w.fb - w.fa, w.fb - w.fa}};
                 for (const auto& r : nr) {
                     const uint32_t b = q4s::row_item(H, r[0], r[1]).gam;
                     slot = b > slot ? b : slot;
                     max_rows = r[0] + r[1] > max_rows ? r[0] + r[1] : max_rows;
                 }
+                const int nkv = (w.k1 - w.k0) + (w.v1 - w.v0);
+                const uint32_t b = q4s::row_item(H, w.k1 - w.k0, w.v1 - w.v0).gam;
+                kv_slot = b > kv_slot ? b : kv_slot;
+                max_kv_rows = nkv > max_kv_rows ? nkv : max_kv_rows;
             }
         const uint32_t co = q4s::col_item(p.ro, qs, p.qspan_s).end, cd = q4s::col_item(p.ro, fs, p.fspan_s).end;
         slot = co > slot ? co : slot;
         slot = cd > slot ? cd : slot;
         slot = q4s::align128(slot);
-        // fixed shared memory: x of both halves (fp32, lane-interleaved) and
-        // their octet sums of squares, this CTA's h block and norm weights,
-        // the row totals, the q / act blocks, the partials, barriers
+        kv_slot = q4s::align128(kv_slot);
+        // fixed shared memory: x of the attention half (two parity buffers)
+        // and of the FFN half (fp32, lane-interleaved) and their octet sums of
+        // squares, this CTA's h block and norm weights, the row totals of the
+        // consumers and of the k / v warps, the q / act blocks, the partials,
+        // barriers, the two k / v slots
         uint32_t off = 0;
         p.off_xs = off;
         p.xs_bytes = q4s::align128((uint32_t)((H / 8 + 127) / 128) * 8u * 32u * 16u);
-        off += 2 * p.xs_bytes;
+        off += 3 * p.xs_bytes;
         p.off_nss = off;
-        off += q4s::align128(2u * (uint32_t)(H / 8) * 4u);
+        off += q4s::align128(3u * (uint32_t)(H / 8) * 4u);
         p.off_hown = off;
         off += q4s::align128((uint32_t)p.ro * 2u);
         p.off_gown = off;
         off += q4s::align128(2u * (uint32_t)L * (uint32_t)p.ro * 2u);
         p.off_rows = off;
         off += q4s::align128((uint32_t)max_rows * 4u);
+        p.off_kvrows = off;
+        off += q4s::align128((uint32_t)(max_kv_rows > 0 ? max_kv_rows : 1) * 4u);
         p.off_qx = off;
         off += q4s::align128((uint32_t)qs * 64u * 4u);
         p.off_ax = off;
@@ -908,13 +1104,16 @@ q4_status step_plan(const StepArgs& a, StepPlan* out, bool* ok) {
         p.off_red = off;
         off += q4s::align128((uint32_t)(1 + (qs > fs ? qs : fs)) * (uint32_t)p.ro * 4u);
         p.off_bar = off;
-        off += q4s::align128((2 * q4s::kMaxSlots + 3) * 8u);
+        off += q4s::align128((2 * q4s::kMaxSlots + 5) * 8u);
+        p.off_kvring = off;
+        off += 2 * kv_slot;
         p.off_ring = off;
         if ((uint32_t)smem_max < off + 2 * slot) continue;
         int slots = (int)(((uint32_t)smem_max - off) / slot);
         if (slots > q4s::kMaxSlots) slots = q4s::kMaxSlots;
         p.slots = slots;
         p.slot_bytes = slot;
+        p.kv_slot_bytes = kv_slot;
         out->S = S;
         out->C = C;
         out->smem = (size_t)off + (size_t)slots * slot;

@@ -22,9 +22,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(HERE)
 sys.path.insert(0, ROOT)
 
-PHASES = ["layer start", "q item in", "q rows done", "q sent", "q block in", "o partial", "published",
-          "k, v done", "h' collected", "h' in", "ffn item in", "gate/up rows done", "act sent",
-          "act block in", "down partial", "published", "h collected", "h in"]
+PHASES = ["layer start", "q rows done", "q sent", "q block in", "o partial", "published", "h' collected",
+          "h' in", "gate/up rows done", "act sent", "act block in", "down partial", "published", "h collected",
+          "h in"]
 
 
 def build_traced() -> str:
