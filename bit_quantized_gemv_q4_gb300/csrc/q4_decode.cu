@@ -39,7 +39,7 @@ struct Layout {
     size_t params = 0;  // per-stage kernel parameters of the persistent launch
     // clustered step (M = 1 without attention): layer descriptors, tensor
     // maps, the partial-sum exchange and its counters
-    size_t step_layers = 0, step_maps = 0, xch = 0, step_ctr = 0, step_end = 0;
+    size_t step_layers = 0, step_maps = 0, xch = 0, htag = 0, step_ctr = 0, step_end = 0;
     // tagged copies of the activations that later stages read, and counters
     size_t h_t = 0, hm_t = 0, q_t = 0, act_t = 0, ctr = 0, tagged_begin = 0, total = 0;
 };
@@ -182,6 +182,7 @@ Layout layout_of(const Dims& d) {
         l.step_layers = take((size_t)d.L * step_layer_desc_bytes() / 2 + 1);
         l.step_maps = take((size_t)6 * d.L * sizeof(CUtensorMap) / 2);
         l.xch = take((size_t)2 * d.L * kStepMaxClusters * d.hidden * 4);
+        l.htag = take((size_t)d.L * d.hidden * 2);
         l.step_ctr = take(64);
         l.step_end = off;
     }
@@ -365,6 +366,7 @@ q4_status plan_fused(Plan& p, const uint16_t* x, cudaStream_t s) {
     a.v = reinterpret_cast<uint16_t*>(ws + p.lay.v);
     a.act = reinterpret_cast<uint16_t*>(ws + p.lay.act);
     a.xch = reinterpret_cast<unsigned long long*>(ws + p.lay.xch);
+    a.htag = reinterpret_cast<uint32_t*>(ws + p.lay.htag);
     a.ctr = reinterpret_cast<uint32_t*>(ws + p.lay.step_ctr);
     bool ok = false;
     q4_status st = step_plan(a, &p.step, &ok);

@@ -126,7 +126,9 @@ q4_status persistent_launch(const PersistentGeom& g, const void* dev_params, cud
 
 // ---- clustered decode step (q4_step.cu) ------------------------------------
 // The layer stack of an M = 1 decode step as one launch of thread-block
-// clusters (two grid-wide hand-offs per layer); lm_head is launched after it.
+// clusters (two grid-wide hand-offs per layer), beside it a launch that
+// computes the k and v rows on the SMs the clusters leave free; lm_head is
+// launched after them.
 constexpr int kStepMaxClusters = 20;  // the exchange buffer holds this many clusters' partials
 
 struct StepArgs {
@@ -138,13 +140,17 @@ struct StepArgs {
     const uint16_t* x = nullptr;
     uint16_t *h = nullptr, *h_mid = nullptr, *q = nullptr, *k = nullptr, *v = nullptr, *act = nullptr;
     unsigned long long* xch = nullptr;         // workspace: 2 L * kStepMaxClusters * H words
-    uint32_t* ctr = nullptr;                   // workspace: step and finished-CTA counters
+    uint32_t* htag = nullptr;                  // workspace: L * H tagged words (each layer's input h)
+    uint32_t* ctr = nullptr;                   // workspace: step and finished-CTA counters (5 words)
 };
 
 struct StepPlan {
     int S = 0, C = 0;  // cluster size and cluster count
     size_t smem = 0;
     alignas(64) unsigned char params[512];
+    int kv_grid = 0;   // the k / v launch
+    size_t kv_smem = 0;
+    alignas(64) unsigned char kv_params[256];
 };
 
 size_t step_layer_desc_bytes();

@@ -52,23 +52,23 @@ namespace q4s {
 // diagnostic build, bit_quantized_gemv_q4_gb300/trace_step.py).
 #ifdef Q4_STEP_TRACE
 __device__ unsigned long long g_step_trace[2 * 4096];
-#define Q4_TRACE(k)                                                                                  \
+#define Q4_TRACE_T(k, t)                                                                             \
     do {                                                                                             \
-        if (tid == 0 && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1) && l < 128)                  \
+        if (tid == (t) && (blockIdx.x == 0 || blockIdx.x == gridDim.x - 1) && l < 128)                \
             g_step_trace[(blockIdx.x ? 4096 : 0) + l * 32 + (k)] = q4d::globaltimer();                \
     } while (0)
 #else
-#define Q4_TRACE(k) \
-    do {            \
+#define Q4_TRACE_T(k, t) \
+    do {                 \
     } while (0)
 #endif
+#define Q4_TRACE(k) Q4_TRACE_T(k, 0)  // the consumers' points (0..14)
 
 constexpr int kWarps = 8;                        // consumer warps (the layer's critical path)
 constexpr int kCT = kWarps * 32;                 // consumer threads
-constexpr int kKvWarps = 4;                      // k / v warps (one per scheduler)
-constexpr int kProducerWarp = kWarps;            // then the k / v warps
-constexpr int kKvWarp0 = kWarps + 1;
-constexpr int kThreads = (kWarps + 1 + kKvWarps) * 32;
+constexpr int kProducerWarp = kWarps;            // streams the weight pieces
+constexpr int kThreads = (kWarps + 1) * 32;
+constexpr int kKvThreads = 256;                  // the k / v kernel's CTA
 constexpr int kMaxSlots = 16;
 constexpr int kItems = 4;                        // ring pieces per layer and CTA: q, o, gate/up, down
 
@@ -89,6 +89,7 @@ struct Params {
     const CUtensorMap* maps;   // device [L][6]: o codes, o scales, o biases, down codes, scales, biases
     const uint16_t* x;         // fp16 [H], input of layer 0
     uint16_t *h, *h_mid, *q, *k, *v, *act;  // fp16 outputs (the last layer's values remain)
+    uint32_t* htag;            // [L][H]: every layer's input h, tagged (fp16 | tag << 16), for the k / v kernel
     unsigned long long* xch;   // [2L][C][H]: (tag << 32) | fp32 partial
     uint32_t* ctr;             // [0] step counter, [1] CTAs finished
     int* err;
@@ -98,16 +99,33 @@ struct Params {
     int qspan, fspan;          // column-block widths in groups (largest cluster share)
     int qspan_s, fspan_s;      // scale / bias box widths in groups (multiples of 8)
     int slots;
-    uint32_t slot_bytes, kv_slot_bytes;
-    // shared memory: x of the attention half (two buffers, by layer parity,
-    // so the k / v warps may still read layer l's while layer l+1's arrives)
-    // and of the FFN half (fp32, lane-interleaved), their per-octet sums of
-    // squares (same three buffers), this CTA's h block and norm weights, row
-    // totals of the consumers and of the k / v warps, q / act blocks,
-    // partials (ro, then span x ro per group), barriers, the k / v ring (two
-    // slots), the ring
-    uint32_t off_xs, xs_bytes, off_nss, off_hown, off_gown, off_rows, off_kvrows, off_qx, off_ax, off_red, off_bar,
-        off_kvring, off_ring;
+    uint32_t slot_bytes;
+    // shared memory: x of the two halves (fp32, lane-interleaved), the
+    // cluster's block sums of squares of both halves ([2][S]), this CTA's
+    // octet sums of squares (layer 0's input: all of them), this CTA's h
+    // block and norm weights, row totals, q / act blocks, partials (ro, then
+    // span x ro per group), barriers, the ring
+    uint32_t off_xs, xs_bytes, off_bsum, off_nss, off_hown, off_gown, off_rows, off_qx, off_ax, off_red, off_bar,
+        off_ring;
+};
+
+// The k / v kernel: the k and v rows of every layer on the SMs the clusters
+// leave free.  It reads each layer's input h from the clustered kernel's
+// tagged copy and normalises it in that kernel's order, so its k and v are
+// the bits the clustered kernel would compute.
+struct KvParams {
+    const LayerDesc* layers;             // device [L]
+    const uint16_t* x;                   // fp16 [H], input of layer 0
+    uint16_t *k, *v;                     // fp16 outputs (the last layer's values remain)
+    const uint32_t* htag;                // the clustered kernel's tagged layer inputs [L][H]
+    uint32_t* ctr;                       // [0] clustered steps done, [3] k / v steps done, [4] k / v CTAs done
+    int* err;
+    int L, H, KVN, S, ro;
+    float eps;
+    uint32_t slot_bytes, xs_bytes;
+    // shared memory: h (fp16), x (fp32, lane-interleaved), octet sums of
+    // squares, row totals, barriers, a ring of two slots
+    uint32_t off_h, off_xs, off_nss, off_rows, off_bar, off_ring;
 };
 
 // [a, b) = part i of n split into `parts` nearly equal pieces.
@@ -457,20 +475,25 @@ __device__ __forceinline__ void publish(unsigned long long* X, const float* part
 
 // Collect every cluster's partials of this CTA's rows, add them in a fixed
 // order to the residual (this CTA's block of h, hown), round to fp16 -- the
-// new block, kept in hown and written to `out` from cluster 0 -- and, when a
-// next phase exists (gnext != nullptr), send every CTA of the cluster that
-// phase's input for these rows: x = h * norm weight in the dot_rows layout
-// (xs_next) and each octet's sum of squares (nss_next).  Warp w takes row
-// octets w, w + 8, ...; in an octet, lane = 8 rs + cc polls cluster cc (cc + 8,
-// ... when there are more than 8 clusters) of rows rs and rs + 4, the 8 lanes
-// of each row add by an xor tree.  Returns false when a poll expired.
+// new block, kept in hown and written to `out` (and tagged to `htag`) from
+// cluster 0 -- and, when a next phase exists (gnext != nullptr), send every
+// CTA of the cluster that phase's input for these rows: x = h * norm weight
+// in the dot_rows layout (xs_next), and this block's sum of squares (octets
+// in order, each octet's squares in order) into bsum_next[rank].  Warp w
+// takes row octets w, w + 8, ...; in an octet, lane = 8 rs + cc polls cluster
+// cc (cc + 8, ... when there are more than 8 clusters) of rows rs and rs + 4,
+// the 8 lanes of each row add by an xor tree.  Every consumer thread calls
+// this (it holds a barrier when gnext is set); `skip` (after a failed wait)
+// leaves out the polls, the writes and the sends.  Returns false when a poll
+// expired.
 __device__ __forceinline__ bool collect(const unsigned long long* X, uint16_t* hown, const uint16_t* gnext,
-                                     float4* xs_next, float* nss_next, uint16_t* out, int C, int H, int S, int oa,
-                                     int ro, uint32_t tag, uint32_t hbar, int* err) {
+                                        float4* xs_next, float* bsum_next, float* octss, uint16_t* out,
+                                        uint32_t* htag, uint32_t htag_tag, int C, int H, int S, int oa, int ro,
+                                        int rank, uint32_t tag, uint32_t hbar, int* err, bool skip) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int cc = lane & 7, rs = lane >> 3;
     bool ok = true;
-    for (int oc = warp; oc < ro / 8; oc += kWarps) {
+    for (int oc = warp; !skip && oc < ro / 8; oc += kWarps) {
         const int rA = 8 * oc + rs, rB = rA + 4;
         float vA = 0.f, vB = 0.f;
         for (int k = cc; k < C; k += 8) {
@@ -509,6 +532,10 @@ __device__ __forceinline__ bool collect(const unsigned long long* X, uint16_t* h
                 out[oa + rA] = __half_as_ushort(hA);
                 out[oa + rB] = __half_as_ushort(hB);
             }
+            if (htag) {
+                q4d::st_relaxed(htag + oa + rA, (htag_tag << 16) | __half_as_ushort(hA));
+                q4d::st_relaxed(htag + oa + rB, (htag_tag << 16) | __half_as_ushort(hB));
+            }
         }
         if (gnext) {
             // the octet's 8 values on every lane: rows 0..3 from lanes 0, 8, 16,
@@ -520,14 +547,16 @@ __device__ __forceinline__ bool collect(const unsigned long long* X, uint16_t* h
                 f[e] = __shfl_sync(0xffffffffu, fA, 8 * e);
                 f[4 + e] = __shfl_sync(0xffffffffu, fB, 8 * e);
             }
-            if (lane < S) {
+            if (lane == 0) {
                 float ss = 0.f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                octss[oc] = ss;
+            }
+            if (lane < S) {
                 float gm[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    ss = fmaf(f[e], f[e], ss);
-                    gm[e] = __half2float(__ushort_as_half(gnext[8 * oc + e]));
-                }
+                for (int e = 0; e < 8; ++e) gm[e] = __half2float(__ushort_as_half(gnext[8 * oc + e]));
                 const int j = (oa >> 3) + oc;
                 const uint32_t xs0 = q4d::smem_addr(xs_next + xs_slot(j));
                 const uint32_t rb = peer_addr(hbar, (uint32_t)lane);
@@ -541,37 +570,61 @@ __device__ __forceinline__ bool collect(const unsigned long long* X, uint16_t* h
                             make_uint4(__float_as_uint(p1.x), __float_as_uint(p1.y), __float_as_uint(p1.z),
                                        __float_as_uint(p1.w)),
                             rb);
-                st_async_b32(peer_addr(q4d::smem_addr(nss_next + j), (uint32_t)lane), __float_as_uint(ss), rb);
             }
+        }
+    }
+    if (gnext) {
+        // the block's sum of squares, to every CTA of the cluster
+        q4d::named_bar(1, kCT);
+        if (!skip && warp == 0 && lane < S) {
+            float t = 0.f;
+            for (int oc = 0; oc < ro / 8; ++oc) t += octss[oc];
+            st_async_b32(peer_addr(q4d::smem_addr(bsum_next + rank), (uint32_t)lane), __float_as_uint(t),
+                         peer_addr(hbar, (uint32_t)lane));
         }
     }
     return ok;
 }
 
-// Hand-off counters between the consumer warps and the k / v warps of a CTA
-// (shared memory, release / acquire at CTA scope).  A counter only grows, so a
-// waiter can never mistake a later hand-off for the one it waits for.
-__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
-    asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(q4d::smem_addr(p)), "r"(v) : "memory");
+// 1/rms from the S block sums of squares (the same order in every CTA).
+__device__ __forceinline__ float rinv_from(const float* bsum, int S, int H, float eps) {
+    float t = 0.f;
+    for (int b = 0; b < S; ++b) t += bsum[b];
+    return rsqrtf(t / (float)H + eps);
 }
-__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+
+// 16-bit tag of layer l's input h in step `step` (never 0, so zeroed words
+// never look current).
+__host__ __device__ inline uint32_t htag_of(uint32_t step, int L, int l) {
+    return 1u + (uint32_t)(((unsigned long long)step * (unsigned)L + (unsigned)l) % 65535ull);
+}
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     uint32_t v;
-    asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(q4d::smem_addr(p)) : "memory");
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
 }
-// Wait until *ctr >= target; false when the CTA aborted or the wait expired.
-__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, const volatile int* abort_flag,
-                                           int* err) {
-    if (ld_acquire_cta(ctr) >= target) return true;
-    const unsigned long long t0 = q4d::globaltimer();
-    while (true) {
-        __nanosleep(32);
-        if (ld_acquire_cta(ctr) >= target) return true;
-        if (*abort_flag) return false;
-        if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
-            atomicOr(err, q4d::kErrTimeout);
-            return false;
-        }
+
+// x * norm weight of one octet (8 inputs) in the dot_rows layout, and its sum
+// of squares: the one formula both kernels use for every layer's input.
+__device__ __forceinline__ void stage_octet(const float* f, const float* g, float4* xs, float* nss, int j) {
+    float ss = 0.f;
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+    nss[j] = ss;
+    float4* d = xs + xs_slot(j);
+    d[0] = make_float4(f[0] * g[0], f[4] * g[4], f[1] * g[1], f[5] * g[5]);
+    d[32] = make_float4(f[2] * g[2], f[6] * g[6], f[3] * g[3], f[7] * g[7]);
+}
+
+// Block sums of squares from all octet sums (block b = octets b ro/8 ..
+// (b+1) ro/8 - 1, in order), by threads 0 .. S-1: the order collect() uses.
+__device__ __forceinline__ void block_sums(const float* nss, float* bsum, int S, int ro) {
+    const int b = threadIdx.x;
+    if (b < S) {
+        float t = 0.f;
+        for (int oc = 0; oc < ro / 8; ++oc) t += nss[b * (ro / 8) + oc];
+        bsum[b] = t;
     }
 }
 
@@ -580,47 +633,33 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
     const int c = (int)cluster_index(), i = (int)cluster_rank();
     const int S = p.S, C = p.C, H = p.H, ro = p.ro, L = p.L;
-    // x of the attention half (by layer parity) and of the FFN half, and
-    // their octet sums of squares
-    auto xs0_of = [&](int l) { return reinterpret_cast<float4*>(smem + p.off_xs + (uint32_t)(l & 1) * p.xs_bytes); };
-    auto nss0_of = [&](int l) { return reinterpret_cast<float*>(smem + p.off_nss) + (l & 1) * (H / 8); };
-    float4* xs1 = reinterpret_cast<float4*>(smem + p.off_xs + 2 * p.xs_bytes);
-    float* nss1 = reinterpret_cast<float*>(smem + p.off_nss) + 2 * (H / 8);
+    // the k / v kernel may start once every CTA of this grid runs
+    q4d::pdl_trigger();
+    float4* xs0 = reinterpret_cast<float4*>(smem + p.off_xs);                 // attention half input
+    float4* xs1 = reinterpret_cast<float4*>(smem + p.off_xs + p.xs_bytes);    // FFN half input
+    float* bsum0 = reinterpret_cast<float*>(smem + p.off_bsum);               // their block sums of squares
+    float* bsum1 = bsum0 + S;
+    float* nss = reinterpret_cast<float*>(smem + p.off_nss);                  // octet sums of squares
     uint16_t* hown = reinterpret_cast<uint16_t*>(smem + p.off_hown);          // this CTA's block of h / h'
     uint16_t* gown = reinterpret_cast<uint16_t*>(smem + p.off_gown);          // [2L][ro] norm weights of that block
     float* rowout = reinterpret_cast<float*>(smem + p.off_rows);              // row totals of a row item
-    float* kvrows = reinterpret_cast<float*>(smem + p.off_kvrows);            // row totals of the k / v rows
     float* qx = reinterpret_cast<float*>(smem + p.off_qx);                    // the cluster's q block
     float* ax = reinterpret_cast<float*>(smem + p.off_ax);                    // the cluster's act block
     float* red = reinterpret_cast<float*>(smem + p.off_red);                  // [0, ro): this CTA's partials
     float* pg = red + ro;                                                     // per-group partials
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
     uint8_t* ring = smem + p.off_ring;
-    uint8_t* kvring = smem + p.off_kvring;
     const uint32_t full0 = q4d::smem_addr(bars), empty0 = q4d::smem_addr(bars + kMaxSlots);
     const uint32_t qbar = q4d::smem_addr(bars + 2 * kMaxSlots), abar = qbar + 8, hbar = qbar + 16;
-    const uint32_t kvfull0 = qbar + 24;  // two: the k / v slots
     const Work w = work_of(p.QN, p.KVN, p.F, C, S, c, i);
     const int oa = i * ro;
     const uint32_t q_bytes = 64u * (uint32_t)(w.qg1 - w.qg0) * 4u, a_bytes = 64u * (uint32_t)(w.fg1 - w.fg0) * 4u;
-    const uint32_t h_bytes = (uint32_t)(H / 8) * 36u;  // per octet: two float4 of x and a sum of squares
+    // per broadcast: two float4 of x per octet and every peer's block sum of squares
+    const uint32_t h_bytes = (uint32_t)(H / 8) * 32u + (uint32_t)S * 4u;
 
     __shared__ uint32_t step_sh;
-    __shared__ int issued_sh, consumed_sh, kv_issued_sh, kv_consumed_sh;
+    __shared__ int issued_sh, consumed_sh;
     __shared__ volatile int abort_sh;
-    // xrdy_sh: layers whose attention-half x is in place (consumers -> k / v
-    // warps); kvdone_sh: layers whose k / v rows are done (k / v warps ->
-    // consumers, who let peers overwrite that x buffer only afterwards)
-    __shared__ uint32_t xrdy_sh, kvdone_sh;
-    // The k / v warps also compute both norms' 1/rms for the consumers:
-    // nss1_sh counts layers whose FFN-half sums of squares are in place
-    // (consumers -> k / v warps), rinv_seq_sh the values published in
-    // rinv_sh (2l+1: attention half of layer l, 2l+2: its FFN half).
-    __shared__ uint32_t nss1_sh, rinv_seq_sh;
-    // pub_sh: layers whose attention-half partials are published; the k / v
-    // rows start then (the consumers only poll while the partials travel)
-    __shared__ uint32_t pub_sh;
-    __shared__ float rinv_sh[2];
     if (tid == 0) {
         for (int s = 0; s < p.slots; ++s) {
             q4d::mbar_init(full0 + 8 * s, 32);
@@ -629,25 +668,16 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         q4d::mbar_init(qbar, 1);
         q4d::mbar_init(abar, 1);
         q4d::mbar_init(hbar, 1);
-        q4d::mbar_init(kvfull0, 1);
-        q4d::mbar_init(kvfull0 + 8, 1);
         q4d::fence_mbar_init();
         step_sh = q4d::ld_relaxed(p.ctr);
         issued_sh = 0;
         consumed_sh = 0x7fffffff;
-        kv_issued_sh = 0;
-        kv_consumed_sh = 0;
         abort_sh = 0;
-        xrdy_sh = 1;
-        kvdone_sh = 0;
-        nss1_sh = 0;
-        rinv_seq_sh = 0;
-        pub_sh = 0;
     }
     // q / act blocks zeroed (their tails past the cluster's share stay zero,
     // so padded columns contribute nothing); the norm weights of this CTA's
     // rows for every layer (ones where a layer has none); this CTA's block of
-    // x; layer 0's input x * attn_norm and its octet sums of squares
+    // x; layer 0's input x * attn_norm and its block sums of squares
     for (int e = tid; e < p.qspan * 64; e += kThreads) qx[e] = 0.f;
     for (int e = tid; e < p.fspan * 64; e += kThreads) ax[e] = 0.f;
     for (int e = tid; e < 2 * L * ro; e += kThreads) {
@@ -658,38 +688,25 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
     for (int r = tid; r < ro; r += kThreads) hown[r] = p.x[oa + r];
     {
         const uint16_t* g0 = p.layers[0].attn_norm;
-        float4* xs = xs0_of(0);
-        float* nss = nss0_of(0);
         for (int j = tid; j < H / 8; j += kThreads) {
             float f[8], g[8];
-            const uint4 raw = *reinterpret_cast<const uint4*>(p.x + 8 * j);
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&wv[e]));
-                f[2 * e] = t.x;
-                f[2 * e + 1] = t.y;
-            }
-            float ss = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                ss = fmaf(f[e], f[e], ss);
+                f[e] = __half2float(__ushort_as_half(p.x[8 * j + e]));
                 g[e] = g0 ? __half2float(__ushort_as_half(g0[8 * j + e])) : 1.f;
             }
-            nss[j] = ss;
-            float4* d = xs + xs_slot(j);
-            d[0] = make_float4(f[0] * g[0], f[4] * g[4], f[1] * g[1], f[5] * g[5]);
-            d[32] = make_float4(f[2] * g[2], f[6] * g[6], f[3] * g[3], f[7] * g[7]);
+            stage_octet(f, g, xs0, nss, j);
         }
     }
     __syncthreads();
+    block_sums(nss, bsum0, S, ro);
     if (tid == 0) {
         // phase 0 of each exchange barrier: this thread's arrival plus the bytes peers send
         q4d::mbar_arrive_expect_tx(qbar, q_bytes);
         q4d::mbar_arrive_expect_tx(abar, a_bytes);
         q4d::mbar_arrive_expect_tx(hbar, h_bytes);
     }
-    cluster_sync();  // every peer's barriers are initialised before anything is sent
+    cluster_sync();  // every peer's barriers are initialised before anything is sent (and bsum0 is complete)
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------ producer warp
@@ -699,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         for (int l = 0; l < L && !abort_sh; ++l) {
             const LayerDesc& Ld = p.layers[l];
             for (int ii = 0; ii < kItems; ++ii, ++n) {
-                const int it = ii < 2 ? ii : ii + 1;  // item kinds 0, 1, 3, 4 (2 is the k / v rows)
+                const int it = ii < 2 ? ii : ii + 1;  // item kinds 0, 1, 3, 4 (2, the k / v rows, is not streamed here)
                 const int st = n % p.slots, k = n / p.slots;
                 if (k > 0) {
                     int ok = 1;
@@ -722,87 +739,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             }
         }
         if (lane == 0) issued_sh = n;
-    } else if (warp >= kKvWarp0) {
-        // ---------------------------------------------------- k / v warps
-        // Layer l's k and v rows, off the layer's critical path: they start
-        // once the attention half's partials are published and need only
-        // layer l's attention-half x, kept in its parity buffer until these
-        // warps are done with it.  Their weights come through a ring of two
-        // slots that these warps refill themselves.  These warps also compute
-        // both halves' 1/rms for the consumers.
-        const int kw = warp - kKvWarp0, ktid = tid - kKvWarp0 * 32;
-        const int nk = w.k1 - w.k0, nv = w.v1 - w.v0;
-        const RowItem ri = row_item(H, nk, nv);
-        const uint64_t pol = q4d::policy_evict_first();
-        auto issue_kv = [&](int l) {  // one thread
-            uint8_t* slot = kvring + (size_t)(l & 1) * p.kv_slot_bytes;
-            const uint32_t fb = kvfull0 + 8 * (l & 1);
-            const uint32_t bytes = issue_item(p, p.layers[l], p.maps + 6 * l, w, 2, i, slot, fb, false, pol);
-            q4d::mbar_arrive_expect_tx(fb, bytes);
-            issue_item(p, p.layers[l], p.maps + 6 * l, w, 2, i, slot, fb, true, pol);
-        };
-        int issued = L < 2 ? L : 2, done = 0;
-        if (ktid == 0)
-            for (int l = 0; l < issued; ++l) issue_kv(l);
-        // Each k / v warp thread waits on `ctr` reaching `target` through lane 0
-        // of its warp; false (every k / v thread alike) when the CTA aborted.
-        auto kv_wait = [&](const uint32_t* ctr, uint32_t target) -> bool {
-            int ok = 1;
-            if (lane == 0) ok = wait_count(ctr, target, &abort_sh, p.err) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (q4d::named_bar_or(2, kKvWarps * 32, !ok)) {
-                if (ktid == 0) abort_sh = 1;
-                return false;
-            }
-            return true;
-        };
-        for (int l = 0; l < L; ++l) {
-            // layer l's attention-half x and this layer's k / v weights
-            if (!kv_wait(&xrdy_sh, (uint32_t)(l + 1))) break;
-            int ok = 1;
-            if (lane == 0) ok = q4d::mbar_wait(kvfull0 + 8 * (l & 1), (l >> 1) & 1, p.err) ? 1 : 0;
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (q4d::named_bar_or(2, kKvWarps * 32, !ok)) {
-                if (ktid == 0) abort_sh = 1;
-                break;
-            }
-            const float rinv = rms_inv(nss0_of(l), H, p.eps, lane);
-            if (ktid == 0) {
-                rinv_sh[0] = rinv;
-                st_release_cta(&rinv_seq_sh, (uint32_t)(2 * l + 1));
-            }
-            // the k and v rows once the attention half's partials are out
-            if (!kv_wait(&pub_sh, (uint32_t)(l + 1))) break;
-            dot_rows<kKvWarps>(kvring + (size_t)(l & 1) * p.kv_slot_bytes, ri, nk, nv, H, xs0_of(l), kw, lane,
-                               kvrows);
-            q4d::named_bar(2, kKvWarps * 32);  // the slot and layer l's x are read
-            ++done;
-            if (ktid == 0) {
-                st_release_cta(&kvdone_sh, (uint32_t)(l + 1));
-                if (l + 2 < L) {
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    issue_kv(l + 2);
-                }
-            }
-            if (l + 2 < L) ++issued;
-            for (int r = ktid; r < nk + nv; r += kKvWarps * 32) {
-                const uint16_t hv = __half_as_ushort(__float2half_rn(kvrows[r] * rinv));
-                if (r < nk) p.k[w.k0 + r] = hv;
-                else p.v[w.v0 + r - nk] = hv;
-            }
-            // the FFN half's 1/rms once the consumers have its sums of squares
-            if (!kv_wait(&nss1_sh, (uint32_t)(l + 1))) break;
-            const float rinv2 = rms_inv(nss1, H, p.eps, lane);
-            if (ktid == 0) {
-                rinv_sh[1] = rinv2;
-                st_release_cta(&rinv_seq_sh, (uint32_t)(2 * l + 2));
-            }
-            q4d::named_bar(2, kKvWarps * 32);  // kvrows is free again
-        }
-        if (ktid == 0) {
-            kv_issued_sh = issued;
-            kv_consumed_sh = done;
-        }
     } else {
         // ---------------------------------------------------------- consumers
         const uint32_t step = step_sh;
@@ -812,8 +748,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         // so `bad` stays uniform within a warp (the warp-wide shuffles need
         // every lane); named_bar_or makes it uniform across the CTA.  A failed
         // or skipped wait returns nullptr and the item is not released (its
-        // copies may still be in flight).  Items are waited for ahead of the
-        // hand-off waits, so their arrival overlaps them.
+        // copies may still be in flight).  Items are waited for behind the
+        // hand-off waits (a completed-phase wait still costs a few hundred
+        // cycles), so that cost overlaps them.
         auto item_wait = [&](int& slot_idx) -> const uint8_t* {
             slot_idx = n % p.slots;
             int ok = 0;
@@ -841,18 +778,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             bad = q4d::named_bar_or(1, kCT, bad);
         };
 
-        // 1/rms of a half from the k / v warps (lane 0 waits, the warp shares it)
-        auto rinv_of = [&](uint32_t seq) -> float {
-            int ok = 0;
-            float r = 0.f;
-            if (lane == 0 && !bad) {
-                ok = wait_count(&rinv_seq_sh, seq, &abort_sh, p.err) ? 1 : 0;
-                r = rinv_sh[(seq - 1) & 1];
-            }
-            if (!__shfl_sync(0xffffffffu, ok, 0)) bad = true;
-            return __shfl_sync(0xffffffffu, r, 0);
-        };
-
         int sl = 0;
         const uint8_t* slot = item_wait(sl);  // layer 0's q rows
         for (int l = 0; l < L && !bad; ++l) {
@@ -863,8 +788,8 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             Q4_TRACE(0);
             const int nq = w.qb - w.qa;
             RowItem ri = row_item(H, nq, 0);
-            if (slot) dot_rows<kWarps>(slot, ri, nq, 0, H, xs0_of(l), warp, lane, rowout);
-            const float rinv = rinv_of((uint32_t)(2 * l + 1));
+            if (slot) dot_rows<kWarps>(slot, ri, nq, 0, H, xs0, warp, lane, rowout);
+            const float rinv = rinv_from(bsum0, S, H, p.eps);
             q4d::named_bar(1, kCT);
             Q4_TRACE(1);
             if (slot) item_done(sl);
@@ -895,15 +820,13 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             if (slot) item_done(sl);
             Q4_TRACE(4);
             publish(Xa, red, c, H, oa, ro, tag_of(2 * l));
-            if (tid == 0) st_release_cta(&pub_sh, (uint32_t)(l + 1));
             Q4_TRACE(5);
-            if (!bad && !collect(Xa, hown, gown + (size_t)(2 * l + 1) * ro, xs1, nss1, c == 0 ? p.h_mid : nullptr,
-                                 C, H, S, oa, ro, tag_of(2 * l), hbar, p.err))
+            if (!collect(Xa, hown, gown + (size_t)(2 * l + 1) * ro, xs1, bsum1, nss, c == 0 ? p.h_mid : nullptr,
+                         nullptr, 0, C, H, S, oa, ro, i, tag_of(2 * l), hbar, p.err, bad))
                 bad = true;
             Q4_TRACE(6);
             slot = item_wait(sl);  // gate / up rows
             wait_h(0);
-            if (tid == 0 && !bad) st_release_cta(&nss1_sh, (uint32_t)(l + 1));  // for the k / v warps' 1/rms
             Q4_TRACE(7);
             if (bad) break;
             // ---------------- FFN half: act = SiLU(gate) * up (sent to the
@@ -912,14 +835,9 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             const int nf = w.fb - w.fa;
             ri = row_item(H, nf, nf);
             if (slot) dot_rows<kWarps>(slot, ri, nf, nf, H, xs1, warp, lane, rowout);
-            const float rinv2 = rinv_of((uint32_t)(2 * l + 2));
-            // This layer's act lets peers reach the exchange that refills the
-            // attention-half x buffer of layer l - 1: the k / v warps must be
-            // done with it.
-            if (tid == 0 && l > 0 && !wait_count(&kvdone_sh, (uint32_t)l, &abort_sh, p.err)) bad = true;
-            bad = q4d::named_bar_or(1, kCT, bad);
+            const float rinv2 = rinv_from(bsum1, S, H, p.eps);
+            q4d::named_bar(1, kCT);
             Q4_TRACE(8);
-            if (bad) break;
             if (slot) item_done(sl);
             for (int idx = tid; idx < (nf / 4) * S; idx += kCT) {
                 const int r4 = idx / S, peer = idx - r4 * S;
@@ -951,15 +869,14 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
             publish(Xf, red, c, H, oa, ro, tag_of(2 * l + 1));
             const bool next = l + 1 < L;
             Q4_TRACE(12);
-            if (!bad && !collect(Xf, hown, next ? gown + (size_t)(2 * l + 2) * ro : nullptr, xs0_of(l + 1),
-                                 nss0_of(l + 1), c == 0 ? p.h : nullptr, C, H, S, oa, ro, tag_of(2 * l + 1), hbar,
-                                 p.err))
+            if (!collect(Xf, hown, next ? gown + (size_t)(2 * l + 2) * ro : nullptr, xs0, bsum0, nss,
+                         c == 0 ? p.h : nullptr, (c == 0 && next) ? p.htag + (size_t)(l + 1) * H : nullptr,
+                         htag_of(step, L, l + 1), C, H, S, oa, ro, i, tag_of(2 * l + 1), hbar, p.err, bad))
                 bad = true;
             Q4_TRACE(13);
             if (next) {
                 slot = item_wait(sl);  // the next layer's q rows
                 wait_h(1);
-                if (tid == 0 && !bad) st_release_cta(&xrdy_sh, (uint32_t)(l + 2));  // layer l+1's x is in place
             }
             Q4_TRACE(14);
         }
@@ -971,8 +888,6 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         // copies still landing in slots nobody will read (after an abort)
         for (int j = consumed_sh; j < issued_sh; ++j)
             q4d::mbar_wait(full0 + 8 * (j % p.slots), (j / p.slots) & 1, nullptr);
-        for (int j = kv_consumed_sh; j < kv_issued_sh; ++j)
-            q4d::mbar_wait(kvfull0 + 8 * (j & 1), (j >> 1) & 1, nullptr);
     }
     __syncthreads();
     cluster_sync();  // no CTA leaves while a peer may still write into its shared memory
@@ -980,7 +895,144 @@ __global__ void __launch_bounds__(kThreads, 1) q4_step_kernel(const __grid_const
         __threadfence();
         if (atomicAdd(p.ctr + 1, 1u) == gridDim.x - 1) {
             p.ctr[1] = 0;
+            __threadfence();
             atomicAdd(p.ctr, 1u);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- k / v kernel
+__global__ void __launch_bounds__(kKvThreads, 1) q4_step_kv_kernel(const __grid_constant__ KvParams p) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, tid = threadIdx.x;
+    const int H = p.H, L = p.L, S = p.S;
+    constexpr int NW = kKvThreads / 32;
+    uint16_t* h = reinterpret_cast<uint16_t*>(smem + p.off_h);  // the layer's input h
+    float4* xs = reinterpret_cast<float4*>(smem + p.off_xs);
+    float* nss = reinterpret_cast<float*>(smem + p.off_nss);
+    float* bsum = nss + H / 8;
+    float* rows = reinterpret_cast<float*>(smem + p.off_rows);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + p.off_bar);
+    uint8_t* ring = smem + p.off_ring;
+    const uint32_t full0 = q4d::smem_addr(bars);
+    // this CTA's rows of the k and v rows taken as one list
+    int a, b;
+    split(2 * p.KVN, (int)gridDim.x, (int)blockIdx.x, a, b);
+    const int k0 = a < p.KVN ? a : p.KVN, k1 = b < p.KVN ? b : p.KVN;
+    const int v0 = (a > p.KVN ? a : p.KVN) - p.KVN, v1 = (b > p.KVN ? b : p.KVN) - p.KVN;
+    const int nk = k1 - k0, nv = v1 - v0;
+    const RowItem ri = row_item(H, nk, nv);
+    __shared__ uint32_t step_sh;
+    if (tid == 0) {
+        q4d::mbar_init(full0, 1);
+        q4d::mbar_init(full0 + 8, 1);
+        q4d::fence_mbar_init();
+        step_sh = q4d::ld_relaxed(p.ctr + 3);  // this kernel's steps so far = the clustered kernel's step
+    }
+    __syncthreads();
+    const uint32_t step = step_sh;
+    const uint64_t pol = q4d::policy_evict_first();
+    auto issue = [&](int l) {  // one thread
+        const LayerDesc& Ld = p.layers[l];
+        uint8_t* slot = ring + (size_t)(l & 1) * p.slot_bytes;
+        const uint32_t fb = full0 + 8 * (l & 1);
+        const uint32_t bytes = (uint32_t)(nk + nv) * ((uint32_t)H / 2 + 2u * ((uint32_t)H / 32));
+        q4d::mbar_arrive_expect_tx(fb, bytes);
+        issue_rows(Ld.k, k0, nk, H, slot + ri.cA, slot + ri.sA, slot + ri.bA, fb, pol);
+        issue_rows(Ld.v, v0, nv, H, slot + ri.cB, slot + ri.sB, slot + ri.bB, fb, pol);
+    };
+    const int first = L < 2 ? L : 2;
+    if (tid == 0)
+        for (int l = 0; l < first; ++l) issue(l);
+    int issued = first, consumed = 0;
+    for (int l = 0; l < L; ++l) {
+        // layer l's input: the step's x, else the clustered kernel's tagged copy
+        if (l == 0) {
+            for (int j = tid; j < H; j += kKvThreads) h[j] = p.x[j];
+        } else {
+            const uint32_t tg = htag_of(step, L, l);
+            const uint32_t* src = p.htag + (size_t)l * H;
+            bool ok = true;
+            for (int j = 4 * tid; ok && j < H; j += 4 * kKvThreads) {
+                uint4 v = q4d::ld_relaxed_v4(src + j);
+                unsigned long long t0 = 0;
+                for (uint32_t it = 1; (v.x >> 16) != tg || (v.y >> 16) != tg || (v.z >> 16) != tg ||
+                                      (v.w >> 16) != tg;
+                     ++it) {
+                    if ((it & 15u) == 0) {
+                        if (t0 == 0) {
+                            t0 = q4d::globaltimer();
+                        } else if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
+                            atomicOr(p.err, q4d::kErrTimeout);
+                            ok = false;
+                            break;
+                        }
+                    }
+                    __nanosleep(256);  // this kernel trails the clusters: poll gently
+                    v = q4d::ld_relaxed_v4(src + j);
+                }
+                *reinterpret_cast<uint2*>(h + j) =
+                    make_uint2((v.x & 0xFFFFu) | (v.y << 16), (v.z & 0xFFFFu) | (v.w << 16));
+            }
+            if (__syncthreads_or(!ok)) break;
+        }
+        __syncthreads();
+        {
+            // x * attn_norm and the sums of squares, in the clustered kernel's order
+            const uint16_t* g = p.layers[l].attn_norm;
+            for (int j = tid; j < H / 8; j += kKvThreads) {
+                float f[8], gm[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    f[e] = __half2float(__ushort_as_half(h[8 * j + e]));
+                    gm[e] = g ? __half2float(__ushort_as_half(g[8 * j + e])) : 1.f;
+                }
+                stage_octet(f, gm, xs, nss, j);
+            }
+        }
+        __syncthreads();
+        block_sums(nss, bsum, S, p.ro);
+        __syncthreads();
+        Q4_TRACE_T(20, 0);
+        const float rinv = rinv_from(bsum, S, H, p.eps);
+        int ok = 0;
+        if (lane == 0) ok = q4d::mbar_wait(full0 + 8 * (l & 1), (l >> 1) & 1, p.err) ? 1 : 0;
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (__syncthreads_or(!ok)) break;
+        dot_rows<NW>(ring + (size_t)(l & 1) * p.slot_bytes, ri, nk, nv, H, xs, warp, lane, rows);
+        __syncthreads();  // the slot and x are read
+        ++consumed;
+        if (tid == 0 && l + 2 < L) {
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            issue(l + 2);
+        }
+        if (l + 2 < L) ++issued;
+        for (int r = tid; r < nk + nv; r += kKvThreads) {
+            const uint16_t hv = __half_as_ushort(__float2half_rn(rows[r] * rinv));
+            if (r < nk) p.k[k0 + r] = hv;
+            else p.v[v0 + r - nk] = hv;
+        }
+        Q4_TRACE_T(21, 0);
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // copies still landing in slots nobody will read (after an abort)
+        for (int j = consumed; j < issued; ++j) q4d::mbar_wait(full0 + 8 * (j & 1), (j >> 1) & 1, nullptr);
+        // The step ends when both kernels have: wait for the clustered kernel
+        // (it counts its finished steps), then count this CTA.
+        const unsigned long long t0 = q4d::globaltimer();
+        while (ld_acquire_gpu(p.ctr) < step + 1u) {
+            __nanosleep(256);
+            if (q4d::globaltimer() - t0 > q4d::kWaitLimitNs) {
+                atomicOr(p.err, q4d::kErrTimeout);
+                break;
+            }
+        }
+        __threadfence();
+        if (atomicAdd(p.ctr + 4, 1u) == gridDim.x - 1) {
+            p.ctr[4] = 0;
+            __threadfence();
+            atomicAdd(p.ctr + 3, 1u);
         }
     }
 }
@@ -1055,10 +1107,9 @@ q4_status step_plan(const StepArgs& a, StepPlan* out, bool* ok) {
         p.qspan_s = (qs + 7 + 7) & ~7;
         p.fspan_s = (fs + 7 + 7) & ~7;
         // slot size: the largest ring item of any CTA (q rows, gate/up rows,
-        // the column blocks) and the largest k / v item; the most rows each
-        // kind of row item has
-        uint32_t slot = 0, kv_slot = 0;
-        int max_rows = 0, max_kv_rows = 0;
+        // the column blocks); the most rows a row item has
+        uint32_t slot = 0;
+        int max_rows = 0;
         for (int cc = 0; cc < C; ++cc)
             for (int ii = 0; ii < S; ++ii) {
                 const q4s::Work w = q4s::work_of(QN, KVN, F, C, S, cc, ii);
@@ -1068,35 +1119,29 @@ q4_status step_plan(const StepArgs& a, StepPlan* out, bool* ok) {
                     slot = b > slot ? b : slot;
                     max_rows = r[0] + r[1] > max_rows ? r[0] + r[1] : max_rows;
                 }
-                const int nkv = (w.k1 - w.k0) + (w.v1 - w.v0);
-                const uint32_t b = q4s::row_item(H, w.k1 - w.k0, w.v1 - w.v0).gam;
-                kv_slot = b > kv_slot ? b : kv_slot;
-                max_kv_rows = nkv > max_kv_rows ? nkv : max_kv_rows;
             }
         const uint32_t co = q4s::col_item(p.ro, qs, p.qspan_s).end, cd = q4s::col_item(p.ro, fs, p.fspan_s).end;
         slot = co > slot ? co : slot;
         slot = cd > slot ? cd : slot;
         slot = q4s::align128(slot);
-        kv_slot = q4s::align128(kv_slot);
-        // fixed shared memory: x of the attention half (two parity buffers)
-        // and of the FFN half (fp32, lane-interleaved) and their octet sums of
-        // squares, this CTA's h block and norm weights, the row totals of the
-        // consumers and of the k / v warps, the q / act blocks, the partials,
-        // barriers, the two k / v slots
+        // fixed shared memory: x of both halves (fp32, lane-interleaved) and
+        // their block sums of squares, the octet sums of squares, this CTA's
+        // h block and norm weights, the row totals, the q / act blocks, the
+        // partials, barriers
         uint32_t off = 0;
         p.off_xs = off;
         p.xs_bytes = q4s::align128((uint32_t)((H / 8 + 127) / 128) * 8u * 32u * 16u);
-        off += 3 * p.xs_bytes;
+        off += 2 * p.xs_bytes;
+        p.off_bsum = off;
+        off += q4s::align128(2u * (uint32_t)S * 4u);
         p.off_nss = off;
-        off += q4s::align128(3u * (uint32_t)(H / 8) * 4u);
+        off += q4s::align128((uint32_t)(H / 8) * 4u);
         p.off_hown = off;
         off += q4s::align128((uint32_t)p.ro * 2u);
         p.off_gown = off;
         off += q4s::align128(2u * (uint32_t)L * (uint32_t)p.ro * 2u);
         p.off_rows = off;
         off += q4s::align128((uint32_t)max_rows * 4u);
-        p.off_kvrows = off;
-        off += q4s::align128((uint32_t)(max_kv_rows > 0 ? max_kv_rows : 1) * 4u);
         p.off_qx = off;
         off += q4s::align128((uint32_t)qs * 64u * 4u);
         p.off_ax = off;
@@ -1104,16 +1149,57 @@ q4_status step_plan(const StepArgs& a, StepPlan* out, bool* ok) {
         p.off_red = off;
         off += q4s::align128((uint32_t)(1 + (qs > fs ? qs : fs)) * (uint32_t)p.ro * 4u);
         p.off_bar = off;
-        off += q4s::align128((2 * q4s::kMaxSlots + 5) * 8u);
-        p.off_kvring = off;
-        off += 2 * kv_slot;
+        off += q4s::align128((2 * q4s::kMaxSlots + 3) * 8u);
         p.off_ring = off;
         if ((uint32_t)smem_max < off + 2 * slot) continue;
         int slots = (int)(((uint32_t)smem_max - off) / slot);
         if (slots > q4s::kMaxSlots) slots = q4s::kMaxSlots;
         p.slots = slots;
         p.slot_bytes = slot;
-        p.kv_slot_bytes = kv_slot;
+
+        // the k / v launch: one CTA on each SM the clusters leave free (at
+        // least 8; any that do not fit beside the clusters run after them)
+        q4s::KvParams kp = {};
+        kp.L = L;
+        kp.H = H;
+        kp.KVN = KVN;
+        kp.S = S;
+        kp.ro = p.ro;
+        kp.eps = a.eps;
+        const int G2 = dev->sms - C * S > 8 ? dev->sms - C * S : 8;
+        uint32_t kslot = 0;
+        int kmax = 0;
+        for (int bb = 0; bb < G2; ++bb) {
+            int ra, rb;
+            q4s::split(2 * KVN, G2, bb, ra, rb);
+            const int nk = (rb < KVN ? rb : KVN) - (ra < KVN ? ra : KVN);
+            const int nv = (rb > KVN ? rb : KVN) - (ra > KVN ? ra : KVN);
+            const uint32_t b2 = q4s::row_item(H, nk, nv).gam;
+            kslot = b2 > kslot ? b2 : kslot;
+            kmax = nk + nv > kmax ? nk + nv : kmax;
+        }
+        kp.slot_bytes = q4s::align128(kslot);
+        kp.xs_bytes = p.xs_bytes;
+        uint32_t ko = 0;
+        kp.off_h = ko;
+        ko += q4s::align128((uint32_t)H * 2u);
+        kp.off_xs = ko;
+        ko += kp.xs_bytes;
+        kp.off_nss = ko;  // the octet sums of squares, then the block sums
+        ko += q4s::align128((uint32_t)(H / 8 + S) * 4u);
+        kp.off_rows = ko;
+        ko += q4s::align128((uint32_t)(kmax > 0 ? kmax : 1) * 4u);
+        kp.off_bar = ko;
+        ko += 128;
+        kp.off_ring = ko;
+        ko += 2 * kp.slot_bytes;
+        if (ko > (uint32_t)smem_max) continue;
+        e = cudaFuncSetAttribute(q4s::q4_step_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)ko);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_step_kv_kernel)");
+        out->kv_grid = G2;
+        out->kv_smem = ko;
+        static_assert(sizeof(q4s::KvParams) <= sizeof(out->kv_params), "StepPlan k / v params storage");
+        memcpy(out->kv_params, &kp, sizeof(kp));
         out->S = S;
         out->C = C;
         out->smem = (size_t)off + (size_t)slots * slot;
@@ -1169,12 +1255,23 @@ q4_status step_bind(StepPlan* sp, const StepArgs& a, void* host_layers, void* ho
     p.v = a.v;
     p.act = a.act;
     p.xch = a.xch;
+    p.htag = a.htag;
     p.ctr = a.ctr;
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
     p.err = dev->err_word;
     memcpy(sp->params, &p, sizeof(p));
+    q4s::KvParams kp;
+    memcpy(&kp, sp->kv_params, sizeof(kp));
+    kp.layers = p.layers;
+    kp.x = a.x;
+    kp.k = a.k;
+    kp.v = a.v;
+    kp.htag = a.htag;
+    kp.ctr = a.ctr;
+    kp.err = dev->err_word;
+    memcpy(sp->kv_params, &kp, sizeof(kp));
     return Q4_OK;
 }
 
@@ -1191,10 +1288,32 @@ q4_status step_launch(const StepPlan& sp, cudaStream_t stream) {
     cfg.blockDim = dim3(q4s::kThreads);
     cfg.dynamicSmemBytes = sp.smem;
     cfg.stream = stream;
+    // cooperative: every cluster is resident at once (the clusters wait on
+    // one another), or the launch fails instead of waiting
+    at[1].id = cudaLaunchAttributeCooperative;
+    at[1].val.cooperative = 1;
     cfg.attrs = at;
-    cfg.numAttrs = 1;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, q4s::q4_step_kernel, p);
+    cfg.numAttrs = 2;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, q4s::q4_step_kernel, p);
     if (e != cudaSuccess) return cuda_fail(e, "clustered decode step launch");
+    // the k / v rows: launched once every clustered CTA runs (programmatic
+    // dependent launch; that kernel triggers at its start), on the free SMs;
+    // it reads only the exchange words, which it polls, and never waits on
+    // the clustered kernel's completion before its own end
+    q4s::KvParams kp;
+    memcpy(&kp, sp.kv_params, sizeof(kp));
+    cudaLaunchConfig_t kc = {};
+    cudaLaunchAttribute ka[1];
+    ka[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    ka[0].val.programmaticStreamSerializationAllowed = 1;
+    kc.gridDim = dim3((unsigned)sp.kv_grid);
+    kc.blockDim = dim3(q4s::kKvThreads);
+    kc.dynamicSmemBytes = sp.kv_smem;
+    kc.stream = stream;
+    kc.attrs = ka;
+    kc.numAttrs = 1;
+    e = cudaLaunchKernelEx(&kc, q4s::q4_step_kv_kernel, kp);
+    if (e != cudaSuccess) return cuda_fail(e, "clustered decode step k / v launch");
     return Q4_OK;
 }
 

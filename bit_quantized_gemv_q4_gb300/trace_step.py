@@ -5,7 +5,8 @@ points compiled in (-DQ4_STEP_TRACE, into _build_trace/), runs the
 Qwen3-0.6B-shaped decode step (M = 1, random Q4 weights drawn on the device)
 with Q4_DECODE_CLUSTERED, and prints, for the first and the last CTA of the
 grid, the median over layers 2..L-1 of the time between consecutive phase
-points of a layer.  The timestamps come from %globaltimer, so they include
+points of a layer (the consumer warps, the layer's critical path), and the
+k / v kernel's points as offsets from the layer's start.  The timestamps come from %globaltimer, so they include
 every wait; the per-step time is taken with CUDA events over 200 steps of
 the ordinary replay (the trace build writes a few extra global words)."""
 from __future__ import annotations
@@ -25,6 +26,9 @@ sys.path.insert(0, ROOT)
 PHASES = ["layer start", "q rows done", "q sent", "q block in", "o partial", "published", "h' collected",
           "h' in", "gate/up rows done", "act sent", "act block in", "down partial", "published", "h collected",
           "h in"]
+# the k / v kernel's first CTA (off the critical path), reported as offsets
+# from the clustered kernel's layer start
+SIDE_POINTS = {20: "k/v kernel: layer's x staged", 21: "k/v kernel: k, v rows stored"}
 
 
 def build_traced() -> str:
@@ -92,7 +96,9 @@ def main():
         for a in range(len(PHASES) - 1):
             d = [int(tr[l, a + 1] - tr[l, a]) for l in range(2, nl - 1)]
             phases[f"{PHASES[a]} -> {PHASES[a + 1]}"] = int(np.median(d))
-        out[name] = {"layer_ns_median": int(np.median(lay)), "phase_ns_median": phases}
+        side = {nm: int(np.median([tr[l, k] - tr[l, 0] for l in range(2, nl - 1)])) for k, nm in SIDE_POINTS.items()}
+        out[name] = {"layer_ns_median": int(np.median(lay)), "phase_ns_median": phases,
+                     "off_path_ns_after_layer_start": side}
     print(json.dumps(out, indent=1))
     t.release()
 

@@ -253,10 +253,14 @@ q4_status q4_gemv_bits(const uint32_t *Wq, const uint16_t *scales, const uint16_
  * With Q4_DECODE_CLUSTERED (M = 1, no attention, every layer of the same
  * shape, hidden, q.N and gate.N multiples of 512, and a device that holds at
  * least two 16- or 8-CTA clusters of one CTA per SM at once; otherwise the
- * flag is ignored) the layer stack is ONE launch of thread-block clusters and
- * lm_head a second launch: cluster c owns a block of whole 64-row groups of q
- * (and of act), its CTAs share those values through distributed shared
- * memory, and each CTA multiplies its rows of the matching column block of
+ * flag is ignored) the layer stack is ONE cooperative launch of thread-block
+ * clusters (all resident at once, or the call fails), the k and v rows a
+ * second launch on the SMs the clusters leave free (it rebuilds each layer's
+ * input from the clusters' exchange words, in their order, so k and v are the
+ * bits the clusters would compute), and lm_head a third: cluster c owns a
+ * block of whole 64-row groups of q (and of act), its CTAs share those
+ * values through distributed shared memory, and each CTA multiplies its
+ * rows of the matching column block of
  * Wo (Wdown); the clusters' partial sums meet in the workspace as 64-bit
  * words tagged with the step and the exchange, every cluster adds them in
  * the same fixed order and rounds h' (h) to fp16 as above -- two grid-wide
