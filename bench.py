@@ -5,13 +5,17 @@ fused QKV (1024 -> 2048+1024+1024), o (2048 -> 1024, + residual), fused
 gate/up (1024 -> 2x3072, SiLU*up), down (3072 -> 1024, + residual), then
 lm_head (1024 -> 151936); Q4 group-64 weights with fp16 scale and bias,
 synthetic and seeded (random-init of that shape; no trained weights).  One
-step = one decode token = one replay of the captured stream (113 kernels).
+step = one decode token = one replay of the captured stream: by default the
+clustered step (Q4_DECODE_CLUSTERED: the layer stack as one launch of
+thread-block clusters, the k / v rows beside it, then lm_head: 3 kernels),
+with `--decode-path per-stage` the 113 GEMV launches.
 
 Prints ONE JSON line (rank 0).  `value` is whole-job decode tok/s with the
 inputs resident in HBM; `e2e` is the same through the C ABI with the input
 vector copied in from pinned host memory and the logits copied out every step;
-`roofline` is the dominant kernel (the Q4 GEMV kernel: every launch of the
-step) against the measured HBM copy bandwidth; `cpu_baseline` is the fp64 CPU
+`roofline` is the step's kernels against the measured HBM copy bandwidth
+(algorithmic bytes per step / step time; the per-kernel shares are in the
+committed ncu launch list); `cpu_baseline` is the fp64 CPU
 oracle timed on the host cores on a bounded sample.  `--impl reference` times
 the oracle instead (the reference arm).
 
@@ -50,7 +54,7 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(path: str = "per-stage") -> str:
     """Hash of the GEMV kernel's code (q4_gemv.cu + q4_device.cuh) with
     comments and whitespace removed, so a comment edit keeps the recorded
     ncu traffic valid while any code change invalidates it.  The opt-in
@@ -58,9 +62,10 @@ def kernel_source_hash() -> str:
     comment to the failure-detection self-test, and its host planning and
     launch, from persistent_plan to the end of the file) is left out: the
     per-stage launches of q4_gemv_kernel that the traffic was measured on do
-    not run that code."""
+    not run that code.  For the clustered step the hash covers q4_step.cu too
+    (its two kernels and the lm_head GEMV run)."""
     h = hashlib.sha256()
-    for nm in ("q4_gemv.cu", "q4_device.cuh"):
+    for nm in (("q4_gemv.cu", "q4_device.cuh") + (("q4_step.cu",) if path == "clustered" else ())):
         with open(os.path.join(ROOT, "bit_quantized_gemv_q4_gb300", "csrc", nm), encoding="utf-8") as f:
             src = f.read()
         if nm == "q4_gemv.cu":
@@ -74,17 +79,22 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic():
-    """Per-launch DRAM bytes of the GEMV kernel from the committed ncu summary,
-    or None if it was taken with a different kernel source."""
-    path = os.path.join(ROOT, "profiles", "q4_gemv_decode_qwen3_0p6b_traffic.txt")
+TRAFFIC_FILES = {"per-stage": "q4_gemv_decode_qwen3_0p6b_traffic.txt",
+                 "clustered": "q4_step_decode_qwen3_0p6b_traffic.txt"}
+
+
+def recorded_traffic(path: str = "per-stage"):
+    """DRAM bytes per step and launches per step of the decode path from the
+    committed ncu summary, or None if it was taken with a different kernel
+    source."""
+    fn = os.path.join(ROOT, "profiles", TRAFFIC_FILES[path])
     try:
         kv = {}
-        for ln in open(path):
+        for ln in open(fn):
             if "=" in ln and not ln.startswith("#"):
                 k, v = ln.split("=", 1)
                 kv[k.strip()] = v.strip()
-        if kv.get("kernel_source_hash") != kernel_source_hash():
+        if kv.get("kernel_source_hash") != kernel_source_hash(path):
             return None
         return float(kv["dram_bytes_per_step"]), int(kv["launches_per_step"])
     except Exception:
@@ -554,10 +564,10 @@ def bits_lm_head(q4, device, widths=(2, 3, 5, 6)):
 
 
 def decode_clustered(q4, device, dl, dlm, shape, x, steps: int = 1000, warmup: int = 20):
-    """The same decode step with the clustered layer stack
-    (Q4_DECODE_CLUSTERED: one launch of thread-block clusters for the layers,
-    two grid-wide hand-offs per layer, then lm_head), device-resident, one
-    timed region of `steps` steps."""
+    """The same decode step through the clustered path (Q4_DECODE_CLUSTERED:
+    the layer stack as one launch of thread-block clusters with two grid-wide
+    hand-offs per layer, the k / v rows as a second launch on the free SMs,
+    then lm_head), device-resident, one timed region of `steps` steps."""
     import torch
     table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=1, flags=q4.Q4_DECODE_CLUSTERED)
     nws = q4.q4_decode_workspace_bytes(table)
@@ -597,6 +607,33 @@ def max_over_ranks(ms: float, world: int, device=None) -> float:
 def job_rate(world: int, tokens_per_rank_step: int, steps: int, ms_max: float) -> float:
     """Whole-job tokens per second: every rank decodes its own tokens."""
     return world * tokens_per_rank_step * steps / (ms_max / 1000.0)
+
+
+def decode_per_stage(q4, device, dl, dlm, shape, x, steps: int = 1000, warmup: int = 20):
+    """The same 0.6B-shaped step through the per-stage path (113 GEMV
+    launches per step, graph + PDL): context beside the clustered headline."""
+    import torch
+    table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=1)
+    nws = q4.q4_decode_workspace_bytes(table)
+    ws = torch.empty(nws, dtype=torch.uint8, device=device)
+    table.set_workspace(ws, nws)
+    lg = torch.empty(1, shape.vocab, dtype=torch.float32, device=device)
+    stream = torch.cuda.current_stream(device)
+    for _ in range(warmup):
+        q4.q4_decode_step(table, x, lg, stream)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(device)
+    e0.record(stream)
+    for _ in range(steps):
+        q4.q4_decode_step(table, x, lg, stream)
+    e1.record(stream)
+    torch.cuda.synchronize(device)
+    ms = e0.elapsed_time(e1) / steps
+    path = q4.q4_decode_path(table)
+    if q4.q4_device_status(stream) != 0:
+        raise RuntimeError("device status after the per-stage decode timing")
+    table.release()
+    return {"ms": ms, "tok_per_s": 1000.0 / ms, "path": path, "launches_per_step": 4 * shape.n_layers + 1}
 
 
 def single_gemv(q4, device, isolated: int = 50, replays: int = 5):
@@ -710,6 +747,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--decode-path", default="clustered", choices=["clustered", "per-stage"],
+                    help="the decode step's path: the clustered step (default; falls back to per-stage launches "
+                         "where it does not plan) or the per-stage GEMV launches")
     ap.add_argument("--section", default="all",
                     choices=["all", "decode", "moe", "lm_head", "prefill", "attention", "streams", "gemv",
                              "clustered"],
@@ -813,7 +853,8 @@ def main():
         print(json.dumps({"decode_clustered": decode_clustered(q4, device, dl, dlm, shape, xc, steps=args.steps,
                                                                warmup=args.warmup)}))
         return
-    table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M)
+    table = q4.LayerTable(dl, dlm, hidden=shape.hidden, M=M,
+                          flags=q4.Q4_DECODE_CLUSTERED if args.decode_path == "clustered" else 0)
     nws = q4.q4_decode_workspace_bytes(table)
     ws = torch.empty(nws, dtype=torch.uint8, device=device)
     table.set_workspace(ws, nws)
@@ -832,6 +873,12 @@ def main():
     st = q4.q4_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {st} after warm-up")
+    path_id = q4.q4_decode_path(table)
+    path = "clustered" if path_id == 3 else "per-stage"
+    launches_per_step = 3 if path == "clustered" else 4 * shape.n_layers + 1
+    config["path"] = ("clustered step: layer stack as one launch of 16-CTA clusters + k/v launch + lm_head "
+                      "GEMV (3 launches per step)" if path == "clustered" else
+                      f"per-stage GEMV launches ({launches_per_step} per step), graph + PDL")
 
     # ---- device-resident timed regions: each exactly K steps between a
     # barrier and a synchronisation on both sides, repeated until the regions
@@ -903,9 +950,8 @@ def main():
     reps_status = q4.q4_device_status(stream)
 
     peak, peak_kind = peaks()
-    launches_per_step = 4 * shape.n_layers + 1
     achieved = algo_bytes / (ms_per_step / 1000.0) / 1e9
-    tr = recorded_traffic()
+    tr = recorded_traffic(path)
     lm_bytes = shape.vocab * shape.hidden * 0.5625 + shape.hidden * 2 + shape.vocab * 4
     out = {
         "metric": METRIC, "value": value, "unit": "tok/s", "n_gpus": world, "steps": args.steps,
@@ -915,10 +961,13 @@ def main():
         "hbm_frac_of_nominal": achieved / NOMINAL_HBM_GBS,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_kind": peak_kind,
-                     "kernel": "q4_gemv_kernel<1> (all 113 launches of a step; achieved = algorithmic bytes "
-                               "per step / step time)",
-                     "traffic": (tr[0] / tr[1]) if tr else None,
-                     "algorithmic_bytes_per_launch": algo_bytes / launches_per_step},
+                     "kernel": ("q4_step_kernel + q4_step_kv_kernel + q4_gemv_kernel<1> (lm_head): the "
+                                "step's 3 launches; achieved = algorithmic bytes per step / step time"
+                                if path == "clustered" else
+                                "q4_gemv_kernel<1> (all 113 launches of a step; achieved = algorithmic bytes "
+                                "per step / step time)"),
+                     "traffic": tr[0] if tr else None, "traffic_unit": "DRAM bytes per step (ncu)",
+                     "algorithmic_bytes_per_step": algo_bytes},
         "lm_head_gemv": {"ms": lm_ms, "gbs": lm_bytes / (lm_ms / 1000.0) / 1e9 if lm_ms else None,
                          "frac": (lm_bytes / (lm_ms / 1000.0) / 1e9) / peak if lm_ms else None,
                          "shape": f"M={M} N={shape.vocab} K={shape.hidden}, 4 rotating copies"},
@@ -939,6 +988,7 @@ def main():
         out["dense_prefill"] = dense_prefill(device, dl, dlm, shape)
         out["decode_attention"] = decode_attention(device, dl, dlm, shape)
         out["decode_clustered"] = decode_clustered(q4, device, dl, dlm, shape, x)
+        out["decode_per_stage"] = decode_per_stage(q4, device, dl, dlm, shape, x)
         out["decode_streams"] = decode_streams(device)
         try:  # context only, measured last; the lines above stand if it fails
             out["single_gemv"] = single_gemv(q4, device)

@@ -1279,7 +1279,7 @@ q4_status step_launch(const StepPlan& sp, cudaStream_t stream) {
     q4s::Params p;
     memcpy(&p, sp.params, sizeof(p));
     cudaLaunchConfig_t cfg = {};
-    cudaLaunchAttribute at[2];
+    cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeClusterDimension;
     at[0].val.clusterDim.x = (unsigned)sp.S;
     at[0].val.clusterDim.y = 1;
@@ -1288,12 +1288,12 @@ q4_status step_launch(const StepPlan& sp, cudaStream_t stream) {
     cfg.blockDim = dim3(q4s::kThreads);
     cfg.dynamicSmemBytes = sp.smem;
     cfg.stream = stream;
-    // cooperative: every cluster is resident at once (the clusters wait on
-    // one another), or the launch fails instead of waiting
-    at[1].id = cudaLaunchAttributeCooperative;
-    at[1].val.cooperative = 1;
+    // The clusters wait on one another, so all of them must be resident at
+    // once: the plan sizes the grid by the occupancy query, the launch follows
+    // the previous step's kernels on the stream (the GPU is otherwise idle for
+    // it), and every cross-cluster wait is bounded.
     cfg.attrs = at;
-    cfg.numAttrs = 2;
+    cfg.numAttrs = 1;
     cudaError_t e = cudaLaunchKernelEx(&cfg, q4s::q4_step_kernel, p);
     if (e != cudaSuccess) return cuda_fail(e, "clustered decode step launch");
     // the k / v rows: launched once every clustered CTA runs (programmatic

@@ -253,8 +253,8 @@ q4_status q4_gemv_bits(const uint32_t *Wq, const uint16_t *scales, const uint16_
  * With Q4_DECODE_CLUSTERED (M = 1, no attention, every layer of the same
  * shape, hidden, q.N and gate.N multiples of 512, and a device that holds at
  * least two 16- or 8-CTA clusters of one CTA per SM at once; otherwise the
- * flag is ignored) the layer stack is ONE cooperative launch of thread-block
- * clusters (all resident at once, or the call fails), the k and v rows a
+ * flag is ignored) the layer stack is ONE launch of thread-block clusters
+ * (sized so that all of them are resident at once), the k and v rows a
  * second launch on the SMs the clusters leave free (it rebuilds each layer's
  * input from the clusters' exchange words, in their order, so k and v are the
  * bits the clusters would compute), and lm_head a third: cluster c owns a
