@@ -346,7 +346,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int ks0 = un.kp * p.ksteps, ks1 = ks0 + p.ksteps;
                 for (int ks = ks0; ks < ks1; ++ks, ++it) {
                     const int s = ip.s, a = ap.s;
-                    if (!wait_bar(sm, sm.in_full[s], ip.r & 1, p.err) || !wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
+                    // A stage a is complete only after every dequant warp has
+                    // waited for input stage s (codes and X land together on
+                    // in_full), so that one wait also covers the X tile: one
+                    // completed-phase wait costs ~200 cycles, and this thread
+                    // sets the pace of the K steps.
+                    if (!wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
                         ok = false;
                         break;
                     }
