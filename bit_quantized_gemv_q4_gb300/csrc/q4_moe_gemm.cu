@@ -47,10 +47,10 @@
 
 namespace q4g {
 
-constexpr int kTN = 128;          // tokens per unit (MMA N, max)
+constexpr int kTN = 128;          // tokens per unit at most (MMA N, max; the launch may take fewer)
 constexpr int kRows = 128;        // weight rows per unit (MMA M)
 constexpr int kKS = 64;           // K per step (one swizzle atom row of fp16, one Q4 group)
-constexpr int kMaxInStages = 8;   // codes + X ring (stage count set per launch)
+constexpr int kMaxInStages = 16;  // codes + X ring (stage count set per launch)
 constexpr int kMaxAStages = 4;    // dequantised A ring (stage count set per launch)
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
@@ -61,10 +61,10 @@ constexpr int kMaxExperts = 256;
 constexpr uint32_t kTmemCols = 512;   // 2 accumulator buffers x (gate + up) x 128 columns
 
 constexpr uint32_t kCodesBytes = kRows * 32;         // one matrix, one K step
-constexpr uint32_t kXBytes = kTN * kKS * 2;          // 16 KB
 constexpr uint32_t kATileBytes = kRows * kKS * 2;    // 16 KB
 // An input stage holds one K step's codes of each matrix, then X (at a
-// 1024-byte multiple, as the 128-byte swizzle needs): 20 KB plain, 24 KB GLU.
+// 1024-byte multiple, as the 128-byte swizzle needs): tn x 128 bytes of X, so
+// 20 KB plain and 24 KB GLU with 128-token units.
 // An A stage holds one dequantised tile per matrix: 16 KB plain, 32 KB GLU.
 
 struct Params {
@@ -77,6 +77,8 @@ struct Params {
     void* Y;
     int E, N, K, R, rows_e, up_off, nmat, glu, out_f16;
     int n_tiles, nK, G;
+    int tn;               // tokens per unit (32, 64 or 128): the X box rows
+    uint32_t x_bytes;     // X bytes per input stage (tn x 64 fp16)
     int kparts, ksteps;   // split of K over units (dense, few units): K steps per part
     float* part;          // kparts > 1: fp32 partials [kparts][nmat][R][N], reduced by reduce_parts_kernel
     int in_stages, a_stages;       // ring depths (the rest of shared memory, see launch_grouped)
@@ -199,8 +201,8 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int
     int a = p.offsets ? p.offsets[lo] : 0, b = p.offsets ? p.offsets[lo + 1] : p.R;
     a = max(0, min(a, p.R));
     b = max(a, min(b, p.R));
-    un.r0 = a + j * kTN;
-    un.tn = min(kTN, b - un.r0);
+    un.r0 = a + j * p.tn;
+    un.tn = min(p.tn, b - un.r0);
     un.nt = u % p.n_tiles;
     un.kp = kp;
     return un;
@@ -248,12 +250,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             q4d::mbar_init(q4d::smem_addr(&sm.a_empty[i]), p.nmat);
         }
         for (int i = 0; i < 2; ++i) {
-            q4d::mbar_init(q4d::smem_addr(&sm.acc_full[i]), p.nmat);
+            q4d::mbar_init(q4d::smem_addr(&sm.acc_full[i]), 2);  // both issuers commit
             q4d::mbar_init(q4d::smem_addr(&sm.acc_empty[i]), kEpiWarps);
         }
         q4d::mbar_init(q4d::smem_addr(&sm.sb_full), 1);
         q4d::mbar_init(q4d::smem_addr(&sm.sb_empty), kDeqWarps);
-        q4d::mbar_init(q4d::smem_addr(&sm.drain), p.nmat);
+        q4d::mbar_init(q4d::smem_addr(&sm.drain), 2);
         sm.abort = 0;
         q4d::fence_mbar_init();
     }
@@ -265,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 sm.prefix[e] = run;
                 int a = p.offsets ? max(0, min(p.offsets[e], p.R)) : 0;
                 int b = p.offsets ? max(a, min(p.offsets[e + 1], p.R)) : p.R;
-                run += (b - a + kTN - 1) / kTN;
+                run += (b - a + p.tn - 1) / p.tn;
             }
             sm.prefix[p.E] = run;
             sm.total_units = run * p.n_tiles * p.kparts;
@@ -313,7 +315,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ip.r > 0 && !wait_bar(sm, sm.in_empty[s], (ip.r - 1) & 1, p.err)) break;
                     uint8_t* st = in_ring + (size_t)s * p.in_bytes;
                     const uint32_t fb = q4d::smem_addr(&sm.in_full[s]);
-                    q4d::mbar_arrive_expect_tx(fb, p.nmat * kCodesBytes + kXBytes);
+                    q4d::mbar_arrive_expect_tx(fb, p.nmat * kCodesBytes + p.x_bytes);
                     tma_load_2d(q4d::smem_addr(st), &tmW, ks * 32, wrow, fb);
                     if (p.glu) tma_load_2d(q4d::smem_addr(st + kCodesBytes), &tmWu, ks * 32, wrow_u, fb);
                     tma_load_2d(q4d::smem_addr(st + p.x_off), &tmX, ks * kKS, un.r0, fb);
@@ -329,10 +331,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp == 1 || warp == kUpMmaWarp) {
         // ------------------------------------------------------------ MMA
-        // matrix mi of the unit (0: the plain matrix or gate, 1: up)
-        const int mi = warp == 1 ? 0 : 1;
-        if (lane == 0 && mi < p.nmat) {
-            int it = 0, acc_it = 0;
+        // Two issuing threads (one tcgen05.mma takes ~70 ns to issue, so one
+        // thread would set the pace).  GLU: issuer r owns matrix r (gate, up)
+        // for every K step.  Plain: both own the one matrix, issuer r the K
+        // steps of parity r of each unit, into an accumulator of its own (the
+        // columns the up matrix has in GLU mode); the epilogue adds the two.
+        const int r = warp == 1 ? 0 : 1;
+        const int mi = p.glu ? r : 0;
+        if (lane == 0) {
+            int acc_it = 0;
             RingPos ip, ap;
             for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++acc_it) {
                 const Unit un = decode_unit(sm, p, u);
@@ -341,33 +348,32 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int buf = acc_it & 1;
                 if (acc_it >= 2 && !wait_bar(sm, sm.acc_empty[buf], ((acc_it >> 1) - 1) & 1, p.err)) break;
                 tc_fence_after();
-                const uint32_t d0 = tmem + (uint32_t)(buf * 2 * kTN);
-                bool ok = true;
+                const uint32_t dm = tmem + (uint32_t)(buf * 2 * kTN) + (uint32_t)(r * kTN);
+                bool ok = true, first = true;
                 const int ks0 = un.kp * p.ksteps, ks1 = ks0 + p.ksteps;
-                for (int ks = ks0; ks < ks1; ++ks, ++it) {
+                for (int ks = ks0; ks < ks1; ++ks) {
                     const int s = ip.s, a = ap.s;
-                    // A stage a is complete only after every dequant warp has
-                    // waited for input stage s (codes and X land together on
-                    // in_full), so that one wait also covers the X tile: one
-                    // completed-phase wait costs ~200 cycles, and this thread
-                    // sets the pace of the K steps.
-                    if (!wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t xs = q4d::smem_addr(in_ring + (size_t)s * p.in_bytes + p.x_off);
-                    const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
-                    {
+                    if (p.glu || ((ks - ks0) & 1) == r) {
+                        // A stage a is complete only after every dequant warp
+                        // has waited for input stage s (codes and X land
+                        // together on in_full), so that one wait also covers
+                        // the X tile: a completed-phase wait costs ~200 cycles.
+                        if (!wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t xs = q4d::smem_addr(in_ring + (size_t)s * p.in_bytes + p.x_off);
+                        const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
                         // K-chunk kk advances both descriptors' start address by 32 bytes
                         const uint64_t ad = sw128_desc(as + mi * kATileBytes), xd = sw128_desc(xs);
-                        const uint32_t dm = d0 + (uint32_t)(mi * kTN);
 #pragma unroll
                         for (int kk = 0; kk < kKS / 16; ++kk)
-                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (ks > ks0 || kk > 0) ? 1u : 0u);
+                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                        first = false;
+                        mma_commit(q4d::smem_addr(&sm.in_empty[s]));
+                        mma_commit(q4d::smem_addr(&sm.a_empty[a]));
                     }
-                    mma_commit(q4d::smem_addr(&sm.in_empty[s]));
-                    mma_commit(q4d::smem_addr(&sm.a_empty[a]));
                     ip.next(IS);
                     ap.next(AS);
                 }
@@ -468,11 +474,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             const int n = un.nt * kRows + row;
             const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * kTN);
+            // plain mode: the second issuer's accumulator holds the odd K steps
+            const bool two = p.glu || p.ksteps >= 2;
             for (int c0 = 0; c0 < un.tn; c0 += 16) {
                 uint32_t g[16], v[16];
                 tmem_ld16(t0 + c0, g);
-                if (p.glu) tmem_ld16(t0 + kTN + c0, v);
+                if (two) tmem_ld16(t0 + kTN + c0, v);
                 tmem_ld_wait();
+                if (!p.glu && two) {
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) g[c] = __float_as_uint(__uint_as_float(g[c]) + __uint_as_float(v[c]));
+                }
 #pragma unroll
                 for (int c = 0; c < 16; ++c) {
                     if (c0 + c < un.tn) {
@@ -505,10 +517,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // Wind down: every role has left its loop (all waits are bounded).  The
     // last accumulator hand-off already waited for all issued MMAs; on abort
-    // give in-flight tensor-core work a bounded moment via one more commit.
+    // give in-flight tensor-core work a bounded moment via one more commit
+    // from each issuer.
     tc_fence_before();
     __syncthreads();
-    if (warp == kUpMmaWarp && sm.abort && p.nmat == 2) {
+    if (warp == kUpMmaWarp && sm.abort) {
         if (lane == 0) {
             // completes once every MMA of both issuers has finished
             mma_commit(q4d::smem_addr(&sm.drain));
@@ -686,20 +699,30 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
     p.err = dev->err_word;
 
-    // Rings: whatever shared memory the scale/bias buffers leave, A ring up to
-    // 4 stages (3 in GLU mode, whose stages are twice the size), input ring
-    // up to 8; at least 2 of each.
+    // Rings: an A ring of 3 stages (2 in GLU mode, whose stages are twice the
+    // size), which turn over in a few hundred ns, and an input ring as deep as
+    // the rest of shared memory allows (up to 16): an input stage waits ~1 us
+    // for its codes, so its depth sets the K-step rate; at least 2 of each.
+    // Tokens per unit: a routed launch with few rows per expert takes a
+    // smaller X box, so its input stages are smaller and the ring deeper (an
+    // expert with more rows than that takes more units).
+    p.tn = q4g::kTN;
+    if (a.offsets) {
+        const long long avg = ((long long)a.R + a.E - 1) / a.E;
+        p.tn = avg <= 16 ? 32 : avg <= 48 ? 64 : q4g::kTN;
+    }
+    p.x_bytes = (uint32_t)p.tn * q4g::kKS * 2u;
     p.x_off = (uint32_t)p.nmat * q4g::kCodesBytes;
-    p.in_bytes = p.x_off + q4g::kXBytes;
+    p.in_bytes = p.x_off + p.x_bytes;
     p.a_bytes = (uint32_t)p.nmat * q4g::kATileBytes;
     const size_t fixed = 1024 + (size_t)p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
     const size_t avail = (size_t)dev->smem_optin > fixed ? (size_t)dev->smem_optin - fixed : 0;
-    int as = glu ? 3 : q4g::kMaxAStages, is = 0;
+    int as = glu ? 2 : 3, is = 0;
     for (; as >= 2; --as) {
         const size_t left = avail > (size_t)as * p.a_bytes ? avail - (size_t)as * p.a_bytes : 0;
         is = (int)(left / p.in_bytes);
         if (is > q4g::kMaxInStages) is = q4g::kMaxInStages;
-        if (is >= 4 || (as == 2 && is >= 2)) break;
+        if (is >= 4 || as == 2) break;
     }
     if (as < 2 || is < 2)
         return fail(Q4_ERR_UNSUPPORTED, "K=%d: its scale/bias buffers leave no room for two pipeline stages", a.K);
@@ -719,7 +742,7 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
         if (st != Q4_OK) return st;
     }
     st = make_map(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, a.X, (uint64_t)a.K, (uint64_t)a.R, (uint64_t)a.K * 2,
-                  q4g::kKS, q4g::kTN, CU_TENSOR_MAP_SWIZZLE_128B);
+                  q4g::kKS, (uint32_t)p.tn, CU_TENSOR_MAP_SWIZZLE_128B);
     if (st != Q4_OK) return st;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

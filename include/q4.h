@@ -423,7 +423,9 @@ typedef struct q4_moe_desc {
  * N must be a multiple of 128 (else Q4_ERR_UNSUPPORTED); Wq, scales, biases
  * and X must be 16-byte aligned (else Q4_ERR_MISALIGNED); a K whose scale/bias
  * buffers leave no room for two pipeline stages in shared memory (with 227 KB
- * per block: K above 3520 in GLU mode, 6464 in PLAIN mode) returns
+ * per block and 128-token units: K above 3520 in GLU mode, 6464 in PLAIN mode;
+ * launches with at most 48 routed rows per expert on average take 64- or
+ * 32-token units, whose smaller stages admit somewhat larger K) returns
  * Q4_ERR_UNSUPPORTED. */
 q4_status q4_moe_gemm(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                       const uint16_t *X, const int32_t *expert_ids, const int32_t *offsets,

@@ -108,8 +108,20 @@ def test_largest_k(mode, K):
         check_plain(W, X, eids, Y, fp16_out=True, what=f"plain K={K}")
 
 
+def test_few_tokens_per_expert_fit_a_larger_k():
+    """Few routed rows per expert take 32-token units, whose smaller X boxes
+    leave room for the scale/bias buffers of a K that 128-token units cannot
+    hold (3584 in GLU mode)."""
+    n_out, K, counts = 128, 3584, [2, 5, 0, 9]
+    W = q4synth.q4_matrix(370, 2 * n_out, K, experts=len(counts))
+    X = q4synth.activations(371, sum(counts), K)
+    Y, eids = run_gemm(W, X, counts, n_out, K, q4.Q4_GEMV_GLU, q4.Q4_F16)
+    check_glu(W, X, eids, Y, n_out, what=f"GLU K={K}, 32-token units")
+
+
 def test_k_beyond_shared_memory_is_refused():
-    E, N, K, R = 1, 128, 3584, 1
+    """128-token units (64 rows for one expert) at K = 3584 in GLU mode."""
+    E, N, K, R = 1, 128, 3584, 64
     Wq = torch.zeros(E, 2 * N, K // 8, dtype=torch.int32, device="cuda")
     s = torch.zeros(E, 2 * N, K // 64, dtype=torch.float16, device="cuda")
     X = torch.zeros(R, K, dtype=torch.float16, device="cuda")
