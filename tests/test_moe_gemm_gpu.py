@@ -217,9 +217,15 @@ def test_qwen3_30b_a3b_layer_sampled_rows(moe, T):
     r = oracle.moe_route(g["logits"], SHAPE.topk)
     assert np.array_equal(g["off"], r["offsets"]) and np.array_equal(g["tok"], r["token_of"])
     assert np.array_equal(g["Xs"].view(np.uint16), g["X"][g["tok"]].view(np.uint16))
-    rows = np.unique(np.random.default_rng(T).integers(0, T * SHAPE.topk, 24))
+    # the first and the last routed row of every expert that has rows (unit and
+    # token-tile edges), and 96 more at random
+    R = T * SHAPE.topk
+    off = g["off"]
+    nonempty = np.nonzero(off[1:] > off[:-1])[0]
+    edges = np.concatenate([off[nonempty], off[nonempty + 1] - 1])
+    rows = np.unique(np.concatenate([edges, np.random.default_rng(T).integers(0, R, 96)]))
     check_glu(gu, g["Xs"].astype(np.float16), g["eid"], g["H"], SHAPE.ffn, rows=rows, what=f"gate/up T={T}")
-    check_plain(dn, g["H"].astype(np.float16), g["eid"], g["Y"], rows=rows[:12], what=f"down T={T}")
+    check_plain(dn, g["H"].astype(np.float16), g["eid"], g["Y"], rows=rows, what=f"down T={T}")
 
 
 def test_qwen3_30b_a3b_layer_end_to_end_small_T(moe):
