@@ -56,9 +56,9 @@ constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kUpMmaWarp = 2 + kDeqWarps + kEpiWarps;  // 14
 constexpr int kThreads = (kUpMmaWarp + 1) * 32;
-constexpr int kDeqThreads = kDeqWarps * 32;
 constexpr int kMaxExperts = 256;
-constexpr uint32_t kTmemCols = 512;   // 2 accumulator buffers x (gate + up) x 128 columns
+constexpr uint32_t kTmemCols = 512;   // 2 accumulator buffers x 2 accumulators x 128 columns; with
+                                      // units of <= 64 tokens: 2 x 2 x tn, and A stages from column 256
 
 constexpr uint32_t kCodesBytes = kRows * 32;         // one matrix, one K step
 constexpr uint32_t kATileBytes = kRows * kKS * 2;    // 16 KB
@@ -79,6 +79,9 @@ struct Params {
     int n_tiles, nK, G;
     int tn;               // tokens per unit (32, 64 or 128): the X box rows
     uint32_t x_bytes;     // X bytes per input stage (tn x 64 fp16)
+    int a_tmem;           // dequantised A tiles in tensor memory (units of <= 64 tokens) instead of shared memory
+    uint32_t acc_cols;    // TMEM columns of one accumulator (tn in TMEM-A mode, else 128)
+    uint32_t a_col0;      // TMEM column of the first A stage (TMEM-A mode)
     int kparts, ksteps;   // split of K over units (dense, few units): K steps per part
     float* part;          // kparts > 1: fp32 partials [kparts][nmat][R][N], reduced by reduce_parts_kernel
     int in_stages, a_stages;       // ring depths (the rest of shared memory, see launch_grouped)
@@ -133,6 +136,39 @@ __device__ __forceinline__ void mma_f16(uint32_t d_tmem, uint64_t a, uint64_t b,
         "l"(a), "l"(b), "r"(idesc), "r"(acc)
         : "memory");
 }
+
+// The same with A in tensor memory (M = 128 lanes, two fp16 K values per
+// 32-bit column) and B by descriptor.
+__device__ __forceinline__ void mma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                               uint32_t acc) {
+    asm volatile(
+        "{ .reg .pred p; setp.ne.b32 p, %4, 0; tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(
+            d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// 16 / 32 consecutive 32-bit TMEM columns of this thread's lane (the warp's
+// lane quarter is in taddr).
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]),
+        "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]),
+        "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
@@ -225,6 +261,10 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t q, __half2 s2, __half2 b2
     return make_uint4(prmt(a0, a1, 0x5410), prmt(a2, a3, 0x5410), prmt(a0, a1, 0x7632), prmt(a2, a3, 0x7632));
 }
 
+// kATmem: the dequantised A tiles live in tensor memory (units of <= 64
+// tokens), else in shared memory; one instantiation per mode keeps each
+// role's loop free of the other's code and registers.
+template <bool kATmem>
 __global__ void __launch_bounds__(kThreads, 1)
     q4_moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
                        const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Params p) {
@@ -348,7 +388,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int buf = acc_it & 1;
                 if (acc_it >= 2 && !wait_bar(sm, sm.acc_empty[buf], ((acc_it >> 1) - 1) & 1, p.err)) break;
                 tc_fence_after();
-                const uint32_t dm = tmem + (uint32_t)(buf * 2 * kTN) + (uint32_t)(r * kTN);
+                const uint32_t dm = tmem + (uint32_t)(buf * 2 + r) * p.acc_cols;
                 bool ok = true, first = true;
                 const int ks0 = un.kp * p.ksteps, ks1 = ks0 + p.ksteps;
                 for (int ks = ks0; ks < ks1; ++ks) {
@@ -364,12 +404,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         tc_fence_after();
                         const uint32_t xs = q4d::smem_addr(in_ring + (size_t)s * p.in_bytes + p.x_off);
-                        const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
-                        // K-chunk kk advances both descriptors' start address by 32 bytes
-                        const uint64_t ad = sw128_desc(as + mi * kATileBytes), xd = sw128_desc(xs);
+                        // K-chunk kk advances the X descriptor's start address by 32 bytes
+                        const uint64_t xd = sw128_desc(xs);
+                        if constexpr (kATmem) {
+                            // 16 fp16 of K = 8 TMEM columns
+                            const uint32_t at = tmem + p.a_col0 + (uint32_t)(a * 2 + mi) * 32u;
 #pragma unroll
-                        for (int kk = 0; kk < kKS / 16; ++kk)
-                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                            for (int kk = 0; kk < kKS / 16; ++kk)
+                                mma_f16_tmem_a(dm, at + 8 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                        } else {
+                            const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
+                            const uint64_t ad = sw128_desc(as + mi * kATileBytes);
+#pragma unroll
+                            for (int kk = 0; kk < kKS / 16; ++kk)
+                                mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                        }
                         first = false;
                         mma_commit(q4d::smem_addr(&sm.in_empty[s]));
                         mma_commit(q4d::smem_addr(&sm.a_empty[a]));
@@ -383,14 +432,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else if (warp < 2 + kDeqWarps) {
         // ------------------------------------------------------------ dequant
-        // Thread dt owns weight row `row` of the tile: in GLU mode matrix
-        // `part` (gate or up), in plain mode words 4*part..4*part+3 of each
-        // 8-word K step.  Its scales/biases live in private shared slots (no
-        // cross-thread sharing, so no barrier that an aborting warp could
-        // leave the others waiting on).
-        const int dt = threadIdx.x - 64;          // 0..255
-        const int row = dt & (kRows - 1);
-        const int part = dt >> 7;
+        // Thread dt owns weight row `row` of the tile -- the TMEM lane its warp
+        // may write, 32 (warp % 4) + lane -- and half `part` of the row's 16
+        // (GLU: gate then up) or 8 (plain) words of each K step: in GLU mode
+        // all 8 words of matrix `part`, in plain mode words 4 part .. 4 part + 3.
+        // Its scales/biases live in private shared slots (no cross-thread
+        // sharing, so no barrier that an aborting warp could leave the others
+        // waiting on).
+        const int dt = threadIdx.x - 64;          // 0 .. 255
+        const int row = 32 * (warp & 3) + lane;
+        const int part = (warp - 2) >> 2;         // 0 or 1
         const int m = p.glu ? part : 0;
         const int G = p.G, Gp = G + 1;
         uint32_t* my_sb = sb + (size_t)dt * Gp;
@@ -432,23 +483,58 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* st = in_ring + (size_t)s * p.in_bytes;
                 uint8_t* at = a_ring + (size_t)a * p.a_bytes;
-                const int w0 = p.glu ? 0 : part * 4, nw = p.glu ? 8 : 4;
+                const int w0 = p.glu ? 0 : 4 * part, nw = p.glu ? 8 : 4;
                 const uint32_t sbv = my_sb[ks];
                 const __half sh = __ushort_as_half((uint16_t)(sbv & 0xFFFF));
                 const __half bh = __ushort_as_half((uint16_t)(sbv >> 16));
                 const __half2 s2 = __halves2half2(sh, sh), b2 = __halves2half2(bh, bh);
                 const uint4* cw = reinterpret_cast<const uint4*>(st + m * kCodesBytes + row * 32);
-                uint8_t* arow = at + m * kATileBytes + (row >> 3) * 1024 + (row & 7) * 128;
-                for (int h = 0; h < nw / 4; ++h) {
-                    const uint4 c = cw[(w0 >> 2) + h];
-                    const uint32_t words[4] = {c.x, c.y, c.z, c.w};
-#pragma unroll
-                    for (int wi = 0; wi < 4; ++wi) {
-                        const int j = w0 + h * 4 + wi;   // 16-byte chunk = 8 consecutive k
-                        *reinterpret_cast<uint4*>(arow + ((j ^ (row & 7)) << 4)) = dequant_word(words[wi], s2, b2);
+                if constexpr (kATmem) {
+                    // the row's fp16 weights in k order, two per 32-bit column
+                    // of its TMEM lane: matrix m of A stage a
+                    tc_fence_after();  // the MMAs that read this A stage before are complete
+                    uint32_t v[32];
+                    const uint32_t* cw32 = reinterpret_cast<const uint32_t*>(cw) + w0;
+                    uint32_t words[8];
+                    {
+                        const uint4 c = *reinterpret_cast<const uint4*>(cw32);
+                        words[0] = c.x; words[1] = c.y; words[2] = c.z; words[3] = c.w;
                     }
+                    if (nw == 8) {
+                        const uint4 c = *reinterpret_cast<const uint4*>(cw32 + 4);
+                        words[4] = c.x; words[5] = c.y; words[6] = c.z; words[7] = c.w;
+                    } else {
+                        words[4] = words[5] = words[6] = words[7] = 0;
+                    }
+#pragma unroll
+                    for (int wi = 0; wi < 8; ++wi) {
+                        if (wi < nw) {
+                            const uint4 d = dequant_word(words[wi], s2, b2);
+                            v[4 * wi + 0] = d.x;
+                            v[4 * wi + 1] = d.y;
+                            v[4 * wi + 2] = d.z;
+                            v[4 * wi + 3] = d.w;
+                        }
+                    }
+                    const uint32_t ta = tmem + ((uint32_t)(32 * (warp & 3)) << 16) + p.a_col0 +
+                                        (uint32_t)(a * 2 + m) * 32u + (uint32_t)(w0 * 4);
+                    if (nw == 8) tmem_st32(ta, v);
+                    else tmem_st16(ta, v);
+                    tmem_st_wait();
+                    tc_fence_before();
+                } else {
+                    uint8_t* arow = at + m * kATileBytes + (row >> 3) * 1024 + (row & 7) * 128;
+                    for (int h = 0; h < nw / 4; ++h) {
+                        const uint4 c = cw[(w0 >> 2) + h];
+                        const uint32_t words[4] = {c.x, c.y, c.z, c.w};
+#pragma unroll
+                        for (int wi = 0; wi < 4; ++wi) {
+                            const int j = w0 + h * 4 + wi;   // 16-byte chunk = 8 consecutive k
+                            *reinterpret_cast<uint4*>(arow + ((j ^ (row & 7)) << 4)) = dequant_word(words[wi], s2, b2);
+                        }
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 if (lane == 0) {
                     q4d::mbar_arrive(q4d::smem_addr(&sm.in_empty[s]));
@@ -473,13 +559,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_fence_after();
             const int n = un.nt * kRows + row;
-            const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2 * kTN);
+            const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2) * p.acc_cols;
             // plain mode: the second issuer's accumulator holds the odd K steps
             const bool two = p.glu || p.ksteps >= 2;
             for (int c0 = 0; c0 < un.tn; c0 += 16) {
                 uint32_t g[16], v[16];
                 tmem_ld16(t0 + c0, g);
-                if (two) tmem_ld16(t0 + kTN + c0, v);
+                if (two) tmem_ld16(t0 + p.acc_cols + c0, v);
                 tmem_ld_wait();
                 if (!p.glu && two) {
 #pragma unroll
@@ -695,7 +781,6 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.kparts = a.kparts > 1 ? a.kparts : 1;
     p.ksteps = p.nK / p.kparts;
     p.part = a.part;
-    p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqThreads * (p.G + 1) * 4 + 127) & ~size_t(127));
     p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
     p.err = dev->err_word;
 
@@ -714,10 +799,18 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.x_bytes = (uint32_t)p.tn * q4g::kKS * 2u;
     p.x_off = (uint32_t)p.nmat * q4g::kCodesBytes;
     p.in_bytes = p.x_off + p.x_bytes;
-    p.a_bytes = (uint32_t)p.nmat * q4g::kATileBytes;
+    // Units of at most 64 tokens leave half the 512 TMEM columns free of
+    // accumulators (2 buffers x 2 accumulators x tn): the dequantised A
+    // stages go there (4 stages x 2 matrices x 32 columns), not into shared
+    // memory, which then holds only the input ring.
+    p.a_tmem = p.tn <= 64 ? 1 : 0;
+    p.acc_cols = p.a_tmem ? (uint32_t)p.tn : (uint32_t)q4g::kTN;
+    p.a_col0 = 256;
+    p.a_bytes = p.a_tmem ? 0u : (uint32_t)p.nmat * q4g::kATileBytes;
+    p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqWarps * 32 * (p.G + 1) * 4 + 127) & ~size_t(127));
     const size_t fixed = 1024 + (size_t)p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
     const size_t avail = (size_t)dev->smem_optin > fixed ? (size_t)dev->smem_optin - fixed : 0;
-    int as = glu ? 2 : 3, is = 0;
+    int as = p.a_tmem ? q4g::kMaxAStages : glu ? 2 : 3, is = 0;
     for (; as >= 2; --as) {
         const size_t left = avail > (size_t)as * p.a_bytes ? avail - (size_t)as * p.a_bytes : 0;
         is = (int)(left / p.in_bytes);
@@ -749,10 +842,13 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (a.offsets)
         q4g::check_routing_kernel<<<(a.R + 255) / 256 < dev->sms ? (a.R + 255) / 256 : dev->sms, 256, 0, s>>>(
             a.expert_ids, a.offsets, a.E, a.R, dev->err_word);
-    static std::atomic<int> smem_marks[64];
-    cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel), smem_marks, (int)smem);
+    static std::atomic<int> smem_marks[2][64];
+    const void* kern = p.a_tmem ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<true>)
+                                : reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false>);
+    cudaError_t e = ensure_smem_attr(kern, smem_marks[p.a_tmem], (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
-    q4g::q4_moe_gemm_kernel<<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
+    if (p.a_tmem) q4g::q4_moe_gemm_kernel<true><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
+    else q4g::q4_moe_gemm_kernel<false><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
     if (p.kparts > 1) {
