@@ -64,7 +64,7 @@ __device__ unsigned long long g_step_trace[2 * 4096];
 #endif
 #define Q4_TRACE(k) Q4_TRACE_T(k, 0)  // the consumers' points (0..14)
 
-constexpr int kWarps = 8;                        // consumer warps (the layer's critical path)
+constexpr int kWarps = 11;                       // consumer warps (the layer's critical path)
 constexpr int kCT = kWarps * 32;                 // consumer threads
 constexpr int kProducerWarp = kWarps;            // streams the weight pieces
 constexpr int kThreads = (kWarps + 1) * 32;
