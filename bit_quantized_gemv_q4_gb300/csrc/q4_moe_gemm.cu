@@ -24,16 +24,20 @@
 //   threads move their row's values into private shared slots at unit start.
 // * Warps 2..9 (dequant): codes -> fp16 w = s*q + b with the code OR-ed into
 //   the mantissa of 1024.0/64.0 (exact), one fp16 subtract and one fp16 FMA per
-//   pair (w rounded once to fp16), written as the A tile in the same swizzled
-//   K-major layout, fenced to the async proxy.
-// * Warp 1 (MMA; in GLU mode warp 14 for the up matrix): one thread per
-//   matrix issues tcgen05.mma kind::f16 (fp16 x fp16 -> fp32) into a
-//   double-buffered TMEM accumulator (gate and up side by side), committing
-//   to mbarriers to release input stages and hand the accumulator to the
-//   epilogue.  With few tokens per unit an MMA is small and the issuing
-//   thread, not the tensor core, sets the pace (a per-role timestamp trace
-//   measured ~70 ns per 128x16x16 tcgen05.mma), so gate and up get an issuer
-//   each.
+//   pair (w rounded once to fp16).  Units of up to 64 tokens: the row's values
+//   go to its TMEM lane with tcgen05.st (A read by the MMA from tensor memory);
+//   larger units: written as the A tile in the swizzled K-major shared-memory
+//   layout, fenced to the async proxy.
+// * Warp 15 (dispatch): one thread waits for each K step's input stage and
+//   free A stage and releases the step to the dequant warps with one mbarrier
+//   arrival (each completed-phase wait costs ~80 ns of the step).
+// * Warp 1 (MMA) and warp 14: two issuing threads (GLU: one per matrix;
+//   plain: alternate K steps into two accumulators, added in the epilogue)
+//   issue tcgen05.mma kind::f16 (fp16 x fp16 -> fp32) into double-buffered
+//   TMEM accumulators, committing to mbarriers to release input stages and
+//   hand the accumulator to the epilogue.  With few tokens per unit an MMA is
+//   small and its issue, not its arithmetic, sets the pace (a per-role
+//   timestamp trace: ~40-100 ns per 128 x 16..32 x 16 MMA).
 // * Warps 10..13 (epilogue): tcgen05.ld of the accumulator, SiLU*up or plain,
 //   coalesced stores.
 // * Every mbarrier wait is bounded; on expiry the CTA latches an error bit,
@@ -55,7 +59,8 @@ constexpr int kMaxAStages = 4;    // dequantised A ring (stage count set per lau
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kUpMmaWarp = 2 + kDeqWarps + kEpiWarps;  // 14
-constexpr int kThreads = (kUpMmaWarp + 1) * 32;
+constexpr int kDispWarp = kUpMmaWarp + 1;               // 15: releases each K step to the dequant warps
+constexpr int kThreads = (kDispWarp + 1) * 32;
 constexpr int kMaxExperts = 256;
 constexpr uint32_t kTmemCols = 512;   // 2 accumulator buffers x 2 accumulators x 128 columns; with
                                       // units of <= 64 tokens: 2 x 2 x tn, and A stages from column 256
@@ -95,6 +100,7 @@ struct Params {
 struct Smem {
     uint64_t in_full[kMaxInStages], in_empty[kMaxInStages];
     uint64_t a_full[kMaxAStages], a_empty[kMaxAStages];
+    uint64_t go[kMaxAStages];    // K step ready for the dequant warps: its input landed, its A stage is free
     uint64_t acc_full[2], acc_empty[2];
     uint64_t sb_full, sb_empty;  // staging buffer of the unit's scales and biases
     uint64_t drain;  // completion probe for in-flight MMAs on the abort path
@@ -288,6 +294,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int i = 0; i < AS; ++i) {
             q4d::mbar_init(q4d::smem_addr(&sm.a_full[i]), kDeqWarps);
             q4d::mbar_init(q4d::smem_addr(&sm.a_empty[i]), p.nmat);
+            q4d::mbar_init(q4d::smem_addr(&sm.go[i]), 1);
         }
         for (int i = 0; i < 2; ++i) {
             q4d::mbar_init(q4d::smem_addr(&sm.acc_full[i]), 2);  // both issuers commit
@@ -391,43 +398,92 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t dm = tmem + (uint32_t)(buf * 2 + r) * p.acc_cols;
                 bool ok = true, first = true;
                 const int ks0 = un.kp * p.ksteps, ks1 = ks0 + p.ksteps;
+                // One K step's MMAs (4 of K = 16) on input stage s, A stage a,
+                // then the commits that release both.
+                auto issue = [&](int s, int a) {
+                    const uint32_t xs = q4d::smem_addr(in_ring + (size_t)s * p.in_bytes + p.x_off);
+                    // K-chunk kk advances the X descriptor's start address by 32 bytes
+                    const uint64_t xd = sw128_desc(xs);
+                    if constexpr (kATmem) {
+                        // 16 fp16 of K = 8 TMEM columns
+                        const uint32_t at = tmem + p.a_col0 + (uint32_t)(a * 2 + mi) * 32u;
+#pragma unroll
+                        for (int kk = 0; kk < kKS / 16; ++kk)
+                            mma_f16_tmem_a(dm, at + 8 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                    } else {
+                        const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
+                        const uint64_t ad = sw128_desc(as + mi * kATileBytes);
+#pragma unroll
+                        for (int kk = 0; kk < kKS / 16; ++kk)
+                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                    }
+                    first = false;
+                    mma_commit(q4d::smem_addr(&sm.in_empty[s]));
+                    mma_commit(q4d::smem_addr(&sm.a_empty[a]));
+                };
+                // With A in tensor memory (4 A stages) this issuer's steps go
+                // in pairs behind one wait: every dequant warp arrives on the
+                // A stages in step order, so the second step's a_full phase
+                // completes after the first's.  A completed-phase wait costs
+                // ~80 ns of the issuer's step.
+                int pend_s = -1, pend_a = 0;
                 for (int ks = ks0; ks < ks1; ++ks) {
                     const int s = ip.s, a = ap.s;
                     if (p.glu || ((ks - ks0) & 1) == r) {
-                        // A stage a is complete only after every dequant warp
-                        // has waited for input stage s (codes and X land
-                        // together on in_full), so that one wait also covers
-                        // the X tile: a completed-phase wait costs ~200 cycles.
-                        if (!wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t xs = q4d::smem_addr(in_ring + (size_t)s * p.in_bytes + p.x_off);
-                        // K-chunk kk advances the X descriptor's start address by 32 bytes
-                        const uint64_t xd = sw128_desc(xs);
-                        if constexpr (kATmem) {
-                            // 16 fp16 of K = 8 TMEM columns
-                            const uint32_t at = tmem + p.a_col0 + (uint32_t)(a * 2 + mi) * 32u;
-#pragma unroll
-                            for (int kk = 0; kk < kKS / 16; ++kk)
-                                mma_f16_tmem_a(dm, at + 8 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                        const bool more = ks + (p.glu ? 1 : 2) < ks1;  // another step of this issuer follows
+                        if (kATmem && pend_s < 0 && more) {
+                            pend_s = s;
+                            pend_a = a;
                         } else {
-                            const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
-                            const uint64_t ad = sw128_desc(as + mi * kATileBytes);
-#pragma unroll
-                            for (int kk = 0; kk < kKS / 16; ++kk)
-                                mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                            // A stage a is complete only after every dequant
+                            // warp was released for input stage s (codes and X
+                            // land together on in_full), so that one wait also
+                            // covers the X tile.
+                            if (!wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            if (pend_s >= 0) {
+                                issue(pend_s, pend_a);
+                                pend_s = -1;
+                            }
+                            issue(s, a);
                         }
-                        first = false;
-                        mma_commit(q4d::smem_addr(&sm.in_empty[s]));
-                        mma_commit(q4d::smem_addr(&sm.a_empty[a]));
                     }
                     ip.next(IS);
                     ap.next(AS);
                 }
                 if (!ok) break;
                 mma_commit(q4d::smem_addr(&sm.acc_full[buf]));
+            }
+        }
+    } else if (warp == kDispWarp) {
+        // ------------------------------------------------------------ dispatch
+        // One thread waits, for every K step, on the two barriers the dequant
+        // warps would otherwise each wait on (the input stage landed, the A
+        // stage's previous MMAs done) and releases the step with one arrival:
+        // a completed-phase wait costs ~80 ns, and this takes one of the two
+        // off the dequant warps' step.  It arrives on go[a] for round r only
+        // after a_empty[a] of round r - 1, which needs every dequant warp's
+        // a_full arrival of that round, so the dequant warps have consumed
+        // the previous phase of go[a] by then.
+        if (lane == 0) {
+            RingPos ip, ap;
+            for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x) {
+                bool ok = true;
+                for (int j = 0; j < p.ksteps; ++j) {
+                    const int s = ip.s, a = ap.s;
+                    if (!wait_bar(sm, sm.in_full[s], ip.r & 1, p.err) ||
+                        (ap.r > 0 && !wait_bar(sm, sm.a_empty[a], (ap.r - 1) & 1, p.err))) {
+                        ok = false;
+                        break;
+                    }
+                    q4d::mbar_arrive(q4d::smem_addr(&sm.go[a]));
+                    ip.next(IS);
+                    ap.next(AS);
+                }
+                if (!ok) break;
             }
         }
     } else if (warp < 2 + kDeqWarps) {
@@ -474,8 +530,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int ks0 = (u % p.kparts) * p.ksteps, ks1 = ks0 + p.ksteps;
             for (int ks = ks0; ks < ks1; ++ks, ++it) {
                 const int s = ip.s, a = ap.s;
-                bool w = wait_bar(sm, sm.in_full[s], ip.r & 1, p.err);
-                if (w && ap.r > 0) w = wait_bar(sm, sm.a_empty[a], (ap.r - 1) & 1, p.err);
+                // released by the dispatch thread: input stage s landed and A stage a is free
+                const bool w = wait_bar(sm, sm.go[a], ap.r & 1, p.err);
                 if (!__all_sync(0xffffffffu, w)) {
                     sm.abort = 1;
                     ok = false;
