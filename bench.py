@@ -55,24 +55,14 @@ def peaks():
 
 
 def kernel_source_hash(path: str = "per-stage") -> str:
-    """Hash of the GEMV kernel's code (q4_gemv.cu + q4_device.cuh) with
-    comments and whitespace removed, so a comment edit keeps the recorded
-    ncu traffic valid while any code change invalidates it.  The opt-in
-    persistent decode step (its kernel, from the "Persistent decode step"
-    comment to the failure-detection self-test, and its host planning and
-    launch, from persistent_plan to the end of the file) is left out: the
-    per-stage launches of q4_gemv_kernel that the traffic was measured on do
-    not run that code.  For the clustered step the hash covers q4_step.cu too
-    (its two kernels and the lm_head GEMV run)."""
+    """Hash of the decode kernels' code (q4_gemv.cu + q4_device.cuh, and
+    q4_step.cu for the clustered step) with comments and whitespace removed:
+    a comment edit keeps the recorded ncu traffic valid, any code change in
+    those files invalidates it (the traffic is then re-captured)."""
     h = hashlib.sha256()
     for nm in (("q4_gemv.cu", "q4_device.cuh") + (("q4_step.cu",) if path == "clustered" else ())):
         with open(os.path.join(ROOT, "bit_quantized_gemv_q4_gb300", "csrc", nm), encoding="utf-8") as f:
             src = f.read()
-        if nm == "q4_gemv.cu":
-            a = src.index("// Persistent decode step.")
-            b = src.index("// Failure-detection self-test")
-            c = src.index("q4_status persistent_plan(")
-            src = src[:a] + src[b:c]
         src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)   # block comments
         src = re.sub(r"//[^\n]*", " ", src)                   # line comments
         h.update(" ".join(src.split()).encode())
