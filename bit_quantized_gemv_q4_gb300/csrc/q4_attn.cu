@@ -35,6 +35,7 @@
 
 #include "q4_device.cuh"
 #include "q4_internal.h"
+#include "q4_tc.cuh"
 
 namespace q4a {
 
@@ -595,6 +596,354 @@ __global__ void __launch_bounds__(kFThreads) prefill_attn_kernel(const uint16_t*
     }
 }
 
+// ------------------------------------------------ prefill, tcgen05 path ---
+// Causal attention of a prompt chunk for head_dim 128 on the 5th-generation
+// tensor cores.  A CTA takes one query head and 128 of the chunk's tokens
+// (the MMA's M) and walks the keys in tiles of 128 positions (its N):
+//   S = Q K^T   two MMA chains per tile (the rotated, scaled query as fp16 hi
+//               and lo parts in shared memory, so the scores carry the fp32
+//               query; the key tile by TMA, K-major), into one of two score
+//               buffers in tensor memory;
+//   P           the softmax warps (thread = query row = TMEM lane) read S,
+//               mask, take exp2 against the row's reference maximum and write
+//               P as fp16 into tensor memory;
+//   O += P V    A = P from tensor memory, B = the value tile read MN-major
+//               (head_dim contiguous in each position's row), O in tensor
+//               memory.
+// The MMA thread issues S of tile j before O += P V of tile j - 1, so the
+// tensor core computes the next scores while the softmax warps work.  The
+// reference maximum moves only when a row's maximum exceeds it by more than
+// 8 (a factor 2^8 in exp2); then O and the row sum are rescaled.  P stays
+// within 2^8 (fp16 keeps its relative precision at any magnitude) and O / sum
+// is the same quotient.  The probabilities enter the value product as fp16;
+// their sum stays fp32.
+constexpr int kTQ = 128;              // query tokens per CTA (MMA M)
+constexpr int kTK = 128;              // key positions per tile (MMA N of the scores)
+constexpr int kTThreads = 256;        // warp 0: key tiles, warp 1: MMA, warp 2: value tiles, 4..7: softmax
+constexpr uint32_t kTTile = 32768;    // one 128 x 128 fp16 tile: two 64-wide 128-byte-swizzled slabs
+constexpr uint32_t kColO = 256;       // TMEM columns: scores 0..127 and 128..255, O 256..383,
+constexpr uint32_t kColP = 384;       //   P 384..447 and 448..511
+
+struct TcBars {
+    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain;
+    uint32_t tmem_base;
+    volatile int abort;
+};
+
+constexpr size_t prefill_tc_smem() { return 1024 + 6 * (size_t)kTTile + sizeof(TcBars); }
+
+// Byte offset of row r, 16-byte chunk c (c < 8) in a 128-byte-swizzled slab.
+__device__ __forceinline__ uint32_t sw_off(int r, int c) {
+    return (uint32_t)((r >> 3) * 1024 + (r & 7) * 128 + ((c ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ bool tc_wait(TcBars& B, uint64_t& bar, uint32_t parity, int* err) {
+    if (B.abort) return false;
+    if (!q4d::mbar_wait(q4d::smem_addr(&bar), parity, err)) {
+        B.abort = 1;
+        return false;
+    }
+    return true;
+}
+
+// Grid (Hq, ceil(C / 128)), 256 threads, one CTA per SM (192 KB of shared
+// memory, all 512 TMEM columns).  Block y takes token block
+// gridDim.y - 1 - y (the blocks with the most keys start first).  tmK / tmV:
+// the layer's caches as 2-D maps [Hkv * max_seq][128] fp16, boxes of 64 x 128.
+__global__ void __launch_bounds__(kTThreads, 1)
+    prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                           const uint16_t* __restrict__ q, const int32_t* pos_p, int t0, int C, int Hq, int G,
+                           int max_seq, const float2* __restrict__ cs, uint16_t* __restrict__ a, int* err) {
+    constexpr int D = 128;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* qh_s = base;                  // query, fp16 hi part (two slabs: head_dim 0..63, 64..127)
+    uint8_t* ql_s = base + kTTile;         // the lo part
+    uint8_t* k_s = base + 2 * kTTile;      // key tiles, 2 stages
+    uint8_t* v_s = base + 4 * kTTile;      // value tiles, 2 stages
+    TcBars& B = *reinterpret_cast<TcBars*>(base + 6 * kTTile);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int h = blockIdx.x, kvh = h / G;
+    const int p0 = *pos_p + t0;
+    if (p0 < 0 || p0 + C > max_seq) return;  // latched by the append kernel
+    const int tq0 = (gridDim.y - 1 - blockIdx.y) * kTQ;
+    const int n_keys = p0 + min(tq0 + kTQ, C);  // keys the block's last token sees
+    const int n_tiles = (n_keys + kTK - 1) / kTK;
+
+    if (tid == 0) {
+        for (int i = 0; i < 2; ++i) {
+            q4d::mbar_init(q4d::smem_addr(&B.k_full[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&B.k_empty[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&B.v_full[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&B.v_empty[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&B.s_full[i]), 1);
+            q4d::mbar_init(q4d::smem_addr(&B.p_full[i]), 4);  // the softmax warps
+            q4d::mbar_init(q4d::smem_addr(&B.pv_done[i]), 1);
+        }
+        q4d::mbar_init(q4d::smem_addr(&B.drain), 1);
+        B.abort = 0;
+        q4d::fence_mbar_init();
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(
+                         q4d::smem_addr(&B.tmem_base))
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    // The block's queries, rotated and scaled by log2(e) / sqrt(d), as fp16 hi
+    // + lo parts in the K-major 128-byte-swizzled layout: thread t takes row
+    // t / 2 and rotation pairs 32 (t % 2) .. + 31 (pair i couples head_dim i
+    // and i + 64, i.e. the same chunk of the two slabs).
+    {
+        const float scale = rsqrtf((float)D) * 1.4426950408889634f;
+        const int r = tid >> 1;
+        const bool live = tq0 + r < C;
+        const uint16_t* qrow = q + (size_t)(tq0 + r) * Hq * D + (size_t)h * D;
+        const float2* csr = cs + (size_t)(tq0 + r) * (D / 2);
+        for (int c = (tid & 1) * 4; c < (tid & 1) * 4 + 4; ++c) {
+            float x1[8], x2[8];
+            if (live) {
+                const uint4 ra = *reinterpret_cast<const uint4*>(qrow + 8 * c);
+                const uint4 rb = *reinterpret_cast<const uint4*>(qrow + 64 + 8 * c);
+                const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const float l0 = __half2float(__ushort_as_half((uint16_t)(wa[e >> 1] >> (16 * (e & 1)))));
+                    const float h0 = __half2float(__ushort_as_half((uint16_t)(wb[e >> 1] >> (16 * (e & 1)))));
+                    const float2 rr = csr[8 * c + e];
+                    x1[e] = (l0 * rr.x - h0 * rr.y) * scale;
+                    x2[e] = (h0 * rr.x + l0 * rr.y) * scale;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x1[e] = x2[e] = 0.f;
+            }
+            uint32_t h1[4], l1[4], h2[4], l2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                split_h2(x1[2 * e], x1[2 * e + 1], h1[e], l1[e]);
+                split_h2(x2[2 * e], x2[2 * e + 1], h2[e], l2[e]);
+            }
+            const uint32_t o = sw_off(r, c);
+            *reinterpret_cast<uint4*>(qh_s + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+            *reinterpret_cast<uint4*>(qh_s + 16384 + o) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            *reinterpret_cast<uint4*>(ql_s + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+            *reinterpret_cast<uint4*>(ql_s + 16384 + o) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads the query through the async proxy
+    q4t::fence_before();
+    __syncthreads();
+    q4t::fence_after();
+    const uint32_t tmem = B.tmem_base;
+
+    if (warp == 0 || warp == 2) {
+        // ------------------------------------------------ key / value tiles
+        if (lane == 0) {
+            const bool keys = warp == 0;
+            const CUtensorMap* map = keys ? &tmK : &tmV;
+            uint8_t* ring = keys ? k_s : v_s;
+            uint64_t* full = keys ? B.k_full : B.v_full;
+            uint64_t* empty = keys ? B.k_empty : B.v_empty;
+            int j = 0;
+            for (; j < n_tiles; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !tc_wait(B, empty[st], ((j - 2) >> 1) & 1, err)) break;
+                const uint32_t fb = q4d::smem_addr(&full[st]);
+                q4d::mbar_arrive_expect_tx(fb, kTTile);
+                const int y = kvh * max_seq + j * kTK;
+                q4t::tma_load_2d(q4d::smem_addr(ring + st * kTTile), map, 0, y, fb);
+                q4t::tma_load_2d(q4d::smem_addr(ring + st * kTTile + 16384), map, 64, y, fb);
+            }
+            if (B.abort) {
+                // copies still in flight land before the CTA can exit
+                for (int i = j > 2 ? j - 2 : 0; i < j; ++i)
+                    q4d::mbar_wait(q4d::smem_addr(&full[i & 1]), (i >> 1) & 1, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issue
+        if (lane == 0) {
+            const uint32_t id_s = q4t::idesc_f16_m128(kTK, 0), id_o = q4t::idesc_f16_m128(D, 1);
+            const uint32_t qh = q4d::smem_addr(qh_s), ql = q4d::smem_addr(ql_s);
+            // O += P_i V_i (A = P from tensor memory, B = the value tile MN-major)
+            auto pv = [&](int i) -> bool {
+                const int st = i & 1;
+                if (!tc_wait(B, B.p_full[st], (i >> 1) & 1, err) || !tc_wait(B, B.v_full[st], (i >> 1) & 1, err))
+                    return false;
+                q4t::fence_after();
+                const uint32_t vb = q4d::smem_addr(v_s + st * kTTile);
+#pragma unroll
+                for (int kk = 0; kk < kTK / 16; ++kk)
+                    q4t::mma_ts(tmem + kColO, tmem + kColP + st * 64 + 8 * kk,
+                                q4t::sw128_desc(vb + kk * 2048, 16384, 1024), id_o, (i > 0 || kk > 0) ? 1u : 0u);
+                q4t::commit(q4d::smem_addr(&B.v_empty[st]));
+                q4t::commit(q4d::smem_addr(&B.pv_done[st]));
+                return true;
+            };
+            bool ok = true;
+            for (int j = 0; j < n_tiles && ok; ++j) {
+                const int st = j & 1;
+                // S_j into score buffer st: the softmax released it with p_full
+                // of tile j - 2, waited for before O += P V of that tile
+                if (!tc_wait(B, B.k_full[st], (j >> 1) & 1, err)) {
+                    ok = false;
+                    break;
+                }
+                q4t::fence_after();
+                const uint32_t kb = q4d::smem_addr(k_s + st * kTTile);
+#pragma unroll
+                for (int part = 0; part < 2; ++part) {
+                    const uint32_t qa = part ? ql : qh;
+#pragma unroll
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
+                        q4t::mma_ss(tmem + st * kTK, q4t::sw128_desc(qa + off, 16, 1024),
+                                    q4t::sw128_desc(kb + off, 16, 1024), id_s, (part > 0 || kk > 0) ? 1u : 0u);
+                    }
+                }
+                q4t::commit(q4d::smem_addr(&B.k_empty[st]));
+                q4t::commit(q4d::smem_addr(&B.s_full[st]));
+                if (j >= 1) ok = pv(j - 1);
+            }
+            if (ok) ok = pv(n_tiles - 1);
+            if (!ok) B.abort = 1;
+            // every MMA issued has finished before the CTA winds down
+            q4t::commit(q4d::smem_addr(&B.drain));
+            q4d::mbar_wait(q4d::smem_addr(&B.drain), 0, nullptr);
+        }
+    } else if (warp >= 4) {
+        // ------------------------------------------------ softmax
+        const int qw = warp & 3;                  // TMEM lane quarter of this warp
+        const int row = qw * 32 + lane;           // query row = TMEM lane
+        const int pq = p0 + tq0 + row;            // its position
+        const uint32_t lt = tmem + ((uint32_t)(qw * 32) << 16);
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < n_tiles; ++j) {
+            const int st = j & 1;
+            if (!tc_wait(B, B.s_full[st], (j >> 1) & 1, err)) {
+                ok = false;
+                break;
+            }
+            q4t::fence_after();
+            const int key0 = j * kTK;
+            const bool mask = key0 + kTK - 1 > p0 + tq0;  // some key above some row's position
+            const uint32_t sc = lt + (uint32_t)(st * kTK);
+            float mx = -INFINITY;
+            for (int c0 = 0; c0 < kTK; c0 += 16) {
+                uint32_t r[16];
+                q4t::ld16(sc + c0, r);
+                q4t::ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const float v = (mask && key0 + c0 + e > pq) ? -INFINITY : __uint_as_float(r[e]);
+                    mx = fmaxf(mx, v);
+                }
+            }
+            float corr = 1.f;
+            bool resc = false;
+            if (mx > m_ref + 8.f) {
+                if (m_ref != -INFINITY) {
+                    corr = exp2f(m_ref - mx);
+                    resc = true;
+                }
+                m_ref = mx;
+            }
+            const float msub = m_ref == -INFINITY ? 0.f : m_ref;
+            uint32_t pk[kTK / 2];
+            float sum = 0.f;
+            for (int c0 = 0; c0 < kTK; c0 += 16) {
+                uint32_t r[16];
+                q4t::ld16(sc + c0, r);
+                q4t::ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    const float v0 = (mask && key0 + c0 + e > pq) ? -INFINITY : __uint_as_float(r[e]);
+                    const float v1 = (mask && key0 + c0 + e + 1 > pq) ? -INFINITY : __uint_as_float(r[e + 1]);
+                    const float e0 = exp2f(v0 - msub), e1 = exp2f(v1 - msub);
+                    sum += e0 + e1;
+                    pk[(c0 + e) >> 1] = pack_h2(e0, e1);
+                }
+            }
+            l = l * corr + sum;
+            // P buffer st was read by O += P V of tile j - 2, and O is written
+            // by that of tile j - 1
+            if (j >= 2 && !tc_wait(B, B.pv_done[st], ((j - 2) >> 1) & 1, err)) {
+                ok = false;
+                break;
+            }
+            if (j >= 1 && !tc_wait(B, B.pv_done[st ^ 1], ((j - 1) >> 1) & 1, err)) {
+                ok = false;
+                break;
+            }
+            q4t::fence_after();
+            if (__any_sync(0xffffffffu, resc)) {  // the TMEM load / store is warp-collective
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    uint32_t r[16];
+                    q4t::ld16(lt + kColO + c0, r);
+                    q4t::ld_wait();
+#pragma unroll
+                    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
+                    q4t::st16(lt + kColO + c0, r);
+                }
+            }
+#pragma unroll
+            for (int c = 0; c < kTK / 2; c += 16) q4t::st16(lt + kColP + st * 64 + c, pk + c);
+            q4t::st_wait();
+            if (j == n_tiles - 1 && (n_keys & (kTK - 1))) {
+                // the last tile's value rows past n_keys: stale cache rows may
+                // hold anything, and 0 * NaN would reach O; zero them
+                if (!tc_wait(B, B.v_full[st], (j >> 1) & 1, err)) {
+                    ok = false;
+                    break;
+                }
+                const int vr = row;
+                if (vr >= n_keys - key0) {
+                    uint8_t* vt = v_s + st * kTTile;
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        *reinterpret_cast<uint4*>(vt + sw_off(vr, c)) = make_uint4(0, 0, 0, 0);
+                        *reinterpret_cast<uint4*>(vt + 16384 + sw_off(vr, c)) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            }
+            q4t::fence_before();
+            __syncwarp();
+            if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&B.p_full[st]));
+        }
+        if (ok) {
+            const int last = n_tiles - 1;
+            if (tc_wait(B, B.pv_done[last & 1], (last >> 1) & 1, err)) {
+                q4t::fence_after();
+                const float inv = 1.0f / l;
+                uint16_t* ar = a + (size_t)(tq0 + row) * Hq * D + (size_t)h * D;
+                const bool live = tq0 + row < C;
+                for (int c0 = 0; c0 < D; c0 += 16) {
+                    uint32_t r[16];
+                    q4t::ld16(lt + kColO + c0, r);
+                    q4t::ld_wait();
+                    uint32_t o[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        o[e] = pack_h2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+                    if (live) {
+                        *reinterpret_cast<uint4*>(ar + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+                        *reinterpret_cast<uint4*>(ar + c0 + 8) = make_uint4(o[4], o[5], o[6], o[7]);
+                    }
+                }
+            }
+        }
+    }
+    q4t::fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        q4t::fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem) : "memory");
+    }
+}
+
 }  // namespace q4a
 
 namespace q4i {
@@ -688,19 +1037,34 @@ q4_status prefill_attn_enqueue(const uint16_t* q, const uint16_t* k, const uint1
     const float2* csp = static_cast<const float2*>(cs);
     q4a::prefill_append_kernel<<<dim3(C, Hkv), D / 2, 0, s>>>(k, v, k_cache, v_cache, pos, t0, C, Hkv, D, max_seq,
                                                               csp, dev->err_word);
-    static std::atomic<int> marks128[64], marks64[64];
-    cudaError_t e = D == 128 ? ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_kernel<128>), marks128,
-                                                (int)q4a::prefill_smem(128))
-                             : ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_kernel<64>), marks64,
-                                                (int)q4a::prefill_smem(64));
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_attn_kernel)");
-    const dim3 grid(Hq, (C + q4a::kFQ - 1) / q4a::kFQ);
-    if (D == 128)
-        q4a::prefill_attn_kernel<128><<<grid, q4a::kFThreads, q4a::prefill_smem(128), s>>>(
-            q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a);
-    else
+    cudaError_t e;
+    if (D == 128) {
+        // tcgen05 path: the caches as 2-D maps [Hkv * max_seq][128], boxes of
+        // 64 head_dim x 128 positions with the 128-byte swizzle
+        CUtensorMap tmK, tmV;
+        const uint64_t rows = (uint64_t)Hkv * (uint64_t)max_seq;
+        if ((st = make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_cache, 128, rows, 256, 64, q4a::kTK,
+                           CU_TENSOR_MAP_SWIZZLE_128B)) != Q4_OK)
+            return st;
+        if ((st = make_map(&tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, v_cache, 128, rows, 256, 64, q4a::kTK,
+                           CU_TENSOR_MAP_SWIZZLE_128B)) != Q4_OK)
+            return st;
+        static std::atomic<int> marks_tc[64];
+        e = ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_tc_kernel), marks_tc,
+                             (int)q4a::prefill_tc_smem());
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_attn_tc_kernel)");
+        const dim3 grid(Hq, (C + q4a::kTQ - 1) / q4a::kTQ);
+        q4a::prefill_attn_tc_kernel<<<grid, q4a::kTThreads, q4a::prefill_tc_smem(), s>>>(
+            tmK, tmV, q, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a, dev->err_word);
+    } else {
+        static std::atomic<int> marks64[64];
+        e = ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_kernel<64>), marks64,
+                             (int)q4a::prefill_smem(64));
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_attn_kernel)");
+        const dim3 grid(Hq, (C + q4a::kFQ - 1) / q4a::kFQ);
         q4a::prefill_attn_kernel<64><<<grid, q4a::kFThreads, q4a::prefill_smem(64), s>>>(
             q, k_cache, v_cache, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a);
+    }
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "prefill attention launch");
     return Q4_OK;

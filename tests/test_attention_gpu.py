@@ -245,6 +245,43 @@ def test_prefill_attention_several_query_blocks(d):
     t.release()
 
 
+@pytest.mark.parametrize("start,T,chunk,nan_tail", [(0, 300, 300, False), (77, 290, 160, True), (5, 37, 16, False)])
+def test_prefill_attention_head_dim_128_tiles(start, T, chunk, nan_tail):
+    """head_dim 128, 16 query heads on 8 kv heads: several 128-token query
+    blocks and 128-position key tiles with ragged ends, a prompt split into
+    chunks after cached positions; with nan_tail every cache row past the
+    prompt holds NaN (stale rows must not reach the output)."""
+    d = 128
+    shape = q4synth.tiny_decode_shape(n_layers=1, hidden=256, q=16 * d, kv=8 * d, ffn=512, vocab=1000)
+    layers, lm = q4synth.decode_weights(shape, base_seed=2100 + start)
+    max_seq = start + T + 40
+    hc = host_caches(shape, max_seq, start, 2101 + start, d)
+    if nan_tail:
+        for kc, vc in hc:
+            kc[:, start + T:] = np.nan
+            vc[:, start + T:] = np.nan
+    dc = [(torch_dev(kc), torch_dev(vc)) for kc, vc in hc]
+    pos = torch.tensor([start], dtype=torch.int32, device="cuda")
+    x = q4synth.activations(2102 + start, T, shape.hidden)
+    t, st, h, lg, ws = prefill_attn_run(shape, layers, lm, dc, pos, x, chunk, d)
+    assert st == 0 and int(pos.item()) == start + T
+    b = q4.q4_prefill_buffers(t, chunk, ws)
+    C = T - (T - 1) // chunk * chunk
+    t0 = T - C
+    kl, vl = dc[-1][0].cpu().numpy(), dc[-1][1].cpu().numpy()
+    for i in range(C):
+        qg = read16(ws, b["q"] + 2 * i * shape.q, shape.q).astype(np.float16)
+        ag = read16(ws, b["a"] + 2 * i * shape.q, shape.q)
+        p = start + t0 + i
+        a_ref, A_a = oracle.attention(qg, kl, vl, p + 1, d, p)
+        assert_parity(ag[None, :], a_ref[None, :], A_a[None, :], fp16_out=True, what=f"t={t0 + i}")
+    h_ref, y_ref, _ = oracle.prefill_attn(layers, lm, x, hc, start, d)
+    r_h = np.linalg.norm(h.float().cpu().numpy() - h_ref) / np.linalg.norm(h_ref.astype(np.float64))
+    r_y = np.linalg.norm(lg.cpu().numpy() - y_ref[0]) / np.linalg.norm(y_ref[0])
+    assert r_h <= 1e-3 and r_y <= 1e-3, (r_h, r_y)
+    t.release()
+
+
 def test_prefill_then_decode_continues_the_sequence():
     shape, layers, lm = attn_model(1700, n_layers=2)
     max_seq, T = 96, 20
