@@ -315,27 +315,92 @@ __global__ void prefill_cs_kernel(const int32_t* pos_p, int t0, int d, double lo
     cs[(size_t)t * (d / 2) + i] = make_float2(c, s);
 }
 
-// Rotated keys and values of the chunk into the caches.  Grid (C, Hkv),
-// block d/2.  k, v: [C][Hkv*d].
+// Two floats as an fp16 pair (round to nearest even), lo in the low half.
+__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
+    const __half2 h = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&h);
+}
+
+// (x, y) as an fp16 pair plus the fp16 pair of what that rounding left out.
+__device__ __forceinline__ void split_h2(float x, float y, uint32_t& hi, uint32_t& lo) {
+    const __half2 h = __floats2half2_rn(x, y);
+    const float2 f = __half22float2(h);
+    hi = *reinterpret_cast<const uint32_t*>(&h);
+    lo = pack_h2(x - f.x, y - f.y);
+}
+
+// Rotated keys and values of the chunk into the caches.  Grid C (one block
+// per token), block 256; a thread takes 8 consecutive rotation pairs of one
+// head (16-byte loads and stores).  k, v: [C][Hkv*d].  With qrot (the
+// tensor-core attention's input), also the token's queries q [C][Hq*d],
+// rotated and scaled by log2(e) / sqrt(d), as fp16 hi + lo parts:
+// qrot[part][head][t][d] (part 0 hi, 1 lo).
+__device__ __forceinline__ void rot8(const uint4& a, const uint4& b, const float2* r, float* x1, float* x2) {
+    const uint32_t wa[4] = {a.x, a.y, a.z, a.w}, wb[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+        const float l0 = __half2float(__ushort_as_half((uint16_t)(wa[e >> 1] >> (16 * (e & 1)))));
+        const float h0 = __half2float(__ushort_as_half((uint16_t)(wb[e >> 1] >> (16 * (e & 1)))));
+        x1[e] = l0 * r[e].x - h0 * r[e].y;
+        x2[e] = h0 * r[e].x + l0 * r[e].y;
+    }
+}
+
 __global__ void prefill_append_kernel(const uint16_t* __restrict__ k, const uint16_t* __restrict__ v,
                                       uint16_t* __restrict__ kc, uint16_t* __restrict__ vc, const int32_t* pos_p,
                                       int t0, int C, int Hkv, int d, int max_seq, const float2* __restrict__ cs,
-                                      int* err) {
-    const int t = blockIdx.x, h = blockIdx.y, i = threadIdx.x, half = d / 2;
+                                      const uint16_t* __restrict__ q, int Hq, uint16_t* __restrict__ qrot, int* err) {
+    const int t = blockIdx.x, half = d / 2, nc = half / 8;  // 16-byte chunks per half row
     const int p0 = *pos_p + t0;
     if (p0 < 0 || p0 + C > max_seq) {
-        if (t == 0 && h == 0 && i == 0) atomicOr(err, q4d::kErrDeviceCheck);
+        if (t == 0 && threadIdx.x == 0) atomicOr(err, q4d::kErrDeviceCheck);
         return;
     }
-    const float2 r = cs[(size_t)t * half + i];
-    const size_t src = (size_t)t * Hkv * d + (size_t)h * d;
-    const float lo = __half2float(__ushort_as_half(k[src + i]));
-    const float hi = __half2float(__ushort_as_half(k[src + i + half]));
-    const size_t base = ((size_t)h * max_seq + p0 + t) * d;
-    kc[base + i] = __half_as_ushort(__float2half_rn(lo * r.x - hi * r.y));
-    kc[base + i + half] = __half_as_ushort(__float2half_rn(hi * r.x + lo * r.y));
-    vc[base + i] = v[src + i];
-    vc[base + i + half] = v[src + i + half];
+    const int nk = Hkv * nc, nq = qrot ? Hq * nc : 0;
+    for (int x = threadIdx.x; x < nk + nq; x += blockDim.x) {
+        const bool isk = x < nk;
+        const int y = isk ? x : x - nk;
+        const int h = y / nc, c = y - h * nc;
+        float2 r[8];
+        const float4* c4 = reinterpret_cast<const float4*>(cs + (size_t)t * half + 8 * c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float4 w = c4[e];
+            r[2 * e] = make_float2(w.x, w.y);
+            r[2 * e + 1] = make_float2(w.z, w.w);
+        }
+        float x1[8], x2[8];
+        if (isk) {
+            const size_t src = (size_t)t * Hkv * d + (size_t)h * d + 8 * c;
+            rot8(*reinterpret_cast<const uint4*>(k + src), *reinterpret_cast<const uint4*>(k + src + half), r, x1, x2);
+            const size_t base = ((size_t)h * max_seq + p0 + t) * d + 8 * c;
+            uint32_t o1[4], o2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                o1[e] = pack_h2(x1[2 * e], x1[2 * e + 1]);
+                o2[e] = pack_h2(x2[2 * e], x2[2 * e + 1]);
+            }
+            *reinterpret_cast<uint4*>(kc + base) = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+            *reinterpret_cast<uint4*>(kc + base + half) = make_uint4(o2[0], o2[1], o2[2], o2[3]);
+            *reinterpret_cast<uint4*>(vc + base) = *reinterpret_cast<const uint4*>(v + src);
+            *reinterpret_cast<uint4*>(vc + base + half) = *reinterpret_cast<const uint4*>(v + src + half);
+        } else {
+            const float scale = rsqrtf((float)d) * 1.4426950408889634f;  // log2(e) / sqrt(d)
+            const size_t src = (size_t)t * Hq * d + (size_t)h * d + 8 * c;
+            rot8(*reinterpret_cast<const uint4*>(q + src), *reinterpret_cast<const uint4*>(q + src + half), r, x1, x2);
+            uint32_t h1[4], l1[4], h2[4], l2[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                split_h2(x1[2 * e] * scale, x1[2 * e + 1] * scale, h1[e], l1[e]);
+                split_h2(x2[2 * e] * scale, x2[2 * e + 1] * scale, h2[e], l2[e]);
+            }
+            const size_t o = ((size_t)h * C + t) * d + 8 * c, part = (size_t)Hq * C * d;
+            *reinterpret_cast<uint4*>(qrot + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
+            *reinterpret_cast<uint4*>(qrot + o + half) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
+            *reinterpret_cast<uint4*>(qrot + part + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
+            *reinterpret_cast<uint4*>(qrot + part + o + half) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
+        }
+    }
 }
 
 // Causal attention of a prompt chunk on the tensor cores (mma.sync
@@ -386,19 +451,6 @@ __device__ __forceinline__ void mma16816(float* c, const uint32_t* a, uint32_t b
         "{%0, %1, %2, %3};"
         : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-
-__device__ __forceinline__ uint32_t pack_h2(float lo, float hi) {
-    const __half2 h = __floats2half2_rn(lo, hi);
-    return *reinterpret_cast<const uint32_t*>(&h);
-}
-
-// (x, y) as an fp16 pair plus the fp16 pair of what that rounding left out.
-__device__ __forceinline__ void split_h2(float x, float y, uint32_t& hi, uint32_t& lo) {
-    const __half2 h = __floats2half2_rn(x, y);
-    const float2 f = __half22float2(h);
-    hi = *reinterpret_cast<const uint32_t*>(&h);
-    lo = pack_h2(x - f.x, y - f.y);
 }
 
 // Grid (Hq, ceil(C / 64)), 128 threads; block y takes token block
@@ -619,15 +671,17 @@ __global__ void __launch_bounds__(kFThreads) prefill_attn_kernel(const uint16_t*
 // their sum stays fp32.
 constexpr int kTQ = 128;              // query tokens per CTA (MMA M)
 constexpr int kTK = 128;              // key positions per tile (MMA N of the scores)
-constexpr int kTThreads = 256;        // warp 0: key tiles, warp 1: MMA, warp 2: value tiles, 4..7: softmax
+constexpr int kTThreads = 384;        // warp 0: key tiles, warp 1: MMA, warp 2: value tiles, 4..11: softmax
 constexpr uint32_t kTTile = 32768;    // one 128 x 128 fp16 tile: two 64-wide 128-byte-swizzled slabs
 constexpr uint32_t kColO = 256;       // TMEM columns: scores 0..127 and 128..255, O 256..383,
 constexpr uint32_t kColP = 384;       //   P 384..447 and 448..511
 
 struct TcBars {
-    uint64_t k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain;
+    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain;
     uint32_t tmem_base;
     volatile int abort;
+    float xmax[2][2][kTQ];  // [tile parity][column half][row]: the halves' row maxima
+    float xsum[2][kTQ];     // [column half][row]: the halves' row sums
 };
 
 constexpr size_t prefill_tc_smem() { return 1024 + 6 * (size_t)kTTile + sizeof(TcBars); }
@@ -646,14 +700,14 @@ __device__ __forceinline__ bool tc_wait(TcBars& B, uint64_t& bar, uint32_t parit
     return true;
 }
 
-// Grid (Hq, ceil(C / 128)), 256 threads, one CTA per SM (192 KB of shared
+// Grid (Hq, ceil(C / 128)), 384 threads, one CTA per SM (192 KB of shared
 // memory, all 512 TMEM columns).  Block y takes token block
 // gridDim.y - 1 - y (the blocks with the most keys start first).  tmK / tmV:
 // the layer's caches as 2-D maps [Hkv * max_seq][128] fp16, boxes of 64 x 128.
 __global__ void __launch_bounds__(kTThreads, 1)
     prefill_attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
-                           const uint16_t* __restrict__ q, const int32_t* pos_p, int t0, int C, int Hq, int G,
-                           int max_seq, const float2* __restrict__ cs, uint16_t* __restrict__ a, int* err) {
+                           const __grid_constant__ CUtensorMap tmQ, const int32_t* pos_p, int t0, int C, int Hq,
+                           int G, int max_seq, uint16_t* __restrict__ a, int* err) {
     constexpr int D = 128;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -677,10 +731,11 @@ __global__ void __launch_bounds__(kTThreads, 1)
             q4d::mbar_init(q4d::smem_addr(&B.v_full[i]), 1);
             q4d::mbar_init(q4d::smem_addr(&B.v_empty[i]), 1);
             q4d::mbar_init(q4d::smem_addr(&B.s_full[i]), 1);
-            q4d::mbar_init(q4d::smem_addr(&B.p_full[i]), 4);  // the softmax warps
+            q4d::mbar_init(q4d::smem_addr(&B.p_full[i]), 8);  // the softmax warps
             q4d::mbar_init(q4d::smem_addr(&B.pv_done[i]), 1);
         }
         q4d::mbar_init(q4d::smem_addr(&B.drain), 1);
+        q4d::mbar_init(q4d::smem_addr(&B.q_full), 1);
         B.abort = 0;
         q4d::fence_mbar_init();
     }
@@ -690,48 +745,31 @@ __global__ void __launch_bounds__(kTThreads, 1)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
     }
-    // The block's queries, rotated and scaled by log2(e) / sqrt(d), as fp16 hi
-    // + lo parts in the K-major 128-byte-swizzled layout: thread t takes row
-    // t / 2 and rotation pairs 32 (t % 2) .. + 31 (pair i couples head_dim i
-    // and i + 64, i.e. the same chunk of the two slabs).
-    {
-        const float scale = rsqrtf((float)D) * 1.4426950408889634f;
-        const int r = tid >> 1;
-        const bool live = tq0 + r < C;
-        const uint16_t* qrow = q + (size_t)(tq0 + r) * Hq * D + (size_t)h * D;
-        const float2* csr = cs + (size_t)(tq0 + r) * (D / 2);
-        for (int c = (tid & 1) * 4; c < (tid & 1) * 4 + 4; ++c) {
-            float x1[8], x2[8];
-            if (live) {
-                const uint4 ra = *reinterpret_cast<const uint4*>(qrow + 8 * c);
-                const uint4 rb = *reinterpret_cast<const uint4*>(qrow + 64 + 8 * c);
-                const uint32_t wa[4] = {ra.x, ra.y, ra.z, ra.w}, wb[4] = {rb.x, rb.y, rb.z, rb.w};
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    const float l0 = __half2float(__ushort_as_half((uint16_t)(wa[e >> 1] >> (16 * (e & 1)))));
-                    const float h0 = __half2float(__ushort_as_half((uint16_t)(wb[e >> 1] >> (16 * (e & 1)))));
-                    const float2 rr = csr[8 * c + e];
-                    x1[e] = (l0 * rr.x - h0 * rr.y) * scale;
-                    x2[e] = (h0 * rr.x + l0 * rr.y) * scale;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x1[e] = x2[e] = 0.f;
-            }
-            uint32_t h1[4], l1[4], h2[4], l2[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                split_h2(x1[2 * e], x1[2 * e + 1], h1[e], l1[e]);
-                split_h2(x2[2 * e], x2[2 * e + 1], h2[e], l2[e]);
-            }
-            const uint32_t o = sw_off(r, c);
-            *reinterpret_cast<uint4*>(qh_s + o) = make_uint4(h1[0], h1[1], h1[2], h1[3]);
-            *reinterpret_cast<uint4*>(qh_s + 16384 + o) = make_uint4(h2[0], h2[1], h2[2], h2[3]);
-            *reinterpret_cast<uint4*>(ql_s + o) = make_uint4(l1[0], l1[1], l1[2], l1[3]);
-            *reinterpret_cast<uint4*>(ql_s + 16384 + o) = make_uint4(l2[0], l2[1], l2[2], l2[3]);
-        }
+    // Key (warp 0) or value (warp 2) tile j into stage j % 2, by lane 0.
+    auto issue_tile = [&](int j) {
+        const bool keys = warp == 0;
+        const int st = j & 1;
+        const uint32_t fb = q4d::smem_addr(keys ? &B.k_full[st] : &B.v_full[st]);
+        uint8_t* dst = (keys ? k_s : v_s) + st * kTTile;
+        q4d::mbar_arrive_expect_tx(fb, kTTile);
+        const int y = kvh * max_seq + j * kTK;
+        q4t::tma_load_2d(q4d::smem_addr(dst), keys ? &tmK : &tmV, 0, y, fb);
+        q4t::tma_load_2d(q4d::smem_addr(dst + 16384), keys ? &tmK : &tmV, 64, y, fb);
+    };
+    __syncthreads();  // barriers initialised
+    if (warp == 0 && lane == 0) {
+        // the block's queries: hi and lo parts, two slabs each (rows past C
+        // read the next head's rows or zeros; those rows are never stored)
+        const uint32_t qb = q4d::smem_addr(&B.q_full);
+        q4d::mbar_arrive_expect_tx(qb, 2 * kTTile);
+        const int yh = h * C + tq0, yl = Hq * C + h * C + tq0;
+        q4t::tma_load_2d(q4d::smem_addr(qh_s), &tmQ, 0, yh, qb);
+        q4t::tma_load_2d(q4d::smem_addr(qh_s + 16384), &tmQ, 64, yh, qb);
+        q4t::tma_load_2d(q4d::smem_addr(ql_s), &tmQ, 0, yl, qb);
+        q4t::tma_load_2d(q4d::smem_addr(ql_s + 16384), &tmQ, 64, yl, qb);
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // the MMA reads the query through the async proxy
+    if ((warp == 0 || warp == 2) && lane == 0)
+        for (int j = 0; j < n_tiles && j < 2; ++j) issue_tile(j);
     q4t::fence_before();
     __syncthreads();
     q4t::fence_after();
@@ -740,24 +778,18 @@ __global__ void __launch_bounds__(kTThreads, 1)
     if (warp == 0 || warp == 2) {
         // ------------------------------------------------ key / value tiles
         if (lane == 0) {
-            const bool keys = warp == 0;
-            const CUtensorMap* map = keys ? &tmK : &tmV;
-            uint8_t* ring = keys ? k_s : v_s;
-            uint64_t* full = keys ? B.k_full : B.v_full;
-            uint64_t* empty = keys ? B.k_empty : B.v_empty;
-            int j = 0;
+            uint64_t* full = warp == 0 ? B.k_full : B.v_full;
+            uint64_t* empty = warp == 0 ? B.k_empty : B.v_empty;
+            int j = 2;
             for (; j < n_tiles; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !tc_wait(B, empty[st], ((j - 2) >> 1) & 1, err)) break;
-                const uint32_t fb = q4d::smem_addr(&full[st]);
-                q4d::mbar_arrive_expect_tx(fb, kTTile);
-                const int y = kvh * max_seq + j * kTK;
-                q4t::tma_load_2d(q4d::smem_addr(ring + st * kTTile), map, 0, y, fb);
-                q4t::tma_load_2d(q4d::smem_addr(ring + st * kTTile + 16384), map, 64, y, fb);
+                if (!tc_wait(B, empty[j & 1], ((j - 2) >> 1) & 1, err)) break;
+                issue_tile(j);
             }
             if (B.abort) {
                 // copies still in flight land before the CTA can exit
-                for (int i = j > 2 ? j - 2 : 0; i < j; ++i)
+                if (warp == 0) q4d::mbar_wait(q4d::smem_addr(&B.q_full), 0, nullptr);
+                const int issued = j < n_tiles ? j : n_tiles;
+                for (int i = issued > 2 ? issued - 2 : 0; i < issued; ++i)
                     q4d::mbar_wait(q4d::smem_addr(&full[i & 1]), (i >> 1) & 1, nullptr);
             }
         }
@@ -781,7 +813,7 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 q4t::commit(q4d::smem_addr(&B.pv_done[st]));
                 return true;
             };
-            bool ok = true;
+            bool ok = tc_wait(B, B.q_full, 0, err);
             for (int j = 0; j < n_tiles && ok; ++j) {
                 const int st = j & 1;
                 // S_j into score buffer st: the softmax released it with p_full
@@ -814,33 +846,48 @@ __global__ void __launch_bounds__(kTThreads, 1)
         }
     } else if (warp >= 4) {
         // ------------------------------------------------ softmax
-        const int qw = warp & 3;                  // TMEM lane quarter of this warp
+        // Two warps per TMEM lane quarter: warp 4 + q takes score columns
+        // 0..63 of rows 32 q .. 32 q + 31 (and O columns 0..63), warp 8 + q
+        // columns 64..127; the pair meets on named barrier 1 + q to share
+        // each tile's row maxima and, at the end, the row sums.
+        const int sw = warp - 4;
+        const int qw = sw & 3;                    // TMEM lane quarter (= warp % 4)
+        const int hf = sw >> 2;                   // which half of the columns
         const int row = qw * 32 + lane;           // query row = TMEM lane
         const int pq = p0 + tq0 + row;            // its position
         const uint32_t lt = tmem + ((uint32_t)(qw * 32) << 16);
+        const uint32_t pair_bar = 1 + qw;
         float m_ref = -INFINITY, l = 0.f;
-        bool ok = true;
+        // `bad` (a failed or skipped wait) is made warp-uniform after every
+        // wait and pair-uniform at the pair's barrier, which both warps reach
+        // once per tile: they leave the loop together, so neither waits on the
+        // named barrier for a partner that has left
+        bool bad = false;
         for (int j = 0; j < n_tiles; ++j) {
             const int st = j & 1;
-            if (!tc_wait(B, B.s_full[st], (j >> 1) & 1, err)) {
-                ok = false;
-                break;
-            }
-            q4t::fence_after();
-            const int key0 = j * kTK;
-            const bool mask = key0 + kTK - 1 > p0 + tq0;  // some key above some row's position
-            const uint32_t sc = lt + (uint32_t)(st * kTK);
-            float mx = -INFINITY;
-            for (int c0 = 0; c0 < kTK; c0 += 16) {
-                uint32_t r[16];
-                q4t::ld16(sc + c0, r);
-                q4t::ld_wait();
+            bad = __any_sync(0xffffffffu, bad || !tc_wait(B, B.s_full[st], (j >> 1) & 1, err));
+            const int key0 = j * kTK + hf * (kTK / 2);  // key of this thread's first column
+            const bool mask = j * kTK + kTK - 1 > p0 + tq0;  // some key of the tile above some row's position
+            uint32_t r[kTK / 2];
+            float mh = -INFINITY;
+            if (!bad) {
+                q4t::fence_after();
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const float v = (mask && key0 + c0 + e > pq) ? -INFINITY : __uint_as_float(r[e]);
-                    mx = fmaxf(mx, v);
+                for (int c0 = 0; c0 < kTK / 2; c0 += 16)
+                    q4t::ld16(lt + (uint32_t)(st * kTK + hf * (kTK / 2) + c0), r + c0);
+                q4t::ld_wait();
+                if (mask) {
+#pragma unroll
+                    for (int e = 0; e < kTK / 2; ++e)
+                        if (key0 + e > pq) r[e] = __float_as_uint(-INFINITY);
                 }
+#pragma unroll
+                for (int e = 0; e < kTK / 2; ++e) mh = fmaxf(mh, __uint_as_float(r[e]));
             }
+            B.xmax[st][hf][row] = mh;
+            bad = q4d::named_bar_or(pair_bar, 64, bad);
+            if (bad) break;
+            const float mx = fmaxf(B.xmax[st][0][row], B.xmax[st][1][row]);
             float corr = 1.f;
             bool resc = false;
             if (mx > m_ref + 8.f) {
@@ -851,61 +898,46 @@ __global__ void __launch_bounds__(kTThreads, 1)
                 m_ref = mx;
             }
             const float msub = m_ref == -INFINITY ? 0.f : m_ref;
-            uint32_t pk[kTK / 2];
+            // P = exp2(s - m_ref) as fp16 pairs, packed in place (pair i
+            // into r[i], whose own score was read for pair i / 2)
             float sum = 0.f;
-            for (int c0 = 0; c0 < kTK; c0 += 16) {
-                uint32_t r[16];
-                q4t::ld16(sc + c0, r);
-                q4t::ld_wait();
 #pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    const float v0 = (mask && key0 + c0 + e > pq) ? -INFINITY : __uint_as_float(r[e]);
-                    const float v1 = (mask && key0 + c0 + e + 1 > pq) ? -INFINITY : __uint_as_float(r[e + 1]);
-                    const float e0 = exp2f(v0 - msub), e1 = exp2f(v1 - msub);
-                    sum += e0 + e1;
-                    pk[(c0 + e) >> 1] = pack_h2(e0, e1);
-                }
+            for (int i2 = 0; i2 < kTK / 4; ++i2) {
+                const float e0 = exp2f(__uint_as_float(r[2 * i2]) - msub);
+                const float e1 = exp2f(__uint_as_float(r[2 * i2 + 1]) - msub);
+                sum += e0 + e1;
+                r[i2] = pack_h2(e0, e1);
             }
             l = l * corr + sum;
             // P buffer st was read by O += P V of tile j - 2, and O is written
             // by that of tile j - 1
-            if (j >= 2 && !tc_wait(B, B.pv_done[st], ((j - 2) >> 1) & 1, err)) {
-                ok = false;
-                break;
-            }
-            if (j >= 1 && !tc_wait(B, B.pv_done[st ^ 1], ((j - 1) >> 1) & 1, err)) {
-                ok = false;
-                break;
-            }
+            if (j >= 2) bad = __any_sync(0xffffffffu, !tc_wait(B, B.pv_done[st], ((j - 2) >> 1) & 1, err));
+            if (j >= 1 && !bad) bad = __any_sync(0xffffffffu, !tc_wait(B, B.pv_done[st ^ 1], ((j - 1) >> 1) & 1, err));
+            const bool zero_tail = j == n_tiles - 1 && (n_keys & (kTK - 1));
+            if (zero_tail && !bad) bad = __any_sync(0xffffffffu, !tc_wait(B, B.v_full[st], (j >> 1) & 1, err));
+            if (bad) continue;  // to the pair's barrier of the next tile (or past the loop)
             q4t::fence_after();
             if (__any_sync(0xffffffffu, resc)) {  // the TMEM load / store is warp-collective
-                for (int c0 = 0; c0 < D; c0 += 16) {
-                    uint32_t r[16];
-                    q4t::ld16(lt + kColO + c0, r);
-                    q4t::ld_wait();
+                uint32_t o[D / 2];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * corr);
-                    q4t::st16(lt + kColO + c0, r);
-                }
+                for (int c0 = 0; c0 < D / 2; c0 += 16) q4t::ld16(lt + kColO + hf * (D / 2) + c0, o + c0);
+                q4t::ld_wait();
+#pragma unroll
+                for (int e = 0; e < D / 2; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * corr);
+#pragma unroll
+                for (int c0 = 0; c0 < D / 2; c0 += 16) q4t::st16(lt + kColO + hf * (D / 2) + c0, o + c0);
             }
 #pragma unroll
-            for (int c = 0; c < kTK / 2; c += 16) q4t::st16(lt + kColP + st * 64 + c, pk + c);
+            for (int c = 0; c < kTK / 4; c += 16) q4t::st16(lt + kColP + st * 64 + hf * (kTK / 4) + c, r + c);
             q4t::st_wait();
-            if (j == n_tiles - 1 && (n_keys & (kTK - 1))) {
+            if (zero_tail) {
                 // the last tile's value rows past n_keys: stale cache rows may
-                // hold anything, and 0 * NaN would reach O; zero them
-                if (!tc_wait(B, B.v_full[st], (j >> 1) & 1, err)) {
-                    ok = false;
-                    break;
-                }
-                const int vr = row;
-                if (vr >= n_keys - key0) {
-                    uint8_t* vt = v_s + st * kTTile;
+                // hold anything, and 0 * NaN would reach O; zero them (this
+                // thread: its row's slab hf)
+                if (row >= n_keys - j * kTK) {
+                    uint8_t* vt = v_s + st * kTTile + hf * 16384;
 #pragma unroll
-                    for (int c = 0; c < 8; ++c) {
-                        *reinterpret_cast<uint4*>(vt + sw_off(vr, c)) = make_uint4(0, 0, 0, 0);
-                        *reinterpret_cast<uint4*>(vt + 16384 + sw_off(vr, c)) = make_uint4(0, 0, 0, 0);
-                    }
+                    for (int c = 0; c < 8; ++c) *reinterpret_cast<uint4*>(vt + sw_off(row, c)) = make_uint4(0, 0, 0, 0);
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
             }
@@ -913,21 +945,27 @@ __global__ void __launch_bounds__(kTThreads, 1)
             __syncwarp();
             if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&B.p_full[st]));
         }
-        if (ok) {
+        // the row sum of both halves (both warps of the pair reach this barrier)
+        B.xsum[hf][row] = l;
+        bad = q4d::named_bar_or(pair_bar, 64, bad);
+        if (!bad) {
             const int last = n_tiles - 1;
             if (tc_wait(B, B.pv_done[last & 1], (last >> 1) & 1, err)) {
                 q4t::fence_after();
-                const float inv = 1.0f / l;
-                uint16_t* ar = a + (size_t)(tq0 + row) * Hq * D + (size_t)h * D;
+                const float inv = 1.0f / (B.xsum[0][row] + B.xsum[1][row]);
+                uint16_t* ar = a + (size_t)(tq0 + row) * Hq * D + (size_t)h * D + hf * (D / 2);
                 const bool live = tq0 + row < C;
-                for (int c0 = 0; c0 < D; c0 += 16) {
-                    uint32_t r[16];
-                    q4t::ld16(lt + kColO + c0, r);
-                    q4t::ld_wait();
+                uint32_t ro[D / 2];
+#pragma unroll
+                for (int c0 = 0; c0 < D / 2; c0 += 16) q4t::ld16(lt + kColO + hf * (D / 2) + c0, ro + c0);
+                q4t::ld_wait();
+#pragma unroll
+                for (int c0 = 0; c0 < D / 2; c0 += 16) {
+                    const uint32_t* rr = ro + c0;
                     uint32_t o[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        o[e] = pack_h2(__uint_as_float(r[2 * e]) * inv, __uint_as_float(r[2 * e + 1]) * inv);
+                        o[e] = pack_h2(__uint_as_float(rr[2 * e]) * inv, __uint_as_float(rr[2 * e + 1]) * inv);
                     if (live) {
                         *reinterpret_cast<uint4*>(ar + c0) = make_uint4(o[0], o[1], o[2], o[3]);
                         *reinterpret_cast<uint4*>(ar + c0 + 8) = make_uint4(o[4], o[5], o[6], o[7]);
@@ -1018,7 +1056,13 @@ q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_
     return Q4_OK;
 }
 
-size_t prefill_attn_cs_bytes(int chunk, int head_dim) { return (size_t)chunk * head_dim / 2 * 8; }
+// The chunk's rotation table, then (head_dim 128) the rotated query's hi / lo
+// parts for the tensor-core attention.
+static size_t cs_table_bytes(int chunk, int head_dim) { return ((size_t)chunk * head_dim / 2 * 8 + 255) & ~size_t(255); }
+
+size_t prefill_attn_cs_bytes(int chunk, int head_dim, int n_q_heads) {
+    return cs_table_bytes(chunk, head_dim) + (head_dim == 128 ? 2 * (size_t)n_q_heads * chunk * head_dim * 2 : 0);
+}
 
 q4_status prefill_attn_table(const int32_t* pos, int t0, int C, int head_dim, float theta, void* cs, cudaStream_t s) {
     q4a::prefill_cs_kernel<<<C, head_dim / 2, 0, s>>>(pos, t0, head_dim, log2((double)theta),
@@ -1030,19 +1074,25 @@ q4_status prefill_attn_table(const int32_t* pos, int t0, int C, int head_dim, fl
 
 q4_status prefill_attn_enqueue(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* k_cache,
                                uint16_t* v_cache, const int32_t* pos, int t0, int C, int Hq, int Hkv, int D,
-                               int max_seq, const void* cs, uint16_t* a, cudaStream_t s) {
+                               int max_seq, void* cs, uint16_t* a, cudaStream_t s) {
     const DeviceInfo* dev = nullptr;
     q4_status st = current_device(&dev);
     if (st != Q4_OK) return st;
     const float2* csp = static_cast<const float2*>(cs);
-    q4a::prefill_append_kernel<<<dim3(C, Hkv), D / 2, 0, s>>>(k, v, k_cache, v_cache, pos, t0, C, Hkv, D, max_seq,
-                                                              csp, dev->err_word);
+    // head_dim 128: the rotated query's hi / lo parts [2][Hq][C][128] after
+    // the rotation table (prefill_attn_cs_bytes sized the region for both)
+    uint16_t* qrot = D == 128 ? reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(cs) + cs_table_bytes(C, D)) : nullptr;
+    q4a::prefill_append_kernel<<<C, 256, 0, s>>>(k, v, k_cache, v_cache, pos, t0, C, Hkv, D, max_seq, csp, q, Hq,
+                                                 qrot, dev->err_word);
     cudaError_t e;
     if (D == 128) {
         // tcgen05 path: the caches as 2-D maps [Hkv * max_seq][128], boxes of
         // 64 head_dim x 128 positions with the 128-byte swizzle
-        CUtensorMap tmK, tmV;
+        CUtensorMap tmK, tmV, tmQ;
         const uint64_t rows = (uint64_t)Hkv * (uint64_t)max_seq;
+        if ((st = make_map(&tmQ, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, qrot, 128, 2 * (uint64_t)Hq * (uint64_t)C, 256, 64,
+                           q4a::kTQ, CU_TENSOR_MAP_SWIZZLE_128B)) != Q4_OK)
+            return st;
         if ((st = make_map(&tmK, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, k_cache, 128, rows, 256, 64, q4a::kTK,
                            CU_TENSOR_MAP_SWIZZLE_128B)) != Q4_OK)
             return st;
@@ -1055,7 +1105,7 @@ q4_status prefill_attn_enqueue(const uint16_t* q, const uint16_t* k, const uint1
         if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(prefill_attn_tc_kernel)");
         const dim3 grid(Hq, (C + q4a::kTQ - 1) / q4a::kTQ);
         q4a::prefill_attn_tc_kernel<<<grid, q4a::kTThreads, q4a::prefill_tc_smem(), s>>>(
-            tmK, tmV, q, pos, t0, C, Hq, Hq / Hkv, max_seq, csp, a, dev->err_word);
+            tmK, tmV, tmQ, pos, t0, C, Hq, Hq / Hkv, max_seq, a, dev->err_word);
     } else {
         static std::atomic<int> marks64[64];
         e = ensure_smem_attr(reinterpret_cast<const void*>(q4a::prefill_attn_kernel<64>), marks64,

@@ -494,7 +494,7 @@ PrefillLayout prefill_layout(const Dims& d, int chunk, const q4_layer_table* t) 
     l.part_bytes = pb;
     l.part = take(pb / 2 + 1);
     if (d.attn) {
-        l.cs = take(prefill_attn_cs_bytes(chunk, d.hd) / 2);
+        l.cs = take(prefill_attn_cs_bytes(chunk, d.hd, d.qN / d.hd) / 2);
         l.a = take(C * (d.qN > 0 ? d.qN : 1));
     }
     l.total = off;

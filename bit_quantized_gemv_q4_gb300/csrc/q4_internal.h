@@ -63,13 +63,15 @@ q4_status attn_validate(const q4_attention_desc& d);
 q4_status attn_enqueue(const q4_attention_desc& d, cudaStream_t s, bool compute_table);
 q4_status pos_advance(int32_t* pos, cudaStream_t s, int by = 1);
 // Prefill with attention: the chunk's rotation table (fp64 angles) in `cs`
-// (prefill_attn_cs_bytes), then per layer the cache append and the causal
-// attention of the chunk's tokens (positions *pos + t0 + t).
-size_t prefill_attn_cs_bytes(int chunk, int head_dim);
+// (prefill_attn_cs_bytes; for head_dim 128 followed by the rotated query's
+// fp16 hi / lo parts, which the append kernel writes), then per layer the
+// cache append and the causal attention of the chunk's tokens (positions
+// *pos + t0 + t).
+size_t prefill_attn_cs_bytes(int chunk, int head_dim, int n_q_heads);
 q4_status prefill_attn_table(const int32_t* pos, int t0, int C, int head_dim, float theta, void* cs, cudaStream_t s);
 q4_status prefill_attn_enqueue(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* k_cache,
                                uint16_t* v_cache, const int32_t* pos, int t0, int C, int Hq, int Hkv, int D,
-                               int max_seq, const void* cs, uint16_t* a, cudaStream_t s);
+                               int max_seq, void* cs, uint16_t* a, cudaStream_t s);
 
 // ---- dense GEMM on the grouped-GEMM kernel (q4_moe_gemm.cu) ---------------
 q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream);
