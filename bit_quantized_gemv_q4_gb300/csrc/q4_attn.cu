@@ -671,13 +671,17 @@ __global__ void __launch_bounds__(kFThreads) prefill_attn_kernel(const uint16_t*
 // their sum stays fp32.
 constexpr int kTQ = 128;              // query tokens per CTA (MMA M)
 constexpr int kTK = 128;              // key positions per tile (MMA N of the scores)
-constexpr int kTThreads = 384;        // warp 0: key tiles, warp 1: MMA, warp 2: value tiles, 4..11: softmax
+constexpr int kTThreads = 384;        // warp 0: key tiles, 1: score MMAs, 2: value tiles, 3: value MMAs,
+                                      // 4..11: softmax
 constexpr uint32_t kTTile = 32768;    // one 128 x 128 fp16 tile: two 64-wide 128-byte-swizzled slabs
-constexpr uint32_t kColO = 256;       // TMEM columns: scores 0..127 and 128..255, O 256..383,
-constexpr uint32_t kColP = 384;       //   P 384..447 and 448..511
+constexpr uint32_t kColS = 0;         // TMEM columns: scores 0..127, O 128..255, P 256..319 and
+constexpr uint32_t kColO = 128;       //   320..383, the query's hi part 384..447 and lo part 448..511
+constexpr uint32_t kColP = 256;       //   (fp16 pairs, the A operand of the score MMAs)
+constexpr uint32_t kColQ = 384;
 
 struct TcBars {
-    uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2], drain;
+    uint64_t q_full, q_tmem, s_free, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2], pv_done[2],
+        drain;
     uint32_t tmem_base;
     volatile int abort;
     float xmax[2][2][kTQ];  // [tile parity][column half][row]: the halves' row maxima
@@ -734,8 +738,10 @@ __global__ void __launch_bounds__(kTThreads, 1)
             q4d::mbar_init(q4d::smem_addr(&B.p_full[i]), 8);  // the softmax warps
             q4d::mbar_init(q4d::smem_addr(&B.pv_done[i]), 1);
         }
-        q4d::mbar_init(q4d::smem_addr(&B.drain), 1);
+        q4d::mbar_init(q4d::smem_addr(&B.drain), 2);  // both issuers' last MMAs
         q4d::mbar_init(q4d::smem_addr(&B.q_full), 1);
+        q4d::mbar_init(q4d::smem_addr(&B.q_tmem), 8);  // the softmax warps copied the query into TMEM
+        q4d::mbar_init(q4d::smem_addr(&B.s_free), 8);  // the softmax warps have read the scores
         B.abort = 0;
         q4d::fence_mbar_init();
     }
@@ -793,54 +799,71 @@ __global__ void __launch_bounds__(kTThreads, 1)
                     q4d::mbar_wait(q4d::smem_addr(&full[i & 1]), (i >> 1) & 1, nullptr);
             }
         }
-    } else if (warp == 1) {
+    } else if (warp == 1 || warp == 3) {
         // ------------------------------------------------ MMA issue
+        // Two issuing threads (one tcgen05.mma takes ~40 ns to issue from a
+        // thread): warp 1 the scores of every tile, warp 3 the value products.
         if (lane == 0) {
             const uint32_t id_s = q4t::idesc_f16_m128(kTK, 0), id_o = q4t::idesc_f16_m128(D, 1);
-            const uint32_t qh = q4d::smem_addr(qh_s), ql = q4d::smem_addr(ql_s);
-            // O += P_i V_i (A = P from tensor memory, B = the value tile MN-major)
-            auto pv = [&](int i) -> bool {
-                const int st = i & 1;
-                if (!tc_wait(B, B.p_full[st], (i >> 1) & 1, err) || !tc_wait(B, B.v_full[st], (i >> 1) & 1, err))
-                    return false;
-                q4t::fence_after();
-                const uint32_t vb = q4d::smem_addr(v_s + st * kTTile);
-#pragma unroll
-                for (int kk = 0; kk < kTK / 16; ++kk)
-                    q4t::mma_ts(tmem + kColO, tmem + kColP + st * 64 + 8 * kk,
-                                q4t::sw128_desc(vb + kk * 2048, 16384, 1024), id_o, (i > 0 || kk > 0) ? 1u : 0u);
-                q4t::commit(q4d::smem_addr(&B.v_empty[st]));
-                q4t::commit(q4d::smem_addr(&B.pv_done[st]));
-                return true;
-            };
-            bool ok = tc_wait(B, B.q_full, 0, err);
-            for (int j = 0; j < n_tiles && ok; ++j) {
-                const int st = j & 1;
-                // S_j into score buffer st: the softmax released it with p_full
-                // of tile j - 2, waited for before O += P V of that tile
-                if (!tc_wait(B, B.k_full[st], (j >> 1) & 1, err)) {
-                    ok = false;
-                    break;
-                }
-                q4t::fence_after();
-                const uint32_t kb = q4d::smem_addr(k_s + st * kTTile);
-#pragma unroll
-                for (int part = 0; part < 2; ++part) {
-                    const uint32_t qa = part ? ql : qh;
-#pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (uint32_t)(kk >> 2) * 16384u + (uint32_t)(kk & 3) * 32u;
-                        q4t::mma_ss(tmem + st * kTK, q4t::sw128_desc(qa + off, 16, 1024),
-                                    q4t::sw128_desc(kb + off, 16, 1024), id_s, (part > 0 || kk > 0) ? 1u : 0u);
+            // every descriptor is a base plus a constant start-address step
+            // (16-byte units; the fields never carry: the tiles sit below
+            // 256 KB), computed once
+            bool ok = true;
+            if (warp == 1) {
+                const uint64_t dk0 = q4t::sw128_desc(q4d::smem_addr(k_s), 16, 1024);
+                const uint64_t dk1 = q4t::sw128_desc(q4d::smem_addr(k_s + kTTile), 16, 1024);
+                ok = tc_wait(B, B.q_tmem, 0, err);
+                for (int j = 0; j < n_tiles && ok; ++j) {
+                    const int st = j & 1;
+                    if (!tc_wait(B, B.k_full[st], (j >> 1) & 1, err)) {
+                        ok = false;
+                        break;
                     }
+                    // the score buffer is free once the softmax warps have read S_{j-1}
+                    if (j >= 1 && !tc_wait(B, B.s_free, (j - 1) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    q4t::fence_after();
+                    const uint64_t kd = st ? dk1 : dk0;
+#pragma unroll
+                    for (int part = 0; part < 2; ++part) {
+#pragma unroll
+                        for (int kk = 0; kk < D / 16; ++kk) {
+                            // A: 16 head_dim = 8 TMEM columns of the query part; B: 32
+                            // bytes within a 64-wide slab of the key tile, slabs 16 KB apart
+                            const uint64_t off = (uint64_t)(((kk >> 2) * 16384 + (kk & 3) * 32) / 16);
+                            q4t::mma_ts(tmem + kColS, tmem + kColQ + part * 64 + 8 * kk, kd + off, id_s,
+                                        (part > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    q4t::commit(q4d::smem_addr(&B.k_empty[st]));
+                    q4t::commit(q4d::smem_addr(&B.s_full[st]));
                 }
-                q4t::commit(q4d::smem_addr(&B.k_empty[st]));
-                q4t::commit(q4d::smem_addr(&B.s_full[st]));
-                if (j >= 1) ok = pv(j - 1);
+            } else {
+                const uint64_t dv0 = q4t::sw128_desc(q4d::smem_addr(v_s), 16384, 1024);
+                const uint64_t dv1 = q4t::sw128_desc(q4d::smem_addr(v_s + kTTile), 16384, 1024);
+                // O += P_i V_i (A = P from tensor memory, B = the value tile MN-major)
+                for (int i = 0; i < n_tiles && ok; ++i) {
+                    const int st = i & 1;
+                    if (!tc_wait(B, B.p_full[st], (i >> 1) & 1, err) ||
+                        !tc_wait(B, B.v_full[st], (i >> 1) & 1, err)) {
+                        ok = false;
+                        break;
+                    }
+                    q4t::fence_after();
+                    const uint64_t vd = st ? dv1 : dv0;
+                    const uint32_t pa = tmem + kColP + st * 64;
+                    q4t::mma_ts(tmem + kColO, pa, vd, id_o, i > 0 ? 1u : 0u);
+#pragma unroll
+                    for (int kk = 1; kk < kTK / 16; ++kk)  // 16 positions = 2048 bytes of the value tile
+                        q4t::mma_ts(tmem + kColO, pa + 8 * kk, vd + (uint64_t)(kk * 2048 / 16), id_o, 1u);
+                    q4t::commit(q4d::smem_addr(&B.v_empty[st]));
+                    q4t::commit(q4d::smem_addr(&B.pv_done[st]));
+                }
             }
-            if (ok) ok = pv(n_tiles - 1);
             if (!ok) B.abort = 1;
-            // every MMA issued has finished before the CTA winds down
+            // every MMA this thread issued has finished before the CTA winds down
             q4t::commit(q4d::smem_addr(&B.drain));
             q4d::mbar_wait(q4d::smem_addr(&B.drain), 0, nullptr);
         }
@@ -858,6 +881,30 @@ __global__ void __launch_bounds__(kTThreads, 1)
         const uint32_t lt = tmem + ((uint32_t)(qw * 32) << 16);
         const uint32_t pair_bar = 1 + qw;
         float m_ref = -INFINITY, l = 0.f;
+        {
+            // the query's part hf (0: hi, 1: lo) of this row into TMEM columns
+            // kColQ + 64 hf ..: the slabs' 16-byte chunks hold 8 consecutive
+            // head_dim values, i.e. 4 columns of fp16 pairs in order
+            bool qbad = __any_sync(0xffffffffu, !tc_wait(B, B.q_full, 0, err));
+            if (!qbad) {
+                const uint8_t* qs = hf ? ql_s : qh_s;
+                uint32_t qv[64];
+#pragma unroll
+                for (int c = 0; c < 16; ++c) {
+                    const uint4 w = *reinterpret_cast<const uint4*>(qs + (c >> 3) * 16384 + sw_off(row, c & 7));
+                    qv[4 * c] = w.x;
+                    qv[4 * c + 1] = w.y;
+                    qv[4 * c + 2] = w.z;
+                    qv[4 * c + 3] = w.w;
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < 64; c0 += 16) q4t::st16(lt + kColQ + hf * 64 + c0, qv + c0);
+                q4t::st_wait();
+                q4t::fence_before();
+                __syncwarp();
+                if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&B.q_tmem));
+            }
+        }
         // `bad` (a failed or skipped wait) is made warp-uniform after every
         // wait and pair-uniform at the pair's barrier, which both warps reach
         // once per tile: they leave the loop together, so neither waits on the
@@ -873,9 +920,12 @@ __global__ void __launch_bounds__(kTThreads, 1)
             if (!bad) {
                 q4t::fence_after();
 #pragma unroll
-                for (int c0 = 0; c0 < kTK / 2; c0 += 16)
-                    q4t::ld16(lt + (uint32_t)(st * kTK + hf * (kTK / 2) + c0), r + c0);
+                for (int c0 = 0; c0 < kTK / 2; c0 += 16) q4t::ld16(lt + kColS + hf * (kTK / 2) + c0, r + c0);
                 q4t::ld_wait();
+                // the scores are in registers: the MMA may write the next tile's
+                q4t::fence_before();
+                __syncwarp();
+                if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&B.s_free));
                 if (mask) {
 #pragma unroll
                     for (int e = 0; e < kTK / 2; ++e)
