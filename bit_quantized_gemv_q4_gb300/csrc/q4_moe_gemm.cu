@@ -425,13 +425,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // in pairs behind one wait: every dequant warp arrives on the
                 // A stages in step order, so the second step's a_full phase
                 // completes after the first's.  A completed-phase wait costs
-                // ~80 ns of the issuer's step.
+                // ~80 ns of the issuer's step.  In plain mode a deferred step
+                // holds its input stage until the issuer's next step (two
+                // steps on) is dequantised, whose codes need a stage of their
+                // own, and the A stage two steps on must be free: pairs only
+                // with 4 A stages and, in plain mode, 3 or more input stages
+                // (a model of the rings' hand-offs finds no deadlock then, and
+                // one with 2 input or 2 A stages).
+                const bool pairs = kATmem && AS >= 4 && (p.glu || IS >= 3);
                 int pend_s = -1, pend_a = 0;
                 for (int ks = ks0; ks < ks1; ++ks) {
                     const int s = ip.s, a = ap.s;
                     if (p.glu || ((ks - ks0) & 1) == r) {
                         const bool more = ks + (p.glu ? 1 : 2) < ks1;  // another step of this issuer follows
-                        if (kATmem && pend_s < 0 && more) {
+                        if (pairs && pend_s < 0 && more) {
                             pend_s = s;
                             pend_a = a;
                         } else {
@@ -867,11 +874,18 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     const size_t fixed = 1024 + (size_t)p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
     const size_t avail = (size_t)dev->smem_optin > fixed ? (size_t)dev->smem_optin - fixed : 0;
     int as = p.a_tmem ? q4g::kMaxAStages : glu ? 2 : 3, is = 0;
-    for (; as >= 2; --as) {
-        const size_t left = avail > (size_t)as * p.a_bytes ? avail - (size_t)as * p.a_bytes : 0;
-        is = (int)(left / p.in_bytes);
+    if (p.a_tmem) {
+        // the A stages live in TMEM: all of shared memory past the fixed part
+        // goes to the input ring
+        is = (int)(avail / p.in_bytes);
         if (is > q4g::kMaxInStages) is = q4g::kMaxInStages;
-        if (is >= 4 || as == 2) break;
+    } else {
+        for (; as >= 2; --as) {
+            const size_t left = avail > (size_t)as * p.a_bytes ? avail - (size_t)as * p.a_bytes : 0;
+            is = (int)(left / p.in_bytes);
+            if (is > q4g::kMaxInStages) is = q4g::kMaxInStages;
+            if (is >= 4 || as == 2) break;
+        }
     }
     if (as < 2 || is < 2)
         return fail(Q4_ERR_UNSUPPORTED, "K=%d: its scale/bias buffers leave no room for two pipeline stages", a.K);
