@@ -59,6 +59,9 @@ constexpr int kMaxAStages = 4;    // dequantised A ring (stage count set per lau
 constexpr int kDeqWarps = 8;
 constexpr int kEpiWarps = 4;
 constexpr int kUpMmaWarp = 2 + kDeqWarps + kEpiWarps;  // 14
+// Epilogue staging: per epilogue warp 16 columns x 32 rows of fp32, turned
+// from one value per lane and column into 8 consecutive outputs per lane
+constexpr uint32_t kEpiStageBytes = kEpiWarps * 16 * 32 * 4;
 constexpr int kDispWarp = kUpMmaWarp + 1;               // 15: releases each K step to the dequant warps
 constexpr int kThreads = (kDispWarp + 1) * 32;
 constexpr int kMaxExperts = 256;
@@ -94,6 +97,7 @@ struct Params {
     uint32_t x_off;                // X's offset in an input stage
     uint32_t sb_bytes;   // private per-thread scale/bias slots
     uint32_t stg_bytes;  // staging buffer: the unit's scale and bias blocks
+    int vec_out;         // epilogue staging tiles present (Y and residual 16-byte aligned, room left)
     int* err;
 };
 
@@ -250,6 +254,10 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int
     return un;
 }
 
+// SiLU(y) = y / (1 + e^-y) with the fast exponential and division (a few
+// ulp of fp32, far below the fp16 rounding of the result; y -> -inf gives 0).
+__device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.0f + __expf(-y)); }
+
 // Dequantise one word of 8 codes to 8 fp16 weights in k order.
 __device__ __forceinline__ uint4 dequant_word(uint32_t q, __half2 s2, __half2 b2) {
     const __half2 m1024 = __float2half2_rn(-1024.f), m64 = __float2half2_rn(-64.f);
@@ -282,7 +290,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* sb = reinterpret_cast<uint32_t*>(a_ring + (size_t)p.a_stages * p.a_bytes);
     const int IS = p.in_stages, AS = p.a_stages;
     uint8_t* stg = reinterpret_cast<uint8_t*>(sb) + p.sb_bytes;
-    Smem& sm = *reinterpret_cast<Smem*>(stg + p.stg_bytes);
+    float* epi_st = reinterpret_cast<float*>(stg + p.stg_bytes);  // vec_out only
+    Smem& sm = *reinterpret_cast<Smem*>(stg + p.stg_bytes + (p.vec_out ? kEpiStageBytes : 0u));
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
@@ -625,36 +634,124 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2) * p.acc_cols;
             // plain mode: the second issuer's accumulator holds the odd K steps
             const bool two = p.glu || p.ksteps >= 2;
-            for (int c0 = 0; c0 < un.tn; c0 += 16) {
-                uint32_t g[16], v[16];
-                tmem_ld16(t0 + c0, g);
-                if (two) tmem_ld16(t0 + p.acc_cols + c0, v);
-                tmem_ld_wait();
-                if (!p.glu && two) {
+            if (p.kparts > 1) {
+                // one K part: raw fp32 sums, reduced (and finished) by reduce_parts_kernel
+                const size_t pr = (size_t)p.R * p.N;
+                for (int c0 = 0; c0 < un.tn; c0 += 16) {
+                    uint32_t g[16], v[16];
+                    tmem_ld16(t0 + c0, g);
+                    if (two) tmem_ld16(t0 + p.acc_cols + c0, v);
+                    tmem_ld_wait();
+                    if (!p.glu && two) {
 #pragma unroll
-                    for (int c = 0; c < 16; ++c) g[c] = __float_as_uint(__uint_as_float(g[c]) + __uint_as_float(v[c]));
-                }
+                        for (int c = 0; c < 16; ++c) g[c] = __float_as_uint(__uint_as_float(g[c]) + __uint_as_float(v[c]));
+                    }
 #pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    if (c0 + c < un.tn) {
-                        const size_t o = (size_t)(un.r0 + c0 + c) * p.N + n;
-                        if (p.kparts > 1) {
-                            // one K part: raw fp32 sums, reduced (and finished) by reduce_parts_kernel
-                            const size_t pr = (size_t)p.R * p.N;
+                    for (int c = 0; c < 16; ++c) {
+                        if (c0 + c < un.tn) {
+                            const size_t o = (size_t)(un.r0 + c0 + c) * p.N + n;
                             p.part[(size_t)(un.kp * p.nmat) * pr + o] = __uint_as_float(g[c]);
                             if (p.glu) p.part[(size_t)(un.kp * p.nmat + 1) * pr + o] = __uint_as_float(v[c]);
-                            continue;
                         }
-                        float y = __uint_as_float(g[c]);
-                        if (p.glu) {
-                            const float up = __uint_as_float(v[c]);
-                            y = y / (1.0f + expf(-y)) * up;
+                    }
+                }
+            } else {
+                // 16 columns (tokens) at a time; the next 16 columns' tensor-memory
+                // loads are in flight while these are finished and stored.  With
+                // an aligned Y the values go through this warp's staging tile, so
+                // that each lane stores runs of 8 consecutive outputs (16 or 32
+                // bytes) instead of one 2- or 4-byte value per column.
+                float* ws = epi_st + q * (16 * 32);
+                const int nb = un.nt * kRows + q * 32;  // this warp's first weight row
+                uint32_t g[16], v[16] = {};
+                tmem_ld16(t0, g);
+                if (two) tmem_ld16(t0 + p.acc_cols, v);
+                for (int c0 = 0; c0 < un.tn; c0 += 16) {
+                    // the residuals this lane adds, loaded before the wait (runs j: column
+                    // (lane + 32 j) / 4, outputs 8 ((lane + 32 j) % 4) ..; scalar: column c)
+                    uint4 rv[2] = {};
+                    float rs[16];
+                    if (p.residual) {
+                        if (p.vec_out) {
+#pragma unroll
+                            for (int j = 0; j < 2; ++j) {
+                                const int k = lane + 32 * j, c = k >> 2;
+                                if (c0 + c < un.tn)
+                                    rv[j] = *reinterpret_cast<const uint4*>(
+                                        p.residual + (size_t)(un.r0 + c0 + c) * p.N + nb + (k & 3) * 8);
+                            }
+                        } else {
+#pragma unroll
+                            for (int c = 0; c < 16; ++c)
+                                rs[c] = c0 + c < un.tn
+                                            ? __half2float(__ushort_as_half(p.residual[(size_t)(un.r0 + c0 + c) * p.N + n]))
+                                            : 0.f;
                         }
-                        if (p.residual) y += __half2float(__ushort_as_half(p.residual[o]));
-                        if (p.out_f16)
-                            static_cast<uint16_t*>(p.Y)[o] = __half_as_ushort(__float2half_rn(y));
-                        else
-                            static_cast<float*>(p.Y)[o] = y;
+                    }
+                    tmem_ld_wait();
+                    float y[16], w[16];
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        y[c] = __uint_as_float(g[c]);
+                        w[c] = __uint_as_float(v[c]);
+                        if (!p.glu && two) y[c] += w[c];
+                    }
+                    if (c0 + 16 < un.tn) {
+                        tmem_ld16(t0 + c0 + 16, g);
+                        if (two) tmem_ld16(t0 + p.acc_cols + c0 + 16, v);
+                    }
+                    if (p.glu) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) y[c] = silu(y[c]) * w[c];
+                    }
+                    if (p.vec_out) {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) ws[c * 32 + lane] = y[c];
+                        __syncwarp();
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const int k = lane + 32 * j, c = k >> 2;
+                            if (c0 + c >= un.tn) continue;
+                            const float4 e0 = *reinterpret_cast<const float4*>(ws + c * 32 + (k & 3) * 8);
+                            const float4 e1 = *reinterpret_cast<const float4*>(ws + c * 32 + (k & 3) * 8 + 4);
+                            const size_t o = (size_t)(un.r0 + c0 + c) * p.N + nb + (k & 3) * 8;
+                            float e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
+                            if (p.residual) {
+                                const uint32_t rw[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&rw[i]));
+                                    e[2 * i] += f.x;
+                                    e[2 * i + 1] += f.y;
+                                }
+                            }
+                            if (p.out_f16) {
+                                uint32_t h[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i) {
+                                    const __half2 t = __floats2half2_rn(e[2 * i], e[2 * i + 1]);
+                                    h[i] = *reinterpret_cast<const uint32_t*>(&t);
+                                }
+                                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.Y) + o) = make_uint4(h[0], h[1], h[2], h[3]);
+                            } else {
+                                float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + o);
+                                d[0] = make_float4(e[0], e[1], e[2], e[3]);
+                                d[1] = make_float4(e[4], e[5], e[6], e[7]);
+                            }
+                        }
+                        __syncwarp();  // the staging tile is read before the next group writes it
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 16; ++c) {
+                            if (c0 + c >= un.tn) continue;
+                            const size_t o = (size_t)(un.r0 + c0 + c) * p.N + n;
+                            float yy = y[c];
+                            if (p.residual) yy += rs[c];
+                            if (p.out_f16)
+                                static_cast<uint16_t*>(p.Y)[o] = __half_as_ushort(__float2half_rn(yy));
+                            else
+                                static_cast<float*>(p.Y)[o] = yy;
+                        }
                     }
                 }
             }
@@ -827,6 +924,7 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.scales_u = a.scales_u;
     p.biases_u = a.biases_u;
     p.residual = a.residual;
+    p.vec_out = aligned16(a.Y) && (!a.residual || aligned16(a.residual)) ? 1 : 0;
     p.offsets = a.offsets;
     p.Y = a.Y;
     p.E = a.E;
@@ -871,27 +969,38 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.a_col0 = 256;
     p.a_bytes = p.a_tmem ? 0u : (uint32_t)p.nmat * q4g::kATileBytes;
     p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqWarps * 32 * (p.G + 1) * 4 + 127) & ~size_t(127));
-    const size_t fixed = 1024 + (size_t)p.sb_bytes + p.stg_bytes + sizeof(q4g::Smem);
-    const size_t avail = (size_t)dev->smem_optin > fixed ? (size_t)dev->smem_optin - fixed : 0;
-    int as = p.a_tmem ? q4g::kMaxAStages : glu ? 2 : 3, is = 0;
-    if (p.a_tmem) {
-        // the A stages live in TMEM: all of shared memory past the fixed part
-        // goes to the input ring
-        is = (int)(avail / p.in_bytes);
-        if (is > q4g::kMaxInStages) is = q4g::kMaxInStages;
-    } else {
-        for (; as >= 2; --as) {
-            const size_t left = avail > (size_t)as * p.a_bytes ? avail - (size_t)as * p.a_bytes : 0;
-            is = (int)(left / p.in_bytes);
+    // The epilogue's staging tiles when Y (and the residual) are 16-byte
+    // aligned and the rings keep their depth without them (else the
+    // epilogue stores one value per lane and column).
+    int as = 0, is = 0;
+    for (int stage_tiles = p.vec_out; stage_tiles >= 0; --stage_tiles) {
+        const size_t fixed = 1024 + (size_t)p.sb_bytes + p.stg_bytes + (stage_tiles ? q4g::kEpiStageBytes : 0u) +
+                             sizeof(q4g::Smem);
+        const size_t avail = (size_t)dev->smem_optin > fixed ? (size_t)dev->smem_optin - fixed : 0;
+        as = p.a_tmem ? q4g::kMaxAStages : glu ? 2 : 3;
+        is = 0;
+        if (p.a_tmem) {
+            // the A stages live in TMEM: all of shared memory past the fixed
+            // part goes to the input ring
+            is = (int)(avail / p.in_bytes);
             if (is > q4g::kMaxInStages) is = q4g::kMaxInStages;
-            if (is >= 4 || as == 2) break;
+        } else {
+            for (; as >= 2; --as) {
+                const size_t left = avail > (size_t)as * p.a_bytes ? avail - (size_t)as * p.a_bytes : 0;
+                is = (int)(left / p.in_bytes);
+                if (is > q4g::kMaxInStages) is = q4g::kMaxInStages;
+                if (is >= 4 || as == 2) break;
+            }
         }
+        p.vec_out = stage_tiles;
+        if (as >= 2 && is >= 2) break;
     }
     if (as < 2 || is < 2)
         return fail(Q4_ERR_UNSUPPORTED, "K=%d: its scale/bias buffers leave no room for two pipeline stages", a.K);
     p.in_stages = is;
     p.a_stages = as;
-    const size_t smem = fixed + (size_t)is * p.in_bytes + (size_t)as * p.a_bytes;
+    const size_t smem = 1024 + (size_t)p.sb_bytes + p.stg_bytes + (p.vec_out ? q4g::kEpiStageBytes : 0u) +
+                        sizeof(q4g::Smem) + (size_t)is * p.in_bytes + (size_t)as * p.a_bytes;
 
     CUtensorMap tmW, tmWu, tmX;
     const uint64_t wrows = (uint64_t)a.E * rows_e;
@@ -936,15 +1045,19 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
 // K parts for a dense GEMM whose output tiles do not fill the GPU: the
 // smallest divisor of the K steps that gives at least 152 units (one per SM
 // of a GB300; a fixed target keeps workspace sizes computable without a
-// device), with at least 4 K steps per unit.
+// device), with at least 4 K steps per unit.  Only for K of 2048 or more:
+// with fewer K steps the partial sums' round trip and the reduction launch
+// cost more than the idle SMs (CUDA-event timings of the Qwen3-0.6B shapes
+// at 512 tokens: K = 1024 is faster unsplit, K = 2048 and 3072 split).
 constexpr int kSplitTargetUnits = 152;
+constexpr int kSplitMinKSteps = 32;
 
 int gemm_split_parts(int M, int N, int K) {
     if (M < 1 || N < 128 || K < 64) return 1;
     const int units = ((M + q4g::kTN - 1) / q4g::kTN) * (N / q4g::kRows);
     const int nK = K / q4g::kKS;
     const int sms = kSplitTargetUnits;
-    if (units >= sms) return 1;
+    if (units >= sms || nK < kSplitMinKSteps) return 1;
     int best = 1;
     for (int d = 2; d <= nK / 4; ++d) {
         if (nK % d) continue;

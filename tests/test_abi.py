@@ -188,7 +188,8 @@ def test_gemm_and_prefill_validation(L):
     # at most 4 K steps), so one 256-byte slice
     assert n8 == 1024 + 2048 + 2048 + 2048 + 4096 + 256
     assert L.q4_gemm_workspace_bytes(512, 1024, 3072, 0) == 6 * 512 * 1024 * 4   # 32 tiles -> 6 parts of 8 K steps
-    assert L.q4_gemm_workspace_bytes(512, 3072, 1024, 1) == 2 * 2 * 512 * 3072 * 4
+    assert L.q4_gemm_workspace_bytes(512, 1024, 2048, 1) == 8 * 2 * 512 * 1024 * 4   # 32 tiles -> 8 parts of 4 K steps
+    assert L.q4_gemm_workspace_bytes(512, 3072, 1024, 1) == 0                     # 16 K steps: faster unsplit
     assert L.q4_gemm_workspace_bytes(2048, 2048, 1024, 0) == 0                    # 256 tiles: no split
     assert L.q4_gemm_workspace_bytes(512, 1024, 192, 0) == 0                      # 3 K steps: too few to split
     assert L.q4_prefill_workspace_bytes(ctypes.byref(t.t), 0) == 0

@@ -92,7 +92,7 @@ def test_gemm_residual_epilogue(in_place):
 def test_gemm_split_k_every_element(M):
     """Few output tiles: K split over units, fp32 partials, reduce kernel
     (plain fp32 and fp16, GLU, residual in place)."""
-    N, K = 256, 1024
+    N, K = 256, 2048
     W = q4synth.q4_matrix(550 + M, N, K)
     X = q4synth.activations(551 + M, M, K)
     y_ref, A = oracle.gemv(W.Wq, W.scales, W.biases, X)
