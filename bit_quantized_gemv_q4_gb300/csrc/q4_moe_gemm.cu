@@ -1043,12 +1043,14 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
 }  // namespace
 
 // K parts for a dense GEMM whose output tiles do not fill the GPU: the
-// smallest divisor of the K steps that gives at least 152 units (one per SM
-// of a GB300; a fixed target keeps workspace sizes computable without a
-// device), with at least 4 K steps per unit.  Only for K of 2048 or more:
+// largest divisor of the K steps whose units still fit one wave of 152 (one
+// per SM of a GB300; a fixed target keeps workspace sizes computable without
+// a device), with at least 4 K steps per unit.  Only for K of 2048 or more:
 // with fewer K steps the partial sums' round trip and the reduction launch
-// cost more than the idle SMs (CUDA-event timings of the Qwen3-0.6B shapes
-// at 512 tokens: K = 1024 is faster unsplit, K = 2048 and 3072 split).
+// cost more than the idle SMs.  CUDA-event timings of the Qwen3-0.6B shapes
+// at 512 tokens: K = 1024 is faster unsplit; o (K = 2048) takes 17.9 us in
+// 4 parts against 22.7 us in 8 (two waves) and 24.8 us unsplit, down
+// (K = 3072) 19.3 us in 4 parts against 22.8 us in 6 and 31.8 us unsplit.
 constexpr int kSplitTargetUnits = 152;
 constexpr int kSplitMinKSteps = 32;
 
@@ -1061,8 +1063,8 @@ int gemm_split_parts(int M, int N, int K) {
     int best = 1;
     for (int d = 2; d <= nK / 4; ++d) {
         if (nK % d) continue;
+        if (units * d > sms) break;
         best = d;
-        if (units * d >= sms) break;
     }
     return best;
 }

@@ -469,8 +469,9 @@ typedef struct q4_gemm_desc {
 } q4_gemm_desc;
 
 /* Workspace bytes that let q4_gemm split K for this shape (0: it would not
- * split).  The split aims at 152 units of work (one per GB300 SM) with at
- * least 4 K steps of 64 per unit. */
+ * split).  Only K of 2048 or more is split, into the most parts whose units
+ * still fit one wave of 152 (one per GB300 SM), at least 4 K steps of 64 per
+ * unit. */
 size_t q4_gemm_workspace_bytes(int M, int N, int K, q4_gemv_mode mode);
 
 /* Y = X W^T on the tensor cores.  N must be a multiple of 128 (else

@@ -187,8 +187,8 @@ def test_gemm_and_prefill_validation(L):
     # to 256 B, then the fp32 partials of split GEMMs: none here (K <= 256 is
     # at most 4 K steps), so one 256-byte slice
     assert n8 == 1024 + 2048 + 2048 + 2048 + 4096 + 256
-    assert L.q4_gemm_workspace_bytes(512, 1024, 3072, 0) == 6 * 512 * 1024 * 4   # 32 tiles -> 6 parts of 8 K steps
-    assert L.q4_gemm_workspace_bytes(512, 1024, 2048, 1) == 8 * 2 * 512 * 1024 * 4   # 32 tiles -> 8 parts of 4 K steps
+    assert L.q4_gemm_workspace_bytes(512, 1024, 3072, 0) == 4 * 512 * 1024 * 4   # 32 tiles -> 4 parts of 12 K steps
+    assert L.q4_gemm_workspace_bytes(512, 1024, 2048, 1) == 4 * 2 * 512 * 1024 * 4   # 32 tiles -> 4 parts of 8 K steps
     assert L.q4_gemm_workspace_bytes(512, 3072, 1024, 1) == 0                     # 16 K steps: faster unsplit
     assert L.q4_gemm_workspace_bytes(2048, 2048, 1024, 0) == 0                    # 256 tiles: no split
     assert L.q4_gemm_workspace_bytes(512, 1024, 192, 0) == 0                      # 3 K steps: too few to split
