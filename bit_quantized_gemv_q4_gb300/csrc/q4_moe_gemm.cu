@@ -97,6 +97,8 @@ struct Params {
     uint32_t x_off;                // X's offset in an input stage
     uint32_t sb_bytes;   // private per-thread scale/bias slots
     uint32_t stg_bytes;  // staging buffer: the unit's scale and bias blocks
+    int sb_global;       // the dequant warps read scales and biases from global memory (no staging;
+                         // the kernel instantiation with kSbGlobal)
     int vec_out;         // epilogue staging tiles present (Y and residual 16-byte aligned, room left)
     int* err;
 };
@@ -258,6 +260,21 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int
 // ulp of fp32, far below the fp16 rounding of the result; y -> -inf gives 0).
 __device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.0f + __expf(-y)); }
 
+// A weight row's scale (low half) and bias (high half) of Q4 group g.
+__device__ __forceinline__ uint32_t load_sb(const uint16_t* s, const uint16_t* b, int g) {
+    return (uint32_t)__ldg(s + g) | ((uint32_t)__ldg(b + g) << 16);
+}
+
+// The scales (qs) and biases (qb) of groups g .. g + 3 of a weight row whose
+// group count G is a multiple of 4 (8-byte loads); left as they are when g is
+// past the row's end.
+__device__ __forceinline__ void load_quad(const uint16_t* s, const uint16_t* b, int g, int G, uint2& qs, uint2& qb) {
+    if (g < G) {
+        qs = __ldg(reinterpret_cast<const uint2*>(s + g));
+        qb = __ldg(reinterpret_cast<const uint2*>(b + g));
+    }
+}
+
 // Dequantise one word of 8 codes to 8 fp16 weights in k order.
 __device__ __forceinline__ uint4 dequant_word(uint32_t q, __half2 s2, __half2 b2) {
     const __half2 m1024 = __float2half2_rn(-1024.f), m64 = __float2half2_rn(-64.f);
@@ -276,9 +293,12 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t q, __half2 s2, __half2 b2
 }
 
 // kATmem: the dequantised A tiles live in tensor memory (units of <= 64
-// tokens), else in shared memory; one instantiation per mode keeps each
-// role's loop free of the other's code and registers.
-template <bool kATmem>
+// tokens), else in shared memory.  kSbGlobal (A in shared memory only): the
+// dequant warps read the scales and biases from global memory instead of a
+// per-unit staging copy.  One instantiation per mode keeps each role's loop
+// free of the other's code and registers (a runtime choice between the two
+// scale sources measured slower than either).
+template <bool kATmem, bool kSbGlobal>
 __global__ void __launch_bounds__(kThreads, 1)
     q4_moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
                        const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Params p) {
@@ -352,9 +372,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const Unit un = decode_unit(sm, p, u);
                 const int wrow = un.e * p.rows_e + un.nt * kRows;
                 const int wrow_u = un.e * p.rows_e + p.up_off + un.nt * kRows;
-                // the staging buffer is free once every dequant warp has read the previous unit's values
-                if (uu > 0 && !wait_bar(sm, sm.sb_empty, (uu - 1) & 1, p.err)) break;
-                {
+                if constexpr (kSbGlobal) {
+                    // the dequant warps read the scales and biases from global
+                    // memory: bring the unit's rows into L2
+                    for (int m = 0; m < p.nmat; ++m) {
+                        const size_t r = (size_t)(m ? wrow_u : wrow) * p.G;
+                        q4d::bulk_prefetch_l2((m ? p.scales_u : p.scales) + r, blk);
+                        q4d::bulk_prefetch_l2((m ? p.biases_u : p.biases) + r, blk);
+                    }
+                } else {
+                    // the staging buffer is free once every dequant warp has read the previous unit's values
+                    if (uu > 0 && !wait_bar(sm, sm.sb_empty, (uu - 1) & 1, p.err)) break;
                     const uint32_t fb = q4d::smem_addr(&sm.sb_full);
                     q4d::mbar_arrive_expect_tx(fb, (uint32_t)p.nmat * 2u * blk);
                     for (int m = 0; m < p.nmat; ++m) {
@@ -523,13 +551,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint16_t* bp = reinterpret_cast<const uint16_t*>(stg + (2 * m + 1) * blk) + (size_t)row * G;
         int it = 0, uu = 0;
         RingPos ip, ap;
+        const bool quads = (G & 3) == 0;
         for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++uu) {
+            // sb_global: this thread's row of scales and biases in global
+            // memory, read ahead of their use four groups to a load
+            // (G % 4 == 0) or two steps ahead one group at a time
+            const Unit un = decode_unit(sm, p, u);
+            const size_t gr = (size_t)(un.e * p.rows_e + (m ? p.up_off : 0) + un.nt * kRows + row) * G;
+            const uint16_t* sr = (m ? p.scales_u : p.scales) + gr;
+            const uint16_t* br = (m ? p.biases_u : p.biases) + gr;
+            if constexpr (!kSbGlobal) {
             // this unit's scales and biases, from the staging buffer into private slots
             if (!__all_sync(0xffffffffu, wait_bar(sm, sm.sb_full, uu & 1, p.err))) {
                 sm.abort = 1;
                 break;
             }
-            if ((G & 3) == 0) {
+            if (quads) {
                 for (int g = 0; g < G; g += 4) {  // 8-byte loads: 4 values of a row
                     const uint2 s4 = *reinterpret_cast<const uint2*>(sp + g);
                     const uint2 b4 = *reinterpret_cast<const uint2*>(bp + g);
@@ -543,10 +580,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             __syncwarp();
             if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&sm.sb_empty));
+            }
             bool ok = true;
-            const int ks0 = (u % p.kparts) * p.ksteps, ks1 = ks0 + p.ksteps;
+            const int ks0 = un.kp * p.ksteps, ks1 = ks0 + p.ksteps;
+            uint2 qs[2] = {}, qb[2] = {};  // [0] the four groups holding step ks, [1] the next four
+            uint32_t sb0 = 0, sb1 = 0;     // G % 4 != 0: steps ks and ks + 1
+            if constexpr (kSbGlobal) {
+                if (quads) {
+                    load_quad(sr, br, ks0 & ~3, G, qs[0], qb[0]);
+                    load_quad(sr, br, (ks0 & ~3) + 4, G, qs[1], qb[1]);
+                } else {
+                    sb0 = load_sb(sr, br, ks0);
+                    sb1 = ks0 + 1 < ks1 ? load_sb(sr, br, ks0 + 1) : 0u;
+                }
+            }
             for (int ks = ks0; ks < ks1; ++ks, ++it) {
                 const int s = ip.s, a = ap.s;
+                uint32_t sbv;
+                if constexpr (!kSbGlobal) {
+                    sbv = my_sb[ks];
+                } else if (quads) {
+                    if ((ks & 3) == 0 && ks != ks0) {
+                        qs[0] = qs[1];
+                        qb[0] = qb[1];
+                        load_quad(sr, br, ks + 4, G, qs[1], qb[1]);
+                    }
+                    const int j = ks & 3;
+                    const uint32_t sw = j < 2 ? qs[0].x : qs[0].y, bw = j < 2 ? qb[0].x : qb[0].y;
+                    sbv = (j & 1) ? prmt(sw, bw, 0x7632) : prmt(sw, bw, 0x5410);
+                } else {
+                    sbv = sb0;
+                    sb0 = sb1;
+                    sb1 = ks + 2 < ks1 ? load_sb(sr, br, ks + 2) : 0u;
+                }
                 // released by the dispatch thread: input stage s landed and A stage a is free
                 const bool w = wait_bar(sm, sm.go[a], ap.r & 1, p.err);
                 if (!__all_sync(0xffffffffu, w)) {
@@ -557,7 +623,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint8_t* st = in_ring + (size_t)s * p.in_bytes;
                 uint8_t* at = a_ring + (size_t)a * p.a_bytes;
                 const int w0 = p.glu ? 0 : 4 * part, nw = p.glu ? 8 : 4;
-                const uint32_t sbv = my_sb[ks];
                 const __half sh = __ushort_as_half((uint16_t)(sbv & 0xFFFF));
                 const __half bh = __ushort_as_half((uint16_t)(sbv >> 16));
                 const __half2 s2 = __halves2half2(sh, sh), b2 = __halves2half2(bh, bh);
@@ -943,13 +1008,14 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.kparts = a.kparts > 1 ? a.kparts : 1;
     p.ksteps = p.nK / p.kparts;
     p.part = a.part;
-    p.stg_bytes = (uint32_t)(((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127));
     p.err = dev->err_word;
 
-    // Rings: an A ring of 3 stages (2 in GLU mode, whose stages are twice the
-    // size), which turn over in a few hundred ns, and an input ring as deep as
-    // the rest of shared memory allows (up to 16): an input stage waits ~1 us
-    // for its codes, so its depth sets the K-step rate; at least 2 of each.
+    // Rings: an A ring of up to 4 stages (4 in tensor memory; in shared
+    // memory 4 when the scales come from global memory, else 3, or 2 in GLU
+    // mode, whose stages are twice the size), giving up stages until the
+    // input ring has 4, and an input ring as deep as the rest of shared
+    // memory allows (up to 16): an input stage waits ~1 us for its codes,
+    // so its depth sets the K-step rate; at least 2 of each.
     // Tokens per unit: a routed launch with few rows per expert takes a
     // smaller X box, so its input stages are smaller and the ring deeper (an
     // expert with more rows than that takes more units).
@@ -969,7 +1035,18 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.acc_cols = p.a_tmem ? (uint32_t)p.tn : (uint32_t)q4g::kTN;
     p.a_col0 = 256;
     p.a_bytes = p.a_tmem ? 0u : (uint32_t)p.nmat * q4g::kATileBytes;
-    p.sb_bytes = (uint32_t)(((size_t)q4g::kDeqWarps * 32 * (p.G + 1) * 4 + 127) & ~size_t(127));
+    // The dequant warps keep each unit's scales and biases in shared memory
+    // (a staging block the TMA thread fills, copied into private per-thread
+    // slots), except with A in shared memory when that would take more than
+    // 32 KB: then they read them from global memory (four groups to a load,
+    // the unit's rows prefetched into L2), which leaves the room to the A
+    // and input rings.  Staged values cost nothing at a unit's start, which
+    // counts for units of few K steps.
+    const size_t stg_need = ((size_t)p.nmat * 2 * q4g::kRows * p.G * 2 + 127) & ~size_t(127);
+    const size_t sb_need = ((size_t)q4g::kDeqWarps * 32 * (p.G + 1) * 4 + 127) & ~size_t(127);
+    p.sb_global = !p.a_tmem && stg_need + sb_need > 32768 ? 1 : 0;
+    p.stg_bytes = p.sb_global ? 0u : (uint32_t)stg_need;
+    p.sb_bytes = p.sb_global ? 0u : (uint32_t)sb_need;
     // The epilogue's staging tiles when Y (and the residual) are 16-byte
     // aligned and the rings keep their depth without them (else the
     // epilogue stores one value per lane and column).
@@ -978,7 +1055,7 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
         const size_t fixed = 1024 + (size_t)p.sb_bytes + p.stg_bytes + (stage_tiles ? q4g::kEpiStageBytes : 0u) +
                              sizeof(q4g::Smem);
         const size_t avail = (size_t)dev->smem_optin > fixed ? (size_t)dev->smem_optin - fixed : 0;
-        as = p.a_tmem ? q4g::kMaxAStages : glu ? 2 : 3;
+        as = p.a_tmem || p.sb_global ? q4g::kMaxAStages : glu ? 2 : 3;
         is = 0;
         if (p.a_tmem) {
             // the A stages live in TMEM: all of shared memory past the fixed
@@ -1022,13 +1099,16 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (a.offsets)
         q4g::check_routing_kernel<<<(a.R + 255) / 256 < dev->sms ? (a.R + 255) / 256 : dev->sms, 256, 0, s>>>(
             a.expert_ids, a.offsets, a.E, a.R, dev->err_word);
-    static std::atomic<int> smem_marks[2][64];
-    const void* kern = p.a_tmem ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<true>)
-                                : reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false>);
-    cudaError_t e = ensure_smem_attr(kern, smem_marks[p.a_tmem], (int)smem);
+    static std::atomic<int> smem_marks[3][64];
+    const int inst = p.a_tmem ? 0 : p.sb_global ? 2 : 1;
+    const void* kern = inst == 0   ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<true, false>)
+                       : inst == 1 ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, false>)
+                                   : reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, true>);
+    cudaError_t e = ensure_smem_attr(kern, smem_marks[inst], (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
-    if (p.a_tmem) q4g::q4_moe_gemm_kernel<true><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
-    else q4g::q4_moe_gemm_kernel<false><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
+    if (inst == 0) q4g::q4_moe_gemm_kernel<true, false><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
+    else if (inst == 1) q4g::q4_moe_gemm_kernel<false, false><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
+    else q4g::q4_moe_gemm_kernel<false, true><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
     if (p.kparts > 1) {

@@ -419,14 +419,14 @@ typedef struct q4_moe_desc {
  * expert_ids: int32 [R], the expert of each row (checked against offsets on
  * the device; a mismatch latches Q4_ERR_DEVICE_CHECK).  Y: [R][N].
  * Runs on the tensor cores (tcgen05, fp16 x fp16 -> fp32), weights
- * dequantised to fp16 in shared memory, never in global memory.
+ * dequantised to fp16 in shared or tensor memory, never in global memory.
  * N must be a multiple of 128 (else Q4_ERR_UNSUPPORTED); Wq, scales, biases
- * and X must be 16-byte aligned (else Q4_ERR_MISALIGNED); a K whose scale/bias
- * buffers leave no room for two pipeline stages in shared memory (with 227 KB
- * per block and 128-token units: K above 3520 in GLU mode, 6464 in PLAIN mode;
- * launches with at most 48 routed rows per expert on average take 64- or
- * 32-token units, whose smaller stages admit somewhat larger K) returns
- * Q4_ERR_UNSUPPORTED. */
+ * and X must be 16-byte aligned (else Q4_ERR_MISALIGNED).  Launches with at
+ * most 48 routed rows per expert on average take 32- or 64-token units,
+ * which stage each unit's scales and biases in shared memory: a K whose
+ * staging leaves no room for two pipeline stages (with 227 KB per block:
+ * GLU above ~6300 (32-token units) or ~6000 (64), PLAIN above ~8800 or
+ * ~8400) returns Q4_ERR_UNSUPPORTED.  Larger units take any K. */
 q4_status q4_moe_gemm(const uint32_t *Wq, const uint16_t *scales, const uint16_t *biases,
                       const uint16_t *X, const int32_t *expert_ids, const int32_t *offsets,
                       void *Y, const q4_moe_desc *desc, q4_stream_t stream);
@@ -475,9 +475,8 @@ typedef struct q4_gemm_desc {
 size_t q4_gemm_workspace_bytes(int M, int N, int K, q4_gemv_mode mode);
 
 /* Y = X W^T on the tensor cores.  N must be a multiple of 128 (else
- * Q4_ERR_UNSUPPORTED); the shared-memory limit on K is that of q4_moe_gemm
- * (K above 3520 in GLU mode or 6464 in PLAIN mode returns
- * Q4_ERR_UNSUPPORTED).  Wq, scales, biases and X must be 16-byte aligned. */
+ * Q4_ERR_UNSUPPORTED); K any multiple of 64.  Wq, scales, biases and X must
+ * be 16-byte aligned. */
 q4_status q4_gemm(const q4_gemm_desc *desc, q4_stream_t stream);
 
 /* Workspace bytes q4_prefill needs with chunks of `chunk` tokens (0 if the
@@ -498,8 +497,7 @@ size_t q4_prefill_workspace_bytes(const q4_layer_table *table, int chunk);
  * the last chunk's n', q, k, v and act (fp16 [chunk][width] each, in that
  * order, each slice 256-byte aligned), then room for the fp32 partial sums of
  * the GEMMs that split K (q4_gemm's workspace).  Every output width of the stack
- * except lm_head must be a multiple of 128 (else Q4_ERR_UNSUPPORTED), and the
- * GEMM's K limit applies.  Uses table->layers, hidden, norm_eps, lm_head,
+ * except lm_head must be a multiple of 128 (else Q4_ERR_UNSUPPORTED).  Uses table->layers, hidden, norm_eps, lm_head,
  * final_norm and logits_dtype; ignores M, workspace and plan, and of the
  * flags reads only Q4_DECODE_ATTENTION: with it, token t of the prompt sits
  * at position p = *table->pos + t, its RoPE-rotated key and value are

@@ -93,11 +93,15 @@ def test_256_experts_mostly_empty():
     check_plain(W, X, eids, Y, fp16_out=True, what="E=256")
 
 
-@pytest.mark.parametrize("mode,K", [(q4.Q4_GEMV_GLU, 3520), (q4.Q4_GEMV_PLAIN, 6464)])
-def test_largest_k(mode, K):
-    """The largest K whose scale/bias buffers leave two pipeline stages in
-    227 KB of shared memory per block."""
-    n_out, counts = 128, [3, 130]
+@pytest.mark.parametrize("mode,K,counts", [(q4.Q4_GEMV_GLU, 8192, [3, 130]), (q4.Q4_GEMV_PLAIN, 9728, [3, 130]),
+                                            (q4.Q4_GEMV_GLU, 6016, [2, 5, 0, 9]),
+                                            (q4.Q4_GEMV_PLAIN, 8384, [2, 5, 0, 9])])
+def test_large_k(mode, K, counts):
+    """128-token units (A in shared memory) read their scales and biases from
+    global memory, so K is not bounded there (GLU at 8192, PLAIN at 9728);
+    32-token units stage them in shared memory, whose room bounds K (GLU up
+    to about 6300, PLAIN about 8800 at 227 KB a block): a K just below that."""
+    n_out = 128
     rows = 2 * n_out if mode == q4.Q4_GEMV_GLU else n_out
     W = q4synth.q4_matrix(360 + K, rows, K, experts=len(counts))
     X = q4synth.activations(361 + K, sum(counts), K)
@@ -108,10 +112,9 @@ def test_largest_k(mode, K):
         check_plain(W, X, eids, Y, fp16_out=True, what=f"plain K={K}")
 
 
-def test_few_tokens_per_expert_fit_a_larger_k():
-    """Few routed rows per expert take 32-token units, whose smaller X boxes
-    leave room for the scale/bias buffers of a K that 128-token units cannot
-    hold (3584 in GLU mode)."""
+def test_few_tokens_per_expert_at_a_larger_k():
+    """Few routed rows per expert take 32-token units (A in tensor memory,
+    scales and biases staged) at K = 3584 in GLU mode."""
     n_out, K, counts = 128, 3584, [2, 5, 0, 9]
     W = q4synth.q4_matrix(370, 2 * n_out, K, experts=len(counts))
     X = q4synth.activations(371, sum(counts), K)
@@ -120,8 +123,9 @@ def test_few_tokens_per_expert_fit_a_larger_k():
 
 
 def test_k_beyond_shared_memory_is_refused():
-    """128-token units (64 rows for one expert) at K = 3584 in GLU mode."""
-    E, N, K, R = 1, 128, 3584, 64
+    """32-token units (8 routed rows for one expert) at K = 6656 in GLU mode:
+    the staged scales and biases leave no room for two input stages."""
+    E, N, K, R = 1, 128, 6656, 8
     Wq = torch.zeros(E, 2 * N, K // 8, dtype=torch.int32, device="cuda")
     s = torch.zeros(E, 2 * N, K // 64, dtype=torch.float16, device="cuda")
     X = torch.zeros(R, K, dtype=torch.float16, device="cuda")
