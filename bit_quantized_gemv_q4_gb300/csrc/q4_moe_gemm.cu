@@ -596,6 +596,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int ks = ks0; ks < ks1; ++ks, ++it) {
                 const int s = ip.s, a = ap.s;
+                // released by the dispatch thread: input stage s landed and A stage a is free
+                const bool w = wait_bar(sm, sm.go[a], ap.r & 1, p.err);
+                if (!__all_sync(0xffffffffu, w)) {
+                    sm.abort = 1;
+                    ok = false;
+                    break;
+                }
+                // (the next scale loads go out after the wait: an outstanding
+                // global load held the acquire wait up by its latency)
                 uint32_t sbv;
                 if constexpr (!kSbGlobal) {
                     sbv = my_sb[ks];
@@ -612,13 +621,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                     sbv = sb0;
                     sb0 = sb1;
                     sb1 = ks + 2 < ks1 ? load_sb(sr, br, ks + 2) : 0u;
-                }
-                // released by the dispatch thread: input stage s landed and A stage a is free
-                const bool w = wait_bar(sm, sm.go[a], ap.r & 1, p.err);
-                if (!__all_sync(0xffffffffu, w)) {
-                    sm.abort = 1;
-                    ok = false;
-                    break;
                 }
                 const uint8_t* st = in_ring + (size_t)s * p.in_bytes;
                 uint8_t* at = a_ring + (size_t)a * p.a_bytes;
