@@ -416,11 +416,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1 || warp == kUpMmaWarp) {
         // ------------------------------------------------------------ MMA
         // Two issuing threads (a thread issues a tcgen05.mma of N <= 64 in
-        // ~46 cycles at best, more beside the dequant warps on its SMSP, while
-        // the SM accepts them faster, so one thread would set the pace).  GLU: issuer r owns matrix r (gate, up)
-        // for every K step.  Plain: both own the one matrix, issuer r the K
-        // steps of parity r of each unit, into an accumulator of its own (the
-        // columns the up matrix has in GLU mode); the epilogue adds the two.
+        // ~46 cycles at best, more beside the dequant warps on its SMSP,
+        // while the SM accepts them faster, so one thread would set the
+        // pace).  GLU: issuer r owns matrix r (gate, up) for every K step.
+        // Plain: both own the one matrix, issuer r the K steps of parity r of
+        // each unit, into an accumulator of its own (the columns the up
+        // matrix has in GLU mode); the epilogue adds the two.
         const int r = warp == 1 ? 0 : 1;
         const int mi = p.glu ? r : 0;
         if (lane == 0) {
