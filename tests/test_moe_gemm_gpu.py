@@ -94,13 +94,17 @@ def test_256_experts_mostly_empty():
 
 
 @pytest.mark.parametrize("mode,K,counts", [(q4.Q4_GEMV_GLU, 8192, [3, 130]), (q4.Q4_GEMV_PLAIN, 9728, [3, 130]),
+                                            (q4.Q4_GEMV_GLU, 1088, [3, 130]), (q4.Q4_GEMV_PLAIN, 1600, [3, 130]),
                                             (q4.Q4_GEMV_GLU, 6016, [2, 5, 0, 9]),
                                             (q4.Q4_GEMV_PLAIN, 8384, [2, 5, 0, 9])])
 def test_large_k(mode, K, counts):
     """128-token units (A in shared memory) read their scales and biases from
-    global memory, so K is not bounded there (GLU at 8192, PLAIN at 9728);
-    32-token units stage them in shared memory, whose room bounds K (GLU up
-    to about 6300, PLAIN about 8800 at 227 KB a block): a K just below that."""
+    global memory once staging them would take more than 32 KB, so K is not
+    bounded there (GLU at 8192, PLAIN at 9728; at 1088 and 1600 the group
+    count is not a multiple of 4, which takes the one-group loads instead of
+    the four-group ones); 32-token units stage them in shared memory, whose
+    room bounds K (GLU up to about 6300, PLAIN about 8800 at 227 KB a block):
+    a K just below that."""
     n_out = 128
     rows = 2 * n_out if mode == q4.Q4_GEMV_GLU else n_out
     W = q4synth.q4_matrix(360 + K, rows, K, experts=len(counts))

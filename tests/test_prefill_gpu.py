@@ -66,6 +66,26 @@ def test_gemm_plain_every_element(M, out_dtype):
     assert_parity(Y, y_ref, A, fp16_out=bool(out_dtype), what=f"gemm M={M}")
 
 
+@pytest.mark.parametrize("M,K", [(300, 1600), (130, 4160)])
+def test_gemm_scales_from_global_every_element(M, K):
+    """K large enough that the dense GEMM reads each row's scales and biases
+    from global memory instead of staging them: K = 1600 (25 groups: one-group
+    loads) and 4160 (65 groups), plain with a residual in place and GLU, every
+    element against the oracle."""
+    N = 256
+    W = q4synth.q4_matrix(580 + K, N, K)
+    X = q4synth.activations(581 + K, M, K)
+    y_ref, A = oracle.gemv(W.Wq, W.scales, W.biases, X)
+    R = q4synth.activations(582 + K, M, N)
+    Y = run_gemm(W, X, out_dtype=q4.Q4_F16, residual=R, in_place=True)
+    r = R.astype(np.float64)
+    assert_parity(Y, r + y_ref, A + np.abs(r), fp16_out=True, what=f"global scales M={M} K={K}")
+    gate, up = q4synth.q4_matrix(583 + K, N, K), q4synth.q4_matrix(584 + K, N, K)
+    H = run_gemm(gate, X, q4.Q4_GEMV_GLU, q4.Q4_F16, up=up)
+    act, A2 = glu_ref(gate, up, X)
+    assert_parity(H, act, A2, fp16_out=True, what=f"global scales glu M={M} K={K}")
+
+
 @pytest.mark.parametrize("M", [5, 130])
 def test_gemm_glu_separate_matrices(M):
     N, K = 384, 256
