@@ -598,9 +598,19 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
             rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.attn_norm, n, C, H, eps);
             cudaError_t e = cudaGetLastError();
             if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
-            if ((st = gemm_of(w.q, nullptr, n, C, q, nullptr, part, pb, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.k, nullptr, n, C, k, nullptr, part, pb, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.v, nullptr, n, C, v, nullptr, part, pb, s)) != Q4_OK) return st;
+            // q, k and v as one launch (their units share the GPU: at 512
+            // tokens each alone fills a quarter to half of it) unless one
+            // of them would split K
+            if (gemm_split_bytes(C, w.q.N, w.q.K, false) == 0 && gemm_split_bytes(C, w.k.N, w.k.K, false) == 0 &&
+                gemm_split_bytes(C, w.v.N, w.v.K, false) == 0) {
+                const q4_linear qkv[3] = {w.q, w.k, w.v};
+                void* const out[3] = {q, k, v};
+                if ((st = gemm_launch_multi(qkv, out, 3, n, C, reinterpret_cast<q4_stream_t>(s))) != Q4_OK) return st;
+            } else {
+                if ((st = gemm_of(w.q, nullptr, n, C, q, nullptr, part, pb, s)) != Q4_OK) return st;
+                if ((st = gemm_of(w.k, nullptr, n, C, k, nullptr, part, pb, s)) != Q4_OK) return st;
+                if ((st = gemm_of(w.v, nullptr, n, C, v, nullptr, part, pb, s)) != Q4_OK) return st;
+            }
             const uint16_t* o_in = q;
             if (d.attn) {
                 if ((st = prefill_attn_enqueue(q, k, v, w.k_cache, w.v_cache, table->pos, t0, C, w.q.N / d.hd,

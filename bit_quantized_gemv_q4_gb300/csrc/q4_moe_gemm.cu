@@ -45,8 +45,10 @@
 #include <cuda.h>
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
+#include <climits>
 
 #include "q4_device.cuh"
+
 #include "q4_internal.h"
 
 namespace q4g {
@@ -62,6 +64,7 @@ constexpr int kUpMmaWarp = 2 + kDeqWarps + kEpiWarps;  // 14
 // Epilogue staging: per epilogue warp 16 columns x 32 rows of fp32, turned
 // from one value per lane and column into 8 consecutive outputs per lane
 constexpr uint32_t kEpiStageBytes = kEpiWarps * 16 * 32 * 4;
+constexpr int kMaxSeg = 3;  // weight matrices one dense launch may cover
 constexpr int kDispWarp = kUpMmaWarp + 1;               // 15: releases each K step to the dequant warps
 constexpr int kThreads = (kDispWarp + 1) * 32;
 constexpr int kMaxExperts = 256;
@@ -97,6 +100,16 @@ struct Params {
     uint32_t x_off;                // X's offset in an input stage
     uint32_t sb_bytes;   // private per-thread scale/bias slots
     uint32_t stg_bytes;  // staging buffer: the unit's scale and bias blocks
+    // Dense PLAIN launches over several weight matrices of one input (q, k, v):
+    // segment i owns the global weight tiles from seg_t0[i] (INT_MAX for a
+    // matrix the launch does not have) to the next segment's first, its own
+    // tensor map (tmW, tmWu, tmW2), scales, biases, output and width.
+    int nseg;
+    int seg_t0[kMaxSeg];
+    const uint16_t* seg_s[kMaxSeg];
+    const uint16_t* seg_b[kMaxSeg];
+    void* seg_Y[kMaxSeg];
+    int seg_N[kMaxSeg];
     int sb_global;       // the dequant warps read scales and biases from global memory (no staging;
                          // the kernel instantiation with kSbGlobal)
     int vec_out;         // epilogue staging tiles present (Y and residual 16-byte aligned, room left)
@@ -231,6 +244,7 @@ __device__ __forceinline__ bool wait_bar(Smem& sm, uint64_t& bar, uint32_t parit
 
 struct Unit {
     int e, r0, tn, nt, kp;  // expert, first token row, valid tokens, output tile index, K part
+    int seg;                // weight matrix of a several-matrix launch (nt counts within it)
 };
 
 __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int u) {
@@ -252,8 +266,18 @@ __device__ __forceinline__ Unit decode_unit(const Smem& sm, const Params& p, int
     un.r0 = a + j * p.tn;
     un.tn = min(p.tn, b - un.r0);
     un.nt = u % p.n_tiles;
+    un.seg = 0;
     un.kp = kp;
     return un;
+}
+
+// The weight matrix of a several-matrix launch that owns the unit's output
+// tile, the tile made relative to it (only the roles that address weights,
+// scales or outputs need it).
+__device__ __forceinline__ void unit_seg(const Params& p, Unit& un) {
+    // seg_t0[i] of a matrix the launch does not have is INT_MAX
+    un.seg = (un.nt >= p.seg_t0[1] ? 1 : 0) + (un.nt >= p.seg_t0[2] ? 1 : 0);
+    un.nt -= un.seg == 0 ? 0 : un.seg == 1 ? p.seg_t0[1] : p.seg_t0[2];
 }
 
 // SiLU(y) = y / (1 + e^-y) with the fast exponential and division (a few
@@ -295,12 +319,14 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t q, __half2 s2, __half2 b2
 // kATmem: the dequantised A tiles live in tensor memory (units of <= 64
 // tokens), else in shared memory.  kSbGlobal (A in shared memory only): the
 // dequant warps read the scales and biases from global memory instead of a
-// per-unit staging copy.  One instantiation per mode keeps each role's loop
+// per-unit staging copy.  kMulti: a dense launch over several weight
+// matrices of one input (each unit finds its matrix from its output tile).  One instantiation per mode keeps each role's loop
 // free of the other's code and registers (a runtime choice between the two
 // scale sources measured slower than either).
-template <bool kATmem, bool kSbGlobal>
+template <bool kATmem, bool kSbGlobal, bool kMulti>
 __global__ void __launch_bounds__(kThreads, 1)
     q4_moe_gemm_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmWu,
+                       const __grid_constant__ CUtensorMap tmW2,
                        const __grid_constant__ CUtensorMap tmX, const __grid_constant__ Params p) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the swizzled tiles.
@@ -369,16 +395,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             RingPos ip;
             const uint32_t blk = (uint32_t)kRows * (uint32_t)p.G * 2u;  // one matrix's scales (or biases) of a unit
             for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++uu) {
-                const Unit un = decode_unit(sm, p, u);
+                Unit un = decode_unit(sm, p, u);
+                if constexpr (kMulti) unit_seg(p, un);
                 const int wrow = un.e * p.rows_e + un.nt * kRows;
                 const int wrow_u = un.e * p.rows_e + p.up_off + un.nt * kRows;
+                const CUtensorMap* mw = !kMulti || un.seg == 0 ? &tmW : un.seg == 1 ? &tmWu : &tmW2;
                 if constexpr (kSbGlobal) {
                     // the dequant warps read the scales and biases from global
                     // memory: bring the unit's rows into L2
                     for (int m = 0; m < p.nmat; ++m) {
                         const size_t r = (size_t)(m ? wrow_u : wrow) * p.G;
-                        q4d::bulk_prefetch_l2((m ? p.scales_u : p.scales) + r, blk);
-                        q4d::bulk_prefetch_l2((m ? p.biases_u : p.biases) + r, blk);
+                        q4d::bulk_prefetch_l2((m ? p.scales_u : kMulti ? p.seg_s[un.seg] : p.scales) + r, blk);
+                        q4d::bulk_prefetch_l2((m ? p.biases_u : kMulti ? p.seg_b[un.seg] : p.biases) + r, blk);
                     }
                 } else {
                     // the staging buffer is free once every dequant warp has read the previous unit's values
@@ -387,8 +415,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     q4d::mbar_arrive_expect_tx(fb, (uint32_t)p.nmat * 2u * blk);
                     for (int m = 0; m < p.nmat; ++m) {
                         const size_t r = (size_t)(m ? wrow_u : wrow) * p.G;
-                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m) * blk), (m ? p.scales_u : p.scales) + r, blk, fb);
-                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m + 1) * blk), (m ? p.biases_u : p.biases) + r, blk,
+                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m) * blk), (m ? p.scales_u : kMulti ? p.seg_s[un.seg] : p.scales) + r,
+                                      blk, fb);
+                        q4d::bulk_g2s(q4d::smem_addr(stg + (2 * m + 1) * blk), (m ? p.biases_u : kMulti ? p.seg_b[un.seg] : p.biases) + r, blk,
                                       fb);
                     }
                     ++staged;
@@ -400,7 +429,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t* st = in_ring + (size_t)s * p.in_bytes;
                     const uint32_t fb = q4d::smem_addr(&sm.in_full[s]);
                     q4d::mbar_arrive_expect_tx(fb, p.nmat * kCodesBytes + p.x_bytes);
-                    tma_load_2d(q4d::smem_addr(st), &tmW, ks * 32, wrow, fb);
+                    tma_load_2d(q4d::smem_addr(st), mw, ks * 32, wrow, fb);
                     if (p.glu) tma_load_2d(q4d::smem_addr(st + kCodesBytes), &tmWu, ks * 32, wrow_u, fb);
                     tma_load_2d(q4d::smem_addr(st + p.x_off), &tmX, ks * kKS, un.r0, fb);
                     ip.next(IS);
@@ -557,10 +586,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             // sb_global: this thread's row of scales and biases in global
             // memory, read ahead of their use four groups to a load
             // (G % 4 == 0) or two steps ahead one group at a time
-            const Unit un = decode_unit(sm, p, u);
+            Unit un = decode_unit(sm, p, u);
+            if constexpr (kSbGlobal && kMulti) unit_seg(p, un);  // (the staged scales need no weight row)
             const size_t gr = (size_t)(un.e * p.rows_e + (m ? p.up_off : 0) + un.nt * kRows + row) * G;
-            const uint16_t* sr = (m ? p.scales_u : p.scales) + gr;
-            const uint16_t* br = (m ? p.biases_u : p.biases) + gr;
+            const uint16_t* sr = (m ? p.scales_u : kMulti ? p.seg_s[un.seg] : p.scales) + gr;
+            const uint16_t* br = (m ? p.biases_u : kMulti ? p.seg_b[un.seg] : p.biases) + gr;
             if constexpr (!kSbGlobal) {
             // this unit's scales and biases, from the staging buffer into private slots
             if (!__all_sync(0xffffffffu, wait_bar(sm, sm.sb_full, uu & 1, p.err))) {
@@ -692,7 +722,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = q * 32 + lane;            // accumulator lane = weight row in the tile
         int acc_it = 0;
         for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++acc_it) {
-            const Unit un = decode_unit(sm, p, u);
+            Unit un = decode_unit(sm, p, u);
+            if constexpr (kMulti) unit_seg(p, un);
             const int buf = acc_it & 1;
             if (!__all_sync(0xffffffffu, wait_bar(sm, sm.acc_full[buf], (acc_it >> 1) & 1, p.err))) {
                 sm.abort = 1;
@@ -703,6 +734,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t t0 = tmem + ((uint32_t)(q * 32) << 16) + (uint32_t)(buf * 2) * p.acc_cols;
             // plain mode: the second issuer's accumulator holds the odd K steps
             const bool two = p.glu || p.ksteps >= 2;
+            // this unit's output: its row width and base
+#define yN (kMulti ? p.seg_N[un.seg] : p.N)
+#define Yp (kMulti ? p.seg_Y[un.seg] : p.Y)
             if (p.kparts > 1) {
                 // one K part: raw fp32 sums, reduced (and finished) by reduce_parts_kernel
                 const size_t pr = (size_t)p.R * p.N;
@@ -747,13 +781,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 const int k = lane + 32 * j, c = k >> 2;
                                 if (c0 + c < un.tn)
                                     rv[j] = *reinterpret_cast<const uint4*>(
-                                        p.residual + (size_t)(un.r0 + c0 + c) * p.N + nb + (k & 3) * 8);
+                                        p.residual + (size_t)(un.r0 + c0 + c) * yN + nb + (k & 3) * 8);
                             }
                         } else {
 #pragma unroll
                             for (int c = 0; c < 16; ++c)
                                 rs[c] = c0 + c < un.tn
-                                            ? __half2float(__ushort_as_half(p.residual[(size_t)(un.r0 + c0 + c) * p.N + n]))
+                                            ? __half2float(__ushort_as_half(p.residual[(size_t)(un.r0 + c0 + c) * yN + n]))
                                             : 0.f;
                         }
                     }
@@ -783,7 +817,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (c0 + c >= un.tn) continue;
                             const float4 e0 = *reinterpret_cast<const float4*>(ws + c * 32 + (k & 3) * 8);
                             const float4 e1 = *reinterpret_cast<const float4*>(ws + c * 32 + (k & 3) * 8 + 4);
-                            const size_t o = (size_t)(un.r0 + c0 + c) * p.N + nb + (k & 3) * 8;
+                            const size_t o = (size_t)(un.r0 + c0 + c) * yN + nb + (k & 3) * 8;
                             float e[8] = {e0.x, e0.y, e0.z, e0.w, e1.x, e1.y, e1.z, e1.w};
                             if (p.residual) {
                                 const uint32_t rw[4] = {rv[j].x, rv[j].y, rv[j].z, rv[j].w};
@@ -801,9 +835,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                                     const __half2 t = __floats2half2_rn(e[2 * i], e[2 * i + 1]);
                                     h[i] = *reinterpret_cast<const uint32_t*>(&t);
                                 }
-                                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.Y) + o) = make_uint4(h[0], h[1], h[2], h[3]);
+                                *reinterpret_cast<uint4*>(static_cast<uint16_t*>(Yp) + o) = make_uint4(h[0], h[1], h[2], h[3]);
                             } else {
-                                float4* d = reinterpret_cast<float4*>(static_cast<float*>(p.Y) + o);
+                                float4* d = reinterpret_cast<float4*>(static_cast<float*>(Yp) + o);
                                 d[0] = make_float4(e[0], e[1], e[2], e[3]);
                                 d[1] = make_float4(e[4], e[5], e[6], e[7]);
                             }
@@ -813,17 +847,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int c = 0; c < 16; ++c) {
                             if (c0 + c >= un.tn) continue;
-                            const size_t o = (size_t)(un.r0 + c0 + c) * p.N + n;
+                            const size_t o = (size_t)(un.r0 + c0 + c) * yN + n;
                             float yy = y[c];
                             if (p.residual) yy += rs[c];
                             if (p.out_f16)
-                                static_cast<uint16_t*>(p.Y)[o] = __half_as_ushort(__float2half_rn(yy));
+                                static_cast<uint16_t*>(Yp)[o] = __half_as_ushort(__float2half_rn(yy));
                             else
-                                static_cast<float*>(p.Y)[o] = yy;
+                                static_cast<float*>(Yp)[o] = yy;
                         }
                     }
                 }
             }
+#undef yN
+#undef Yp
             tc_fence_before();
             __syncwarp();
             if (lane == 0) q4d::mbar_arrive(q4d::smem_addr(&sm.acc_empty[buf]));
@@ -963,6 +999,15 @@ struct GroupedArgs {
     q4_dtype out_dtype;
     int kparts = 1;        // split K over this many units (dense only); 1 = no split
     float* part = nullptr; // kparts > 1: fp32 [kparts][nmat][R][N]
+    // Several weight matrices of one input (dense PLAIN, no residual, no
+    // split): matrix 0 is Wq / scales / biases / Y with N = seg_N[0], the
+    // others follow; N is then their total.
+    int nseg = 1;
+    const uint32_t* seg_Wq[q4g::kMaxSeg] = {};
+    const uint16_t* seg_s[q4g::kMaxSeg] = {};
+    const uint16_t* seg_b[q4g::kMaxSeg] = {};
+    void* seg_Y[q4g::kMaxSeg] = {};
+    int seg_N[q4g::kMaxSeg] = {};
 };
 
 q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
@@ -980,6 +1025,22 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (!aligned16(a.Wq) || !aligned16(a.X) || !aligned16(a.scales) || !aligned16(a.biases) ||
         (glu && (!aligned16(a.Wq_u) || !aligned16(a.scales_u) || !aligned16(a.biases_u))))
         return fail(Q4_ERR_MISALIGNED, "Wq, X, scales and biases must be 16-byte aligned");
+    if (a.nseg < 1 || a.nseg > q4g::kMaxSeg) return fail(Q4_ERR_INVALID_ARG, "nseg=%d", a.nseg);
+    if (a.nseg > 1) {
+        if (glu || a.offsets || a.residual || a.kparts > 1)
+            return fail(Q4_ERR_INVALID_ARG, "several matrices need dense PLAIN mode without residual or split");
+        int total = 0;
+        for (int i = 0; i < a.nseg; ++i) {
+            if (!a.seg_Wq[i] || !a.seg_s[i] || !a.seg_b[i] || !a.seg_Y[i])
+                return fail(Q4_ERR_INVALID_ARG, "NULL pointer of matrix %d", i);
+            if (a.seg_N[i] < 128 || a.seg_N[i] % 128)
+                return fail(Q4_ERR_UNSUPPORTED, "N=%d of matrix %d is not a multiple of 128", a.seg_N[i], i);
+            if (!aligned16(a.seg_Wq[i]) || !aligned16(a.seg_s[i]) || !aligned16(a.seg_b[i]))
+                return fail(Q4_ERR_MISALIGNED, "matrix %d: Wq, scales and biases must be 16-byte aligned", i);
+            total += a.seg_N[i];
+        }
+        if (total != a.N) return fail(Q4_ERR_INVALID_ARG, "N=%d is not the matrices' total %d", a.N, total);
+    }
     const int rows_e = a.offsets ? (glu ? 2 : 1) * a.N : a.N;
     if ((long long)a.E * rows_e > (1ll << 31)) return fail(Q4_ERR_UNSUPPORTED, "too many weight rows");
     const DeviceInfo* dev = nullptr;
@@ -994,6 +1055,23 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     p.biases_u = a.biases_u;
     p.residual = a.residual;
     p.vec_out = aligned16(a.Y) && (!a.residual || aligned16(a.residual)) ? 1 : 0;
+    p.nseg = a.nseg;
+    for (int i = 0; i < q4g::kMaxSeg; ++i) p.seg_t0[i] = i == 0 ? 0 : INT_MAX;
+    if (a.nseg == 1) {
+        p.seg_s[0] = a.scales;
+        p.seg_b[0] = a.biases;
+        p.seg_Y[0] = a.Y;
+        p.seg_N[0] = a.N;
+    } else {
+        for (int i = 0; i < a.nseg; ++i) {
+            p.seg_s[i] = a.seg_s[i];
+            p.seg_b[i] = a.seg_b[i];
+            p.seg_Y[i] = a.seg_Y[i];
+            p.seg_N[i] = a.seg_N[i];
+            if (i > 0) p.seg_t0[i] = p.seg_t0[i - 1] + a.seg_N[i - 1] / q4g::kRows;
+            if (!aligned16(a.seg_Y[i])) p.vec_out = 0;
+        }
+    }
     p.offsets = a.offsets;
     p.Y = a.Y;
     p.E = a.E;
@@ -1083,12 +1161,19 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     const size_t smem = 1024 + (size_t)p.sb_bytes + p.stg_bytes + (p.vec_out ? q4g::kEpiStageBytes : 0u) +
                         sizeof(q4g::Smem) + (size_t)is * p.in_bytes + (size_t)as * p.a_bytes;
 
-    CUtensorMap tmW, tmWu, tmX;
-    const uint64_t wrows = (uint64_t)a.E * rows_e;
-    st = make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq, (uint64_t)a.K / 2, wrows, (uint64_t)a.K / 2, 32,
-                  q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+    CUtensorMap tmW, tmWu, tmW2, tmX;
+    const uint64_t wrows = a.nseg > 1 ? (uint64_t)a.seg_N[0] : (uint64_t)a.E * rows_e;
+    st = make_map(&tmW, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.nseg > 1 ? a.seg_Wq[0] : a.Wq, (uint64_t)a.K / 2, wrows,
+                  (uint64_t)a.K / 2, 32, q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
     if (st != Q4_OK) return st;
     tmWu = tmW;
+    tmW2 = tmW;
+    // several matrices: each its own map over its own rows (tmWu, tmW2)
+    for (int i = 1; i < a.nseg; ++i) {
+        st = make_map(i == 1 ? &tmWu : &tmW2, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.seg_Wq[i], (uint64_t)a.K / 2,
+                      (uint64_t)a.seg_N[i], (uint64_t)a.K / 2, 32, q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+        if (st != Q4_OK) return st;
+    }
     if (glu && a.Wq_u != a.Wq) {
         st = make_map(&tmWu, CU_TENSOR_MAP_DATA_TYPE_UINT8, a.Wq_u, (uint64_t)a.K / 2, wrows, (uint64_t)a.K / 2, 32,
                       q4g::kRows, CU_TENSOR_MAP_SWIZZLE_NONE);
@@ -1102,16 +1187,27 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (a.offsets)
         q4g::check_routing_kernel<<<(a.R + 255) / 256 < dev->sms ? (a.R + 255) / 256 : dev->sms, 256, 0, s>>>(
             a.expert_ids, a.offsets, a.E, a.R, dev->err_word);
-    static std::atomic<int> smem_marks[3][64];
-    const int inst = p.a_tmem ? 0 : p.sb_global ? 2 : 1;
-    const void* kern = inst == 0   ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<true, false>)
-                       : inst == 1 ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, false>)
-                                   : reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, true>);
+    static std::atomic<int> smem_marks[5][64];
+    // instantiation: A in TMEM; A in shared memory with staged / global
+    // scales; the same two over several weight matrices
+    const int inst = p.a_tmem ? 0 : (p.sb_global ? 2 : 1) + (p.nseg > 1 ? 2 : 0);
+    const void* kern = inst == 0   ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<true, false, false>)
+                       : inst == 1 ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, false, false>)
+                       : inst == 2 ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, true, false>)
+                       : inst == 3 ? reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, false, true>)
+                                   : reinterpret_cast<const void*>(q4g::q4_moe_gemm_kernel<false, true, true>);
     cudaError_t e = ensure_smem_attr(kern, smem_marks[inst], (int)smem);
     if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(q4_moe_gemm_kernel)");
-    if (inst == 0) q4g::q4_moe_gemm_kernel<true, false><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
-    else if (inst == 1) q4g::q4_moe_gemm_kernel<false, false><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
-    else q4g::q4_moe_gemm_kernel<false, true><<<dev->sms, q4g::kThreads, smem, s>>>(tmW, tmWu, tmX, p);
+    const unsigned nb = dev->sms;
+    if (inst == 0) q4g::q4_moe_gemm_kernel<true, false, false><<<nb, q4g::kThreads, smem, s>>>(tmW, tmWu, tmW2, tmX, p);
+    else if (inst == 1)
+        q4g::q4_moe_gemm_kernel<false, false, false><<<nb, q4g::kThreads, smem, s>>>(tmW, tmWu, tmW2, tmX, p);
+    else if (inst == 2)
+        q4g::q4_moe_gemm_kernel<false, true, false><<<nb, q4g::kThreads, smem, s>>>(tmW, tmWu, tmW2, tmX, p);
+    else if (inst == 3)
+        q4g::q4_moe_gemm_kernel<false, false, true><<<nb, q4g::kThreads, smem, s>>>(tmW, tmWu, tmW2, tmX, p);
+    else
+        q4g::q4_moe_gemm_kernel<false, true, true><<<nb, q4g::kThreads, smem, s>>>(tmW, tmWu, tmW2, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
     if (p.kparts > 1) {
@@ -1156,6 +1252,36 @@ int gemm_split_parts(int M, int N, int K) {
 size_t gemm_split_bytes(int M, int N, int K, bool glu) {
     const int kp = gemm_split_parts(M, N, K);
     return kp > 1 ? (size_t)kp * (glu ? 2 : 1) * (size_t)M * N * 4 : 0;
+}
+
+q4_status gemm_launch_multi(const q4_linear* w, void* const* Y, int nseg, const uint16_t* X, int M,
+                            q4_stream_t stream) {
+    if (!w || !Y || !X) return fail(Q4_ERR_INVALID_ARG, "NULL pointer argument");
+    if (nseg < 1 || nseg > q4g::kMaxSeg) return fail(Q4_ERR_INVALID_ARG, "nseg=%d outside 1..%d", nseg, q4g::kMaxSeg);
+    if (M < 0) return fail(Q4_ERR_INVALID_ARG, "M=%d", M);
+    GroupedArgs a = {};
+    a.nseg = nseg;
+    a.N = 0;
+    for (int i = 0; i < nseg; ++i) {
+        if (w[i].K != w[0].K) return fail(Q4_ERR_INVALID_ARG, "matrix %d: K=%d, matrix 0: K=%d", i, w[i].K, w[0].K);
+        a.seg_Wq[i] = w[i].Wq;
+        a.seg_s[i] = w[i].scales;
+        a.seg_b[i] = w[i].biases;
+        a.seg_Y[i] = Y[i];
+        a.seg_N[i] = w[i].N;
+        a.N += w[i].N;
+    }
+    a.Wq = a.Wq_u = w[0].Wq;
+    a.scales = a.scales_u = w[0].scales;
+    a.biases = a.biases_u = w[0].biases;
+    a.X = X;
+    a.Y = Y[0];
+    a.E = 1;
+    a.K = w[0].K;
+    a.R = M;
+    a.mode = Q4_GEMV_PLAIN;
+    a.out_dtype = Q4_F16;
+    return launch_grouped(a, stream);
 }
 
 q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream) {
