@@ -93,12 +93,6 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
         : "memory");
 }
 
-// Bulk prefetch of global memory into L2; bytes a multiple of 16, address
-// 16-byte aligned.
-__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
-}
-
 // Same with an L2 eviction-priority hint (weights are streamed once).
 __device__ __forceinline__ void bulk_g2s_evict_first(uint32_t dst, const void* src,
                                                      uint32_t bytes, uint32_t bar,

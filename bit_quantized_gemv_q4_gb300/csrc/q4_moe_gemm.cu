@@ -284,6 +284,12 @@ __device__ __forceinline__ void unit_seg(const Params& p, Unit& un) {
 // ulp of fp32, far below the fp16 rounding of the result; y -> -inf gives 0).
 __device__ __forceinline__ float silu(float y) { return __fdividef(y, 1.0f + __expf(-y)); }
 
+// Bulk prefetch of global memory into L2; bytes a multiple of 16, address
+// 16-byte aligned.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // A weight row's scale (low half) and bias (high half) of Q4 group g.
 __device__ __forceinline__ uint32_t load_sb(const uint16_t* s, const uint16_t* b, int g) {
     return (uint32_t)__ldg(s + g) | ((uint32_t)__ldg(b + g) << 16);
@@ -405,8 +411,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // memory: bring the unit's rows into L2
                     for (int m = 0; m < p.nmat; ++m) {
                         const size_t r = (size_t)(m ? wrow_u : wrow) * p.G;
-                        q4d::bulk_prefetch_l2((m ? p.scales_u : kMulti ? p.seg_s[un.seg] : p.scales) + r, blk);
-                        q4d::bulk_prefetch_l2((m ? p.biases_u : kMulti ? p.seg_b[un.seg] : p.biases) + r, blk);
+                        bulk_prefetch_l2((m ? p.scales_u : kMulti ? p.seg_s[un.seg] : p.scales) + r, blk);
+                        bulk_prefetch_l2((m ? p.biases_u : kMulti ? p.seg_b[un.seg] : p.biases) + r, blk);
                     }
                 } else {
                     // the staging buffer is free once every dequant warp has read the previous unit's values
