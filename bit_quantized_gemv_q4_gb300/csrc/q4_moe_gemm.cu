@@ -195,6 +195,31 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* r) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// Warp-wide forms: the whole (converged) warp executes them and one elected
+// lane issues (the warp's values stay uniform, which a clean issue loop
+// measured ~13 % cheaper per MMA than one lane issuing alone).
+__device__ __forceinline__ void mma_f16_w(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, uint32_t acc) {
+    asm volatile(
+        "{ .reg .pred p, e; elect.sync _|e, 0xffffffff; setp.ne.b32 p, %4, 0;\n"
+        "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p; }" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_f16_tmem_a_w(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t acc) {
+    asm volatile(
+        "{ .reg .pred p, e; elect.sync _|e, 0xffffffff; setp.ne.b32 p, %4, 0;\n"
+        "  @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p; }" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_w(uint32_t bar) {
+    asm volatile(
+        "{ .reg .pred e; elect.sync _|e, 0xffffffff;\n"
+        "  @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0]; }" ::"r"(bar)
+        : "memory");
+}
+
 __device__ __forceinline__ void mma_commit(uint32_t bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                  : "memory");
@@ -459,7 +484,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // matrix has in GLU mode); the epilogue adds the two.
         const int r = warp == 1 ? 0 : 1;
         const int mi = p.glu ? r : 0;
-        if (lane == 0) {
+        // the whole warp runs the loop (uniform values); one elected lane issues
+        {
             int acc_it = 0;
             RingPos ip, ap;
             for (int u = blockIdx.x; u < U && !sm.abort; u += gridDim.x, ++acc_it) {
@@ -467,7 +493,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int npad = ((un.tn + 15) / 16) * 16;
                 const uint32_t idesc = idesc_f16(npad);
                 const int buf = acc_it & 1;
-                if (acc_it >= 2 && !wait_bar(sm, sm.acc_empty[buf], ((acc_it >> 1) - 1) & 1, p.err)) break;
+                if (acc_it >= 2 &&
+                    !__all_sync(0xffffffffu, wait_bar(sm, sm.acc_empty[buf], ((acc_it >> 1) - 1) & 1, p.err)))
+                    break;
                 tc_fence_after();
                 const uint32_t dm = tmem + (uint32_t)(buf * 2 + r) * p.acc_cols;
                 bool ok = true, first = true;
@@ -483,17 +511,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t at = tmem + p.a_col0 + (uint32_t)(a * 2 + mi) * 32u;
 #pragma unroll
                         for (int kk = 0; kk < kKS / 16; ++kk)
-                            mma_f16_tmem_a(dm, at + 8 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                            mma_f16_tmem_a_w(dm, at + 8 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
                     } else {
                         const uint32_t as = q4d::smem_addr(a_ring + (size_t)a * p.a_bytes);
                         const uint64_t ad = sw128_desc(as + mi * kATileBytes);
 #pragma unroll
                         for (int kk = 0; kk < kKS / 16; ++kk)
-                            mma_f16(dm, ad + 2 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
+                            mma_f16_w(dm, ad + 2 * kk, xd + 2 * kk, idesc, (!first || kk > 0) ? 1u : 0u);
                     }
                     first = false;
-                    mma_commit(q4d::smem_addr(&sm.in_empty[s]));
-                    mma_commit(q4d::smem_addr(&sm.a_empty[a]));
+                    mma_commit_w(q4d::smem_addr(&sm.in_empty[s]));
+                    mma_commit_w(q4d::smem_addr(&sm.a_empty[a]));
                 };
                 // With A in tensor memory (4 A stages) this issuer's steps go
                 // in pairs behind one wait: every dequant warp arrives on the
@@ -520,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // warp was released for input stage s (codes and X
                             // land together on in_full), so that one wait also
                             // covers the X tile.
-                            if (!wait_bar(sm, sm.a_full[a], ap.r & 1, p.err)) {
+                            if (!__all_sync(0xffffffffu, wait_bar(sm, sm.a_full[a], ap.r & 1, p.err))) {
                                 ok = false;
                                 break;
                             }
@@ -536,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ap.next(AS);
                 }
                 if (!ok) break;
-                mma_commit(q4d::smem_addr(&sm.acc_full[buf]));
+                mma_commit_w(q4d::smem_addr(&sm.acc_full[buf]));
             }
         }
     } else if (warp == kDispWarp) {
