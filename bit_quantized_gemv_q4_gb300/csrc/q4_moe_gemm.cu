@@ -1147,6 +1147,7 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     // stages go there (4 stages x 2 matrices x 32 columns), not into shared
     // memory, which then holds only the input ring.
     p.a_tmem = p.tn <= 64 ? 1 : 0;
+    if (p.a_tmem && p.nseg > 1) return fail(Q4_ERR_UNSUPPORTED, "several matrices need 128-token units");
     p.acc_cols = p.a_tmem ? (uint32_t)p.tn : (uint32_t)q4g::kTN;
     p.a_col0 = 256;
     p.a_bytes = p.a_tmem ? 0u : (uint32_t)p.nmat * q4g::kATileBytes;
