@@ -366,6 +366,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* a_ring = in_ring + (size_t)p.in_stages * p.in_bytes;
     uint32_t* sb = reinterpret_cast<uint32_t*>(a_ring + (size_t)p.a_stages * p.a_bytes);
     const int IS = p.in_stages, AS = p.a_stages;
+    // Plain mode, A in shared memory, staged scales: each half of the
+    // dequant warps takes every other K step whole (all 8 words of its rows)
+    // instead of half of every step, so a warp waits once per two steps;
+    // elsewhere all 8 warps take every step (with A in tensor memory this
+    // measured no faster and cost the GLU launches of the same kernel 5 %).
+    const bool step_split = !kATmem && !p.glu && !kSbGlobal;
+    const int deq_per_step = step_split ? kDeqWarps / 2 : kDeqWarps;  // dequant arrivals per K step
     uint8_t* stg = reinterpret_cast<uint8_t*>(sb) + p.sb_bytes;
     float* epi_st = reinterpret_cast<float*>(stg + p.stg_bytes);  // vec_out only
     Smem& sm = *reinterpret_cast<Smem*>(stg + p.stg_bytes + (p.vec_out ? kEpiStageBytes : 0u));
@@ -375,10 +382,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < IS; ++i) {
             q4d::mbar_init(q4d::smem_addr(&sm.in_full[i]), 1);
-            q4d::mbar_init(q4d::smem_addr(&sm.in_empty[i]), kDeqWarps + p.nmat);
+            q4d::mbar_init(q4d::smem_addr(&sm.in_empty[i]), deq_per_step + p.nmat);
         }
         for (int i = 0; i < AS; ++i) {
-            q4d::mbar_init(q4d::smem_addr(&sm.a_full[i]), kDeqWarps);
+            q4d::mbar_init(q4d::smem_addr(&sm.a_full[i]), deq_per_step);
             q4d::mbar_init(q4d::smem_addr(&sm.a_empty[i]), p.nmat);
             q4d::mbar_init(q4d::smem_addr(&sm.go[i]), 1);
         }
@@ -599,8 +606,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ------------------------------------------------------------ dequant
         // Thread dt owns weight row `row` of the tile -- the TMEM lane its warp
         // may write, 32 (warp % 4) + lane -- and half `part` of the row's 16
-        // (GLU: gate then up) or 8 (plain) words of each K step: in GLU mode
-        // all 8 words of matrix `part`, in plain mode words 4 part .. 4 part + 3.
+        // (GLU: gate then up) or 8 (plain) words of a K step: in GLU mode all
+        // 8 words of matrix `part` of every step; in plain mode with staged
+        // scales all 8 words of the steps of parity `part` (step_split), else
+        // words 4 part .. 4 part + 3 of every step.
         // Its scales/biases live in private shared slots (no cross-thread
         // sharing, so no barrier that an aborting warp could leave the others
         // waiting on).
@@ -661,6 +670,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             for (int ks = ks0; ks < ks1; ++ks, ++it) {
                 const int s = ip.s, a = ap.s;
+                if (step_split && ((ks - ks0) & 1) != part) {  // the other half's step
+                    ip.next(IS);
+                    ap.next(AS);
+                    continue;
+                }
                 // released by the dispatch thread: input stage s landed and A stage a is free
                 const bool w = wait_bar(sm, sm.go[a], ap.r & 1, p.err);
                 if (!__all_sync(0xffffffffu, w)) {
@@ -689,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t* st = in_ring + (size_t)s * p.in_bytes;
                 uint8_t* at = a_ring + (size_t)a * p.a_bytes;
-                const int w0 = p.glu ? 0 : 4 * part, nw = p.glu ? 8 : 4;
+                const int w0 = p.glu || step_split ? 0 : 4 * part, nw = p.glu || step_split ? 8 : 4;
                 const __half sh = __ushort_as_half((uint16_t)(sbv & 0xFFFF));
                 const __half bh = __ushort_as_half((uint16_t)(sbv >> 16));
                 const __half2 s2 = __halves2half2(sh, sh), b2 = __halves2half2(bh, bh);
