@@ -460,6 +460,64 @@ __global__ void rmsnorm_rows_kernel(const uint16_t* __restrict__ h, const uint16
     }
 }
 
+// A split GEMM's fp32 partial sums added in part order to the residual,
+// rounded to fp16 into h (in place over the residual), then the RMSNorm of
+// that row into n -- the reduce kernel's and rmsnorm_rows_kernel's
+// arithmetic in one pass over the row (one warp per row; the same lane owns
+// the same 8 values in both passes).  part: fp32 [kparts][rows][hidden].
+__global__ void reduce_norm_rows_kernel(const float* __restrict__ part, int kparts, uint16_t* h,
+                                        const uint16_t* __restrict__ gamma, uint16_t* __restrict__ n, int rows,
+                                        int hidden, float eps) {
+    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
+    if (warp >= rows) return;
+    const size_t pr = (size_t)rows * hidden;
+    uint4* hrow = reinterpret_cast<uint4*>(h + (size_t)warp * hidden);
+    const int nv = hidden / 8;
+    float ss = 0.f;
+    for (int i = lane; i < nv; i += 32) {
+        const size_t o = (size_t)warp * hidden + (size_t)i * 8;
+        float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int k = 0; k < kparts; ++k) {
+            const float4 a = *reinterpret_cast<const float4*>(part + (size_t)k * pr + o);
+            const float4 b = *reinterpret_cast<const float4*>(part + (size_t)k * pr + o + 4);
+            y[0] += a.x; y[1] += a.y; y[2] += a.z; y[3] += a.w;
+            y[4] += b.x; y[5] += b.y; y[6] += b.z; y[7] += b.w;
+        }
+        const uint4 rv = hrow[i];
+        const uint32_t rw[4] = {rv.x, rv.y, rv.z, rv.w};
+        uint32_t out[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&rw[j]));
+            const __half2 hv = __floats2half2_rn(y[2 * j] + r.x, y[2 * j + 1] + r.y);
+            out[j] = *reinterpret_cast<const uint32_t*>(&hv);
+            const float2 f = __half22float2(hv);
+            ss = fmaf(f.x, f.x, ss);
+            ss = fmaf(f.y, f.y, ss);
+        }
+        hrow[i] = make_uint4(out[0], out[1], out[2], out[3]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float r = rsqrtf(ss / (float)hidden + eps);
+    uint4* dst = reinterpret_cast<uint4*>(n + (size_t)warp * hidden);
+    const uint4* gv = reinterpret_cast<const uint4*>(gamma);
+    for (int i = lane; i < nv; i += 32) {
+        const uint4 v = hrow[i];
+        const uint4 g = gamma ? gv[i] : make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+            const float2 gg = __half22float2(*reinterpret_cast<const __half2*>(&gw[j]));
+            const __half2 hv = __floats2half2_rn(f.x * r * gg.x, f.y * r * gg.y);
+            o[j] = *reinterpret_cast<const uint32_t*>(&hv);
+        }
+        dst[i] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
 struct PrefillLayout {
     size_t n = 0, q = 0, k = 0, v = 0, act = 0, part = 0, part_bytes = 0, total = 0;
     size_t cs = 0, a = 0;  // with attention: the chunk's rotation table and attention output
@@ -523,6 +581,23 @@ q4_status gemm_of(const q4_linear& w, const q4_linear* up, const uint16_t* X, in
     g.workspace = part;
     g.workspace_bytes = part_bytes;
     return gemm_launch(&g, reinterpret_cast<q4_stream_t>(s));
+}
+
+// PLAIN GEMM with an fp16 residual (h = h + W x, in place) whose split-K
+// partials, when it splits, are left for reduce_norm_rows_kernel (*kparts > 1).
+q4_status gemm_res_parts(const q4_linear& w, const uint16_t* X, int M, uint16_t* h, void* part, size_t part_bytes,
+                         cudaStream_t s, int* kparts) {
+    q4_gemm_desc g = {};
+    g.M = M;
+    g.X = X;
+    g.w = w;
+    g.mode = Q4_GEMV_PLAIN;
+    g.out_dtype = Q4_F16;
+    g.Y = h;
+    g.residual = h;
+    g.workspace = part;
+    g.workspace_bytes = part_bytes;
+    return gemm_launch_parts(&g, reinterpret_cast<q4_stream_t>(s), kparts);
 }
 
 }  // namespace
@@ -593,11 +668,15 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
         const int nb = (C + 7) / 8;
         if (d.attn && (st = prefill_attn_table(table->pos, t0, C, d.hd, table->rope_theta, cs, s)) != Q4_OK)
             return st;
+        bool n_ready = false;  // the previous layer's down launch already wrote this layer's n
         for (int i = 0; i < d.L; ++i) {
             const q4_layer_weights& w = table->layers[i];
-            rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.attn_norm, n, C, H, eps);
-            cudaError_t e = cudaGetLastError();
-            if (e != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+            cudaError_t e;
+            if (!n_ready) {
+                rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.attn_norm, n, C, H, eps);
+                if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+            }
+            n_ready = false;
             // q, k and v as one launch (their units share the GPU: at 512
             // tokens each alone fills a quarter to half of it) unless one
             // of them would split K
@@ -618,11 +697,31 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
                     return st;
                 o_in = a_buf;
             }
-            if ((st = gemm_of(w.o, nullptr, o_in, C, hc, hc, part, pb, s)) != Q4_OK) return st;  // h' = h + Wo a
-            rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.ffn_norm, n, C, H, eps);
+            // h' = h + Wo a and n' = rms(h') ffn_norm: when the GEMM splits K,
+            // one kernel adds its partials to h and normalises (no separate
+            // reduce and RMSNorm launches)
+            int kp = 1;
+            if ((st = gemm_res_parts(w.o, o_in, C, hc, part, pb, s, &kp)) != Q4_OK) return st;
+            if (kp > 1)
+                reduce_norm_rows_kernel<<<nb, 256, 0, s>>>(static_cast<const float*>(part), kp, hc, w.ffn_norm, n, C,
+                                                           H, eps);
+            else
+                rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.ffn_norm, n, C, H, eps);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
             if ((st = gemm_of(w.gate, &w.up, n, C, act, nullptr, part, pb, s)) != Q4_OK) return st;
-            if ((st = gemm_of(w.down, nullptr, act, C, hc, hc, part, pb, s)) != Q4_OK) return st;  // h = h' + Wdown act
+            // h = h' + Wdown act; when it splits K (and a layer follows), the
+            // next layer's attention RMSNorm goes into the same kernel
+            if (i + 1 < d.L) {
+                if ((st = gemm_res_parts(w.down, act, C, hc, part, pb, s, &kp)) != Q4_OK) return st;
+                if (kp > 1) {
+                    reduce_norm_rows_kernel<<<nb, 256, 0, s>>>(static_cast<const float*>(part), kp, hc,
+                                                               table->layers[i + 1].attn_norm, n, C, H, eps);
+                    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
+                    n_ready = true;
+                }
+            } else if ((st = gemm_of(w.down, nullptr, act, C, hc, hc, part, pb, s)) != Q4_OK) {
+                return st;
+            }
         }
     }
     if (d.attn && T > 0 && (st = pos_advance(table->pos, s, T)) != Q4_OK) return st;

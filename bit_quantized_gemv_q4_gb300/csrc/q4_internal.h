@@ -75,6 +75,10 @@ q4_status prefill_attn_enqueue(const uint16_t* q, const uint16_t* k, const uint1
 
 // ---- dense GEMM on the grouped-GEMM kernel (q4_moe_gemm.cu) ---------------
 q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream);
+// The same, but when K splits (*kparts > 1) the fp32 partial sums are left
+// in the workspace ([kparts][M][N]) for the caller to add: no reduce kernel,
+// no epilogue (residual) applied.
+q4_status gemm_launch_parts(const q4_gemm_desc* d, q4_stream_t stream, int* kparts);
 // Y[i] = X W_i^T (fp16 [M][N_i]) for nseg <= 3 PLAIN matrices of one K, as
 // one launch (the units of all matrices share the GPU); no residual, no split.
 q4_status gemm_launch_multi(const q4_linear* w, void* const* Y, int nseg, const uint16_t* X, int M,

@@ -1047,6 +1047,7 @@ struct GroupedArgs {
     q4_dtype out_dtype;
     int kparts = 1;        // split K over this many units (dense only); 1 = no split
     float* part = nullptr; // kparts > 1: fp32 [kparts][nmat][R][N]
+    bool skip_reduce = false;  // kparts > 1: leave the partials for the caller to add
     // Several weight matrices of one input (dense PLAIN, no residual, no
     // split): matrix 0 is Wq / scales / biases / Y with N = seg_N[0], the
     // others follow; N is then their total.
@@ -1259,7 +1260,7 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
         q4g::q4_moe_gemm_kernel<false, true, true><<<nb, q4g::kThreads, smem, s>>>(tmW, tmWu, tmW2, tmX, p);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "grouped GEMM launch");
-    if (p.kparts > 1) {
+    if (p.kparts > 1 && !a.skip_reduce) {
         const size_t quads = (size_t)a.R * a.N / 4;
         q4g::reduce_parts_kernel<<<(unsigned)((quads + 255) / 256), 256, 0, s>>>(
             p.part, p.kparts, p.nmat, a.R, a.N, p.glu, a.residual, a.Y, p.out_f16);
@@ -1333,7 +1334,21 @@ q4_status gemm_launch_multi(const q4_linear* w, void* const* Y, int nseg, const 
     return launch_grouped(a, stream);
 }
 
+namespace {
+q4_status gemm_launch_impl(const q4_gemm_desc* d, q4_stream_t stream, bool skip_reduce, int* kparts);
+}  // namespace
+
 q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream) {
+    return gemm_launch_impl(d, stream, false, nullptr);
+}
+
+q4_status gemm_launch_parts(const q4_gemm_desc* d, q4_stream_t stream, int* kparts) {
+    return gemm_launch_impl(d, stream, true, kparts);
+}
+
+namespace {
+q4_status gemm_launch_impl(const q4_gemm_desc* d, q4_stream_t stream, bool skip_reduce, int* kparts) {
+    if (kparts) *kparts = 1;
     if (!d) return fail(Q4_ERR_INVALID_ARG, "desc is NULL");
     const bool glu = d->mode == Q4_GEMV_GLU;
     if (!d->w.Wq || !d->w.scales || !d->w.biases || !d->X || !d->Y)
@@ -1367,8 +1382,11 @@ q4_status gemm_launch(const q4_gemm_desc* d, q4_stream_t stream) {
             a.part = static_cast<float*>(d->workspace);
         }
     }
+    a.skip_reduce = skip_reduce && a.kparts > 1;
+    if (kparts) *kparts = a.kparts;
     return launch_grouped(a, stream);
 }
+}  // namespace
 
 }  // namespace q4i
 
