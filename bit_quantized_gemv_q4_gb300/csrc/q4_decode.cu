@@ -463,19 +463,27 @@ __global__ void rmsnorm_rows_kernel(const uint16_t* __restrict__ h, const uint16
 // A split GEMM's fp32 partial sums added in part order to the residual,
 // rounded to fp16 into h (in place over the residual), then the RMSNorm of
 // that row into n -- the reduce kernel's and rmsnorm_rows_kernel's
-// arithmetic in one pass over the row (one warp per row; the same lane owns
-// the same 8 values in both passes).  part: fp32 [kparts][rows][hidden].
-__global__ void reduce_norm_rows_kernel(const float* __restrict__ part, int kparts, uint16_t* h,
-                                        const uint16_t* __restrict__ gamma, uint16_t* __restrict__ n, int rows,
-                                        int hidden, float eps) {
-    const int warp = (blockIdx.x * blockDim.x + threadIdx.x) >> 5, lane = threadIdx.x & 31;
-    if (warp >= rows) return;
+// arithmetic in one launch.  One block of 4 warps per row: the warps share
+// the partial sums (chunk i = lane + 32 t of the row goes to warp t % 4) and
+// keep the rounded row in shared memory; warp 0 then forms the sum of
+// squares in rmsnorm_rows_kernel's order (lane L over chunks L, L + 32, ...;
+// a butterfly across lanes).  part: fp32 [kparts][rows][hidden]; dynamic
+// shared memory: hidden fp16.
+constexpr int kRnWarps = 4;
+
+__global__ void __launch_bounds__(32 * kRnWarps) reduce_norm_rows_kernel(const float* __restrict__ part, int kparts,
+                                                                        uint16_t* h, const uint16_t* __restrict__ gamma,
+                                                                        uint16_t* __restrict__ n, int rows,
+                                                                        int hidden, float eps) {
+    extern __shared__ uint4 hs[];  // the row's rounded values
+    __shared__ float r_row;
+    const int row = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (row >= rows) return;
     const size_t pr = (size_t)rows * hidden;
-    uint4* hrow = reinterpret_cast<uint4*>(h + (size_t)warp * hidden);
+    uint4* hrow = reinterpret_cast<uint4*>(h + (size_t)row * hidden);
     const int nv = hidden / 8;
-    float ss = 0.f;
-    for (int i = lane; i < nv; i += 32) {
-        const size_t o = (size_t)warp * hidden + (size_t)i * 8;
+    for (int i = lane + 32 * warp; i < nv; i += 32 * kRnWarps) {
+        const size_t o = (size_t)row * hidden + (size_t)i * 8;
         float y[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
         for (int k = 0; k < kparts; ++k) {
             const float4 a = *reinterpret_cast<const float4*>(part + (size_t)k * pr + o);
@@ -491,19 +499,34 @@ __global__ void reduce_norm_rows_kernel(const float* __restrict__ part, int kpar
             const float2 r = __half22float2(*reinterpret_cast<const __half2*>(&rw[j]));
             const __half2 hv = __floats2half2_rn(y[2 * j] + r.x, y[2 * j + 1] + r.y);
             out[j] = *reinterpret_cast<const uint32_t*>(&hv);
-            const float2 f = __half22float2(hv);
-            ss = fmaf(f.x, f.x, ss);
-            ss = fmaf(f.y, f.y, ss);
         }
-        hrow[i] = make_uint4(out[0], out[1], out[2], out[3]);
+        const uint4 hv4 = make_uint4(out[0], out[1], out[2], out[3]);
+        hrow[i] = hv4;
+        hs[i] = hv4;
     }
+    __syncthreads();
+    if (warp == 0) {
+        float ss = 0.f;
+        for (int i = lane; i < nv; i += 32) {
+            const uint4 v = hs[i];
+            const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-    const float r = rsqrtf(ss / (float)hidden + eps);
-    uint4* dst = reinterpret_cast<uint4*>(n + (size_t)warp * hidden);
+            for (int j = 0; j < 4; ++j) {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+                ss = fmaf(f.x, f.x, ss);
+                ss = fmaf(f.y, f.y, ss);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+        if (lane == 0) r_row = rsqrtf(ss / (float)hidden + eps);
+    }
+    __syncthreads();
+    const float r = r_row;
+    uint4* dst = reinterpret_cast<uint4*>(n + (size_t)row * hidden);
     const uint4* gv = reinterpret_cast<const uint4*>(gamma);
-    for (int i = lane; i < nv; i += 32) {
-        const uint4 v = hrow[i];
+    for (int i = lane + 32 * warp; i < nv; i += 32 * kRnWarps) {
+        const uint4 v = hs[i];
         const uint4 g = gamma ? gv[i] : make_uint4(0x3C003C00u, 0x3C003C00u, 0x3C003C00u, 0x3C003C00u);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w}, gw[4] = {g.x, g.y, g.z, g.w};
         uint32_t o[4];
@@ -669,6 +692,8 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
         if (d.attn && (st = prefill_attn_table(table->pos, t0, C, d.hd, table->rope_theta, cs, s)) != Q4_OK)
             return st;
         bool n_ready = false;  // the previous layer's down launch already wrote this layer's n
+        // the fused reduce + RMSNorm keeps a row in (default-sized) shared memory
+        const bool fuse_rn = (size_t)H * 2 <= 48 * 1024;
         for (int i = 0; i < d.L; ++i) {
             const q4_layer_weights& w = table->layers[i];
             cudaError_t e;
@@ -701,21 +726,25 @@ q4_status q4_prefill(const q4_layer_table* table, uint16_t* h, int T, int chunk,
             // one kernel adds its partials to h and normalises (no separate
             // reduce and RMSNorm launches)
             int kp = 1;
-            if ((st = gemm_res_parts(w.o, o_in, C, hc, part, pb, s, &kp)) != Q4_OK) return st;
+            if (!fuse_rn) {
+                if ((st = gemm_of(w.o, nullptr, o_in, C, hc, hc, part, pb, s)) != Q4_OK) return st;
+            } else if ((st = gemm_res_parts(w.o, o_in, C, hc, part, pb, s, &kp)) != Q4_OK) {
+                return st;
+            }
             if (kp > 1)
-                reduce_norm_rows_kernel<<<nb, 256, 0, s>>>(static_cast<const float*>(part), kp, hc, w.ffn_norm, n, C,
-                                                           H, eps);
+                reduce_norm_rows_kernel<<<C, 32 * kRnWarps, (size_t)H * 2, s>>>(static_cast<const float*>(part), kp,
+                                                                                hc, w.ffn_norm, n, C, H, eps);
             else
                 rmsnorm_rows_kernel<<<nb, 256, 0, s>>>(hc, w.ffn_norm, n, C, H, eps);
             if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
             if ((st = gemm_of(w.gate, &w.up, n, C, act, nullptr, part, pb, s)) != Q4_OK) return st;
             // h = h' + Wdown act; when it splits K (and a layer follows), the
             // next layer's attention RMSNorm goes into the same kernel
-            if (i + 1 < d.L) {
+            if (fuse_rn && i + 1 < d.L) {
                 if ((st = gemm_res_parts(w.down, act, C, hc, part, pb, s, &kp)) != Q4_OK) return st;
                 if (kp > 1) {
-                    reduce_norm_rows_kernel<<<nb, 256, 0, s>>>(static_cast<const float*>(part), kp, hc,
-                                                               table->layers[i + 1].attn_norm, n, C, H, eps);
+                    reduce_norm_rows_kernel<<<C, 32 * kRnWarps, (size_t)H * 2, s>>>(
+                        static_cast<const float*>(part), kp, hc, table->layers[i + 1].attn_norm, n, C, H, eps);
                     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "rmsnorm launch");
                     n_ready = true;
                 }
