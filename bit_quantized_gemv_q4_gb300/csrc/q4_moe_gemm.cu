@@ -79,6 +79,7 @@ constexpr uint32_t kATileBytes = kRows * kKS * 2;    // 16 KB
 // An A stage holds one dequantised tile per matrix: 16 KB plain, 32 KB GLU.
 
 struct Params {
+    const int32_t* expert_ids;  // routed launches: checked against offsets by the epilogue warps
     const uint16_t* scales;
     const uint16_t* biases;
     const uint16_t* scales_u;  // the up matrix's scales and biases (GLU): its rows are
@@ -766,6 +767,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
     } else {
         // ------------------------------------------------------------ epilogue
+        // Routed launches: the device check that expert_ids agrees with
+        // offsets (and that offsets are a monotone partition of 0..R-1), one
+        // thread per check over the grid's epilogue threads, while the first
+        // units' main loops run; a mismatch latches kErrDeviceCheck.
+        if (p.offsets && p.expert_ids) {
+            const int nthr = (int)gridDim.x * 32 * kEpiWarps;
+            const int t = (int)blockIdx.x * 32 * kEpiWarps + ((int)threadIdx.x - 32 * (2 + kDeqWarps));
+            if (t == 0 && (p.offsets[0] != 0 || p.offsets[p.E] != p.R)) atomicOr(p.err, q4d::kErrDeviceCheck);
+            for (int e = t; e < p.E; e += nthr)
+                if (p.offsets[e] > p.offsets[e + 1]) atomicOr(p.err, q4d::kErrDeviceCheck);
+            for (int r = t; r < p.R; r += nthr) {
+                const int e = p.expert_ids[r];
+                if (e < 0 || e >= p.E || r < p.offsets[e] || r >= p.offsets[e + 1]) atomicOr(p.err, q4d::kErrDeviceCheck);
+            }
+        }
         const int q = warp & 3;                   // TMEM lane quarter this warp may access
         const int row = q * 32 + lane;            // accumulator lane = weight row in the tile
         int acc_it = 0;
@@ -976,20 +992,6 @@ __global__ void reduce_parts_kernel(const float* __restrict__ part, int kparts, 
     }
 }
 
-// Device-side check that expert_ids agrees with offsets (and that offsets
-// are a monotone partition of 0..R-1); every check is one thread's work.
-__global__ void check_routing_kernel(const int32_t* __restrict__ expert_ids, const int32_t* __restrict__ offsets,
-                                     int E, int R, int* err) {
-    const int tid = blockIdx.x * blockDim.x + threadIdx.x, nthr = gridDim.x * blockDim.x;
-    if (tid == 0 && (offsets[0] != 0 || offsets[E] != R)) atomicOr(err, q4d::kErrDeviceCheck);
-    for (int e = tid; e < E; e += nthr)
-        if (offsets[e] > offsets[e + 1]) atomicOr(err, q4d::kErrDeviceCheck);
-    for (int r = tid; r < R; r += nthr) {
-        const int e = expert_ids[r];
-        if (e < 0 || e >= E || r < offsets[e] || r >= offsets[e + 1]) atomicOr(err, q4d::kErrDeviceCheck);
-    }
-}
-
 }  // namespace q4g
 
 namespace q4i {
@@ -1098,6 +1100,7 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (a.R == 0) return Q4_OK;
 
     q4g::Params p = {};
+    p.expert_ids = a.expert_ids;
     p.scales = a.scales;
     p.biases = a.biases;
     p.scales_u = a.scales_u;
@@ -1234,9 +1237,6 @@ q4_status launch_grouped(const GroupedArgs& a, q4_stream_t stream) {
     if (st != Q4_OK) return st;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (a.offsets)
-        q4g::check_routing_kernel<<<(a.R + 255) / 256 < dev->sms ? (a.R + 255) / 256 : dev->sms, 256, 0, s>>>(
-            a.expert_ids, a.offsets, a.E, a.R, dev->err_word);
     static std::atomic<int> smem_marks[5][64];
     // instantiation: A in TMEM; A in shared memory with staged / global
     // scales; the same two over several weight matrices
