@@ -21,7 +21,7 @@ namespace q4m {
 
 constexpr int kMaxTopk = 8;
 constexpr int kMaxExperts = 256;
-constexpr int kBlockTokens = 32;  // tokens per counting block (one warp)
+constexpr int kBlockTokens = 32;  // tokens per counting block (one warp per token)
 // Largest token count either routing entry point accepts: keeps every index
 // the kernels form (token, block * experts, rows = tokens * topk) inside int.
 constexpr int kMaxRouteTokens = 1 << 24;
@@ -33,11 +33,18 @@ __device__ __forceinline__ uint32_t half_key(uint16_t h) {
 }
 
 // One warp per token: top-k by repeated warp arg-max over (key, -expert).
-__global__ void route_topk_kernel(const uint16_t* __restrict__ logits, int T, int E, int topk,
-                                  int32_t* __restrict__ ids, float* __restrict__ wts) {
+// Launched with kBlockTokens warps a block: the block also counts its
+// tokens' experts into count[e * B + b] (the histogram route_scan_kernel
+// turns into offsets), so no separate counting launch.
+__global__ void __launch_bounds__(32 * kBlockTokens)
+    route_topk_kernel(const uint16_t* __restrict__ logits, int T, int E, int topk, int32_t* __restrict__ ids,
+                      float* __restrict__ wts, int B, int32_t* __restrict__ count) {
+    __shared__ int32_t c[kMaxExperts];
+    for (int e = threadIdx.x; e < E; e += blockDim.x) c[e] = 0;
+    __syncthreads();
     const long long gw = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
-    if (gw >= T) return;
+    if (gw < T) {
     const int warp = (int)gw;
     const uint16_t* row = logits + (size_t)warp * E;
     constexpr int kPer = kMaxExperts / 32;
@@ -77,21 +84,11 @@ __global__ void route_topk_kernel(const uint16_t* __restrict__ logits, int T, in
             sum += l[k];
         }
         for (int k = 0; k < topk; ++k) wts[(size_t)warp * topk + k] = l[k] / sum;
+        for (int k = 0; k < topk; ++k) atomicAdd(&c[0xFFFF - (int)(chosen[k] & 0xFFFFu)], 1);
     }
-}
-
-// count[e * B + b] = tokens of block b routed to expert e.  One warp per block.
-__global__ void route_count_kernel(const int32_t* __restrict__ ids, int T, int E, int topk, int B,
-                                   int32_t* __restrict__ count) {
-    __shared__ int32_t c[kMaxExperts];
-    const int b = blockIdx.x;
-    for (int e = threadIdx.x; e < E; e += 32) c[e] = 0;
-    __syncwarp();
-    const int t = b * kBlockTokens + threadIdx.x;
-    if (t < T)
-        for (int k = 0; k < topk; ++k) atomicAdd(&c[ids[(size_t)t * topk + k]], 1);
-    __syncwarp();
-    for (int e = threadIdx.x; e < E; e += 32) count[(size_t)e * B + b] = c[e];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += blockDim.x) count[(size_t)e * B + blockIdx.x] = c[e];
 }
 
 // Exclusive scan of count[E*B] in (expert, block) order, in place; also
@@ -284,8 +281,8 @@ q4_status q4_moe_route(const uint16_t* logits, int T, int E, int topk, int32_t* 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int B = (T + q4m::kBlockTokens - 1) / q4m::kBlockTokens;
     int32_t* count = static_cast<int32_t*>(workspace);
-    q4m::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights);
-    q4m::route_count_kernel<<<B, 32, 0, s>>>(topk_ids, T, E, topk, B, count);
+    q4m::route_topk_kernel<<<B, 32 * q4m::kBlockTokens, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights, B,
+                                                                count);
     q4m::route_scan_kernel<<<1, 1024, 0, s>>>(count, E, B, offsets);
     q4m::route_scatter_kernel<<<B, 32, 0, s>>>(topk_ids, T, E, topk, B, count, token_of, expert_of, pos);
     cudaError_t e = cudaGetLastError();
@@ -410,12 +407,12 @@ extern "C" q4_status q4_moe_route_noalloc(const uint16_t* logits, int T, int E, 
         }
         scratch = g_route_scratch_ptr[dev->device];
     }
-    // Every counter the kernels read is written first by route_count_kernel,
+    // Every counter the kernels read is written first by route_topk_kernel,
     // so nothing in the array has to start at zero.
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int Bi = (int)B;
-    q4m::route_topk_kernel<<<(T + 7) / 8, 256, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights);
-    q4m::route_count_kernel<<<Bi, 32, 0, s>>>(topk_ids, T, E, topk, Bi, scratch);
+    q4m::route_topk_kernel<<<Bi, 32 * q4m::kBlockTokens, 0, s>>>(logits, T, E, topk, topk_ids, topk_weights, Bi,
+                                                                 scratch);
     q4m::route_scan_kernel<<<1, 1024, 0, s>>>(scratch, E, Bi, offsets);
     q4m::route_scatter_kernel<<<Bi, 32, 0, s>>>(topk_ids, T, E, topk, Bi, scratch, token_of, expert_of, pos);
     cudaError_t e = cudaGetLastError();
